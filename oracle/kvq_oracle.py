@@ -1,0 +1,394 @@
+"""CPU oracle for Jensen-bias-corrected low-bit KV-cache chunk attention.
+
+TEST INFRASTRUCTURE ONLY.  Nothing in the product path may import, call or
+execute this module: only ``tests/``, ``__graft_entry__.smoke()`` and the
+``cpu_baseline`` / ``--impl reference`` legs of ``bench.py`` use it.  It shares
+no code with the CUDA path (``quantized_kv_cache_quantize_gb300/csrc``).
+
+Source: "Quantized Keys Steal Attention: Bias Correction for KV-Cache
+Compression in Video Diffusion" (Tuncer, Becker, Pfeil), cited below as
+"the paper", by section / equation / figure:
+
+* section 3 "Integer quantization", Eq. (1): asymmetric round-to-nearest
+  x_q = clamp(round(x / Delta) + z, 0, 2^B - 1), x_hat = (x_q - z) * Delta,
+  |x_hat - x| <= Delta / 2, Delta and z chosen to cover [min, max];
+* section 3 "Quantization granularity": per-token groups of g channels, each
+  group with its own (Delta, z);
+* section 3 "Hadamard rotation": a randomized Hadamard H (H^T H = I) applied to
+  keys and queries, which preserves scores (Hq)^T (Hk) = q^T k; Figure 1's
+  caption applies QuaRot + RTN to keys and values;
+* Figure 3 caption, abstract and section 1: quantization noise
+  delta ~ Uniform[-Delta/2, Delta/2] on a score makes E[exp(s + delta)] exceed
+  exp(s) (the Jensen bias); a per-score correction b, computed from the cached
+  keys' step sizes and the query norm, is subtracted before the softmax from
+  cached-key scores only, with a second-order Taylor approximation;
+* Figure 2 caption / section 1: the attention masses P_S (cached block) and
+  P_R (current chunk).
+
+Everything is fp64 except two steps that are fp32 on purpose, because the
+GPU must reproduce them bit for bit: the rotation that feeds the quantizer
+(``rotate_fp32``, the textbook fast Walsh-Hadamard transform in fp32) and the
+code decision (``quantize_groups``).  Where the paper is silent the readings
+are listed in each docstring.
+
+Parity status: every function here is pinned by ``tests/test_oracle_pins.py``
+(closed forms, hand-worked fixtures under ``tests/golden``, brute force,
+Monte-Carlo, invariants).  The magnitude of the attention-mass shift and the
+end-to-end output on the synthetic workloads have no printed value in the
+paper: beyond the invariants those two are "parity unpinned".
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+
+# ---------------------------------------------------------------------------
+# BF16 rounding (storage format of the step sizes, zero points and tensors)
+# ---------------------------------------------------------------------------
+
+
+def bf16_round(x) -> np.ndarray:
+    """Round float32 values to the nearest BF16 (ties to even), returned as
+    float32.  BF16 keeps the top 16 bits of an IEEE float32; finite inputs
+    only."""
+    a = np.ascontiguousarray(np.asarray(x, dtype=np.float32))
+    bits = a.view(np.uint32).astype(np.uint64)
+    lsb = (bits >> np.uint64(16)) & np.uint64(1)
+    bits = (bits + np.uint64(0x7FFF) + lsb) >> np.uint64(16)
+    out = (bits << np.uint64(16)).astype(np.uint32)
+    return out.view(np.float32).reshape(a.shape)
+
+
+def bf16_bits(x) -> np.ndarray:
+    """The 16-bit pattern of float32 values that are already BF16-exact."""
+    a = np.ascontiguousarray(np.asarray(x, dtype=np.float32))
+    return (a.view(np.uint32) >> np.uint32(16)).astype(np.uint16)
+
+
+def from_bf16_bits(b) -> np.ndarray:
+    b = np.asarray(b, dtype=np.uint16).astype(np.uint32) << np.uint32(16)
+    return b.view(np.float32)
+
+
+# ---------------------------------------------------------------------------
+# Randomized Hadamard rotation (paper section 3, "Hadamard rotation")
+# ---------------------------------------------------------------------------
+
+
+def sylvester_hadamard(d: int) -> np.ndarray:
+    """Sylvester construction: H_1 = [1], H_2n = [[H_n, H_n], [H_n, -H_n]].
+
+    Reading: the paper names a "randomized Hadamard rotation" without its
+    construction; we take the Sylvester matrix times a random sign diagonal,
+    normalised by 1/sqrt(d) (the QuaRot construction it cites)."""
+    if d < 1 or d & (d - 1):
+        raise ValueError("d must be a power of two")
+    h = np.ones((1, 1))
+    while h.shape[0] < d:
+        h = np.block([[h, h], [h, -h]])
+    return h
+
+
+def rotation_matrix(signs) -> np.ndarray:
+    """R = (1/sqrt(d)) * H_Sylvester * diag(signs); orthogonal, so R^T R = I."""
+    s = np.asarray(signs, dtype=np.float64)
+    d = s.shape[0]
+    return sylvester_hadamard(d) * s[None, :] / math.sqrt(d)
+
+
+def rotate(x, signs) -> np.ndarray:
+    """x' = R x for each row x (fp64)."""
+    return np.asarray(x, dtype=np.float64) @ rotation_matrix(signs).T
+
+
+def unrotate(y, signs) -> np.ndarray:
+    """x = R^T y for each row y (fp64), the inverse of ``rotate``."""
+    return np.asarray(y, dtype=np.float64) @ rotation_matrix(signs)
+
+
+def rotate_fp32(x, signs) -> np.ndarray:
+    """The rotation in fp32, as the fast Walsh-Hadamard transform.
+
+    Steps (each a correctly rounded IEEE fp32 operation): multiply by the
+    signs (exact); then for h = 1, 2, 4, ..., d/2, for every index i whose bit
+    h is clear, replace (x[i], x[i+h]) by (x[i] + x[i+h], x[i] - x[i+h]);
+    finally multiply by the fp32 constant fl(1/sqrt(d)).  In exact
+    arithmetic this equals ``rotate``; in fp32 it fixes one rounding order,
+    which the quantizer's bit-exact contract is defined on."""
+    y = np.array(x, dtype=np.float32, copy=True)
+    lead = y.shape[:-1]
+    d = y.shape[-1]
+    y = y * np.asarray(signs, dtype=np.float32)
+    h = 1
+    while h < d:
+        v = y.reshape(*lead, d // (2 * h), 2, h)
+        a = v[..., 0, :]
+        b = v[..., 1, :]
+        y = np.stack([a + b, a - b], axis=-2).reshape(*lead, d)
+        h *= 2
+    inv = np.float32(1.0 / math.sqrt(float(d)))
+    return (y * inv).astype(np.float32)
+
+
+# ---------------------------------------------------------------------------
+# Asymmetric per-token-group quantization (paper section 3, Eq. (1))
+# ---------------------------------------------------------------------------
+
+
+def quantize_groups(y, bits: int, group: int):
+    """Quantize fp32 rows y [..., d] per token and group of ``group`` channels.
+
+    Returns (codes uint8 [..., d], delta float32 [..., G], zero float32
+    [..., G]); delta and zero are BF16-exact (they are stored as BF16).
+
+    Per group, in fp32:
+      mn, mx   = min, max of the group            (Eq. (1): cover [min, max])
+      delta    = bf16(fl((mx - mn) / (2^B - 1)))
+      if delta == 0: delta = bf16(|mn|), and 1 if that is 0 too
+      zero     = bf16(rint(fl(-mn / delta)) + 0)   (integer zero point)
+      code     = clamp(rint(fl(y / delta)) + zero, 0, 2^B - 1)
+
+    Readings where the paper is silent: rint rounds half to even; z is an
+    integer and is not clamped (all-positive or all-negative groups need
+    that); codes are computed with the stored BF16 delta and zero so that
+    quantize and dequantize agree; "+ 0" turns a -0 zero point into +0; a
+    constant group (delta would be 0) takes delta = |mn| so that it
+    dequantizes to its own value."""
+    y = np.asarray(y, dtype=np.float32)
+    d = y.shape[-1]
+    if d % group:
+        raise ValueError("group must divide d")
+    lead = y.shape[:-1]
+    g_n = d // group
+    yg = y.reshape(*lead, g_n, group)
+    mn = yg.min(axis=-1)
+    mx = yg.max(axis=-1)
+    qmax = np.float32(2 ** bits - 1)
+    delta = bf16_round((mx - mn) / qmax)
+    fb = bf16_round(np.abs(mn))
+    fb = np.where(fb == 0, np.float32(1.0), fb).astype(np.float32)
+    delta = np.where(delta == 0, fb, delta).astype(np.float32)
+    zero = bf16_round(np.rint((-mn) / delta) + np.float32(0.0))
+    codes = np.rint(yg / delta[..., None]) + zero[..., None]
+    codes = np.clip(codes, np.float32(0.0), qmax)
+    return codes.astype(np.uint8).reshape(*lead, d), delta, zero
+
+
+def dequantize(codes, delta, zero, group: int) -> np.ndarray:
+    """x_hat = (x_q - z) * delta per group, in fp64 (Eq. (1))."""
+    c = np.asarray(codes, dtype=np.float64)
+    lead = c.shape[:-1]
+    d = c.shape[-1]
+    cg = c.reshape(*lead, d // group, group)
+    out = (cg - np.asarray(zero, np.float64)[..., None]) * np.asarray(delta, np.float64)[..., None]
+    return out.reshape(*lead, d)
+
+
+# ---------------------------------------------------------------------------
+# Packed code layout (a storage format of this library; the paper fixes none)
+# ---------------------------------------------------------------------------
+
+
+def pack_codes(codes, bits: int) -> np.ndarray:
+    """Pack codes [..., d] into bytes [..., d * bits / 8].
+
+    Little-endian 32-bit words of 32/bits codes each.  INT2: channel
+    16w + 2k + h (k < 8, h < 2) sits at bits [2k + 16h, 2k + 16h + 2) of word
+    w.  INT4: channel 8w + 2k + h (k < 4) sits at bits [4k + 16h, 4k + 16h + 4).
+    Adjacent channel pairs thus land 16 bits apart in one word."""
+    c = np.asarray(codes, dtype=np.uint32)
+    lead = c.shape[:-1]
+    d = c.shape[-1]
+    per = 32 // bits
+    half = per // 2
+    cw = c.reshape(*lead, d // per, half, 2)
+    words = np.zeros((*lead, d // per), dtype=np.uint32)
+    for k in range(half):
+        for h in range(2):
+            shift = np.uint32(bits * k + 16 * h)
+            words |= cw[..., k, h] << shift
+    return np.ascontiguousarray(words.astype("<u4")).view(np.uint8).reshape(*lead, d * bits // 8)
+
+
+def unpack_codes(packed, bits: int, d: int) -> np.ndarray:
+    p = np.ascontiguousarray(np.asarray(packed, dtype=np.uint8))
+    lead = p.shape[:-1]
+    words = p.view("<u4").astype(np.uint32).reshape(*lead, -1)
+    per = 32 // bits
+    half = per // 2
+    mask = np.uint32(2 ** bits - 1)
+    out = np.zeros((*lead, d // per, half, 2), dtype=np.uint8)
+    for k in range(half):
+        for h in range(2):
+            out[..., k, h] = (words >> np.uint32(bits * k + 16 * h)) & mask
+    return out.reshape(*lead, d)
+
+
+def quantize_rows(x_bf16, signs, bits: int, group: int):
+    """What one quantize-append computes for rows of BF16 values x [..., d]:
+    the fp32 rotation, then the per-group quantizer.  Returns
+    (packed codes, delta, zero, rotated fp32, codes)."""
+    y = rotate_fp32(np.asarray(x_bf16, dtype=np.float32), signs)
+    codes, delta, zero = quantize_groups(y, bits, group)
+    return pack_codes(codes, bits), delta, zero, y, codes
+
+
+# ---------------------------------------------------------------------------
+# Jensen-bias correction (paper: abstract, section 1, Figure 3 caption)
+# ---------------------------------------------------------------------------
+
+
+def group_sq_norms(q_rot, group: int) -> np.ndarray:
+    """n_{j,g} = ||q'_{j,g}||^2 per query row and channel group (fp64)."""
+    q = np.asarray(q_rot, dtype=np.float64)
+    lead = q.shape[:-1]
+    d = q.shape[-1]
+    return (q.reshape(*lead, d // group, group) ** 2).sum(axis=-1)
+
+
+def jensen_bias_taylor(q_rot, delta, scale: float, group: int) -> np.ndarray:
+    """Second-order correction b_ij = Var[delta_ij] / 2 for queries q'_j
+    [Nq, d] (rotated) and cached keys with steps delta_{i,g} [Ns, G].
+
+    The score noise is delta_ij = scale * q'_j . eps_i with independent
+    eps_{i,c} ~ Uniform[-D/2, D/2], D = delta_{i,g(c)} (Figure 3 caption; the
+    bound of Eq. (1)); it has zero mean and variance
+    scale^2 * sum_g ||q'_{j,g}||^2 * delta_{i,g}^2 / 12.  A second-order
+    Taylor expansion gives E[exp(s + delta)] ~ exp(s + Var/2), so
+    b = scale^2 / 24 * sum_g n_{j,g} * delta_{i,g}^2.  Returns [Nq, Ns]."""
+    n = group_sq_norms(q_rot, group)                      # [Nq, G]
+    dl = np.asarray(delta, dtype=np.float64)              # [Ns, G]
+    return (scale * scale / 24.0) * (n @ (dl * dl).T)
+
+
+def log_sinhc(a) -> np.ndarray:
+    """log(sinh(a) / a) for a >= 0, the exact log-moment of Uniform[-a, a]
+    (E[exp(u)] = sinh(a)/a).
+
+    Below a = 1 it is log1p of sinh(a)/a - 1 = sum_{k>=1} a^(2k) / (2k+1)!
+    (summed to k = 12, far below fp64 resolution), which keeps full relative
+    precision for small a; above, a + log((1 - exp(-2a)) / 2) - log(a)."""
+    a = np.abs(np.asarray(a, dtype=np.float64))
+    out = np.empty_like(a)
+    small = a < 1.0
+    a2 = a[small] ** 2
+    term = np.ones_like(a2)
+    acc = np.zeros_like(a2)
+    for k in range(1, 13):
+        term = term * a2 / ((2 * k) * (2 * k + 1))
+        acc = acc + term
+    out[small] = np.log1p(acc)
+    big = ~small
+    ab = a[big]
+    out[big] = ab + np.log1p(-np.exp(-2.0 * ab)) - math.log(2.0) - np.log(ab)
+    return out
+
+
+def jensen_bias_exact(q_rot, delta, scale: float, group: int) -> np.ndarray:
+    """Exact correction for independent uniform noise:
+    b_ij = log E[exp(delta_ij)] = sum_c log(sinh(a_c) / a_c) with
+    a_c = scale * |q'_{j,c}| * delta_{i,g(c)} / 2.  Returns [Nq, Ns].
+    (The paper mentions the exact term only as the quantity the Taylor term
+    approximates; this is its closed form for uniform noise.)"""
+    q = np.abs(np.asarray(q_rot, dtype=np.float64))       # [Nq, d]
+    dl = np.asarray(delta, dtype=np.float64)              # [Ns, G]
+    nq, d = q.shape
+    out = np.zeros((nq, dl.shape[0]))
+    for c in range(d):
+        a = 0.5 * scale * q[:, c][:, None] * dl[:, c // group][None, :]
+        out += log_sinhc(a)
+    return out
+
+
+# ---------------------------------------------------------------------------
+# Chunk attention over [cached window ; current chunk]
+# ---------------------------------------------------------------------------
+
+CORR_NONE = 0
+CORR_TAYLOR = 1
+CORR_EXACT = 2
+
+
+def chunk_attention(q, k_hat_rot, v_hat_rot, delta_k, k_cur, v_cur, signs,
+                    scale: float, group: int, corr: int = CORR_TAYLOR):
+    """Attention of the current chunk's queries over the dequantized cached
+    window and the unquantized current chunk, one head.
+
+    q [Nq, d], k_cur/v_cur [Nr, d]: original basis (BF16 values as floats).
+    k_hat_rot/v_hat_rot [Ns, d]: dequantized cached keys/values, rotated
+    basis.  delta_k [Ns, G]: the cached keys' step sizes.
+
+    Steps (fp64):
+      q' = R q                                   (section 3, Hadamard rotation)
+      cached scores  s_ij = scale * q'_j . k_hat'_i - b_ij
+                     (b from ``corr``; subtracted before the softmax, cached
+                     keys only: abstract, section 1)
+      current scores s_ij = scale * q_j . k_i    (unquantized; (Hq)^T(Hk) = q^T k)
+      p = softmax over the concatenation [cached ; current] (max-subtracted)
+      P_S = sum of p over cached keys, P_R = sum over current keys
+      O = sum_i p_i v_i, cached values un-rotated: v_hat = R^T v_hat'.
+
+    Readings: no mask inside the chunk or across the window (chunk-wise
+    attention); masses are per query row.  Returns (O [Nq, d], P_S [Nq],
+    P_R [Nq])."""
+    q = np.asarray(q, dtype=np.float64)
+    kc = np.asarray(k_cur, dtype=np.float64).reshape(-1, q.shape[1])
+    vc = np.asarray(v_cur, dtype=np.float64).reshape(-1, q.shape[1])
+    ks = np.asarray(k_hat_rot, dtype=np.float64).reshape(-1, q.shape[1])
+    vs = np.asarray(v_hat_rot, dtype=np.float64).reshape(-1, q.shape[1])
+    q_rot = rotate(q, signs)
+    s_cache = scale * (q_rot @ ks.T)
+    if corr == CORR_TAYLOR:
+        s_cache = s_cache - jensen_bias_taylor(q_rot, delta_k, scale, group)
+    elif corr == CORR_EXACT:
+        s_cache = s_cache - jensen_bias_exact(q_rot, delta_k, scale, group)
+    elif corr != CORR_NONE:
+        raise ValueError("unknown correction mode")
+    s_cur = scale * (q @ kc.T)
+    s = np.concatenate([s_cache, s_cur], axis=1)
+    m = s.max(axis=1, keepdims=True)
+    e = np.exp(s - m)
+    denom = e.sum(axis=1, keepdims=True)
+    p = e / denom
+    ns = ks.shape[0]
+    p_s = p[:, :ns].sum(axis=1)
+    p_r = p[:, ns:].sum(axis=1)
+    v_hat = unrotate(vs, signs)
+    o = p[:, :ns] @ v_hat + p[:, ns:] @ vc
+    return o, p_s, p_r
+
+
+# ---------------------------------------------------------------------------
+# Sliding-window ring of chunk slots (host bookkeeping of the cache)
+# ---------------------------------------------------------------------------
+
+
+def ring_append(length: int, head_slot: int, n_new: int, chunk_tokens: int,
+                n_chunks: int):
+    """Where an append of ``n_new`` tokens lands and the cache state after it.
+
+    The cache holds the last ``n_chunks`` chunks (the sliding window over the
+    last n cached chunks of MAGI-1, paper section 1) in ``n_chunks`` slots of
+    ``chunk_tokens`` tokens; attention reads tokens [0, length).  Rules:
+      * 0 <= n_new <= chunk_tokens; n_new == 0 changes nothing;
+      * while the cache is not full, every earlier slot must be full
+        (length == head_slot * chunk_tokens); the chunk goes to slot
+        head_slot and length grows by n_new -- so a partial chunk can only be
+        the last one appended;
+      * once full, only whole chunks may overwrite the oldest slot.
+    Returns (first_token, new_length, new_head_slot), or None when the append
+    is refused."""
+    cap = chunk_tokens * n_chunks
+    if n_new < 0 or n_new > chunk_tokens:
+        return None
+    first = head_slot * chunk_tokens
+    if n_new == 0:
+        return first, length, head_slot
+    if length < cap:
+        if length != first:
+            return None
+        return first, length + n_new, (head_slot + 1) % n_chunks
+    if n_new != chunk_tokens:
+        return None
+    return first, cap, (head_slot + 1) % n_chunks

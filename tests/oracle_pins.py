@@ -1,0 +1,407 @@
+"""Checks that pin the CPU oracle to facts outside itself.
+
+Each ``check_*`` raises AssertionError when the oracle disagrees with what
+the paper ("Quantized Keys Steal Attention: Bias Correction for KV-Cache
+Compression in Video Diffusion") or plain mathematics fixes.  They are run
+by ``test_oracle_pins.py`` and, with mistakes planted in the oracle, by
+``test_oracle_mutations.py`` (which expects them to fail).
+"""
+from __future__ import annotations
+
+import math
+import os
+
+import numpy as np
+import torch
+
+from oracle import kvq_oracle as O
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+def _rows(name):
+    out = []
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            out.append(line)
+    return out
+
+
+# --------------------------------------------------------------------------
+# Rotation (section 3, "Hadamard rotation")
+# --------------------------------------------------------------------------
+
+
+def check_hadamard_hand_d4():
+    rows = dict(r.split(":", 1) for r in _rows("hadamard_d4.txt"))
+    syl = np.array([[float(v) for v in rows[f"sylvester_row{i}"].split()] for i in range(4)])
+    assert np.array_equal(O.sylvester_hadamard(4), syl)
+    signs = np.array([float(v) for v in rows["signs"].split()])
+    x = np.array([float(v) for v in rows["x"].split()])
+    want = np.array([float(v) for v in rows["rotated"].split()])
+    assert np.allclose(O.rotate(x[None], signs)[0], want, rtol=0, atol=1e-14)
+    got32 = O.rotate_fp32(x[None].astype(np.float32), signs.astype(np.float32))[0]
+    assert np.array_equal(got32, want.astype(np.float32))
+    assert np.allclose(O.unrotate(want[None], signs)[0], x, rtol=0, atol=1e-14)
+
+
+def check_rotation_orthogonal_and_score_invariant():
+    rng = np.random.default_rng(1)
+    for d in (2, 4, 64, 128):
+        s = np.where(rng.integers(0, 2, d) == 1, -1.0, 1.0)
+        r = O.rotation_matrix(s)
+        assert np.abs(r @ r.T - np.eye(d)).max() < 1e-12
+        q = rng.standard_normal((5, d))
+        k = rng.standard_normal((7, d))
+        # (Hq)^T (Hk) = q^T k
+        assert np.abs(O.rotate(q, s) @ O.rotate(k, s).T - q @ k.T).max() < 1e-11
+        assert np.abs(O.unrotate(O.rotate(q, s), s) - q).max() < 1e-12
+
+
+def check_fwht_fp32_matches_fp64():
+    rng = np.random.default_rng(2)
+    for d in (64, 128):
+        s = np.where(rng.integers(0, 2, d) == 1, -1.0, 1.0).astype(np.float32)
+        x = (rng.standard_normal((200, d)) * 3).astype(np.float32)
+        y32 = O.rotate_fp32(x, s).astype(np.float64)
+        y64 = O.rotate(x.astype(np.float64), s)
+        # log2(d) rounded additions + one rounded scaling per element
+        bound = (math.log2(d) + 2) * 2.0 ** -24 * np.abs(x).sum(axis=1, keepdims=True) / math.sqrt(d)
+        assert np.all(np.abs(y32 - y64) <= bound)
+        # a basis vector e_i becomes +-fl(1/sqrt(d)) times column i of Sylvester
+        e = np.eye(d, dtype=np.float32)
+        inv = np.float32(1.0 / math.sqrt(d))
+        want = (O.sylvester_hadamard(d).T * s[:, None]).astype(np.float32) * inv
+        assert np.array_equal(O.rotate_fp32(e, s), want.astype(np.float32))
+
+
+def check_bf16_round_matches_torch():
+    rng = np.random.default_rng(3)
+    x = np.concatenate([
+        rng.standard_normal(4000).astype(np.float32) * 10,
+        np.array([0.0, -0.0, 1.0, 1.00390625, 1.005859375, 1.0 + 2 ** -8,
+                  1.0 + 3 * 2 ** -9, 65280.0, 1e-40, -3.0e38], dtype=np.float32),
+    ]).astype(np.float32)
+    # exact ties at both parities of the kept last bit
+    ties = (np.arange(1000, dtype=np.uint32) << np.uint32(16)) | np.uint32(0x3F808000)
+    x = np.concatenate([x, ties.view(np.float32)])
+    want = torch.from_numpy(x).to(torch.bfloat16).to(torch.float32).numpy()
+    assert np.array_equal(O.bf16_round(x), want)
+
+
+# --------------------------------------------------------------------------
+# Quantization (section 3, Eq. (1) and "Quantization granularity")
+# --------------------------------------------------------------------------
+
+
+def check_quant_hand_fixture():
+    for line in _rows("quant_eq1.txt"):
+        parts = [p.strip() for p in line.split("|")]
+        bits = int(parts[0])
+        x = np.array([float(v) for v in parts[1].split()], dtype=np.float32)
+        d_want = float(parts[2])
+        z_want = float(parts[3])
+        c_want = np.array([int(v) for v in parts[4].split()])
+        xh_want = np.array([float(v) for v in parts[5].split()])
+        codes, delta, zero = O.quantize_groups(x[None], bits, x.size)
+        assert float(delta[0, 0]) == d_want, (line, delta)
+        assert float(zero[0, 0]) == z_want, (line, zero)
+        assert np.array_equal(codes[0], c_want), (line, codes)
+        xh = O.dequantize(codes, delta, zero, x.size)[0]
+        assert np.array_equal(xh, xh_want), (line, xh)
+        # a zero point of -0 would differ in its bits from +0
+        assert O.bf16_bits(zero)[0, 0] != 0x8000
+
+
+def check_quant_bounds_and_brute_force():
+    """|x_hat - x| <= D/2 for elements whose code is not clamped; every code
+    is the nearest grid point (brute force over all 2^B codes)."""
+    rng = np.random.default_rng(4)
+    for bits, group in ((2, 32), (4, 64), (2, 4), (4, 8)):
+        y = (rng.standard_normal((300, 128)) * rng.uniform(0.1, 5, (300, 1))
+             + rng.standard_normal((300, 1))).astype(np.float32)
+        codes, delta, zero = O.quantize_groups(y, bits, group)
+        qmax = 2 ** bits - 1
+        assert codes.max() <= qmax
+        xh = O.dequantize(codes, delta, zero, group)
+        g_n = 128 // group
+        dfull = np.repeat(delta, group, axis=1).astype(np.float64)
+        zfull = np.repeat(zero, group, axis=1).astype(np.float64)
+        err = np.abs(xh - y)
+        unclamped = (codes > 0) & (codes < qmax)
+        assert np.all(err[unclamped] <= dfull[unclamped] / 2 * (1 + 1e-6))
+        cands = (np.arange(qmax + 1)[None, None, :] - zfull[..., None]) * dfull[..., None]
+        best = np.abs(cands - y[..., None].astype(np.float64)).min(axis=-1)
+        assert np.all(err <= best + 1e-6 * dfull)
+        # the grid covers [min, max] up to the BF16 rounding of D
+        yg = y.reshape(300, g_n, group)
+        # (slack: half a step, plus qmax times the BF16 rounding of the step)
+        lo = (0 - zero.astype(np.float64)) * delta
+        hi = (qmax - zero.astype(np.float64)) * delta
+        d_exact = (yg.max(-1).astype(np.float64) - yg.min(-1)) / qmax
+        slack = delta * 0.5 + qmax * np.abs(delta - d_exact) + 1e-6 * delta
+        assert np.all(lo <= yg.min(-1) + slack)
+        assert np.all(hi >= yg.max(-1) - slack)
+        assert np.all(np.abs(delta - (yg.max(-1) - yg.min(-1)) / qmax) <= delta * 2 ** -8 + 1e-30)
+
+
+def check_smaller_groups_smaller_error():
+    """Section 3 "Quantization granularity": smaller groups give a smaller
+    quantization error (and more memory)."""
+    rng = np.random.default_rng(5)
+    y = rng.standard_normal((2000, 128)).astype(np.float32)
+    y[:, :3] *= 10
+    errs = []
+    for g in (16, 32, 64, 128):
+        c, dl, z = O.quantize_groups(y, 2, g)
+        errs.append(np.abs(O.dequantize(c, dl, z, g) - y).mean())
+    assert errs[0] < errs[1] < errs[2] < errs[3], errs
+
+
+def check_pack_hand_fixture():
+    for line in _rows("pack_layout.txt"):
+        bits_s, codes_s, bytes_s = [p.strip() for p in line.split("|")]
+        bits = int(bits_s)
+        codes = np.array([int(v) for v in codes_s.split()], dtype=np.uint8)
+        want = np.array([int(v, 16) for v in bytes_s.split()], dtype=np.uint8)
+        got = O.pack_codes(codes[None], bits)[0]
+        assert np.array_equal(got, want), (bits, got, want)
+        assert np.array_equal(O.unpack_codes(got[None], bits, codes.size)[0], codes)
+
+
+def check_pack_roundtrip():
+    rng = np.random.default_rng(6)
+    for bits in (2, 4):
+        for d in (64, 128):
+            c = rng.integers(0, 2 ** bits, (50, d)).astype(np.uint8)
+            p = O.pack_codes(c, bits)
+            assert p.shape == (50, d * bits // 8)
+            assert np.array_equal(O.unpack_codes(p, bits, d), c)
+
+
+# --------------------------------------------------------------------------
+# Jensen bias (Figure 3 caption; abstract; section 1)
+# --------------------------------------------------------------------------
+
+
+def check_log_sinhc_closed_form():
+    import mpmath as mp
+    mp.mp.dps = 40
+    a = np.array([1e-6, 1e-4, 5e-4, 1e-3, 2e-3, 0.01, 0.1, 0.5, 0.999, 1.0, 2.0, 7.0, 30.0])
+    want = np.array([float(mp.log(mp.sinh(mp.mpf(v)) / mp.mpf(v))) for v in a])
+    got = O.log_sinhc(a)
+    assert np.all(np.abs(got - want) <= 1e-14 * np.abs(want)), (got, want)
+    assert abs(O.log_sinhc(np.array([1.0]))[0] - 0.161439362) < 1e-9
+    assert abs(O.log_sinhc(np.array([0.5]))[0] - 0.041324855) < 1e-9
+
+
+def check_bias_forms():
+    """b_Taylor = sum_c a_c^2 / 6 (a_c = scale |q'_c| D_g(c) / 2), the
+    second-order term of b_exact = sum_c log(sinh a_c / a_c); the gap is
+    -sum a^4 / 180 to leading order; D -> 0 gives b = 0."""
+    rng = np.random.default_rng(7)
+    d, group, scale = 64, 16, 1 / 8
+    q = rng.standard_normal((6, d))
+    dl = rng.uniform(0.01, 0.05, (9, d // group))
+    bt = O.jensen_bias_taylor(q, dl, scale, group)
+    a = 0.5 * scale * np.abs(q)[:, None, :] * np.repeat(dl, group, axis=1)[None, :, :]
+    assert np.allclose(bt, (a ** 2).sum(-1) / 6, rtol=1e-12, atol=0)
+    be = O.jensen_bias_exact(q, dl, scale, group)
+    assert np.allclose(be - bt, -(a ** 4).sum(-1) / 180, rtol=2e-3, atol=1e-18)
+    assert np.all(be < bt)   # the Taylor term over-corrects slightly
+    z = np.zeros_like(dl)
+    assert np.all(O.jensen_bias_taylor(q, z, scale, group) == 0)
+    assert np.all(O.jensen_bias_exact(q, z, scale, group) == 0)
+
+
+def check_monte_carlo_jensen():
+    """Figure 3: uniform zero-mean noise leaves s_hat unbiased, inflates
+    E[exp(s_hat)] above exp(s); subtracting b_exact removes that in
+    expectation, and b_Taylor nearly so (O(a^4))."""
+    rng = np.random.default_rng(8)
+    d, group, scale = 32, 32, 1 / math.sqrt(32)
+    q = rng.standard_normal((1, d)) * 1.5
+    delta = np.array([[1.2]])
+    n = 400_000
+    eps = (rng.random((n, d)) - 0.5) * delta[0, 0]
+    noise = scale * (eps @ q[0])                      # s_hat - s per draw
+    se = noise.std() / math.sqrt(n)
+    assert abs(noise.mean()) < 5 * se                 # unbiased score
+    var_pred = scale ** 2 * (q[0] ** 2).sum() * delta[0, 0] ** 2 / 12
+    assert abs(noise.var() / var_pred - 1) < 0.02
+    e = np.exp(noise)
+    se_e = e.std() / math.sqrt(n)
+    jensen = e.mean() - 1.0
+    assert jensen > 20 * se_e                         # E[e^s_hat] > e^s
+    b_ex = O.jensen_bias_exact(q, delta, scale, group)[0, 0]
+    b_ty = O.jensen_bias_taylor(q, delta, scale, group)[0, 0]
+    assert abs(b_ty - var_pred / 2) < 1e-12
+    r_ex = np.exp(noise - b_ex).mean() - 1.0
+    r_ty = np.exp(noise - b_ty).mean() - 1.0
+    assert abs(r_ex) < 5 * se_e
+    assert abs(r_ty) < abs(jensen) / 5
+    a4 = ((0.5 * scale * np.abs(q[0]) * delta[0, 0]) ** 4).sum() / 180
+    assert abs(r_ty) < 2 * a4 + 5 * se_e
+
+
+# --------------------------------------------------------------------------
+# Attention and masses
+# --------------------------------------------------------------------------
+
+
+def _brute_attention(q, ks_rot, vs_rot, dl, kc, vc, signs, scale, group, corr):
+    """Pure-Python loops, fp64, tiny sizes only."""
+    d = len(signs)
+    r = O.rotation_matrix(signs)
+    out, ps, pr = [], [], []
+    for qj in q:
+        qr = [sum(r[a][c] * qj[c] for c in range(d)) for a in range(d)]
+        scores = []
+        for i, ki in enumerate(ks_rot):
+            s = scale * sum(qr[c] * ki[c] for c in range(d))
+            if corr == O.CORR_TAYLOR:
+                b = 0.0
+                for c in range(d):
+                    b += (scale * qr[c] * dl[i][c // group]) ** 2 / 24
+                s -= b
+            elif corr == O.CORR_EXACT:
+                b = 0.0
+                for c in range(d):
+                    a = 0.5 * scale * abs(qr[c]) * dl[i][c // group]
+                    b += math.log(math.sinh(a) / a) if a > 0 else 0.0
+                s -= b
+            scores.append(s)
+        for ki in kc:
+            scores.append(scale * sum(qj[c] * ki[c] for c in range(d)))
+        m = max(scores)
+        e = [math.exp(s - m) for s in scores]
+        tot = sum(e)
+        p = [x / tot for x in e]
+        ns = len(ks_rot)
+        ps.append(sum(p[:ns]))
+        pr.append(sum(p[ns:]))
+        vals = [[sum(r[a][c] * vi[a] for a in range(d)) for c in range(d)] for vi in vs_rot]
+        vals += [list(v) for v in vc]
+        out.append([sum(p[i] * vals[i][c] for i in range(len(p))) for c in range(d)])
+    return np.array(out), np.array(ps), np.array(pr)
+
+
+def check_attention_brute_force():
+    rng = np.random.default_rng(9)
+    d, group, scale = 4, 2, 0.5
+    s = np.array([1.0, -1.0, -1.0, 1.0])
+    q = rng.standard_normal((3, d))
+    ks = rng.standard_normal((5, d))
+    vs = rng.standard_normal((5, d))
+    dl = rng.uniform(0.2, 0.9, (5, d // group))
+    kc = rng.standard_normal((2, d))
+    vc = rng.standard_normal((2, d))
+    for corr in (O.CORR_NONE, O.CORR_TAYLOR, O.CORR_EXACT):
+        o, ps, pr = O.chunk_attention(q, ks, vs, dl, kc, vc, s, scale, group, corr)
+        ob, psb, prb = _brute_attention(q, ks, vs, dl, kc, vc, s, scale, group, corr)
+        assert np.allclose(o, ob, rtol=0, atol=1e-12)
+        assert np.allclose(ps, psb, rtol=0, atol=1e-13)
+        assert np.allclose(pr, prb, rtol=0, atol=1e-13)
+        assert np.allclose(ps + pr, 1.0, atol=1e-14)
+
+
+def _sdpa(q, k, v, scale):
+    t = lambda a: torch.from_numpy(np.asarray(a, np.float64))[None, None]
+    return torch.nn.functional.scaled_dot_product_attention(
+        t(q), t(k), t(v), scale=scale)[0, 0].numpy()
+
+
+def check_attention_special_cases():
+    """Empty cache = textbook softmax attention over the current chunk; a
+    rotated cache with zero step sizes (b = 0) = textbook attention over the
+    union of cached and current tokens, in the original basis."""
+    rng = np.random.default_rng(10)
+    d, group, scale = 64, 32, 1 / 8
+    s = np.where(rng.integers(0, 2, d) == 1, -1.0, 1.0)
+    q = rng.standard_normal((17, d))
+    kc = rng.standard_normal((11, d))
+    vc = rng.standard_normal((11, d))
+    e = np.zeros((0, d))
+    o, ps, pr = O.chunk_attention(q, e, e, np.zeros((0, 2)), kc, vc, s, scale, group)
+    assert np.allclose(o, _sdpa(q, kc, vc, scale), atol=1e-12)
+    assert np.all(ps == 0) and np.allclose(pr, 1.0, atol=1e-14)
+    k = rng.standard_normal((13, d))
+    v = rng.standard_normal((13, d))
+    for corr in (O.CORR_NONE, O.CORR_TAYLOR, O.CORR_EXACT):
+        o, ps, pr = O.chunk_attention(q, O.rotate(k, s), O.rotate(v, s), np.zeros((13, 2)),
+                                      kc, vc, s, scale, group, corr)
+        want = _sdpa(q, np.concatenate([k, kc]), np.concatenate([v, vc]), scale)
+        assert np.allclose(o, want, atol=1e-12)
+    o, ps, pr = O.chunk_attention(q, O.rotate(k, s), O.rotate(v, s), np.zeros((13, 2)),
+                                  e, e, s, scale, group)
+    assert np.allclose(ps, 1.0, atol=1e-14) and np.all(pr == 0)
+    assert np.allclose(o, _sdpa(q, k, v, scale), atol=1e-12)
+
+
+def _quantized_head(bits, group, seed=11, n_q=256, n_s=1024, n_r=256, d=64):
+    rng = np.random.default_rng(seed)
+    s = np.where(rng.integers(0, 2, d) == 1, -1.0, 1.0).astype(np.float32)
+    q = O.bf16_round(rng.standard_normal((n_q, d)).astype(np.float32))
+    kc = O.bf16_round(rng.standard_normal((n_r, d)).astype(np.float32))
+    vc = O.bf16_round(rng.standard_normal((n_r, d)).astype(np.float32))
+    k = rng.standard_normal((n_s, d)).astype(np.float32)
+    k[:, :4] *= 8
+    k = O.bf16_round(k)
+    v = O.bf16_round(rng.standard_normal((n_s, d)).astype(np.float32))
+    _, kd, kz, _, kcodes = O.quantize_rows(k, s, bits, group)
+    _, vd, vz, _, vcodes = O.quantize_rows(v, s, bits, group)
+    qd = dict(kh=O.dequantize(kcodes, kd, kz, group), vh=O.dequantize(vcodes, vd, vz, group),
+              kd=kd)
+    return q, k, v, kc, vc, s, qd
+
+
+def check_mass_shift_and_correction():
+    """Figure 2 / Figure 4 / section 1: with an INT2 cache, attention mass
+    moves to the cached block (P_S grows) relative to unquantized keys, and
+    the correction brings P_S back toward the unquantized value.  Direction
+    only: the paper prints no magnitudes."""
+    q, k, v, kc, vc, s, qd = _quantized_head(2, 32)
+    scale = 1 / 8
+    _, ps_ref, _ = O.chunk_attention(q, O.rotate(k, s), O.rotate(v, s), np.zeros((k.shape[0], 2)),
+                                     kc, vc, s, scale, 32, O.CORR_NONE)
+    _, ps_q, _ = O.chunk_attention(q, qd["kh"], qd["vh"], qd["kd"], kc, vc, s, scale, 32, O.CORR_NONE)
+    _, ps_c, _ = O.chunk_attention(q, qd["kh"], qd["vh"], qd["kd"], kc, vc, s, scale, 32, O.CORR_TAYLOR)
+    _, ps_e, _ = O.chunk_attention(q, qd["kh"], qd["vh"], qd["kd"], kc, vc, s, scale, 32, O.CORR_EXACT)
+    shift = ps_q.mean() - ps_ref.mean()
+    assert shift > 1e-3
+    assert abs(ps_c.mean() - ps_ref.mean()) < 0.5 * shift
+    assert abs(ps_e.mean() - ps_ref.mean()) < 0.5 * shift
+    assert np.mean(ps_q > ps_ref) > 0.8
+
+
+def check_int4_beats_int2_uncorrected():
+    """Section 1: INT4 keeps reasonable quality, INT2 distorts far more --
+    here, the attention output error against unquantized keys/values."""
+    errs = {}
+    for bits, group in ((2, 32), (4, 64)):
+        q, k, v, kc, vc, s, qd = _quantized_head(bits, group)
+        o_ref, _, _ = O.chunk_attention(q, O.rotate(k, s), O.rotate(v, s),
+                                        np.zeros((k.shape[0], 2)), kc, vc, s, 1 / 8, 32)
+        o, _, _ = O.chunk_attention(q, qd["kh"], qd["vh"], qd["kd"], kc, vc, s, 1 / 8, group,
+                                    O.CORR_NONE)
+        errs[bits] = np.abs(o - o_ref).mean()
+    assert errs[4] < errs[2] / 2, errs
+
+
+def check_ring_rules():
+    C, n = 10, 3
+    assert O.ring_append(0, 0, 10, C, n) == (0, 10, 1)
+    assert O.ring_append(10, 1, 10, C, n) == (10, 20, 2)
+    assert O.ring_append(20, 2, 4, C, n) == (20, 24, 0)        # partial newest chunk
+    assert O.ring_append(24, 0, 10, C, n) is None               # nothing after a partial one
+    assert O.ring_append(20, 2, 10, C, n) == (20, 30, 0)
+    assert O.ring_append(30, 0, 10, C, n) == (0, 30, 1)         # wrap: overwrite oldest
+    assert O.ring_append(30, 1, 9, C, n) is None                # full: whole chunks only
+    assert O.ring_append(30, 1, 0, C, n) == (10, 30, 1)
+    assert O.ring_append(0, 0, 11, C, n) is None
+
+
+ALL_CHECKS = [v for k, v in sorted(globals().items()) if k.startswith("check_")]
