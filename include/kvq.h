@@ -1,0 +1,198 @@
+/*
+ * kvq.h -- C ABI of libkvq: Jensen-bias-corrected low-bit KV-cache chunk
+ * attention for NVIDIA GB300 (sm_103a).
+ *
+ * Method: "Quantized Keys Steal Attention: Bias Correction for KV-Cache
+ * Compression in Video Diffusion" (Tuncer, Becker, Pfeil).  Each entry point
+ * names the passage that defines the operation it runs.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - Tensors are contiguous, row-major, BF16 stored as raw uint16_t bits:
+ *   [batch][heads][tokens][head_dim].  All pointers to tensor data are DEVICE
+ *   pointers of the current CUDA device, at least 16-byte aligned.
+ * - The caller owns every buffer (cache, inputs, outputs, workspace).  No
+ *   entry point allocates or frees memory.
+ * - Work is enqueued asynchronously on `stream` (a cudaStream_t passed as
+ *   void*, NULL = the legacy default stream).  Argument errors are detected on
+ *   the host and returned before anything is launched; a failed launch returns
+ *   KVQ_ERR_CUDA.  Faults detected inside a kernel (a bounded wait that ran
+ *   out) are recorded in a device status word read by
+ *   kvq_last_device_status().
+ * - Inputs must be finite.
+ */
+#ifndef KVQ_H
+#define KVQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  KVQ_OK = 0,
+  KVQ_ERR_INVALID_ARG = 1,  /* null pointer, bad size or mode               */
+  KVQ_ERR_UNSUPPORTED = 2,  /* head_dim / bits / group not built            */
+  KVQ_ERR_CAPACITY = 3,     /* append refused by the window rules           */
+  KVQ_ERR_CUDA = 4,         /* a CUDA runtime/driver call failed            */
+  KVQ_ERR_TIMEOUT = 5,      /* a kernel's bounded wait ran out              */
+  KVQ_ERR_ALIGNMENT = 6     /* a pointer is not 16-byte aligned             */
+} kvq_status;
+
+/* Correction applied to cached-key scores before the softmax. */
+typedef enum {
+  KVQ_CORR_NONE = 0,   /* plain quantized attention (the ablation)         */
+  KVQ_CORR_TAYLOR = 1  /* second-order Jensen-bias correction              */
+} kvq_corr;
+
+/*
+ * Quantized sliding-window KV cache (paper section 1: the current chunk
+ * attends to the last n cached chunks; section 3 "Integer quantization",
+ * Eq. (1), and "Quantization granularity": per-token groups of `group`
+ * channels with their own step size and zero point).
+ *
+ * Geometry (set by the caller, checked by every call):
+ *   head_dim in {64, 128}; bits in {2, 4}; group in {32, 64}, group <= head_dim;
+ *   capacity = chunk_tokens * n_chunks tokens per (batch, head).
+ * Ring state (owned by the library, updated by kvq_quantize_append):
+ *   len       valid tokens; attention reads tokens [0, len) of every head;
+ *   head_slot chunk slot the next append writes.
+ * Rotation: sign_bits[c / 32] bit (c % 32) set means sigma_c = -1 in the
+ *   randomized Hadamard rotation H = (1/sqrt(d)) * Sylvester(d) * diag(sigma)
+ *   (paper section 3 "Hadamard rotation").  Host values.
+ * Device buffers (caller-allocated; sizes from kvq_cache_bytes):
+ *   k_codes, v_codes  uint8  [batch][heads][capacity][head_dim * bits / 8]
+ *       packed codes: little-endian 32-bit words; INT2 channel 16w + 2k + h
+ *       at bits [2k + 16h, +2) of word w; INT4 channel 8w + 2k + h at bits
+ *       [4k + 16h, +4).
+ *   k_sz, v_sz        bf16   [batch][heads][capacity][head_dim / group][2]
+ *       (step size, zero point) per token and group; the zero point is an
+ *       integer stored as BF16.
+ */
+typedef struct kvq_cache {
+  int32_t batch, heads, head_dim, bits, group;
+  int32_t chunk_tokens, n_chunks;
+  int32_t len, head_slot;
+  uint32_t sign_bits[4];
+  uint8_t *k_codes, *v_codes;
+  uint16_t *k_sz, *v_sz;
+} kvq_cache;
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char *kvq_status_string(kvq_status s);
+
+/* Library ABI version (increments on any change of this header's ABI). */
+int32_t kvq_abi_version(void);
+
+/*
+ * Bytes of ONE codes buffer and ONE (step, zero) buffer for this geometry
+ * (k and v each need one of both).  Returns KVQ_ERR_INVALID_ARG /
+ * KVQ_ERR_UNSUPPORTED for a bad geometry.  Host only; no CUDA call.
+ */
+kvq_status kvq_cache_bytes(const kvq_cache *cache, size_t *codes_bytes,
+                           size_t *sz_bytes);
+
+/*
+ * Quantize-append one chunk (paper section 3: Hadamard rotation, then
+ * Eq. (1) per token and group; Figure 1 caption: keys AND values, QuaRot +
+ * RTN).  k_new, v_new: BF16 [batch][heads][n_new][head_dim] device.
+ * Per row: x' = H x in fp32 (fast Walsh-Hadamard transform, butterflies in
+ * the order h = 1, 2, ..., d/2, then times fl(1/sqrt(d))); per group
+ * mn/mx; D = bf16((mx - mn) / (2^bits - 1)) (constant group: D = bf16(|mn|),
+ * or 1); z = bf16(rint(-mn / D)); code = clamp(rint(x' / D) + z, 0, 2^bits-1)
+ * (IEEE fp32, ties to even).  Writes slot `head_slot` (tokens
+ * [head_slot * chunk_tokens, + n_new)).
+ * Window rules: 0 <= n_new <= chunk_tokens (0 is a no-op); while the cache is
+ * not full every earlier slot must be full (a partial chunk can only be the
+ * last one appended); once full only whole chunks overwrite the oldest slot.
+ * Otherwise KVQ_ERR_CAPACITY and nothing changes.  On success updates
+ * cache->len and cache->head_slot (host side, no synchronization).
+ */
+kvq_status kvq_quantize_append(kvq_cache *cache, const uint16_t *k_new,
+                               const uint16_t *v_new, int32_t n_new,
+                               void *stream);
+
+/*
+ * Workspace bytes kvq_attention_corrected / kvq_attention_mass need for n_q
+ * queries and n_r current-chunk tokens (rotated BF16 copies of q, k_cur,
+ * v_cur).  0 on a bad geometry.
+ */
+size_t kvq_workspace_bytes(const kvq_cache *cache, int32_t n_q, int32_t n_r);
+
+/*
+ * Corrected chunk attention (paper abstract and section 1; Figure 3 caption).
+ * Queries q [batch][heads][n_q][d] of the current chunk attend over the
+ * dequantized cached window (tokens [0, cache->len), rotated basis) and the
+ * unquantized current chunk k_cur, v_cur [batch][heads][n_r][d].  No mask.
+ *   cached score  s_ij = scale * q'_j . k_hat'_i - b_ij,
+ *   b_ij = scale^2 / 24 * sum_g ||q'_{j,g}||^2 * D_{i,g}^2   (corr = TAYLOR;
+ *          0 for corr = NONE) -- the second-order Jensen-bias correction;
+ *   current score s_ij = scale * q_j . k_i;
+ *   one softmax over both segments; out = sum_i p_ij v_i in the ORIGINAL
+ *   basis (cached values un-rotated).
+ * out: BF16 [batch][heads][n_q][d] device (required).  p_s, p_r: optional
+ * (NULL to skip) fp32 [batch][heads][n_q] device: the attention masses of the
+ * cached block and of the current chunk per query row (Figure 2 caption).
+ * workspace: device, >= kvq_workspace_bytes(cache, n_q, n_r) bytes, 16-byte
+ * aligned; its contents are scratch.  Requires cache->len + n_r >= 1 when
+ * n_q > 0.  n_q == 0 is a no-op.
+ */
+kvq_status kvq_attention_corrected(const kvq_cache *cache, const uint16_t *q,
+                                   const uint16_t *k_cur, const uint16_t *v_cur,
+                                   int32_t n_q, int32_t n_r, float scale,
+                                   int32_t corr, void *workspace,
+                                   size_t workspace_bytes, uint16_t *out,
+                                   float *p_s, float *p_r, void *stream);
+
+/*
+ * Attention masses only (paper Figure 2 caption and section 1: P_S of the
+ * cached block, P_R of the current chunk; P_S + P_R = 1 per row), with the
+ * same scores as kvq_attention_corrected.  v_cur is not read.  p_s, p_r:
+ * fp32 [batch][heads][n_q] device (both required).
+ */
+kvq_status kvq_attention_mass(const kvq_cache *cache, const uint16_t *q,
+                              const uint16_t *k_cur, int32_t n_q, int32_t n_r,
+                              float scale, int32_t corr, void *workspace,
+                              size_t workspace_bytes, float *p_s, float *p_r,
+                              void *stream);
+
+/*
+ * The rotation alone (paper section 3 "Hadamard rotation"), for checking:
+ * x' = H x per row of x [rows][d] BF16 device, written as fp32 [rows][d]
+ * (out_f32) -- exactly the fp32 values kvq_quantize_append quantizes -- or
+ * as BF16 round-to-nearest (out_bf16).  Exactly one of out_f32 / out_bf16
+ * must be non-NULL.  d in {64, 128}.
+ */
+kvq_status kvq_rotate(const uint16_t *x, int64_t rows, int32_t d,
+                      const uint32_t sign_bits[4], float *out_f32,
+                      uint16_t *out_bf16, void *stream);
+
+/*
+ * Synchronizes `stream`, then returns and clears the device status word
+ * (KVQ_OK, or the first in-kernel error since the last call, e.g.
+ * KVQ_ERR_TIMEOUT).  Returns KVQ_ERR_CUDA if the synchronization failed.
+ */
+kvq_status kvq_last_device_status(void *stream);
+
+/*
+ * Limit, in nanoseconds, of every bounded wait inside the kernels (default
+ * 2e9).  Exceeding it makes the kernel record KVQ_ERR_TIMEOUT, release its
+ * tensor memory and return.  Host setting, applies to later launches.
+ */
+kvq_status kvq_set_wait_limit_ns(uint64_t limit_ns);
+
+/*
+ * Self-test of the bounded-wait path: one block waits on a shared-memory
+ * barrier that nothing ever arrives on, for at most limit_ns, then records
+ * KVQ_ERR_TIMEOUT and returns.  No counterpart in the paper; it exists so the
+ * error path can be exercised without faulting or hanging a GPU.
+ */
+kvq_status kvq_selftest_wait_timeout(uint64_t limit_ns, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KVQ_H */

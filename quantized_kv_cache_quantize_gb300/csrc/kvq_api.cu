@@ -1,0 +1,278 @@
+// extern "C" entry points of libkvq: argument validation, the sliding-window
+// ring bookkeeping, workspace carving and kernel dispatch.  Every check here
+// runs on the host before anything is launched.
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+
+#include "kvq_internal.h"
+
+namespace {
+
+std::atomic<unsigned long long> g_wait_limit_ns{2000000000ull};
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+kvq_status check_geometry(const kvq_cache* c, kvq::Geometry* g) {
+  if (c == nullptr) return KVQ_ERR_INVALID_ARG;
+  if (c->batch < 1 || c->heads < 1 || c->chunk_tokens < 1 || c->n_chunks < 1)
+    return KVQ_ERR_INVALID_ARG;
+  if (c->head_dim != 64 && c->head_dim != 128) return KVQ_ERR_UNSUPPORTED;
+  if (c->bits != 2 && c->bits != 4) return KVQ_ERR_UNSUPPORTED;
+  if (c->group != 32 && c->group != 64) return KVQ_ERR_UNSUPPORTED;
+  if (c->group > c->head_dim) return KVQ_ERR_UNSUPPORTED;
+  const long long bh = (long long)c->batch * c->heads;
+  const long long cap = (long long)c->chunk_tokens * c->n_chunks;
+  if (bh > (1 << 16) || cap > (1LL << 30) || bh * cap > (1LL << 40)) return KVQ_ERR_INVALID_ARG;
+  if (c->len < 0 || c->len > cap || c->head_slot < 0 || c->head_slot >= c->n_chunks)
+    return KVQ_ERR_INVALID_ARG;
+  g->bh = (int)bh;
+  g->d = c->head_dim;
+  g->bits = c->bits;
+  g->group = c->group;
+  g->g = c->head_dim / c->group;
+  g->cap = (int)cap;
+  g->code_bytes = c->head_dim * c->bits / 8;
+  return KVQ_OK;
+}
+
+kvq_status check_cache_buffers(const kvq_cache* c) {
+  if (!c->k_codes || !c->v_codes || !c->k_sz || !c->v_sz) return KVQ_ERR_INVALID_ARG;
+  if (!aligned16(c->k_codes) || !aligned16(c->v_codes) || !aligned16(c->k_sz) ||
+      !aligned16(c->v_sz))
+    return KVQ_ERR_ALIGNMENT;
+  return KVQ_OK;
+}
+
+struct Workspace {
+  uint16_t* q;
+  uint16_t* k;
+  uint16_t* v;
+  size_t bytes;
+};
+
+Workspace carve(void* base, const kvq::Geometry& g, int n_q, int n_r) {
+  Workspace w;
+  const size_t qb = round_up((size_t)g.bh * n_q * g.d * 2, 256);
+  const size_t rb = round_up((size_t)g.bh * n_r * g.d * 2, 256);
+  uint8_t* p = static_cast<uint8_t*>(base);
+  w.q = reinterpret_cast<uint16_t*>(p);
+  w.k = reinterpret_cast<uint16_t*>(p + qb);
+  w.v = reinterpret_cast<uint16_t*>(p + qb + rb);
+  w.bytes = qb + 2 * rb;
+  return w;
+}
+
+kvq_status attention_common(const kvq_cache* cache, const uint16_t* q, const uint16_t* k_cur,
+                            const uint16_t* v_cur, int32_t n_q, int32_t n_r, float scale,
+                            int32_t corr, void* workspace, size_t workspace_bytes,
+                            uint16_t* out, float* p_s, float* p_r, bool mass_only,
+                            void* stream) {
+  kvq::Geometry g;
+  kvq_status st = check_geometry(cache, &g);
+  if (st != KVQ_OK) return st;
+  if (n_q < 0 || n_r < 0 || n_q > (1 << 30) || n_r > (1 << 30)) return KVQ_ERR_INVALID_ARG;
+  if (corr != KVQ_CORR_NONE && corr != KVQ_CORR_TAYLOR) return KVQ_ERR_INVALID_ARG;
+  if (!std::isfinite(scale) || scale <= 0.f) return KVQ_ERR_INVALID_ARG;
+  if ((p_s == nullptr) != (p_r == nullptr)) return KVQ_ERR_INVALID_ARG;
+  if (mass_only && p_s == nullptr) return KVQ_ERR_INVALID_ARG;
+  if (!mass_only && out == nullptr) return KVQ_ERR_INVALID_ARG;
+  if (n_q == 0) return KVQ_OK;
+  if (cache->len + n_r < 1) return KVQ_ERR_INVALID_ARG;
+  if (cache->len > 0) {
+    st = check_cache_buffers(cache);
+    if (st != KVQ_OK) return st;
+  }
+  if (q == nullptr || (n_r > 0 && k_cur == nullptr) || (!mass_only && n_r > 0 && v_cur == nullptr))
+    return KVQ_ERR_INVALID_ARG;
+  if (!aligned16(q) || (k_cur && !aligned16(k_cur)) || (v_cur && !aligned16(v_cur)) ||
+      (out && !aligned16(out)) || !aligned16(workspace))
+    return KVQ_ERR_ALIGNMENT;
+  if (workspace == nullptr) return KVQ_ERR_INVALID_ARG;
+  const Workspace ws = carve(workspace, g, n_q, n_r);
+  if (workspace_bytes < ws.bytes) return KVQ_ERR_INVALID_ARG;
+
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // rotate Q, K_cur, V_cur into the workspace (BF16, rotated basis)
+  kvq::RotateArgs ra{};
+  ra.src[0] = q;
+  ra.dst[0] = ws.q;
+  ra.rows[0] = (long long)g.bh * n_q;
+  ra.src[1] = k_cur;
+  ra.dst[1] = ws.k;
+  ra.rows[1] = (long long)g.bh * n_r;
+  ra.src[2] = v_cur;
+  ra.dst[2] = ws.v;
+  ra.rows[2] = mass_only ? 0 : (long long)g.bh * n_r;
+  for (int i = 0; i < 4; ++i) ra.sign_bits[i] = cache->sign_bits[i];
+  ra.inv_sqrt_d = (float)(1.0 / std::sqrt((double)g.d));
+  ra.out_f32 = 0;
+  if (kvq::launch_rotate(ra, g.d, s) != cudaSuccess) return KVQ_ERR_CUDA;
+
+  kvq::AttnLaunch a{};
+  a.k_codes = cache->k_codes;
+  a.v_codes = cache->v_codes;
+  a.k_sz = reinterpret_cast<const uint32_t*>(cache->k_sz);
+  a.v_sz = reinterpret_cast<const uint32_t*>(cache->v_sz);
+  a.n_s = cache->len;
+  a.cap = g.cap;
+  a.q_rot = ws.q;
+  a.k_rot = ws.k;
+  a.v_rot = ws.v;
+  a.n_q = n_q;
+  a.n_r = n_r;
+  a.bh = g.bh;
+  a.scale = scale;
+  a.corr = corr;
+  a.mass_only = mass_only ? 1 : 0;
+  a.out = out;
+  a.p_s = p_s;
+  a.p_r = p_r;
+  for (int i = 0; i < 4; ++i) a.sign_bits[i] = cache->sign_bits[i];
+  a.wait_limit_ns = g_wait_limit_ns.load();
+  return kvq::launch_attention(a, g.d, g.bits, g.group, s);
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* kvq_status_string(kvq_status s) {
+  switch (s) {
+    case KVQ_OK: return "ok";
+    case KVQ_ERR_INVALID_ARG: return "invalid argument";
+    case KVQ_ERR_UNSUPPORTED: return "unsupported head_dim/bits/group";
+    case KVQ_ERR_CAPACITY: return "append refused by the cache window rules";
+    case KVQ_ERR_CUDA: return "CUDA call failed";
+    case KVQ_ERR_TIMEOUT: return "bounded wait in a kernel ran out";
+    case KVQ_ERR_ALIGNMENT: return "pointer not 16-byte aligned";
+  }
+  return "unknown status";
+}
+
+int32_t kvq_abi_version(void) { return 1; }
+
+kvq_status kvq_cache_bytes(const kvq_cache* cache, size_t* codes_bytes, size_t* sz_bytes) {
+  kvq::Geometry g;
+  const kvq_status st = check_geometry(cache, &g);
+  if (st != KVQ_OK) return st;
+  if (codes_bytes) *codes_bytes = (size_t)g.bh * g.cap * g.code_bytes;
+  if (sz_bytes) *sz_bytes = (size_t)g.bh * g.cap * g.g * 4;
+  return KVQ_OK;
+}
+
+kvq_status kvq_quantize_append(kvq_cache* cache, const uint16_t* k_new, const uint16_t* v_new,
+                               int32_t n_new, void* stream) {
+  kvq::Geometry g;
+  kvq_status st = check_geometry(cache, &g);
+  if (st != KVQ_OK) return st;
+  if (n_new < 0) return KVQ_ERR_INVALID_ARG;
+  if (n_new > cache->chunk_tokens) return KVQ_ERR_CAPACITY;
+  if (n_new == 0) return KVQ_OK;
+  st = check_cache_buffers(cache);
+  if (st != KVQ_OK) return st;
+  if (k_new == nullptr || v_new == nullptr) return KVQ_ERR_INVALID_ARG;
+  if (!aligned16(k_new) || !aligned16(v_new)) return KVQ_ERR_ALIGNMENT;
+  // window rules: fill slots in order, a partial chunk only as the last one,
+  // whole chunks only once full
+  const int first = cache->head_slot * cache->chunk_tokens;
+  int new_len;
+  if (cache->len < g.cap) {
+    if (cache->len != first) return KVQ_ERR_CAPACITY;
+    new_len = cache->len + n_new;
+  } else {
+    if (n_new != cache->chunk_tokens) return KVQ_ERR_CAPACITY;
+    new_len = g.cap;
+  }
+  kvq::QuantArgs a{};
+  a.k_new = k_new;
+  a.v_new = v_new;
+  a.k_codes = cache->k_codes;
+  a.v_codes = cache->v_codes;
+  a.k_sz = reinterpret_cast<uint32_t*>(cache->k_sz);
+  a.v_sz = reinterpret_cast<uint32_t*>(cache->v_sz);
+  a.bh = g.bh;
+  a.n_new = n_new;
+  a.cap = g.cap;
+  a.first = first;
+  for (int i = 0; i < 4; ++i) a.sign_bits[i] = cache->sign_bits[i];
+  a.inv_sqrt_d = (float)(1.0 / std::sqrt((double)g.d));
+  bool supported = true;
+  if (kvq::launch_quantize_append(a, g.d, g.bits, g.group, static_cast<cudaStream_t>(stream),
+                                  &supported) != cudaSuccess)
+    return KVQ_ERR_CUDA;
+  if (!supported) return KVQ_ERR_UNSUPPORTED;
+  cache->len = new_len;
+  cache->head_slot = (cache->head_slot + 1) % cache->n_chunks;
+  return KVQ_OK;
+}
+
+size_t kvq_workspace_bytes(const kvq_cache* cache, int32_t n_q, int32_t n_r) {
+  kvq::Geometry g;
+  if (check_geometry(cache, &g) != KVQ_OK || n_q < 0 || n_r < 0) return 0;
+  return carve(nullptr, g, n_q, n_r).bytes;
+}
+
+kvq_status kvq_attention_corrected(const kvq_cache* cache, const uint16_t* q,
+                                   const uint16_t* k_cur, const uint16_t* v_cur, int32_t n_q,
+                                   int32_t n_r, float scale, int32_t corr, void* workspace,
+                                   size_t workspace_bytes, uint16_t* out, float* p_s, float* p_r,
+                                   void* stream) {
+  return attention_common(cache, q, k_cur, v_cur, n_q, n_r, scale, corr, workspace,
+                          workspace_bytes, out, p_s, p_r, false, stream);
+}
+
+kvq_status kvq_attention_mass(const kvq_cache* cache, const uint16_t* q, const uint16_t* k_cur,
+                              int32_t n_q, int32_t n_r, float scale, int32_t corr,
+                              void* workspace, size_t workspace_bytes, float* p_s, float* p_r,
+                              void* stream) {
+  if (p_s == nullptr || p_r == nullptr) return KVQ_ERR_INVALID_ARG;
+  return attention_common(cache, q, k_cur, nullptr, n_q, n_r, scale, corr, workspace,
+                          workspace_bytes, nullptr, p_s, p_r, true, stream);
+}
+
+kvq_status kvq_rotate(const uint16_t* x, int64_t rows, int32_t d, const uint32_t sign_bits[4],
+                      float* out_f32, uint16_t* out_bf16, void* stream) {
+  if (d != 64 && d != 128) return KVQ_ERR_UNSUPPORTED;
+  if (rows < 0 || sign_bits == nullptr) return KVQ_ERR_INVALID_ARG;
+  if ((out_f32 == nullptr) == (out_bf16 == nullptr)) return KVQ_ERR_INVALID_ARG;
+  if (rows == 0) return KVQ_OK;
+  if (x == nullptr) return KVQ_ERR_INVALID_ARG;
+  if (!aligned16(x) || (out_f32 && !aligned16(out_f32)) || (out_bf16 && !aligned16(out_bf16)))
+    return KVQ_ERR_ALIGNMENT;
+  kvq::RotateArgs a{};
+  a.src[0] = x;
+  a.dst[0] = out_f32 ? static_cast<void*>(out_f32) : static_cast<void*>(out_bf16);
+  a.rows[0] = rows;
+  for (int i = 0; i < 4; ++i) a.sign_bits[i] = sign_bits[i];
+  a.inv_sqrt_d = (float)(1.0 / std::sqrt((double)d));
+  a.out_f32 = out_f32 ? 1 : 0;
+  return kvq::launch_rotate(a, d, static_cast<cudaStream_t>(stream)) == cudaSuccess ? KVQ_OK
+                                                                                    : KVQ_ERR_CUDA;
+}
+
+kvq_status kvq_last_device_status(void* stream) {
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return KVQ_ERR_CUDA;
+  int st = 0;
+  if (kvq::read_and_clear_attention_status(&st) != KVQ_OK) return KVQ_ERR_CUDA;
+  return static_cast<kvq_status>(st);
+}
+
+kvq_status kvq_set_wait_limit_ns(uint64_t limit_ns) {
+  if (limit_ns == 0) return KVQ_ERR_INVALID_ARG;
+  g_wait_limit_ns.store(limit_ns);
+  return KVQ_OK;
+}
+
+kvq_status kvq_selftest_wait_timeout(uint64_t limit_ns, void* stream) {
+  if (limit_ns == 0 || limit_ns > 10000000000ull) return KVQ_ERR_INVALID_ARG;
+  return kvq::launch_wait_selftest(limit_ns, static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? KVQ_OK
+             : KVQ_ERR_CUDA;
+}
+
+}  // extern "C"

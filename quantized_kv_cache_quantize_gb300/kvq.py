@@ -1,0 +1,252 @@
+"""Thin Python binding of libkvq (ctypes).  Argument marshalling only: every
+step of the computation runs in the library's CUDA kernels; torch is used for
+device memory and streams.  There is no CPU fallback: if libkvq.so is missing
+the first call raises."""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+
+import numpy as np
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libkvq.so")
+
+KVQ_OK = 0
+KVQ_ERR_INVALID_ARG = 1
+KVQ_ERR_UNSUPPORTED = 2
+KVQ_ERR_CAPACITY = 3
+KVQ_ERR_CUDA = 4
+KVQ_ERR_TIMEOUT = 5
+KVQ_ERR_ALIGNMENT = 6
+
+CORR_NONE = 0
+CORR_TAYLOR = 1
+
+
+class KVQError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {status_string(status)} (status {status})")
+
+
+class CacheStruct(ctypes.Structure):
+    """Mirror of ``kvq_cache`` in include/kvq.h."""
+    _fields_ = [
+        ("batch", ctypes.c_int32), ("heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
+        ("bits", ctypes.c_int32), ("group", ctypes.c_int32),
+        ("chunk_tokens", ctypes.c_int32), ("n_chunks", ctypes.c_int32),
+        ("len", ctypes.c_int32), ("head_slot", ctypes.c_int32),
+        ("sign_bits", ctypes.c_uint32 * 4),
+        ("k_codes", ctypes.c_void_p), ("v_codes", ctypes.c_void_p),
+        ("k_sz", ctypes.c_void_p), ("v_sz", ctypes.c_void_p),
+    ]
+
+
+_P = ctypes.c_void_p
+_SIGNATURES = {
+    "kvq_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+    "kvq_abi_version": (ctypes.c_int32, []),
+    "kvq_cache_bytes": (ctypes.c_int, [_P, ctypes.POINTER(ctypes.c_size_t),
+                                       ctypes.POINTER(ctypes.c_size_t)]),
+    "kvq_quantize_append": (ctypes.c_int, [_P, _P, _P, ctypes.c_int32, _P]),
+    "kvq_workspace_bytes": (ctypes.c_size_t, [_P, ctypes.c_int32, ctypes.c_int32]),
+    "kvq_attention_corrected": (ctypes.c_int, [_P, _P, _P, _P, ctypes.c_int32, ctypes.c_int32,
+                                               ctypes.c_float, ctypes.c_int32, _P, ctypes.c_size_t,
+                                               _P, _P, _P, _P]),
+    "kvq_attention_mass": (ctypes.c_int, [_P, _P, _P, ctypes.c_int32, ctypes.c_int32,
+                                          ctypes.c_float, ctypes.c_int32, _P, ctypes.c_size_t,
+                                          _P, _P, _P]),
+    "kvq_rotate": (ctypes.c_int, [_P, ctypes.c_int64, ctypes.c_int32, _P, _P, _P, _P]),
+    "kvq_last_device_status": (ctypes.c_int, [_P]),
+    "kvq_set_wait_limit_ns": (ctypes.c_int, [ctypes.c_uint64]),
+    "kvq_selftest_wait_timeout": (ctypes.c_int, [ctypes.c_uint64, _P]),
+}
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded libkvq.so; raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"libkvq.so not built ({LIB_PATH}); run __graft_entry__.build()")
+        h = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in _SIGNATURES.items():
+            f = getattr(h, name)
+            f.restype = res
+            f.argtypes = args
+        _lib = h
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return lib().kvq_status_string(status).decode()
+
+
+def _check(status: int, what: str):
+    if status != KVQ_OK:
+        raise KVQError(status, what)
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _ptr(t: torch.Tensor | None) -> ctypes.c_void_p:
+    return ctypes.c_void_p(0 if t is None else t.data_ptr())
+
+
+def sign_bits(signs) -> list[int]:
+    """Bit c of word c // 32 set where sigma_c = -1."""
+    s = np.asarray(signs).reshape(-1)
+    words = [0, 0, 0, 0]
+    for c, v in enumerate(s):
+        if v < 0:
+            words[c >> 5] |= 1 << (c & 31)
+    return words
+
+
+def _bf16_dev(t: torch.Tensor, name: str) -> torch.Tensor:
+    if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous CUDA bfloat16 tensor")
+    return t
+
+
+class KVCache:
+    """A quantized sliding-window KV cache in device memory (torch-allocated)
+    and its ``kvq_cache`` descriptor."""
+
+    def __init__(self, batch: int, heads: int, head_dim: int, bits: int, group: int,
+                 chunk_tokens: int, n_chunks: int, signs, device="cuda"):
+        c = CacheStruct()
+        c.batch, c.heads, c.head_dim = batch, heads, head_dim
+        c.bits, c.group = bits, group
+        c.chunk_tokens, c.n_chunks = chunk_tokens, n_chunks
+        c.len, c.head_slot = 0, 0
+        for i, w in enumerate(sign_bits(signs)):
+            c.sign_bits[i] = w
+        codes_b, sz_b = ctypes.c_size_t(), ctypes.c_size_t()
+        _check(lib().kvq_cache_bytes(ctypes.byref(c), ctypes.byref(codes_b), ctypes.byref(sz_b)),
+               "kvq_cache_bytes")
+        self.signs = np.asarray(signs, dtype=np.float32)
+        self.k_codes = torch.zeros(codes_b.value, dtype=torch.uint8, device=device)
+        self.v_codes = torch.zeros(codes_b.value, dtype=torch.uint8, device=device)
+        self.k_sz = torch.zeros(sz_b.value // 2, dtype=torch.int16, device=device)
+        self.v_sz = torch.zeros(sz_b.value // 2, dtype=torch.int16, device=device)
+        c.k_codes, c.v_codes = self.k_codes.data_ptr(), self.v_codes.data_ptr()
+        c.k_sz, c.v_sz = self.k_sz.data_ptr(), self.v_sz.data_ptr()
+        self.struct = c
+
+    # geometry
+    batch = property(lambda self: self.struct.batch)
+    heads = property(lambda self: self.struct.heads)
+    head_dim = property(lambda self: self.struct.head_dim)
+    bits = property(lambda self: self.struct.bits)
+    group = property(lambda self: self.struct.group)
+    chunk_tokens = property(lambda self: self.struct.chunk_tokens)
+    n_chunks = property(lambda self: self.struct.n_chunks)
+    capacity = property(lambda self: self.struct.chunk_tokens * self.struct.n_chunks)
+    len = property(lambda self: self.struct.len)
+    head_slot = property(lambda self: self.struct.head_slot)
+
+    def codes_view(self, which: str) -> torch.Tensor:
+        t = self.k_codes if which == "k" else self.v_codes
+        return t.view(self.batch, self.heads, self.capacity, self.head_dim * self.bits // 8)
+
+    def sz_view(self, which: str) -> torch.Tensor:
+        t = self.k_sz if which == "k" else self.v_sz
+        return t.view(self.batch, self.heads, self.capacity, self.head_dim // self.group, 2)
+
+    def workspace_bytes(self, n_q: int, n_r: int) -> int:
+        return int(lib().kvq_workspace_bytes(ctypes.byref(self.struct), n_q, n_r))
+
+
+def quantize_append(cache: KVCache, k_new: torch.Tensor, v_new: torch.Tensor, stream=None):
+    """kvq_quantize_append: k_new/v_new [B, H, n_new, d] bf16 on the device."""
+    _bf16_dev(k_new, "k_new")
+    _bf16_dev(v_new, "v_new")
+    n_new = k_new.shape[-2] if k_new.dim() >= 2 else 0
+    if tuple(k_new.shape) != tuple(v_new.shape):
+        raise ValueError("k_new and v_new shapes differ")
+    _check(lib().kvq_quantize_append(ctypes.byref(cache.struct), _ptr(k_new), _ptr(v_new),
+                                     n_new, _stream(stream)), "kvq_quantize_append")
+
+
+def attention_corrected(cache: KVCache, q, k_cur, v_cur, scale: float | None = None,
+                        corr: int = CORR_TAYLOR, out=None, with_mass: bool = False,
+                        workspace=None, stream=None):
+    """kvq_attention_corrected.  q [B, H, n_q, d], k_cur/v_cur [B, H, n_r, d]
+    bf16 on the device.  Returns out (and (p_s, p_r) when with_mass)."""
+    _bf16_dev(q, "q")
+    _bf16_dev(k_cur, "k_cur")
+    _bf16_dev(v_cur, "v_cur")
+    n_q, n_r = q.shape[-2], k_cur.shape[-2]
+    d = cache.head_dim
+    scale = 1.0 / math.sqrt(d) if scale is None else scale
+    if out is None:
+        out = torch.empty_like(q)
+    ps = pr = None
+    if with_mass:
+        ps = torch.empty(q.shape[:-1], dtype=torch.float32, device=q.device)
+        pr = torch.empty_like(ps)
+    ws_bytes = cache.workspace_bytes(n_q, n_r)
+    if workspace is None:
+        workspace = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=q.device)
+    _check(lib().kvq_attention_corrected(
+        ctypes.byref(cache.struct), _ptr(q), _ptr(k_cur), _ptr(v_cur), n_q, n_r,
+        ctypes.c_float(scale), corr, _ptr(workspace), workspace.numel(), _ptr(out),
+        _ptr(ps), _ptr(pr), _stream(stream)), "kvq_attention_corrected")
+    return (out, ps, pr) if with_mass else out
+
+
+def attention_mass(cache: KVCache, q, k_cur, scale: float | None = None,
+                   corr: int = CORR_TAYLOR, workspace=None, stream=None):
+    """kvq_attention_mass: returns (p_s, p_r), each [B, H, n_q] fp32."""
+    _bf16_dev(q, "q")
+    _bf16_dev(k_cur, "k_cur")
+    n_q, n_r = q.shape[-2], k_cur.shape[-2]
+    scale = 1.0 / math.sqrt(cache.head_dim) if scale is None else scale
+    ps = torch.empty(q.shape[:-1], dtype=torch.float32, device=q.device)
+    pr = torch.empty_like(ps)
+    ws_bytes = cache.workspace_bytes(n_q, n_r)
+    if workspace is None:
+        workspace = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=q.device)
+    _check(lib().kvq_attention_mass(
+        ctypes.byref(cache.struct), _ptr(q), _ptr(k_cur), n_q, n_r, ctypes.c_float(scale), corr,
+        _ptr(workspace), workspace.numel(), _ptr(ps), _ptr(pr), _stream(stream)),
+        "kvq_attention_mass")
+    return ps, pr
+
+
+def rotate(x: torch.Tensor, signs, out_dtype=torch.float32, stream=None) -> torch.Tensor:
+    """kvq_rotate: x [..., d] bf16 -> H x in fp32 (the values the quantizer
+    sees) or bf16."""
+    _bf16_dev(x, "x")
+    d = x.shape[-1]
+    rows = x.numel() // d if d else 0
+    out = torch.empty(x.shape, dtype=out_dtype, device=x.device)
+    sb = (ctypes.c_uint32 * 4)(*sign_bits(signs))
+    f32 = out if out_dtype == torch.float32 else None
+    b16 = out if out_dtype == torch.bfloat16 else None
+    _check(lib().kvq_rotate(_ptr(x), rows, d, sb, _ptr(f32), _ptr(b16), _stream(stream)),
+           "kvq_rotate")
+    return out
+
+
+def last_device_status(stream=None) -> int:
+    return int(lib().kvq_last_device_status(_stream(stream)))
+
+
+def set_wait_limit_ns(limit_ns: int):
+    _check(lib().kvq_set_wait_limit_ns(int(limit_ns)), "kvq_set_wait_limit_ns")
+
+
+def selftest_wait_timeout(limit_ns: int, stream=None):
+    _check(lib().kvq_selftest_wait_timeout(int(limit_ns), _stream(stream)),
+           "kvq_selftest_wait_timeout")

@@ -1,0 +1,54 @@
+"""Shared helpers of the GPU parity tests: build a cache through the C-ABI,
+and compute the oracle's answer from the same seeded BF16 inputs (never from
+anything the CUDA path produced)."""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+from oracle import kvq_oracle as O
+from quantized_kv_cache_quantize_gb300 import kvq, synth
+
+O_TOL = 2e-2      # max-abs error of O, relative to max |O_ref| over compared rows
+MASS_TOL = 1e-3   # absolute error of P_S, P_R per row
+
+
+def build_cache(w: synth.Workload, x: dict, signs, n_s: int | None = None) -> kvq.KVCache:
+    """Quantize-append the window k_win/v_win chunk by chunk (the last chunk
+    may be partial)."""
+    n_s = x["k_win"].shape[-2] if n_s is None else n_s
+    cache = kvq.KVCache(x["k_win"].shape[0], x["k_win"].shape[1], w.head_dim, w.bits, w.group,
+                        w.chunk_tokens, w.n_chunks, signs)
+    kw = x["k_win"].cuda()
+    vw = x["v_win"].cuda()
+    for c0 in range(0, n_s, w.chunk_tokens):
+        c1 = min(n_s, c0 + w.chunk_tokens)
+        kvq.quantize_append(cache, kw[:, :, c0:c1].contiguous(), vw[:, :, c0:c1].contiguous())
+    return cache
+
+
+def oracle_head(w: synth.Workload, x: dict, signs, b: int, h: int, rows, corr: int,
+                n_s: int | None = None):
+    """Oracle O, P_S, P_R of query rows ``rows`` of head (b, h)."""
+    n_s = x["k_win"].shape[-2] if n_s is None else n_s
+    kf = x["k_win"][b, h, :n_s].float().numpy()
+    vf = x["v_win"][b, h, :n_s].float().numpy()
+    _, kd, kz, _, kc = O.quantize_rows(kf, signs, w.bits, w.group)
+    _, vd, vz, _, vc = O.quantize_rows(vf, signs, w.bits, w.group)
+    q = x["q"][b, h].float().numpy()[rows]
+    return O.chunk_attention(q, O.dequantize(kc, kd, kz, w.group), O.dequantize(vc, vd, vz, w.group),
+                             kd, x["k_cur"][b, h].float().numpy(), x["v_cur"][b, h].float().numpy(),
+                             signs, w.scale, w.group, corr)
+
+
+def assert_close(o_gpu, o_ref, ps_gpu=None, ps_ref=None, pr_gpu=None, pr_ref=None, what=""):
+    o_gpu = np.asarray(o_gpu, dtype=np.float64)
+    err = np.abs(o_gpu - o_ref).max()
+    ref = np.abs(o_ref).max()
+    assert np.all(np.isfinite(o_gpu)), what
+    assert err <= O_TOL * ref, f"{what}: max|dO| {err:.4g} > {O_TOL} * {ref:.4g}"
+    if ps_gpu is not None:
+        e_s = np.abs(np.asarray(ps_gpu, np.float64) - ps_ref).max()
+        e_r = np.abs(np.asarray(pr_gpu, np.float64) - pr_ref).max()
+        assert e_s <= MASS_TOL and e_r <= MASS_TOL, f"{what}: mass err {e_s:.3g} {e_r:.3g}"
+    return err / ref

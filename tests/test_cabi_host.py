@@ -1,0 +1,147 @@
+"""The C-ABI library on the host (no GPU needed): it loads, exports every
+symbol include/kvq.h declares, and rejects bad arguments before launching
+anything."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+from oracle import kvq_oracle as O
+from quantized_kv_cache_quantize_gb300 import kvq
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared():
+    src = open(os.path.join(ROOT, "include", "kvq.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(kvq_[a-z0-9_]+)\s*\(", src)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(kvq.LIB_PATH):
+        import __graft_entry__
+        __graft_entry__.build()
+    return kvq.lib()
+
+
+def test_exports_every_declared_symbol(lib):
+    names = _declared()
+    assert len(names) >= 10
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_status_strings(lib):
+    for s in range(7):
+        assert kvq.status_string(s)
+    assert kvq.status_string(99) == "unknown status"
+
+
+def _cache(**kw):
+    c = kvq.CacheStruct()
+    c.batch, c.heads, c.head_dim, c.bits, c.group = 1, 2, 128, 2, 32
+    c.chunk_tokens, c.n_chunks, c.len, c.head_slot = 10, 3, 0, 0
+    # fake, aligned, never dereferenced: every call below fails validation
+    # (or is a no-op) before anything touches device memory
+    c.k_codes = c.v_codes = c.k_sz = c.v_sz = 0x10000
+    for k, v in kw.items():
+        setattr(c, k, v)
+    return c
+
+
+def test_cache_bytes(lib):
+    c = _cache()
+    cb, sb = ctypes.c_size_t(), ctypes.c_size_t()
+    assert lib.kvq_cache_bytes(ctypes.byref(c), ctypes.byref(cb), ctypes.byref(sb)) == 0
+    assert cb.value == 2 * 30 * 32 and sb.value == 2 * 30 * 4 * 4
+    c = _cache(bits=4, group=64)
+    assert lib.kvq_cache_bytes(ctypes.byref(c), ctypes.byref(cb), ctypes.byref(sb)) == 0
+    assert cb.value == 2 * 30 * 64 and sb.value == 2 * 30 * 2 * 4
+
+
+@pytest.mark.parametrize("field,value,status", [
+    ("head_dim", 96, kvq.KVQ_ERR_UNSUPPORTED),
+    ("bits", 3, kvq.KVQ_ERR_UNSUPPORTED),
+    ("group", 16, kvq.KVQ_ERR_UNSUPPORTED),
+    ("batch", 0, kvq.KVQ_ERR_INVALID_ARG),
+    ("n_chunks", 0, kvq.KVQ_ERR_INVALID_ARG),
+    ("len", 31, kvq.KVQ_ERR_INVALID_ARG),
+    ("head_slot", 3, kvq.KVQ_ERR_INVALID_ARG),
+])
+def test_bad_geometry(lib, field, value, status):
+    c = _cache(**{field: value})
+    assert lib.kvq_cache_bytes(ctypes.byref(c), None, None) == status
+    assert lib.kvq_quantize_append(ctypes.byref(c), 0x10000, 0x10000, 5, None) == status
+
+
+def test_append_window_rules_match_oracle(lib):
+    """Every refused append is refused on the host, with the state untouched;
+    the accepted ones agree with the oracle's ring rules."""
+    C, n = 10, 3
+    cases = [(20, 2, 4), (24, 0, 10), (30, 1, 9), (0, 0, 11), (10, 0, 10), (5, 0, 10)]
+    for length, head, n_new in cases:
+        want = O.ring_append(length, head, n_new, C, n)
+        c = _cache(len=length, head_slot=head)
+        if want is None:
+            st = lib.kvq_quantize_append(ctypes.byref(c), 0x10000, 0x10000, n_new, None)
+            assert st == kvq.KVQ_ERR_CAPACITY, (length, head, n_new, st)
+            assert (c.len, c.head_slot) == (length, head)
+    # zero-length append is a no-op that succeeds without touching anything
+    c = _cache(len=24, head_slot=0)
+    assert lib.kvq_quantize_append(ctypes.byref(c), 0x10000, 0x10000, 0, None) == 0
+    assert (c.len, c.head_slot) == (24, 0)
+
+
+def test_append_argument_checks(lib):
+    c = _cache()
+    assert lib.kvq_quantize_append(ctypes.byref(c), 0, 0x10000, 5, None) == kvq.KVQ_ERR_INVALID_ARG
+    assert lib.kvq_quantize_append(ctypes.byref(c), 0x10008, 0x10000, 5, None) == kvq.KVQ_ERR_ALIGNMENT
+    assert lib.kvq_quantize_append(ctypes.byref(c), 0x10000, 0x10000, -1, None) == kvq.KVQ_ERR_INVALID_ARG
+    c = _cache(k_codes=0x10004)
+    assert lib.kvq_quantize_append(ctypes.byref(c), 0x10000, 0x10000, 5, None) == kvq.KVQ_ERR_ALIGNMENT
+    assert lib.kvq_quantize_append(None, 0x10000, 0x10000, 5, None) == kvq.KVQ_ERR_INVALID_ARG
+
+
+def test_attention_argument_checks(lib):
+    c = _cache(len=30)
+    ws = lib.kvq_workspace_bytes(ctypes.byref(c), 100, 10)
+    assert ws >= 2 * 100 * 128 * 2 + 2 * 2 * 10 * 128 * 2
+    f = lib.kvq_attention_corrected
+    P = 0x10000
+    # bad correction mode, bad scale, missing output, workspace too small
+    assert f(ctypes.byref(c), P, P, P, 100, 10, 0.1, 7, P, ws, P, None, None, None) == 1
+    assert f(ctypes.byref(c), P, P, P, 100, 10, float("nan"), 1, P, ws, P, None, None, None) == 1
+    assert f(ctypes.byref(c), P, P, P, 100, 10, -1.0, 1, P, ws, P, None, None, None) == 1
+    assert f(ctypes.byref(c), P, P, P, 100, 10, 0.1, 1, P, ws, None, None, None, None) == 1
+    assert f(ctypes.byref(c), P, P, P, 100, 10, 0.1, 1, P, ws - 16, P, None, None, None) == 1
+    assert f(ctypes.byref(c), P, P, P, 100, 10, 0.1, 1, P, ws, P, P, None, None) == 1
+    assert f(ctypes.byref(c), P + 2, P, P, 100, 10, 0.1, 1, P, ws, P, None, None, None) == 6
+    # nothing to attend to
+    c0 = _cache(len=0)
+    assert f(ctypes.byref(c0), P, P, P, 100, 0, 0.1, 1, P, ws, P, None, None, None) == 1
+    # no queries: a no-op
+    assert f(ctypes.byref(c), P, P, P, 0, 10, 0.1, 1, P, ws, P, None, None, None) == 0
+    g = lib.kvq_attention_mass
+    assert g(ctypes.byref(c), P, P, 100, 10, 0.1, 1, P, ws, None, None, None) == 1
+
+
+def test_rotate_argument_checks(lib):
+    sb = (ctypes.c_uint32 * 4)(0, 0, 0, 0)
+    assert lib.kvq_rotate(0x10000, 4, 96, sb, 0x10000, None, None) == kvq.KVQ_ERR_UNSUPPORTED
+    assert lib.kvq_rotate(0x10000, 4, 64, sb, 0x10000, 0x10000, None) == kvq.KVQ_ERR_INVALID_ARG
+    assert lib.kvq_rotate(0x10000, 4, 64, sb, None, None, None) == kvq.KVQ_ERR_INVALID_ARG
+    assert lib.kvq_rotate(0x10000, 0, 64, sb, 0x10000, None, None) == 0
+    assert lib.kvq_set_wait_limit_ns(0) == kvq.KVQ_ERR_INVALID_ARG
+    assert lib.kvq_selftest_wait_timeout(0, None) == kvq.KVQ_ERR_INVALID_ARG
+
+
+def test_sign_bits_roundtrip():
+    rng = np.random.default_rng(0)
+    s = np.where(rng.integers(0, 2, 128) == 1, -1.0, 1.0)
+    words = kvq.sign_bits(s)
+    back = [(-1.0 if (words[c >> 5] >> (c & 31)) & 1 else 1.0) for c in range(128)]
+    assert np.array_equal(back, s)

@@ -1,0 +1,141 @@
+"""GPU parity of the corrected chunk attention and the attention masses
+against the oracle, through the C-ABI: O within 2e-2 x max|O_ref| (max-abs),
+P_S and P_R within 1e-3 per row.  Small cases compare every row; the full
+workloads compare sampled rows of every head."""
+import numpy as np
+import pytest
+import torch
+
+from oracle import kvq_oracle as O
+from quantized_kv_cache_quantize_gb300 import kvq, synth
+from tests.gpu_common import assert_close, build_cache, oracle_head
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.mark.parametrize("corr", [kvq.CORR_TAYLOR, kvq.CORR_NONE])
+def test_tiny_all_rows(corr):
+    w = synth.WORKLOADS["tiny"]
+    x = synth.inputs(w)
+    s = synth.hadamard_signs(w.head_dim)
+    cache = build_cache(w, x, s)
+    out, ps, pr = kvq.attention_corrected(cache, x["q"].cuda(), x["k_cur"].cuda(),
+                                          x["v_cur"].cuda(), corr=corr, with_mass=True)
+    torch.cuda.synchronize()
+    assert kvq.last_device_status() == 0
+    rows = np.arange(w.n_q)
+    o_ref, ps_ref, pr_ref = oracle_head(w, x, s, 0, 0, rows, corr)
+    assert_close(out[0, 0].float().cpu().numpy(), o_ref, ps[0, 0].cpu().numpy(), ps_ref,
+                 pr[0, 0].cpu().numpy(), pr_ref, what=f"tiny corr={corr}")
+    # the masses sum to one and the mass-only entry point agrees
+    ps2, pr2 = kvq.attention_mass(cache, x["q"].cuda(), x["k_cur"].cuda(), corr=corr)
+    assert torch.allclose(ps2, ps, atol=1e-6) and torch.allclose(pr2, pr, atol=1e-6)
+    assert torch.allclose(ps + pr, torch.ones_like(ps), atol=1e-5)
+
+
+RAGGED = [
+    # (d, bits, group, n_q, n_s, n_r, chunk, n_chunks, heads)
+    (64, 2, 32, 1, 1, 1, 1, 1, 1),
+    (64, 2, 32, 129, 300, 130, 128, 3, 2),
+    (128, 2, 32, 127, 129, 1, 129, 1, 2),
+    (128, 4, 64, 257, 127, 257, 64, 2, 1),
+    (128, 2, 64, 200, 0, 77, 50, 2, 2),
+    (64, 4, 32, 140, 256, 0, 128, 2, 1),
+    (128, 4, 32, 64, 390, 5, 100, 4, 3),
+    (64, 4, 64, 33, 70, 70, 35, 2, 1),
+]
+
+
+@pytest.mark.parametrize("case", RAGGED, ids=lambda c: "d{}b{}g{}_q{}_s{}_r{}".format(*c[:6]))
+@pytest.mark.parametrize("corr", [kvq.CORR_TAYLOR, kvq.CORR_NONE])
+def test_ragged_all_rows(case, corr):
+    """Sizes that are not multiples of the 128-token tile, an empty cache, an
+    empty current chunk, single tokens."""
+    d, bits, group, n_q, n_s, n_r, chunk, n_chunks, heads = case
+    w = synth.Workload("ragged", heads=heads, head_dim=d, chunk_tokens=chunk, n_chunks=n_chunks,
+                       bits=bits, group=group, n_outliers_fixed=2, outlier_scale=6.0,
+                       offset_std=0.3)
+    x = synth.inputs(w, n_q=n_q, n_s=n_s, n_r=n_r)
+    s = synth.hadamard_signs(d, seed=3)
+    cache = build_cache(w, x, s, n_s=n_s)
+    assert cache.len == n_s
+    out, ps, pr = kvq.attention_corrected(cache, x["q"].cuda(), x["k_cur"].cuda(),
+                                          x["v_cur"].cuda(), corr=corr, with_mass=True)
+    torch.cuda.synchronize()
+    assert kvq.last_device_status() == 0
+    for h in range(heads):
+        o_ref, ps_ref, pr_ref = oracle_head(w, x, s, 0, h, np.arange(n_q), corr, n_s=n_s)
+        assert_close(out[0, h].float().cpu().numpy(), o_ref, ps[0, h].cpu().numpy(), ps_ref,
+                     pr[0, h].cpu().numpy(), pr_ref, what=f"{case} h{h}")
+
+
+def test_batch_and_heads_layout():
+    """batch 2 x heads 3: each (b, h) attends to its own cache and chunk."""
+    w = synth.Workload("bh", heads=3, head_dim=128, chunk_tokens=100, n_chunks=2, bits=2,
+                       group=32, n_outliers_fixed=3, outlier_scale=10.0, offset_std=0.5)
+    xs = [synth.inputs(w, seed=sd, n_q=150, n_s=200, n_r=90) for sd in (1, 2)]
+    x = {k: torch.cat([xs[0][k], xs[1][k]], dim=0).contiguous() for k in xs[0]}
+    s = synth.hadamard_signs(128, seed=5)
+    cache = build_cache(w, x, s)
+    out, ps, pr = kvq.attention_corrected(cache, x["q"].cuda(), x["k_cur"].cuda(),
+                                          x["v_cur"].cuda(), with_mass=True)
+    torch.cuda.synchronize()
+    for b in range(2):
+        for h in range(3):
+            o_ref, ps_ref, pr_ref = oracle_head(w, x, s, b, h, np.arange(150), O.CORR_TAYLOR)
+            assert_close(out[b, h].float().cpu().numpy(), o_ref, ps[b, h].cpu().numpy(), ps_ref,
+                         pr[b, h].cpu().numpy(), pr_ref, what=f"b{b} h{h}")
+
+
+def test_correction_restores_mass():
+    """Figure 2 / Figure 4 direction on the GPU: the INT2 cache raises P_S
+    over unquantized keys; the correction brings it back."""
+    w = synth.WORKLOADS["tiny"]
+    x = synth.inputs(w)
+    s = synth.hadamard_signs(w.head_dim)
+    cache = build_cache(w, x, s)
+    q, kc = x["q"].cuda(), x["k_cur"].cuda()
+    ps_none, _ = kvq.attention_mass(cache, q, kc, corr=kvq.CORR_NONE)
+    ps_corr, _ = kvq.attention_mass(cache, q, kc, corr=kvq.CORR_TAYLOR)
+    kf = x["k_win"][0, 0].float().numpy()
+    _, ps_ref, _ = O.chunk_attention(x["q"][0, 0].float().numpy(), O.rotate(kf, s),
+                                     O.rotate(x["v_win"][0, 0].float().numpy(), s),
+                                     np.zeros((kf.shape[0], 2)), x["k_cur"][0, 0].float().numpy(),
+                                     x["v_cur"][0, 0].float().numpy(), s, w.scale, w.group,
+                                     O.CORR_NONE)
+    shift = ps_none.mean().item() - ps_ref.mean()
+    assert shift > 0
+    assert abs(ps_corr.mean().item() - ps_ref.mean()) < 0.5 * shift
+
+
+@pytest.mark.parametrize("name", ["w4_int2", "w4_int4", "w8_int2", "hires_t3"])
+def test_full_workload_sampled_rows(name):
+    """Full-size workloads in the launch configuration the benchmark times:
+    all heads, 48 sampled query rows per head (always including the first
+    and last rows) against the oracle."""
+    w = synth.WORKLOADS[name]
+    x = synth.inputs(w)
+    s = synth.hadamard_signs(w.head_dim)
+    cache = build_cache(w, x, s)
+    out, ps, pr = kvq.attention_corrected(cache, x["q"].cuda(), x["k_cur"].cuda(),
+                                          x["v_cur"].cuda(), with_mass=True)
+    torch.cuda.synchronize()
+    assert kvq.last_device_status() == 0
+    rng = np.random.default_rng(11)
+    heads = range(w.heads) if w.heads <= 24 else rng.choice(w.heads, 12, replace=False)
+    for h in heads:
+        rows = np.unique(np.concatenate([[0, w.n_q - 1], rng.choice(w.n_q, 46, replace=False)]))
+        o_ref, ps_ref, pr_ref = oracle_head(w, x, s, 0, int(h), rows, O.CORR_TAYLOR)
+        assert_close(out[0, h, rows].float().cpu().numpy(), o_ref, ps[0, h, rows].cpu().numpy(),
+                     ps_ref, pr[0, h, rows].cpu().numpy(), pr_ref, what=f"{name} h{h}")
+
+
+def test_bounded_wait_reports_timeout():
+    """A kernel waits on a barrier nothing arrives on: the wait runs out after
+    the limit, the kernel returns, the status reads TIMEOUT once, and the
+    context stays usable."""
+    kvq.selftest_wait_timeout(2_000_000)          # 2 ms
+    assert kvq.last_device_status() == kvq.KVQ_ERR_TIMEOUT
+    assert kvq.last_device_status() == kvq.KVQ_OK
+    t = torch.ones(10, device="cuda")
+    assert float(t.sum().item()) == 10.0
