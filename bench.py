@@ -1,0 +1,387 @@
+"""Benchmark of the hot path: one streaming step = quantize-append of a new
+chunk into the INT2 window cache, rotation of the current chunk, and the
+Jensen-bias-corrected chunk attention with P_S / P_R (all through libkvq).
+
+Default workload: one layer, 24 heads, head_dim 128, a 4680-token chunk
+(3 latent frames x 30 x 52) over a 4-chunk (18720-token) INT2 g32 window --
+the configuration the headline metric is quoted on.  Synthetic inputs.
+
+Prints ONE JSON line (rank 0).  ``--impl reference`` times the CPU oracle on a
+bounded sample of the same workload instead.
+
+Multi-GPU: heads are independent, so each rank runs its own full workload
+(weak scaling, no collective on the data path); the step time is the max over
+ranks and the value the sum of all ranks' FLOPs over that time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "corrected INT2-KV chunk-attention TFLOP/s and % of roofline; quantize GB/s"
+UNIT = "TFLOP/s"
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return p.get("hbm_gbs", 6800.0), p.get("bf16_tflops", 1900.0), \
+            p.get("bf16_tflops_sustained", 1700.0), "measured"
+    return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+def _workload(name):
+    from quantized_kv_cache_quantize_gb300 import synth
+    return synth.WORKLOADS[name]
+
+
+def _config(w, extra=None):
+    cfg = {"workload": f"{w.name}: {w.heads} heads, head_dim {w.head_dim}, chunk {w.chunk_tokens} "
+                       f"tokens (queries = current keys), window {w.n_chunks} chunks = {w.n_s} "
+                       f"tokens INT{w.bits} g{w.group}, batch {w.batch}",
+           "step": "quantize-append 1 chunk + rotate current chunk + corrected attention with "
+                   "P_S/P_R"}
+    if extra:
+        cfg.update(extra)
+    return cfg
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.proc = None
+        self.gpu = gpu_index
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+def _traffic_for_current_kernel():
+    """DRAM bytes per attention launch from the committed ncu summary, or
+    None when the kernel source changed since it was captured."""
+    path = os.path.join(ROOT, "profiles", "attn_traffic.json")
+    src = os.path.join(ROOT, "quantized_kv_cache_quantize_gb300", "csrc", "kvq_attn.cu")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        rec = json.load(f)
+    with open(src, "rb") as f:
+        h = hashlib.sha256(f.read()).hexdigest()[:16]
+    if rec.get("source_sha256_16") != h:
+        return None
+    return rec.get("dram_bytes_per_launch_full")
+
+
+def run_gpu(args):
+    import torch
+    import torch.distributed as dist
+
+    from quantized_kv_cache_quantize_gb300 import kvq, synth
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    w = _workload(args.workload)
+    x = synth.inputs(w, seed=args.seed)
+    signs = synth.hadamard_signs(w.head_dim, seed=args.seed)
+    B, H, d = w.batch, w.heads, w.head_dim
+
+    cache = kvq.KVCache(B, H, d, w.bits, w.group, w.chunk_tokens, w.n_chunks, signs, device=dev)
+    kwin, vwin = x["k_win"].to(dev), x["v_win"].to(dev)
+    for c in range(w.n_chunks):
+        sl = slice(c * w.chunk_tokens, (c + 1) * w.chunk_tokens)
+        kvq.quantize_append(cache, kwin[:, :, sl].contiguous(), vwin[:, :, sl].contiguous())
+    del kwin, vwin
+    q, kc, vc = x["q"].to(dev), x["k_cur"].to(dev), x["v_cur"].to(dev)
+    kn, vn = x["k_new"].to(dev), x["v_new"].to(dev)
+    out = torch.empty_like(q)
+    ps = torch.empty(q.shape[:-1], dtype=torch.float32, device=dev)
+    pr = torch.empty_like(ps)
+    ws = torch.empty(cache.workspace_bytes(w.n_q, w.n_r), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        kvq.quantize_append(cache, kn, vn, stream=stream)
+        kvq.lib().kvq_attention_corrected(
+            kvq.ctypes.byref(cache.struct), kvq._ptr(q), kvq._ptr(kc), kvq._ptr(vc), w.n_q, w.n_r,
+            kvq.ctypes.c_float(w.scale), kvq.CORR_TAYLOR, kvq._ptr(ws), ws.numel(),
+            kvq._ptr(out), kvq._ptr(ps), kvq._ptr(pr), kvq._stream(stream))
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    assert kvq.last_device_status() == 0
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    kvq.profile_begin()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    prof = kvq.profile_end()
+    if world > 1:
+        dist.barrier()
+    clk = clocks.stop()
+    ms_step = e0.elapsed_time(e1) / args.steps
+    status = kvq.last_device_status()
+    if status != 0:
+        raise RuntimeError(f"device status {status} after the timed region")
+
+    t = torch.tensor([ms_step], device=dev)
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    ms_max = float(t.item())
+    flops = w.attention_flops()
+    value = flops * world / (ms_max * 1e-3) / 1e12
+
+    # per-kernel device times inside the timed region (CUDA events on the launch stream)
+    k3_ms = prof["attention"]["ms_total"] / max(1, prof["attention"]["launches"])
+    k1_ms = prof["quantize_append"]["ms_total"] / max(1, prof["quantize_append"]["launches"])
+    k2_ms = prof["rotate"]["ms_total"] / max(1, prof["rotate"]["launches"])
+    hbm, bf16_burst, bf16_sust, peak_kind = _peaks()
+    k3_tflops = flops / (k3_ms * 1e-3) / 1e12
+    # the timed loop runs back to back for ~seconds: the sustained (power-capped) peak applies
+    # when the region is long, the burst peak otherwise
+    region_s = ms_step * args.steps / 1e3
+    peak = bf16_sust if region_s >= 1.0 else bf16_burst
+    q_bytes = w.append_bytes()
+    k1_gbs = q_bytes / (k1_ms * 1e-3) / 1e9
+    rot_bytes = 2.0 * (w.n_q + 2 * w.n_r) * d * B * H * 2
+    launches = sum(v["launches"] for v in prof.values())
+
+    # end to end through the public API with host buffers (pinned), copies inside the timed region
+    host = {k: x[k].pin_memory() for k in ("q", "k_cur", "v_cur", "k_new", "v_new")}
+    dev_in = {k: torch.empty_like(host[k], device=dev) for k in host}
+    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    ps_h = torch.empty(ps.shape, dtype=ps.dtype).pin_memory()
+    pr_h = torch.empty(pr.shape, dtype=pr.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = sum(t.numel() * t.element_size() for t in (out_h, ps_h, pr_h))
+
+    def e2e_step():
+        for k in host:
+            dev_in[k].copy_(host[k], non_blocking=True)
+        kvq.quantize_append(cache, dev_in["k_new"], dev_in["v_new"], stream=stream)
+        kvq.lib().kvq_attention_corrected(
+            kvq.ctypes.byref(cache.struct), kvq._ptr(dev_in["q"]), kvq._ptr(dev_in["k_cur"]),
+            kvq._ptr(dev_in["v_cur"]), w.n_q, w.n_r, kvq.ctypes.c_float(w.scale),
+            kvq.CORR_TAYLOR, kvq._ptr(ws), ws.numel(), kvq._ptr(out), kvq._ptr(ps), kvq._ptr(pr),
+            kvq._stream(stream))
+        out_h.copy_(out, non_blocking=True)
+        ps_h.copy_(ps, non_blocking=True)
+        pr_h.copy_(pr, non_blocking=True)
+
+    e2e_steps = max(3, min(args.steps, 50))
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    t = torch.tensor([e2e_ms], device=dev)
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    e2e_ms = float(t.item())
+
+    result = None
+    if rank == 0:
+        cpu = cpu_baseline(w, args) if (world == 1 and not args.no_cpu_baseline) else None
+        ws_bytes = (w.append_bytes() + 2 * w.n_s * d * w.bits / 8 * B * H
+                    + 3 * w.n_q * d * 2 * B * H)
+        result = {
+            "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_max, 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "fp16 MMA operands / fp32 accumulate over an INT2 cache (BF16 I/O)",
+            "data": "synthetic (seeded; video-shaped token counts; random K/V/Q with outlier "
+                    "channels)",
+            "config": _config(w, {
+                "l2": f"inputs larger than L2: {ws_bytes / 1e6:.0f} MB read per step vs 129 MB L2",
+                "parallelism": f"replicas x{world} (heads independent, no collective)"}),
+            "clocks": clk,
+            "e2e": {"value": round(flops * world / (e2e_ms * 1e-3) / 1e12, 3), "unit": UNIT,
+                    "ms_per_step": round(e2e_ms, 4),
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+            "gpu_launches": launches,
+            "kernels_ms": {"quantize_append": round(k1_ms, 5), "rotate": round(k2_ms, 5),
+                           "attention": round(k3_ms, 5)},
+            "quantize_gbs": round(k1_gbs, 1),
+            "quantize_frac_of_hbm": round(k1_gbs / hbm, 4),
+            "rotate_gbs": round(rot_bytes / (k2_ms * 1e-3) / 1e9, 1),
+            "roofline": {"bound": "tensor", "achieved": round(k3_tflops, 2),
+                         "peak": peak, "unit": "TFLOP/s", "frac": round(k3_tflops / peak, 4),
+                         "peak_source": f"{peak_kind} bf16 "
+                                        f"{'sustained' if peak == bf16_sust else 'burst'} "
+                                        "(FP16 dense rate = BF16 rate)",
+                         "traffic": _traffic_for_current_kernel(),
+                         "kernel": "attention (fused corrected chunk attention)"},
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(result), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return result
+
+
+def _oracle_sample(w, head: int, rows: int, seed: int):
+    """One bounded sample of the step on the CPU oracle: quantize-append of
+    one head's chunk (K and V) and the corrected attention of ``rows`` query
+    rows of that head over its full window and current chunk."""
+    import numpy as np
+
+    from oracle import kvq_oracle as O
+    from quantized_kv_cache_quantize_gb300 import synth
+    x = synth.head_inputs(w, head, seed=seed)
+    s = synth.hadamard_signs(w.head_dim, seed=seed)
+    t0 = time.perf_counter()
+    O.quantize_rows(x["k_new"].float().numpy(), s, w.bits, w.group)
+    O.quantize_rows(x["v_new"].float().numpy(), s, w.bits, w.group)
+    _, kd, kz, _, kc = O.quantize_rows(x["k_win"].float().numpy(), s, w.bits, w.group)
+    _, vd, vz, _, vcod = O.quantize_rows(x["v_win"].float().numpy(), s, w.bits, w.group)
+    O.chunk_attention(x["q"].float().numpy()[:rows], O.dequantize(kc, kd, kz, w.group),
+                      O.dequantize(vcod, vd, vz, w.group), kd, x["k_cur"].float().numpy(),
+                      x["v_cur"].float().numpy(), s, w.scale, w.group, O.CORR_TAYLOR)
+    dt = time.perf_counter() - t0
+    flops = w.attention_flops(n_q=rows, heads=1)
+    return flops, dt
+
+
+def _cores():
+    for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS"):
+        if os.environ.get(var):
+            return int(os.environ[var])
+    return os.cpu_count()
+
+
+def cpu_baseline(w, args):
+    rows = args.cpu_rows
+    flops, dt = _oracle_sample(w, 0, rows, args.seed)
+    return {"value": round(flops / dt / 1e12, 6), "unit": UNIT, "cores": _cores(),
+            "kind": "oracle",
+            "sample": f"head 0 of {w.name}: oracle quantize of its window + new chunk (K,V) and "
+                      f"corrected attention of {rows} query rows over {w.n_s} cached + {w.n_r} "
+                      f"current keys; value = those rows' attention FLOPs / wall time "
+                      f"({dt:.2f} s)"}
+
+
+def run_reference(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return None
+    w = _workload(args.workload)
+    rows = args.ref_rows
+    for _ in range(args.warmup):
+        _oracle_sample(w, 0, rows, args.seed)
+    tot_f, tot_t = 0.0, 0.0
+    for k in range(args.steps):
+        f, dt = _oracle_sample(w, k % w.heads, rows, args.seed)
+        tot_f += f
+        tot_t += dt
+    value = tot_f / tot_t / 1e12
+    sample = (f"per step one head of {w.name}: oracle quantize (window + new chunk, K and V) and "
+              f"corrected attention of {rows} query rows over {w.n_s} cached + {w.n_r} current "
+              f"keys")
+    result = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": UNIT,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(tot_t / args.steps * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64 (fp32 quantizer)",
+        "data": "synthetic (seeded)", "config": _config(w),
+        "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "cores": _cores(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 6), "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(result), flush=True)
+    return result
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="w4_int2")
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--cpu-rows", type=int, default=1024,
+                    help="query rows of the oracle sample behind cpu_baseline")
+    ap.add_argument("--ref-rows", type=int, default=128,
+                    help="query rows per step of the --impl reference sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    args.warmup = max(3, args.warmup)   # at least 3 untimed warm-up steps
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

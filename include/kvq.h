@@ -136,7 +136,9 @@ size_t kvq_workspace_bytes(const kvq_cache *cache, int32_t n_q, int32_t n_r);
  * (NULL to skip) fp32 [batch][heads][n_q] device: the attention masses of the
  * cached block and of the current chunk per query row (Figure 2 caption).
  * workspace: device, >= kvq_workspace_bytes(cache, n_q, n_r) bytes, 16-byte
- * aligned; its contents are scratch.  Requires cache->len + n_r >= 1 when
+ * aligned; its contents are scratch (rotated FP16 copies of q, k_cur, v_cur,
+ * the tensor-core operands).  Values after rotation must stay within the FP16
+ * range (|x| < 65504).  Requires cache->len + n_r >= 1 when
  * n_q > 0.  n_q == 0 is a no-op.
  */
 kvq_status kvq_attention_corrected(const kvq_cache *cache, const uint16_t *q,
@@ -162,12 +164,13 @@ kvq_status kvq_attention_mass(const kvq_cache *cache, const uint16_t *q,
  * The rotation alone (paper section 3 "Hadamard rotation"), for checking:
  * x' = H x per row of x [rows][d] BF16 device, written as fp32 [rows][d]
  * (out_f32) -- exactly the fp32 values kvq_quantize_append quantizes -- or
- * as BF16 round-to-nearest (out_bf16).  Exactly one of out_f32 / out_bf16
- * must be non-NULL.  d in {64, 128}.
+ * rounded to FP16 (out_f16) -- exactly the tensor-core operands the
+ * attention kernels read for q and the current chunk.  Exactly one of
+ * out_f32 / out_f16 must be non-NULL.  d in {64, 128}.
  */
 kvq_status kvq_rotate(const uint16_t *x, int64_t rows, int32_t d,
                       const uint32_t sign_bits[4], float *out_f32,
-                      uint16_t *out_bf16, void *stream);
+                      uint16_t *out_f16, void *stream);
 
 /*
  * Synchronizes `stream`, then returns and clears the device status word
@@ -190,6 +193,18 @@ kvq_status kvq_set_wait_limit_ns(uint64_t limit_ns);
  * error path can be exercised without faulting or hanging a GPU.
  */
 kvq_status kvq_selftest_wait_timeout(uint64_t limit_ns, void *stream);
+
+/*
+ * Instrumentation (no counterpart in the paper).  Between kvq_profile_begin
+ * and kvq_profile_end the library records a pair of CUDA events around each
+ * of its kernel launches, on the stream the kernel is launched on.
+ * kvq_profile_end waits for those events and returns, per kernel kind
+ * (0 quantize-append, 1 rotation, 2 attention), the summed device time in
+ * milliseconds and the number of launches, then stops recording.  At most
+ * 16384 launches per kind are recorded.  Process-global; not thread-safe.
+ */
+kvq_status kvq_profile_begin(void);
+kvq_status kvq_profile_end(double ms_total[3], int32_t launches[3]);
 
 #ifdef __cplusplus
 }

@@ -6,6 +6,7 @@
 #include <atomic>
 #include <cmath>
 #include <cstdint>
+#include <vector>
 
 #include "kvq_internal.h"
 
@@ -16,6 +17,38 @@ std::atomic<unsigned long long> g_wait_limit_ns{2000000000ull};
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// ---- launch timing (kvq_profile_begin / kvq_profile_end) ----
+constexpr int kKinds = 3;
+constexpr int kMaxPairs = 16384;
+struct Profiler {
+  bool on = false;
+  std::vector<cudaEvent_t> pool[kKinds];  // 2 events per launch
+  int used[kKinds] = {0, 0, 0};
+};
+Profiler g_prof;
+
+struct ProfScope {
+  int kind;
+  cudaStream_t s;
+  bool active;
+  ProfScope(int k, cudaStream_t st) : kind(k), s(st), active(false) {
+    if (!g_prof.on || g_prof.used[k] >= kMaxPairs) return;
+    auto& pool = g_prof.pool[k];
+    const size_t need = 2 * (size_t)(g_prof.used[k] + 1);
+    while (pool.size() < need) {
+      cudaEvent_t e;
+      if (cudaEventCreate(&e) != cudaSuccess) return;
+      pool.push_back(e);
+    }
+    if (cudaEventRecord(pool[2 * g_prof.used[k]], s) == cudaSuccess) active = true;
+  }
+  ~ProfScope() {
+    if (!active) return;
+    if (cudaEventRecord(g_prof.pool[kind][2 * g_prof.used[kind] + 1], s) == cudaSuccess)
+      ++g_prof.used[kind];
+  }
+};
 
 kvq_status check_geometry(const kvq_cache* c, kvq::Geometry* g) {
   if (c == nullptr) return KVQ_ERR_INVALID_ARG;
@@ -97,7 +130,7 @@ kvq_status attention_common(const kvq_cache* cache, const uint16_t* q, const uin
   if (workspace_bytes < ws.bytes) return KVQ_ERR_INVALID_ARG;
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  // rotate Q, K_cur, V_cur into the workspace (BF16, rotated basis)
+  // rotate Q, K_cur, V_cur into the workspace (FP16, rotated basis)
   kvq::RotateArgs ra{};
   ra.src[0] = q;
   ra.dst[0] = ws.q;
@@ -111,7 +144,10 @@ kvq_status attention_common(const kvq_cache* cache, const uint16_t* q, const uin
   for (int i = 0; i < 4; ++i) ra.sign_bits[i] = cache->sign_bits[i];
   ra.inv_sqrt_d = (float)(1.0 / std::sqrt((double)g.d));
   ra.out_f32 = 0;
-  if (kvq::launch_rotate(ra, g.d, s) != cudaSuccess) return KVQ_ERR_CUDA;
+  {
+    ProfScope prof(1, s);
+    if (kvq::launch_rotate(ra, g.d, s) != cudaSuccess) return KVQ_ERR_CUDA;
+  }
 
   kvq::AttnLaunch a{};
   a.k_codes = cache->k_codes;
@@ -134,6 +170,7 @@ kvq_status attention_common(const kvq_cache* cache, const uint16_t* q, const uin
   a.p_r = p_r;
   for (int i = 0; i < 4; ++i) a.sign_bits[i] = cache->sign_bits[i];
   a.wait_limit_ns = g_wait_limit_ns.load();
+  ProfScope prof(2, s);
   return kvq::launch_attention(a, g.d, g.bits, g.group, s);
 }
 
@@ -202,6 +239,7 @@ kvq_status kvq_quantize_append(kvq_cache* cache, const uint16_t* k_new, const ui
   for (int i = 0; i < 4; ++i) a.sign_bits[i] = cache->sign_bits[i];
   a.inv_sqrt_d = (float)(1.0 / std::sqrt((double)g.d));
   bool supported = true;
+  ProfScope prof(0, static_cast<cudaStream_t>(stream));
   if (kvq::launch_quantize_append(a, g.d, g.bits, g.group, static_cast<cudaStream_t>(stream),
                                   &supported) != cudaSuccess)
     return KVQ_ERR_CUDA;
@@ -236,17 +274,17 @@ kvq_status kvq_attention_mass(const kvq_cache* cache, const uint16_t* q, const u
 }
 
 kvq_status kvq_rotate(const uint16_t* x, int64_t rows, int32_t d, const uint32_t sign_bits[4],
-                      float* out_f32, uint16_t* out_bf16, void* stream) {
+                      float* out_f32, uint16_t* out_f16, void* stream) {
   if (d != 64 && d != 128) return KVQ_ERR_UNSUPPORTED;
   if (rows < 0 || sign_bits == nullptr) return KVQ_ERR_INVALID_ARG;
-  if ((out_f32 == nullptr) == (out_bf16 == nullptr)) return KVQ_ERR_INVALID_ARG;
+  if ((out_f32 == nullptr) == (out_f16 == nullptr)) return KVQ_ERR_INVALID_ARG;
   if (rows == 0) return KVQ_OK;
   if (x == nullptr) return KVQ_ERR_INVALID_ARG;
-  if (!aligned16(x) || (out_f32 && !aligned16(out_f32)) || (out_bf16 && !aligned16(out_bf16)))
+  if (!aligned16(x) || (out_f32 && !aligned16(out_f32)) || (out_f16 && !aligned16(out_f16)))
     return KVQ_ERR_ALIGNMENT;
   kvq::RotateArgs a{};
   a.src[0] = x;
-  a.dst[0] = out_f32 ? static_cast<void*>(out_f32) : static_cast<void*>(out_bf16);
+  a.dst[0] = out_f32 ? static_cast<void*>(out_f32) : static_cast<void*>(out_f16);
   a.rows[0] = rows;
   for (int i = 0; i < 4; ++i) a.sign_bits[i] = sign_bits[i];
   a.inv_sqrt_d = (float)(1.0 / std::sqrt((double)d));
@@ -273,6 +311,34 @@ kvq_status kvq_selftest_wait_timeout(uint64_t limit_ns, void* stream) {
   return kvq::launch_wait_selftest(limit_ns, static_cast<cudaStream_t>(stream)) == cudaSuccess
              ? KVQ_OK
              : KVQ_ERR_CUDA;
+}
+
+kvq_status kvq_profile_begin(void) {
+  for (int k = 0; k < kKinds; ++k) g_prof.used[k] = 0;
+  g_prof.on = true;
+  return KVQ_OK;
+}
+
+kvq_status kvq_profile_end(double ms_total[3], int32_t launches[3]) {
+  g_prof.on = false;
+  kvq_status st = KVQ_OK;
+  for (int k = 0; k < kKinds; ++k) {
+    double tot = 0.0;
+    for (int i = 0; i < g_prof.used[k]; ++i) {
+      float ms = 0.f;
+      if (cudaEventSynchronize(g_prof.pool[k][2 * i + 1]) != cudaSuccess ||
+          cudaEventElapsedTime(&ms, g_prof.pool[k][2 * i], g_prof.pool[k][2 * i + 1]) !=
+              cudaSuccess) {
+        st = KVQ_ERR_CUDA;
+        continue;
+      }
+      tot += ms;
+    }
+    if (ms_total) ms_total[k] = tot;
+    if (launches) launches[k] = g_prof.used[k];
+    g_prof.used[k] = 0;
+  }
+  return st;
 }
 
 }  // extern "C"

@@ -12,19 +12,26 @@
 // One CTA of 128 threads owns 128 query rows of one (batch, head); thread r
 // owns row r (TMEM lane r).  Per 128-key tile:
 //   cached tile : every thread dequantizes one key's packed K and V row into
-//                 BF16 tiles in shared memory (128-byte swizzle), plus the
+//                 FP16 tiles in shared memory (128-byte swizzle), plus the
 //                 bias columns of that key;
-//   current tile: TMA loads the rotated BF16 K and V tiles;
+//   current tile: TMA loads the rotated FP16 K and V tiles;
 //   S = Q' K^T  : tcgen05 MMAs (M 128, N 128, K 16 steps) into TMEM; on cached
 //                 tiles one more K=16 MMA adds -(scale/24) sum_g n_jg D_ig^2
 //                 through 16 extra columns (bias folded into the contraction);
 //   softmax     : online, one shared running max, two running sums (cached,
-//                 current); P to shared memory as BF16;
+//                 current); P to shared memory as FP16;
 //   O += P V    : tcgen05 MMAs into TMEM (V operand MN-major).
 // Epilogue: O / (l_S + l_R), inverse rotation per row (FWHT in registers),
 // BF16 store; P_S = l_S / (l_S + l_R), P_R = l_R / (l_S + l_R).
+//
+// Operand precision: the tensor-core operands are FP16 (11 significant bits,
+// the same MMA rate as BF16).  INT2 dequantized values (code - z) * D with a
+// BF16 step D need at most 10 significant bits, so the cached K/V tiles are
+// exact; the rotated queries and current-chunk K/V carry one FP16 rounding.
+// Requires |values| < 65504 after rotation (FP16 range).
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
@@ -60,7 +67,7 @@ struct AttnParams {
 constexpr int kThreads = 128;
 constexpr int kBlockM = 128;
 constexpr int kBlockN = 128;
-constexpr int kHalf = 16384;  // one [128 rows][64 bf16] swizzled sub-tile
+constexpr int kHalf = 16384;  // one [128 rows][64 x 16-bit] swizzled sub-tile
 
 template <int D>
 struct Smem {
@@ -68,8 +75,8 @@ struct Smem {
   static constexpr int kQ = 0;
   static constexpr int kK = kQ + kTile;
   static constexpr int kV = kK + kTile;
-  static constexpr int kP = kV + kTile;              // 128 x 128 bf16
-  static constexpr int kQx = kP + 2 * kHalf;         // 128 x 16 bf16, no swizzle
+  static constexpr int kP = kV + kTile;              // 128 x 128 fp16
+  static constexpr int kQx = kP + 2 * kHalf;         // 128 x 16 fp16, no swizzle
   static constexpr int kKx = kQx + 4096;
   static constexpr int kBar = kKx + 4096;
   static constexpr int kBytes = kBar + 64;
@@ -91,10 +98,10 @@ __device__ bool wait_bounded(uint32_t bar, uint32_t parity, unsigned long long l
 }
 
 // byte offset of 16-byte chunk `c` (0..7) of row `r` in a 128-byte-swizzled
-// [rows][64 bf16] sub-tile
+// [rows][64 x 16-bit] sub-tile
 __device__ __forceinline__ int sw128(int r, int c) { return r * 128 + ((c ^ (r & 7)) << 4); }
 
-// byte offset of element (row, k) of a [128][16] bf16 K-major tile without
+// byte offset of element (row, k) of a [128][16] 16-bit K-major tile without
 // swizzle: 8-row x 16-byte core matrices, K chunks 128 B apart, row groups 256 B
 __device__ __forceinline__ int noswz16(int r, int kchunk) {
   return (r >> 3) * 256 + kchunk * 128 + (r & 7) * 16;
@@ -105,11 +112,19 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
+__device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
+  __half2 v = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+__device__ __forceinline__ float h_lo(uint32_t w) { return __half2float(__ushort_as_half((unsigned short)(w & 0xFFFFu))); }
+__device__ __forceinline__ float h_hi(uint32_t w) { return __half2float(__ushort_as_half((unsigned short)(w >> 16))); }
+
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
 // Dequantize one packed row (codes + per-group (step, zero) words) into a
-// BF16 row of the swizzled tile at `tile` (row r): x_hat = (code - z) * D,
+// FP16 row of the swizzled tile at `tile` (row r): x_hat = (code - z) * D,
 // Eq. (1).  Returns nothing; writes D/8 16-byte chunks.
 template <int D, int BITS, int GROUP>
 __device__ __forceinline__ void dequant_row(const uint32_t* words, const uint32_t* sz,
@@ -135,7 +150,7 @@ __device__ __forceinline__ void dequant_row(const uint32_t* words, const uint32_
       }
       const float v0 = __fmul_rn(__fsub_rn((float)c0, zero), delta);
       const float v1 = __fmul_rn(__fsub_rn((float)c1, zero), delta);
-      out[i] = pack_bf16x2(v0, v1);
+      out[i] = pack_h2(v0, v1);
     }
     const int half = c >> 3;
     *reinterpret_cast<uint4*>(tile + half * kHalf + sw128(r, c & 7)) =
@@ -153,18 +168,18 @@ __device__ __forceinline__ void zero_row(uint8_t* tile, int r) {
 
 // 16 bias columns of one row: per group g, three columns (hi, hi, lo) on the
 // query side against (hi, lo, hi) on the key side, so that their product sum
-// is a_g * b_g to ~2^-16 relative with BF16 operands.
+// is a_g * b_g to ~2^-21 relative with FP16 operands.
 __device__ __forceinline__ void write_ext_row(uint8_t* tile, int r, const float* cols16) {
   uint32_t w[8];
 #pragma unroll
-  for (int i = 0; i < 8; ++i) w[i] = pack_bf16x2(cols16[2 * i], cols16[2 * i + 1]);
+  for (int i = 0; i < 8; ++i) w[i] = pack_h2(cols16[2 * i], cols16[2 * i + 1]);
   *reinterpret_cast<uint4*>(tile + noswz16(r, 0)) = make_uint4(w[0], w[1], w[2], w[3]);
   *reinterpret_cast<uint4*>(tile + noswz16(r, 1)) = make_uint4(w[4], w[5], w[6], w[7]);
 }
 
-__device__ __forceinline__ void split_bf16(float v, float& hi, float& lo) {
-  hi = __bfloat162float(__float2bfloat16_rn(v));
-  lo = __bfloat162float(__float2bfloat16_rn(v - hi));
+__device__ __forceinline__ void split_h(float v, float& hi, float& lo) {
+  hi = __half2float(__float2half_rn(v));
+  lo = __half2float(__float2half_rn(v - hi));
 }
 
 template <int D, int BITS, int GROUP>
@@ -218,7 +233,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t ph_load = 0, ph_mma = 0;
   const unsigned long long lim = p.wait_limit_ns;
 
-  // ---- Q tile (rotated BF16) by TMA ----
+  // ---- Q tile (rotated FP16) by TMA ----
   if (tid == 0) {
     ptx::mbar_expect_tx(bar_load, NKH * kHalf);
 #pragma unroll
@@ -239,7 +254,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       float acc = 0.f;
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
-        const float a = bf16_lo(w[i]), b = bf16_hi(w[i]);
+        const float a = h_lo(w[i]), b = h_hi(w[i]);
         acc = fmaf(a, a, acc);
         acc = fmaf(b, b, acc);
       }
@@ -251,7 +266,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
     for (int g = 0; g < G; ++g) {
       float hi, lo;
-      split_bf16(p.alpha_coef * nrm[g], hi, lo);
+      split_h(p.alpha_coef * nrm[g], hi, lo);
       cols[3 * g] = hi;
       cols[3 * g + 1] = hi;
       cols[3 * g + 2] = lo;
@@ -264,8 +279,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int n_rt = (p.n_r + kBlockN - 1) / kBlockN;
   const bool use_bias = p.corr != 0;
   const bool do_pv = !p.mass_only;
-  constexpr uint32_t kIdescS = ptx::idesc_bf16(kBlockM, kBlockN, false);
-  constexpr uint32_t kIdescO = ptx::idesc_bf16(kBlockM, D, true);
+  constexpr uint32_t kIdescS = ptx::idesc_f16kind(kBlockM, kBlockN, false, false);
+  constexpr uint32_t kIdescO = ptx::idesc_f16kind(kBlockM, D, true, false);
 
   float m_run = -INFINITY, l_s = 0.f, l_r = 0.f;
   const size_t head_tok = static_cast<size_t>(bh) * p.cap;
@@ -301,7 +316,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int g = 0; g < G; ++g) {
           const float dl = bf16_lo(ksz[g]);
           float hi, lo;
-          split_bf16(dl * dl, hi, lo);
+          split_h(dl * dl, hi, lo);
           cols[3 * g] = hi;
           cols[3 * g + 1] = lo;
           cols[3 * g + 2] = hi;
@@ -350,11 +365,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int s = 0; s < D / 16; ++s) {
         const uint32_t off = (s >> 2) * kHalf + (s & 3) * 32;
-        ptx::mma_bf16(t_s, ptx::smem_desc(s_q + off, 16, 1024, ptx::kLayoutSw128),
+        ptx::mma_f16(t_s, ptx::smem_desc(s_q + off, 16, 1024, ptx::kLayoutSw128),
                       ptx::smem_desc(s_k + off, 16, 1024, ptx::kLayoutSw128), kIdescS, s > 0);
       }
       if (cached && use_bias) {
-        ptx::mma_bf16(t_s, ptx::smem_desc(s_qx, 128, 256, ptx::kLayoutNone),
+        ptx::mma_f16(t_s, ptx::smem_desc(s_qx, 128, 256, ptx::kLayoutNone),
                       ptx::smem_desc(s_kx, 128, 256, ptx::kLayoutNone), kIdescS, 1);
       }
       ptx::mma_commit(bar_mma);
@@ -390,13 +405,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     m_run = m_new;
 
     if (do_pv) {
-      // P (BF16) into the swizzled A tile, row tid
+      // P (FP16) into the swizzled A tile, row tid
 #pragma unroll
       for (int c = 0; c < kBlockN / 8; ++c) {
-        const uint4 v = make_uint4(pack_bf16x2(sc[8 * c], sc[8 * c + 1]),
-                                   pack_bf16x2(sc[8 * c + 2], sc[8 * c + 3]),
-                                   pack_bf16x2(sc[8 * c + 4], sc[8 * c + 5]),
-                                   pack_bf16x2(sc[8 * c + 6], sc[8 * c + 7]));
+        const uint4 v = make_uint4(pack_h2(sc[8 * c], sc[8 * c + 1]),
+                                   pack_h2(sc[8 * c + 2], sc[8 * c + 3]),
+                                   pack_h2(sc[8 * c + 4], sc[8 * c + 5]),
+                                   pack_h2(sc[8 * c + 6], sc[8 * c + 7]));
         *reinterpret_cast<uint4*>(smem + L::kP + (c >> 3) * kHalf + sw128(tid, c & 7)) = v;
       }
       // rescale the running output when the max moved (warp-uniform decision)
@@ -424,7 +439,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int s = 0; s < kBlockN / 16; ++s) {
           const uint32_t a_off = (s >> 2) * kHalf + (s & 3) * 32;
           const uint32_t b_off = s * 16 * 128;
-          ptx::mma_bf16(t_o, ptx::smem_desc(s_p + a_off, 16, 1024, ptx::kLayoutSw128),
+          ptx::mma_f16(t_o, ptx::smem_desc(s_p + a_off, 16, 1024, ptx::kLayoutSw128),
                         ptx::smem_desc(s_v + b_off, kHalf, 1024, ptx::kLayoutSw128), kIdescO,
                         (it > 0 || s > 0) ? 1u : 0u);
         }
@@ -523,7 +538,7 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// 3-D map over a [bh][n][d] BF16 tensor, box [1][128][64], 128-byte swizzle,
+// 3-D map over a [bh][n][d] FP16 tensor, box [1][128][64], 128-byte swizzle,
 // zero fill outside the tensor.
 bool make_map(CUtensorMap* m, const void* base, int d, int n, int bh) {
   auto fn = encode_fn();
@@ -532,7 +547,7 @@ bool make_map(CUtensorMap* m, const void* base, int d, int n, int bh) {
   cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)n * d * 2};
   cuuint32_t box[3] = {64, 128, 1};
   cuuint32_t estr[3] = {1, 1, 1};
-  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void*>(base), dims, strides,
                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;

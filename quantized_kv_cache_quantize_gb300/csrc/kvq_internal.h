@@ -42,7 +42,7 @@ struct RotateArgs {
   long long rows[3];
   uint32_t sign_bits[4];
   float inv_sqrt_d;
-  int out_f32;  // 1: fp32 output, 0: bf16
+  int out_f32;  // 1: fp32 output, 0: fp16 (the attention kernel's operand format)
 };
 
 cudaError_t launch_quantize_append(const QuantArgs& a, int d, int bits, int group,

@@ -12,6 +12,7 @@
 // The kernel is bound by HBM bandwidth: per row it reads 2d bytes and writes
 // d*bits/8 + 4*(d/group) bytes.
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 #include "kvq_fwht.cuh"
@@ -25,6 +26,10 @@ constexpr int kThreads = 256;
 
 __device__ __forceinline__ uint32_t shfl_idx(uint32_t v, int src) {
   return __shfl_sync(0xffffffffu, v, src);
+}
+
+__device__ __forceinline__ uint32_t h_bits_rn(float v) {
+  return (uint32_t)__half_as_ushort(__float2half_rn(v));
 }
 
 // sign word of lane t's channels without indexing a kernel-parameter array at
@@ -182,10 +187,10 @@ __global__ void __launch_bounds__(kThreads) rotate_kernel(const RotateArgs a) {
       dst[1] = make_float4(x[4], x[5], x[6], x[7]);
     } else {
       uint4 o;
-      o.x = bf16_bits_rn(x[0]) | (bf16_bits_rn(x[1]) << 16);
-      o.y = bf16_bits_rn(x[2]) | (bf16_bits_rn(x[3]) << 16);
-      o.z = bf16_bits_rn(x[4]) | (bf16_bits_rn(x[5]) << 16);
-      o.w = bf16_bits_rn(x[6]) | (bf16_bits_rn(x[7]) << 16);
+      o.x = h_bits_rn(x[0]) | (h_bits_rn(x[1]) << 16);
+      o.y = h_bits_rn(x[2]) | (h_bits_rn(x[3]) << 16);
+      o.z = h_bits_rn(x[4]) | (h_bits_rn(x[5]) << 16);
+      o.w = h_bits_rn(x[6]) | (h_bits_rn(x[7]) << 16);
       *reinterpret_cast<uint4*>(static_cast<uint16_t*>(dstp) + rr * D + 8 * t) = o;
     }
   }

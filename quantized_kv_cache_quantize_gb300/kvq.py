@@ -63,6 +63,8 @@ _SIGNATURES = {
     "kvq_last_device_status": (ctypes.c_int, [_P]),
     "kvq_set_wait_limit_ns": (ctypes.c_int, [ctypes.c_uint64]),
     "kvq_selftest_wait_timeout": (ctypes.c_int, [ctypes.c_uint64, _P]),
+    "kvq_profile_begin": (ctypes.c_int, []),
+    "kvq_profile_end": (ctypes.c_int, [_P, _P]),
 }
 
 _lib = None
@@ -226,15 +228,17 @@ def attention_mass(cache: KVCache, q, k_cur, scale: float | None = None,
 
 def rotate(x: torch.Tensor, signs, out_dtype=torch.float32, stream=None) -> torch.Tensor:
     """kvq_rotate: x [..., d] bf16 -> H x in fp32 (the values the quantizer
-    sees) or bf16."""
+    sees) or fp16 (the attention kernel's tensor-core operands)."""
     _bf16_dev(x, "x")
     d = x.shape[-1]
     rows = x.numel() // d if d else 0
     out = torch.empty(x.shape, dtype=out_dtype, device=x.device)
     sb = (ctypes.c_uint32 * 4)(*sign_bits(signs))
+    if out_dtype not in (torch.float32, torch.float16):
+        raise ValueError("out_dtype must be float32 or float16")
     f32 = out if out_dtype == torch.float32 else None
-    b16 = out if out_dtype == torch.bfloat16 else None
-    _check(lib().kvq_rotate(_ptr(x), rows, d, sb, _ptr(f32), _ptr(b16), _stream(stream)),
+    f16 = out if out_dtype == torch.float16 else None
+    _check(lib().kvq_rotate(_ptr(x), rows, d, sb, _ptr(f32), _ptr(f16), _stream(stream)),
            "kvq_rotate")
     return out
 
@@ -250,3 +254,17 @@ def set_wait_limit_ns(limit_ns: int):
 def selftest_wait_timeout(limit_ns: int, stream=None):
     _check(lib().kvq_selftest_wait_timeout(int(limit_ns), _stream(stream)),
            "kvq_selftest_wait_timeout")
+
+
+def profile_begin():
+    """Start recording CUDA events around every libkvq kernel launch."""
+    _check(lib().kvq_profile_begin(), "kvq_profile_begin")
+
+
+def profile_end() -> dict:
+    """Stop recording; per kernel kind, summed device ms and launch count."""
+    ms = (ctypes.c_double * 3)()
+    n = (ctypes.c_int32 * 3)()
+    _check(lib().kvq_profile_end(ms, n), "kvq_profile_end")
+    kinds = ("quantize_append", "rotate", "attention")
+    return {k: {"ms_total": float(ms[i]), "launches": int(n[i])} for i, k in enumerate(kinds)}
