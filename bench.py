@@ -159,7 +159,7 @@ def run_gpu(args):
         kvq.quantize_append(cache, kn, vn, stream=stream)
         kvq.lib().kvq_attention_corrected(
             kvq.ctypes.byref(cache.struct), kvq._ptr(q), kvq._ptr(kc), kvq._ptr(vc), w.n_q, w.n_r,
-            kvq.ctypes.c_float(w.scale), kvq.CORR_TAYLOR, kvq._ptr(ws), ws.numel(),
+            kvq.ctypes.c_float(w.scale), kvq.CORR_TAYLOR, args.flags, kvq._ptr(ws), ws.numel(),
             kvq._ptr(out), kvq._ptr(ps), kvq._ptr(pr), kvq._stream(stream))
 
     for _ in range(args.warmup):
@@ -228,8 +228,8 @@ def run_gpu(args):
         kvq.lib().kvq_attention_corrected(
             kvq.ctypes.byref(cache.struct), kvq._ptr(dev_in["q"]), kvq._ptr(dev_in["k_cur"]),
             kvq._ptr(dev_in["v_cur"]), w.n_q, w.n_r, kvq.ctypes.c_float(w.scale),
-            kvq.CORR_TAYLOR, kvq._ptr(ws), ws.numel(), kvq._ptr(out), kvq._ptr(ps), kvq._ptr(pr),
-            kvq._stream(stream))
+            kvq.CORR_TAYLOR, args.flags, kvq._ptr(ws), ws.numel(), kvq._ptr(out), kvq._ptr(ps),
+            kvq._ptr(pr), kvq._stream(stream))
         out_h.copy_(out, non_blocking=True)
         ps_h.copy_(ps, non_blocking=True)
         pr_h.copy_(pr, non_blocking=True)
@@ -376,6 +376,8 @@ def main(argv=None):
     ap.add_argument("--ref-rows", type=int, default=128,
                     help="query rows per step of the --impl reference sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--precise-query", dest="flags", action="store_const", const=1, default=0,
+                    help="split the rotated query into FP16 high + low parts")
     args = ap.parse_args(argv)
     args.warmup = max(3, args.warmup)   # at least 3 untimed warm-up steps
     if args.impl == "reference":

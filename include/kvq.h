@@ -48,6 +48,18 @@ typedef enum {
 } kvq_corr;
 
 /*
+ * Attention flags.
+ * KVQ_FLAG_PRECISE_QUERY: the rotated query, a tensor-core operand of the
+ *   cached-segment scores, is split into FP16 high and low parts and both are
+ *   contracted with the cached keys (one extra QK^T pass on cached tiles,
+ *   ~+40 % time).  Without it the rotated query carries one FP16 rounding
+ *   (2^-11 relative), which moves a score by ~2^-12 of its magnitude: below
+ *   1e-3 on the attention masses for moderate scores, but not for keys with
+ *   extreme outliers (scores of order 100).  No counterpart in the paper.
+ */
+#define KVQ_FLAG_PRECISE_QUERY 1
+
+/*
  * Quantized sliding-window KV cache (paper section 1: the current chunk
  * attends to the last n cached chunks; section 3 "Integer quantization",
  * Eq. (1), and "Quantization granularity": per-token groups of `group`
@@ -129,22 +141,24 @@ size_t kvq_workspace_bytes(const kvq_cache *cache, int32_t n_q, int32_t n_r);
  *   cached score  s_ij = scale * q'_j . k_hat'_i - b_ij,
  *   b_ij = scale^2 / 24 * sum_g ||q'_{j,g}||^2 * D_{i,g}^2   (corr = TAYLOR;
  *          0 for corr = NONE) -- the second-order Jensen-bias correction;
- *   current score s_ij = scale * q_j . k_i;
+ *   current score s_ij = scale * q_j . k_i on the unrotated BF16 inputs
+ *          (exact products, fp32 accumulation);
  *   one softmax over both segments; out = sum_i p_ij v_i in the ORIGINAL
  *   basis (cached values un-rotated).
+ * flags: 0 or KVQ_FLAG_PRECISE_QUERY.
  * out: BF16 [batch][heads][n_q][d] device (required).  p_s, p_r: optional
  * (NULL to skip) fp32 [batch][heads][n_q] device: the attention masses of the
  * cached block and of the current chunk per query row (Figure 2 caption).
  * workspace: device, >= kvq_workspace_bytes(cache, n_q, n_r) bytes, 16-byte
- * aligned; its contents are scratch (rotated FP16 copies of q, k_cur, v_cur,
- * the tensor-core operands).  Values after rotation must stay within the FP16
- * range (|x| < 65504).  Requires cache->len + n_r >= 1 when
+ * aligned; its contents are scratch (the rotated query as FP16 high and low
+ * parts and the rotated current values in FP16: tensor-core operands).
+ * Values after rotation must stay within the FP16 range (|x| < 65504).  Requires cache->len + n_r >= 1 when
  * n_q > 0.  n_q == 0 is a no-op.
  */
 kvq_status kvq_attention_corrected(const kvq_cache *cache, const uint16_t *q,
                                    const uint16_t *k_cur, const uint16_t *v_cur,
                                    int32_t n_q, int32_t n_r, float scale,
-                                   int32_t corr, void *workspace,
+                                   int32_t corr, int32_t flags, void *workspace,
                                    size_t workspace_bytes, uint16_t *out,
                                    float *p_s, float *p_r, void *stream);
 
@@ -156,7 +170,8 @@ kvq_status kvq_attention_corrected(const kvq_cache *cache, const uint16_t *q,
  */
 kvq_status kvq_attention_mass(const kvq_cache *cache, const uint16_t *q,
                               const uint16_t *k_cur, int32_t n_q, int32_t n_r,
-                              float scale, int32_t corr, void *workspace,
+                              float scale, int32_t corr, int32_t flags,
+                              void *workspace,
                               size_t workspace_bytes, float *p_s, float *p_r,
                               void *stream);
 

@@ -82,9 +82,9 @@ kvq_status check_cache_buffers(const kvq_cache* c) {
 }
 
 struct Workspace {
-  uint16_t* q;
-  uint16_t* k;
-  uint16_t* v;
+  uint16_t* q_hi;  // rotated queries, FP16
+  uint16_t* q_lo;  // FP16 remainder of the rotated queries
+  uint16_t* v;     // rotated current-chunk values, FP16
   size_t bytes;
 };
 
@@ -93,16 +93,16 @@ Workspace carve(void* base, const kvq::Geometry& g, int n_q, int n_r) {
   const size_t qb = round_up((size_t)g.bh * n_q * g.d * 2, 256);
   const size_t rb = round_up((size_t)g.bh * n_r * g.d * 2, 256);
   uint8_t* p = static_cast<uint8_t*>(base);
-  w.q = reinterpret_cast<uint16_t*>(p);
-  w.k = reinterpret_cast<uint16_t*>(p + qb);
-  w.v = reinterpret_cast<uint16_t*>(p + qb + rb);
-  w.bytes = qb + 2 * rb;
+  w.q_hi = reinterpret_cast<uint16_t*>(p);
+  w.q_lo = reinterpret_cast<uint16_t*>(p + qb);
+  w.v = reinterpret_cast<uint16_t*>(p + 2 * qb);
+  w.bytes = 2 * qb + rb;
   return w;
 }
 
 kvq_status attention_common(const kvq_cache* cache, const uint16_t* q, const uint16_t* k_cur,
                             const uint16_t* v_cur, int32_t n_q, int32_t n_r, float scale,
-                            int32_t corr, void* workspace, size_t workspace_bytes,
+                            int32_t corr, int32_t flags, void* workspace, size_t workspace_bytes,
                             uint16_t* out, float* p_s, float* p_r, bool mass_only,
                             void* stream) {
   kvq::Geometry g;
@@ -110,6 +110,8 @@ kvq_status attention_common(const kvq_cache* cache, const uint16_t* q, const uin
   if (st != KVQ_OK) return st;
   if (n_q < 0 || n_r < 0 || n_q > (1 << 30) || n_r > (1 << 30)) return KVQ_ERR_INVALID_ARG;
   if (corr != KVQ_CORR_NONE && corr != KVQ_CORR_TAYLOR) return KVQ_ERR_INVALID_ARG;
+  if ((flags & ~KVQ_FLAG_PRECISE_QUERY) != 0) return KVQ_ERR_INVALID_ARG;
+  const bool precise = (flags & KVQ_FLAG_PRECISE_QUERY) != 0;
   if (!std::isfinite(scale) || scale <= 0.f) return KVQ_ERR_INVALID_ARG;
   if ((p_s == nullptr) != (p_r == nullptr)) return KVQ_ERR_INVALID_ARG;
   if (mass_only && p_s == nullptr) return KVQ_ERR_INVALID_ARG;
@@ -130,17 +132,16 @@ kvq_status attention_common(const kvq_cache* cache, const uint16_t* q, const uin
   if (workspace_bytes < ws.bytes) return KVQ_ERR_INVALID_ARG;
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  // rotate Q, K_cur, V_cur into the workspace (FP16, rotated basis)
+  // rotate Q (FP16 hi, and lo when precise) and V_cur (FP16) into the workspace
   kvq::RotateArgs ra{};
   ra.src[0] = q;
-  ra.dst[0] = ws.q;
+  ra.dst[0] = ws.q_hi;
+  ra.dst_lo[0] = precise ? ws.q_lo : nullptr;
   ra.rows[0] = (long long)g.bh * n_q;
-  ra.src[1] = k_cur;
-  ra.dst[1] = ws.k;
-  ra.rows[1] = (long long)g.bh * n_r;
-  ra.src[2] = v_cur;
-  ra.dst[2] = ws.v;
-  ra.rows[2] = mass_only ? 0 : (long long)g.bh * n_r;
+  ra.src[1] = v_cur;
+  ra.dst[1] = ws.v;
+  ra.dst_lo[1] = nullptr;
+  ra.rows[1] = mass_only ? 0 : (long long)g.bh * n_r;
   for (int i = 0; i < 4; ++i) ra.sign_bits[i] = cache->sign_bits[i];
   ra.inv_sqrt_d = (float)(1.0 / std::sqrt((double)g.d));
   ra.out_f32 = 0;
@@ -156,14 +157,17 @@ kvq_status attention_common(const kvq_cache* cache, const uint16_t* q, const uin
   a.v_sz = reinterpret_cast<const uint32_t*>(cache->v_sz);
   a.n_s = cache->len;
   a.cap = g.cap;
-  a.q_rot = ws.q;
-  a.k_rot = ws.k;
+  a.q_rot = ws.q_hi;
+  a.q_rot_lo = ws.q_lo;
+  a.q_orig = q;
+  a.k_cur = k_cur;
   a.v_rot = ws.v;
   a.n_q = n_q;
   a.n_r = n_r;
   a.bh = g.bh;
   a.scale = scale;
   a.corr = corr;
+  a.precise_query = precise ? 1 : 0;
   a.mass_only = mass_only ? 1 : 0;
   a.out = out;
   a.p_s = p_s;
@@ -257,19 +261,19 @@ size_t kvq_workspace_bytes(const kvq_cache* cache, int32_t n_q, int32_t n_r) {
 
 kvq_status kvq_attention_corrected(const kvq_cache* cache, const uint16_t* q,
                                    const uint16_t* k_cur, const uint16_t* v_cur, int32_t n_q,
-                                   int32_t n_r, float scale, int32_t corr, void* workspace,
-                                   size_t workspace_bytes, uint16_t* out, float* p_s, float* p_r,
-                                   void* stream) {
-  return attention_common(cache, q, k_cur, v_cur, n_q, n_r, scale, corr, workspace,
+                                   int32_t n_r, float scale, int32_t corr, int32_t flags,
+                                   void* workspace, size_t workspace_bytes, uint16_t* out,
+                                   float* p_s, float* p_r, void* stream) {
+  return attention_common(cache, q, k_cur, v_cur, n_q, n_r, scale, corr, flags, workspace,
                           workspace_bytes, out, p_s, p_r, false, stream);
 }
 
 kvq_status kvq_attention_mass(const kvq_cache* cache, const uint16_t* q, const uint16_t* k_cur,
-                              int32_t n_q, int32_t n_r, float scale, int32_t corr,
+                              int32_t n_q, int32_t n_r, float scale, int32_t corr, int32_t flags,
                               void* workspace, size_t workspace_bytes, float* p_s, float* p_r,
                               void* stream) {
   if (p_s == nullptr || p_r == nullptr) return KVQ_ERR_INVALID_ARG;
-  return attention_common(cache, q, k_cur, nullptr, n_q, n_r, scale, corr, workspace,
+  return attention_common(cache, q, k_cur, nullptr, n_q, n_r, scale, corr, flags, workspace,
                           workspace_bytes, nullptr, p_s, p_r, true, stream);
 }
 
@@ -285,7 +289,9 @@ kvq_status kvq_rotate(const uint16_t* x, int64_t rows, int32_t d, const uint32_t
   kvq::RotateArgs a{};
   a.src[0] = x;
   a.dst[0] = out_f32 ? static_cast<void*>(out_f32) : static_cast<void*>(out_f16);
+  a.dst_lo[0] = nullptr;
   a.rows[0] = rows;
+  a.rows[1] = 0;
   for (int i = 0; i < 4; ++i) a.sign_bits[i] = sign_bits[i];
   a.inv_sqrt_d = (float)(1.0 / std::sqrt((double)d));
   a.out_f32 = out_f32 ? 1 : 0;

@@ -14,21 +14,26 @@
 //   cached tile : every thread dequantizes one key's packed K and V row into
 //                 FP16 tiles in shared memory (128-byte swizzle), plus the
 //                 bias columns of that key;
-//   current tile: TMA loads the rotated FP16 K and V tiles;
-//   S = Q' K^T  : tcgen05 MMAs (M 128, N 128, K 16 steps) into TMEM; on cached
-//                 tiles one more K=16 MMA adds -(scale/24) sum_g n_jg D_ig^2
-//                 through 16 extra columns (bias folded into the contraction);
+//   current tile: TMA loads the ORIGINAL BF16 keys and the rotated FP16
+//                 values;
+//   S           : tcgen05 MMAs (M 128, N 128, K 16 steps) into TMEM.  Cached
+//                 tiles: Q' K_hat'^T in FP16 (plus Q'_lo K_hat'^T with the
+//                 precise-query flag), then one K=16 MMA adds
+//                 -(scale/24) sum_g n_jg D_ig^2 through 16 extra columns (bias
+//                 folded into the contraction).  Current tiles: Q K^T on the
+//                 unrotated BF16 inputs (exact products);
 //   softmax     : online, one shared running max, two running sums (cached,
 //                 current); P to shared memory as FP16;
 //   O += P V    : tcgen05 MMAs into TMEM (V operand MN-major).
 // Epilogue: O / (l_S + l_R), inverse rotation per row (FWHT in registers),
 // BF16 store; P_S = l_S / (l_S + l_R), P_R = l_R / (l_S + l_R).
 //
-// Operand precision: the tensor-core operands are FP16 (11 significant bits,
+// Operand precision: cached-segment operands are FP16 (11 significant bits,
 // the same MMA rate as BF16).  INT2 dequantized values (code - z) * D with a
 // BF16 step D need at most 10 significant bits, so the cached K/V tiles are
-// exact; the rotated queries and current-chunk K/V carry one FP16 rounding.
-// Requires |values| < 65504 after rotation (FP16 range).
+// exact; the rotated query carries one FP16 rounding unless it is split into
+// high and low parts.  Current-segment scores use the BF16 inputs as they
+// are.  Requires |values| < 65504 after rotation (FP16 range).
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -55,6 +60,7 @@ struct AttnParams {
   float scale_log2;   // scale * log2(e)
   float alpha_coef;   // -(scale / 24) with the correction, 0 without
   int corr;
+  int precise_query;
   int mass_only;
   uint16_t* out;
   float* p_s;
@@ -72,8 +78,10 @@ constexpr int kHalf = 16384;  // one [128 rows][64 x 16-bit] swizzled sub-tile
 template <int D>
 struct Smem {
   static constexpr int kTile = kBlockM * D * 2;
-  static constexpr int kQ = 0;
-  static constexpr int kK = kQ + kTile;
+  static constexpr int kQ = 0;                       // rotated queries, FP16 (high part)
+  static constexpr int kQlo = kQ + kTile;            // FP16 low part
+  static constexpr int kQo = kQlo + kTile;           // original queries, BF16
+  static constexpr int kK = kQo + kTile;
   static constexpr int kV = kK + kTile;
   static constexpr int kP = kV + kTile;              // 128 x 128 fp16
   static constexpr int kQx = kP + 2 * kHalf;         // 128 x 16 fp16, no swizzle
@@ -184,7 +192,8 @@ __device__ __forceinline__ void split_h(float v, float& hi, float& lo) {
 
 template <int D, int BITS, int GROUP>
 __global__ void __launch_bounds__(kThreads, 1)
-    attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+    attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_qlo,
+                const __grid_constant__ CUtensorMap tm_qo, const __grid_constant__ CUtensorMap tm_k,
                 const __grid_constant__ CUtensorMap tm_v, const AttnParams p) {
   using L = Smem<D>;
   constexpr int G = D / GROUP;
@@ -207,6 +216,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kBar + 16);
 
   const uint32_t s_q = ptx::smem_u32(smem + L::kQ);
+  const uint32_t s_qlo = ptx::smem_u32(smem + L::kQlo);
+  const uint32_t s_qo = ptx::smem_u32(smem + L::kQo);
+  const bool precise = p.precise_query != 0;
   const uint32_t s_k = ptx::smem_u32(smem + L::kK);
   const uint32_t s_v = ptx::smem_u32(smem + L::kV);
   const uint32_t s_p = ptx::smem_u32(smem + L::kP);
@@ -233,11 +245,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t ph_load = 0, ph_mma = 0;
   const unsigned long long lim = p.wait_limit_ns;
 
-  // ---- Q tile (rotated FP16) by TMA ----
+  // ---- query tiles by TMA: rotated FP16 (+ low part), original BF16 ----
   if (tid == 0) {
-    ptx::mbar_expect_tx(bar_load, NKH * kHalf);
+    const int n_tiles = 1 + (precise ? 1 : 0) + (p.n_r > 0 ? 1 : 0);
+    ptx::mbar_expect_tx(bar_load, n_tiles * NKH * kHalf);
 #pragma unroll
-    for (int h = 0; h < NKH; ++h) ptx::tma_load_3d(s_q + h * kHalf, &tm_q, 64 * h, q0, bh, bar_load);
+    for (int h = 0; h < NKH; ++h) {
+      ptx::tma_load_3d(s_q + h * kHalf, &tm_q, 64 * h, q0, bh, bar_load);
+      if (precise) ptx::tma_load_3d(s_qlo + h * kHalf, &tm_qlo, 64 * h, q0, bh, bar_load);
+      if (p.n_r > 0) ptx::tma_load_3d(s_qo + h * kHalf, &tm_qo, 64 * h, q0, bh, bar_load);
+    }
   }
   bool ok = wait_bounded(bar_load, ph_load, lim);
   ph_load ^= 1;
@@ -249,12 +266,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int g = 0; g < G; ++g) nrm[g] = 0.f;
 #pragma unroll
     for (int c = 0; c < D / 8; ++c) {
-      const uint4 v = *reinterpret_cast<const uint4*>(smem + L::kQ + (c >> 3) * kHalf + sw128(tid, c & 7));
+      const int off = (c >> 3) * kHalf + sw128(tid, c & 7);
+      const uint4 v = *reinterpret_cast<const uint4*>(smem + L::kQ + off);
+      uint4 vl = make_uint4(0u, 0u, 0u, 0u);
+      if (precise) vl = *reinterpret_cast<const uint4*>(smem + L::kQlo + off);
       const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+      const uint32_t wl[4] = {vl.x, vl.y, vl.z, vl.w};
       float acc = 0.f;
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
-        const float a = h_lo(w[i]), b = h_hi(w[i]);
+        const float a = h_lo(w[i]) + h_lo(wl[i]), b = h_hi(w[i]) + h_hi(wl[i]);
         acc = fmaf(a, a, acc);
         acc = fmaf(b, b, acc);
       }
@@ -280,6 +301,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const bool use_bias = p.corr != 0;
   const bool do_pv = !p.mass_only;
   constexpr uint32_t kIdescS = ptx::idesc_f16kind(kBlockM, kBlockN, false, false);
+  constexpr uint32_t kIdescSbf = ptx::idesc_f16kind(kBlockM, kBlockN, false, true);
   constexpr uint32_t kIdescO = ptx::idesc_f16kind(kBlockM, D, true, false);
 
   float m_run = -INFINITY, l_s = 0.f, l_r = 0.f;
@@ -359,14 +381,24 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
 
-    // ---- S = Q' K^T (+ bias columns) ----
+    // ---- S = Q' K_hat'^T (+ low part, + bias columns) or Q K^T ----
     if (tid == 0) {
       ptx::tc_fence_after();
+      const uint32_t a_base = cached ? s_q : s_qo;
+      const uint32_t idesc = cached ? kIdescS : kIdescSbf;
 #pragma unroll
       for (int s = 0; s < D / 16; ++s) {
         const uint32_t off = (s >> 2) * kHalf + (s & 3) * 32;
-        ptx::mma_f16(t_s, ptx::smem_desc(s_q + off, 16, 1024, ptx::kLayoutSw128),
-                      ptx::smem_desc(s_k + off, 16, 1024, ptx::kLayoutSw128), kIdescS, s > 0);
+        ptx::mma_f16(t_s, ptx::smem_desc(a_base + off, 16, 1024, ptx::kLayoutSw128),
+                      ptx::smem_desc(s_k + off, 16, 1024, ptx::kLayoutSw128), idesc, s > 0);
+      }
+      if (cached && precise) {
+#pragma unroll
+        for (int s = 0; s < D / 16; ++s) {
+          const uint32_t off = (s >> 2) * kHalf + (s & 3) * 32;
+          ptx::mma_f16(t_s, ptx::smem_desc(s_qlo + off, 16, 1024, ptx::kLayoutSw128),
+                        ptx::smem_desc(s_k + off, 16, 1024, ptx::kLayoutSw128), kIdescS, 1);
+        }
       }
       if (cached && use_bias) {
         ptx::mma_f16(t_s, ptx::smem_desc(s_qx, 128, 256, ptx::kLayoutNone),
@@ -538,16 +570,16 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// 3-D map over a [bh][n][d] FP16 tensor, box [1][128][64], 128-byte swizzle,
-// zero fill outside the tensor.
-bool make_map(CUtensorMap* m, const void* base, int d, int n, int bh) {
+// 3-D map over a [bh][n][d] 16-bit tensor, box [1][128][64], 128-byte
+// swizzle, zero fill outside the tensor.
+bool make_map(CUtensorMap* m, const void* base, int d, int n, int bh, bool bf16) {
   auto fn = encode_fn();
   if (fn == nullptr) return false;
   cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)n, (cuuint64_t)bh};
   cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)n * d * 2};
   cuuint32_t box[3] = {64, 128, 1};
   cuuint32_t estr[3] = {1, 1, 1};
-  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void*>(base), dims, strides,
+  CUresult r = fn(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void*>(base), dims, strides,
                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
@@ -564,11 +596,17 @@ kvq_status launch_t(const AttnLaunch& a, cudaStream_t stream) {
       return KVQ_ERR_CUDA;
     attr_set = true;
   }
-  CUtensorMap mq, mk, mv;
-  if (!make_map(&mq, a.q_rot, D, a.n_q, a.bh)) return KVQ_ERR_CUDA;
+  CUtensorMap mq, mqlo, mqo, mk, mv;
+  if (!make_map(&mq, a.q_rot, D, a.n_q, a.bh, false)) return KVQ_ERR_CUDA;
+  if (!make_map(&mqlo, a.q_rot_lo, D, a.n_q, a.bh, false)) return KVQ_ERR_CUDA;
+  if (!make_map(&mqo, a.q_orig, D, a.n_q, a.bh, true)) return KVQ_ERR_CUDA;
   if (a.n_r > 0) {
-    if (!make_map(&mk, a.k_rot, D, a.n_r, a.bh)) return KVQ_ERR_CUDA;
-    if (!make_map(&mv, a.mass_only ? a.k_rot : a.v_rot, D, a.n_r, a.bh)) return KVQ_ERR_CUDA;
+    if (!make_map(&mk, a.k_cur, D, a.n_r, a.bh, true)) return KVQ_ERR_CUDA;
+    if (a.mass_only) {
+      mv = mk;
+    } else if (!make_map(&mv, a.v_rot, D, a.n_r, a.bh, false)) {
+      return KVQ_ERR_CUDA;
+    }
   } else {
     mk = mq;
     mv = mq;
@@ -585,6 +623,7 @@ kvq_status launch_t(const AttnLaunch& a, cudaStream_t stream) {
   p.scale_log2 = a.scale * 1.4426950408889634f;
   p.alpha_coef = a.corr ? -(a.scale / 24.0f) : 0.0f;
   p.corr = a.corr;
+  p.precise_query = a.precise_query;
   p.mass_only = a.mass_only;
   p.out = a.out;
   p.p_s = a.p_s;
@@ -593,7 +632,7 @@ kvq_status launch_t(const AttnLaunch& a, cudaStream_t stream) {
   p.inv_sqrt_d = (float)(1.0 / sqrt((double)D));
   p.wait_limit_ns = a.wait_limit_ns;
   dim3 grid((a.n_q + kBlockM - 1) / kBlockM, a.bh);
-  kern<<<grid, kThreads, L::kAlloc, stream>>>(mq, mk, mv, p);
+  kern<<<grid, kThreads, L::kAlloc, stream>>>(mq, mqlo, mqo, mk, mv, p);
   return cudaGetLastError() == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
 }
 

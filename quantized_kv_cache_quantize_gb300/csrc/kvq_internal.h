@@ -35,14 +35,17 @@ struct QuantArgs {
   float inv_sqrt_d;
 };
 
-// Arguments of the rotation kernel: up to three row segments in one launch.
+// Arguments of the rotation kernel: up to two row segments in one launch.
+// Per segment: fp32 output (out_f32), or FP16 output in dst plus, when
+// dst_lo is set, the FP16 rounding remainder fp16(x - fp16(x)) in dst_lo.
 struct RotateArgs {
-  const uint16_t* src[3];
-  void* dst[3];
-  long long rows[3];
+  const uint16_t* src[2];
+  void* dst[2];
+  uint16_t* dst_lo[2];
+  long long rows[2];
   uint32_t sign_bits[4];
   float inv_sqrt_d;
-  int out_f32;  // 1: fp32 output, 0: fp16 (the attention kernel's operand format)
+  int out_f32;
 };
 
 cudaError_t launch_quantize_append(const QuantArgs& a, int d, int bits, int group,
@@ -59,13 +62,17 @@ struct AttnLaunch {
   const uint32_t* v_sz;
   int n_s;   // valid cached tokens per head
   int cap;
-  // rotated current-chunk tensors (workspace)
+  // queries: rotated FP16 (hi and lo parts, workspace) and original BF16
   const uint16_t* q_rot;
-  const uint16_t* k_rot;
+  const uint16_t* q_rot_lo;
+  const uint16_t* q_orig;
+  // current chunk: original BF16 keys, rotated FP16 values (workspace)
+  const uint16_t* k_cur;
   const uint16_t* v_rot;
   int n_q, n_r, bh;
   float scale;
   int corr;
+  int precise_query;
   int mass_only;
   uint16_t* out;
   float* p_s;

@@ -153,7 +153,7 @@ __global__ void __launch_bounds__(kThreads) rotate_kernel(const RotateArgs a) {
   constexpr int RPW = 32 / LPR;
   const int lane = threadIdx.x & 31;
   const int t = lane % LPR;
-  const long long total = a.rows[0] + a.rows[1] + a.rows[2];
+  const long long total = a.rows[0] + a.rows[1];
   const long long warp0 = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const long long nwarps = ((long long)gridDim.x * blockDim.x) >> 5;
   const uint32_t sign_word = sign_word_for(a.sign_bits, t);
@@ -162,17 +162,11 @@ __global__ void __launch_bounds__(kThreads) rotate_kernel(const RotateArgs a) {
     const long long r = r0 + lane / LPR;
     const bool valid = r < total;
     long long rr = valid ? r : 0;
-    int seg = 0;
-    if (rr >= a.rows[0]) {
-      rr -= a.rows[0];
-      seg = 1;
-      if (rr >= a.rows[1]) {
-        rr -= a.rows[1];
-        seg = 2;
-      }
-    }
-    const uint16_t* srcp = seg == 0 ? a.src[0] : (seg == 1 ? a.src[1] : a.src[2]);
-    void* dstp = seg == 0 ? a.dst[0] : (seg == 1 ? a.dst[1] : a.dst[2]);
+    const bool seg1 = rr >= a.rows[0];
+    if (seg1) rr -= a.rows[0];
+    const uint16_t* srcp = seg1 ? a.src[1] : a.src[0];
+    void* dstp = seg1 ? a.dst[1] : a.dst[0];
+    uint16_t* lop = seg1 ? a.dst_lo[1] : a.dst_lo[0];
     uint4 raw = make_uint4(0u, 0u, 0u, 0u);
     if (valid) raw = __ldg(reinterpret_cast<const uint4*>(srcp + rr * D + 8 * t));
     float x[8];
@@ -186,12 +180,21 @@ __global__ void __launch_bounds__(kThreads) rotate_kernel(const RotateArgs a) {
       dst[0] = make_float4(x[0], x[1], x[2], x[3]);
       dst[1] = make_float4(x[4], x[5], x[6], x[7]);
     } else {
-      uint4 o;
-      o.x = h_bits_rn(x[0]) | (h_bits_rn(x[1]) << 16);
-      o.y = h_bits_rn(x[2]) | (h_bits_rn(x[3]) << 16);
-      o.z = h_bits_rn(x[4]) | (h_bits_rn(x[5]) << 16);
-      o.w = h_bits_rn(x[6]) | (h_bits_rn(x[7]) << 16);
-      *reinterpret_cast<uint4*>(static_cast<uint16_t*>(dstp) + rr * D + 8 * t) = o;
+      uint32_t hb[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) hb[e] = h_bits_rn(x[e]);
+      *reinterpret_cast<uint4*>(static_cast<uint16_t*>(dstp) + rr * D + 8 * t) =
+          make_uint4(hb[0] | (hb[1] << 16), hb[2] | (hb[3] << 16), hb[4] | (hb[5] << 16),
+                     hb[6] | (hb[7] << 16));
+      if (lop != nullptr) {
+        uint32_t lb[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+          lb[e] = h_bits_rn(__fsub_rn(x[e], __half2float(__ushort_as_half((unsigned short)hb[e]))));
+        *reinterpret_cast<uint4*>(lop + rr * D + 8 * t) =
+            make_uint4(lb[0] | (lb[1] << 16), lb[2] | (lb[3] << 16), lb[4] | (lb[5] << 16),
+                       lb[6] | (lb[7] << 16));
+      }
     }
   }
 }
@@ -246,7 +249,7 @@ cudaError_t launch_quantize_append(const QuantArgs& a, int d, int bits, int grou
 }
 
 cudaError_t launch_rotate(const RotateArgs& a, int d, cudaStream_t stream) {
-  const long long rows = a.rows[0] + a.rows[1] + a.rows[2];
+  const long long rows = a.rows[0] + a.rows[1];
   if (rows == 0) return cudaSuccess;
   const int rows_per_block = (kThreads / 32) * (32 / (d / 8));
   const unsigned grid = (unsigned)grid_for_rows(rows, rows_per_block);

@@ -24,6 +24,7 @@ KVQ_ERR_ALIGNMENT = 6
 
 CORR_NONE = 0
 CORR_TAYLOR = 1
+FLAG_PRECISE_QUERY = 1
 
 
 class KVQError(RuntimeError):
@@ -54,11 +55,11 @@ _SIGNATURES = {
     "kvq_quantize_append": (ctypes.c_int, [_P, _P, _P, ctypes.c_int32, _P]),
     "kvq_workspace_bytes": (ctypes.c_size_t, [_P, ctypes.c_int32, ctypes.c_int32]),
     "kvq_attention_corrected": (ctypes.c_int, [_P, _P, _P, _P, ctypes.c_int32, ctypes.c_int32,
-                                               ctypes.c_float, ctypes.c_int32, _P, ctypes.c_size_t,
-                                               _P, _P, _P, _P]),
+                                               ctypes.c_float, ctypes.c_int32, ctypes.c_int32, _P,
+                                               ctypes.c_size_t, _P, _P, _P, _P]),
     "kvq_attention_mass": (ctypes.c_int, [_P, _P, _P, ctypes.c_int32, ctypes.c_int32,
-                                          ctypes.c_float, ctypes.c_int32, _P, ctypes.c_size_t,
-                                          _P, _P, _P]),
+                                          ctypes.c_float, ctypes.c_int32, ctypes.c_int32, _P,
+                                          ctypes.c_size_t, _P, _P, _P]),
     "kvq_rotate": (ctypes.c_int, [_P, ctypes.c_int64, ctypes.c_int32, _P, _P, _P, _P]),
     "kvq_last_device_status": (ctypes.c_int, [_P]),
     "kvq_set_wait_limit_ns": (ctypes.c_int, [ctypes.c_uint64]),
@@ -182,7 +183,7 @@ def quantize_append(cache: KVCache, k_new: torch.Tensor, v_new: torch.Tensor, st
 
 def attention_corrected(cache: KVCache, q, k_cur, v_cur, scale: float | None = None,
                         corr: int = CORR_TAYLOR, out=None, with_mass: bool = False,
-                        workspace=None, stream=None):
+                        workspace=None, stream=None, flags: int = 0):
     """kvq_attention_corrected.  q [B, H, n_q, d], k_cur/v_cur [B, H, n_r, d]
     bf16 on the device.  Returns out (and (p_s, p_r) when with_mass)."""
     _bf16_dev(q, "q")
@@ -202,13 +203,13 @@ def attention_corrected(cache: KVCache, q, k_cur, v_cur, scale: float | None = N
         workspace = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=q.device)
     _check(lib().kvq_attention_corrected(
         ctypes.byref(cache.struct), _ptr(q), _ptr(k_cur), _ptr(v_cur), n_q, n_r,
-        ctypes.c_float(scale), corr, _ptr(workspace), workspace.numel(), _ptr(out),
+        ctypes.c_float(scale), corr, flags, _ptr(workspace), workspace.numel(), _ptr(out),
         _ptr(ps), _ptr(pr), _stream(stream)), "kvq_attention_corrected")
     return (out, ps, pr) if with_mass else out
 
 
 def attention_mass(cache: KVCache, q, k_cur, scale: float | None = None,
-                   corr: int = CORR_TAYLOR, workspace=None, stream=None):
+                   corr: int = CORR_TAYLOR, workspace=None, stream=None, flags: int = 0):
     """kvq_attention_mass: returns (p_s, p_r), each [B, H, n_q] fp32."""
     _bf16_dev(q, "q")
     _bf16_dev(k_cur, "k_cur")
@@ -221,7 +222,7 @@ def attention_mass(cache: KVCache, q, k_cur, scale: float | None = None,
         workspace = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=q.device)
     _check(lib().kvq_attention_mass(
         ctypes.byref(cache.struct), _ptr(q), _ptr(k_cur), n_q, n_r, ctypes.c_float(scale), corr,
-        _ptr(workspace), workspace.numel(), _ptr(ps), _ptr(pr), _stream(stream)),
+        flags, _ptr(workspace), workspace.numel(), _ptr(ps), _ptr(pr), _stream(stream)),
         "kvq_attention_mass")
     return ps, pr
 

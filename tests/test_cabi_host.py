@@ -109,24 +109,25 @@ def test_append_argument_checks(lib):
 def test_attention_argument_checks(lib):
     c = _cache(len=30)
     ws = lib.kvq_workspace_bytes(ctypes.byref(c), 100, 10)
-    assert ws >= 2 * 100 * 128 * 2 + 2 * 2 * 10 * 128 * 2
+    assert ws >= 2 * (2 * 100 * 128 * 2) + 2 * 10 * 128 * 2
     f = lib.kvq_attention_corrected
     P = 0x10000
-    # bad correction mode, bad scale, missing output, workspace too small
-    assert f(ctypes.byref(c), P, P, P, 100, 10, 0.1, 7, P, ws, P, None, None, None) == 1
-    assert f(ctypes.byref(c), P, P, P, 100, 10, float("nan"), 1, P, ws, P, None, None, None) == 1
-    assert f(ctypes.byref(c), P, P, P, 100, 10, -1.0, 1, P, ws, P, None, None, None) == 1
-    assert f(ctypes.byref(c), P, P, P, 100, 10, 0.1, 1, P, ws, None, None, None, None) == 1
-    assert f(ctypes.byref(c), P, P, P, 100, 10, 0.1, 1, P, ws - 16, P, None, None, None) == 1
-    assert f(ctypes.byref(c), P, P, P, 100, 10, 0.1, 1, P, ws, P, P, None, None) == 1
-    assert f(ctypes.byref(c), P + 2, P, P, 100, 10, 0.1, 1, P, ws, P, None, None, None) == 6
+    # bad correction mode, bad flags, bad scale, missing output, workspace too small
+    assert f(ctypes.byref(c), P, P, P, 100, 10, 0.1, 7, 0, P, ws, P, None, None, None) == 1
+    assert f(ctypes.byref(c), P, P, P, 100, 10, 0.1, 1, 6, P, ws, P, None, None, None) == 1
+    assert f(ctypes.byref(c), P, P, P, 100, 10, float("nan"), 1, 0, P, ws, P, None, None, None) == 1
+    assert f(ctypes.byref(c), P, P, P, 100, 10, -1.0, 1, 0, P, ws, P, None, None, None) == 1
+    assert f(ctypes.byref(c), P, P, P, 100, 10, 0.1, 1, 0, P, ws, None, None, None, None) == 1
+    assert f(ctypes.byref(c), P, P, P, 100, 10, 0.1, 1, 0, P, ws - 16, P, None, None, None) == 1
+    assert f(ctypes.byref(c), P, P, P, 100, 10, 0.1, 1, 0, P, ws, P, P, None, None) == 1
+    assert f(ctypes.byref(c), P + 2, P, P, 100, 10, 0.1, 1, 0, P, ws, P, None, None, None) == 6
     # nothing to attend to
     c0 = _cache(len=0)
-    assert f(ctypes.byref(c0), P, P, P, 100, 0, 0.1, 1, P, ws, P, None, None, None) == 1
+    assert f(ctypes.byref(c0), P, P, P, 100, 0, 0.1, 1, 0, P, ws, P, None, None, None) == 1
     # no queries: a no-op
-    assert f(ctypes.byref(c), P, P, P, 0, 10, 0.1, 1, P, ws, P, None, None, None) == 0
+    assert f(ctypes.byref(c), P, P, P, 0, 10, 0.1, 1, 1, P, ws, P, None, None, None) == 0
     g = lib.kvq_attention_mass
-    assert g(ctypes.byref(c), P, P, 100, 10, 0.1, 1, P, ws, None, None, None) == 1
+    assert g(ctypes.byref(c), P, P, 100, 10, 0.1, 1, 0, P, ws, None, None, None) == 1
 
 
 def test_rotate_argument_checks(lib):
