@@ -214,6 +214,7 @@ kvq_status kvq_quantize_append(kvq_cache* cache, const uint16_t* k_new, const ui
   if (n_new < 0) return KVQ_ERR_INVALID_ARG;
   if (n_new > cache->chunk_tokens) return KVQ_ERR_CAPACITY;
   if (n_new == 0) return KVQ_OK;
+  if (2LL * g.bh * n_new >= (1LL << 31)) return KVQ_ERR_INVALID_ARG;  // 32-bit row index
   st = check_cache_buffers(cache);
   if (st != KVQ_OK) return st;
   if (k_new == nullptr || v_new == nullptr) return KVQ_ERR_INVALID_ARG;

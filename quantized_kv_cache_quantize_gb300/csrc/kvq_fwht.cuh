@@ -31,31 +31,44 @@ __device__ __forceinline__ void fwht_row(float (&x)[8], int t) {
   }
 #pragma unroll
   for (int dl = 1; dl < LPR; dl <<= 1) {
-    const bool upper = (t & dl) != 0;
+    // lower lane holds x_i: x_i + x_{i+h}; upper lane holds x_{i+h}:
+    // x_i - x_{i+h}.  One fused multiply-add with a +-1 factor rounds the
+    // exact sum once, exactly like the separate add / subtract.
+    const float sgn = (t & dl) ? -1.0f : 1.0f;
 #pragma unroll
     for (int e = 0; e < 8; ++e) {
       const float p = __shfl_xor_sync(0xffffffffu, x[e], dl);
-      // lower lane holds x_i: x_i + x_{i+h}; upper lane holds x_{i+h}: x_i - x_{i+h}
-      x[e] = upper ? __fsub_rn(p, x[e]) : __fadd_rn(x[e], p);
+      x[e] = __fmaf_rn(sgn, x[e], p);
     }
   }
 }
 
-// Unpack 8 BF16 values (one 16-byte vector) to fp32 and apply the sign flips
-// of channels 8t .. 8t + 7 (exact: only the sign bit changes).
-__device__ __forceinline__ void load8_signed(const uint4& raw, uint32_t sign_word, int t,
-                                             float (&x)[8]) {
-  const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+// Sign-bit masks of channels 8t .. 8t + 7 (bit 31 set where sigma_c = -1).
+__device__ __forceinline__ void sign_masks(uint32_t sign_word, int t, uint32_t (&m)[8]) {
   const uint32_t sbits = (sign_word >> ((t & 3) * 8)) & 0xFFu;
 #pragma unroll
+  for (int e = 0; e < 8; ++e) m[e] = ((sbits >> e) & 1u) << 31;
+}
+
+// Unpack 8 BF16 values (one 16-byte vector) to fp32 and flip the signs given
+// by the masks (exact: only the sign bit changes).
+__device__ __forceinline__ void load8_masked(const uint4& raw, const uint32_t (&m)[8],
+                                             float (&x)[8]) {
+  const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
   for (int i = 0; i < 4; ++i) {
-    uint32_t lo = w[i] << 16;
-    uint32_t hi = w[i] & 0xFFFF0000u;
-    lo ^= ((sbits >> (2 * i)) & 1u) << 31;
-    hi ^= ((sbits >> (2 * i + 1)) & 1u) << 31;
-    x[2 * i] = __uint_as_float(lo);
-    x[2 * i + 1] = __uint_as_float(hi);
+    x[2 * i] = __uint_as_float((w[i] << 16) ^ m[2 * i]);
+    x[2 * i + 1] = __uint_as_float((w[i] & 0xFFFF0000u) ^ m[2 * i + 1]);
   }
+}
+
+// Unpack 8 BF16 values (one 16-byte vector) to fp32 and apply the sign flips
+// of channels 8t .. 8t + 7.
+__device__ __forceinline__ void load8_signed(const uint4& raw, uint32_t sign_word, int t,
+                                             float (&x)[8]) {
+  uint32_t m[8];
+  sign_masks(sign_word, t, m);
+  load8_masked(raw, m, x);
 }
 
 __device__ __forceinline__ uint32_t bf16_bits_rn(float v) {

@@ -39,6 +39,18 @@ __device__ __forceinline__ uint32_t sign_word_for(const uint32_t (&sb)[4], int t
   return i == 0 ? sb[0] : i == 1 ? sb[1] : i == 2 ? sb[2] : sb[3];
 }
 
+// rint(fl(x / delta)) (IEEE quotient, ties to even).  q = fl(x * fl(1/delta))
+// is within 2^-22 |q| of fl(x / delta), so unless q lies within 2^-20
+// max(1, |q|) of a half-integer both round to the same integer; near a
+// half-integer (and for non-finite q) the correctly rounded division decides.
+__device__ __forceinline__ float rint_div(float x, float delta, float rcp) {
+  const float q = __fmul_rn(x, rcp);
+  const float n = rintf(q);
+  const float margin = __fsub_rn(0.5f, fabsf(__fsub_rn(q, n)));
+  if (!(margin > 0x1p-20f * fmaxf(1.0f, fabsf(q)))) return rintf(__fdiv_rn(x, delta));
+  return n;
+}
+
 template <int D, int BITS, int GROUP>
 __global__ void __launch_bounds__(kThreads) quantize_append_kernel(const QuantArgs a) {
   constexpr int LPR = D / 8;                 // lanes per row
@@ -55,37 +67,43 @@ __global__ void __launch_bounds__(kThreads) quantize_append_kernel(const QuantAr
   const int lane = threadIdx.x & 31;
   const int t = lane % LPR;                  // lane within the row group
   const int rbase = lane - t;
-  const long long per_kv = (long long)a.bh * a.n_new;
-  const long long rows_total = 2 * per_kv;
-  const long long warp0 = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  const long long nwarps = ((long long)gridDim.x * blockDim.x) >> 5;
-  const uint32_t sign_word = sign_word_for(a.sign_bits, t);
+  const unsigned per_kv = (unsigned)a.bh * (unsigned)a.n_new;   // < 2^31 (host check)
+  const unsigned rows_total = 2u * per_kv;
+  const unsigned warp0 = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const unsigned stride = ((gridDim.x * blockDim.x) >> 5) * RPW;
+  uint32_t smask[8];
+  sign_masks(sign_word_for(a.sign_bits, t), t, smask);
 
-  for (long long r0 = warp0 * RPW; r0 < rows_total; r0 += nwarps * RPW) {
-    const long long r = r0 + lane / LPR;
-    const bool valid = r < rows_total;
-    const long long rr = valid ? r : 0;
-    const bool is_v = rr >= per_kv;
-    const long long rk = is_v ? rr - per_kv : rr;
-    const long long bh = rk / a.n_new;
-    const long long tok = rk - bh * a.n_new;
-    const uint16_t* src = (is_v ? a.v_new : a.k_new) + rk * D + 8 * t;
+  auto load_row = [&](unsigned r) {
     uint4 raw = make_uint4(0u, 0u, 0u, 0u);
-    if (valid) raw = __ldg(reinterpret_cast<const uint4*>(src));
+    if (r < rows_total) {
+      const bool is_v = r >= per_kv;
+      const unsigned rk = is_v ? r - per_kv : r;
+      raw = __ldg(reinterpret_cast<const uint4*>((is_v ? a.v_new : a.k_new) + (size_t)rk * D + 8 * t));
+    }
+    return raw;
+  };
+
+  unsigned r = warp0 * RPW + lane / LPR;
+  uint4 raw = load_row(r);
+  for (unsigned r0 = warp0 * RPW; r0 < rows_total; r0 += stride, r += stride) {
+    const uint4 next = load_row(r + stride);   // keep the next row's load in flight
+    const bool valid = r < rows_total;
+    const bool is_v = r >= per_kv;
+    const unsigned rk = is_v ? r - per_kv : r;
+    const unsigned bh = rk / (unsigned)a.n_new;
+    const unsigned tok = rk - bh * (unsigned)a.n_new;
 
     float x[8];
-    load8_signed(raw, sign_word, t, x);
+    load8_masked(raw, smask, x);
+    raw = next;
     fwht_row<LPR>(x, t);
 #pragma unroll
     for (int e = 0; e < 8; ++e) x[e] = __fmul_rn(x[e], a.inv_sqrt_d);
 
     // group min / max (exact operations: order does not matter)
-    float mn = x[0], mx = x[0];
-#pragma unroll
-    for (int e = 1; e < 8; ++e) {
-      mn = fminf(mn, x[e]);
-      mx = fmaxf(mx, x[e]);
-    }
+    float mn = fminf(fminf(fminf(x[0], x[1]), fminf(x[2], x[3])), fminf(fminf(x[4], x[5]), fminf(x[6], x[7])));
+    float mx = fmaxf(fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3])), fmaxf(fmaxf(x[4], x[5]), fmaxf(x[6], x[7])));
 #pragma unroll
     for (int dl = 1; dl < LPG; dl <<= 1) {
       mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, dl));
@@ -98,13 +116,14 @@ __global__ void __launch_bounds__(kThreads) quantize_append_kernel(const QuantAr
       if (bf16_value(dbits) == 0.0f) dbits = 0x3F80u;  // 1.0
     }
     const float delta = bf16_value(dbits);
+    const float rcp = __frcp_rn(delta);
     const uint32_t zbits = bf16_bits_rn(__fadd_rn(rintf(__fdiv_rn(-mn, delta)), 0.0f));
     const float zero = bf16_value(zbits);
 
     uint32_t word = 0;
 #pragma unroll
     for (int e = 0; e < 8; ++e) {
-      float c = __fadd_rn(rintf(__fdiv_rn(x[e], delta)), zero);
+      float c = __fadd_rn(rint_div(x[e], delta, rcp), zero);
       c = fminf(fmaxf(c, 0.0f), qmax);
       const uint32_t code = (uint32_t)__float2int_rn(c);
       if (BITS == 2) {
@@ -117,13 +136,13 @@ __global__ void __launch_bounds__(kThreads) quantize_append_kernel(const QuantAr
 
     // 16-byte code chunks: chunk j = words 4j .. 4j+3
     const int j = t / LPC;
-    const int stride = (BITS == 2) ? (LPC / 4) : 1;
+    const int wstride = (BITS == 2) ? (LPC / 4) : 1;
     uint4 chunk;
-    chunk.x = shfl_idx(word, rbase + LPC * j + 0 * stride);
-    chunk.y = shfl_idx(word, rbase + LPC * j + 1 * stride);
-    chunk.z = shfl_idx(word, rbase + LPC * j + 2 * stride);
-    chunk.w = shfl_idx(word, rbase + LPC * j + 3 * stride);
-    const long long dst_tok = bh * a.cap + a.first + tok;
+    chunk.x = shfl_idx(word, rbase + LPC * j + 0 * wstride);
+    chunk.y = shfl_idx(word, rbase + LPC * j + 1 * wstride);
+    chunk.z = shfl_idx(word, rbase + LPC * j + 2 * wstride);
+    chunk.w = shfl_idx(word, rbase + LPC * j + 3 * wstride);
+    const size_t dst_tok = (size_t)bh * a.cap + a.first + tok;
     if (valid && (t % LPC) == 0) {
       uint8_t* dst = (is_v ? a.v_codes : a.k_codes) + dst_tok * CODE_BYTES + 16 * j;
       *reinterpret_cast<uint4*>(dst) = chunk;
@@ -221,10 +240,19 @@ long long grid_for_rows(long long rows, int rows_per_block) {
 
 template <int D, int BITS, int GROUP>
 cudaError_t launch_q(const QuantArgs& a, cudaStream_t s) {
+  static int resident = 0;
+  if (resident == 0) {
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+            &resident, quantize_append_kernel<D, BITS, GROUP>, kThreads, 0) != cudaSuccess ||
+        resident < 1)
+      resident = 1;
+  }
   const long long rows = 2LL * a.bh * a.n_new;
   const int rows_per_block = (kThreads / 32) * (32 / (D / 8));
-  quantize_append_kernel<D, BITS, GROUP>
-      <<<(unsigned)grid_for_rows(rows, rows_per_block), kThreads, 0, s>>>(a);
+  long long blocks = (rows + rows_per_block - 1) / rows_per_block;
+  const long long cap = (long long)sm_count() * resident;
+  if (blocks > cap) blocks = cap;
+  quantize_append_kernel<D, BITS, GROUP><<<(unsigned)blocks, kThreads, 0, s>>>(a);
   return cudaGetLastError();
 }
 

@@ -67,10 +67,12 @@ def test_append_bitexact_ring(d, bits, group):
         _check_slot(cache, "v", v, s, first, C)
 
 
-@pytest.mark.parametrize("d,bits,group", [(128, 2, 32), (64, 4, 64)])
+@pytest.mark.parametrize("d,bits,group", [(128, 2, 32), (64, 4, 64), (64, 2, 32)])
 def test_append_partial_and_degenerate(d, bits, group):
     """A partial last chunk; rows with constant groups, all-zero rows,
-    all-positive rows, tiny and huge magnitudes."""
+    all-positive rows, tiny and huge magnitudes, and (d = 64) a row whose
+    rotated values sit exactly on half steps: 12 e_1 rotates to +-1.5, so
+    D = 1 and both the zero point and the codes are exact ties."""
     s = synth.hadamard_signs(d)
     cache = kvq.KVCache(1, 2, d, bits, group, 16, 2, np.ones(d, np.float32))
     rows = np.zeros((1, 2, 16, d), np.float32)
@@ -81,6 +83,8 @@ def test_append_partial_and_degenerate(d, bits, group):
     rows[0, 0, 4] = rng.standard_normal(d) * 1e30
     rows[0, 1] = rng.standard_normal((16, d))
     rows[0, 1, 5, :group] = 0.25
+    rows[0, 1, 6] = 0.0
+    rows[0, 1, 6, 1] = 12.0
     k = _bf16(rows)
     v = _bf16(rows[:, ::-1].copy())
     kvq.quantize_append(cache, k.cuda(), v.cuda())
