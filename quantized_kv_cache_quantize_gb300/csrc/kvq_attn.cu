@@ -84,9 +84,9 @@ struct Smem {
   static constexpr int kK = kQo + kTile;
   static constexpr int kV = kK + kTile;
   static constexpr int kP = kV + kTile;              // 128 x 128 fp16
-  static constexpr int kQx = kP + 2 * kHalf;         // 128 x 16 fp16, no swizzle
-  static constexpr int kKx = kQx + 4096;
-  static constexpr int kBar = kKx + 4096;
+  static constexpr int kQx = kP + 2 * kHalf;         // 2 x [128 x 16] fp16, no swizzle
+  static constexpr int kKx = kQx + 8192;
+  static constexpr int kBar = kKx + 8192;
   static constexpr int kBytes = kBar + 64;
   static constexpr int kAlloc = kBytes + 1024;       // slack for 1024-byte alignment
 };
@@ -131,17 +131,19 @@ __device__ __forceinline__ float h_hi(uint32_t w) { return __half2float(__ushort
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
-// Dequantize one packed row (codes + per-group (step, zero) words) into a
-// FP16 row of the swizzled tile at `tile` (row r): x_hat = (code - z) * D,
-// Eq. (1).  Returns nothing; writes D/8 16-byte chunks.
-template <int D, int BITS, int GROUP>
+// Dequantize one packed row (codes + per-group (step, zero) words) into an
+// FP16 row of the swizzled tile at `tile` (row r).  WITH_ZERO: x_hat =
+// (code - z) * D (Eq. (1)); without: code * D only, which is exact in FP16
+// for INT2 (<= 10 significant bits) -- the zero-point term of the keys is
+// added through the extension columns instead.  Writes D/8 16-byte chunks.
+template <int D, int BITS, int GROUP, bool WITH_ZERO>
 __device__ __forceinline__ void dequant_row(const uint32_t* words, const uint32_t* sz,
                                             uint8_t* tile, int r) {
 #pragma unroll
   for (int c = 0; c < D / 8; ++c) {
     const int g = (8 * c) / GROUP;
     const float delta = bf16_lo(sz[g]);
-    const float zero = bf16_hi(sz[g]);
+    const float zero = WITH_ZERO ? bf16_hi(sz[g]) : 0.0f;
     uint32_t out[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
@@ -174,9 +176,12 @@ __device__ __forceinline__ void zero_row(uint8_t* tile, int r) {
   }
 }
 
-// 16 bias columns of one row: per group g, three columns (hi, hi, lo) on the
-// query side against (hi, lo, hi) on the key side, so that their product sum
-// is a_g * b_g to ~2^-21 relative with FP16 operands.
+// 16 extension columns of one row.  A rank-G term sum_g a_jg * b_ig enters the
+// score as three columns per group: (hi, hi, lo) of a on the query side
+// against (hi, lo, hi) of b on the key side (FP16 high/low splits), so the
+// column products sum to a * b to ~2^-21 relative.  Extension tile 0 holds
+// the Jensen bias (a = -(scale/24) ||q'_g||^2, b = D_g^2), tile 1 the
+// zero-point term of the keys (a = sum of q'_g, b = -z_g * D_g).
 __device__ __forceinline__ void write_ext_row(uint8_t* tile, int r, const float* cols16) {
   uint32_t w[8];
 #pragma unroll
@@ -259,11 +264,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   bool ok = wait_bounded(bar_load, ph_load, lim);
   ph_load ^= 1;
 
-  // ---- per-row group norms n_g = ||q'_g||^2 and the query bias columns ----
+  // ---- per-row group norms n_g = ||q'_g||^2, group sums, extension columns ----
   {
-    float nrm[G];
+    float nrm[G], qsum[G];
 #pragma unroll
-    for (int g = 0; g < G; ++g) nrm[g] = 0.f;
+    for (int g = 0; g < G; ++g) nrm[g] = qsum[g] = 0.f;
 #pragma unroll
     for (int c = 0; c < D / 8; ++c) {
       const int off = (c >> 3) * kHalf + sw128(tid, c & 7);
@@ -272,18 +277,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (precise) vl = *reinterpret_cast<const uint4*>(smem + L::kQlo + off);
       const uint32_t w[4] = {v.x, v.y, v.z, v.w};
       const uint32_t wl[4] = {vl.x, vl.y, vl.z, vl.w};
-      float acc = 0.f;
+      float acc = 0.f, sum = 0.f;
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         const float a = h_lo(w[i]) + h_lo(wl[i]), b = h_hi(w[i]) + h_hi(wl[i]);
         acc = fmaf(a, a, acc);
         acc = fmaf(b, b, acc);
+        sum += a + b;
       }
       nrm[(8 * c) / GROUP] += acc;
+      qsum[(8 * c) / GROUP] += sum;
     }
-    float cols[16];
+    float cols[16], cols_z[16];
 #pragma unroll
-    for (int i = 0; i < 16; ++i) cols[i] = 0.f;
+    for (int i = 0; i < 16; ++i) cols[i] = cols_z[i] = 0.f;
 #pragma unroll
     for (int g = 0; g < G; ++g) {
       float hi, lo;
@@ -291,8 +298,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       cols[3 * g] = hi;
       cols[3 * g + 1] = hi;
       cols[3 * g + 2] = lo;
+      split_h(qsum[g], hi, lo);
+      cols_z[3 * g] = hi;
+      cols_z[3 * g + 1] = hi;
+      cols_z[3 * g + 2] = lo;
     }
     write_ext_row(smem + L::kQx, tid, cols);
+    write_ext_row(smem + L::kQx + 4096, tid, cols_z);
     ptx::fence_proxy_async_smem();
   }
 
@@ -330,10 +342,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
 #pragma unroll
         for (int g = 0; g < G; ++g) ksz[g] = __ldg(p.k_sz + tok * G + g);
-        dequant_row<D, BITS, GROUP>(kw, ksz, smem + L::kK, tid);
-        float cols[16];
+        dequant_row<D, BITS, GROUP, false>(kw, ksz, smem + L::kK, tid);
+        float cols[16], cols_z[16];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) cols[i] = 0.f;
+        for (int i = 0; i < 16; ++i) cols[i] = cols_z[i] = 0.f;
 #pragma unroll
         for (int g = 0; g < G; ++g) {
           const float dl = bf16_lo(ksz[g]);
@@ -342,8 +354,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           cols[3 * g] = hi;
           cols[3 * g + 1] = lo;
           cols[3 * g + 2] = hi;
+          split_h(-bf16_hi(ksz[g]) * dl, hi, lo);
+          cols_z[3 * g] = hi;
+          cols_z[3 * g + 1] = lo;
+          cols_z[3 * g + 2] = hi;
         }
         write_ext_row(smem + L::kKx, tid, cols);
+        write_ext_row(smem + L::kKx + 4096, tid, cols_z);
         if (do_pv) {
           uint32_t vw[NW], vsz[G > 0 ? G : 1];
           const uint4* vc = reinterpret_cast<const uint4*>(p.v_codes + tok * CB);
@@ -354,13 +371,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
 #pragma unroll
           for (int g = 0; g < G; ++g) vsz[g] = __ldg(p.v_sz + tok * G + g);
-          dequant_row<D, BITS, GROUP>(vw, vsz, smem + L::kV, tid);
+          dequant_row<D, BITS, GROUP, true>(vw, vsz, smem + L::kV, tid);
         }
       } else {
         zero_row<D>(smem + L::kK, tid);
         if (do_pv) zero_row<D>(smem + L::kV, tid);
         const float zeros[16] = {0.f};
         write_ext_row(smem + L::kKx, tid, zeros);
+        write_ext_row(smem + L::kKx + 4096, tid, zeros);
       }
       ptx::fence_proxy_async_smem();
       __syncthreads();
@@ -400,9 +418,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                         ptx::smem_desc(s_k + off, 16, 1024, ptx::kLayoutSw128), kIdescS, 1);
         }
       }
-      if (cached && use_bias) {
-        ptx::mma_f16(t_s, ptx::smem_desc(s_qx, 128, 256, ptx::kLayoutNone),
-                      ptx::smem_desc(s_kx, 128, 256, ptx::kLayoutNone), kIdescS, 1);
+      if (cached) {
+        // zero-point term of the keys, then (with the correction) the bias
+        ptx::mma_f16(t_s, ptx::smem_desc(s_qx + 4096, 128, 256, ptx::kLayoutNone),
+                      ptx::smem_desc(s_kx + 4096, 128, 256, ptx::kLayoutNone), kIdescS, 1);
+        if (use_bias)
+          ptx::mma_f16(t_s, ptx::smem_desc(s_qx, 128, 256, ptx::kLayoutNone),
+                        ptx::smem_desc(s_kx, 128, 256, ptx::kLayoutNone), kIdescS, 1);
       }
       ptx::mma_commit(bar_mma);
     }
