@@ -1,5 +1,6 @@
 // Fused Jensen-bias-corrected chunk attention over a low-bit KV window
-// (sm_103a: TMA, tcgen05 MMA into tensor memory).
+// (sm_103a: TMA, tcgen05 MMA with tensor-memory accumulators, warp
+// specialization).
 //
 // Paper: "Quantized Keys Steal Attention" -- abstract and section 1 (the
 // current chunk attends over the cached window and itself; a per-score
@@ -9,31 +10,32 @@
 // (Eq. (1) dequantization, Hadamard rotation), Figure 2 caption (the masses
 // P_S and P_R).
 //
-// One CTA of 128 threads owns 128 query rows of one (batch, head); thread r
-// owns row r (TMEM lane r).  Per 128-key tile:
-//   cached tile : every thread dequantizes one key's packed K and V row into
-//                 FP16 tiles in shared memory (128-byte swizzle), plus the
-//                 bias columns of that key;
-//   current tile: TMA loads the ORIGINAL BF16 keys and the rotated FP16
-//                 values;
-//   S           : tcgen05 MMAs (M 128, N 128, K 16 steps) into TMEM.  Cached
-//                 tiles: Q' K_hat'^T in FP16 (plus Q'_lo K_hat'^T with the
-//                 precise-query flag), then one K=16 MMA adds
-//                 -(scale/24) sum_g n_jg D_ig^2 through 16 extra columns (bias
-//                 folded into the contraction).  Current tiles: Q K^T on the
-//                 unrotated BF16 inputs (exact products);
-//   softmax     : online, one shared running max, two running sums (cached,
-//                 current); P to shared memory as FP16;
-//   O += P V    : tcgen05 MMAs into TMEM (V operand MN-major).
-// Epilogue: O / (l_S + l_R), inverse rotation per row (FWHT in registers),
-// BF16 store; P_S = l_S / (l_S + l_R), P_R = l_R / (l_S + l_R).
+// One CTA owns NQ tiles of 128 query rows of one (batch, head) and walks the
+// key tiles (128 keys) of the cached window, then of the current chunk.
+// Roles (warps):
+//   softmax   NQ warpgroups; thread r of group q owns row r of query tile q
+//             (TMEM lane r): online softmax with one running max and two
+//             running sums (cached, current), P written back into TMEM;
+//   dequant   one warpgroup; thread r turns key r of a cached tile into FP16
+//             K and V rows in shared memory (128-byte swizzle) plus its
+//             extension columns;
+//   MMA       one thread issues every tcgen05.mma: S = Q K^T (both operands in
+//             shared memory), O += P V (P from tensor memory);
+//   TMA       one thread loads the query tiles and the current-chunk tiles.
+// Hand-offs are mbarriers (two K/V stages, S ready, P ready, stage free);
+// every wait is bounded by a time limit.
 //
-// Operand precision: cached-segment operands are FP16 (11 significant bits,
-// the same MMA rate as BF16).  INT2 dequantized values (code - z) * D with a
-// BF16 step D need at most 10 significant bits, so the cached K/V tiles are
-// exact; the rotated query carries one FP16 rounding unless it is split into
-// high and low parts.  Current-segment scores use the BF16 inputs as they
-// are.  Requires |values| < 65504 after rotation (FP16 range).
+// Numerics.  Cached scores: the K tile holds code * D, exact in FP16 for INT2
+// (<= 10 significant bits); two rank-G terms enter through 16-column
+// extension tiles contracted on the tensor core: the keys' zero points
+// (sum_g (sum_{c in g} q'_c) * (-z_g D_g)) and, with the correction, the Jensen
+// bias -(scale/24) sum_g ||q'_g||^2 D_g^2 (per group three columns, FP16
+// high/low splits, so the products carry ~2^-21 relative error).  The rotated
+// query is FP16 (or FP16 high + low parts with the precise-query flag: one
+// more QK pass on cached tiles).  Current scores use the BF16 inputs as they
+// are (exact products).  P and the rotated current values are FP16; V tiles
+// hold (code - z) * D rounded once to FP16.  Limits: |values| < 65504 after
+// rotation, step sizes < 4096.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -58,9 +60,8 @@ struct AttnParams {
   const uint32_t* v_sz;
   int n_s, cap, n_q, n_r;
   float scale_log2;   // scale * log2(e)
-  float alpha_coef;   // -(scale / 24) with the correction, 0 without
+  float alpha_coef;   // -(scale / 24) * 2^8 with the correction, 0 without
   int corr;
-  int precise_query;
   int mass_only;
   uint16_t* out;
   float* p_s;
@@ -70,34 +71,71 @@ struct AttnParams {
   unsigned long long wait_limit_ns;
 };
 
-constexpr int kThreads = 128;
 constexpr int kBlockM = 128;
 constexpr int kBlockN = 128;
-constexpr int kHalf = 16384;  // one [128 rows][64 x 16-bit] swizzled sub-tile
+constexpr int kHalf = 16384;   // one [128 rows][64 x 16-bit] swizzled sub-tile
+constexpr int kExt = 4096;     // one [128 rows][16 x 16-bit] tile, no swizzle
+constexpr float kRescaleThreshold = 8.0f;  // log2 units the exponent base may lag
 
-template <int D>
-struct Smem {
+// Extension-column scalings keeping every FP16 operand in range: bias
+// a * 2^8 against D^2 * 2^-8, zero-point term q-sum * 2^4 against -z D * 2^-4.
+constexpr float kBiasKeyScale = 1.0f / 256.0f;
+constexpr float kZeroQueryScale = 16.0f;
+constexpr float kZeroKeyScale = 1.0f / 16.0f;
+
+template <int D, int NQ, bool PRECISE>
+struct Cfg {
   static constexpr int kTile = kBlockM * D * 2;
-  static constexpr int kQ = 0;                       // rotated queries, FP16 (high part)
-  static constexpr int kQlo = kQ + kTile;            // FP16 low part
-  static constexpr int kQo = kQlo + kTile;           // original queries, BF16
-  static constexpr int kK = kQo + kTile;
-  static constexpr int kV = kK + kTile;
-  static constexpr int kP = kV + kTile;              // 128 x 128 fp16
-  static constexpr int kQx = kP + 2 * kHalf;         // 2 x [128 x 16] fp16, no swizzle
-  static constexpr int kKx = kQx + 8192;
-  static constexpr int kBar = kKx + 8192;
-  static constexpr int kBytes = kBar + 64;
-  static constexpr int kAlloc = kBytes + 1024;       // slack for 1024-byte alignment
+  static constexpr int kNKH = D / 64;
+  static constexpr int kSBuf = NQ == 1 ? 2 : 1;            // S buffers per query tile
+  // shared memory
+  static constexpr int kQ = 0;                             // NQ hi tiles [, NQ lo tiles]
+  static constexpr int kQx = kQ + NQ * kTile * (PRECISE ? 2 : 1);
+  static constexpr int kStageBytes = 2 * kTile + 2 * kExt;  // K, V, Kx (bias), Kx (zero)
+  static constexpr int kStages = kQx + NQ * 2 * kExt;
+  static constexpr int kBar = kStages + 2 * kStageBytes;
+  static constexpr int kBytes = kBar + 256;
+  static constexpr int kAlloc = kBytes + 1024;
+  // warps
+  static constexpr int kSoftmaxWarps = 4 * NQ;
+  static constexpr int kDequantWarp = kSoftmaxWarps;
+  static constexpr int kMmaWarp = kSoftmaxWarps + 4;
+  static constexpr int kTmaWarp = kSoftmaxWarps + 5;
+  static constexpr int kThreads = (kSoftmaxWarps + 6) * 32;
+  // tensor memory columns: S buffers, then the O tiles
+  static constexpr int kTO = NQ * kSBuf * 128;
+  static constexpr int kTCols = 512;
+  static_assert(kTO + NQ * D <= kTCols, "tensor memory");
+  static_assert(kAlloc <= 232448, "shared memory");
 };
 
-// Wait for an mbarrier phase with a time limit; false (and the status word
-// set) when the limit ran out.
-__device__ bool wait_bounded(uint32_t bar, uint32_t parity, unsigned long long limit_ns) {
+// mbarrier slots
+enum : int {
+  kBarQ = 0,        // query tiles landed (phase 0: rotated, phase 1: original)
+  kBarQFree = 1,    // all cached-tile QK MMAs done: query buffers reusable
+  kBarQx = 2,       // query extension columns written (NQ * 128 arrivals)
+  kBarFullDq = 3,   // [2] cached stage dequantized (128 arrivals)
+  kBarFullTma = 5,  // [2] current stage loaded (TMA)
+  kBarEmpty = 7,    // [2] stage consumed (MMA commit)
+  kBarS = 9,        // [2] S buffer ready (MMA commit)
+  kBarP = 11,       // [NQ] P written, O rescaled (128 arrivals)
+  kBarOStep = 13,   // [NQ] PV of a tile done (MMA commit; one-tile schedule)
+  kBarODone = 15,   // [NQ] every MMA done (MMA commit)
+  kBarCount = 17
+};
+constexpr int kAbortOffset = kBarCount * 8;
+constexpr int kTmemSlotOffset = kAbortOffset + 4;
+
+// Bounded wait on an mbarrier phase: false when the time limit ran out (the
+// status word and the CTA's abort flag are set) or another role aborted.
+__device__ bool wait_bar(uint32_t bar, uint32_t parity, unsigned long long limit_ns,
+                         volatile int* abort) {
   if (ptx::mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = ptx::globaltimer();
   while (!ptx::mbar_try_wait(bar, parity)) {
+    if (*abort) return false;
     if (ptx::globaltimer() - t0 > limit_ns) {
+      *abort = 1;
       atomicCAS(&g_attn_status, 0, (int)KVQ_ERR_TIMEOUT);
       return false;
     }
@@ -109,61 +147,81 @@ __device__ bool wait_bounded(uint32_t bar, uint32_t parity, unsigned long long l
 // [rows][64 x 16-bit] sub-tile
 __device__ __forceinline__ int sw128(int r, int c) { return r * 128 + ((c ^ (r & 7)) << 4); }
 
-// byte offset of element (row, k) of a [128][16] 16-bit K-major tile without
-// swizzle: 8-row x 16-byte core matrices, K chunks 128 B apart, row groups 256 B
-__device__ __forceinline__ int noswz16(int r, int kchunk) {
-  return (r >> 3) * 256 + kchunk * 128 + (r & 7) * 16;
-}
-
-__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
-  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
-  return *reinterpret_cast<uint32_t*>(&v);
+// byte offset of 16-byte K-chunk `kc` (0..1) of row r of a [128][16] 16-bit
+// K-major tile without swizzle: 8-row x 16-byte core matrices, K chunks
+// 128 B apart, row groups 256 B apart
+__device__ __forceinline__ int noswz16(int r, int kc) {
+  return (r >> 3) * 256 + kc * 128 + (r & 7) * 16;
 }
 
 __device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
   __half2 v = __floats2half2_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);
 }
-
-__device__ __forceinline__ float h_lo(uint32_t w) { return __half2float(__ushort_as_half((unsigned short)(w & 0xFFFFu))); }
-__device__ __forceinline__ float h_hi(uint32_t w) { return __half2float(__ushort_as_half((unsigned short)(w >> 16))); }
-
+__device__ __forceinline__ uint32_t pack_bf2(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+__device__ __forceinline__ float h_lo(uint32_t w) {
+  return __half2float(__ushort_as_half((unsigned short)(w & 0xFFFFu)));
+}
+__device__ __forceinline__ float h_hi(uint32_t w) {
+  return __half2float(__ushort_as_half((unsigned short)(w >> 16)));
+}
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+__device__ __forceinline__ __half2 as_h2(uint32_t w) { return *reinterpret_cast<__half2*>(&w); }
+__device__ __forceinline__ uint32_t as_u32(__half2 h) { return *reinterpret_cast<uint32_t*>(&h); }
 
-// Dequantize one packed row (codes + per-group (step, zero) words) into an
-// FP16 row of the swizzled tile at `tile` (row r).  WITH_ZERO: x_hat =
-// (code - z) * D (Eq. (1)); without: code * D only, which is exact in FP16
-// for INT2 (<= 10 significant bits) -- the zero-point term of the keys is
-// added through the extension columns instead.  Writes D/8 16-byte chunks.
-template <int D, int BITS, int GROUP, bool WITH_ZERO>
-__device__ __forceinline__ void dequant_row(const uint32_t* words, const uint32_t* sz,
-                                            uint8_t* tile, int r) {
+__device__ __forceinline__ void split_h(float v, float& hi, float& lo) {
+  hi = __half2float(__float2half_rn(v));
+  lo = __half2float(__float2half_rn(v - hi));
+}
+
+// 16 extension columns of one row: three per group g, (hi, hi, lo) of a on
+// the query side against (hi, lo, hi) of b on the key side.
+__device__ __forceinline__ void write_ext_row(uint8_t* tile, int r, const float (&cols)[16]) {
+  uint32_t w[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) w[i] = pack_h2(cols[2 * i], cols[2 * i + 1]);
+  *reinterpret_cast<uint4*>(tile + noswz16(r, 0)) = make_uint4(w[0], w[1], w[2], w[3]);
+  *reinterpret_cast<uint4*>(tile + noswz16(r, 1)) = make_uint4(w[4], w[5], w[6], w[7]);
+}
+
+// The code pair k of a packed word (low code at bit BITS*k, high code 16 bits
+// up) moved to bits [6, 6 + BITS) of each 16-bit half and ORed into FP16 16.0
+// (0x4C00, unit 1/64): each half is then exactly 16 + code.
+template <int BITS>
+__device__ __forceinline__ uint32_t code_pair_f16(uint32_t w, int k) {
+  const int pos = BITS * k;
+  const uint32_t t = pos <= 6 ? (w << (6 - pos)) : (w >> (pos - 6));
+  const uint32_t mask = BITS == 2 ? 0x00C000C0u : 0x03C003C0u;
+  return (t & mask) | 0x4C004C00u;
+}
+
+// Dequantize one packed key row into row r of a swizzled FP16 tile.
+// ZERO = false (keys): code * D = (16 + code) D - 16 D in one FMA, exact for
+// INT2.  ZERO = true (values): (code - z) * D, the integer difference exact,
+// one rounding of the product.
+template <int D, int BITS, int GROUP, bool ZERO>
+__device__ __forceinline__ void dequant_row(const uint32_t (&words)[D * BITS / 32],
+                                            const uint32_t (&sz)[D / GROUP], uint8_t* tile,
+                                            int r) {
 #pragma unroll
   for (int c = 0; c < D / 8; ++c) {
     const int g = (8 * c) / GROUP;
-    const float delta = bf16_lo(sz[g]);
-    const float zero = WITH_ZERO ? bf16_hi(sz[g]) : 0.0f;
+    const __half2 d2 = __float2half2_rn(bf16_lo(sz[g]));
+    const __half2 k2 = ZERO ? __float2half2_rn(16.0f + bf16_hi(sz[g]))
+                            : __float2half2_rn(-16.0f * bf16_lo(sz[g]));
     uint32_t out[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      uint32_t c0, c1;
-      if (BITS == 2) {
-        const uint32_t w = words[c >> 1];
-        const int k = 4 * (c & 1) + i;
-        c0 = (w >> (2 * k)) & 3u;
-        c1 = (w >> (2 * k + 16)) & 3u;
-      } else {
-        const uint32_t w = words[c];
-        c0 = (w >> (4 * i)) & 15u;
-        c1 = (w >> (4 * i + 16)) & 15u;
-      }
-      const float v0 = __fmul_rn(__fsub_rn((float)c0, zero), delta);
-      const float v1 = __fmul_rn(__fsub_rn((float)c1, zero), delta);
-      out[i] = pack_h2(v0, v1);
+      const uint32_t v = BITS == 2 ? code_pair_f16<2>(words[c >> 1], 4 * (c & 1) + i)
+                                   : code_pair_f16<4>(words[c], i);
+      const __half2 res = ZERO ? __hmul2(__hsub2(as_h2(v), k2), d2) : __hfma2(as_h2(v), d2, k2);
+      out[i] = as_u32(res);
     }
-    const int half = c >> 3;
-    *reinterpret_cast<uint4*>(tile + half * kHalf + sw128(r, c & 7)) =
+    *reinterpret_cast<uint4*>(tile + (c >> 3) * kHalf + sw128(r, c & 7)) =
         make_uint4(out[0], out[1], out[2], out[3]);
   }
 }
@@ -171,169 +229,290 @@ __device__ __forceinline__ void dequant_row(const uint32_t* words, const uint32_
 template <int D>
 __device__ __forceinline__ void zero_row(uint8_t* tile, int r) {
 #pragma unroll
-  for (int c = 0; c < D / 8; ++c) {
+  for (int c = 0; c < D / 8; ++c)
     *reinterpret_cast<uint4*>(tile + (c >> 3) * kHalf + sw128(r, c & 7)) = make_uint4(0, 0, 0, 0);
-  }
 }
 
-// 16 extension columns of one row.  A rank-G term sum_g a_jg * b_ig enters the
-// score as three columns per group: (hi, hi, lo) of a on the query side
-// against (hi, lo, hi) of b on the key side (FP16 high/low splits), so the
-// column products sum to a * b to ~2^-21 relative.  Extension tile 0 holds
-// the Jensen bias (a = -(scale/24) ||q'_g||^2, b = D_g^2), tile 1 the
-// zero-point term of the keys (a = sum of q'_g, b = -z_g * D_g).
-__device__ __forceinline__ void write_ext_row(uint8_t* tile, int r, const float* cols16) {
-  uint32_t w[8];
-#pragma unroll
-  for (int i = 0; i < 8; ++i) w[i] = pack_h2(cols16[2 * i], cols16[2 * i + 1]);
-  *reinterpret_cast<uint4*>(tile + noswz16(r, 0)) = make_uint4(w[0], w[1], w[2], w[3]);
-  *reinterpret_cast<uint4*>(tile + noswz16(r, 1)) = make_uint4(w[4], w[5], w[6], w[7]);
-}
-
-__device__ __forceinline__ void split_h(float v, float& hi, float& lo) {
-  hi = __half2float(__float2half_rn(v));
-  lo = __half2float(__float2half_rn(v - hi));
-}
-
-template <int D, int BITS, int GROUP>
-__global__ void __launch_bounds__(kThreads, 1)
+template <int D, int BITS, int GROUP, int NQ, bool PRECISE>
+__global__ void __launch_bounds__(Cfg<D, NQ, PRECISE>::kThreads, 1)
     attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_qlo,
                 const __grid_constant__ CUtensorMap tm_qo, const __grid_constant__ CUtensorMap tm_k,
                 const __grid_constant__ CUtensorMap tm_v, const AttnParams p) {
-  using L = Smem<D>;
+  using C = Cfg<D, NQ, PRECISE>;
   constexpr int G = D / GROUP;
-  constexpr int NKH = D / 64;            // 64-channel halves of a row
   constexpr int CB = D * BITS / 8;       // packed bytes per token
   constexpr int NW = CB / 4;             // packed words per token
-  static_assert(3 * G <= 16, "bias columns");
+  constexpr int NKH = C::kNKH;
+  static_assert(3 * G <= 16, "extension columns");
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
-  const int q0 = blockIdx.x * kBlockM;
+  const int lane = tid & 31;
+  const int q0 = blockIdx.x * (kBlockM * NQ);
   const int bh = blockIdx.y;
 
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBar);
-  const uint32_t bar_load = ptx::smem_u32(&bars[0]);
-  const uint32_t bar_mma = ptx::smem_u32(&bars[1]);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kBar + 16);
-
-  const uint32_t s_q = ptx::smem_u32(smem + L::kQ);
-  const uint32_t s_qlo = ptx::smem_u32(smem + L::kQlo);
-  const uint32_t s_qo = ptx::smem_u32(smem + L::kQo);
-  const bool precise = p.precise_query != 0;
-  const uint32_t s_k = ptx::smem_u32(smem + L::kK);
-  const uint32_t s_v = ptx::smem_u32(smem + L::kV);
-  const uint32_t s_p = ptx::smem_u32(smem + L::kP);
-  const uint32_t s_qx = ptx::smem_u32(smem + L::kQx);
-  const uint32_t s_kx = ptx::smem_u32(smem + L::kKx);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kBar);
+  volatile int* abort = reinterpret_cast<volatile int*>(smem + C::kBar + kAbortOffset);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kBar + kTmemSlotOffset);
+  const uint32_t bar0 = ptx::smem_u32(bars);
+#define BAR(i) (bar0 + 8u * (uint32_t)(i))
 
   if (tid == 0) {
-    ptx::mbar_init(bar_load, 1);
-    ptx::mbar_init(bar_mma, 1);
+    ptx::mbar_init(BAR(kBarQ), 1);
+    ptx::mbar_init(BAR(kBarQFree), 1);
+    ptx::mbar_init(BAR(kBarQx), NQ * 128);
+    for (int s = 0; s < 2; ++s) {
+      ptx::mbar_init(BAR(kBarFullDq + s), 128);
+      ptx::mbar_init(BAR(kBarFullTma + s), 1);
+      ptx::mbar_init(BAR(kBarEmpty + s), 1);
+      ptx::mbar_init(BAR(kBarS + s), 1);
+      ptx::mbar_init(BAR(kBarP + s), 128);
+      ptx::mbar_init(BAR(kBarOStep + s), 1);
+      ptx::mbar_init(BAR(kBarODone + s), 1);
+    }
+    *abort = 0;
     ptx::fence_mbar_init();
   }
   if (warp == 0) {
-    ptx::tmem_alloc(ptx::smem_u32(tmem_slot), 256);
+    ptx::tmem_alloc(ptx::smem_u32(tmem_slot), C::kTCols);
     ptx::tmem_relinquish();
   }
   ptx::tc_fence_before();
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
-  const uint32_t t_s = tmem;              // S: columns [0, 128)
-  const uint32_t t_o = tmem + 128;        // O: columns [128, 128 + D)
-
-  uint32_t ph_load = 0, ph_mma = 0;
-  const unsigned long long lim = p.wait_limit_ns;
-
-  // ---- query tiles by TMA: rotated FP16 (+ low part), original BF16 ----
-  if (tid == 0) {
-    const int n_tiles = 1 + (precise ? 1 : 0) + (p.n_r > 0 ? 1 : 0);
-    ptx::mbar_expect_tx(bar_load, n_tiles * NKH * kHalf);
-#pragma unroll
-    for (int h = 0; h < NKH; ++h) {
-      ptx::tma_load_3d(s_q + h * kHalf, &tm_q, 64 * h, q0, bh, bar_load);
-      if (precise) ptx::tma_load_3d(s_qlo + h * kHalf, &tm_qlo, 64 * h, q0, bh, bar_load);
-      if (p.n_r > 0) ptx::tma_load_3d(s_qo + h * kHalf, &tm_qo, 64 * h, q0, bh, bar_load);
-    }
-  }
-  bool ok = wait_bounded(bar_load, ph_load, lim);
-  ph_load ^= 1;
-
-  // ---- per-row group norms n_g = ||q'_g||^2, group sums, extension columns ----
-  {
-    float nrm[G], qsum[G];
-#pragma unroll
-    for (int g = 0; g < G; ++g) nrm[g] = qsum[g] = 0.f;
-#pragma unroll
-    for (int c = 0; c < D / 8; ++c) {
-      const int off = (c >> 3) * kHalf + sw128(tid, c & 7);
-      const uint4 v = *reinterpret_cast<const uint4*>(smem + L::kQ + off);
-      uint4 vl = make_uint4(0u, 0u, 0u, 0u);
-      if (precise) vl = *reinterpret_cast<const uint4*>(smem + L::kQlo + off);
-      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-      const uint32_t wl[4] = {vl.x, vl.y, vl.z, vl.w};
-      float acc = 0.f, sum = 0.f;
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const float a = h_lo(w[i]) + h_lo(wl[i]), b = h_hi(w[i]) + h_hi(wl[i]);
-        acc = fmaf(a, a, acc);
-        acc = fmaf(b, b, acc);
-        sum += a + b;
-      }
-      nrm[(8 * c) / GROUP] += acc;
-      qsum[(8 * c) / GROUP] += sum;
-    }
-    float cols[16], cols_z[16];
-#pragma unroll
-    for (int i = 0; i < 16; ++i) cols[i] = cols_z[i] = 0.f;
-#pragma unroll
-    for (int g = 0; g < G; ++g) {
-      float hi, lo;
-      split_h(p.alpha_coef * nrm[g], hi, lo);
-      cols[3 * g] = hi;
-      cols[3 * g + 1] = hi;
-      cols[3 * g + 2] = lo;
-      split_h(qsum[g], hi, lo);
-      cols_z[3 * g] = hi;
-      cols_z[3 * g + 1] = hi;
-      cols_z[3 * g + 2] = lo;
-    }
-    write_ext_row(smem + L::kQx, tid, cols);
-    write_ext_row(smem + L::kQx + 4096, tid, cols_z);
-    ptx::fence_proxy_async_smem();
-  }
 
   const int n_ct = (p.n_s + kBlockN - 1) / kBlockN;
-  const int n_rt = (p.n_r + kBlockN - 1) / kBlockN;
-  const bool use_bias = p.corr != 0;
-  const bool do_pv = !p.mass_only;
-  constexpr uint32_t kIdescS = ptx::idesc_f16kind(kBlockM, kBlockN, false, false);
-  constexpr uint32_t kIdescSbf = ptx::idesc_f16kind(kBlockM, kBlockN, false, true);
-  constexpr uint32_t kIdescO = ptx::idesc_f16kind(kBlockM, D, true, false);
+  const int n_t = n_ct + (p.n_r + kBlockN - 1) / kBlockN;
+  const bool mass_only = p.mass_only != 0;
+  const unsigned long long lim = p.wait_limit_ns;
 
-  float m_run = -INFINITY, l_s = 0.f, l_r = 0.f;
-  const size_t head_tok = static_cast<size_t>(bh) * p.cap;
-
-  for (int it = 0; it < n_ct + n_rt; ++it) {
-    if (!__syncthreads_and(ok)) {
-      ok = false;
-      break;
+  if (warp < C::kSoftmaxWarps) {
+    // =========================== softmax ===========================
+    const int q = warp >> 2;
+    const int r = tid - q * 128;                      // row within the query tile
+    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    bool ok = wait_bar(BAR(kBarQ), 0, lim, abort);
+    {
+      // group norms ||q'_g||^2 and group sums of the rotated query row
+      float nrm[G], qsum[G];
+#pragma unroll
+      for (int g = 0; g < G; ++g) nrm[g] = qsum[g] = 0.f;
+      const uint8_t* qt = smem + C::kQ + q * C::kTile;
+#pragma unroll
+      for (int c = 0; c < D / 8; ++c) {
+        const int off = (c >> 3) * kHalf + sw128(r, c & 7);
+        const uint4 v = *reinterpret_cast<const uint4*>(qt + off);
+        uint4 vl = make_uint4(0u, 0u, 0u, 0u);
+        if (PRECISE) vl = *reinterpret_cast<const uint4*>(qt + NQ * C::kTile + off);
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+        const uint32_t wl[4] = {vl.x, vl.y, vl.z, vl.w};
+        float acc = 0.f, sum = 0.f;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float a = h_lo(w[i]) + h_lo(wl[i]), b = h_hi(w[i]) + h_hi(wl[i]);
+          acc = fmaf(a, a, acc);
+          acc = fmaf(b, b, acc);
+          sum += a + b;
+        }
+        nrm[(8 * c) / GROUP] += acc;
+        qsum[(8 * c) / GROUP] += sum;
+      }
+      float cb[16], cz[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) cb[i] = cz[i] = 0.f;
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        float hi, lo;
+        split_h(p.alpha_coef * nrm[g], hi, lo);
+        cb[3 * g] = hi; cb[3 * g + 1] = hi; cb[3 * g + 2] = lo;
+        split_h(kZeroQueryScale * qsum[g], hi, lo);
+        cz[3 * g] = hi; cz[3 * g + 1] = hi; cz[3 * g + 2] = lo;
+      }
+      write_ext_row(smem + C::kQx + q * 2 * kExt, r, cb);
+      write_ext_row(smem + C::kQx + q * 2 * kExt + kExt, r, cz);
+      ptx::fence_proxy_async_smem();
+      ptx::mbar_arrive(BAR(kBarQx));
     }
-    const bool cached = it < n_ct;
-    const int key0 = cached ? it * kBlockN : (it - n_ct) * kBlockN;
-    const int n_valid = min(kBlockN, (cached ? p.n_s : p.n_r) - key0);
 
-    if (cached) {
-      // ---- dequantize key row `tid` of this tile into sK / sV / sKx ----
-      const bool valid = tid < n_valid;
+    float m = -INFINITY, l_s = 0.f, l_r = 0.f;
+    const float sl2 = p.scale_log2;
+    const uint32_t t_o = tmem + C::kTO + q * D + lane_off;
+    for (int j = 0; j < n_t && ok; ++j) {
+      const int b = NQ == 2 ? 0 : (j & 1);
+      const uint32_t t_s = tmem + (q * C::kSBuf + b) * 128 + lane_off;
+      const uint32_t par = NQ == 2 ? (j & 1) : ((j >> 1) & 1);
+      if (!wait_bar(BAR(kBarS + q * C::kSBuf + b), par, lim, abort)) { ok = false; break; }
+      ptx::tc_fence_after();
+      const int nv = j < n_ct ? min(kBlockN, p.n_s - j * kBlockN)
+                              : min(kBlockN, p.n_r - (j - n_ct) * kBlockN);
+      // pass 1: row max of the tile
+      float mx = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < kBlockN / 32; ++c) {
+        uint32_t v[32];
+        ptx::tmem_ld32(t_s + 32 * c, v);
+        if (nv == kBlockN) {
+#pragma unroll
+          for (int k = 0; k < 32; ++k) mx = fmaxf(mx, __uint_as_float(v[k]));
+        } else {
+#pragma unroll
+          for (int k = 0; k < 32; ++k) mx = (32 * c + k < nv) ? fmaxf(mx, __uint_as_float(v[k])) : mx;
+        }
+      }
+      // the exponent base may lag the row max by up to 8 (P <= 256); rescale
+      // only when a row's max moved further (warp-uniform: TMEM accesses are)
+      const float m_cand = mx * sl2;
+      const bool need = m_cand > m + kRescaleThreshold;
+      if (NQ == 1 && j > 0) {
+        // one-tile schedule: QK of this tile was issued before the previous
+        // PV; O and the P-ready phases wait for that PV
+        if (!wait_bar(BAR(kBarOStep), (j - 1) & 1, lim, abort)) { ok = false; break; }
+        ptx::tc_fence_after();
+      }
+      if (__any_sync(0xffffffffu, need)) {
+        const float m_new = need ? m_cand : m;
+        const float alpha = exp2f(m - m_new);
+        l_s *= alpha;
+        l_r *= alpha;
+        m = m_new;
+        if (j > 0 && !mass_only) {
+#pragma unroll
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t v[32];
+            ptx::tmem_ld32(t_o + 32 * c, v);
+#pragma unroll
+            for (int k = 0; k < 32; ++k) v[k] = __float_as_uint(__uint_as_float(v[k]) * alpha);
+            ptx::tmem_st32(t_o + 32 * c, v);
+          }
+        }
+      }
+      // pass 2: exponentials, sums, P (FP16 pairs) into the S buffer
+      float sum = 0.f;
+#pragma unroll
+      for (int c = 0; c < kBlockN / 32; ++c) {
+        uint32_t v[32];
+        ptx::tmem_ld32(t_s + 32 * c, v);
+        uint32_t pk[16];
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+          float e0 = exp2f(fmaf(__uint_as_float(v[2 * k]), sl2, -m));
+          float e1 = exp2f(fmaf(__uint_as_float(v[2 * k + 1]), sl2, -m));
+          if (nv != kBlockN) {
+            e0 = (32 * c + 2 * k < nv) ? e0 : 0.f;
+            e1 = (32 * c + 2 * k + 1 < nv) ? e1 : 0.f;
+          }
+          sum += e0 + e1;
+          pk[k] = pack_h2(e0, e1);
+        }
+        if (!mass_only) ptx::tmem_st16(t_s + 16 * c, pk);
+      }
+      if (j < n_ct) l_s += sum; else l_r += sum;
+      ptx::tmem_st_wait();
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(BAR(kBarP + q));
+    }
+
+    // epilogue: O / (l_S + l_R), inverse rotation, BF16 store; masses
+    const int row = q0 + q * kBlockM + r;
+    if (ok) ok = wait_bar(BAR(kBarODone + q), 0, lim, abort);
+    if (ok && !*abort) {
+      ptx::tc_fence_after();
+      const float inv = 1.0f / (l_s + l_r);
+      if (!mass_only) {
+        // O = H^T O' = (1/sqrt(d)) diag(sigma) Sylvester(d) O', one row per
+        // thread: butterflies h < 64 on each 64-column half in registers
+        // (written back to TMEM), then h = 64 chunk by chunk
+#pragma unroll
+        for (int half = 0; half < D / 64; ++half) {
+          float o[64];
+#pragma unroll
+          for (int c = 0; c < 2; ++c) {
+            uint32_t v[32];
+            ptx::tmem_ld32(t_o + 64 * half + 32 * c, v);
+#pragma unroll
+            for (int k = 0; k < 32; ++k) o[32 * c + k] = __uint_as_float(v[k]) * inv;
+          }
+#pragma unroll
+          for (int h = 1; h < 64; h <<= 1) {
+#pragma unroll
+            for (int i = 0; i < 64; ++i) {
+              if ((i & h) == 0) {
+                const float a = o[i], bb = o[i + h];
+                o[i] = a + bb;
+                o[i + h] = a - bb;
+              }
+            }
+          }
+#pragma unroll
+          for (int c = 0; c < 2; ++c) {
+            uint32_t v[32];
+#pragma unroll
+            for (int k = 0; k < 32; ++k) v[k] = __float_as_uint(o[32 * c + k]);
+            ptx::tmem_st32(t_o + 64 * half + 32 * c, v);
+          }
+        }
+        ptx::tmem_st_wait();
+        if (row < p.n_q) {
+          uint16_t* dst = p.out + (static_cast<size_t>(bh) * p.n_q + row) * D;
+          auto store8 = [&](int ch0, const float* v8) {
+            const uint32_t sw = p.sign_bits[ch0 >> 5];
+            float v[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+              v[e] = v8[e] * (((sw >> ((ch0 + e) & 31)) & 1u) ? -p.inv_sqrt_d : p.inv_sqrt_d);
+            *reinterpret_cast<uint4*>(dst + ch0) =
+                make_uint4(pack_bf2(v[0], v[1]), pack_bf2(v[2], v[3]), pack_bf2(v[4], v[5]),
+                           pack_bf2(v[6], v[7]));
+          };
+#pragma unroll
+          for (int c = 0; c < 2; ++c) {
+            uint32_t a[32], bq[32];
+            ptx::tmem_ld32(t_o + 32 * c, a);
+            float lo[32], hi[32];
+            if (D == 128) {
+              ptx::tmem_ld32(t_o + 64 + 32 * c, bq);
+#pragma unroll
+              for (int k = 0; k < 32; ++k) {
+                lo[k] = __uint_as_float(a[k]) + __uint_as_float(bq[k]);
+                hi[k] = __uint_as_float(a[k]) - __uint_as_float(bq[k]);
+              }
+            } else {
+#pragma unroll
+              for (int k = 0; k < 32; ++k) lo[k] = __uint_as_float(a[k]);
+            }
+#pragma unroll
+            for (int e = 0; e < 4; ++e) store8(32 * c + 8 * e, lo + 8 * e);
+            if (D == 128) {
+#pragma unroll
+              for (int e = 0; e < 4; ++e) store8(64 + 32 * c + 8 * e, hi + 8 * e);
+            }
+          }
+        }
+      }
+      if (row < p.n_q && p.p_s != nullptr) {
+        p.p_s[static_cast<size_t>(bh) * p.n_q + row] = l_s * inv;
+        p.p_r[static_cast<size_t>(bh) * p.n_q + row] = l_r * inv;
+      }
+    }
+  } else if (warp < C::kMmaWarp) {
+    // =========================== dequant ===========================
+    const int r = tid - C::kDequantWarp * 32;
+    const size_t head_tok = static_cast<size_t>(bh) * p.cap;
+    for (int j = 0; j < n_ct; ++j) {
+      if (*abort) break;
+      const int s = j & 1;
+      const bool valid = j * kBlockN + r < p.n_s;
+      uint32_t kw[NW], ksz[G], vw[NW], vsz[G];
+#pragma unroll
+      for (int i = 0; i < NW; ++i) kw[i] = vw[i] = 0u;
+#pragma unroll
+      for (int g = 0; g < G; ++g) ksz[g] = vsz[g] = 0u;
       if (valid) {
-        const size_t tok = head_tok + key0 + tid;
-        uint32_t kw[NW], ksz[G > 0 ? G : 1];
+        const size_t tok = head_tok + j * kBlockN + r;
         const uint4* kc = reinterpret_cast<const uint4*>(p.k_codes + tok * CB);
 #pragma unroll
         for (int i = 0; i < NW / 4; ++i) {
@@ -342,27 +521,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
 #pragma unroll
         for (int g = 0; g < G; ++g) ksz[g] = __ldg(p.k_sz + tok * G + g);
-        dequant_row<D, BITS, GROUP, false>(kw, ksz, smem + L::kK, tid);
-        float cols[16], cols_z[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) cols[i] = cols_z[i] = 0.f;
-#pragma unroll
-        for (int g = 0; g < G; ++g) {
-          const float dl = bf16_lo(ksz[g]);
-          float hi, lo;
-          split_h(dl * dl, hi, lo);
-          cols[3 * g] = hi;
-          cols[3 * g + 1] = lo;
-          cols[3 * g + 2] = hi;
-          split_h(-bf16_hi(ksz[g]) * dl, hi, lo);
-          cols_z[3 * g] = hi;
-          cols_z[3 * g + 1] = lo;
-          cols_z[3 * g + 2] = hi;
-        }
-        write_ext_row(smem + L::kKx, tid, cols);
-        write_ext_row(smem + L::kKx + 4096, tid, cols_z);
-        if (do_pv) {
-          uint32_t vw[NW], vsz[G > 0 ? G : 1];
+        if (!mass_only) {
           const uint4* vc = reinterpret_cast<const uint4*>(p.v_codes + tok * CB);
 #pragma unroll
           for (int i = 0; i < NW / 4; ++i) {
@@ -371,208 +530,236 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
 #pragma unroll
           for (int g = 0; g < G; ++g) vsz[g] = __ldg(p.v_sz + tok * G + g);
-          dequant_row<D, BITS, GROUP, true>(vw, vsz, smem + L::kV, tid);
+        }
+      }
+      if (j >= 2 && !wait_bar(BAR(kBarEmpty + s), ((j >> 1) - 1) & 1, lim, abort)) break;
+      uint8_t* st = smem + C::kStages + s * C::kStageBytes;
+      float cb[16], cz[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) cb[i] = cz[i] = 0.f;
+      if (valid) {
+        dequant_row<D, BITS, GROUP, false>(kw, ksz, st, r);
+        if (!mass_only) dequant_row<D, BITS, GROUP, true>(vw, vsz, st + C::kTile, r);
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+          const float dl = bf16_lo(ksz[g]);
+          float hi, lo;
+          split_h(dl * dl * kBiasKeyScale, hi, lo);
+          cb[3 * g] = hi; cb[3 * g + 1] = lo; cb[3 * g + 2] = hi;
+          split_h(-bf16_hi(ksz[g]) * dl * kZeroKeyScale, hi, lo);
+          cz[3 * g] = hi; cz[3 * g + 1] = lo; cz[3 * g + 2] = hi;
         }
       } else {
-        zero_row<D>(smem + L::kK, tid);
-        if (do_pv) zero_row<D>(smem + L::kV, tid);
-        const float zeros[16] = {0.f};
-        write_ext_row(smem + L::kKx, tid, zeros);
-        write_ext_row(smem + L::kKx + 4096, tid, zeros);
+        zero_row<D>(st, r);
+        if (!mass_only) zero_row<D>(st + C::kTile, r);
       }
+      write_ext_row(st + 2 * C::kTile, r, cb);
+      write_ext_row(st + 2 * C::kTile + kExt, r, cz);
       ptx::fence_proxy_async_smem();
-      __syncthreads();
-    } else {
-      if (tid == 0) {
-        ptx::mbar_expect_tx(bar_load, (do_pv ? 2 : 1) * NKH * kHalf);
-#pragma unroll
-        for (int h = 0; h < NKH; ++h) {
-          ptx::tma_load_3d(s_k + h * kHalf, &tm_k, 64 * h, key0, bh, bar_load);
-          if (do_pv) ptx::tma_load_3d(s_v + h * kHalf, &tm_v, 64 * h, key0, bh, bar_load);
-        }
-      }
-      ok = wait_bounded(bar_load, ph_load, lim);
-      ph_load ^= 1;
-      if (!__syncthreads_and(ok)) {
-        ok = false;
-        break;
-      }
+      ptx::mbar_arrive(BAR(kBarFullDq + s));
     }
+  } else if (warp == C::kMmaWarp) {
+    // ============================= MMA =============================
+    if (lane == 0) {
+      constexpr uint32_t kIdS = ptx::idesc_f16kind(kBlockM, kBlockN, false, false);
+      constexpr uint32_t kIdSbf = ptx::idesc_f16kind(kBlockM, kBlockN, false, true);
+      constexpr uint32_t kIdO = ptx::idesc_f16kind(kBlockM, D, true, false);
+      const bool use_bias = p.corr != 0;
+      const uint32_t s_base = ptx::smem_u32(smem);
+      bool ok = wait_bar(BAR(kBarQ), 0, lim, abort) && wait_bar(BAR(kBarQx), 0, lim, abort);
+      if (ok && n_ct == 0) ptx::mbar_arrive(BAR(kBarQFree));
+      bool q_orig_ready = false;
 
-    // ---- S = Q' K_hat'^T (+ low part, + bias columns) or Q K^T ----
-    if (tid == 0) {
-      ptx::tc_fence_after();
-      const uint32_t a_base = cached ? s_q : s_qo;
-      const uint32_t idesc = cached ? kIdescS : kIdescSbf;
-#pragma unroll
-      for (int s = 0; s < D / 16; ++s) {
-        const uint32_t off = (s >> 2) * kHalf + (s & 3) * 32;
-        ptx::mma_f16(t_s, ptx::smem_desc(a_base + off, 16, 1024, ptx::kLayoutSw128),
-                      ptx::smem_desc(s_k + off, 16, 1024, ptx::kLayoutSw128), idesc, s > 0);
-      }
-      if (cached && precise) {
+      auto wait_full = [&](int j) -> bool {
+        const int s = j & 1;
+        // cached tiles are uses 0, 1, ... of their stage's dequant barrier;
+        // current tiles count only the TMA barrier's own uses of that stage
+        const int use = j < n_ct ? (j >> 1) : (j >> 1) - ((n_ct + 1 - s) >> 1);
+        if (!wait_bar(BAR(j < n_ct ? kBarFullDq + s : kBarFullTma + s), use & 1, lim, abort))
+          return false;
+        if (j >= n_ct && !q_orig_ready) {
+          if (!wait_bar(BAR(kBarQ), 1, lim, abort)) return false;
+          q_orig_ready = true;
+        }
+        ptx::tc_fence_after();
+        return true;
+      };
+      auto issue_qk = [&](int j, int q, uint32_t d_tmem) {
+        const uint32_t st = s_base + C::kStages + (j & 1) * C::kStageBytes;
+        const uint32_t qa = s_base + C::kQ + q * C::kTile;
+        const bool cached = j < n_ct;
 #pragma unroll
         for (int s = 0; s < D / 16; ++s) {
           const uint32_t off = (s >> 2) * kHalf + (s & 3) * 32;
-          ptx::mma_f16(t_s, ptx::smem_desc(s_qlo + off, 16, 1024, ptx::kLayoutSw128),
-                        ptx::smem_desc(s_k + off, 16, 1024, ptx::kLayoutSw128), kIdescS, 1);
+          ptx::mma_f16(d_tmem, ptx::smem_desc(qa + off, 16, 1024, ptx::kLayoutSw128),
+                       ptx::smem_desc(st + off, 16, 1024, ptx::kLayoutSw128),
+                       cached ? kIdS : kIdSbf, s > 0);
         }
-      }
-      if (cached) {
-        // zero-point term of the keys, then (with the correction) the bias
-        ptx::mma_f16(t_s, ptx::smem_desc(s_qx + 4096, 128, 256, ptx::kLayoutNone),
-                      ptx::smem_desc(s_kx + 4096, 128, 256, ptx::kLayoutNone), kIdescS, 1);
-        if (use_bias)
-          ptx::mma_f16(t_s, ptx::smem_desc(s_qx, 128, 256, ptx::kLayoutNone),
-                        ptx::smem_desc(s_kx, 128, 256, ptx::kLayoutNone), kIdescS, 1);
-      }
-      ptx::mma_commit(bar_mma);
-    }
-    ok = wait_bounded(bar_mma, ph_mma, lim);
-    ph_mma ^= 1;
-    ptx::tc_fence_after();
-
-    // ---- online softmax of row tid ----
-    float sc[kBlockN];
+        if (cached) {
+          if (PRECISE) {
 #pragma unroll
-    for (int c = 0; c < kBlockN / 32; ++c) {
-      uint32_t r[32];
-      ptx::tmem_ld32(t_s + lane_off + 32 * c, r);
-#pragma unroll
-      for (int j = 0; j < 32; ++j) sc[32 * c + j] = __uint_as_float(r[j]);
-    }
-    float mx = -INFINITY;
-#pragma unroll
-    for (int j = 0; j < kBlockN; ++j) mx = (j < n_valid) ? fmaxf(mx, sc[j]) : mx;
-    const float m_new = fmaxf(m_run, mx * p.scale_log2);
-    const float alpha = exp2f(m_run - m_new);
-    float sum = 0.f;
-#pragma unroll
-    for (int j = 0; j < kBlockN; ++j) {
-      const float e = (j < n_valid) ? exp2f(fmaf(sc[j], p.scale_log2, -m_new)) : 0.f;
-      sc[j] = e;
-      sum += e;
-    }
-    l_s *= alpha;
-    l_r *= alpha;
-    if (cached) l_s += sum; else l_r += sum;
-    m_run = m_new;
-
-    if (do_pv) {
-      // P (FP16) into the swizzled A tile, row tid
-#pragma unroll
-      for (int c = 0; c < kBlockN / 8; ++c) {
-        const uint4 v = make_uint4(pack_h2(sc[8 * c], sc[8 * c + 1]),
-                                   pack_h2(sc[8 * c + 2], sc[8 * c + 3]),
-                                   pack_h2(sc[8 * c + 4], sc[8 * c + 5]),
-                                   pack_h2(sc[8 * c + 6], sc[8 * c + 7]));
-        *reinterpret_cast<uint4*>(smem + L::kP + (c >> 3) * kHalf + sw128(tid, c & 7)) = v;
-      }
-      // rescale the running output when the max moved (warp-uniform decision)
-      if (it > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
-#pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t r[32];
-          ptx::tmem_ld32(t_o + lane_off + 32 * c, r);
-#pragma unroll
-          for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) * alpha);
-          ptx::tmem_st32(t_o + lane_off + 32 * c, r);
+            for (int s = 0; s < D / 16; ++s) {
+              const uint32_t off = (s >> 2) * kHalf + (s & 3) * 32;
+              ptx::mma_f16(d_tmem,
+                           ptx::smem_desc(qa + NQ * C::kTile + off, 16, 1024, ptx::kLayoutSw128),
+                           ptx::smem_desc(st + off, 16, 1024, ptx::kLayoutSw128), kIdS, 1);
+            }
+          }
+          const uint32_t qx = s_base + C::kQx + q * 2 * kExt;
+          const uint32_t kx = st + 2 * C::kTile;
+          ptx::mma_f16(d_tmem, ptx::smem_desc(qx + kExt, 128, 256, ptx::kLayoutNone),
+                       ptx::smem_desc(kx + kExt, 128, 256, ptx::kLayoutNone), kIdS, 1);
+          if (use_bias)
+            ptx::mma_f16(d_tmem, ptx::smem_desc(qx, 128, 256, ptx::kLayoutNone),
+                         ptx::smem_desc(kx, 128, 256, ptx::kLayoutNone), kIdS, 1);
         }
-        ptx::tmem_st_wait();
-      }
-      ptx::fence_proxy_async_smem();
-    }
-    ptx::tc_fence_before();
-    __syncthreads();
-
-    if (do_pv) {
-      // ---- O += P V ----
-      if (tid == 0) {
-        ptx::tc_fence_after();
+      };
+      auto issue_pv = [&](int j, int q, uint32_t p_tmem) {
+        const uint32_t vt = s_base + C::kStages + (j & 1) * C::kStageBytes + C::kTile;
+        const uint32_t o_tmem = tmem + C::kTO + q * D;
 #pragma unroll
         for (int s = 0; s < kBlockN / 16; ++s) {
-          const uint32_t a_off = (s >> 2) * kHalf + (s & 3) * 32;
-          const uint32_t b_off = s * 16 * 128;
-          ptx::mma_f16(t_o, ptx::smem_desc(s_p + a_off, 16, 1024, ptx::kLayoutSw128),
-                        ptx::smem_desc(s_v + b_off, kHalf, 1024, ptx::kLayoutSw128), kIdescO,
-                        (it > 0 || s > 0) ? 1u : 0u);
+          ptx::mma_f16_ts(o_tmem, p_tmem + 8 * s,
+                          ptx::smem_desc(vt + s * 2048, kHalf, 1024, ptx::kLayoutSw128), kIdO,
+                          (j > 0 || s > 0) ? 1u : 0u);
         }
-        ptx::mma_commit(bar_mma);
+      };
+      auto after_qk = [&](int j, int q) {   // query buffers free after the last cached QK
+        if (j == n_ct - 1 && q == NQ - 1) ptx::mma_commit(BAR(kBarQFree));
+      };
+
+      if (ok && n_t > 0) {
+        if (NQ == 2) {
+          ok = wait_full(0);
+          if (ok) {
+            issue_qk(0, 0, tmem);
+            ptx::mma_commit(BAR(kBarS + 0));
+            issue_qk(0, 1, tmem + 128);
+            ptx::mma_commit(BAR(kBarS + 1));
+            after_qk(0, 1);
+          }
+          for (int j = 0; j < n_t && ok; ++j) {
+            if (!(ok = wait_bar(BAR(kBarP + 0), j & 1, lim, abort))) break;
+            ptx::tc_fence_after();
+            if (!mass_only) issue_pv(j, 0, tmem);
+            const bool more = j + 1 < n_t;
+            if (more) {
+              if (!(ok = wait_full(j + 1))) break;
+              issue_qk(j + 1, 0, tmem);
+              ptx::mma_commit(BAR(kBarS + 0));
+            }
+            if (!(ok = wait_bar(BAR(kBarP + 1), j & 1, lim, abort))) break;
+            ptx::tc_fence_after();
+            if (!mass_only) issue_pv(j, 1, tmem + 128);
+            ptx::mma_commit(BAR(kBarEmpty + (j & 1)));
+            if (more) {
+              issue_qk(j + 1, 1, tmem + 128);
+              ptx::mma_commit(BAR(kBarS + 1));
+              after_qk(j + 1, 1);
+            }
+          }
+        } else {
+          ok = wait_full(0);
+          if (ok) {
+            issue_qk(0, 0, tmem);
+            ptx::mma_commit(BAR(kBarS + 0));
+            after_qk(0, 0);
+          }
+          for (int j = 0; j < n_t && ok; ++j) {
+            if (j + 1 < n_t) {
+              if (!(ok = wait_full(j + 1))) break;
+              issue_qk(j + 1, 0, tmem + ((j + 1) & 1) * 128);
+              ptx::mma_commit(BAR(kBarS + ((j + 1) & 1)));
+              after_qk(j + 1, 0);
+            }
+            if (!(ok = wait_bar(BAR(kBarP + 0), j & 1, lim, abort))) break;
+            ptx::tc_fence_after();
+            if (!mass_only) issue_pv(j, 0, tmem + (j & 1) * 128);
+            // also in mass-only mode: keeps the softmax one tile behind
+            ptx::mma_commit(BAR(kBarOStep));
+            ptx::mma_commit(BAR(kBarEmpty + (j & 1)));
+          }
+        }
       }
-      ok = wait_bounded(bar_mma, ph_mma, lim) && ok;
-      ph_mma ^= 1;
-      ptx::tc_fence_after();
+      // completion of every MMA issued: final O for the epilogues and a
+      // drained tensor pipe before the tensor memory is released
+      for (int q = 0; q < NQ; ++q) ptx::mma_commit(BAR(kBarODone + q));
+      int drained = 0;
+      wait_bar(BAR(kBarODone), 0, lim, &drained);
     }
+    __syncwarp();
+  } else {
+    // ============================== TMA ==============================
+    if (lane == 0) {
+      const uint32_t s_base = ptx::smem_u32(smem);
+      ptx::mbar_expect_tx(BAR(kBarQ), NQ * (PRECISE ? 2 : 1) * NKH * kHalf);
+      for (int q = 0; q < NQ; ++q) {
+        for (int h = 0; h < NKH; ++h) {
+          ptx::tma_load_3d(s_base + C::kQ + q * C::kTile + h * kHalf, &tm_q, 64 * h,
+                           q0 + q * kBlockM, bh, BAR(kBarQ));
+          if (PRECISE)
+            ptx::tma_load_3d(s_base + C::kQ + (NQ + q) * C::kTile + h * kHalf, &tm_qlo, 64 * h,
+                             q0 + q * kBlockM, bh, BAR(kBarQ));
+        }
+      }
+      int last = -1;
+      for (int j = n_ct; j < n_t; ++j) {
+        if (*abort) break;
+        const int s = j & 1;
+        if (j == n_ct) {
+          // the original BF16 queries replace the rotated ones once every
+          // cached-tile QK MMA has completed
+          if (!wait_bar(BAR(kBarQFree), 0, lim, abort)) break;
+          ptx::mbar_expect_tx(BAR(kBarQ), NQ * NKH * kHalf);
+          for (int q = 0; q < NQ; ++q)
+            for (int h = 0; h < NKH; ++h)
+              ptx::tma_load_3d(s_base + C::kQ + q * C::kTile + h * kHalf, &tm_qo, 64 * h,
+                               q0 + q * kBlockM, bh, BAR(kBarQ));
+        }
+        if (j >= 2 && !wait_bar(BAR(kBarEmpty + s), ((j >> 1) - 1) & 1, lim, abort)) break;
+        const int key0 = (j - n_ct) * kBlockN;
+        const uint32_t st = s_base + C::kStages + s * C::kStageBytes;
+        ptx::mbar_expect_tx(BAR(kBarFullTma + s), (mass_only ? 1 : 2) * NKH * kHalf);
+        for (int h = 0; h < NKH; ++h) {
+          ptx::tma_load_3d(st + h * kHalf, &tm_k, 64 * h, key0, bh, BAR(kBarFullTma + s));
+          if (!mass_only)
+            ptx::tma_load_3d(st + C::kTile + h * kHalf, &tm_v, 64 * h, key0, bh,
+                             BAR(kBarFullTma + s));
+        }
+        last = j;
+      }
+      // on an abort, let the copies already issued land before the CTA exits
+      if (*abort && last >= 0) {
+        const int s = last & 1;
+        const int use = (last >> 1) - ((n_ct + 1 - s) >> 1);
+        int ignore = 0;
+        wait_bar(BAR(kBarFullTma + s), use & 1, lim, &ignore);
+      }
+    }
+    __syncwarp();
   }
 
-  // ---- epilogue ----
-  ok = __syncthreads_and(ok) != 0;
-  if (ok) {
-    const float denom = l_s + l_r;
-    const float inv = 1.0f / denom;
-    const int row = q0 + tid;
-    const bool row_ok = row < p.n_q;
-    if (do_pv) {
-      float o[D];
-#pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
-        uint32_t r[32];
-        ptx::tmem_ld32(t_o + lane_off + 32 * c, r);
-#pragma unroll
-        for (int j = 0; j < 32; ++j) o[32 * c + j] = __uint_as_float(r[j]) * inv;
-      }
-      // O = H^T O' = (1/sqrt(d)) diag(sigma) Sylvester(d) O'
-#pragma unroll
-      for (int h = 1; h < D; h <<= 1) {
-#pragma unroll
-        for (int i = 0; i < D; ++i) {
-          if ((i & h) == 0) {
-            const float a = o[i], b = o[i + h];
-            o[i] = a + b;
-            o[i + h] = a - b;
-          }
-        }
-      }
-      if (row_ok) {
-        uint16_t* dst = p.out + (static_cast<size_t>(bh) * p.n_q + row) * D;
-#pragma unroll
-        for (int c = 0; c < D / 8; ++c) {
-          float v[8];
-#pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            const int ch = 8 * c + e;
-            const float s = ((p.sign_bits[ch >> 5] >> (ch & 31)) & 1u) ? -p.inv_sqrt_d : p.inv_sqrt_d;
-            v[e] = o[ch] * s;
-          }
-          *reinterpret_cast<uint4*>(dst + 8 * c) =
-              make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]),
-                         pack_bf16x2(v[4], v[5]), pack_bf16x2(v[6], v[7]));
-        }
-      }
-    }
-    if (row_ok && p.p_s != nullptr) {
-      p.p_s[static_cast<size_t>(bh) * p.n_q + row] = l_s * inv;
-      p.p_r[static_cast<size_t>(bh) * p.n_q + row] = l_r * inv;
-    }
-  }
   ptx::tc_fence_before();
   __syncthreads();
   if (warp == 0) {
     ptx::tc_fence_after();
-    ptx::tmem_dealloc(tmem, 256);
+    ptx::tmem_dealloc(tmem, C::kTCols);
   }
+#undef BAR
 }
 
 __global__ void wait_selftest_kernel(unsigned long long limit_ns) {
-  __shared__ __align__(8) uint64_t bar;
-  const uint32_t b = ptx::smem_u32(&bar);
+  __shared__ __align__(8) uint64_t b;
+  __shared__ int abort_flag;
+  const uint32_t a = ptx::smem_u32(&b);
   if (threadIdx.x == 0) {
-    ptx::mbar_init(b, 1);
+    ptx::mbar_init(a, 1);
+    abort_flag = 0;
     ptx::fence_mbar_init();
   }
   __syncthreads();
   // nothing ever arrives on this barrier: the wait must run out and return
-  wait_bounded(b, 0, limit_ns);
+  wait_bar(a, 0, limit_ns, &abort_flag);
 }
 
 // ---- host side -------------------------------------------------------------
@@ -601,19 +788,20 @@ bool make_map(CUtensorMap* m, const void* base, int d, int n, int bh, bool bf16)
   cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)n * d * 2};
   cuuint32_t box[3] = {64, 128, 1};
   cuuint32_t estr[3] = {1, 1, 1};
-  CUresult r = fn(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void*>(base), dims, strides,
-                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  CUresult r = fn(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
+                  const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
 
-template <int D, int BITS, int GROUP>
+template <int D, int BITS, int GROUP, int NQ, bool PRECISE>
 kvq_status launch_t(const AttnLaunch& a, cudaStream_t stream) {
-  using L = Smem<D>;
+  using C = Cfg<D, NQ, PRECISE>;
   static bool attr_set = false;
-  auto kern = attn_kernel<D, BITS, GROUP>;
+  auto kern = attn_kernel<D, BITS, GROUP, NQ, PRECISE>;
   if (!attr_set) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc) !=
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kAlloc) !=
         cudaSuccess)
       return KVQ_ERR_CUDA;
     attr_set = true;
@@ -643,9 +831,8 @@ kvq_status launch_t(const AttnLaunch& a, cudaStream_t stream) {
   p.n_q = a.n_q;
   p.n_r = a.n_r;
   p.scale_log2 = a.scale * 1.4426950408889634f;
-  p.alpha_coef = a.corr ? -(a.scale / 24.0f) : 0.0f;
+  p.alpha_coef = a.corr ? -(a.scale / 24.0f) * 256.0f : 0.0f;
   p.corr = a.corr;
-  p.precise_query = a.precise_query;
   p.mass_only = a.mass_only;
   p.out = a.out;
   p.p_s = a.p_s;
@@ -653,16 +840,22 @@ kvq_status launch_t(const AttnLaunch& a, cudaStream_t stream) {
   for (int i = 0; i < 4; ++i) p.sign_bits[i] = a.sign_bits[i];
   p.inv_sqrt_d = (float)(1.0 / sqrt((double)D));
   p.wait_limit_ns = a.wait_limit_ns;
-  dim3 grid((a.n_q + kBlockM - 1) / kBlockM, a.bh);
-  kern<<<grid, kThreads, L::kAlloc, stream>>>(mq, mqlo, mqo, mk, mv, p);
+  dim3 grid((a.n_q + kBlockM * NQ - 1) / (kBlockM * NQ), a.bh);
+  kern<<<grid, C::kThreads, C::kAlloc, stream>>>(mq, mqlo, mqo, mk, mv, p);
   return cudaGetLastError() == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
+}
+
+template <int D, int BITS, int GROUP>
+kvq_status launch_mode(const AttnLaunch& a, cudaStream_t stream) {
+  if (a.precise_query) return launch_t<D, BITS, GROUP, 1, true>(a, stream);
+  return launch_t<D, BITS, GROUP, 2, false>(a, stream);
 }
 
 }  // namespace
 
 kvq_status launch_attention(const AttnLaunch& a, int d, int bits, int group, cudaStream_t stream) {
 #define KVQ_A(D_, B_, G_) \
-  if (d == D_ && bits == B_ && group == G_) return launch_t<D_, B_, G_>(a, stream);
+  if (d == D_ && bits == B_ && group == G_) return launch_mode<D_, B_, G_>(a, stream);
   KVQ_A(64, 2, 32)
   KVQ_A(64, 4, 32)
   KVQ_A(64, 2, 64)
