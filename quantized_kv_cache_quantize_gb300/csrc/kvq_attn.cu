@@ -100,7 +100,6 @@ struct Cfg {
   static constexpr int kSoftmaxWarps = 4 * NQ;
   static constexpr int kDequantWarp = kSoftmaxWarps;
   static constexpr int kMmaWarp = kSoftmaxWarps + 4;
-  static constexpr int kTmaWarp = kSoftmaxWarps + 5;
   static constexpr int kThreads = (kSoftmaxWarps + 6) * 32;
   // tensor memory columns: S buffers, then the O tiles
   static constexpr int kTO = NQ * kSBuf * 128;
@@ -295,7 +294,9 @@ __global__ void __launch_bounds__(Cfg<D, NQ, PRECISE>::kThreads, 1)
     const int q = warp >> 2;
     const int r = tid - q * 128;                      // row within the query tile
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    bool ok = wait_bar(BAR(kBarQ), 0, lim, abort);
+    // every decision guarding a tcgen05 access is made warp-uniform: the
+    // tensor-memory loads and stores are warp-collective
+    bool ok = __all_sync(0xffffffffu, wait_bar(BAR(kBarQ), 0, lim, abort));
     {
       // group norms ||q'_g||^2 and group sums of the rotated query row
       float nrm[G], qsum[G];
@@ -345,7 +346,10 @@ __global__ void __launch_bounds__(Cfg<D, NQ, PRECISE>::kThreads, 1)
       const int b = NQ == 2 ? 0 : (j & 1);
       const uint32_t t_s = tmem + (q * C::kSBuf + b) * 128 + lane_off;
       const uint32_t par = NQ == 2 ? (j & 1) : ((j >> 1) & 1);
-      if (!wait_bar(BAR(kBarS + q * C::kSBuf + b), par, lim, abort)) { ok = false; break; }
+      if (!__all_sync(0xffffffffu, wait_bar(BAR(kBarS + q * C::kSBuf + b), par, lim, abort))) {
+        ok = false;
+        break;
+      }
       ptx::tc_fence_after();
       const int nv = j < n_ct ? min(kBlockN, p.n_s - j * kBlockN)
                               : min(kBlockN, p.n_r - (j - n_ct) * kBlockN);
@@ -370,7 +374,10 @@ __global__ void __launch_bounds__(Cfg<D, NQ, PRECISE>::kThreads, 1)
       if (NQ == 1 && j > 0) {
         // one-tile schedule: QK of this tile was issued before the previous
         // PV; O and the P-ready phases wait for that PV
-        if (!wait_bar(BAR(kBarOStep), (j - 1) & 1, lim, abort)) { ok = false; break; }
+        if (!__all_sync(0xffffffffu, wait_bar(BAR(kBarOStep), (j - 1) & 1, lim, abort))) {
+          ok = false;
+          break;
+        }
         ptx::tc_fence_after();
       }
       if (__any_sync(0xffffffffu, need)) {
@@ -419,7 +426,8 @@ __global__ void __launch_bounds__(Cfg<D, NQ, PRECISE>::kThreads, 1)
     // epilogue: O / (l_S + l_R), inverse rotation, BF16 store; masses
     const int row = q0 + q * kBlockM + r;
     if (ok) ok = wait_bar(BAR(kBarODone + q), 0, lim, abort);
-    if (ok && !*abort) {
+    ok = __all_sync(0xffffffffu, ok && !*abort);
+    if (ok) {
       ptx::tc_fence_after();
       const float inv = 1.0f / (l_s + l_r);
       if (!mass_only) {
@@ -456,39 +464,41 @@ __global__ void __launch_bounds__(Cfg<D, NQ, PRECISE>::kThreads, 1)
           }
         }
         ptx::tmem_st_wait();
-        if (row < p.n_q) {
-          uint16_t* dst = p.out + (static_cast<size_t>(bh) * p.n_q + row) * D;
-          auto store8 = [&](int ch0, const float* v8) {
-            const uint32_t sw = p.sign_bits[ch0 >> 5];
-            float v[8];
+        // the tensor-memory loads are warp-collective: every lane takes part,
+        // only the stores depend on the row being inside the chunk
+        const bool store = row < p.n_q;
+        uint16_t* dst = p.out + (static_cast<size_t>(bh) * p.n_q + (store ? row : 0)) * D;
 #pragma unroll
-            for (int e = 0; e < 8; ++e)
-              v[e] = v8[e] * (((sw >> ((ch0 + e) & 31)) & 1u) ? -p.inv_sqrt_d : p.inv_sqrt_d);
-            *reinterpret_cast<uint4*>(dst + ch0) =
-                make_uint4(pack_bf2(v[0], v[1]), pack_bf2(v[2], v[3]), pack_bf2(v[4], v[5]),
-                           pack_bf2(v[6], v[7]));
-          };
+        for (int c = 0; c < 2; ++c) {
+          uint32_t a[32], bq[32];
+          ptx::tmem_ld32(t_o + 32 * c, a);
+          if (D == 128) ptx::tmem_ld32(t_o + 64 + 32 * c, bq);
 #pragma unroll
-          for (int c = 0; c < 2; ++c) {
-            uint32_t a[32], bq[32];
-            ptx::tmem_ld32(t_o + 32 * c, a);
-            float lo[32], hi[32];
-            if (D == 128) {
-              ptx::tmem_ld32(t_o + 64 + 32 * c, bq);
+          for (int part = 0; part < (D == 128 ? 2 : 1); ++part) {
+            const int ch_base = 64 * part + 32 * c;
+            const uint32_t sw = p.sign_bits[ch_base >> 5];
+            uint32_t pk[16];
 #pragma unroll
-              for (int k = 0; k < 32; ++k) {
-                lo[k] = __uint_as_float(a[k]) + __uint_as_float(bq[k]);
-                hi[k] = __uint_as_float(a[k]) - __uint_as_float(bq[k]);
+            for (int k = 0; k < 32; k += 2) {
+              float v0, v1;
+              if (D == 128) {
+                v0 = part == 0 ? __uint_as_float(a[k]) + __uint_as_float(bq[k])
+                               : __uint_as_float(a[k]) - __uint_as_float(bq[k]);
+                v1 = part == 0 ? __uint_as_float(a[k + 1]) + __uint_as_float(bq[k + 1])
+                               : __uint_as_float(a[k + 1]) - __uint_as_float(bq[k + 1]);
+              } else {
+                v0 = __uint_as_float(a[k]);
+                v1 = __uint_as_float(a[k + 1]);
               }
-            } else {
-#pragma unroll
-              for (int k = 0; k < 32; ++k) lo[k] = __uint_as_float(a[k]);
+              v0 *= ((sw >> k) & 1u) ? -p.inv_sqrt_d : p.inv_sqrt_d;
+              v1 *= ((sw >> (k + 1)) & 1u) ? -p.inv_sqrt_d : p.inv_sqrt_d;
+              pk[k >> 1] = pack_bf2(v0, v1);
             }
+            if (store) {
 #pragma unroll
-            for (int e = 0; e < 4; ++e) store8(32 * c + 8 * e, lo + 8 * e);
-            if (D == 128) {
-#pragma unroll
-              for (int e = 0; e < 4; ++e) store8(64 + 32 * c + 8 * e, hi + 8 * e);
+              for (int e = 0; e < 4; ++e)
+                *reinterpret_cast<uint4*>(dst + ch_base + 8 * e) =
+                    make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
             }
           }
         }
@@ -692,17 +702,22 @@ __global__ void __launch_bounds__(Cfg<D, NQ, PRECISE>::kThreads, 1)
     // ============================== TMA ==============================
     if (lane == 0) {
       const uint32_t s_base = ptx::smem_u32(smem);
+      // a query tile starting past the last row is loaded from the last row
+      // instead (its rows are computed but never stored): no box lies wholly
+      // outside the tensor
+      auto q_row = [&](int q) { return min(q0 + q * kBlockM, p.n_q - 1); };
       ptx::mbar_expect_tx(BAR(kBarQ), NQ * (PRECISE ? 2 : 1) * NKH * kHalf);
       for (int q = 0; q < NQ; ++q) {
         for (int h = 0; h < NKH; ++h) {
-          ptx::tma_load_3d(s_base + C::kQ + q * C::kTile + h * kHalf, &tm_q, 64 * h,
-                           q0 + q * kBlockM, bh, BAR(kBarQ));
+          ptx::tma_load_3d(s_base + C::kQ + q * C::kTile + h * kHalf, &tm_q, 64 * h, q_row(q), bh,
+                           BAR(kBarQ));
           if (PRECISE)
             ptx::tma_load_3d(s_base + C::kQ + (NQ + q) * C::kTile + h * kHalf, &tm_qlo, 64 * h,
-                             q0 + q * kBlockM, bh, BAR(kBarQ));
+                             q_row(q), bh, BAR(kBarQ));
         }
       }
       int last = -1;
+      bool q_orig_issued = false;
       for (int j = n_ct; j < n_t; ++j) {
         if (*abort) break;
         const int s = j & 1;
@@ -714,7 +729,8 @@ __global__ void __launch_bounds__(Cfg<D, NQ, PRECISE>::kThreads, 1)
           for (int q = 0; q < NQ; ++q)
             for (int h = 0; h < NKH; ++h)
               ptx::tma_load_3d(s_base + C::kQ + q * C::kTile + h * kHalf, &tm_qo, 64 * h,
-                               q0 + q * kBlockM, bh, BAR(kBarQ));
+                               q_row(q), bh, BAR(kBarQ));
+          q_orig_issued = true;
         }
         if (j >= 2 && !wait_bar(BAR(kBarEmpty + s), ((j >> 1) - 1) & 1, lim, abort)) break;
         const int key0 = (j - n_ct) * kBlockN;
@@ -729,11 +745,14 @@ __global__ void __launch_bounds__(Cfg<D, NQ, PRECISE>::kThreads, 1)
         last = j;
       }
       // on an abort, let the copies already issued land before the CTA exits
-      if (*abort && last >= 0) {
-        const int s = last & 1;
-        const int use = (last >> 1) - ((n_ct + 1 - s) >> 1);
+      if (*abort) {
         int ignore = 0;
-        wait_bar(BAR(kBarFullTma + s), use & 1, lim, &ignore);
+        wait_bar(BAR(kBarQ), q_orig_issued ? 1 : 0, lim, &ignore);
+        if (last >= 0) {
+          const int s = last & 1;
+          const int use = (last >> 1) - ((n_ct + 1 - s) >> 1);
+          wait_bar(BAR(kBarFullTma + s), use & 1, lim, &ignore);
+        }
       }
     }
     __syncwarp();
