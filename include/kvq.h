@@ -38,7 +38,8 @@ typedef enum {
   KVQ_ERR_CAPACITY = 3,     /* append refused by the window rules           */
   KVQ_ERR_CUDA = 4,         /* a CUDA runtime/driver call failed            */
   KVQ_ERR_TIMEOUT = 5,      /* a kernel's bounded wait ran out              */
-  KVQ_ERR_ALIGNMENT = 6     /* a pointer is not 16-byte aligned             */
+  KVQ_ERR_ALIGNMENT = 6,    /* a pointer is not 16-byte aligned             */
+  KVQ_ERR_TOO_LARGE = 7     /* needs more than the built-in scratch holds   */
 } kvq_status;
 
 /* Correction applied to cached-key scores before the softmax. */
@@ -208,6 +209,36 @@ kvq_status kvq_set_wait_limit_ns(uint64_t limit_ns);
  * error path can be exercised without faulting or hanging a GPU.
  */
 kvq_status kvq_selftest_wait_timeout(uint64_t limit_ns, void *stream);
+
+/*
+ * kvq_attention_corrected without a workspace argument, for callers that
+ * cannot allocate device memory when they call: for instance a plugin whose
+ * host process owns every byte of the device through its own pool, a
+ * real-time loop that may not take the allocator's locks or its implicit
+ * synchronization, or a deployment whose device-memory budget is fixed when
+ * the library is loaded.  No counterpart in the paper.
+ *
+ * Same arguments, meaning and results as kvq_attention_corrected, minus the
+ * workspace.  The scratch space comes from one fixed device buffer of
+ * KVQ_NOALLOC_SCRATCH_BYTES (32 MiB) inside the library; every device that
+ * loads the library holds it until the process exits.  Problems that need
+ * more (kvq_workspace_bytes(cache, n_q, n_r) > KVQ_NOALLOC_SCRATCH_BYTES)
+ * return KVQ_ERR_TOO_LARGE before anything is launched.
+ * - The first call on a device looks up the buffer's device address (once per
+ *   device, with that device current); make that first call before any
+ *   stream capture.
+ * - All calls share the one buffer and it keeps the previous call's contents
+ *   (nothing in it needs to start at zero: each call overwrites what it
+ *   reads).  Calls whose kernels overlap on the GPU -- on different streams,
+ *   or from different host threads -- race on it; serialize them.
+ * - Allocates nothing: no cudaMalloc, no cudaFree, no allocating library call.
+ */
+#define KVQ_NOALLOC_SCRATCH_BYTES (32u << 20)
+kvq_status kvq_attention_corrected_noalloc(const kvq_cache *cache, const uint16_t *q,
+                                           const uint16_t *k_cur, const uint16_t *v_cur,
+                                           int32_t n_q, int32_t n_r, float scale,
+                                           int32_t corr, int32_t flags, uint16_t *out,
+                                           float *p_s, float *p_r, void *stream);
 
 /*
  * Instrumentation (no counterpart in the paper).  Between kvq_profile_begin

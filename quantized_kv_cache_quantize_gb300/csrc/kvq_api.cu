@@ -6,6 +6,7 @@
 #include <atomic>
 #include <cmath>
 #include <cstdint>
+#include <mutex>
 #include <vector>
 
 #include "kvq_internal.h"
@@ -191,6 +192,8 @@ const char* kvq_status_string(kvq_status s) {
     case KVQ_ERR_CUDA: return "CUDA call failed";
     case KVQ_ERR_TIMEOUT: return "bounded wait in a kernel ran out";
     case KVQ_ERR_ALIGNMENT: return "pointer not 16-byte aligned";
+    case KVQ_ERR_TOO_LARGE:
+      return "problem needs more scratch than kvq_attention_corrected_noalloc's built-in buffer";
   }
   return "unknown status";
 }
@@ -349,3 +352,51 @@ kvq_status kvq_profile_end(double ms_total[3], int32_t launches[3]) {
 }
 
 }  // extern "C"
+
+// ---- attention without a workspace argument ---------------------------------
+// Scratch of kvq_attention_corrected_noalloc: one fixed device buffer, present
+// on every device that loads the library until the process exits.  In host
+// code this name is only a host-side stand-in; the device address comes from
+// cudaGetSymbolAddress below.
+static __device__ __align__(256) uint8_t g_noalloc_scratch[KVQ_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+std::mutex g_noalloc_mutex;
+void* g_noalloc_ptr[kMaxDevices] = {nullptr};
+
+// Device address of the scratch buffer on the current device, looked up once
+// per device (with that device current).
+kvq_status noalloc_scratch(void** ptr) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return KVQ_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+  if (g_noalloc_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr)
+      return KVQ_ERR_CUDA;
+    g_noalloc_ptr[dev] = p;
+  }
+  *ptr = g_noalloc_ptr[dev];
+  return KVQ_OK;
+}
+
+}  // namespace
+
+extern "C" kvq_status kvq_attention_corrected_noalloc(const kvq_cache* cache, const uint16_t* q,
+                                                      const uint16_t* k_cur, const uint16_t* v_cur,
+                                                      int32_t n_q, int32_t n_r, float scale,
+                                                      int32_t corr, int32_t flags, uint16_t* out,
+                                                      float* p_s, float* p_r, void* stream) {
+  kvq::Geometry g;
+  const kvq_status st = check_geometry(cache, &g);
+  if (st != KVQ_OK) return st;
+  if (n_q < 0 || n_r < 0) return KVQ_ERR_INVALID_ARG;
+  if (carve(nullptr, g, n_q, n_r).bytes > (size_t)KVQ_NOALLOC_SCRATCH_BYTES) return KVQ_ERR_TOO_LARGE;
+  void* scratch = nullptr;
+  const kvq_status sst = noalloc_scratch(&scratch);
+  if (sst != KVQ_OK) return sst;
+  return attention_common(cache, q, k_cur, v_cur, n_q, n_r, scale, corr, flags, scratch,
+                          (size_t)KVQ_NOALLOC_SCRATCH_BYTES, out, p_s, p_r, false, stream);
+}

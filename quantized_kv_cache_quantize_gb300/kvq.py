@@ -21,6 +21,8 @@ KVQ_ERR_CAPACITY = 3
 KVQ_ERR_CUDA = 4
 KVQ_ERR_TIMEOUT = 5
 KVQ_ERR_ALIGNMENT = 6
+KVQ_ERR_TOO_LARGE = 7
+NOALLOC_SCRATCH_BYTES = 32 << 20
 
 CORR_NONE = 0
 CORR_TAYLOR = 1
@@ -64,6 +66,10 @@ _SIGNATURES = {
     "kvq_last_device_status": (ctypes.c_int, [_P]),
     "kvq_set_wait_limit_ns": (ctypes.c_int, [ctypes.c_uint64]),
     "kvq_selftest_wait_timeout": (ctypes.c_int, [ctypes.c_uint64, _P]),
+    "kvq_attention_corrected_noalloc": (ctypes.c_int, [_P, _P, _P, _P, ctypes.c_int32,
+                                                       ctypes.c_int32, ctypes.c_float,
+                                                       ctypes.c_int32, ctypes.c_int32, _P, _P, _P,
+                                                       _P]),
     "kvq_profile_begin": (ctypes.c_int, []),
     "kvq_profile_end": (ctypes.c_int, [_P, _P]),
 }
@@ -205,6 +211,31 @@ def attention_corrected(cache: KVCache, q, k_cur, v_cur, scale: float | None = N
         ctypes.byref(cache.struct), _ptr(q), _ptr(k_cur), _ptr(v_cur), n_q, n_r,
         ctypes.c_float(scale), corr, flags, _ptr(workspace), workspace.numel(), _ptr(out),
         _ptr(ps), _ptr(pr), _stream(stream)), "kvq_attention_corrected")
+    return (out, ps, pr) if with_mass else out
+
+
+def attention_corrected_noalloc(cache: KVCache, q, k_cur, v_cur, scale: float | None = None,
+                                corr: int = CORR_TAYLOR, out=None, with_mass: bool = False,
+                                stream=None, flags: int = 0):
+    """kvq_attention_corrected_noalloc: like attention_corrected, with the
+    library's built-in scratch buffer instead of a workspace (for callers
+    that cannot allocate device memory when they call).  Outputs are still
+    the caller's (allocated here by torch when not given)."""
+    _bf16_dev(q, "q")
+    _bf16_dev(k_cur, "k_cur")
+    _bf16_dev(v_cur, "v_cur")
+    n_q, n_r = q.shape[-2], k_cur.shape[-2]
+    scale = 1.0 / math.sqrt(cache.head_dim) if scale is None else scale
+    if out is None:
+        out = torch.empty_like(q)
+    ps = pr = None
+    if with_mass:
+        ps = torch.empty(q.shape[:-1], dtype=torch.float32, device=q.device)
+        pr = torch.empty_like(ps)
+    _check(lib().kvq_attention_corrected_noalloc(
+        ctypes.byref(cache.struct), _ptr(q), _ptr(k_cur), _ptr(v_cur), n_q, n_r,
+        ctypes.c_float(scale), corr, flags, _ptr(out), _ptr(ps), _ptr(pr), _stream(stream)),
+        "kvq_attention_corrected_noalloc")
     return (out, ps, pr) if with_mass else out
 
 

@@ -146,3 +146,16 @@ def test_sign_bits_roundtrip():
     words = kvq.sign_bits(s)
     back = [(-1.0 if (words[c >> 5] >> (c & 31)) & 1 else 1.0) for c in range(128)]
     assert np.array_equal(back, s)
+
+
+def test_noalloc_rejects_problems_beyond_its_scratch(lib):
+    """The allocation-free entry point refuses, on the host, problems whose
+    scratch would not fit its built-in buffer."""
+    c = _cache(len=30, heads=64)
+    P = 0x10000
+    n = 4096   # 64 heads x 4096 rows x 128 x 2 B x 2 (hi, lo) > 32 MiB
+    assert lib.kvq_workspace_bytes(ctypes.byref(c), n, n) > kvq.NOALLOC_SCRATCH_BYTES
+    st = lib.kvq_attention_corrected_noalloc(ctypes.byref(c), P, P, P, n, n, 0.1, 1, 0, P, None,
+                                             None, None)
+    assert st == kvq.KVQ_ERR_TOO_LARGE
+    assert "scratch" in kvq.status_string(st)
