@@ -361,7 +361,8 @@ __global__ void __launch_bounds__(Cfg<D, NQ, PRECISE>::kThreads, 1)
         ptx::tmem_ld32(t_s + 32 * c, v);
         if (nv == kBlockN) {
 #pragma unroll
-          for (int k = 0; k < 32; ++k) mx = fmaxf(mx, __uint_as_float(v[k]));
+          for (int k = 0; k < 32; k += 2)
+            mx = ptx::max3(mx, __uint_as_float(v[k]), __uint_as_float(v[k + 1]));
         } else {
 #pragma unroll
           for (int k = 0; k < 32; ++k) mx = (32 * c + k < nv) ? fmaxf(mx, __uint_as_float(v[k])) : mx;
@@ -387,18 +388,28 @@ __global__ void __launch_bounds__(Cfg<D, NQ, PRECISE>::kThreads, 1)
         l_r *= alpha;
         m = m_new;
         if (j > 0 && !mass_only) {
+          const uint64_t a2 = ptx::f2_pack(alpha, alpha);
 #pragma unroll
           for (int c = 0; c < D / 32; ++c) {
             uint32_t v[32];
             ptx::tmem_ld32(t_o + 32 * c, v);
 #pragma unroll
-            for (int k = 0; k < 32; ++k) v[k] = __float_as_uint(__uint_as_float(v[k]) * alpha);
+            for (int k = 0; k < 32; k += 2) {
+              float lo, hi;
+              ptx::f2_unpack(ptx::f2_mul(ptx::f2_pack(__uint_as_float(v[k]), __uint_as_float(v[k + 1])), a2),
+                             lo, hi);
+              v[k] = __float_as_uint(lo);
+              v[k + 1] = __float_as_uint(hi);
+            }
             ptx::tmem_st32(t_o + 32 * c, v);
           }
         }
       }
-      // pass 2: exponentials, sums, P (FP16 pairs) into the S buffer
-      float sum = 0.f;
+      // pass 2: exponentials (special-function unit), sums, P (FP16 pairs)
+      // written back into the S buffer; pairs of scores in packed fp32 ops
+      const uint64_t sl2x2 = ptx::f2_pack(sl2, sl2);
+      const uint64_t negm2 = ptx::f2_pack(-m, -m);
+      uint64_t acc2 = ptx::f2_pack(0.f, 0.f);
 #pragma unroll
       for (int c = 0; c < kBlockN / 32; ++c) {
         uint32_t v[32];
@@ -406,17 +417,24 @@ __global__ void __launch_bounds__(Cfg<D, NQ, PRECISE>::kThreads, 1)
         uint32_t pk[16];
 #pragma unroll
         for (int k = 0; k < 16; ++k) {
-          float e0 = exp2f(fmaf(__uint_as_float(v[2 * k]), sl2, -m));
-          float e1 = exp2f(fmaf(__uint_as_float(v[2 * k + 1]), sl2, -m));
+          float x0, x1;
+          ptx::f2_unpack(ptx::f2_fma(ptx::f2_pack(__uint_as_float(v[2 * k]), __uint_as_float(v[2 * k + 1])),
+                                     sl2x2, negm2),
+                         x0, x1);
+          float e0 = ptx::ex2_approx(x0);
+          float e1 = ptx::ex2_approx(x1);
           if (nv != kBlockN) {
             e0 = (32 * c + 2 * k < nv) ? e0 : 0.f;
             e1 = (32 * c + 2 * k + 1 < nv) ? e1 : 0.f;
           }
-          sum += e0 + e1;
-          pk[k] = pack_h2(e0, e1);
+          acc2 = ptx::f2_add(acc2, ptx::f2_pack(e0, e1));
+          pk[k] = ptx::f16x2_rn(e0, e1);
         }
         if (!mass_only) ptx::tmem_st16(t_s + 16 * c, pk);
       }
+      float sum_lo, sum_hi;
+      ptx::f2_unpack(acc2, sum_lo, sum_hi);
+      const float sum = sum_lo + sum_hi;
       if (j < n_ct) l_s += sum; else l_r += sum;
       ptx::tmem_st_wait();
       ptx::tc_fence_before();
@@ -512,37 +530,44 @@ __global__ void __launch_bounds__(Cfg<D, NQ, PRECISE>::kThreads, 1)
     // =========================== dequant ===========================
     const int r = tid - C::kDequantWarp * 32;
     const size_t head_tok = static_cast<size_t>(bh) * p.cap;
-    for (int j = 0; j < n_ct; ++j) {
-      if (*abort) break;
-      const int s = j & 1;
-      const bool valid = j * kBlockN + r < p.n_s;
-      uint32_t kw[NW], ksz[G], vw[NW], vsz[G];
+    // packed words of key r of tile j (zeros past the end of the window)
+    auto load_key = [&](int j, uint32_t (&kw)[NW], uint32_t (&ksz)[G], uint32_t (&vw)[NW],
+                        uint32_t (&vsz)[G]) {
 #pragma unroll
       for (int i = 0; i < NW; ++i) kw[i] = vw[i] = 0u;
 #pragma unroll
       for (int g = 0; g < G; ++g) ksz[g] = vsz[g] = 0u;
-      if (valid) {
-        const size_t tok = head_tok + j * kBlockN + r;
-        const uint4* kc = reinterpret_cast<const uint4*>(p.k_codes + tok * CB);
+      if (j >= n_ct || j * kBlockN + r >= p.n_s) return;
+      const size_t tok = head_tok + j * kBlockN + r;
+      const uint4* kc = reinterpret_cast<const uint4*>(p.k_codes + tok * CB);
+#pragma unroll
+      for (int i = 0; i < NW / 4; ++i) {
+        const uint4 v = __ldg(kc + i);
+        kw[4 * i] = v.x; kw[4 * i + 1] = v.y; kw[4 * i + 2] = v.z; kw[4 * i + 3] = v.w;
+      }
+#pragma unroll
+      for (int g = 0; g < G; ++g) ksz[g] = __ldg(p.k_sz + tok * G + g);
+      if (!mass_only) {
+        const uint4* vc = reinterpret_cast<const uint4*>(p.v_codes + tok * CB);
 #pragma unroll
         for (int i = 0; i < NW / 4; ++i) {
-          const uint4 v = __ldg(kc + i);
-          kw[4 * i] = v.x; kw[4 * i + 1] = v.y; kw[4 * i + 2] = v.z; kw[4 * i + 3] = v.w;
+          const uint4 v = __ldg(vc + i);
+          vw[4 * i] = v.x; vw[4 * i + 1] = v.y; vw[4 * i + 2] = v.z; vw[4 * i + 3] = v.w;
         }
 #pragma unroll
-        for (int g = 0; g < G; ++g) ksz[g] = __ldg(p.k_sz + tok * G + g);
-        if (!mass_only) {
-          const uint4* vc = reinterpret_cast<const uint4*>(p.v_codes + tok * CB);
-#pragma unroll
-          for (int i = 0; i < NW / 4; ++i) {
-            const uint4 v = __ldg(vc + i);
-            vw[4 * i] = v.x; vw[4 * i + 1] = v.y; vw[4 * i + 2] = v.z; vw[4 * i + 3] = v.w;
-          }
-#pragma unroll
-          for (int g = 0; g < G; ++g) vsz[g] = __ldg(p.v_sz + tok * G + g);
-        }
+        for (int g = 0; g < G; ++g) vsz[g] = __ldg(p.v_sz + tok * G + g);
       }
+    };
+    uint32_t kw[NW], ksz[G], vw[NW], vsz[G];
+    load_key(0, kw, ksz, vw, vsz);
+    for (int j = 0; j < n_ct; ++j) {
+      if (*abort) break;
+      const int s = j & 1;
+      const bool valid = j * kBlockN + r < p.n_s;
       if (j >= 2 && !wait_bar(BAR(kBarEmpty + s), ((j >> 1) - 1) & 1, lim, abort)) break;
+      // the next tile's words are in flight while this one is converted
+      uint32_t nkw[NW], nksz[G], nvw[NW], nvsz[G];
+      load_key(j + 1, nkw, nksz, nvw, nvsz);
       uint8_t* st = smem + C::kStages + s * C::kStageBytes;
       float cb[16], cz[16];
 #pragma unroll
@@ -567,6 +592,10 @@ __global__ void __launch_bounds__(Cfg<D, NQ, PRECISE>::kThreads, 1)
       write_ext_row(st + 2 * C::kTile + kExt, r, cz);
       ptx::fence_proxy_async_smem();
       ptx::mbar_arrive(BAR(kBarFullDq + s));
+#pragma unroll
+      for (int i = 0; i < NW; ++i) { kw[i] = nkw[i]; vw[i] = nvw[i]; }
+#pragma unroll
+      for (int g = 0; g < G; ++g) { ksz[g] = nksz[g]; vsz[g] = nvsz[g]; }
     }
   } else if (warp == C::kMmaWarp) {
     // ============================= MMA =============================
