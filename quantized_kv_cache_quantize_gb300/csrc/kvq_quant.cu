@@ -17,6 +17,7 @@
 
 #include "kvq_fwht.cuh"
 #include "kvq_internal.h"
+#include "kvq_sm100.cuh"
 
 namespace kvq {
 
@@ -39,75 +40,98 @@ __device__ __forceinline__ uint32_t sign_word_for(const uint32_t (&sb)[4], int t
   return i == 0 ? sb[0] : i == 1 ? sb[1] : i == 2 ? sb[2] : sb[3];
 }
 
-// rint(fl(x / delta)) (IEEE quotient, ties to even).  q = fl(x * fl(1/delta))
-// is within 2^-22 |q| of fl(x / delta), so unless q lies within 2^-20
-// max(1, |q|) of a half-integer both round to the same integer; near a
-// half-integer (and for non-finite q) the correctly rounded division decides.
-__device__ __forceinline__ float rint_div(float x, float delta, float rcp) {
-  const float q = __fmul_rn(x, rcp);
+// Sign flips of the randomized rotation in the BF16 pair domain: word i of
+// a row holds channels 2i (low half) and 2i + 1 (high half); XOR with m[i]
+// flips their sign bits (bit 15, bit 31).
+struct PairSigns {
+  uint32_t m[64];
+};
+
+constexpr int kRowThreads = 128;
+
+// rint of q = fl(x * fl(1/delta)), folding |q - rint(q)| and |q| into running
+// maxima.  q is within 2^-22 |q| of fl(x / delta), so when every q of a group
+// stays more than 2^-20 max(1, |q|) away from a half-integer, rint(q) equals
+// rint(fl(x / delta)) (IEEE quotient, ties to even) for all of them; otherwise
+// (or for non-finite q) the group takes the correctly rounded division.
+__device__ __forceinline__ float rint_q(float q, float& max_frac, float& max_q) {
   const float n = rintf(q);
-  const float margin = __fsub_rn(0.5f, fabsf(__fsub_rn(q, n)));
-  if (!(margin > 0x1p-20f * fmaxf(1.0f, fabsf(q)))) return rintf(__fdiv_rn(x, delta));
+  max_frac = fmaxf(max_frac, fabsf(__fsub_rn(q, n)));
+  max_q = fmaxf(max_q, fabsf(q));
   return n;
 }
 
+// One thread per row (one token's K or V row of one head): the whole row in
+// registers, so the rotation needs no data exchange between threads.  Per
+// row: d/8 16-byte loads, fp32 butterflies in the order h = 1, 2, ..., d/2
+// (packed fp32 pairs from h = 2 on: each lane is the same correctly rounded
+// add or subtract), per-group min/max, Eq. (1) codes, packed 16-byte stores.
 template <int D, int BITS, int GROUP>
-__global__ void __launch_bounds__(kThreads) quantize_append_kernel(const QuantArgs a) {
-  constexpr int LPR = D / 8;                 // lanes per row
-  constexpr int RPW = 32 / LPR;              // rows per warp
-  constexpr int G = D / GROUP;               // groups per row
-  constexpr int LPG = GROUP / 8;             // lanes per group
-  constexpr int W = D * BITS / 32;           // 32-bit code words per row
-  constexpr int NCH = W / 4;                 // 16-byte code chunks per row
-  constexpr int LPC = LPR / NCH;             // lanes per chunk
+__global__ void __launch_bounds__(kRowThreads) quantize_rows_kernel(const QuantArgs a,
+                                                                    const PairSigns sg) {
+  constexpr int G = D / GROUP;
   constexpr int CODE_BYTES = D * BITS / 8;
-  static_assert(NCH >= 1 && LPC >= 1, "layout");
+  constexpr int PER_WORD = 32 / BITS;
   const float qmax = float((1 << BITS) - 1);
 
-  const int lane = threadIdx.x & 31;
-  const int t = lane % LPR;                  // lane within the row group
-  const int rbase = lane - t;
   const unsigned per_kv = (unsigned)a.bh * (unsigned)a.n_new;   // < 2^31 (host check)
-  const unsigned rows_total = 2u * per_kv;
-  const unsigned warp0 = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  const unsigned stride = ((gridDim.x * blockDim.x) >> 5) * RPW;
-  uint32_t smask[8];
-  sign_masks(sign_word_for(a.sign_bits, t), t, smask);
+  const unsigned r = blockIdx.x * kRowThreads + threadIdx.x;
+  if (r >= 2u * per_kv) return;
+  const bool is_v = r >= per_kv;
+  const unsigned rk = is_v ? r - per_kv : r;
+  const unsigned bh = rk / (unsigned)a.n_new;
+  const unsigned tok = rk - bh * (unsigned)a.n_new;
 
-  auto load_row = [&](unsigned r) {
-    uint4 raw = make_uint4(0u, 0u, 0u, 0u);
-    if (r < rows_total) {
-      const bool is_v = r >= per_kv;
-      const unsigned rk = is_v ? r - per_kv : r;
-      raw = __ldg(reinterpret_cast<const uint4*>((is_v ? a.v_new : a.k_new) + (size_t)rk * D + 8 * t));
+  const uint4* src = reinterpret_cast<const uint4*>((is_v ? a.v_new : a.k_new) + (size_t)rk * D);
+  float x[D];
+#pragma unroll
+  for (int i = 0; i < D / 8; ++i) {
+    const uint4 raw = __ldg(src + i);
+    const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const uint32_t ws = w[k] ^ sg.m[4 * i + k];
+      x[8 * i + 2 * k] = __uint_as_float(ws << 16);
+      x[8 * i + 2 * k + 1] = __uint_as_float(ws & 0xFFFF0000u);
     }
-    return raw;
-  };
-
-  unsigned r = warp0 * RPW + lane / LPR;
-  uint4 raw = load_row(r);
-  for (unsigned r0 = warp0 * RPW; r0 < rows_total; r0 += stride, r += stride) {
-    const uint4 next = load_row(r + stride);   // keep the next row's load in flight
-    const bool valid = r < rows_total;
-    const bool is_v = r >= per_kv;
-    const unsigned rk = is_v ? r - per_kv : r;
-    const unsigned bh = rk / (unsigned)a.n_new;
-    const unsigned tok = rk - bh * (unsigned)a.n_new;
-
-    float x[8];
-    load8_masked(raw, smask, x);
-    raw = next;
-    fwht_row<LPR>(x, t);
+  }
+  // butterflies: h = 1 on scalars, then packed pairs (x_i, x_i+1)
 #pragma unroll
-    for (int e = 0; e < 8; ++e) x[e] = __fmul_rn(x[e], a.inv_sqrt_d);
-
-    // group min / max (exact operations: order does not matter)
-    float mn = fminf(fminf(fminf(x[0], x[1]), fminf(x[2], x[3])), fminf(fminf(x[4], x[5]), fminf(x[6], x[7])));
-    float mx = fmaxf(fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3])), fmaxf(fmaxf(x[4], x[5]), fmaxf(x[6], x[7])));
+  for (int i = 0; i < D; i += 2) {
+    const float u = x[i], v = x[i + 1];
+    x[i] = __fadd_rn(u, v);
+    x[i + 1] = __fsub_rn(u, v);
+  }
 #pragma unroll
-    for (int dl = 1; dl < LPG; dl <<= 1) {
-      mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, dl));
-      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, dl));
+  for (int h = 2; h < D; h <<= 1) {
+#pragma unroll
+    for (int i = 0; i < D; i += 2) {
+      if ((i & h) == 0) {
+        const uint64_t A = ptx::f2_pack(x[i], x[i + 1]);
+        const uint64_t B = ptx::f2_pack(x[i + h], x[i + h + 1]);
+        ptx::f2_unpack(ptx::f2_add(A, B), x[i], x[i + 1]);
+        ptx::f2_unpack(ptx::f2_sub(A, B), x[i + h], x[i + h + 1]);
+      }
+    }
+  }
+  {
+    const uint64_t s2 = ptx::f2_pack(a.inv_sqrt_d, a.inv_sqrt_d);
+#pragma unroll
+    for (int i = 0; i < D; i += 2) ptx::f2_unpack(ptx::f2_mul(ptx::f2_pack(x[i], x[i + 1]), s2), x[i], x[i + 1]);
+  }
+
+  uint32_t words[D * BITS / 32];
+#pragma unroll
+  for (int i = 0; i < D * BITS / 32; ++i) words[i] = 0u;
+  uint32_t rec[G];
+#pragma unroll
+  for (int g = 0; g < G; ++g) {
+    float mn = x[GROUP * g], mx = x[GROUP * g];
+#pragma unroll
+    for (int c = 1; c < GROUP; c += 2) {
+      const float u = x[GROUP * g + c], v = c + 1 < GROUP ? x[GROUP * g + c + 1] : u;
+      mn = fminf(mn, fminf(u, v));
+      mx = fmaxf(mx, fmaxf(u, v));
     }
     // Eq. (1): step covering [min, max], integer zero point, both stored BF16
     uint32_t dbits = bf16_bits_rn(__fdiv_rn(__fsub_rn(mx, mn), qmax));
@@ -119,50 +143,50 @@ __global__ void __launch_bounds__(kThreads) quantize_append_kernel(const QuantAr
     const float rcp = __frcp_rn(delta);
     const uint32_t zbits = bf16_bits_rn(__fadd_rn(rintf(__fdiv_rn(-mn, delta)), 0.0f));
     const float zero = bf16_value(zbits);
+    rec[g] = dbits | (zbits << 16);
 
-    uint32_t word = 0;
+    // codes: fast route for the whole group, exact division when any
+    // element's quotient came within 2^-20 max(1, |q|) of a half-integer
+    float n[GROUP];
+    float max_frac = 0.f, max_q = 0.f;
+    {
+      const uint64_t r2 = ptx::f2_pack(rcp, rcp);
 #pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      float c = __fadd_rn(rint_div(x[e], delta, rcp), zero);
-      c = fminf(fmaxf(c, 0.0f), qmax);
-      const uint32_t code = (uint32_t)__float2int_rn(c);
-      if (BITS == 2) {
-        word |= code << (8 * (t & 1) + 2 * (e >> 1) + 16 * (e & 1));
-      } else {
-        word |= code << (4 * (e >> 1) + 16 * (e & 1));
+      for (int c = 0; c < GROUP; c += 2) {
+        float q0, q1;
+        ptx::f2_unpack(ptx::f2_mul(ptx::f2_pack(x[GROUP * g + c], x[GROUP * g + c + 1]), r2), q0, q1);
+        n[c] = rint_q(q0, max_frac, max_q);
+        n[c + 1] = rint_q(q1, max_frac, max_q);
       }
     }
-    if (BITS == 2) word |= __shfl_xor_sync(0xffffffffu, word, 1);
-
-    // 16-byte code chunks: chunk j = words 4j .. 4j+3
-    const int j = t / LPC;
-    const int wstride = (BITS == 2) ? (LPC / 4) : 1;
-    uint4 chunk;
-    chunk.x = shfl_idx(word, rbase + LPC * j + 0 * wstride);
-    chunk.y = shfl_idx(word, rbase + LPC * j + 1 * wstride);
-    chunk.z = shfl_idx(word, rbase + LPC * j + 2 * wstride);
-    chunk.w = shfl_idx(word, rbase + LPC * j + 3 * wstride);
-    const size_t dst_tok = (size_t)bh * a.cap + a.first + tok;
-    if (valid && (t % LPC) == 0) {
-      uint8_t* dst = (is_v ? a.v_codes : a.k_codes) + dst_tok * CODE_BYTES + 16 * j;
-      *reinterpret_cast<uint4*>(dst) = chunk;
-    }
-
-    // (step, zero) record of the token: G words gathered into lane t == 0
-    const uint32_t szw = dbits | (zbits << 16);
-    uint32_t rec[4] = {0u, 0u, 0u, 0u};
+    if (!(__fsub_rn(0.5f, max_frac) > 0x1p-20f * fmaxf(1.0f, max_q))) {
 #pragma unroll
-    for (int gi = 0; gi < G; ++gi) rec[gi] = shfl_idx(szw, rbase + gi * LPG);
-    if (valid && t == 0) {
-      uint32_t* dst = (is_v ? a.v_sz : a.k_sz) + dst_tok * G;
-      if (G == 4) {
-        *reinterpret_cast<uint4*>(dst) = make_uint4(rec[0], rec[1], rec[2], rec[3]);
-      } else if (G == 2) {
-        *reinterpret_cast<uint2*>(dst) = make_uint2(rec[0], rec[1]);
-      } else {
-        dst[0] = rec[0];
-      }
+      for (int c = 0; c < GROUP; ++c) n[c] = rintf(__fdiv_rn(x[GROUP * g + c], delta));
     }
+#pragma unroll
+    for (int c = 0; c < GROUP; ++c) {
+      float t = __fadd_rn(n[c], zero);
+      t = fminf(fmaxf(t, 0.0f), qmax);
+      const uint32_t code = (uint32_t)__float2int_rn(t);
+      // channel ch = 16w + 2k + h (INT2) / 8w + 2k + h (INT4) -> bits BITS*k + 16h
+      const int ch = GROUP * g + c;
+      const int w = ch / PER_WORD, k = (ch % PER_WORD) >> 1, hh = ch & 1;
+      words[w] |= code << (BITS * k + 16 * hh);
+    }
+  }
+
+  const size_t dst_tok = (size_t)bh * a.cap + a.first + tok;
+  uint4* dc = reinterpret_cast<uint4*>((is_v ? a.v_codes : a.k_codes) + dst_tok * CODE_BYTES);
+#pragma unroll
+  for (int i = 0; i < CODE_BYTES / 16; ++i)
+    dc[i] = make_uint4(words[4 * i], words[4 * i + 1], words[4 * i + 2], words[4 * i + 3]);
+  uint32_t* ds = (is_v ? a.v_sz : a.k_sz) + dst_tok * G;
+  if (G == 4) {
+    *reinterpret_cast<uint4*>(ds) = make_uint4(rec[0], rec[1 % G], rec[2 % G], rec[3 % G]);
+  } else if (G == 2) {
+    *reinterpret_cast<uint2*>(ds) = make_uint2(rec[0], rec[1 % G]);
+  } else {
+    ds[0] = rec[0];
   }
 }
 
@@ -240,19 +264,16 @@ long long grid_for_rows(long long rows, int rows_per_block) {
 
 template <int D, int BITS, int GROUP>
 cudaError_t launch_q(const QuantArgs& a, cudaStream_t s) {
-  static int resident = 0;
-  if (resident == 0) {
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-            &resident, quantize_append_kernel<D, BITS, GROUP>, kThreads, 0) != cudaSuccess ||
-        resident < 1)
-      resident = 1;
+  PairSigns sg;
+  for (int i = 0; i < 64; ++i) {
+    const int c0 = 2 * i, c1 = 2 * i + 1;
+    const uint32_t s0 = c0 < D ? (a.sign_bits[c0 >> 5] >> (c0 & 31)) & 1u : 0u;
+    const uint32_t s1 = c1 < D ? (a.sign_bits[c1 >> 5] >> (c1 & 31)) & 1u : 0u;
+    sg.m[i] = (s0 << 15) | (s1 << 31);
   }
   const long long rows = 2LL * a.bh * a.n_new;
-  const int rows_per_block = (kThreads / 32) * (32 / (D / 8));
-  long long blocks = (rows + rows_per_block - 1) / rows_per_block;
-  const long long cap = (long long)sm_count() * resident;
-  if (blocks > cap) blocks = cap;
-  quantize_append_kernel<D, BITS, GROUP><<<(unsigned)blocks, kThreads, 0, s>>>(a);
+  const unsigned blocks = (unsigned)((rows + kRowThreads - 1) / kRowThreads);
+  quantize_rows_kernel<D, BITS, GROUP><<<blocks, kRowThreads, 0, s>>>(a, sg);
   return cudaGetLastError();
 }
 
