@@ -353,20 +353,25 @@ __global__ void __launch_bounds__(Cfg<D, NQ, PRECISE>::kThreads, 1)
       ptx::tc_fence_after();
       const int nv = j < n_ct ? min(kBlockN, p.n_s - j * kBlockN)
                               : min(kBlockN, p.n_r - (j - n_ct) * kBlockN);
-      // pass 1: row max of the tile
-      float mx = -INFINITY;
+      // pass 1: row max of the tile (four independent max chains)
+      float mx;
+      {
+        float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-      for (int c = 0; c < kBlockN / 32; ++c) {
-        uint32_t v[32];
-        ptx::tmem_ld32(t_s + 32 * c, v);
-        if (nv == kBlockN) {
+        for (int c = 0; c < kBlockN / 32; ++c) {
+          uint32_t v[32];
+          ptx::tmem_ld32(t_s + 32 * c, v);
+          if (nv == kBlockN) {
 #pragma unroll
-          for (int k = 0; k < 32; k += 2)
-            mx = ptx::max3(mx, __uint_as_float(v[k]), __uint_as_float(v[k + 1]));
-        } else {
+            for (int k = 0; k < 32; k += 2)
+              m4[(k >> 1) & 3] = ptx::max3(m4[(k >> 1) & 3], __uint_as_float(v[k]), __uint_as_float(v[k + 1]));
+          } else {
 #pragma unroll
-          for (int k = 0; k < 32; ++k) mx = (32 * c + k < nv) ? fmaxf(mx, __uint_as_float(v[k])) : mx;
+            for (int k = 0; k < 32; ++k)
+              m4[k & 3] = (32 * c + k < nv) ? fmaxf(m4[k & 3], __uint_as_float(v[k])) : m4[k & 3];
+          }
         }
+        mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
       }
       // the exponent base may lag the row max by up to 8 (P <= 256); rescale
       // only when a row's max moved further (warp-uniform: TMEM accesses are)
@@ -409,16 +414,20 @@ __global__ void __launch_bounds__(Cfg<D, NQ, PRECISE>::kThreads, 1)
       // written back into the S buffer; pairs of scores in packed fp32 ops
       const uint64_t sl2x2 = ptx::f2_pack(sl2, sl2);
       const uint64_t negm2 = ptx::f2_pack(-m, -m);
-      uint64_t acc2 = ptx::f2_pack(0.f, 0.f);
+      uint64_t acc[1];
+      acc[0] = ptx::f2_pack(0.f, 0.f);
 #pragma unroll
       for (int c = 0; c < kBlockN / 32; ++c) {
-        uint32_t v[32];
-        ptx::tmem_ld32(t_s + 32 * c, v);
+        uint32_t cur[32];
+        ptx::tmem_ld32(t_s + 32 * c, cur);
+        // P of columns [32c, 32c + 32) -> TMEM columns [16c, 16c + 16): all
+        // of them already read (this chunk sits in registers)
         uint32_t pk[16];
 #pragma unroll
         for (int k = 0; k < 16; ++k) {
           float x0, x1;
-          ptx::f2_unpack(ptx::f2_fma(ptx::f2_pack(__uint_as_float(v[2 * k]), __uint_as_float(v[2 * k + 1])),
+          ptx::f2_unpack(ptx::f2_fma(ptx::f2_pack(__uint_as_float(cur[2 * k]),
+                                                  __uint_as_float(cur[2 * k + 1])),
                                      sl2x2, negm2),
                          x0, x1);
           float e0 = ptx::ex2_approx(x0);
@@ -427,13 +436,13 @@ __global__ void __launch_bounds__(Cfg<D, NQ, PRECISE>::kThreads, 1)
             e0 = (32 * c + 2 * k < nv) ? e0 : 0.f;
             e1 = (32 * c + 2 * k + 1 < nv) ? e1 : 0.f;
           }
-          acc2 = ptx::f2_add(acc2, ptx::f2_pack(e0, e1));
+          acc[0] = ptx::f2_add(acc[0], ptx::f2_pack(e0, e1));
           pk[k] = ptx::f16x2_rn(e0, e1);
         }
         if (!mass_only) ptx::tmem_st16(t_s + 16 * c, pk);
       }
       float sum_lo, sum_hi;
-      ptx::f2_unpack(acc2, sum_lo, sum_hi);
+      ptx::f2_unpack(acc[0], sum_lo, sum_hi);
       const float sum = sum_lo + sum_hi;
       if (j < n_ct) l_s += sum; else l_r += sum;
       ptx::tmem_st_wait();
@@ -565,9 +574,6 @@ __global__ void __launch_bounds__(Cfg<D, NQ, PRECISE>::kThreads, 1)
       const int s = j & 1;
       const bool valid = j * kBlockN + r < p.n_s;
       if (j >= 2 && !wait_bar(BAR(kBarEmpty + s), ((j >> 1) - 1) & 1, lim, abort)) break;
-      // the next tile's words are in flight while this one is converted
-      uint32_t nkw[NW], nksz[G], nvw[NW], nvsz[G];
-      load_key(j + 1, nkw, nksz, nvw, nvsz);
       uint8_t* st = smem + C::kStages + s * C::kStageBytes;
       float cb[16], cz[16];
 #pragma unroll
@@ -588,14 +594,13 @@ __global__ void __launch_bounds__(Cfg<D, NQ, PRECISE>::kThreads, 1)
         zero_row<D>(st, r);
         if (!mass_only) zero_row<D>(st + C::kTile, r);
       }
+      // the next tile's words travel while this one is handed over and the
+      // next stage is awaited
+      load_key(j + 1, kw, ksz, vw, vsz);
       write_ext_row(st + 2 * C::kTile, r, cb);
       write_ext_row(st + 2 * C::kTile + kExt, r, cz);
       ptx::fence_proxy_async_smem();
       ptx::mbar_arrive(BAR(kBarFullDq + s));
-#pragma unroll
-      for (int i = 0; i < NW; ++i) { kw[i] = nkw[i]; vw[i] = nvw[i]; }
-#pragma unroll
-      for (int g = 0; g < G; ++g) { ksz[g] = nksz[g]; vsz[g] = nvsz[g]; }
     }
   } else if (warp == C::kMmaWarp) {
     // ============================= MMA =============================
@@ -623,43 +628,47 @@ __global__ void __launch_bounds__(Cfg<D, NQ, PRECISE>::kThreads, 1)
         ptx::tc_fence_after();
         return true;
       };
+      // descriptors: built once, then advanced by (byte offset >> 4) in the
+      // start-address field (the low 14 bits never carry: every operand lies
+      // inside the 256 KB shared window)
+      const uint64_t dsw = ptx::smem_desc(s_base, 16, 1024, ptx::kLayoutSw128);
+      const uint64_t dvw = ptx::smem_desc(s_base, kHalf, 1024, ptx::kLayoutSw128);
+      const uint64_t dex = ptx::smem_desc(s_base, 128, 256, ptx::kLayoutNone);
+      auto at = [](uint64_t d, uint32_t off) { return d + (uint64_t)(off >> 4); };
+      // per MMA only a 64-bit add of a compile-time step: operand bases are
+      // turned into descriptors once per call
       auto issue_qk = [&](int j, int q, uint32_t d_tmem) {
-        const uint32_t st = s_base + C::kStages + (j & 1) * C::kStageBytes;
-        const uint32_t qa = s_base + C::kQ + q * C::kTile;
+        const uint32_t st = C::kStages + (j & 1) * C::kStageBytes;
+        const uint32_t qa = C::kQ + q * C::kTile;
         const bool cached = j < n_ct;
+        const uint32_t idq = cached ? kIdS : kIdSbf;
+        const uint64_t da = at(dsw, qa), db = at(dsw, st);
 #pragma unroll
         for (int s = 0; s < D / 16; ++s) {
-          const uint32_t off = (s >> 2) * kHalf + (s & 3) * 32;
-          ptx::mma_f16(d_tmem, ptx::smem_desc(qa + off, 16, 1024, ptx::kLayoutSw128),
-                       ptx::smem_desc(st + off, 16, 1024, ptx::kLayoutSw128),
-                       cached ? kIdS : kIdSbf, s > 0);
+          const uint64_t off = (uint64_t)(((s >> 2) * kHalf + (s & 3) * 32) >> 4);
+          ptx::mma_f16(d_tmem, da + off, db + off, idq, s > 0);
         }
         if (cached) {
           if (PRECISE) {
+            const uint64_t dl = at(dsw, qa + NQ * C::kTile);
 #pragma unroll
             for (int s = 0; s < D / 16; ++s) {
-              const uint32_t off = (s >> 2) * kHalf + (s & 3) * 32;
-              ptx::mma_f16(d_tmem,
-                           ptx::smem_desc(qa + NQ * C::kTile + off, 16, 1024, ptx::kLayoutSw128),
-                           ptx::smem_desc(st + off, 16, 1024, ptx::kLayoutSw128), kIdS, 1);
+              const uint64_t off = (uint64_t)(((s >> 2) * kHalf + (s & 3) * 32) >> 4);
+              ptx::mma_f16(d_tmem, dl + off, db + off, kIdS, 1);
             }
           }
-          const uint32_t qx = s_base + C::kQx + q * 2 * kExt;
-          const uint32_t kx = st + 2 * C::kTile;
-          ptx::mma_f16(d_tmem, ptx::smem_desc(qx + kExt, 128, 256, ptx::kLayoutNone),
-                       ptx::smem_desc(kx + kExt, 128, 256, ptx::kLayoutNone), kIdS, 1);
-          if (use_bias)
-            ptx::mma_f16(d_tmem, ptx::smem_desc(qx, 128, 256, ptx::kLayoutNone),
-                         ptx::smem_desc(kx, 128, 256, ptx::kLayoutNone), kIdS, 1);
+          const uint64_t dqx = at(dex, C::kQx + q * 2 * kExt);
+          const uint64_t dkx = at(dex, st + 2 * C::kTile);
+          ptx::mma_f16(d_tmem, dqx + (kExt >> 4), dkx + (kExt >> 4), kIdS, 1);
+          if (use_bias) ptx::mma_f16(d_tmem, dqx, dkx, kIdS, 1);
         }
       };
       auto issue_pv = [&](int j, int q, uint32_t p_tmem) {
-        const uint32_t vt = s_base + C::kStages + (j & 1) * C::kStageBytes + C::kTile;
+        const uint64_t dv = at(dvw, C::kStages + (j & 1) * C::kStageBytes + C::kTile);
         const uint32_t o_tmem = tmem + C::kTO + q * D;
 #pragma unroll
         for (int s = 0; s < kBlockN / 16; ++s) {
-          ptx::mma_f16_ts(o_tmem, p_tmem + 8 * s,
-                          ptx::smem_desc(vt + s * 2048, kHalf, 1024, ptx::kLayoutSw128), kIdO,
+          ptx::mma_f16_ts(o_tmem, p_tmem + 8 * s, dv + (uint64_t)((s * 2048) >> 4), kIdO,
                           (j > 0 || s > 0) ? 1u : 0u);
         }
       };
