@@ -131,7 +131,9 @@ __device__ bool wait_bar(uint32_t bar, uint32_t parity, unsigned long long limit
                          volatile int* abort) {
   if (ptx::mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = ptx::globaltimer();
-  while (!ptx::mbar_try_wait(bar, parity)) {
+  // suspended in the wait instruction (up to 20 us per try) instead of
+  // spinning: waiting warps leave the issue slots to the working ones
+  while (!ptx::mbar_try_wait_sleep(bar, parity, 20000u)) {
     if (*abort) return false;
     if (ptx::globaltimer() - t0 > limit_ns) {
       *abort = 1;
