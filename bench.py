@@ -320,14 +320,22 @@ def _cores():
 
 
 def cpu_baseline(w, args):
-    rows = args.cpu_rows
-    flops, dt = _oracle_sample(w, 0, rows, args.seed)
-    return {"value": round(flops / dt / 1e12, 6), "unit": UNIT, "cores": _cores(),
+    """Oracle throughput on a bounded sample: whole heads (all query rows of
+    the chunk) are run one after another until ``--cpu-seconds`` of wall time
+    have been spent (at least one head, at most all of them)."""
+    rows = min(args.cpu_rows, w.n_q) if args.cpu_rows > 0 else w.n_q
+    tot_f, tot_t, heads = 0.0, 0.0, 0
+    while heads < w.heads and (heads == 0 or tot_t < args.cpu_seconds):
+        f, dt = _oracle_sample(w, heads, rows, args.seed)
+        tot_f += f
+        tot_t += dt
+        heads += 1
+    return {"value": round(tot_f / tot_t / 1e12, 6), "unit": UNIT, "cores": _cores(),
             "kind": "oracle",
-            "sample": f"head 0 of {w.name}: oracle quantize of its window + new chunk (K,V) and "
-                      f"corrected attention of {rows} query rows over {w.n_s} cached + {w.n_r} "
-                      f"current keys; value = those rows' attention FLOPs / wall time "
-                      f"({dt:.2f} s)"}
+            "sample": f"{heads} head(s) of {w.name}, each: oracle quantize of its window + new "
+                      f"chunk (K,V) and corrected attention of {rows} query rows over {w.n_s} "
+                      f"cached + {w.n_r} current keys; value = those rows' attention FLOPs / "
+                      f"wall time ({tot_t:.1f} s)"}
 
 
 def run_reference(args):
@@ -371,8 +379,10 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="w4_int2")
     ap.add_argument("--seed", type=int, default=0)
-    ap.add_argument("--cpu-rows", type=int, default=1024,
-                    help="query rows of the oracle sample behind cpu_baseline")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0,
+                    help="wall-time budget of the oracle CPU baseline sample")
+    ap.add_argument("--cpu-rows", type=int, default=0,
+                    help="query rows per head of the cpu_baseline sample (0: the whole chunk)")
     ap.add_argument("--ref-rows", type=int, default=128,
                     help="query rows per step of the --impl reference sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
