@@ -75,7 +75,7 @@ constexpr int kBlockM = 128;
 constexpr int kBlockN = 128;
 constexpr int kHalf = 16384;   // one [128 rows][64 x 16-bit] swizzled sub-tile
 constexpr int kExt = 4096;     // one [128 rows][16 x 16-bit] tile, no swizzle
-constexpr float kRescaleThreshold = 8.0f;  // log2 units the exponent base may lag
+constexpr float kChunkSumLimit = 32768.0f;  // 2^15: every P of the chunk stays FP16
 
 // Extension-column scalings keeping every FP16 operand in range: bias
 // a * 2^8 against D^2 * 2^-8, zero-point term q-sum * 2^4 against -z D * 2^-4.
@@ -227,6 +227,31 @@ __device__ __forceinline__ void dequant_row(const uint32_t (&words)[D * BITS / 3
   }
 }
 
+// Exponentials of one 32-column chunk of scores against the base m: P pairs
+// in FP16 (low column in the low half) and the packed pair of partial sums;
+// columns at or past `valid` give 0.
+__device__ __forceinline__ uint64_t exp_chunk(const uint32_t (&s)[32], uint64_t sl2x2, float m,
+                                              int valid, uint32_t (&pk)[16]) {
+  const uint64_t negm2 = ptx::f2_pack(-m, -m);
+  uint64_t acc = ptx::f2_pack(0.f, 0.f);
+#pragma unroll
+  for (int k = 0; k < 16; ++k) {
+    float x0, x1;
+    ptx::f2_unpack(ptx::f2_fma(ptx::f2_pack(__uint_as_float(s[2 * k]), __uint_as_float(s[2 * k + 1])),
+                               sl2x2, negm2),
+                   x0, x1);
+    float e0 = ptx::ex2_approx(x0);
+    float e1 = ptx::ex2_approx(x1);
+    if (valid < 32) {
+      e0 = (2 * k < valid) ? e0 : 0.f;
+      e1 = (2 * k + 1 < valid) ? e1 : 0.f;
+    }
+    acc = ptx::f2_add(acc, ptx::f2_pack(e0, e1));
+    pk[k] = ptx::f16x2_rn(e0, e1);
+  }
+  return acc;
+}
+
 template <int D>
 __device__ __forceinline__ void zero_row(uint8_t* tile, int r) {
 #pragma unroll
@@ -355,30 +380,51 @@ __global__ void __launch_bounds__(Cfg<D, NQ, PRECISE>::kThreads, 1)
       ptx::tc_fence_after();
       const int nv = j < n_ct ? min(kBlockN, p.n_s - j * kBlockN)
                               : min(kBlockN, p.n_r - (j - n_ct) * kBlockN);
-      // pass 1: row max of the tile (four independent max chains)
-      float mx;
-      {
-        float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+      // One pass over the tile, 32 columns at a time, with the running base
+      // m: P = 2^(s * scale * log2(e) - m).  The base only has to keep every
+      // P inside the FP16 range, so it is raised only when a chunk's sum of
+      // exponentials passes 2^15 (a bound on each of its terms); the chunk is
+      // then recomputed from its scores, still in registers, against
+      // max(m, chunk max), and the tile's earlier P chunks and sum are scaled
+      // to the new base.  O and the running sums follow once per tile.
+      const float m_in = m;
+      const uint64_t sl2x2 = ptx::f2_pack(sl2, sl2);
+      uint64_t acc = ptx::f2_pack(0.f, 0.f);
+#pragma unroll 1
+      for (int c = 0; c < kBlockN / 32; ++c) {
+        uint32_t cur[32];
+        ptx::tmem_ld32(t_s + 32 * c, cur);
+        uint32_t pk[16];
+        uint64_t cs = exp_chunk(cur, sl2x2, m, nv - 32 * c, pk);
+        float cs_lo, cs_hi;
+        ptx::f2_unpack(cs, cs_lo, cs_hi);
+        // NaN-safe: an infinite or undefined sum also takes the slow path
+        if (__any_sync(0xffffffffu, !(cs_lo + cs_hi <= kChunkSumLimit))) {
+          float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-        for (int c = 0; c < kBlockN / 32; ++c) {
-          uint32_t v[32];
-          ptx::tmem_ld32(t_s + 32 * c, v);
-          if (nv == kBlockN) {
+          for (int k = 0; k < 32; ++k)
+            m4[k & 3] = (32 * c + k < nv) ? fmaxf(m4[k & 3], __uint_as_float(cur[k])) : m4[k & 3];
+          const float m_new = fmaxf(m, fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * sl2);
+          const float alpha = exp2f(m - m_new);   // 0 from the initial -inf base
+          acc = ptx::f2_mul(acc, ptx::f2_pack(alpha, alpha));
+          if (!mass_only && c > 0) {
+            ptx::tmem_st_wait();
+            for (int cc = 0; cc < c; ++cc) {
+              uint32_t v[16];
+              ptx::tmem_ld16(t_s + 16 * cc, v);
 #pragma unroll
-            for (int k = 0; k < 32; k += 2)
-              m4[(k >> 1) & 3] = ptx::max3(m4[(k >> 1) & 3], __uint_as_float(v[k]), __uint_as_float(v[k + 1]));
-          } else {
-#pragma unroll
-            for (int k = 0; k < 32; ++k)
-              m4[k & 3] = (32 * c + k < nv) ? fmaxf(m4[k & 3], __uint_as_float(v[k])) : m4[k & 3];
+              for (int k = 0; k < 16; ++k) v[k] = ptx::f16x2_rn(h_lo(v[k]) * alpha, h_hi(v[k]) * alpha);
+              ptx::tmem_st16(t_s + 16 * cc, v);
+            }
           }
+          m = m_new;
+          cs = exp_chunk(cur, sl2x2, m, nv - 32 * c, pk);
         }
-        mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+        acc = ptx::f2_add(acc, cs);
+        // P of columns [32c, 32c + 32) -> TMEM columns [16c, 16c + 16): all
+        // of them already read
+        if (!mass_only) ptx::tmem_st16(t_s + 16 * c, pk);
       }
-      // the exponent base may lag the row max by up to 8 (P <= 256); rescale
-      // only when a row's max moved further (warp-uniform: TMEM accesses are)
-      const float m_cand = mx * sl2;
-      const bool need = m_cand > m + kRescaleThreshold;
       if (NQ == 1 && j > 0) {
         // one-tile schedule: QK of this tile was issued before the previous
         // PV; O and the P-ready phases wait for that PV
@@ -388,12 +434,10 @@ __global__ void __launch_bounds__(Cfg<D, NQ, PRECISE>::kThreads, 1)
         }
         ptx::tc_fence_after();
       }
-      if (__any_sync(0xffffffffu, need)) {
-        const float m_new = need ? m_cand : m;
-        const float alpha = exp2f(m - m_new);
+      if (__any_sync(0xffffffffu, m != m_in)) {
+        const float alpha = exp2f(m_in - m);
         l_s *= alpha;
         l_r *= alpha;
-        m = m_new;
         if (j > 0 && !mass_only) {
           const uint64_t a2 = ptx::f2_pack(alpha, alpha);
 #pragma unroll
@@ -412,39 +456,8 @@ __global__ void __launch_bounds__(Cfg<D, NQ, PRECISE>::kThreads, 1)
           }
         }
       }
-      // pass 2: exponentials (special-function unit), sums, P (FP16 pairs)
-      // written back into the S buffer; pairs of scores in packed fp32 ops
-      const uint64_t sl2x2 = ptx::f2_pack(sl2, sl2);
-      const uint64_t negm2 = ptx::f2_pack(-m, -m);
-      uint64_t acc[1];
-      acc[0] = ptx::f2_pack(0.f, 0.f);
-#pragma unroll
-      for (int c = 0; c < kBlockN / 32; ++c) {
-        uint32_t cur[32];
-        ptx::tmem_ld32(t_s + 32 * c, cur);
-        // P of columns [32c, 32c + 32) -> TMEM columns [16c, 16c + 16): all
-        // of them already read (this chunk sits in registers)
-        uint32_t pk[16];
-#pragma unroll
-        for (int k = 0; k < 16; ++k) {
-          float x0, x1;
-          ptx::f2_unpack(ptx::f2_fma(ptx::f2_pack(__uint_as_float(cur[2 * k]),
-                                                  __uint_as_float(cur[2 * k + 1])),
-                                     sl2x2, negm2),
-                         x0, x1);
-          float e0 = ptx::ex2_approx(x0);
-          float e1 = ptx::ex2_approx(x1);
-          if (nv != kBlockN) {
-            e0 = (32 * c + 2 * k < nv) ? e0 : 0.f;
-            e1 = (32 * c + 2 * k + 1 < nv) ? e1 : 0.f;
-          }
-          acc[0] = ptx::f2_add(acc[0], ptx::f2_pack(e0, e1));
-          pk[k] = ptx::f16x2_rn(e0, e1);
-        }
-        if (!mass_only) ptx::tmem_st16(t_s + 16 * c, pk);
-      }
       float sum_lo, sum_hi;
-      ptx::f2_unpack(acc[0], sum_lo, sum_hi);
+      ptx::f2_unpack(acc, sum_lo, sum_hi);
       const float sum = sum_lo + sum_hi;
       if (j < n_ct) l_s += sum; else l_r += sum;
       ptx::tmem_st_wait();

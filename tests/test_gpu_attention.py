@@ -145,3 +145,41 @@ def test_bounded_wait_reports_timeout():
     assert kvq.last_device_status() == kvq.KVQ_OK
     t = torch.ones(10, device="cuda")
     assert float(t.sum().item()) == 10.0
+
+
+@pytest.mark.parametrize("corr,flags", [(kvq.CORR_TAYLOR, 0), (kvq.CORR_NONE, 0),
+                                        (kvq.CORR_TAYLOR, kvq.FLAG_PRECISE_QUERY)])
+def test_rising_scores_rebase(corr, flags):
+    """Keys planted along a direction every query shares, with scores jumping
+    by ~16 (natural units) several times: late in a key tile's first, second,
+    third and last 32-key chunk of the cache and in the current chunk.  Every
+    jump pushes the exponentials of the streaming softmax past the FP16 range
+    of P unless the exponent base is raised mid-tile, so this checks that the
+    base change rescales what the tile already produced."""
+    d = 128
+    w = synth.Workload("rebase", heads=2, head_dim=d, chunk_tokens=256, n_chunks=2, bits=2,
+                       group=32, n_outliers_fixed=0, offset_std=0.0)
+    n_q, n_s, n_r = 200, 512, 200
+    x = synth.inputs(w, seed=11, n_q=n_q, n_s=n_s, n_r=n_r)
+    g = torch.Generator().manual_seed(7)
+    u = torch.randn(d, generator=g)
+    u = u / u.norm()
+    q = x["q"].float() + 11.3 * u                  # q . u ~ 11.3 for every query
+    kw = x["k_win"].float()
+    kc = x["k_cur"].float()
+    for idx, mult in ((40, 8.0), (100, 16.0), (300, 32.0), (470, 48.0)):
+        kw[:, :, idx] = mult * u
+    kc[:, :, 150] = 40.0 * u
+    x = dict(x, q=q.bfloat16().contiguous(), k_win=kw.bfloat16().contiguous(),
+             k_cur=kc.bfloat16().contiguous())
+    s = synth.hadamard_signs(d, seed=3)
+    cache = build_cache(w, x, s, n_s=n_s)
+    out, ps, pr = kvq.attention_corrected(cache, x["q"].cuda(), x["k_cur"].cuda(),
+                                          x["v_cur"].cuda(), corr=corr, with_mass=True,
+                                          flags=flags)
+    torch.cuda.synchronize()
+    assert kvq.last_device_status() == 0
+    for h in range(w.heads):
+        o_ref, ps_ref, pr_ref = oracle_head(w, x, s, 0, h, np.arange(n_q), corr, n_s=n_s)
+        assert_close(out[0, h].float().cpu().numpy(), o_ref, ps[0, h].cpu().numpy(), ps_ref,
+                     pr[0, h].cpu().numpy(), pr_ref, what=f"rebase h{h}")
