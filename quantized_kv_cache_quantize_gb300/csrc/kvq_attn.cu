@@ -26,11 +26,14 @@
 // every wait is bounded by a time limit.
 //
 // Numerics.  Cached scores: the K tile holds code * D, exact in FP16 for INT2
-// (<= 10 significant bits); two rank-G terms enter through 16-column
-// extension tiles contracted on the tensor core: the keys' zero points
-// (sum_g (sum_{c in g} q'_c) * (-z_g D_g)) and, with the correction, the Jensen
-// bias -(scale/24) sum_g ||q'_g||^2 D_g^2 (per group three columns, FP16
-// high/low splits, so the products carry ~2^-21 relative error).  The rotated
+// (<= 10 significant bits); two rank-G terms enter through one 16-column
+// extension tile contracted on the tensor core: the keys' zero points
+// (sum_g (sum_{c in g} q'_c) * (-z_g D_g), three columns per group, FP16
+// high/low splits, so the products carry ~2^-21 relative error) and, with the
+// correction, the Jensen bias -(scale/24) sum_g ||q'_g||^2 D_g^2 (one column
+// per group, ~2^-11 relative error on a term that is a small fraction of the
+// score; with the precise-query flag a second extension tile carries it with
+// three columns per group as well).  The rotated
 // query is FP16 (or FP16 high + low parts with the precise-query flag: one
 // more QK pass on cached tiles).  Current scores use the BF16 inputs as they
 // are (exact products).  P and the rotated current values are FP16; V tiles
@@ -91,8 +94,9 @@ struct Cfg {
   // shared memory
   static constexpr int kQ = 0;                             // NQ hi tiles [, NQ lo tiles]
   static constexpr int kQx = kQ + NQ * kTile * (PRECISE ? 2 : 1);
-  static constexpr int kStageBytes = 2 * kTile + 2 * kExt;  // K, V, Kx (bias), Kx (zero)
-  static constexpr int kStages = kQx + NQ * 2 * kExt;
+  static constexpr int kNExt = PRECISE ? 2 : 1;              // extension tiles
+  static constexpr int kStageBytes = 2 * kTile + kNExt * kExt;  // K, V, Kx
+  static constexpr int kStages = kQx + NQ * kNExt * kExt;
   static constexpr int kBar = kStages + 2 * kStageBytes;
   static constexpr int kBytes = kBar + 256;
   static constexpr int kAlloc = kBytes + 1024;
@@ -179,8 +183,12 @@ __device__ __forceinline__ void split_h(float v, float& hi, float& lo) {
   lo = __half2float(__float2half_rn(v - hi));
 }
 
-// 16 extension columns of one row: three per group g, (hi, hi, lo) of a on
-// the query side against (hi, lo, hi) of b on the key side.
+// 16 extension columns of one row.  Merged tile: columns [0, G) hold the
+// bias factors of the G groups (query side a_g, key side b_g), columns
+// G + 3g .. G + 3g + 2 the zero-point factors of group g as (hi, hi, lo) on the
+// query side against (hi, lo, hi) on the key side.  Precise layout: tile 0 the
+// bias factors split the same way in columns 3g .. 3g + 2, tile 1 the
+// zero-point factors in columns 3g .. 3g + 2.  Unused columns are zero.
 __device__ __forceinline__ void write_ext_row(uint8_t* tile, int r, const float (&cols)[16]) {
   uint32_t w[8];
 #pragma unroll
@@ -269,7 +277,7 @@ __global__ void __launch_bounds__(Cfg<D, NQ, PRECISE>::kThreads, 1)
   constexpr int CB = D * BITS / 8;       // packed bytes per token
   constexpr int NW = CB / 4;             // packed words per token
   constexpr int NKH = C::kNKH;
-  static_assert(3 * G <= 16, "extension columns");
+  static_assert((PRECISE ? 3 : 4) * G <= 16, "extension columns");
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -349,19 +357,25 @@ __global__ void __launch_bounds__(Cfg<D, NQ, PRECISE>::kThreads, 1)
         nrm[(8 * c) / GROUP] += acc;
         qsum[(8 * c) / GROUP] += sum;
       }
-      float cb[16], cz[16];
+      float cx[16], cz[16];
 #pragma unroll
-      for (int i = 0; i < 16; ++i) cb[i] = cz[i] = 0.f;
+      for (int i = 0; i < 16; ++i) cx[i] = cz[i] = 0.f;
 #pragma unroll
       for (int g = 0; g < G; ++g) {
         float hi, lo;
-        split_h(p.alpha_coef * nrm[g], hi, lo);
-        cb[3 * g] = hi; cb[3 * g + 1] = hi; cb[3 * g + 2] = lo;
+        const int zc = PRECISE ? 3 * g : G + 3 * g;
+        float(&zt)[16] = PRECISE ? cz : cx;
         split_h(kZeroQueryScale * qsum[g], hi, lo);
-        cz[3 * g] = hi; cz[3 * g + 1] = hi; cz[3 * g + 2] = lo;
+        zt[zc] = hi; zt[zc + 1] = hi; zt[zc + 2] = lo;
+        if (PRECISE) {
+          split_h(p.alpha_coef * nrm[g], hi, lo);
+          cx[3 * g] = hi; cx[3 * g + 1] = hi; cx[3 * g + 2] = lo;
+        } else {
+          cx[g] = p.alpha_coef * nrm[g];
+        }
       }
-      write_ext_row(smem + C::kQx + q * 2 * kExt, r, cb);
-      write_ext_row(smem + C::kQx + q * 2 * kExt + kExt, r, cz);
+      write_ext_row(smem + C::kQx + q * C::kNExt * kExt, r, cx);
+      if (PRECISE) write_ext_row(smem + C::kQx + q * C::kNExt * kExt + kExt, r, cz);
       ptx::fence_proxy_async_smem();
       ptx::mbar_arrive(BAR(kBarQx));
     }
@@ -590,9 +604,9 @@ __global__ void __launch_bounds__(Cfg<D, NQ, PRECISE>::kThreads, 1)
       const bool valid = j * kBlockN + r < p.n_s;
       if (j >= 2 && !wait_bar(BAR(kBarEmpty + s), ((j >> 1) - 1) & 1, lim, abort)) break;
       uint8_t* st = smem + C::kStages + s * C::kStageBytes;
-      float cb[16], cz[16];
+      float cx[16], cz[16];
 #pragma unroll
-      for (int i = 0; i < 16; ++i) cb[i] = cz[i] = 0.f;
+      for (int i = 0; i < 16; ++i) cx[i] = cz[i] = 0.f;
       if (valid) {
         dequant_row<D, BITS, GROUP, false>(kw, ksz, st, r);
         if (!mass_only) dequant_row<D, BITS, GROUP, true>(vw, vsz, st + C::kTile, r);
@@ -600,10 +614,16 @@ __global__ void __launch_bounds__(Cfg<D, NQ, PRECISE>::kThreads, 1)
         for (int g = 0; g < G; ++g) {
           const float dl = bf16_lo(ksz[g]);
           float hi, lo;
-          split_h(dl * dl * kBiasKeyScale, hi, lo);
-          cb[3 * g] = hi; cb[3 * g + 1] = lo; cb[3 * g + 2] = hi;
+          const int zc = PRECISE ? 3 * g : G + 3 * g;
+          float(&zt)[16] = PRECISE ? cz : cx;
           split_h(-bf16_hi(ksz[g]) * dl * kZeroKeyScale, hi, lo);
-          cz[3 * g] = hi; cz[3 * g + 1] = lo; cz[3 * g + 2] = hi;
+          zt[zc] = hi; zt[zc + 1] = lo; zt[zc + 2] = hi;
+          if (PRECISE) {
+            split_h(dl * dl * kBiasKeyScale, hi, lo);
+            cx[3 * g] = hi; cx[3 * g + 1] = lo; cx[3 * g + 2] = hi;
+          } else {
+            cx[g] = dl * dl * kBiasKeyScale;
+          }
         }
       } else {
         zero_row<D>(st, r);
@@ -612,8 +632,8 @@ __global__ void __launch_bounds__(Cfg<D, NQ, PRECISE>::kThreads, 1)
       // the next tile's words travel while this one is handed over and the
       // next stage is awaited
       load_key(j + 1, kw, ksz, vw, vsz);
-      write_ext_row(st + 2 * C::kTile, r, cb);
-      write_ext_row(st + 2 * C::kTile + kExt, r, cz);
+      write_ext_row(st + 2 * C::kTile, r, cx);
+      if (PRECISE) write_ext_row(st + 2 * C::kTile + kExt, r, cz);
       ptx::fence_proxy_async_smem();
       ptx::mbar_arrive(BAR(kBarFullDq + s));
     }
@@ -623,7 +643,6 @@ __global__ void __launch_bounds__(Cfg<D, NQ, PRECISE>::kThreads, 1)
       constexpr uint32_t kIdS = ptx::idesc_f16kind(kBlockM, kBlockN, false, false);
       constexpr uint32_t kIdSbf = ptx::idesc_f16kind(kBlockM, kBlockN, false, true);
       constexpr uint32_t kIdO = ptx::idesc_f16kind(kBlockM, D, true, false);
-      const bool use_bias = p.corr != 0;
       const uint32_t s_base = ptx::smem_u32(smem);
       bool ok = wait_bar(BAR(kBarQ), 0, lim, abort) && wait_bar(BAR(kBarQx), 0, lim, abort);
       if (ok && n_ct == 0) ptx::mbar_arrive(BAR(kBarQFree));
@@ -672,10 +691,12 @@ __global__ void __launch_bounds__(Cfg<D, NQ, PRECISE>::kThreads, 1)
               ptx::mma_f16(d_tmem, dl + off, db + off, kIdS, 1);
             }
           }
-          const uint64_t dqx = at(dex, C::kQx + q * 2 * kExt);
+          // zero points and bias (its query columns are zero without the
+          // correction); the precise layout spends a tile on each
+          const uint64_t dqx = at(dex, C::kQx + q * C::kNExt * kExt);
           const uint64_t dkx = at(dex, st + 2 * C::kTile);
-          ptx::mma_f16(d_tmem, dqx + (kExt >> 4), dkx + (kExt >> 4), kIdS, 1);
-          if (use_bias) ptx::mma_f16(d_tmem, dqx, dkx, kIdS, 1);
+          ptx::mma_f16(d_tmem, dqx, dkx, kIdS, 1);
+          if (PRECISE) ptx::mma_f16(d_tmem, dqx + (kExt >> 4), dkx + (kExt >> 4), kIdS, 1);
         }
       };
       auto issue_pv = [&](int j, int q, uint32_t p_tmem) {
