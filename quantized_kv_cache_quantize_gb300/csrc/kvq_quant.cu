@@ -49,18 +49,6 @@ struct PairSigns {
 
 constexpr int kRowThreads = 128;
 
-// rint of q = fl(x * fl(1/delta)), folding |q - rint(q)| and |q| into running
-// maxima.  q is within 2^-22 |q| of fl(x / delta), so when every q of a group
-// stays more than 2^-20 max(1, |q|) away from a half-integer, rint(q) equals
-// rint(fl(x / delta)) (IEEE quotient, ties to even) for all of them; otherwise
-// (or for non-finite q) the group takes the correctly rounded division.
-__device__ __forceinline__ float rint_q(float q, float& max_frac, float& max_q) {
-  const float n = rintf(q);
-  max_frac = fmaxf(max_frac, fabsf(__fsub_rn(q, n)));
-  max_q = fmaxf(max_q, fabsf(q));
-  return n;
-}
-
 // One thread per row (one token's K or V row of one head): the whole row in
 // registers, so the rotation needs no data exchange between threads.  Per
 // row: d/8 16-byte loads, fp32 butterflies in the order h = 1, 2, ..., d/2
@@ -120,9 +108,6 @@ __global__ void __launch_bounds__(kRowThreads) quantize_rows_kernel(const QuantA
     for (int i = 0; i < D; i += 2) ptx::f2_unpack(ptx::f2_mul(ptx::f2_pack(x[i], x[i + 1]), s2), x[i], x[i + 1]);
   }
 
-  uint32_t words[D * BITS / 32];
-#pragma unroll
-  for (int i = 0; i < D * BITS / 32; ++i) words[i] = 0u;
   uint32_t rec[G];
 #pragma unroll
   for (int g = 0; g < G; ++g) {
@@ -145,34 +130,68 @@ __global__ void __launch_bounds__(kRowThreads) quantize_rows_kernel(const QuantA
     const float zero = bf16_value(zbits);
     rec[g] = dbits | (zbits << 16);
 
-    // codes: fast route for the whole group, exact division when any
-    // element's quotient came within 2^-20 max(1, |q|) of a half-integer
-    float n[GROUP];
-    float max_frac = 0.f, max_q = 0.f;
-    {
+    // codes.  Fast route: q = fl(x / delta) exactly, from the correctly
+    // rounded reciprocal r and one residual step (q0 = fl(x r), e = x - q0 delta
+    // exact by FMA, q = fl(q0 + e r): correctly rounded while nothing over- or
+    // underflows); rint(q) by adding 1.5 * 2^23 (ties to even, |q| < 2^21);
+    // the integer zero point added after the rounding.  K = 1.5 * 2^23 + code
+    // then carries the code in its low mantissa bits.  Codes are monotone in
+    // x, so those of the group's min and max bound them all and the clamp to
+    // [0, 2^B - 1] is needed only when one of those two falls outside.
+    const float kMagic = 12582912.0f;   // 1.5 * 2^23
+    const bool fast = rcp < 0x1p100f && fabsf(mn) * rcp < 0x1p21f && fabsf(mx) * rcp < 0x1p21f;
+    float* xg = x + GROUP * g;
+    if (fast) {
+      auto code_of = [&](float v) {
+        const float q0 = __fmul_rn(v, rcp);
+        const float q = __fmaf_rn(__fmaf_rn(-q0, delta, v), rcp, q0);
+        return __fadd_rn(__fadd_rn(q, kMagic), zero) - kMagic;
+      };
+      const bool clamp = code_of(mn) < 0.0f || code_of(mx) > qmax;
       const uint64_t r2 = ptx::f2_pack(rcp, rcp);
+      const uint64_t nd2 = ptx::f2_pack(-delta, -delta);
+      const uint64_t m2 = ptx::f2_pack(kMagic, kMagic);
+      const uint64_t z2 = ptx::f2_pack(zero, zero);
 #pragma unroll
       for (int c = 0; c < GROUP; c += 2) {
-        float q0, q1;
-        ptx::f2_unpack(ptx::f2_mul(ptx::f2_pack(x[GROUP * g + c], x[GROUP * g + c + 1]), r2), q0, q1);
-        n[c] = rint_q(q0, max_frac, max_q);
-        n[c + 1] = rint_q(q1, max_frac, max_q);
+        const uint64_t xv = ptx::f2_pack(xg[c], xg[c + 1]);
+        const uint64_t q0 = ptx::f2_mul(xv, r2);
+        const uint64_t e = ptx::f2_fma(q0, nd2, xv);
+        const uint64_t q = ptx::f2_fma(e, r2, q0);
+        ptx::f2_unpack(ptx::f2_add(ptx::f2_add(q, m2), z2), xg[c], xg[c + 1]);
+      }
+      if (clamp) {
+#pragma unroll
+        for (int c = 0; c < GROUP; ++c) xg[c] = fminf(fmaxf(xg[c], kMagic), kMagic + qmax);
+      }
+    } else {
+      // exact division element by element (huge quotients, tiny steps)
+#pragma unroll
+      for (int c = 0; c < GROUP; ++c) {
+        float t = __fadd_rn(rintf(__fdiv_rn(xg[c], delta)), zero);
+        t = fminf(fmaxf(t, 0.0f), qmax);
+        xg[c] = __fadd_rn(t, kMagic);
       }
     }
-    if (!(__fsub_rn(0.5f, max_frac) > 0x1p-20f * fmaxf(1.0f, max_q))) {
+  }
+
+  // pack: channel ch = 16w + 2k + h (INT2) / 8w + 2k + h (INT4) -> bits
+  // BITS*k + 16h.  The low 16 bits of 1.5 * 2^23 are zero, so a Horner sum
+  // of the K bit patterns (times 2^BITS per code) leaves exactly the codes
+  // in the low half-word.
+  uint32_t words[D * BITS / 32];
 #pragma unroll
-      for (int c = 0; c < GROUP; ++c) n[c] = rintf(__fdiv_rn(x[GROUP * g + c], delta));
-    }
+  for (int w = 0; w < D * BITS / 32; ++w) {
+    uint32_t half[2];
 #pragma unroll
-    for (int c = 0; c < GROUP; ++c) {
-      float t = __fadd_rn(n[c], zero);
-      t = fminf(fmaxf(t, 0.0f), qmax);
-      const uint32_t code = (uint32_t)__float2int_rn(t);
-      // channel ch = 16w + 2k + h (INT2) / 8w + 2k + h (INT4) -> bits BITS*k + 16h
-      const int ch = GROUP * g + c;
-      const int w = ch / PER_WORD, k = (ch % PER_WORD) >> 1, hh = ch & 1;
-      words[w] |= code << (BITS * k + 16 * hh);
+    for (int hh = 0; hh < 2; ++hh) {
+      uint32_t acc = __float_as_uint(x[PER_WORD * w + hh + 2 * (PER_WORD / 2 - 1)]);
+#pragma unroll
+      for (int k = PER_WORD / 2 - 2; k >= 0; --k)
+        acc = acc * (1u << BITS) + __float_as_uint(x[PER_WORD * w + hh + 2 * k]);
+      half[hh] = acc;
     }
+    words[w] = __byte_perm(half[0], half[1], 0x5410);
   }
 
   const size_t dst_tok = (size_t)bh * a.cap + a.first + tok;
