@@ -891,14 +891,9 @@ bool make_map(CUtensorMap* m, const void* base, int d, int n, int bh, bool bf16)
 template <int D, int BITS, int GROUP, int NQ, bool PRECISE>
 kvq_status launch_t(const AttnLaunch& a, cudaStream_t stream) {
   using C = Cfg<D, NQ, PRECISE>;
-  static bool attr_set = false;
+  static std::atomic<uint64_t> limit_set{0};   // per template instance and device
   auto kern = attn_kernel<D, BITS, GROUP, NQ, PRECISE>;
-  if (!attr_set) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kAlloc) !=
-        cudaSuccess)
-      return KVQ_ERR_CUDA;
-    attr_set = true;
-  }
+  if (ensure_smem_limit(kern, C::kAlloc, limit_set) != cudaSuccess) return KVQ_ERR_CUDA;
   CUtensorMap mq, mqlo, mqo, mk, mv;
   if (!make_map(&mq, a.q_rot, D, a.n_q, a.bh, false)) return KVQ_ERR_CUDA;
   if (!make_map(&mqlo, a.q_rot_lo, D, a.n_q, a.bh, false)) return KVQ_ERR_CUDA;

@@ -4,6 +4,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "../../include/kvq.h"
 
 namespace kvq {
@@ -47,6 +49,21 @@ struct RotateArgs {
   float inv_sqrt_d;
   int out_f32;
 };
+
+// Raise a kernel's dynamic shared-memory limit once per device (the
+// attribute belongs to the current device's context); `done` holds one bit
+// per device ordinal below 64.
+template <typename Kernel>
+cudaError_t ensure_smem_limit(Kernel kern, int bytes, std::atomic<uint64_t>& done) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const uint64_t bit = dev < 64 ? (uint64_t{1} << dev) : 0;
+  if (bit != 0 && (done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess && bit != 0) done.fetch_or(bit, std::memory_order_release);
+  return e;
+}
 
 cudaError_t launch_quantize_append(const QuantArgs& a, int d, int bits, int group,
                                    cudaStream_t stream, bool* supported);

@@ -5,11 +5,12 @@
 // round-to-nearest, step and zero point covering [min, max]) and pack the
 // codes into the chunk slot of the sliding-window cache.
 //
-// Mapping: a row of d channels is held by d/8 consecutive lanes, 8 channels
-// (one 16-byte load) per lane; a warp holds 32/(d/8) rows.  The transform,
-// the group min/max and the packing all move data with warp shuffles; codes
-// leave in 16-byte stores, the (step, zero) record of a token in one store.
-// The kernel is bound by HBM bandwidth: per row it reads 2d bytes and writes
+// Mapping: one thread per row (the whole row in registers, so the rotation
+// needs no data exchange between threads); each warp owns tiles of 32 rows
+// and stages the next tile into shared memory with asynchronous 16-byte
+// copies while it quantizes the current one.  Codes leave in 16-byte
+// stores, the (step, zero) records of a token in one store.  The kernel is
+// bound by HBM bandwidth: per row it reads 2d bytes and writes
 // d*bits/8 + 4*(d/group) bytes.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -25,10 +26,6 @@ namespace {
 
 constexpr int kThreads = 256;
 
-__device__ __forceinline__ uint32_t shfl_idx(uint32_t v, int src) {
-  return __shfl_sync(0xffffffffu, v, src);
-}
-
 __device__ __forceinline__ uint32_t h_bits_rn(float v) {
   return (uint32_t)__half_as_ushort(__float2half_rn(v));
 }
@@ -40,55 +37,186 @@ __device__ __forceinline__ uint32_t sign_word_for(const uint32_t (&sb)[4], int t
   return i == 0 ? sb[0] : i == 1 ? sb[1] : i == 2 ? sb[2] : sb[3];
 }
 
-// Sign flips of the randomized rotation in the BF16 pair domain: word i of
-// a row holds channels 2i (low half) and 2i + 1 (high half); XOR with m[i]
-// flips their sign bits (bit 15, bit 31).
+// Sign flips of the randomized rotation: word i of a BF16 row holds channels
+// 2i (low half) and 2i + 1 (high half).  XOR with m[i] flips the sign bit of
+// channel 2i + 1 (bit 31); channel 2i enters the first butterfly through an
+// FMA by sl[i] = +-1 (an exact product, so the butterfly still rounds once).
 struct PairSigns {
   uint32_t m[64];
+  float sl[64];
 };
 
-constexpr int kRowThreads = 128;
+// fl(x / d) from r = fl(1 / d): q0 = fl(x r), the exact residual x - q0 d by
+// FMA, one correction step.  Correctly rounded while neither the residual
+// nor the quotient leaves the normal range (Markstein's correction with a
+// correctly rounded reciprocal).
+__device__ __forceinline__ float div_step(float x, float d, float r) {
+  const float q0 = __fmul_rn(x, r);
+  return __fmaf_rn(__fmaf_rn(-q0, d, x), r, q0);
+}
 
-// One thread per row (one token's K or V row of one head): the whole row in
-// registers, so the rotation needs no data exchange between threads.  Per
-// row: d/8 16-byte loads, fp32 butterflies in the order h = 1, 2, ..., d/2
-// (packed fp32 pairs from h = 2 on: each lane is the same correctly rounded
-// add or subtract), per-group min/max, Eq. (1) codes, packed 16-byte stores.
+constexpr int kQWarps = 4;        // warps per block of the quantizer
+constexpr int kQBlocksPerSm = 3;
+
+__device__ __forceinline__ void cp_async16(void* smem_dst, const void* gmem_src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(ptx::smem_u32(smem_dst)),
+               "l"(gmem_src)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// Eq. (1) for one group (or the part of it one thread holds) given the
+// group's min and max: step covering [min, max] and integer zero point, both
+// stored BF16 and returned as the record (step | zero << 16); the n values
+// xg[0..n) are replaced by 1.5 * 2^23 + code - zfold, zfold being the zero
+// point when it is left for the packing to add (0 otherwise).
+template <int BITS, int N>
+__device__ __forceinline__ uint32_t group_codes(float* xg, float mn, float mx, int& zfold) {
+  const float qmax = float((1 << BITS) - 1);
+  // Eq. (1): step covering [min, max], integer zero point, both stored BF16
+  constexpr float kInvQmax = 1.0f / float((1 << BITS) - 1);   // fl(1 / qmax)
+  const float span = __fsub_rn(mx, mn);
+  uint32_t dbits = bf16_bits_rn(span >= 0x1p-100f && span < 0x1p100f
+                                    ? div_step(span, qmax, kInvQmax)
+                                    : __fdiv_rn(span, qmax));
+  if (bf16_value(dbits) == 0.0f) {
+    dbits = bf16_bits_rn(fabsf(mn));
+    if (bf16_value(dbits) == 0.0f) dbits = 0x3F80u;  // 1.0
+  }
+  const float delta = bf16_value(dbits);
+  const float rcp = __frcp_rn(delta);
+  const bool fast = rcp < 0x1p100f && fabsf(mn) * rcp < 0x1p21f && fabsf(mx) * rcp < 0x1p21f;
+  const float zq = fast ? div_step(-mn, delta, rcp) : __fdiv_rn(-mn, delta);
+  const uint32_t zbits = bf16_bits_rn(__fadd_rn(rintf(zq), 0.0f));
+  const float zero = bf16_value(zbits);
+
+  // codes.  Fast route: q = fl(x / delta) exactly, from the correctly
+  // rounded reciprocal r and one residual step (q0 = fl(x r), e = x - q0 delta
+  // exact by FMA, q = fl(q0 + e r): correctly rounded while nothing over- or
+  // underflows); rint(q) by adding 1.5 * 2^23 (ties to even, |q| < 2^21);
+  // the integer zero point added after the rounding.  K = 1.5 * 2^23 + code
+  // then carries the code in its low mantissa bits.  Codes are monotone in
+  // x, so those of the group's min and max bound them all and the clamp to
+  // [0, 2^B - 1] is needed only when one of those two falls outside; when
+  // it is not, the zero point is left to the packing (which adds it to a
+  // whole half-word of codes at once).
+  const float kMagic = 12582912.0f;   // 1.5 * 2^23
+  if (fast) {
+    auto code_of = [&](float v) {
+      const float q0 = __fmul_rn(v, rcp);
+      const float q = __fmaf_rn(__fmaf_rn(-q0, delta, v), rcp, q0);
+      return __fadd_rn(__fadd_rn(q, kMagic), zero) - kMagic;
+    };
+    const bool clamp = code_of(mn) < 0.0f || code_of(mx) > qmax;
+    const uint64_t r2 = ptx::f2_pack(rcp, rcp);
+    const uint64_t nd2 = ptx::f2_pack(-delta, -delta);
+    const uint64_t m2 = ptx::f2_pack(kMagic, kMagic);
+#pragma unroll
+    for (int c = 0; c < N; c += 2) {
+      const uint64_t xv = ptx::f2_pack(xg[c], xg[c + 1]);
+      const uint64_t q0 = ptx::f2_mul(xv, r2);
+      const uint64_t e = ptx::f2_fma(q0, nd2, xv);
+      const uint64_t q = ptx::f2_fma(e, r2, q0);
+      ptx::f2_unpack(ptx::f2_add(q, m2), xg[c], xg[c + 1]);
+    }
+    zfold = __float2int_rn(zero);
+    if (clamp) {
+#pragma unroll
+      for (int c = 0; c < N; ++c) xg[c] = fminf(fmaxf(__fadd_rn(xg[c], zero), kMagic), kMagic + qmax);
+      zfold = 0;
+    }
+  } else {
+    zfold = 0;
+    // exact division element by element (huge quotients, tiny steps)
+#pragma unroll
+    for (int c = 0; c < N; ++c) {
+      float t = __fadd_rn(rintf(__fdiv_rn(xg[c], delta)), zero);
+      t = fminf(fmaxf(t, 0.0f), qmax);
+      xg[c] = __fadd_rn(t, kMagic);
+    }
+  }
+  return dbits | (zbits << 16);
+}
+
+// One packed word from the 32/BITS consecutive channels xw[0..) (each value
+// 1.5 * 2^23 + code): channel 2k + h of the word at bits BITS*k + 16h.  The
+// low 16 bits of 1.5 * 2^23 are zero, so a Horner sum of the bit patterns
+// (times 2^BITS per code) leaves the codes in the low half-word, given the
+// group's folded zero point (all channels of a word share one group).
+template <int BITS>
+__device__ __forceinline__ uint32_t pack_word(const float* xw, int zfold) {
+  constexpr int PER_WORD = 32 / BITS;
+  // zfold times (1 + 2^BITS + 2^(2 BITS) + ...) over a half-word's codes
+  constexpr uint32_t kOnes = BITS == 2 ? 0x5555u : 0x1111u;
+  uint32_t half[2];
+#pragma unroll
+  for (int hh = 0; hh < 2; ++hh) {
+    uint32_t acc = __float_as_uint(xw[hh + 2 * (PER_WORD / 2 - 1)]);
+#pragma unroll
+    for (int k = PER_WORD / 2 - 2; k >= 0; --k) acc = acc * (1u << BITS) + __float_as_uint(xw[hh + 2 * k]);
+    half[hh] = acc + (uint32_t)zfold * kOnes;
+  }
+  return __byte_perm(half[0], half[1], 0x5410);
+}
+
+// min and max of n values (two new values per 3-input min / max)
+template <int N>
+__device__ __forceinline__ void min_max(const float* v, float& mn, float& mx) {
+  mn = v[0];
+  mx = v[0];
+#pragma unroll
+  for (int c = 1; c < N; c += 2) {
+    const float u = v[c], w = c + 1 < N ? v[c + 1] : u;
+    mn = fminf(mn, fminf(u, w));
+    mx = fmaxf(mx, fmaxf(u, w));
+  }
+}
+
+// One row (one token's K or V row of one head), read from its warp's staged
+// tile: d/8 16-byte chunks, chunk i of the tile's row `row` stored at
+// 16 (i ^ (row mod d/8)) so that neither the copies nor the reads of a
+// quarter-warp meet in a shared-memory bank.  fp32 butterflies in the order
+// h = 1, 2, ..., d/2 (packed fp32 pairs from h = 2 on: each lane is the same
+// correctly rounded add or subtract), per-group min/max, Eq. (1) codes,
+// packed 16-byte stores.
 template <int D, int BITS, int GROUP>
-__global__ void __launch_bounds__(kRowThreads) quantize_rows_kernel(const QuantArgs a,
-                                                                    const PairSigns sg) {
+__device__ __forceinline__ void quantize_row(const QuantArgs& a, const PairSigns& sg,
+                                             const uint8_t* tile, int row, unsigned r,
+                                             unsigned per_kv) {
   constexpr int G = D / GROUP;
   constexpr int CODE_BYTES = D * BITS / 8;
   constexpr int PER_WORD = 32 / BITS;
+  constexpr int CH = D / 8;
   const float qmax = float((1 << BITS) - 1);
 
-  const unsigned per_kv = (unsigned)a.bh * (unsigned)a.n_new;   // < 2^31 (host check)
-  const unsigned r = blockIdx.x * kRowThreads + threadIdx.x;
-  if (r >= 2u * per_kv) return;
   const bool is_v = r >= per_kv;
   const unsigned rk = is_v ? r - per_kv : r;
   const unsigned bh = rk / (unsigned)a.n_new;
   const unsigned tok = rk - bh * (unsigned)a.n_new;
 
-  const uint4* src = reinterpret_cast<const uint4*>((is_v ? a.v_new : a.k_new) + (size_t)rk * D);
+  const uint8_t* rowp = tile + row * (2 * D);
   float x[D];
 #pragma unroll
   for (int i = 0; i < D / 8; ++i) {
-    const uint4 raw = __ldg(src + i);
+    const uint4 raw = *reinterpret_cast<const uint4*>(rowp + ((i ^ (row & (CH - 1))) << 4));
     const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
-      const uint32_t ws = w[k] ^ sg.m[4 * i + k];
-      x[8 * i + 2 * k] = __uint_as_float(ws << 16);
-      x[8 * i + 2 * k + 1] = __uint_as_float(ws & 0xFFFF0000u);
+      x[8 * i + 2 * k] = __uint_as_float(w[k] << 16);               // sign applied below
+      x[8 * i + 2 * k + 1] = __uint_as_float((w[k] ^ sg.m[4 * i + k]) & 0xFFFF0000u);
     }
   }
-  // butterflies: h = 1 on scalars, then packed pairs (x_i, x_i+1)
+  // butterflies: h = 1 on scalars (with the low channel's sign), then
+  // packed pairs (x_i, x_i+1)
 #pragma unroll
   for (int i = 0; i < D; i += 2) {
     const float u = x[i], v = x[i + 1];
-    x[i] = __fadd_rn(u, v);
-    x[i + 1] = __fsub_rn(u, v);
+    x[i] = __fmaf_rn(sg.sl[i / 2], u, v);
+    x[i + 1] = __fmaf_rn(sg.sl[i / 2], u, -v);
   }
 #pragma unroll
   for (int h = 2; h < D; h <<= 1) {
@@ -109,90 +237,19 @@ __global__ void __launch_bounds__(kRowThreads) quantize_rows_kernel(const QuantA
   }
 
   uint32_t rec[G];
+  int zf[G];
 #pragma unroll
   for (int g = 0; g < G; ++g) {
-    float mn = x[GROUP * g], mx = x[GROUP * g];
-#pragma unroll
-    for (int c = 1; c < GROUP; c += 2) {
-      const float u = x[GROUP * g + c], v = c + 1 < GROUP ? x[GROUP * g + c + 1] : u;
-      mn = fminf(mn, fminf(u, v));
-      mx = fmaxf(mx, fmaxf(u, v));
-    }
-    // Eq. (1): step covering [min, max], integer zero point, both stored BF16
-    uint32_t dbits = bf16_bits_rn(__fdiv_rn(__fsub_rn(mx, mn), qmax));
-    if (bf16_value(dbits) == 0.0f) {
-      dbits = bf16_bits_rn(fabsf(mn));
-      if (bf16_value(dbits) == 0.0f) dbits = 0x3F80u;  // 1.0
-    }
-    const float delta = bf16_value(dbits);
-    const float rcp = __frcp_rn(delta);
-    const uint32_t zbits = bf16_bits_rn(__fadd_rn(rintf(__fdiv_rn(-mn, delta)), 0.0f));
-    const float zero = bf16_value(zbits);
-    rec[g] = dbits | (zbits << 16);
-
-    // codes.  Fast route: q = fl(x / delta) exactly, from the correctly
-    // rounded reciprocal r and one residual step (q0 = fl(x r), e = x - q0 delta
-    // exact by FMA, q = fl(q0 + e r): correctly rounded while nothing over- or
-    // underflows); rint(q) by adding 1.5 * 2^23 (ties to even, |q| < 2^21);
-    // the integer zero point added after the rounding.  K = 1.5 * 2^23 + code
-    // then carries the code in its low mantissa bits.  Codes are monotone in
-    // x, so those of the group's min and max bound them all and the clamp to
-    // [0, 2^B - 1] is needed only when one of those two falls outside.
-    const float kMagic = 12582912.0f;   // 1.5 * 2^23
-    const bool fast = rcp < 0x1p100f && fabsf(mn) * rcp < 0x1p21f && fabsf(mx) * rcp < 0x1p21f;
-    float* xg = x + GROUP * g;
-    if (fast) {
-      auto code_of = [&](float v) {
-        const float q0 = __fmul_rn(v, rcp);
-        const float q = __fmaf_rn(__fmaf_rn(-q0, delta, v), rcp, q0);
-        return __fadd_rn(__fadd_rn(q, kMagic), zero) - kMagic;
-      };
-      const bool clamp = code_of(mn) < 0.0f || code_of(mx) > qmax;
-      const uint64_t r2 = ptx::f2_pack(rcp, rcp);
-      const uint64_t nd2 = ptx::f2_pack(-delta, -delta);
-      const uint64_t m2 = ptx::f2_pack(kMagic, kMagic);
-      const uint64_t z2 = ptx::f2_pack(zero, zero);
-#pragma unroll
-      for (int c = 0; c < GROUP; c += 2) {
-        const uint64_t xv = ptx::f2_pack(xg[c], xg[c + 1]);
-        const uint64_t q0 = ptx::f2_mul(xv, r2);
-        const uint64_t e = ptx::f2_fma(q0, nd2, xv);
-        const uint64_t q = ptx::f2_fma(e, r2, q0);
-        ptx::f2_unpack(ptx::f2_add(ptx::f2_add(q, m2), z2), xg[c], xg[c + 1]);
-      }
-      if (clamp) {
-#pragma unroll
-        for (int c = 0; c < GROUP; ++c) xg[c] = fminf(fmaxf(xg[c], kMagic), kMagic + qmax);
-      }
-    } else {
-      // exact division element by element (huge quotients, tiny steps)
-#pragma unroll
-      for (int c = 0; c < GROUP; ++c) {
-        float t = __fadd_rn(rintf(__fdiv_rn(xg[c], delta)), zero);
-        t = fminf(fmaxf(t, 0.0f), qmax);
-        xg[c] = __fadd_rn(t, kMagic);
-      }
-    }
+    float mn, mx;
+    min_max<GROUP>(x + GROUP * g, mn, mx);
+    rec[g] = group_codes<BITS, GROUP>(x + GROUP * g, mn, mx, zf[g]);
   }
 
   // pack: channel ch = 16w + 2k + h (INT2) / 8w + 2k + h (INT4) -> bits
-  // BITS*k + 16h.  The low 16 bits of 1.5 * 2^23 are zero, so a Horner sum
-  // of the K bit patterns (times 2^BITS per code) leaves exactly the codes
-  // in the low half-word.
+  // BITS*k + 16h
   uint32_t words[D * BITS / 32];
 #pragma unroll
-  for (int w = 0; w < D * BITS / 32; ++w) {
-    uint32_t half[2];
-#pragma unroll
-    for (int hh = 0; hh < 2; ++hh) {
-      uint32_t acc = __float_as_uint(x[PER_WORD * w + hh + 2 * (PER_WORD / 2 - 1)]);
-#pragma unroll
-      for (int k = PER_WORD / 2 - 2; k >= 0; --k)
-        acc = acc * (1u << BITS) + __float_as_uint(x[PER_WORD * w + hh + 2 * k]);
-      half[hh] = acc;
-    }
-    words[w] = __byte_perm(half[0], half[1], 0x5410);
-  }
+  for (int w = 0; w < D * BITS / 32; ++w) words[w] = pack_word<BITS>(x + PER_WORD * w, zf[(PER_WORD * w) / GROUP]);
 
   const size_t dst_tok = (size_t)bh * a.cap + a.first + tok;
   uint4* dc = reinterpret_cast<uint4*>((is_v ? a.v_codes : a.k_codes) + dst_tok * CODE_BYTES);
@@ -206,6 +263,269 @@ __global__ void __launch_bounds__(kRowThreads) quantize_rows_kernel(const QuantA
     *reinterpret_cast<uint2*>(ds) = make_uint2(rec[0], rec[1 % G]);
   } else {
     ds[0] = rec[0];
+  }
+}
+
+// Each warp walks tiles of 32 consecutive rows (the K rows of all (batch,
+// head) pairs, then the V rows) with stride = all warps of the grid; the
+// next tile is copied into the warp's other shared-memory stage (each copy
+// instruction moves 32/(d/8) whole rows, 512 contiguous bytes) while the
+// current one is quantized.
+template <int D, int BITS, int GROUP>
+__global__ void __launch_bounds__(kQWarps * 32, kQBlocksPerSm)
+    quantize_rows_kernel(const QuantArgs a, const PairSigns sg) {
+  constexpr int RB = 2 * D;          // bytes of one BF16 row
+  constexpr int CH = D / 8;          // 16-byte chunks per row
+  constexpr int RPI = 32 / CH;       // rows per copy instruction
+  constexpr int TILE = 32 * RB;      // one warp's 32 rows
+  extern __shared__ __align__(16) uint8_t qsm[];
+  const int lane = threadIdx.x & 31;
+  const int wib = threadIdx.x >> 5;
+  uint8_t* stage = qsm + wib * 2 * TILE;
+  const unsigned per_kv = (unsigned)a.bh * (unsigned)a.n_new;   // < 2^30 (host check)
+  const unsigned total = 2u * per_kv;
+  const unsigned n_tiles = (total + 31u) / 32u;
+  const unsigned n_warps = gridDim.x * kQWarps;
+  auto issue = [&](unsigned tile, uint8_t* dst) {
+#pragma unroll
+    for (int j = 0; j < CH; ++j) {
+      const int row = j * RPI + lane / CH, chunk = lane % CH;
+      const unsigned r = tile * 32u + (unsigned)row;
+      if (r < total) {
+        const bool is_v = r >= per_kv;
+        const uint16_t* src = (is_v ? a.v_new : a.k_new) + (size_t)(is_v ? r - per_kv : r) * D + chunk * 8;
+        cp_async16(dst + row * RB + ((chunk ^ (row & (CH - 1))) << 4), src);
+      }
+    }
+    cp_async_commit();
+  };
+  unsigned tile = blockIdx.x * kQWarps + wib;
+  if (tile < n_tiles) issue(tile, stage);
+  for (int k = 0; tile < n_tiles; ++k, tile += n_warps) {
+    const unsigned next = tile + n_warps;
+    if (next < n_tiles) {
+      issue(next, stage + ((k + 1) & 1) * TILE);
+      cp_async_wait<1>();
+    } else {
+      cp_async_wait<0>();
+    }
+    __syncwarp();
+    const unsigned r = tile * 32u + (unsigned)lane;
+    if (r < total) quantize_row<D, BITS, GROUP>(a, sg, stage + (k & 1) * TILE, lane, r, per_kv);
+    // every lane is done with this stage before the copy two tiles on
+    __syncwarp();
+  }
+}
+
+// ---- d = 128: each row split between the two warps of a pair ----------------
+//
+// Warp HF of a pair holds channels [64 HF, 64 HF + 64) of the pair's 32 rows
+// (one row per lane), so a thread keeps 64 values instead of 128: half the
+// registers and half the code per warp.  The butterflies h = 1 .. 32 stay
+// inside a half; h = 64 pairs channel c with c + 64 across the two warps and
+// goes through shared memory: HF = 0 keeps channels [0, 32) and sends
+// [32, 64), HF = 1 keeps [96, 128) and sends [64, 96), so that afterwards
+// HF = 0 owns channels [0, 32) and [64, 96), HF = 1 owns [32, 64) and
+// [96, 128).  Groups of 32 channels then lie in one warp; groups of 64 swap
+// their partial min / max once more.
+constexpr int kSplitWarps = 4;                  // two warp pairs per block
+constexpr int kSplitBlocksPerSm = 4;
+constexpr int kSplitStages = 3;
+constexpr int kHalfRowBytes = 128;              // 64 BF16 channels
+constexpr int kSplitTile = 32 * kHalfRowBytes;  // one warp's 32 half-rows
+constexpr int kSplitSmem = kSplitWarps * (kSplitStages * kSplitTile + 32 * 4 * 4);
+
+// named barrier of one warp pair (ids 1 and 2; 0 is __syncthreads)
+__device__ __forceinline__ void pair_sync(int id) {
+  asm volatile("bar.sync %0, 64;" ::"r"(id) : "memory");
+}
+
+// 16-byte chunk i (0..7) of lane l's 128-byte slot, XOR-swizzled so that a
+// quarter-warp's eight lanes use eight different bank groups
+__device__ __forceinline__ int half_slot(int l, int i) { return l * kHalfRowBytes + ((i ^ (l & 7)) << 4); }
+
+template <int BITS, int GROUP, int HF>
+__device__ __forceinline__ void quantize_half_row(const QuantArgs& a, const PairSigns& sg,
+                                                  uint8_t* own, const uint8_t* partner,
+                                                  float* mm, const float* pmm, int lane,
+                                                  unsigned rk, bool valid, bool is_v, int bar) {
+  constexpr int H = 64, Q = 32;
+  constexpr int G = 128 / GROUP;
+  float x[H];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const uint4 raw = *reinterpret_cast<const uint4*>(own + half_slot(lane, i));
+    const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int pl = 4 * i + k, pg = HF * 32 + pl;  // pair within the half / the row
+      x[2 * pl] = __uint_as_float(w[k] << 16);      // sign applied below
+      x[2 * pl + 1] = __uint_as_float((w[k] ^ sg.m[pg]) & 0xFFFF0000u);
+    }
+  }
+#pragma unroll
+  for (int pl = 0; pl < H / 2; ++pl) {
+    const float u = x[2 * pl], v = x[2 * pl + 1];
+    x[2 * pl] = __fmaf_rn(sg.sl[HF * 32 + pl], u, v);
+    x[2 * pl + 1] = __fmaf_rn(sg.sl[HF * 32 + pl], u, -v);
+  }
+#pragma unroll
+  for (int h = 2; h < H; h <<= 1) {
+#pragma unroll
+    for (int i = 0; i < H; i += 2) {
+      if ((i & h) == 0) {
+        const uint64_t A = ptx::f2_pack(x[i], x[i + 1]);
+        const uint64_t B = ptx::f2_pack(x[i + h], x[i + h + 1]);
+        ptx::f2_unpack(ptx::f2_add(A, B), x[i], x[i + 1]);
+        ptx::f2_unpack(ptx::f2_sub(A, B), x[i + h], x[i + h + 1]);
+      }
+    }
+  }
+  // h = 64 across the pair: every lane has read its staged half-row, so the
+  // stage slot carries the 32 values the partner needs
+  constexpr int kSend = HF == 0 ? Q : 0, kKeep = HF == 0 ? 0 : Q;
+  __syncwarp();
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+    *reinterpret_cast<uint4*>(own + half_slot(lane, i)) =
+        make_uint4(__float_as_uint(x[kSend + 4 * i]), __float_as_uint(x[kSend + 4 * i + 1]),
+                   __float_as_uint(x[kSend + 4 * i + 2]), __float_as_uint(x[kSend + 4 * i + 3]));
+  pair_sync(bar);
+  // in place: x[0..32) <- channels 32 HF + j (sums), x[32..64) <- channels
+  // 64 + 32 HF + j (differences); the low channel of each butterfly first
+  const uint64_t s2 = ptx::f2_pack(a.inv_sqrt_d, a.inv_sqrt_d);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const uint4 v = *reinterpret_cast<const uint4*>(partner + half_slot(lane, i));
+    const float rv[4] = {__uint_as_float(v.x), __uint_as_float(v.y), __uint_as_float(v.z),
+                         __uint_as_float(v.w)};
+#pragma unroll
+    for (int e = 0; e < 4; e += 2) {
+      const int j = 4 * i + e;
+      const uint64_t kept = ptx::f2_pack(x[kKeep + j], x[kKeep + j + 1]);
+      const uint64_t recv = ptx::f2_pack(rv[e], rv[e + 1]);
+      const uint64_t lo = HF == 0 ? kept : recv, hi = HF == 0 ? recv : kept;
+      ptx::f2_unpack(ptx::f2_mul(ptx::f2_add(lo, hi), s2), x[j], x[j + 1]);
+      ptx::f2_unpack(ptx::f2_mul(ptx::f2_sub(lo, hi), s2), x[Q + j], x[Q + j + 1]);
+    }
+  }
+  uint32_t rec[2];
+  int zf[2];
+  if (GROUP == 32) {
+    // x[0..32) is group HF, x[32..64) group 2 + HF
+#pragma unroll
+    for (int part = 0; part < 2; ++part) {
+      float mn, mx;
+      min_max<Q>(x + Q * part, mn, mx);
+      rec[part] = group_codes<BITS, Q>(x + Q * part, mn, mx, zf[part]);
+    }
+  } else {
+    // x[0..32) is half of group 0, x[32..64) half of group 1
+    float mn[2], mx[2];
+#pragma unroll
+    for (int part = 0; part < 2; ++part) min_max<Q>(x + Q * part, mn[part], mx[part]);
+    *reinterpret_cast<float4*>(mm + 4 * lane) = make_float4(mn[0], mx[0], mn[1], mx[1]);
+    pair_sync(bar);
+    const float4 o = *reinterpret_cast<const float4*>(pmm + 4 * lane);
+    mn[0] = fminf(mn[0], o.x);
+    mx[0] = fmaxf(mx[0], o.y);
+    mn[1] = fminf(mn[1], o.z);
+    mx[1] = fmaxf(mx[1], o.w);
+#pragma unroll
+    for (int part = 0; part < 2; ++part)
+      rec[part] = group_codes<BITS, Q>(x + Q * part, mn[part], mx[part], zf[part]);
+  }
+  if (!valid) return;
+  const unsigned bh = rk / (unsigned)a.n_new;
+  const unsigned tok = rk - bh * (unsigned)a.n_new;
+  const size_t dst_tok = (size_t)bh * a.cap + a.first + tok;
+  // codes: channels [32 HF, 32 HF + 32) and [64 + 32 HF, ...) -> bytes
+  // [4 HF BITS, ...) and [8 BITS + 4 HF BITS, ...)
+  constexpr int PER_WORD = 32 / BITS;
+  constexpr int WPP = Q / PER_WORD;   // words per 32-channel part
+  uint8_t* dc = (is_v ? a.v_codes : a.k_codes) + dst_tok * (128 * BITS / 8);
+#pragma unroll
+  for (int part = 0; part < 2; ++part) {
+    uint32_t wd[WPP];
+#pragma unroll
+    for (int w = 0; w < WPP; ++w) wd[w] = pack_word<BITS>(x + Q * part + PER_WORD * w, zf[part]);
+    uint8_t* d = dc + (part * 64 + HF * 32) * BITS / 8;
+    if (WPP == 2) {
+      *reinterpret_cast<uint2*>(d) = make_uint2(wd[0], wd[1 % WPP]);
+    } else {
+      *reinterpret_cast<uint4*>(d) = make_uint4(wd[0], wd[1 % WPP], wd[2 % WPP], wd[3 % WPP]);
+    }
+  }
+  uint32_t* ds = (is_v ? a.v_sz : a.k_sz) + dst_tok * G;
+  if (GROUP == 32) {
+    ds[HF] = rec[0];
+    ds[2 + HF] = rec[1];
+  } else if (HF == 0) {
+    *reinterpret_cast<uint2*>(ds) = make_uint2(rec[0], rec[1]);
+  }
+}
+
+// Warp pairs walk tiles of 32 consecutive rows of one tensor (the K rows of
+// all (batch, head) pairs in tiles [0, T), then the V rows in tiles [T, 2T))
+// with stride = all pairs of the grid; each warp copies its half of the next
+// tile (128-byte runs) into the next of its three shared-memory stages while
+// it works on the current one.  Three stages because a stage slot also
+// carries the h = 64 exchange: the copy into it waits until the partner has
+// passed the following exchange.
+template <int BITS, int GROUP>
+__global__ void __launch_bounds__(kSplitWarps * 32, kSplitBlocksPerSm)
+    quantize_split_kernel(const QuantArgs a, const PairSigns sg) {
+  extern __shared__ __align__(16) uint8_t qsm[];
+  const int lane = threadIdx.x & 31;
+  const int wib = threadIdx.x >> 5;
+  const int hf = wib & 1;
+  uint8_t* stages = qsm + wib * kSplitStages * kSplitTile;
+  const uint8_t* pstages = qsm + (wib ^ 1) * kSplitStages * kSplitTile;
+  float* mm_base = reinterpret_cast<float*>(qsm + kSplitWarps * kSplitStages * kSplitTile);
+  float* mm = mm_base + wib * 128;
+  const float* pmm = mm_base + (wib ^ 1) * 128;
+  const unsigned per_kv = (unsigned)a.bh * (unsigned)a.n_new;   // < 2^30 (host check)
+  const unsigned tiles_per = (per_kv + 31u) / 32u;
+  const unsigned n_tiles = 2u * tiles_per;
+  const unsigned n_pairs = gridDim.x * (kSplitWarps / 2);
+  // this lane's share of a copy: rows 4j + lane / 8, chunk lane % 8
+  const int crow = lane >> 3, cchunk = lane & 7;
+  const int src_lane = crow * 128 + hf * 64 + cchunk * 8;   // BF16 elements
+  const int dst_even = half_slot(crow, cchunk), dst_odd = half_slot(crow + 4, cchunk);
+  auto issue = [&](unsigned tile, uint8_t* dst) {
+    const bool v = tile >= tiles_per;
+    const unsigned row0 = (v ? tile - tiles_per : tile) * 32u;
+    const uint16_t* src = (v ? a.v_new : a.k_new) + (size_t)row0 * 128 + src_lane;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      if (row0 + 4u * j + (unsigned)crow < per_kv)
+        cp_async16(dst + 512 * (j & ~1) + ((j & 1) ? dst_odd : dst_even), src + 512 * j);
+    }
+    cp_async_commit();
+  };
+  unsigned tile = blockIdx.x * (kSplitWarps / 2) + (wib >> 1);
+  if (tile < n_tiles) issue(tile, stages);
+  int s = 0;
+  for (int k = 0; tile < n_tiles; ++k, tile += n_pairs) {
+    const unsigned next = tile + n_pairs;
+    const int sn = s == kSplitStages - 1 ? 0 : s + 1;
+    if (next < n_tiles) {
+      issue(next, stages + sn * kSplitTile);
+      cp_async_wait<1>();
+    } else {
+      cp_async_wait<0>();
+    }
+    __syncwarp();
+    const bool is_v = tile >= tiles_per;
+    const unsigned rk = (is_v ? tile - tiles_per : tile) * 32u + (unsigned)lane;
+    const bool valid = rk < per_kv;
+    uint8_t* own = stages + s * kSplitTile;
+    const uint8_t* par = pstages + s * kSplitTile;
+    const int bar = 1 + (wib >> 1);
+    if (hf == 0) quantize_half_row<BITS, GROUP, 0>(a, sg, own, par, mm, pmm, lane, rk, valid, is_v, bar);
+    else quantize_half_row<BITS, GROUP, 1>(a, sg, own, par, mm, pmm, lane, rk, valid, is_v, bar);
+    __syncwarp();
+    s = sn;
   }
 }
 
@@ -289,11 +609,31 @@ cudaError_t launch_q(const QuantArgs& a, cudaStream_t s) {
     const uint32_t s0 = c0 < D ? (a.sign_bits[c0 >> 5] >> (c0 & 31)) & 1u : 0u;
     const uint32_t s1 = c1 < D ? (a.sign_bits[c1 >> 5] >> (c1 & 31)) & 1u : 0u;
     sg.m[i] = (s0 << 15) | (s1 << 31);
+    sg.sl[i] = s0 ? -1.0f : 1.0f;
   }
   const long long rows = 2LL * a.bh * a.n_new;
-  const unsigned blocks = (unsigned)((rows + kRowThreads - 1) / kRowThreads);
-  quantize_rows_kernel<D, BITS, GROUP><<<blocks, kRowThreads, 0, s>>>(a, sg);
-  return cudaGetLastError();
+  if (rows == 0) return cudaSuccess;
+  const long long tiles = (rows + 31) / 32;
+  if constexpr (D == 128) {
+    const long long want = (tiles + 1) / 2;
+    const long long cap = (long long)sm_count() * kSplitBlocksPerSm;
+    const unsigned blocks = (unsigned)(want < cap ? want : cap);
+    static std::atomic<uint64_t> limit_set{0};   // per template instance and device
+    const cudaError_t e = ensure_smem_limit(quantize_split_kernel<BITS, GROUP>, kSplitSmem, limit_set);
+    if (e != cudaSuccess) return e;
+    quantize_split_kernel<BITS, GROUP><<<blocks, kSplitWarps * 32, kSplitSmem, s>>>(a, sg);
+    return cudaGetLastError();
+  } else {
+    const long long want = (tiles + kQWarps - 1) / kQWarps;
+    const long long cap = (long long)sm_count() * kQBlocksPerSm;
+    const unsigned blocks = (unsigned)(want < cap ? want : cap);
+    const int smem = kQWarps * 2 * 32 * 2 * D;
+    static std::atomic<uint64_t> limit_set{0};   // per template instance and device
+    const cudaError_t e = ensure_smem_limit(quantize_rows_kernel<D, BITS, GROUP>, smem, limit_set);
+    if (e != cudaSuccess) return e;
+    quantize_rows_kernel<D, BITS, GROUP><<<blocks, kQWarps * 32, smem, s>>>(a, sg);
+    return cudaGetLastError();
+  }
 }
 
 }  // namespace
