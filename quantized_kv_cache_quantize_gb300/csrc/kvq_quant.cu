@@ -131,13 +131,20 @@ __device__ __forceinline__ uint32_t group_codes(float* xg, float mn, float mx, i
     }
   } else {
     zfold = 0;
-    // exact division element by element (huge quotients, tiny steps)
+    // exact division element by element (huge quotients, tiny steps): a rare
+    // path, kept as one rolled loop over a local copy so that its divisions
+    // do not sit unrolled in the kernel's hot code
+    float tmp[N];
 #pragma unroll
+    for (int c = 0; c < N; ++c) tmp[c] = xg[c];
+#pragma unroll 1
     for (int c = 0; c < N; ++c) {
-      float t = __fadd_rn(rintf(__fdiv_rn(xg[c], delta)), zero);
+      float t = __fadd_rn(rintf(__fdiv_rn(tmp[c], delta)), zero);
       t = fminf(fmaxf(t, 0.0f), qmax);
-      xg[c] = __fadd_rn(t, kMagic);
+      tmp[c] = __fadd_rn(t, kMagic);
     }
+#pragma unroll
+    for (int c = 0; c < N; ++c) xg[c] = tmp[c];
   }
   return dbits | (zbits << 16);
 }
@@ -345,7 +352,7 @@ __device__ __forceinline__ void pair_sync(int id) {
 __device__ __forceinline__ int half_slot(int l, int i) { return l * kHalfRowBytes + ((i ^ (l & 7)) << 4); }
 
 template <int BITS, int GROUP, int HF>
-__device__ __forceinline__ void quantize_half_row(const QuantArgs& a, const PairSigns& sg,
+__device__ __forceinline__ void quantize_half_row(const QuantArgs& a, const PairSigns sg,
                                                   uint8_t* own, const uint8_t* partner,
                                                   float* mm, const float* pmm, int lane,
                                                   unsigned rk, bool valid, bool is_v, int bar) {
