@@ -198,20 +198,31 @@ __device__ __forceinline__ void write_ext_row(uint8_t* tile, int r, const float 
 }
 
 // The code pair k of a packed word (low code at bit BITS*k, high code 16 bits
-// up) moved to bits [6, 6 + BITS) of each 16-bit half and ORed into FP16 16.0
-// (0x4C00, unit 1/64): each half is then exactly 16 + code.
+// up), ORed into an FP16 constant of each half so that the half reads
+// exactly magic + code.  INT2: a code at bits [6, 8) of a half under 16.0
+// (0x4C00, unit 1/64) or at bits [8, 10) under 4.0 (0x4400, unit 1/256) has
+// weight 1, so one shifted copy of the word serves two pairs: w << 6 (pairs
+// 0, 1), w << 2 (2), w (3, 4), w >> 4 (5, 6), w >> 8 (7); four shifts per
+// word.  INT4: bits [6, 10) under 16.0, one shift per pair.
+template <int BITS>
+__device__ __forceinline__ int pair_magic(int k) {   // 16 or 4
+  return BITS == 4 ? 16 : ((k == 1 || k == 4 || k == 6) ? 4 : 16);
+}
 template <int BITS>
 __device__ __forceinline__ uint32_t code_pair_f16(uint32_t w, int k) {
-  const int pos = BITS * k;
-  const uint32_t t = pos <= 6 ? (w << (6 - pos)) : (w >> (pos - 6));
-  const uint32_t mask = BITS == 2 ? 0x00C000C0u : 0x03C003C0u;
-  return (t & mask) | 0x4C004C00u;
+  if (BITS == 4) {
+    const int pos = 4 * k;
+    const uint32_t t = pos <= 6 ? (w << (6 - pos)) : (w >> (pos - 6));
+    return (t & 0x03C003C0u) | 0x4C004C00u;
+  }
+  const uint32_t t = k <= 1 ? (w << 6) : k == 2 ? (w << 2) : k <= 4 ? w : k <= 6 ? (w >> 4) : (w >> 8);
+  return pair_magic<2>(k) == 4 ? ((t & 0x03000300u) | 0x44004400u) : ((t & 0x00C000C0u) | 0x4C004C00u);
 }
 
 // Dequantize one packed key row into row r of a swizzled FP16 tile.
-// ZERO = false (keys): code * D = (16 + code) D - 16 D in one FMA, exact for
-// INT2.  ZERO = true (values): (code - z) * D, the integer difference exact,
-// one rounding of the product.
+// ZERO = false (keys): code * D = (magic + code) D - magic D in one FMA,
+// exact for INT2.  ZERO = true (values): (code - z) * D, the integer
+// difference exact, one rounding of the product.
 template <int D, int BITS, int GROUP, bool ZERO>
 __device__ __forceinline__ void dequant_row(const uint32_t (&words)[D * BITS / 32],
                                             const uint32_t (&sz)[D / GROUP], uint8_t* tile,
@@ -220,13 +231,14 @@ __device__ __forceinline__ void dequant_row(const uint32_t (&words)[D * BITS / 3
   for (int c = 0; c < D / 8; ++c) {
     const int g = (8 * c) / GROUP;
     const __half2 d2 = __float2half2_rn(bf16_lo(sz[g]));
-    const __half2 k2 = ZERO ? __float2half2_rn(16.0f + bf16_hi(sz[g]))
-                            : __float2half2_rn(-16.0f * bf16_lo(sz[g]));
     uint32_t out[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      const uint32_t v = BITS == 2 ? code_pair_f16<2>(words[c >> 1], 4 * (c & 1) + i)
-                                   : code_pair_f16<4>(words[c], i);
+      const int k = BITS == 2 ? 4 * (c & 1) + i : i;
+      const float mg = (float)pair_magic<BITS>(k);
+      const __half2 k2 = ZERO ? __float2half2_rn(mg + bf16_hi(sz[g]))
+                              : __float2half2_rn(-mg * bf16_lo(sz[g]));
+      const uint32_t v = BITS == 2 ? code_pair_f16<2>(words[c >> 1], k) : code_pair_f16<4>(words[c], k);
       const __half2 res = ZERO ? __hmul2(__hsub2(as_h2(v), k2), d2) : __hfma2(as_h2(v), d2, k2);
       out[i] = as_u32(res);
     }
