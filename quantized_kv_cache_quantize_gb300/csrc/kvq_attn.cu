@@ -416,7 +416,7 @@ __global__ void __launch_bounds__(Cfg<D, NQ, PRECISE>::kThreads, 1)
       const float m_in = m;
       const uint64_t sl2x2 = ptx::f2_pack(sl2, sl2);
       uint64_t acc = ptx::f2_pack(0.f, 0.f);
-#pragma unroll 1
+#pragma unroll 2
       for (int c = 0; c < kBlockN / 32; ++c) {
         uint32_t cur[32];
         ptx::tmem_ld32(t_s + 32 * c, cur);
