@@ -198,7 +198,6 @@ __device__ __forceinline__ void quantize_row(const QuantArgs& a, const PairSigns
   constexpr int CODE_BYTES = D * BITS / 8;
   constexpr int PER_WORD = 32 / BITS;
   constexpr int CH = D / 8;
-  const float qmax = float((1 << BITS) - 1);
 
   const bool is_v = r >= per_kv;
   const unsigned rk = is_v ? r - per_kv : r;
