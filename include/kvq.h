@@ -59,6 +59,14 @@ typedef enum {
  *   extreme outliers (scores of order 100).  No counterpart in the paper.
  */
 #define KVQ_FLAG_PRECISE_QUERY 1
+/*
+ * KVQ_FLAG_NO_KV_SPLIT: when batch * heads * query tiles do not fill the GPU
+ * (small chunks), the attention divides the key tiles among several CTAs
+ * per query tile and merges their partial softmax states (an implementation
+ * choice of this library, not part of the method).  This flag turns the
+ * split off (for comparisons).
+ */
+#define KVQ_FLAG_NO_KV_SPLIT 2
 
 /*
  * Quantized sliding-window KV cache (paper section 1: the current chunk
@@ -129,8 +137,10 @@ kvq_status kvq_quantize_append(kvq_cache *cache, const uint16_t *k_new,
 
 /*
  * Workspace bytes kvq_attention_corrected / kvq_attention_mass need for n_q
- * queries and n_r current-chunk tokens (rotated BF16 copies of q, k_cur,
- * v_cur).  0 on a bad geometry.
+ * queries and n_r current-chunk tokens: the rotated query (FP16 high and low
+ * parts), the rotated current values (FP16) and, when the launch would not
+ * fill the current device, the partial results of the key-range split
+ * (fp32).  Depends on the current device's SM count.  0 on a bad geometry.
  */
 size_t kvq_workspace_bytes(const kvq_cache *cache, int32_t n_q, int32_t n_r);
 
@@ -146,13 +156,14 @@ size_t kvq_workspace_bytes(const kvq_cache *cache, int32_t n_q, int32_t n_r);
  *          (exact products, fp32 accumulation);
  *   one softmax over both segments; out = sum_i p_ij v_i in the ORIGINAL
  *   basis (cached values un-rotated).
- * flags: 0 or KVQ_FLAG_PRECISE_QUERY.
+ * flags: 0, KVQ_FLAG_PRECISE_QUERY, KVQ_FLAG_NO_KV_SPLIT or both.
  * out: BF16 [batch][heads][n_q][d] device (required).  p_s, p_r: optional
  * (NULL to skip) fp32 [batch][heads][n_q] device: the attention masses of the
  * cached block and of the current chunk per query row (Figure 2 caption).
  * workspace: device, >= kvq_workspace_bytes(cache, n_q, n_r) bytes, 16-byte
  * aligned; its contents are scratch (the rotated query as FP16 high and low
- * parts and the rotated current values in FP16: tensor-core operands).
+ * parts and the rotated current values in FP16: tensor-core operands; the
+ * key-range split's partial results).
  * Values after rotation must stay within the FP16 range (|x| < 65504).  Requires cache->len + n_r >= 1 when
  * n_q > 0.  n_q == 0 is a no-op.
  */

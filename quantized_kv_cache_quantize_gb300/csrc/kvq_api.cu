@@ -86,19 +86,56 @@ struct Workspace {
   uint16_t* q_hi;  // rotated queries, FP16
   uint16_t* q_lo;  // FP16 remainder of the rotated queries
   uint16_t* v;     // rotated current-chunk values, FP16
+  float* o_part;   // key-range split: partial O, fp32 (splits > 1)
+  float* st_part;  // key-range split: base and sums per row (splits > 1)
   size_t bytes;
 };
 
-Workspace carve(void* base, const kvq::Geometry& g, int n_q, int n_r) {
+Workspace carve(void* base, const kvq::Geometry& g, int n_q, int n_r, int splits) {
   Workspace w;
   const size_t qb = round_up((size_t)g.bh * n_q * g.d * 2, 256);
   const size_t rb = round_up((size_t)g.bh * n_r * g.d * 2, 256);
+  const size_t ob = splits > 1 ? round_up((size_t)splits * g.bh * n_q * g.d * 4, 256) : 0;
+  const size_t sb = splits > 1 ? round_up((size_t)splits * g.bh * n_q * 3 * 4, 256) : 0;
   uint8_t* p = static_cast<uint8_t*>(base);
   w.q_hi = reinterpret_cast<uint16_t*>(p);
   w.q_lo = reinterpret_cast<uint16_t*>(p + qb);
   w.v = reinterpret_cast<uint16_t*>(p + 2 * qb);
-  w.bytes = 2 * qb + rb;
+  w.o_part = reinterpret_cast<float*>(p + 2 * qb + rb);
+  w.st_part = reinterpret_cast<float*>(p + 2 * qb + rb + ob);
+  w.bytes = 2 * qb + rb + ob + sb;
   return w;
+}
+
+int device_sm_count() {
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  return sms;
+}
+
+// key-range split of one launch (1 = none); rows per CTA: 256, or 128 with
+// the precise-query flag
+int split_for(const kvq::Geometry& g, int n_q, int n_s, int n_r, bool precise, int sms,
+              int* per) {
+  int splits = 1;
+  kvq::attention_split(g.bh, n_q, n_s, n_r, precise ? 128 : 256, sms, &splits, per);
+  return splits;
+}
+
+// workspace for either query mode and any window length up to n_s: sized for
+// the largest split the current device would use (the split bound grows with
+// the tile count; the split actually taken never exceeds it)
+size_t workspace_bytes_any(const kvq::Geometry& g, int n_q, int n_s, int n_r) {
+  const int sms = device_sm_count();
+  const int n_t = (n_s + 127) / 128 + (n_r + 127) / 128;
+  size_t best = 0;
+  for (int precise = 0; precise < 2; ++precise) {
+    const int sp = kvq::attention_split_bound(g.bh, n_q, n_t, precise ? 128 : 256, sms);
+    const size_t b = carve(nullptr, g, n_q, n_r, sp).bytes;
+    if (b > best) best = b;
+  }
+  return best;
 }
 
 kvq_status attention_common(const kvq_cache* cache, const uint16_t* q, const uint16_t* k_cur,
@@ -111,7 +148,7 @@ kvq_status attention_common(const kvq_cache* cache, const uint16_t* q, const uin
   if (st != KVQ_OK) return st;
   if (n_q < 0 || n_r < 0 || n_q > (1 << 30) || n_r > (1 << 30)) return KVQ_ERR_INVALID_ARG;
   if (corr != KVQ_CORR_NONE && corr != KVQ_CORR_TAYLOR) return KVQ_ERR_INVALID_ARG;
-  if ((flags & ~KVQ_FLAG_PRECISE_QUERY) != 0) return KVQ_ERR_INVALID_ARG;
+  if ((flags & ~(KVQ_FLAG_PRECISE_QUERY | KVQ_FLAG_NO_KV_SPLIT)) != 0) return KVQ_ERR_INVALID_ARG;
   const bool precise = (flags & KVQ_FLAG_PRECISE_QUERY) != 0;
   if (!std::isfinite(scale) || scale <= 0.f) return KVQ_ERR_INVALID_ARG;
   if ((p_s == nullptr) != (p_r == nullptr)) return KVQ_ERR_INVALID_ARG;
@@ -129,7 +166,13 @@ kvq_status attention_common(const kvq_cache* cache, const uint16_t* q, const uin
       (out && !aligned16(out)) || !aligned16(workspace))
     return KVQ_ERR_ALIGNMENT;
   if (workspace == nullptr) return KVQ_ERR_INVALID_ARG;
-  const Workspace ws = carve(workspace, g, n_q, n_r);
+  // key-range split when the grid would not fill the device (and the
+  // workspace holds the partial results; otherwise one range)
+  int per = 0, splits = 1;
+  if ((flags & KVQ_FLAG_NO_KV_SPLIT) == 0)
+    splits = split_for(g, n_q, cache->len, n_r, precise, device_sm_count(), &per);
+  if (splits > 1 && workspace_bytes < carve(nullptr, g, n_q, n_r, splits).bytes) splits = 1;
+  const Workspace ws = carve(workspace, g, n_q, n_r, splits);
   if (workspace_bytes < ws.bytes) return KVQ_ERR_INVALID_ARG;
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -175,6 +218,10 @@ kvq_status attention_common(const kvq_cache* cache, const uint16_t* q, const uin
   a.p_r = p_r;
   for (int i = 0; i < 4; ++i) a.sign_bits[i] = cache->sign_bits[i];
   a.wait_limit_ns = g_wait_limit_ns.load();
+  a.splits = splits;
+  a.tiles_per_split = per;
+  a.o_part = ws.o_part;
+  a.st_part = ws.st_part;
   ProfScope prof(2, s);
   return kvq::launch_attention(a, g.d, g.bits, g.group, s);
 }
@@ -260,7 +307,8 @@ kvq_status kvq_quantize_append(kvq_cache* cache, const uint16_t* k_new, const ui
 size_t kvq_workspace_bytes(const kvq_cache* cache, int32_t n_q, int32_t n_r) {
   kvq::Geometry g;
   if (check_geometry(cache, &g) != KVQ_OK || n_q < 0 || n_r < 0) return 0;
-  return carve(nullptr, g, n_q, n_r).bytes;
+  // the split is sized for a full window (len can only grow up to capacity)
+  return workspace_bytes_any(g, n_q, g.cap, n_r);
 }
 
 kvq_status kvq_attention_corrected(const kvq_cache* cache, const uint16_t* q,
@@ -393,7 +441,7 @@ extern "C" kvq_status kvq_attention_corrected_noalloc(const kvq_cache* cache, co
   const kvq_status st = check_geometry(cache, &g);
   if (st != KVQ_OK) return st;
   if (n_q < 0 || n_r < 0) return KVQ_ERR_INVALID_ARG;
-  if (carve(nullptr, g, n_q, n_r).bytes > (size_t)KVQ_NOALLOC_SCRATCH_BYTES) return KVQ_ERR_TOO_LARGE;
+  if (carve(nullptr, g, n_q, n_r, 1).bytes > (size_t)KVQ_NOALLOC_SCRATCH_BYTES) return KVQ_ERR_TOO_LARGE;
   void* scratch = nullptr;
   const kvq_status sst = noalloc_scratch(&scratch);
   if (sst != KVQ_OK) return sst;

@@ -47,6 +47,7 @@
 
 #include <mutex>
 
+#include "kvq_fwht.cuh"
 #include "kvq_internal.h"
 #include "kvq_sm100.cuh"
 
@@ -72,6 +73,12 @@ struct AttnParams {
   uint32_t sign_bits[4];
   float inv_sqrt_d;
   unsigned long long wait_limit_ns;
+  // key-range split (blockIdx.z = split): each CTA walks key tiles
+  // [z * tiles_per_split, ...) of the cached tiles followed by the current
+  // ones; with o_part set it leaves partial results for the merge kernel
+  int tiles_per_split;
+  float* o_part;    // [splits][B*H][n_q][D] fp32, unnormalized, rotated basis
+  float* st_part;   // [splits][B*H][n_q][3]: base m (log2 units), l_S, l_R
 };
 
 constexpr int kBlockM = 128;
@@ -331,8 +338,17 @@ __global__ void __launch_bounds__(Cfg<D, NQ, PRECISE>::kThreads, 1)
   ptx::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  const int n_ct = (p.n_s + kBlockN - 1) / kBlockN;
-  const int n_t = n_ct + (p.n_r + kBlockN - 1) / kBlockN;
+  // this CTA's key tiles: [jb, je) of the cached tiles followed by the
+  // current ones; n_t, n_ct and every loop index below are local to the
+  // range, kb and cb map them back to cached / current tile numbers
+  const int n_ct_all = (p.n_s + kBlockN - 1) / kBlockN;
+  const int n_t_all = n_ct_all + (p.n_r + kBlockN - 1) / kBlockN;
+  const int jb = blockIdx.z * p.tiles_per_split;
+  const int je = min(n_t_all, jb + p.tiles_per_split);
+  const int n_t = max(0, je - jb);
+  const int n_ct = max(0, min(n_ct_all, je) - jb);
+  const int kb = jb;                        // cached tile = kb + j for j < n_ct
+  const int cb = max(0, jb - n_ct_all);     // current tile = cb + (j - n_ct) for j >= n_ct
   const bool mass_only = p.mass_only != 0;
   const unsigned long long lim = p.wait_limit_ns;
 
@@ -404,8 +420,8 @@ __global__ void __launch_bounds__(Cfg<D, NQ, PRECISE>::kThreads, 1)
         break;
       }
       ptx::tc_fence_after();
-      const int nv = j < n_ct ? min(kBlockN, p.n_s - j * kBlockN)
-                              : min(kBlockN, p.n_r - (j - n_ct) * kBlockN);
+      const int nv = j < n_ct ? min(kBlockN, p.n_s - (kb + j) * kBlockN)
+                              : min(kBlockN, p.n_r - (cb + j - n_ct) * kBlockN);
       // One pass over the tile, 32 columns at a time, with the running base
       // m: P = 2^(s * scale * log2(e) - m).  The base only has to keep every
       // P inside the FP16 range, so it is raised only when a chunk's sum of
@@ -495,7 +511,32 @@ __global__ void __launch_bounds__(Cfg<D, NQ, PRECISE>::kThreads, 1)
     const int row = q0 + q * kBlockM + r;
     if (ok) ok = wait_bar(BAR(kBarODone + q), 0, lim, abort);
     ok = __all_sync(0xffffffffu, ok && !*abort);
-    if (ok) {
+    if (ok && p.o_part != nullptr) {
+      // key-range split: the unnormalized O' (rotated basis), the base and
+      // both running sums of this range, for the merge kernel
+      ptx::tc_fence_after();
+      const bool store = row < p.n_q;
+      const size_t base = ((size_t)blockIdx.z * gridDim.y + bh) * p.n_q + (store ? row : 0);
+      if (!mass_only) {
+        float4* dst = reinterpret_cast<float4*>(p.o_part + base * D);
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t v[32];
+          ptx::tmem_ld32(t_o + 32 * c, v);
+          if (store) {
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+              dst[8 * c + e] = make_float4(__uint_as_float(v[4 * e]), __uint_as_float(v[4 * e + 1]),
+                                           __uint_as_float(v[4 * e + 2]), __uint_as_float(v[4 * e + 3]));
+          }
+        }
+      }
+      if (store) {
+        p.st_part[base * 3] = m;
+        p.st_part[base * 3 + 1] = l_s;
+        p.st_part[base * 3 + 2] = l_r;
+      }
+    } else if (ok) {
       ptx::tc_fence_after();
       const float inv = 1.0f / (l_s + l_r);
       if (!mass_only) {
@@ -587,8 +628,8 @@ __global__ void __launch_bounds__(Cfg<D, NQ, PRECISE>::kThreads, 1)
       for (int i = 0; i < NW; ++i) kw[i] = vw[i] = 0u;
 #pragma unroll
       for (int g = 0; g < G; ++g) ksz[g] = vsz[g] = 0u;
-      if (j >= n_ct || j * kBlockN + r >= p.n_s) return;
-      const size_t tok = head_tok + j * kBlockN + r;
+      if (j >= n_ct || (kb + j) * kBlockN + r >= p.n_s) return;
+      const size_t tok = head_tok + (size_t)(kb + j) * kBlockN + r;
       const uint4* kc = reinterpret_cast<const uint4*>(p.k_codes + tok * CB);
 #pragma unroll
       for (int i = 0; i < NW / 4; ++i) {
@@ -613,7 +654,7 @@ __global__ void __launch_bounds__(Cfg<D, NQ, PRECISE>::kThreads, 1)
     for (int j = 0; j < n_ct; ++j) {
       if (*abort) break;
       const int s = j & 1;
-      const bool valid = j * kBlockN + r < p.n_s;
+      const bool valid = (kb + j) * kBlockN + r < p.n_s;
       if (j >= 2 && !wait_bar(BAR(kBarEmpty + s), ((j >> 1) - 1) & 1, lim, abort)) break;
       uint8_t* st = smem + C::kStages + s * C::kStageBytes;
       float cx[16], cz[16];
@@ -819,7 +860,7 @@ __global__ void __launch_bounds__(Cfg<D, NQ, PRECISE>::kThreads, 1)
           q_orig_issued = true;
         }
         if (j >= 2 && !wait_bar(BAR(kBarEmpty + s), ((j >> 1) - 1) & 1, lim, abort)) break;
-        const int key0 = (j - n_ct) * kBlockN;
+        const int key0 = (cb + j - n_ct) * kBlockN;
         const uint32_t st = s_base + C::kStages + s * C::kStageBytes;
         ptx::mbar_expect_tx(BAR(kBarFullTma + s), (mass_only ? 1 : 2) * NKH * kHalf);
         for (int h = 0; h < NKH; ++h) {
@@ -851,6 +892,92 @@ __global__ void __launch_bounds__(Cfg<D, NQ, PRECISE>::kThreads, 1)
     ptx::tmem_dealloc(tmem, C::kTCols);
   }
 #undef BAR
+}
+
+// ---- key-range split: merge of the partial results -------------------------
+//
+// Every key range left its unnormalized O'_s (rotated basis), base m_s (log2
+// units) and running sums l_S,s, l_R,s.  With m* = max_s m_s and
+// w_s = 2^(m_s - m*):  O' = sum_s w_s O'_s / L, L = sum_s w_s (l_S,s + l_R,s),
+// P_S = sum_s w_s l_S,s / L, P_R = sum_s w_s l_R,s / L -- the online-softmax
+// combination of disjoint key sets -- then O = H^T O' (inverse rotation) to
+// BF16.  A row is held by d/8 lanes, 8 channels each.
+struct MergeArgs {
+  const float* o_part;
+  const float* st_part;
+  int splits;
+  long long rows;      // (B*H) * n_q
+  uint16_t* out;
+  float* p_s;
+  float* p_r;
+  uint32_t sign_bits[4];
+  float inv_sqrt_d;
+  int mass_only;
+};
+
+template <int D>
+__global__ void __launch_bounds__(256) merge_splits_kernel(const MergeArgs a) {
+  constexpr int LPR = D / 8;
+  constexpr int RPW = 32 / LPR;
+  const int lane = threadIdx.x & 31;
+  const int t = lane % LPR;
+  const long long warp0 = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const long long nwarps = ((long long)gridDim.x * blockDim.x) >> 5;
+  const int ch0 = 8 * t;
+  // (selects, not a run-time index into the parameter array)
+  const int wi = ch0 >> 5;
+  const uint32_t sw = (wi == 0 ? a.sign_bits[0] : wi == 1 ? a.sign_bits[1]
+                       : wi == 2 ? a.sign_bits[2] : a.sign_bits[3]) >> (ch0 & 31);
+  for (long long r0 = warp0 * RPW; r0 < a.rows; r0 += nwarps * RPW) {
+    const long long r = r0 + lane / LPR;
+    const bool valid = r < a.rows;
+    const long long rr = valid ? r : 0;
+    // one pass over the ranges with a running base (loads of four ranges in
+    // flight at a time)
+    float mst = -INFINITY, ls = 0.f, lr = 0.f, o[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) o[e] = 0.f;
+#pragma unroll 4
+    for (int s = 0; s < a.splits; ++s) {
+      const float* st = a.st_part + (s * a.rows + rr) * 3;
+      const float ms = st[0], ss = st[1], sr = st[2];
+      float4 v0 = make_float4(0.f, 0.f, 0.f, 0.f), v1 = v0;
+      if (!a.mass_only) {
+        const float4* src = reinterpret_cast<const float4*>(a.o_part + (s * a.rows + rr) * D + ch0);
+        v0 = src[0];
+        v1 = src[1];
+      }
+      const float mn = fmaxf(mst, ms);
+      const float c_old = mst == -INFINITY ? 0.f : exp2f(mst - mn);
+      const float w = ms == -INFINITY ? 0.f : exp2f(ms - mn);
+      mst = mn;
+      ls = fmaf(w, ss, ls * c_old);
+      lr = fmaf(w, sr, lr * c_old);
+      o[0] = fmaf(w, v0.x, o[0] * c_old); o[1] = fmaf(w, v0.y, o[1] * c_old);
+      o[2] = fmaf(w, v0.z, o[2] * c_old); o[3] = fmaf(w, v0.w, o[3] * c_old);
+      o[4] = fmaf(w, v1.x, o[4] * c_old); o[5] = fmaf(w, v1.y, o[5] * c_old);
+      o[6] = fmaf(w, v1.z, o[6] * c_old); o[7] = fmaf(w, v1.w, o[7] * c_old);
+    }
+    const float inv = 1.0f / (ls + lr);
+    if (!a.mass_only) {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) o[e] *= inv;
+      fwht_row<LPR>(o, t);   // all lanes: warp-collective shuffles
+      uint32_t pk[4];
+#pragma unroll
+      for (int e = 0; e < 8; e += 2) {
+        const float v0 = o[e] * (((sw >> e) & 1u) ? -a.inv_sqrt_d : a.inv_sqrt_d);
+        const float v1 = o[e + 1] * (((sw >> (e + 1)) & 1u) ? -a.inv_sqrt_d : a.inv_sqrt_d);
+        __nv_bfloat162 b = __floats2bfloat162_rn(v0, v1);
+        pk[e / 2] = *reinterpret_cast<uint32_t*>(&b);
+      }
+      if (valid) *reinterpret_cast<uint4*>(a.out + r * D + ch0) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+    }
+    if (valid && t == 0 && a.p_s != nullptr) {
+      a.p_s[r] = ls * inv;
+      a.p_r[r] = lr * inv;
+    }
+  }
 }
 
 __global__ void wait_selftest_kernel(unsigned long long limit_ns) {
@@ -940,9 +1067,31 @@ kvq_status launch_t(const AttnLaunch& a, cudaStream_t stream) {
   for (int i = 0; i < 4; ++i) p.sign_bits[i] = a.sign_bits[i];
   p.inv_sqrt_d = (float)(1.0 / sqrt((double)D));
   p.wait_limit_ns = a.wait_limit_ns;
-  dim3 grid((a.n_q + kBlockM * NQ - 1) / (kBlockM * NQ), a.bh);
+  const bool split = a.splits > 1;
+  p.tiles_per_split = split ? a.tiles_per_split : (1 << 30);
+  p.o_part = split ? a.o_part : nullptr;
+  p.st_part = split ? a.st_part : nullptr;
+  dim3 grid((a.n_q + kBlockM * NQ - 1) / (kBlockM * NQ), a.bh, split ? a.splits : 1);
   kern<<<grid, C::kThreads, C::kAlloc, stream>>>(mq, mqlo, mqo, mk, mv, p);
-  return cudaGetLastError() == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
+  if (cudaGetLastError() != cudaSuccess) return KVQ_ERR_CUDA;
+  if (split) {
+    MergeArgs m;
+    m.o_part = a.o_part;
+    m.st_part = a.st_part;
+    m.splits = a.splits;
+    m.rows = (long long)a.bh * a.n_q;
+    m.out = a.out;
+    m.p_s = a.p_s;
+    m.p_r = a.p_r;
+    for (int i = 0; i < 4; ++i) m.sign_bits[i] = a.sign_bits[i];
+    m.inv_sqrt_d = p.inv_sqrt_d;
+    m.mass_only = a.mass_only;
+    const long long warps = (m.rows + (32 / (D / 8)) - 1) / (32 / (D / 8));
+    const unsigned blocks = (unsigned)((warps + 7) / 8);
+    merge_splits_kernel<D><<<blocks, 256, 0, stream>>>(m);
+    if (cudaGetLastError() != cudaSuccess) return KVQ_ERR_CUDA;
+  }
+  return KVQ_OK;
 }
 
 template <int D, int BITS, int GROUP>

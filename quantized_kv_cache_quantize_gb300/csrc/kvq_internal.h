@@ -96,7 +96,55 @@ struct AttnLaunch {
   float* p_r;
   uint32_t sign_bits[4];
   unsigned long long wait_limit_ns;
+  // key-range split (splits > 1): partial results, then a merge kernel
+  int splits, tiles_per_split;
+  float* o_part;    // [splits][bh][n_q][d] fp32
+  float* st_part;   // [splits][bh][n_q][3] fp32
 };
+
+// Key-range split of a launch whose grid (bh * query tiles of rows_per_cta)
+// does not fill the GPU: enough ranges for about one wave of CTAs, each at
+// least two key tiles of 128, at most 16.  1 when the grid is full.
+// Key-range split of the attention grid.  One attention CTA fills an SM
+// (its shared memory allows no second one), so a launch of n CTAs runs in
+// ceil(n / sms) waves.  Splitting every (head, query block) into sp ranges of
+// `per` key tiles costs about ceil(ctas * sp / sms) * (per + kCtaFixed)
+// tile-times (kCtaFixed: a CTA's set-up, pipeline fill and epilogue) plus one
+// for writing and merging the partials; the split taken is the cheapest (the
+// smallest on ties) with at least two tiles per range, at most 64 ranges and
+// at most four waves' worth of CTAs.  The upper bound grows with the tile
+// count, and the split taken never exceeds it: workspaces are sized by it.
+inline int attention_split_bound(long long bh, int n_q, int n_t, int rows_per_cta, int sms) {
+  const long long ctas = bh * ((n_q + rows_per_cta - 1) / rows_per_cta);
+  if (ctas <= 0 || sms <= 0) return 1;
+  long long sp = (4LL * sms) / ctas;
+  if (sp > 64) sp = 64;
+  if (sp > n_t / 2) sp = n_t / 2;
+  return sp < 1 ? 1 : (int)sp;
+}
+
+constexpr int kCtaFixed = 2;
+
+inline void attention_split(long long bh, int n_q, int n_s, int n_r, int rows_per_cta, int sms,
+                            int* splits, int* tiles_per_split) {
+  const int n_t = (n_s + 127) / 128 + (n_r + 127) / 128;
+  *splits = 1;
+  *tiles_per_split = n_t > 0 ? n_t : 1;
+  const int bound = attention_split_bound(bh, n_q, n_t, rows_per_cta, sms);
+  if (bound <= 1) return;
+  const long long ctas = bh * ((n_q + rows_per_cta - 1) / rows_per_cta);
+  long long best = ((ctas + sms - 1) / sms) * (long long)(n_t + kCtaFixed);
+  for (int sp = 2; sp <= bound; ++sp) {
+    const int per = (n_t + sp - 1) / sp;
+    const int used = (n_t + per - 1) / per;
+    const long long cost = ((ctas * used + sms - 1) / sms) * (long long)(per + kCtaFixed) + 1;
+    if (cost < best) {
+      best = cost;
+      *splits = used;
+      *tiles_per_split = per;
+    }
+  }
+}
 
 kvq_status launch_attention(const AttnLaunch& a, int d, int bits, int group,
                             cudaStream_t stream);

@@ -27,6 +27,7 @@ NOALLOC_SCRATCH_BYTES = 32 << 20
 CORR_NONE = 0
 CORR_TAYLOR = 1
 FLAG_PRECISE_QUERY = 1
+FLAG_NO_KV_SPLIT = 2
 
 
 class KVQError(RuntimeError):

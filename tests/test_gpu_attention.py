@@ -47,11 +47,14 @@ RAGGED = [
 
 
 @pytest.mark.parametrize("case", RAGGED, ids=lambda c: "d{}b{}g{}_q{}_s{}_r{}".format(*c[:6]))
-@pytest.mark.parametrize("corr,flags", [(kvq.CORR_TAYLOR, 0), (kvq.CORR_NONE, 0),
-                                        (kvq.CORR_TAYLOR, kvq.FLAG_PRECISE_QUERY)])
+@pytest.mark.parametrize("corr,flags", [
+    (kvq.CORR_TAYLOR, 0), (kvq.CORR_NONE, 0), (kvq.CORR_TAYLOR, kvq.FLAG_PRECISE_QUERY),
+    (kvq.CORR_TAYLOR, kvq.FLAG_NO_KV_SPLIT),
+    (kvq.CORR_NONE, kvq.FLAG_PRECISE_QUERY | kvq.FLAG_NO_KV_SPLIT)])
 def test_ragged_all_rows(case, corr, flags):
     """Sizes that are not multiples of the 128-token tile, an empty cache, an
-    empty current chunk, single tokens."""
+    empty current chunk, single tokens; with and without the key-range split
+    (these grids are far smaller than the GPU, so by default they split)."""
     d, bits, group, n_q, n_s, n_r, chunk, n_chunks, heads = case
     w = synth.Workload("ragged", heads=heads, head_dim=d, chunk_tokens=chunk, n_chunks=n_chunks,
                        bits=bits, group=group, n_outliers_fixed=2, outlier_scale=6.0,
