@@ -117,21 +117,22 @@ int device_sm_count() {
 // key-range split of one launch (1 = none); rows per CTA: 256, or 128 with
 // the precise-query flag
 int split_for(const kvq::Geometry& g, int n_q, int n_s, int n_r, bool precise, int sms,
-              int* per) {
+              int max_splits, int* per) {
   int splits = 1;
-  kvq::attention_split(g.bh, n_q, n_s, n_r, precise ? 128 : 256, sms, &splits, per);
+  kvq::attention_split(g.bh, n_q, n_s, n_r, g.d, precise ? 128 : 256, sms, max_splits, &splits,
+                       per);
   return splits;
 }
 
-// workspace for either query mode and any window length up to n_s: sized for
-// the largest split the current device would use (the split bound grows with
-// the tile count; the split actually taken never exceeds it)
+// workspace for either query mode, with room for the split the current device
+// takes on a full window (n_s = the cache's capacity); a shorter window whose
+// best split needs more room takes the best split that fits
 size_t workspace_bytes_any(const kvq::Geometry& g, int n_q, int n_s, int n_r) {
   const int sms = device_sm_count();
-  const int n_t = (n_s + 127) / 128 + (n_r + 127) / 128;
   size_t best = 0;
   for (int precise = 0; precise < 2; ++precise) {
-    const int sp = kvq::attention_split_bound(g.bh, n_q, n_t, precise ? 128 : 256, sms);
+    int per = 0;
+    const int sp = split_for(g, n_q, n_s, n_r, precise != 0, sms, 64, &per);
     const size_t b = carve(nullptr, g, n_q, n_r, sp).bytes;
     if (b > best) best = b;
   }
@@ -169,9 +170,12 @@ kvq_status attention_common(const kvq_cache* cache, const uint16_t* q, const uin
   // key-range split when the grid would not fill the device (and the
   // workspace holds the partial results; otherwise one range)
   int per = 0, splits = 1;
-  if ((flags & KVQ_FLAG_NO_KV_SPLIT) == 0)
-    splits = split_for(g, n_q, cache->len, n_r, precise, device_sm_count(), &per);
-  if (splits > 1 && workspace_bytes < carve(nullptr, g, n_q, n_r, splits).bytes) splits = 1;
+  if ((flags & KVQ_FLAG_NO_KV_SPLIT) == 0) {
+    int max_splits = 64;
+    while (max_splits > 1 && carve(nullptr, g, n_q, n_r, max_splits).bytes > workspace_bytes)
+      --max_splits;
+    splits = split_for(g, n_q, cache->len, n_r, precise, device_sm_count(), max_splits, &per);
+  }
   const Workspace ws = carve(workspace, g, n_q, n_r, splits);
   if (workspace_bytes < ws.bytes) return KVQ_ERR_INVALID_ARG;
 

@@ -107,37 +107,34 @@ struct AttnLaunch {
 // least two key tiles of 128, at most 16.  1 when the grid is full.
 // Key-range split of the attention grid.  One attention CTA fills an SM
 // (its shared memory allows no second one), so a launch of n CTAs runs in
-// ceil(n / sms) waves.  Splitting every (head, query block) into sp ranges of
-// `per` key tiles costs about ceil(ctas * sp / sms) * (per + kCtaFixed)
-// tile-times (kCtaFixed: a CTA's set-up, pipeline fill and epilogue) plus one
-// for writing and merging the partials; the split taken is the cheapest (the
-// smallest on ties) with at least two tiles per range, at most 64 ranges and
-// at most four waves' worth of CTAs.  The upper bound grows with the tile
-// count, and the split taken never exceeds it: workspaces are sized by it.
-inline int attention_split_bound(long long bh, int n_q, int n_t, int rows_per_cta, int sms) {
-  const long long ctas = bh * ((n_q + rows_per_cta - 1) / rows_per_cta);
-  if (ctas <= 0 || sms <= 0) return 1;
-  long long sp = (4LL * sms) / ctas;
-  if (sp > 64) sp = 64;
-  if (sp > n_t / 2) sp = n_t / 2;
-  return sp < 1 ? 1 : (int)sp;
-}
-
+// ceil(n / sms) waves.  Splitting every (head, query block) into ranges of
+// `per` key tiles costs about ceil(ctas * ranges / sms) * (per + kCtaFixed)
+// tile-times (kCtaFixed: a CTA's set-up, pipeline fill and epilogue), plus
+// the partial results written and merged (ranges * rows * (4d + 12) bytes,
+// twice, at kBytesPerTileTime).  The split taken is the cheapest, the
+// smallest on ties, with at least two tiles per range and at most
+// min(64, max_splits) ranges; it helps small grids (few heads or query rows)
+// and grids whose last wave is mostly empty.
 constexpr int kCtaFixed = 2;
+constexpr double kBytesPerTileTime = 12e6;
 
-inline void attention_split(long long bh, int n_q, int n_s, int n_r, int rows_per_cta, int sms,
-                            int* splits, int* tiles_per_split) {
+inline void attention_split(long long bh, int n_q, int n_s, int n_r, int d, int rows_per_cta,
+                            int sms, int max_splits, int* splits, int* tiles_per_split) {
   const int n_t = (n_s + 127) / 128 + (n_r + 127) / 128;
   *splits = 1;
   *tiles_per_split = n_t > 0 ? n_t : 1;
-  const int bound = attention_split_bound(bh, n_q, n_t, rows_per_cta, sms);
-  if (bound <= 1) return;
   const long long ctas = bh * ((n_q + rows_per_cta - 1) / rows_per_cta);
-  long long best = ((ctas + sms - 1) / sms) * (long long)(n_t + kCtaFixed);
-  for (int sp = 2; sp <= bound; ++sp) {
+  if (n_t < 4 || ctas <= 0 || sms <= 0 || max_splits < 2) return;
+  int lim = n_t / 2;
+  if (lim > 64) lim = 64;
+  if (lim > max_splits) lim = max_splits;
+  double best = (double)((ctas + sms - 1) / sms) * (n_t + kCtaFixed);
+  const double row_bytes = 2.0 * (double)bh * n_q * (4.0 * d + 12.0);
+  for (int sp = 2; sp <= lim; ++sp) {
     const int per = (n_t + sp - 1) / sp;
     const int used = (n_t + per - 1) / per;
-    const long long cost = ((ctas * used + sms - 1) / sms) * (long long)(per + kCtaFixed) + 1;
+    const double cost = (double)((ctas * used + sms - 1) / sms) * (per + kCtaFixed) + 1.0 +
+                        used * row_bytes / kBytesPerTileTime;
     if (cost < best) {
       best = cost;
       *splits = used;
