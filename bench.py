@@ -31,6 +31,7 @@ if ROOT not in sys.path:
 
 METRIC = "corrected INT2-KV chunk-attention TFLOP/s and % of roofline; quantize GB/s"
 UNIT = "TFLOP/s"
+CORR_NAMES = {0: "none", 1: "taylor", 2: "exact"}
 
 
 def _peaks():
@@ -159,7 +160,7 @@ def run_gpu(args):
         kvq.quantize_append(cache, kn, vn, stream=stream)
         kvq.lib().kvq_attention_corrected(
             kvq.ctypes.byref(cache.struct), kvq._ptr(q), kvq._ptr(kc), kvq._ptr(vc), w.n_q, w.n_r,
-            kvq.ctypes.c_float(w.scale), kvq.CORR_TAYLOR, args.flags, kvq._ptr(ws), ws.numel(),
+            kvq.ctypes.c_float(w.scale), args.corr, args.flags, kvq._ptr(ws), ws.numel(),
             kvq._ptr(out), kvq._ptr(ps), kvq._ptr(pr), kvq._stream(stream))
 
     for _ in range(args.warmup):
@@ -247,7 +248,7 @@ def run_gpu(args):
         kvq.lib().kvq_attention_corrected(
             kvq.ctypes.byref(cache.struct), kvq._ptr(di["q"]), kvq._ptr(di["k_cur"]),
             kvq._ptr(di["v_cur"]), w.n_q, w.n_r, kvq.ctypes.c_float(w.scale),
-            kvq.CORR_TAYLOR, args.flags, kvq._ptr(ws), ws.numel(), kvq._ptr(o_d), kvq._ptr(ps_d),
+            args.corr, args.flags, kvq._ptr(ws), ws.numel(), kvq._ptr(o_d), kvq._ptr(ps_d),
             kvq._ptr(pr_d), kvq._stream(stream))
         ev_done[b_].record(stream)
         s_out.wait_event(ev_done[b_])
@@ -286,7 +287,8 @@ def run_gpu(args):
                     "channels)",
             "config": _config(w, {
                 "l2": f"inputs larger than L2: {ws_bytes / 1e6:.0f} MB read per step vs 129 MB L2",
-                "parallelism": f"replicas x{world} (heads independent, no collective)"}),
+                "parallelism": f"replicas x{world} (heads independent, no collective)",
+                "correction": CORR_NAMES[args.corr], "flags": args.flags}),
             "clocks": clk,
             "e2e": {"value": round(flops * world / (e2e_ms * 1e-3) / 1e12, 3), "unit": UNIT,
                     "ms_per_step": round(e2e_ms, 4),
@@ -314,7 +316,7 @@ def run_gpu(args):
     return result
 
 
-def _oracle_sample(w, head: int, rows: int, seed: int):
+def _oracle_sample(w, head: int, rows: int, seed: int, corr: int = 1):
     """One bounded sample of the step on the CPU oracle: quantize-append of
     one head's chunk (K and V) and the corrected attention of ``rows`` query
     rows of that head over its full window and current chunk."""
@@ -331,7 +333,7 @@ def _oracle_sample(w, head: int, rows: int, seed: int):
     _, vd, vz, _, vcod = O.quantize_rows(x["v_win"].float().numpy(), s, w.bits, w.group)
     O.chunk_attention(x["q"].float().numpy()[:rows], O.dequantize(kc, kd, kz, w.group),
                       O.dequantize(vcod, vd, vz, w.group), kd, x["k_cur"].float().numpy(),
-                      x["v_cur"].float().numpy(), s, w.scale, w.group, O.CORR_TAYLOR)
+                      x["v_cur"].float().numpy(), s, w.scale, w.group, corr)
     dt = time.perf_counter() - t0
     flops = w.attention_flops(n_q=rows, heads=1)
     return flops, dt
@@ -348,10 +350,12 @@ def cpu_baseline(w, args):
     """Oracle throughput on a bounded sample: whole heads (all query rows of
     the chunk) are run one after another until ``--cpu-seconds`` of wall time
     have been spent (at least one head, at most all of them)."""
-    rows = min(args.cpu_rows, w.n_q) if args.cpu_rows > 0 else w.n_q
+    # the oracle's exact correction evaluates log(sinh a / a) per channel and
+    # score: its default sample is 128 query rows per head instead of the chunk
+    rows = min(args.cpu_rows, w.n_q) if args.cpu_rows > 0 else (128 if args.corr == 2 else w.n_q)
     tot_f, tot_t, heads = 0.0, 0.0, 0
     while heads < w.heads and (heads == 0 or tot_t < args.cpu_seconds):
-        f, dt = _oracle_sample(w, heads, rows, args.seed)
+        f, dt = _oracle_sample(w, heads, rows, args.seed, args.corr)
         tot_f += f
         tot_t += dt
         heads += 1
@@ -371,10 +375,10 @@ def run_reference(args):
     w = _workload(args.workload)
     rows = args.ref_rows
     for _ in range(args.warmup):
-        _oracle_sample(w, 0, rows, args.seed)
+        _oracle_sample(w, 0, rows, args.seed, args.corr)
     tot_f, tot_t = 0.0, 0.0
     for k in range(args.steps):
-        f, dt = _oracle_sample(w, k % w.heads, rows, args.seed)
+        f, dt = _oracle_sample(w, k % w.heads, rows, args.seed, args.corr)
         tot_f += f
         tot_t += dt
     value = tot_f / tot_t / 1e12
@@ -413,8 +417,12 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--precise-query", dest="flags", action="store_const", const=1, default=0,
                     help="split the rotated query into FP16 high + low parts")
+    ap.add_argument("--corr", choices=["taylor", "exact", "none"], default="taylor",
+                    help="correction of the cached scores (default: the second-order Taylor "
+                         "term; exact: log(sinh a / a) per channel)")
     args = ap.parse_args(argv)
     args.warmup = max(3, args.warmup)   # at least 3 untimed warm-up steps
+    args.corr = {v: k for k, v in CORR_NAMES.items()}[args.corr]
     if args.impl == "reference":
         return run_reference(args)
     return run_gpu(args)

@@ -45,7 +45,8 @@ typedef enum {
 /* Correction applied to cached-key scores before the softmax. */
 typedef enum {
   KVQ_CORR_NONE = 0,   /* plain quantized attention (the ablation)         */
-  KVQ_CORR_TAYLOR = 1  /* second-order Jensen-bias correction              */
+  KVQ_CORR_TAYLOR = 1, /* second-order Jensen-bias correction              */
+  KVQ_CORR_EXACT = 2   /* the exact log-moment of uniform noise (below)    */
 } kvq_corr;
 
 /*
@@ -152,6 +153,15 @@ size_t kvq_workspace_bytes(const kvq_cache *cache, int32_t n_q, int32_t n_r);
  *   cached score  s_ij = scale * q'_j . k_hat'_i - b_ij,
  *   b_ij = scale^2 / 24 * sum_g ||q'_{j,g}||^2 * D_{i,g}^2   (corr = TAYLOR;
  *          0 for corr = NONE) -- the second-order Jensen-bias correction;
+ *   corr = EXACT: b_ij = sum_c log(sinh(a_c) / a_c), a_c = scale/2 *
+ *          |q'_{j,c}| * D_{i,g(c)} -- log E[exp(delta)] for independent
+ *          uniform rounding noise on every rotated key channel, of which the
+ *          TAYLOR term is the leading a^2/6 part (Figure 3 caption; the
+ *          paper's correction is the Taylor one, this mode measures what the
+ *          truncation leaves out).  Evaluated in fp32: a power series in the
+ *          key's step size against per-row moments of the query while every
+ *          a_c of a group is <= 1, per channel otherwise.  Runs with one
+ *          query tile per CTA and costs several times the TAYLOR mode;
  *   current score s_ij = scale * q_j . k_i on the unrotated BF16 inputs
  *          (exact products, fp32 accumulation);
  *   one softmax over both segments; out = sum_i p_ij v_i in the ORIGINAL

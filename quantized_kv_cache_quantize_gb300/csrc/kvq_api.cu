@@ -115,24 +115,25 @@ int device_sm_count() {
 }
 
 // key-range split of one launch (1 = none); rows per CTA: 256, or 128 with
-// the precise-query flag
-int split_for(const kvq::Geometry& g, int n_q, int n_s, int n_r, bool precise, int sms,
+// the precise-query flag or the exact correction (one query tile per CTA)
+int split_for(const kvq::Geometry& g, int n_q, int n_s, int n_r, bool one_tile, int sms,
               int max_splits, int* per) {
   int splits = 1;
-  kvq::attention_split(g.bh, n_q, n_s, n_r, g.d, precise ? 128 : 256, sms, max_splits, &splits,
+  kvq::attention_split(g.bh, n_q, n_s, n_r, g.d, one_tile ? 128 : 256, sms, max_splits, &splits,
                        per);
   return splits;
 }
 
-// workspace for either query mode, with room for the split the current device
-// takes on a full window (n_s = the cache's capacity); a shorter window whose
-// best split needs more room takes the best split that fits
+// workspace for either CTA shape (two query tiles or one), with room for the
+// split the current device takes on a full window (n_s = the cache's
+// capacity); a shorter window whose best split needs more room takes the best
+// split that fits
 size_t workspace_bytes_any(const kvq::Geometry& g, int n_q, int n_s, int n_r) {
   const int sms = device_sm_count();
   size_t best = 0;
-  for (int precise = 0; precise < 2; ++precise) {
+  for (int one_tile = 0; one_tile < 2; ++one_tile) {
     int per = 0;
-    const int sp = split_for(g, n_q, n_s, n_r, precise != 0, sms, 64, &per);
+    const int sp = split_for(g, n_q, n_s, n_r, one_tile != 0, sms, 64, &per);
     const size_t b = carve(nullptr, g, n_q, n_r, sp).bytes;
     if (b > best) best = b;
   }
@@ -148,9 +149,11 @@ kvq_status attention_common(const kvq_cache* cache, const uint16_t* q, const uin
   kvq_status st = check_geometry(cache, &g);
   if (st != KVQ_OK) return st;
   if (n_q < 0 || n_r < 0 || n_q > (1 << 30) || n_r > (1 << 30)) return KVQ_ERR_INVALID_ARG;
-  if (corr != KVQ_CORR_NONE && corr != KVQ_CORR_TAYLOR) return KVQ_ERR_INVALID_ARG;
+  if (corr != KVQ_CORR_NONE && corr != KVQ_CORR_TAYLOR && corr != KVQ_CORR_EXACT)
+    return KVQ_ERR_INVALID_ARG;
   if ((flags & ~(KVQ_FLAG_PRECISE_QUERY | KVQ_FLAG_NO_KV_SPLIT)) != 0) return KVQ_ERR_INVALID_ARG;
   const bool precise = (flags & KVQ_FLAG_PRECISE_QUERY) != 0;
+  const bool one_tile = precise || corr == KVQ_CORR_EXACT;   // one query tile per CTA
   if (!std::isfinite(scale) || scale <= 0.f) return KVQ_ERR_INVALID_ARG;
   if ((p_s == nullptr) != (p_r == nullptr)) return KVQ_ERR_INVALID_ARG;
   if (mass_only && p_s == nullptr) return KVQ_ERR_INVALID_ARG;
@@ -174,7 +177,7 @@ kvq_status attention_common(const kvq_cache* cache, const uint16_t* q, const uin
     int max_splits = 64;
     while (max_splits > 1 && carve(nullptr, g, n_q, n_r, max_splits).bytes > workspace_bytes)
       --max_splits;
-    splits = split_for(g, n_q, cache->len, n_r, precise, device_sm_count(), max_splits, &per);
+    splits = split_for(g, n_q, cache->len, n_r, one_tile, device_sm_count(), max_splits, &per);
   }
   const Workspace ws = carve(workspace, g, n_q, n_r, splits);
   if (workspace_bytes < ws.bytes) return KVQ_ERR_INVALID_ARG;

@@ -64,7 +64,8 @@ struct AttnParams {
   const uint32_t* v_sz;
   int n_s, cap, n_q, n_r;
   float scale_log2;   // scale * log2(e)
-  float alpha_coef;   // -(scale / 24) * 2^8 with the correction, 0 without
+  float alpha_coef;   // -(scale / 24) * 2^8 with the Taylor correction, 0 otherwise
+  float half_scale;   // scale / 2 (exact correction: a_c = half_scale * |q'_c| * D)
   int corr;
   int mass_only;
   uint16_t* out;
@@ -93,7 +94,7 @@ constexpr float kBiasKeyScale = 1.0f / 256.0f;
 constexpr float kZeroQueryScale = 16.0f;
 constexpr float kZeroKeyScale = 1.0f / 16.0f;
 
-template <int D, int NQ, bool PRECISE>
+template <int D, int NQ, bool PRECISE, bool EXACT>
 struct Cfg {
   static constexpr int kTile = kBlockM * D * 2;
   static constexpr int kNKH = D / 64;
@@ -102,7 +103,12 @@ struct Cfg {
   static constexpr int kQ = 0;                             // NQ hi tiles [, NQ lo tiles]
   static constexpr int kQx = kQ + NQ * kTile * (PRECISE ? 2 : 1);
   static constexpr int kNExt = PRECISE ? 2 : 1;              // extension tiles
-  static constexpr int kStageBytes = 2 * kTile + kNExt * kExt;  // K, V, Kx
+  // exact correction: per stage [4 groups][128 keys] fp32 (scale * D / 2)^2,
+  // then [4 groups][4 warps] maxima over the tile; padded so that both
+  // stages stay 1024-byte aligned
+  static constexpr int kDsq = 2 * kTile + kNExt * kExt;    // offset inside a stage
+  static constexpr int kDsqBytes = EXACT ? 3072 : 0;
+  static constexpr int kStageBytes = 2 * kTile + kNExt * kExt + kDsqBytes;  // K, V, Kx [, dsq]
   static constexpr int kStages = kQx + NQ * kNExt * kExt;
   static constexpr int kBar = kStages + 2 * kStageBytes;
   static constexpr int kBytes = kBar + 256;
@@ -114,8 +120,11 @@ struct Cfg {
   static constexpr int kThreads = (kSoftmaxWarps + 6) * 32;
   // tensor memory columns: S buffers, then the O tiles
   static constexpr int kTO = NQ * kSBuf * 128;
+  static constexpr int kTQ = kTO + NQ * D;   // exact correction: the row's rotated query, fp32
   static constexpr int kTCols = 512;
-  static_assert(kTO + NQ * D <= kTCols, "tensor memory");
+  static_assert(kTO + NQ * D * (EXACT ? 2 : 1) <= kTCols, "tensor memory");
+  static_assert(!EXACT || NQ == 1, "exact correction: one query tile per CTA");
+  static_assert(kStageBytes % 1024 == 0, "stage alignment");
   static_assert(kAlloc <= 232448, "shared memory");
 };
 
@@ -279,6 +288,179 @@ __device__ __forceinline__ uint64_t exp_chunk(const uint32_t (&s)[32], uint64_t 
   return acc;
 }
 
+// ---- exact correction -------------------------------------------------------
+//
+// For independent uniform noise on the cached key's rotated channels,
+// E[exp(delta_ij)] = prod_c sinh(a_c) / a_c with a_c = (scale / 2) |q'_c| D_g(c),
+// so the exact correction is b_ij = sum_c f(a_c), f(a) = log(sinh(a) / a).
+// f has the power series f(a) = sum_k c_k a^(2k), c_k = 2^(2k) B_2k / (2k (2k)!)
+// (B_2k the Bernoulli numbers), convergent for a < pi.  For one query row and
+// group g with mu_g = max_{c in g} q'_c^2 and T = mu_g (scale D_g / 2)^2, the
+// group's term is sum_k c_k M_k T^k with the row's normalized moments
+// M_k = sum_{c in g} (q'_c^2 / mu_g)^k: a polynomial in the key's T, exact to
+// |c_8| T^8 <= 1.4e-9 per channel while T <= 1 (every a_c of the group <= 1).
+// Larger T takes the per-channel evaluation.
+constexpr int kSeriesTerms = 7;
+__host__ __device__ constexpr float sinhc_coef(int k) {   // c_(k+1)
+  return k == 0 ? 1.0f / 6.0f
+       : k == 1 ? -1.0f / 180.0f
+       : k == 2 ? 1.0f / 2835.0f
+       : k == 3 ? -1.0f / 37800.0f
+       : k == 4 ? 1.0f / 467775.0f
+       : k == 5 ? -691.0f / 3831077250.0f
+                : 2.0f / 127702575.0f;
+}
+constexpr float kLog2e = 1.4426950408889634f;
+
+// f(a) = log(sinh(a) / a) for a >= 0: the series above for a < 1, else
+// a + log((1 - exp(-2a)) / (2a))
+__device__ __forceinline__ float log_sinhc(float a) {
+  if (a < 1.0f) {
+    const float t = a * a;
+    float p = sinhc_coef(kSeriesTerms - 1);
+#pragma unroll
+    for (int k = kSeriesTerms - 2; k >= 0; --k) p = fmaf(p, t, sinhc_coef(k));
+    return p * t;
+  }
+  return a + __logf(__fdividef(1.0f - __expf(-2.0f * a), a + a));
+}
+
+// exp_chunk with a per-column additive term nb (log2 units, pairs packed):
+// 2^(s * scale * log2(e) + nb - m)
+__device__ __forceinline__ uint64_t exp_chunk_b(const uint32_t (&s)[32], const uint64_t (&nb)[16],
+                                                uint64_t sl2x2, float m, int valid,
+                                                uint32_t (&pk)[16]) {
+  const uint64_t negm2 = ptx::f2_pack(-m, -m);
+  uint64_t acc = ptx::f2_pack(0.f, 0.f);
+#pragma unroll
+  for (int k = 0; k < 16; ++k) {
+    float x0, x1;
+    ptx::f2_unpack(ptx::f2_fma(ptx::f2_pack(__uint_as_float(s[2 * k]), __uint_as_float(s[2 * k + 1])),
+                               sl2x2, ptx::f2_add(nb[k], negm2)),
+                   x0, x1);
+    float e0 = ptx::ex2_approx(x0);
+    float e1 = ptx::ex2_approx(x1);
+    if (valid < 32) {
+      e0 = (2 * k < valid) ? e0 : 0.f;
+      e1 = (2 * k + 1 < valid) ? e1 : 0.f;
+    }
+    acc = ptx::f2_add(acc, ptx::f2_pack(e0, e1));
+    pk[k] = ptx::f16x2_rn(e0, e1);
+  }
+  return acc;
+}
+
+// The exact correction of 32 cached keys for one query row, in log2 units
+// and negated (nb = -log2(e) b), by the series: dq points at the chunk's
+// (scale D_g / 2)^2 values ([group][128 keys] layout), mu2 / a2 hold the row's
+// mu_g and -log2(e) c_k M_k as packed pairs.  Valid for the keys whose
+// T = mu_g (scale D_g / 2)^2 <= 1 in every group; the others get whatever
+// the polynomial gives (exact_fix replaces them).
+template <int G>
+__device__ __forceinline__ void exact_series(const float* dq, const uint64_t (&mu2)[G],
+                                             const uint64_t (&a2)[G][kSeriesTerms],
+                                             uint64_t (&nb)[16]) {
+#pragma unroll
+  for (int k = 0; k < 16; ++k) nb[k] = 0ull;   // (+0, +0)
+#pragma unroll
+  for (int g = 0; g < G; ++g) {
+#pragma unroll
+    for (int k4 = 0; k4 < 8; ++k4) {
+      const float4 d4 = *reinterpret_cast<const float4*>(dq + g * kBlockN + 4 * k4);
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const uint64_t t2 = ptx::f2_mul(mu2[g], h ? ptx::f2_pack(d4.z, d4.w) : ptx::f2_pack(d4.x, d4.y));
+        uint64_t pp = a2[g][kSeriesTerms - 1];
+#pragma unroll
+        for (int i = kSeriesTerms - 2; i >= 0; --i) pp = ptx::f2_fma(pp, t2, a2[g][i]);
+        nb[2 * k4 + h] = ptx::f2_fma(pp, t2, nb[2 * k4 + h]);
+      }
+    }
+  }
+}
+
+// Keys of the chunk with T > 1 in some group (some a_c above 1): their term
+// is rebuilt from the series of the other groups and, for the groups above
+// the bound, the per-channel sum of log(sinh(a_c) / a_c) over the row's
+// rotated query in tensor memory (t_q, fp32).  Warp-collective (tensor
+// memory loads): called by whole warps.
+template <int G, int D, int GROUP>
+__device__ __noinline__ void exact_fix(const float* dq, const uint64_t (&mu2)[G],
+                                       const uint64_t (&a2)[G][kSeriesTerms], uint32_t t_q,
+                                       uint64_t (&nb)[16]) {
+  float mu[G];
+#pragma unroll
+  for (int g = 0; g < G; ++g) {
+    float unused;
+    ptx::f2_unpack(mu2[g], mu[g], unused);
+  }
+  uint32_t vm[G];
+  uint32_t any = 0;
+#pragma unroll
+  for (int g = 0; g < G; ++g) {
+    vm[g] = 0u;
+#pragma unroll 4
+    for (int k = 0; k < 32; ++k) vm[g] |= (mu[g] * dq[g * kBlockN + k] > 1.0f ? 1u : 0u) << k;
+    any |= vm[g];
+  }
+  if (!__any_sync(0xffffffffu, any != 0u)) return;
+  float fix[32];
+  // series part of the groups within the bound
+#pragma unroll 1
+  for (int k = 0; k < 32; ++k) {
+    float acc = 0.f;
+    if ((any >> k) & 1u) {
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        const float t = mu[g] * dq[g * kBlockN + k];
+        if (t <= 1.0f) {
+          float a, unused;
+          ptx::f2_unpack(a2[g][kSeriesTerms - 1], a, unused);
+          float pp = a;
+#pragma unroll
+          for (int i = kSeriesTerms - 2; i >= 0; --i) {
+            ptx::f2_unpack(a2[g][i], a, unused);
+            pp = fmaf(pp, t, a);
+          }
+          acc = fmaf(pp, t, acc);
+        }
+      }
+    }
+    fix[k] = acc;
+  }
+  // per-channel terms of the groups above the bound, 32 channels at a time
+  uint32_t vmr[G];
+#pragma unroll
+  for (int g = 0; g < G; ++g) vmr[g] = vm[g];
+#pragma unroll 1
+  for (int cb = 0; cb < D / 32; ++cb) {
+    const int g = (32 * cb) / GROUP;
+    uint32_t mk = 0u;
+#pragma unroll
+    for (int gg = 0; gg < G; ++gg) mk = gg == g ? vmr[gg] : mk;
+    if (!__any_sync(0xffffffffu, mk != 0u)) continue;
+    uint32_t qv[32];
+    ptx::tmem_ld32(t_q + 32 * cb, qv);
+    while (mk != 0u) {
+      const int k = __ffs(mk) - 1;
+      mk &= mk - 1u;
+      const float dt = sqrtf(dq[g * kBlockN + k]);
+      float sum = 0.f;
+#pragma unroll
+      for (int i = 0; i < 32; ++i) sum += log_sinhc(fabsf(__uint_as_float(qv[i])) * dt);
+      fix[k] = fmaf(-kLog2e, sum, fix[k]);
+    }
+  }
+#pragma unroll
+  for (int k2 = 0; k2 < 16; ++k2) {
+    float lo, hi;
+    ptx::f2_unpack(nb[k2], lo, hi);
+    if ((any >> (2 * k2)) & 1u) lo = fix[2 * k2];
+    if ((any >> (2 * k2 + 1)) & 1u) hi = fix[2 * k2 + 1];
+    nb[k2] = ptx::f2_pack(lo, hi);
+  }
+}
+
 template <int D>
 __device__ __forceinline__ void zero_row(uint8_t* tile, int r) {
 #pragma unroll
@@ -286,12 +468,12 @@ __device__ __forceinline__ void zero_row(uint8_t* tile, int r) {
     *reinterpret_cast<uint4*>(tile + (c >> 3) * kHalf + sw128(r, c & 7)) = make_uint4(0, 0, 0, 0);
 }
 
-template <int D, int BITS, int GROUP, int NQ, bool PRECISE>
-__global__ void __launch_bounds__(Cfg<D, NQ, PRECISE>::kThreads, 1)
+template <int D, int BITS, int GROUP, int NQ, bool PRECISE, bool EXACT>
+__global__ void __launch_bounds__(Cfg<D, NQ, PRECISE, EXACT>::kThreads, 1)
     attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_qlo,
                 const __grid_constant__ CUtensorMap tm_qo, const __grid_constant__ CUtensorMap tm_k,
                 const __grid_constant__ CUtensorMap tm_v, const AttnParams p) {
-  using C = Cfg<D, NQ, PRECISE>;
+  using C = Cfg<D, NQ, PRECISE, EXACT>;
   constexpr int G = D / GROUP;
   constexpr int CB = D * BITS / 8;       // packed bytes per token
   constexpr int NW = CB / 4;             // packed words per token
@@ -404,9 +586,79 @@ __global__ void __launch_bounds__(Cfg<D, NQ, PRECISE>::kThreads, 1)
       }
       write_ext_row(smem + C::kQx + q * C::kNExt * kExt, r, cx);
       if (PRECISE) write_ext_row(smem + C::kQx + q * C::kNExt * kExt + kExt, r, cz);
-      ptx::fence_proxy_async_smem();
-      ptx::mbar_arrive(BAR(kBarQx));
     }
+    // exact correction: the row's rotated query (fp32) goes to tensor memory
+    // for the per-channel terms; per group the maximum mu_g of q'_c^2 and the
+    // series coefficients -log2(e) c_k M_k (pairs packed, two keys at a time).
+    // Read from the query tile before the first QK can be issued (the tile is
+    // overwritten once the cached QKs are done).
+    constexpr int GE = EXACT ? G : 1;
+    uint64_t mu2[GE], a2[GE][kSeriesTerms];
+    const uint32_t t_q = tmem + C::kTQ + lane_off;
+    if (EXACT) {
+      const uint8_t* qt = smem + C::kQ + q * C::kTile;
+      float mu[GE], mom[GE][kSeriesTerms];
+#pragma unroll
+      for (int g = 0; g < GE; ++g) {
+        mu[g] = 0.f;
+#pragma unroll
+        for (int k = 0; k < kSeriesTerms; ++k) mom[g][k] = 0.f;
+      }
+#pragma unroll
+      for (int cc = 0; cc < D / 32; ++cc) {
+        uint32_t v[32];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int c = 4 * cc + e;
+          const int off = (c >> 3) * kHalf + sw128(r, c & 7);
+          const uint4 hv = *reinterpret_cast<const uint4*>(qt + off);
+          uint4 lv = make_uint4(0u, 0u, 0u, 0u);
+          if (PRECISE) lv = *reinterpret_cast<const uint4*>(qt + NQ * C::kTile + off);
+          const uint32_t w[4] = {hv.x, hv.y, hv.z, hv.w};
+          const uint32_t wl[4] = {lv.x, lv.y, lv.z, lv.w};
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            v[8 * e + 2 * i] = __float_as_uint(h_lo(w[i]) + h_lo(wl[i]));
+            v[8 * e + 2 * i + 1] = __float_as_uint(h_hi(w[i]) + h_hi(wl[i]));
+          }
+        }
+        ptx::tmem_st32(t_q + 32 * cc, v);
+        const int g = (32 * cc) / GROUP;
+#pragma unroll
+        for (int k = 0; k < 32; ++k) mu[g] = fmaxf(mu[g], __uint_as_float(v[k]) * __uint_as_float(v[k]));
+      }
+      ptx::tmem_st_wait();
+#pragma unroll
+      for (int cc = 0; cc < D / 32; ++cc) {
+        uint32_t v[32];
+        ptx::tmem_ld32(t_q + 32 * cc, v);
+        const int g = (32 * cc) / GROUP;
+        const float inv = mu[g] > 0.f ? 1.0f / mu[g] : 0.f;
+#pragma unroll
+        for (int k = 0; k < 32; ++k) {
+          const float x = __uint_as_float(v[k]);
+          const float u = x * x * inv;
+          float pw = u;
+          mom[g][0] += pw;
+#pragma unroll
+          for (int t = 1; t < kSeriesTerms; ++t) {
+            pw *= u;
+            mom[g][t] += pw;
+          }
+        }
+      }
+#pragma unroll
+      for (int g = 0; g < GE; ++g) {
+        mu2[g] = ptx::f2_pack(mu[g], mu[g]);
+#pragma unroll
+        for (int t = 0; t < kSeriesTerms; ++t) {
+          const float a = -kLog2e * sinhc_coef(t) * mom[g][t];
+          a2[g][t] = ptx::f2_pack(a, a);
+        }
+      }
+    }
+    ptx::fence_proxy_async_smem();
+    ptx::mbar_arrive(BAR(kBarQx));
 
     float m = -INFINITY, l_s = 0.f, l_r = 0.f;
     const float sl2 = p.scale_log2;
@@ -432,21 +684,66 @@ __global__ void __launch_bounds__(Cfg<D, NQ, PRECISE>::kThreads, 1)
       const float m_in = m;
       const uint64_t sl2x2 = ptx::f2_pack(sl2, sl2);
       uint64_t acc = ptx::f2_pack(0.f, 0.f);
-#pragma unroll 2
+      // exact correction on cached tiles: (scale D_g / 2)^2 of the tile's keys
+      // from the dequant warps, read after acquiring their writes through the
+      // stage's dequant barrier (its phase for this tile has completed and
+      // cannot advance before this tile's P is handed over); the series alone
+      // when every group of every key stays within T <= 1
+      const bool exact_tile = EXACT && j < n_ct;
+      const float* dq =
+          reinterpret_cast<const float*>(smem + C::kStages + (j & 1) * C::kStageBytes + C::kDsq);
+      bool fast = true;
+      if (exact_tile) {
+        if (!__all_sync(0xffffffffu, wait_bar(BAR(kBarFullDq + (j & 1)), (j >> 1) & 1, lim, abort))) {
+          ok = false;
+          break;
+        }
+#pragma unroll
+        for (int g = 0; g < GE; ++g) {
+          const float4 tm = *reinterpret_cast<const float4*>(dq + 4 * kBlockN + 4 * g);
+          float mu, unused;
+          ptx::f2_unpack(mu2[g], mu, unused);
+          fast = fast && mu * fmaxf(fmaxf(tm.x, tm.y), fmaxf(tm.z, tm.w)) <= 1.0f;
+        }
+        fast = __all_sync(0xffffffffu, fast);
+      }
+#pragma unroll(EXACT ? 1 : 2)
       for (int c = 0; c < kBlockN / 32; ++c) {
+        uint64_t nb[16];
+        if (exact_tile) {   // before the scores are loaded: fewer live registers
+          exact_series<GE>(dq + 32 * c, mu2, a2, nb);
+          if (!fast) exact_fix<GE, D, GROUP>(dq + 32 * c, mu2, a2, t_q, nb);
+        }
         uint32_t cur[32];
         ptx::tmem_ld32(t_s + 32 * c, cur);
         uint32_t pk[16];
-        uint64_t cs = exp_chunk(cur, sl2x2, m, nv - 32 * c, pk);
+        uint64_t cs = exact_tile ? exp_chunk_b(cur, nb, sl2x2, m, nv - 32 * c, pk)
+                                 : exp_chunk(cur, sl2x2, m, nv - 32 * c, pk);
         float cs_lo, cs_hi;
         ptx::f2_unpack(cs, cs_lo, cs_hi);
         // NaN-safe: an infinite or undefined sum also takes the slow path
         if (__any_sync(0xffffffffu, !(cs_lo + cs_hi <= kChunkSumLimit))) {
           float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+          float cmax;
+          if (exact_tile) {
 #pragma unroll
-          for (int k = 0; k < 32; ++k)
-            m4[k & 3] = (32 * c + k < nv) ? fmaxf(m4[k & 3], __uint_as_float(cur[k])) : m4[k & 3];
-          const float m_new = fmaxf(m, fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * sl2);
+            for (int k2 = 0; k2 < 16; ++k2) {
+              float b0, b1;
+              ptx::f2_unpack(nb[k2], b0, b1);
+              const float x0 = fmaf(__uint_as_float(cur[2 * k2]), sl2, b0);
+              const float x1 = fmaf(__uint_as_float(cur[2 * k2 + 1]), sl2, b1);
+              m4[(2 * k2) & 3] = (32 * c + 2 * k2 < nv) ? fmaxf(m4[(2 * k2) & 3], x0) : m4[(2 * k2) & 3];
+              m4[(2 * k2 + 1) & 3] =
+                  (32 * c + 2 * k2 + 1 < nv) ? fmaxf(m4[(2 * k2 + 1) & 3], x1) : m4[(2 * k2 + 1) & 3];
+            }
+            cmax = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+          } else {
+#pragma unroll
+            for (int k = 0; k < 32; ++k)
+              m4[k & 3] = (32 * c + k < nv) ? fmaxf(m4[k & 3], __uint_as_float(cur[k])) : m4[k & 3];
+            cmax = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * sl2;
+          }
+          const float m_new = fmaxf(m, cmax);
           const float alpha = exp2f(m - m_new);   // 0 from the initial -inf base
           acc = ptx::f2_mul(acc, ptx::f2_pack(alpha, alpha));
           if (!mass_only && c > 0) {
@@ -460,7 +757,8 @@ __global__ void __launch_bounds__(Cfg<D, NQ, PRECISE>::kThreads, 1)
             }
           }
           m = m_new;
-          cs = exp_chunk(cur, sl2x2, m, nv - 32 * c, pk);
+          cs = exact_tile ? exp_chunk_b(cur, nb, sl2x2, m, nv - 32 * c, pk)
+                          : exp_chunk(cur, sl2x2, m, nv - 32 * c, pk);
         }
         acc = ptx::f2_add(acc, cs);
         // P of columns [32c, 32c + 32) -> TMEM columns [16c, 16c + 16): all
@@ -681,6 +979,20 @@ __global__ void __launch_bounds__(Cfg<D, NQ, PRECISE>::kThreads, 1)
       } else {
         zero_row<D>(st, r);
         if (!mass_only) zero_row<D>(st + C::kTile, r);
+      }
+      if (EXACT) {
+        // (scale D_g / 2)^2 of this key (0 past the window) and, per group,
+        // the maximum over the warp's 32 keys
+        float* dq = reinterpret_cast<float*>(st + C::kDsq);
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+          float dt = p.half_scale * bf16_lo(ksz[g]);
+          dt *= dt;
+          dq[g * kBlockN + r] = dt;
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) dt = fmaxf(dt, __shfl_xor_sync(0xffffffffu, dt, o));
+          if ((r & 31) == 0) dq[4 * kBlockN + 4 * g + (r >> 5)] = dt;
+        }
       }
       // the next tile's words travel while this one is handed over and the
       // next stage is awaited
@@ -1027,11 +1339,11 @@ bool make_map(CUtensorMap* m, const void* base, int d, int n, int bh, bool bf16)
   return r == CUDA_SUCCESS;
 }
 
-template <int D, int BITS, int GROUP, int NQ, bool PRECISE>
+template <int D, int BITS, int GROUP, int NQ, bool PRECISE, bool EXACT>
 kvq_status launch_t(const AttnLaunch& a, cudaStream_t stream) {
-  using C = Cfg<D, NQ, PRECISE>;
+  using C = Cfg<D, NQ, PRECISE, EXACT>;
   static std::atomic<uint64_t> limit_set{0};   // per template instance and device
-  auto kern = attn_kernel<D, BITS, GROUP, NQ, PRECISE>;
+  auto kern = attn_kernel<D, BITS, GROUP, NQ, PRECISE, EXACT>;
   if (ensure_smem_limit(kern, C::kAlloc, limit_set) != cudaSuccess) return KVQ_ERR_CUDA;
   CUtensorMap mq, mqlo, mqo, mk, mv;
   if (!make_map(&mq, a.q_rot, D, a.n_q, a.bh, false)) return KVQ_ERR_CUDA;
@@ -1058,7 +1370,8 @@ kvq_status launch_t(const AttnLaunch& a, cudaStream_t stream) {
   p.n_q = a.n_q;
   p.n_r = a.n_r;
   p.scale_log2 = a.scale * 1.4426950408889634f;
-  p.alpha_coef = a.corr ? -(a.scale / 24.0f) * 256.0f : 0.0f;
+  p.alpha_coef = a.corr == KVQ_CORR_TAYLOR ? -(a.scale / 24.0f) * 256.0f : 0.0f;
+  p.half_scale = 0.5f * a.scale;
   p.corr = a.corr;
   p.mass_only = a.mass_only;
   p.out = a.out;
@@ -1096,8 +1409,12 @@ kvq_status launch_t(const AttnLaunch& a, cudaStream_t stream) {
 
 template <int D, int BITS, int GROUP>
 kvq_status launch_mode(const AttnLaunch& a, cudaStream_t stream) {
-  if (a.precise_query) return launch_t<D, BITS, GROUP, 1, true>(a, stream);
-  return launch_t<D, BITS, GROUP, 2, false>(a, stream);
+  if (a.corr == KVQ_CORR_EXACT) {
+    if (a.precise_query) return launch_t<D, BITS, GROUP, 1, true, true>(a, stream);
+    return launch_t<D, BITS, GROUP, 1, false, true>(a, stream);
+  }
+  if (a.precise_query) return launch_t<D, BITS, GROUP, 1, true, false>(a, stream);
+  return launch_t<D, BITS, GROUP, 2, false, false>(a, stream);
 }
 
 }  // namespace

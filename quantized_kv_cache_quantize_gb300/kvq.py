@@ -26,6 +26,7 @@ NOALLOC_SCRATCH_BYTES = 32 << 20
 
 CORR_NONE = 0
 CORR_TAYLOR = 1
+CORR_EXACT = 2
 FLAG_PRECISE_QUERY = 1
 FLAG_NO_KV_SPLIT = 2
 

@@ -114,6 +114,7 @@ def test_attention_argument_checks(lib):
     P = 0x10000
     # bad correction mode, bad flags, bad scale, missing output, workspace too small
     assert f(ctypes.byref(c), P, P, P, 100, 10, 0.1, 7, 0, P, ws, P, None, None, None) == 1
+    assert f(ctypes.byref(c), P, P, P, 100, 10, 0.1, 3, 0, P, ws, P, None, None, None) == 1
     assert f(ctypes.byref(c), P, P, P, 100, 10, 0.1, 1, 6, P, ws, P, None, None, None) == 1
     assert f(ctypes.byref(c), P, P, P, 100, 10, float("nan"), 1, 0, P, ws, P, None, None, None) == 1
     assert f(ctypes.byref(c), P, P, P, 100, 10, -1.0, 1, 0, P, ws, P, None, None, None) == 1

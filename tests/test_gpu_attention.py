@@ -13,7 +13,7 @@ from tests.gpu_common import assert_close, build_cache, oracle_head
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("corr", [kvq.CORR_TAYLOR, kvq.CORR_NONE])
+@pytest.mark.parametrize("corr", [kvq.CORR_TAYLOR, kvq.CORR_NONE, kvq.CORR_EXACT])
 def test_tiny_all_rows(corr):
     w = synth.WORKLOADS["tiny"]
     x = synth.inputs(w)
@@ -50,7 +50,8 @@ RAGGED = [
 @pytest.mark.parametrize("corr,flags", [
     (kvq.CORR_TAYLOR, 0), (kvq.CORR_NONE, 0), (kvq.CORR_TAYLOR, kvq.FLAG_PRECISE_QUERY),
     (kvq.CORR_TAYLOR, kvq.FLAG_NO_KV_SPLIT),
-    (kvq.CORR_NONE, kvq.FLAG_PRECISE_QUERY | kvq.FLAG_NO_KV_SPLIT)])
+    (kvq.CORR_NONE, kvq.FLAG_PRECISE_QUERY | kvq.FLAG_NO_KV_SPLIT),
+    (kvq.CORR_EXACT, 0), (kvq.CORR_EXACT, kvq.FLAG_PRECISE_QUERY | kvq.FLAG_NO_KV_SPLIT)])
 def test_ragged_all_rows(case, corr, flags):
     """Sizes that are not multiples of the 128-token tile, an empty cache, an
     empty current chunk, single tokens; with and without the key-range split
@@ -186,3 +187,75 @@ def test_rising_scores_rebase(corr, flags):
         o_ref, ps_ref, pr_ref = oracle_head(w, x, s, 0, h, np.arange(n_q), corr, n_s=n_s)
         assert_close(out[0, h].float().cpu().numpy(), o_ref, ps[0, h].cpu().numpy(), ps_ref,
                      pr[0, h].cpu().numpy(), pr_ref, what=f"rebase h{h}")
+
+
+EXACT_BIG = [
+    # (d, bits, group, key outlier scale, query scale, flags)
+    (128, 2, 32, 30.0, 1.5, kvq.FLAG_PRECISE_QUERY),
+    (128, 2, 64, 30.0, 1.5, kvq.FLAG_PRECISE_QUERY),
+    (64, 2, 32, 30.0, 1.5, kvq.FLAG_PRECISE_QUERY),
+    (64, 2, 64, 30.0, 1.5, kvq.FLAG_PRECISE_QUERY),
+    (128, 2, 64, 20.0, 1.0, 0),
+    (64, 2, 64, 12.0, 1.0, 0),
+]
+
+
+@pytest.mark.parametrize("case", EXACT_BIG, ids=lambda c: "d{}b{}g{}_o{}_q{}_f{}".format(*c))
+def test_exact_large_steps(case):
+    """Exact correction where many (query, key, group) triples leave the
+    series' range (some a_c = scale/2 |q'_c| D above 1): keys with large
+    outliers give large step sizes, so both the series and the per-channel
+    terms run, in tiles that mix them (every row against the oracle's exact
+    log(sinh a / a) sum).  Scores reach ~60 with the strongest outliers; there
+    the FP16 rounding of the rotated query alone moves the masses by ~1.1e-3
+    (in every correction mode), so those inputs run with the precise-query
+    split and the milder ones without it."""
+    d, bits, group, osc, qs, flags = case
+    w = synth.Workload("big", heads=2, head_dim=d, chunk_tokens=160, n_chunks=3, bits=bits,
+                       group=group, n_outliers_fixed=4, outlier_scale=osc, offset_std=1.0)
+    n_q, n_s, n_r = 200, 450, 100
+    x = synth.inputs(w, seed=4, n_q=n_q, n_s=n_s, n_r=n_r)
+    x = dict(x, q=(x["q"].float() * qs).bfloat16().contiguous())
+    s = synth.hadamard_signs(d, seed=9)
+    cache = build_cache(w, x, s, n_s=n_s)
+    out, ps, pr = kvq.attention_corrected(cache, x["q"].cuda(), x["k_cur"].cuda(),
+                                          x["v_cur"].cuda(), corr=kvq.CORR_EXACT, with_mass=True,
+                                          flags=flags)
+    torch.cuda.synchronize()
+    assert kvq.last_device_status() == 0
+    big = 0
+    for h in range(w.heads):
+        o_ref, ps_ref, pr_ref = oracle_head(w, x, s, 0, h, np.arange(n_q), O.CORR_EXACT, n_s=n_s)
+        assert_close(out[0, h].float().cpu().numpy(), o_ref, ps[0, h].cpu().numpy(), ps_ref,
+                     pr[0, h].cpu().numpy(), pr_ref, what=f"exact big d{d} g{group} h{h}")
+        # the case does reach the per-channel terms: a_c above 1 for some triples
+        kf = x["k_win"][0, h, :n_s].float().numpy()
+        _, kd, _, _, _ = O.quantize_rows(kf, s, w.bits, w.group)
+        qr = O.rotate(x["q"][0, h].float().numpy(), s)
+        amax = np.abs(qr).reshape(n_q, -1, group).max(-1)
+        big += int((0.5 * w.scale * amax[:, None, :] * kd[None, :, :] > 1.0).sum())
+    assert big > 0
+
+
+@pytest.mark.parametrize("name,flags,heads,rows", [("w4_int2", 0, 4, 32),
+                                                   ("hires_t3", kvq.FLAG_PRECISE_QUERY, 3, 16)])
+def test_full_workload_exact_sampled(name, flags, heads, rows):
+    """The exact correction on full-size workloads (the launch configuration
+    of ``bench.py --corr exact``): sampled heads and rows against the oracle.
+    The Gaussian-key window stays almost entirely within the series' range;
+    the heavy-tailed one (step sizes up to ~60) mostly leaves it."""
+    w = synth.WORKLOADS[name]
+    x = synth.inputs(w)
+    s = synth.hadamard_signs(w.head_dim)
+    cache = build_cache(w, x, s)
+    out, ps, pr = kvq.attention_corrected(cache, x["q"].cuda(), x["k_cur"].cuda(),
+                                          x["v_cur"].cuda(), corr=kvq.CORR_EXACT, with_mass=True,
+                                          flags=flags)
+    torch.cuda.synchronize()
+    assert kvq.last_device_status() == 0
+    rng = np.random.default_rng(12)
+    for h in rng.choice(w.heads, heads, replace=False):
+        sel = np.unique(np.concatenate([[0, w.n_q - 1], rng.choice(w.n_q, rows - 2, replace=False)]))
+        o_ref, ps_ref, pr_ref = oracle_head(w, x, s, 0, int(h), sel, O.CORR_EXACT)
+        assert_close(out[0, h, sel].float().cpu().numpy(), o_ref, ps[0, h, sel].cpu().numpy(),
+                     ps_ref, pr[0, h, sel].cpu().numpy(), pr_ref, what=f"exact {name} h{h}")
