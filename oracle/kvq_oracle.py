@@ -23,7 +23,11 @@ Compression in Video Diffusion" (Tuncer, Becker, Pfeil), cited below as
   keys' step sizes and the query norm, is subtracted before the softmax from
   cached-key scores only, with a second-order Taylor approximation;
 * Figure 2 caption / section 1: the attention masses P_S (cached block) and
-  P_R (current chunk).
+  P_R (current chunk);
+* section 2 (related work): per-channel key quantization (KIVI) is among the
+  schemes the correction is said to be orthogonal to -- the per-channel key
+  mode below quantizes each key channel over blocks of 128 tokens with the
+  same Eq. (1), and the correction keeps its form with one channel per group.
 
 Everything is fp64 except two steps that are fp32 on purpose, because the
 GPU must reproduce them bit for bit: the rotation that feeds the quantizer
@@ -183,6 +187,76 @@ def dequantize(codes, delta, zero, group: int) -> np.ndarray:
     cg = c.reshape(*lead, d // group, group)
     out = (cg - np.asarray(zero, np.float64)[..., None]) * np.asarray(delta, np.float64)[..., None]
     return out.reshape(*lead, d)
+
+
+# ---------------------------------------------------------------------------
+# Per-channel key quantization over token blocks (KIVI-style; the paper's
+# section 2 lists per-channel key quantization among the KV-cache schemes its
+# correction is orthogonal to)
+# ---------------------------------------------------------------------------
+
+KEY_BLOCK = 128
+
+
+def chunk_blocks(n_tokens: int, block: int = KEY_BLOCK):
+    """[start, end) of the token blocks of one appended chunk: consecutive
+    blocks of ``block`` tokens from the chunk's first token, the last one
+    shorter when the chunk is not a multiple of ``block``.
+
+    Reading: the scheme groups keys per channel along tokens; blocks restart
+    at every chunk, so a chunk is quantized when it is appended and never
+    again (no block spans two chunks)."""
+    return [(b, min(b + block, n_tokens)) for b in range(0, n_tokens, block)]
+
+
+def quantize_key_channels(y, bits: int, block: int = KEY_BLOCK):
+    """Per-channel quantization of one chunk's rotated fp32 keys y [n, d]:
+    for every block of tokens and every channel, Eq. (1) over that channel's
+    values in the block -- the same step, zero point and rounding as
+    ``quantize_groups``, with the group running along tokens instead of
+    channels.  Returns (codes uint8 [n, d], delta float32 [n_blocks, d],
+    zero float32 [n_blocks, d])."""
+    y = np.asarray(y, dtype=np.float32)
+    n, d = y.shape
+    blocks = chunk_blocks(n, block)
+    codes = np.empty((n, d), dtype=np.uint8)
+    delta = np.empty((len(blocks), d), dtype=np.float32)
+    zero = np.empty((len(blocks), d), dtype=np.float32)
+    for i, (a, b) in enumerate(blocks):
+        c, dl, z = quantize_groups(np.ascontiguousarray(y[a:b].T), bits, b - a)
+        codes[a:b] = c.T
+        delta[i] = dl[:, 0]
+        zero[i] = z[:, 0]
+    return codes, delta, zero
+
+
+def key_channel_token_steps(values, n_tokens: int, block: int = KEY_BLOCK) -> np.ndarray:
+    """Per-token view [n, d] of per-block, per-channel values [n_blocks, d]
+    (each token gets the row of its block)."""
+    v = np.asarray(values)
+    idx = np.array([i for i, (a, b) in enumerate(chunk_blocks(n_tokens, block)) for _ in range(a, b)],
+                   dtype=np.int64)
+    return v[idx]
+
+
+def dequantize_key_channels(codes, delta, zero, block: int = KEY_BLOCK) -> np.ndarray:
+    """x_hat = (x_q - z) * delta with each token's block's per-channel step
+    and zero point, fp64 (Eq. (1))."""
+    c = np.asarray(codes, dtype=np.float64)
+    n = c.shape[0]
+    dl = key_channel_token_steps(np.asarray(delta, np.float64), n, block)
+    z = key_channel_token_steps(np.asarray(zero, np.float64), n, block)
+    return (c - z) * dl
+
+
+def quantize_key_chunk(x_bf16, signs, bits: int, block: int = KEY_BLOCK):
+    """What one quantize-append computes for one chunk of BF16 keys [n, d]
+    in the per-channel key mode: the fp32 rotation, then
+    ``quantize_key_channels``.  Returns (packed codes, delta, zero, rotated
+    fp32, codes)."""
+    y = rotate_fp32(np.asarray(x_bf16, dtype=np.float32), signs)
+    codes, delta, zero = quantize_key_channels(y, bits, block)
+    return pack_codes(codes, bits), delta, zero, y, codes
 
 
 # ---------------------------------------------------------------------------

@@ -183,6 +183,118 @@ def check_pack_roundtrip():
 
 
 # --------------------------------------------------------------------------
+# Per-channel key quantization over token blocks (section 2: KIVI-style
+# per-channel keys; Eq. (1) per group)
+# --------------------------------------------------------------------------
+
+
+def check_key_channel_hand_fixture():
+    for line in _rows("key_channel.txt"):
+        parts = [p.strip() for p in line.split("|")]
+        bits = int(parts[0])
+        y = np.array([[float(v) for v in t.split()] for t in parts[1].split(";")], dtype=np.float32)
+        d_want = np.array([float(v) for v in parts[2].split()])
+        z_want = np.array([float(v) for v in parts[3].split()])
+        c_want = np.array([[int(v) for v in t.split()] for t in parts[4].split(";")])
+        codes, delta, zero = O.quantize_key_channels(y, bits)
+        assert np.array_equal(delta[0], d_want.astype(np.float32)), (line, delta)
+        assert np.array_equal(zero[0], z_want.astype(np.float32)), (line, zero)
+        assert np.array_equal(codes, c_want), (line, codes)
+        xh = O.dequantize_key_channels(codes, delta, zero)
+        assert np.array_equal(xh, (c_want - z_want[None]) * d_want[None])
+
+
+def check_key_channel_blocks():
+    """Blocks of 128 tokens from each chunk's first token (the last one
+    shorter); a block's steps, zero points and codes depend on its own
+    tokens only; every unclamped element within half a step, every code the
+    nearest grid point of its channel (brute force over all codes)."""
+    assert O.chunk_blocks(300) == [(0, 128), (128, 256), (256, 300)]
+    assert O.chunk_blocks(128) == [(0, 128)]
+    assert O.chunk_blocks(1) == [(0, 1)]
+    rng = np.random.default_rng(21)
+    for bits in (2, 4):
+        y = (rng.standard_normal((300, 64)) * rng.uniform(0.2, 4, (1, 64))
+             + rng.standard_normal((1, 64))).astype(np.float32)
+        codes, delta, zero = O.quantize_key_channels(y, bits)
+        assert delta.shape == (3, 64) and codes.shape == (300, 64)
+        y2 = y.copy()
+        y2[5] *= 7.0                                 # a token of block 0 only
+        c2, d2, z2 = O.quantize_key_channels(y2, bits)
+        assert np.array_equal(c2[128:], codes[128:]) and np.array_equal(d2[1:], delta[1:])
+        assert not np.array_equal(d2[0], delta[0])
+        qmax = 2 ** bits - 1
+        dl = O.key_channel_token_steps(delta.astype(np.float64), 300)
+        zz = O.key_channel_token_steps(zero.astype(np.float64), 300)
+        xh = O.dequantize_key_channels(codes, delta, zero)
+        err = np.abs(xh - y)
+        unclamped = (codes > 0) & (codes < qmax)
+        assert np.all(err[unclamped] <= dl[unclamped] / 2 * (1 + 1e-6))
+        cands = (np.arange(qmax + 1)[None, None, :] - zz[..., None]) * dl[..., None]
+        best = np.abs(cands - y[..., None].astype(np.float64)).min(axis=-1)
+        assert np.all(err <= best + 1e-6 * dl)
+        # per channel, the step covers the block's range (BF16 rounding aside)
+        for i, (a, b) in enumerate(O.chunk_blocks(300)):
+            rng_c = y[a:b].max(0).astype(np.float64) - y[a:b].min(0)
+            assert np.all(np.abs(delta[i] - rng_c / qmax) <= delta[i] * 2 ** -8 + 1e-30)
+
+
+def check_key_channel_bias_brute_force():
+    """With per-channel key steps the correction keeps its form with one
+    channel per group: b_Taylor = scale^2 / 24 * sum_c q'_c^2 D_c^2 and
+    b_exact = sum_c log(sinh a_c / a_c), a_c = scale |q'_c| D_c / 2, D_c the
+    step of the key's block in channel c (loops, fp64)."""
+    rng = np.random.default_rng(22)
+    d, scale = 8, 0.35
+    q = rng.standard_normal((3, d))
+    dl = rng.uniform(0.05, 1.5, (4, d))
+    bt = O.jensen_bias_taylor(q, dl, scale, 1)
+    be = O.jensen_bias_exact(q, dl, scale, 1)
+    for j in range(3):
+        for i in range(4):
+            t = sum(scale * scale / 24 * q[j, c] ** 2 * dl[i, c] ** 2 for c in range(d))
+            e = 0.0
+            for c in range(d):
+                a = 0.5 * scale * abs(q[j, c]) * dl[i, c]
+                e += math.log(math.sinh(a) / a)
+            assert abs(bt[j, i] - t) <= 1e-14 * abs(t)
+            assert abs(be[j, i] - e) <= 1e-12 * abs(e)
+
+
+def check_key_channel_mass_shift():
+    """The per-channel key scheme shows the same Jensen effect (Figure 2 /
+    section 1: quantized keys take mass from the current chunk) and the same
+    correction, with per-channel steps, undoes most of it (section 2: the
+    correction is orthogonal to the quantization scheme)."""
+    rng = np.random.default_rng(23)
+    d, n_q, n_r, chunk, n_chunks, scale = 64, 256, 256, 256, 4, 1 / 8
+    s = np.where(rng.integers(0, 2, d) == 1, -1.0, 1.0).astype(np.float32)
+    q = O.bf16_round(rng.standard_normal((n_q, d)).astype(np.float32))
+    kc = O.bf16_round(rng.standard_normal((n_r, d)).astype(np.float32))
+    vc = O.bf16_round(rng.standard_normal((n_r, d)).astype(np.float32))
+    k = rng.standard_normal((chunk * n_chunks, d)).astype(np.float32)
+    k[:, :4] *= 8
+    k = O.bf16_round(k)
+    v = O.bf16_round(rng.standard_normal((chunk * n_chunks, d)).astype(np.float32))
+    kh, steps = [], []
+    for c0 in range(0, k.shape[0], chunk):
+        _, kd, kz, _, codes = O.quantize_key_chunk(k[c0:c0 + chunk], s, 2)
+        kh.append(O.dequantize_key_channels(codes, kd, kz))
+        steps.append(O.key_channel_token_steps(kd, chunk))
+    kh = np.concatenate(kh)
+    steps = np.concatenate(steps)
+    vr = O.rotate(v, s)
+    _, ps_ref, _ = O.chunk_attention(q, O.rotate(k, s), vr, np.zeros((k.shape[0], 1)), kc, vc, s,
+                                     scale, 1, O.CORR_NONE)
+    ps = {c: O.chunk_attention(q, kh, vr, steps, kc, vc, s, scale, 1, c)[1]
+          for c in (O.CORR_NONE, O.CORR_TAYLOR, O.CORR_EXACT)}
+    shift = ps[O.CORR_NONE].mean() - ps_ref.mean()
+    assert shift > 1e-2
+    assert abs(ps[O.CORR_TAYLOR].mean() - ps_ref.mean()) < 0.25 * shift
+    assert abs(ps[O.CORR_EXACT].mean() - ps_ref.mean()) < 0.25 * shift
+
+
+# --------------------------------------------------------------------------
 # Jensen bias (Figure 3 caption; abstract; section 1)
 # --------------------------------------------------------------------------
 

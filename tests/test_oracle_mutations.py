@@ -100,7 +100,27 @@ def _fwht_no_scale(x, signs):
     return (_real_fwht(x, signs) * np.float32(np.sqrt(np.asarray(x).shape[-1]))).astype(np.float32)
 
 
+_real_key_channels = O.quantize_key_channels
+
+
+def _key_channels_per_token(y, bits, block=O.KEY_BLOCK):
+    # wrong axis: one group per token (all its channels) instead of per channel
+    y = np.asarray(y, dtype=np.float32)
+    n, d = y.shape
+    codes, dl, z = O.quantize_groups(y, bits, d)
+    blocks = O.chunk_blocks(n, block)
+    return (codes, np.stack([np.full(d, dl[a, 0]) for a, _ in blocks]).astype(np.float32),
+            np.stack([np.full(d, z[a, 0]) for a, _ in blocks]).astype(np.float32))
+
+
+def _chunk_blocks_whole_chunk(n_tokens, block=O.KEY_BLOCK):
+    # wrong partition: one block over the whole chunk
+    return [(0, n_tokens)]
+
+
 MUTANTS = {
+    "key_channels_per_token": ("quantize_key_channels", _key_channels_per_token),
+    "key_blocks_whole_chunk": ("chunk_blocks", _chunk_blocks_whole_chunk),
     "bias_sign_flipped": ("jensen_bias_taylor", _bias_sign_flipped),
     "bias_factor_12": ("jensen_bias_taylor", _bias_factor_12),
     "bias_dropped_group_terms": ("jensen_bias_taylor", _bias_unrotated_norms),
