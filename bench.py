@@ -142,7 +142,8 @@ def run_gpu(args):
     signs = synth.hadamard_signs(w.head_dim, seed=args.seed)
     B, H, d = w.batch, w.heads, w.head_dim
 
-    cache = kvq.KVCache(B, H, d, w.bits, w.group, w.chunk_tokens, w.n_chunks, signs, device=dev)
+    cache = kvq.KVCache(B, H, d, w.bits, w.group, w.chunk_tokens, w.n_chunks, signs, device=dev,
+                        key_mode=args.key_mode)
     kwin, vwin = x["k_win"].to(dev), x["v_win"].to(dev)
     for c in range(w.n_chunks):
         sl = slice(c * w.chunk_tokens, (c + 1) * w.chunk_tokens)
@@ -200,7 +201,9 @@ def run_gpu(args):
 
     # per-kernel device times inside the timed region (CUDA events on the launch stream)
     k3_ms = prof["attention"]["ms_total"] / max(1, prof["attention"]["launches"])
-    k1_ms = prof["quantize_append"]["ms_total"] / max(1, prof["quantize_append"]["launches"])
+    # per step: the per-channel key mode appends with two launches (values per
+    # token, keys per channel)
+    k1_ms = prof["quantize_append"]["ms_total"] / args.steps
     k2_ms = prof["rotate"]["ms_total"] / max(1, prof["rotate"]["launches"])
     hbm, bf16_burst, bf16_sust, peak_kind = _peaks()
     k3_tflops = flops / (k3_ms * 1e-3) / 1e12
@@ -288,7 +291,9 @@ def run_gpu(args):
             "config": _config(w, {
                 "l2": f"inputs larger than L2: {ws_bytes / 1e6:.0f} MB read per step vs 129 MB L2",
                 "parallelism": f"replicas x{world} (heads independent, no collective)",
-                "correction": CORR_NAMES[args.corr], "flags": args.flags}),
+                "correction": CORR_NAMES[args.corr], "flags": args.flags,
+                "keys": "per channel over 128-token blocks" if args.key_mode else
+                        "per token and group"}),
             "clocks": clk,
             "e2e": {"value": round(flops * world / (e2e_ms * 1e-3) / 1e12, 3), "unit": UNIT,
                     "ms_per_step": round(e2e_ms, 4),
@@ -417,12 +422,16 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--precise-query", dest="flags", action="store_const", const=1, default=0,
                     help="split the rotated query into FP16 high + low parts")
+    ap.add_argument("--keys", choices=["token", "channel"], default="token",
+                    help="key quantization: per token and group (default) or per channel over "
+                         "128-token blocks of each chunk (KIVI-style)")
     ap.add_argument("--corr", choices=["taylor", "exact", "none"], default="taylor",
                     help="correction of the cached scores (default: the second-order Taylor "
                          "term; exact: log(sinh a / a) per channel)")
     args = ap.parse_args(argv)
     args.warmup = max(3, args.warmup)   # at least 3 untimed warm-up steps
     args.corr = {v: k for k, v in CORR_NAMES.items()}[args.corr]
+    args.key_mode = 1 if args.keys == "channel" else 0
     if args.impl == "reference":
         return run_reference(args)
     return run_gpu(args)

@@ -70,6 +70,23 @@ typedef enum {
 #define KVQ_FLAG_NO_KV_SPLIT 2
 
 /*
+ * Key quantization scheme of a cache (kvq_cache.key_mode).
+ * KVQ_KEYS_PER_TOKEN: keys like values, per token and group of `group`
+ *   channels (paper section 3, "Quantization granularity").
+ * KVQ_KEYS_PER_CHANNEL: keys per channel over blocks of KVQ_KEY_BLOCK tokens,
+ *   the blocks counted from the first token of every appended chunk (the
+ *   last block of a chunk may be shorter); values stay per token and group.
+ *   This is the KIVI-style per-channel key quantization the paper's section 2
+ *   lists among the schemes its correction is orthogonal to.  The correction
+ *   keeps its form with one channel per group:
+ *   b_ij = scale^2 / 24 * sum_c q'_{j,c}^2 * D_{c,blk(i)}^2 (TAYLOR), or the
+ *   exact sum_c log(sinh a_c / a_c) with a_c = scale/2 |q'_{j,c}| D_{c,blk(i)}.
+ */
+#define KVQ_KEYS_PER_TOKEN 0
+#define KVQ_KEYS_PER_CHANNEL 1
+#define KVQ_KEY_BLOCK 128
+
+/*
  * Quantized sliding-window KV cache (paper section 1: the current chunk
  * attends to the last n cached chunks; section 3 "Integer quantization",
  * Eq. (1), and "Quantization granularity": per-token groups of `group`
@@ -92,6 +109,12 @@ typedef enum {
  *   k_sz, v_sz        bf16   [batch][heads][capacity][head_dim / group][2]
  *       (step size, zero point) per token and group; the zero point is an
  *       integer stored as BF16.
+ *   With key_mode = KVQ_KEYS_PER_CHANNEL, k_sz instead holds
+ *       bf16 [batch][heads][n_chunks][ceil(chunk_tokens / KVQ_KEY_BLOCK)]
+ *       [head_dim][2]: (step size, zero point) per key block and channel
+ *       (block b of slot s covers tokens s * chunk_tokens + [128 b, 128 b +
+ *       128)); k_codes keeps the per-token layout above.
+ * key_mode: KVQ_KEYS_PER_TOKEN (0) or KVQ_KEYS_PER_CHANNEL (1).
  */
 typedef struct kvq_cache {
   int32_t batch, heads, head_dim, bits, group;
@@ -100,6 +123,7 @@ typedef struct kvq_cache {
   uint32_t sign_bits[4];
   uint8_t *k_codes, *v_codes;
   uint16_t *k_sz, *v_sz;
+  int32_t key_mode;
 } kvq_cache;
 
 /* Human-readable name of a status code (static string, never NULL). */
@@ -109,12 +133,21 @@ const char *kvq_status_string(kvq_status s);
 int32_t kvq_abi_version(void);
 
 /*
- * Bytes of ONE codes buffer and ONE (step, zero) buffer for this geometry
- * (k and v each need one of both).  Returns KVQ_ERR_INVALID_ARG /
- * KVQ_ERR_UNSUPPORTED for a bad geometry.  Host only; no CUDA call.
+ * Bytes of ONE codes buffer and of the larger of the two (step, zero)
+ * buffers for this geometry (k and v each need a codes buffer of
+ * codes_bytes; sz_bytes is enough for either of k_sz and v_sz).  Returns
+ * KVQ_ERR_INVALID_ARG / KVQ_ERR_UNSUPPORTED for a bad geometry.  Host only;
+ * no CUDA call.
  */
 kvq_status kvq_cache_bytes(const kvq_cache *cache, size_t *codes_bytes,
                            size_t *sz_bytes);
+
+/*
+ * Exact bytes of k_sz and of v_sz (they differ with KVQ_KEYS_PER_CHANNEL).
+ * Host only; no CUDA call.
+ */
+kvq_status kvq_cache_meta_bytes(const kvq_cache *cache, size_t *k_sz_bytes,
+                                size_t *v_sz_bytes);
 
 /*
  * Quantize-append one chunk (paper section 3: Hadamard rotation, then
@@ -125,7 +158,9 @@ kvq_status kvq_cache_bytes(const kvq_cache *cache, size_t *codes_bytes,
  * mn/mx; D = bf16((mx - mn) / (2^bits - 1)) (constant group: D = bf16(|mn|),
  * or 1); z = bf16(rint(-mn / D)); code = clamp(rint(x' / D) + z, 0, 2^bits-1)
  * (IEEE fp32, ties to even).  Writes slot `head_slot` (tokens
- * [head_slot * chunk_tokens, + n_new)).
+ * [head_slot * chunk_tokens, + n_new)).  With KVQ_KEYS_PER_CHANNEL the keys
+ * take the same steps per channel over each block of KVQ_KEY_BLOCK tokens of
+ * the chunk (mn/mx over the block's values of that channel).
  * Window rules: 0 <= n_new <= chunk_tokens (0 is a no-op); while the cache is
  * not full every earlier slot must be full (a partial chunk can only be the
  * last one appended); once full only whole chunks overwrite the oldest slot.

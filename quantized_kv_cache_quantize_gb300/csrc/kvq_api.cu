@@ -64,6 +64,8 @@ kvq_status check_geometry(const kvq_cache* c, kvq::Geometry* g) {
   if (bh > (1 << 16) || cap > (1LL << 30) || bh * cap > (1LL << 40)) return KVQ_ERR_INVALID_ARG;
   if (c->len < 0 || c->len > cap || c->head_slot < 0 || c->head_slot >= c->n_chunks)
     return KVQ_ERR_INVALID_ARG;
+  if (c->key_mode != KVQ_KEYS_PER_TOKEN && c->key_mode != KVQ_KEYS_PER_CHANNEL)
+    return KVQ_ERR_INVALID_ARG;
   g->bh = (int)bh;
   g->d = c->head_dim;
   g->bits = c->bits;
@@ -71,7 +73,15 @@ kvq_status check_geometry(const kvq_cache* c, kvq::Geometry* g) {
   g->g = c->head_dim / c->group;
   g->cap = (int)cap;
   g->code_bytes = c->head_dim * c->bits / 8;
+  g->key_mode = c->key_mode;
+  g->bpc = (c->chunk_tokens + KVQ_KEY_BLOCK - 1) / KVQ_KEY_BLOCK;
   return KVQ_OK;
+}
+
+// bytes of k_sz and v_sz
+void meta_bytes(const kvq::Geometry& g, int n_chunks, size_t* k, size_t* v) {
+  *v = (size_t)g.bh * g.cap * g.g * 4;
+  *k = g.key_mode == KVQ_KEYS_PER_CHANNEL ? (size_t)g.bh * n_chunks * g.bpc * g.d * 4 : *v;
 }
 
 kvq_status check_cache_buffers(const kvq_cache* c) {
@@ -88,22 +98,32 @@ struct Workspace {
   uint16_t* v;     // rotated current-chunk values, FP16
   float* o_part;   // key-range split: partial O, fp32 (splits > 1)
   float* st_part;  // key-range split: base and sums per row (splits > 1)
+  float* kch_c;    // per-channel keys: correction per row and cached tile
   size_t bytes;
 };
 
-Workspace carve(void* base, const kvq::Geometry& g, int n_q, int n_r, int splits) {
+// the largest number of cached tiles a window of this cache can have
+int max_cached_tiles(const kvq::Geometry& g, int n_chunks, int chunk) {
+  return kvq::cached_tiles(g.key_mode, n_chunks * chunk, chunk, g.bpc);
+}
+
+// kch_tiles: cached tiles the per-(row, tile) correction table holds (0
+// without per-channel keys)
+Workspace carve(void* base, const kvq::Geometry& g, int n_q, int n_r, int splits, int kch_tiles) {
   Workspace w;
   const size_t qb = round_up((size_t)g.bh * n_q * g.d * 2, 256);
   const size_t rb = round_up((size_t)g.bh * n_r * g.d * 2, 256);
   const size_t ob = splits > 1 ? round_up((size_t)splits * g.bh * n_q * g.d * 4, 256) : 0;
   const size_t sb = splits > 1 ? round_up((size_t)splits * g.bh * n_q * 3 * 4, 256) : 0;
+  const size_t cb = round_up((size_t)kch_tiles * g.bh * n_q * 4, 256);
   uint8_t* p = static_cast<uint8_t*>(base);
   w.q_hi = reinterpret_cast<uint16_t*>(p);
   w.q_lo = reinterpret_cast<uint16_t*>(p + qb);
   w.v = reinterpret_cast<uint16_t*>(p + 2 * qb);
   w.o_part = reinterpret_cast<float*>(p + 2 * qb + rb);
   w.st_part = reinterpret_cast<float*>(p + 2 * qb + rb + ob);
-  w.bytes = 2 * qb + rb + ob + sb;
+  w.kch_c = reinterpret_cast<float*>(p + 2 * qb + rb + ob + sb);
+  w.bytes = 2 * qb + rb + ob + sb + cb;
   return w;
 }
 
@@ -116,10 +136,10 @@ int device_sm_count() {
 
 // key-range split of one launch (1 = none); rows per CTA: 256, or 128 with
 // the precise-query flag or the exact correction (one query tile per CTA)
-int split_for(const kvq::Geometry& g, int n_q, int n_s, int n_r, bool one_tile, int sms,
+int split_for(const kvq::Geometry& g, int n_q, int n_ct, int n_r, bool one_tile, int sms,
               int max_splits, int* per) {
   int splits = 1;
-  kvq::attention_split(g.bh, n_q, n_s, n_r, g.d, one_tile ? 128 : 256, sms, max_splits, &splits,
+  kvq::attention_split(g.bh, n_q, n_ct, n_r, g.d, one_tile ? 128 : 256, sms, max_splits, &splits,
                        per);
   return splits;
 }
@@ -128,13 +148,14 @@ int split_for(const kvq::Geometry& g, int n_q, int n_s, int n_r, bool one_tile, 
 // split the current device takes on a full window (n_s = the cache's
 // capacity); a shorter window whose best split needs more room takes the best
 // split that fits
-size_t workspace_bytes_any(const kvq::Geometry& g, int n_q, int n_s, int n_r) {
+size_t workspace_bytes_any(const kvq::Geometry& g, int n_q, int n_ct, int n_r) {
   const int sms = device_sm_count();
+  const int kch = g.key_mode == KVQ_KEYS_PER_CHANNEL ? n_ct : 0;
   size_t best = 0;
   for (int one_tile = 0; one_tile < 2; ++one_tile) {
     int per = 0;
-    const int sp = split_for(g, n_q, n_s, n_r, one_tile != 0, sms, 64, &per);
-    const size_t b = carve(nullptr, g, n_q, n_r, sp).bytes;
+    const int sp = split_for(g, n_q, n_ct, n_r, one_tile != 0, sms, 64, &per);
+    const size_t b = carve(nullptr, g, n_q, n_r, sp, kch).bytes;
     if (b > best) best = b;
   }
   return best;
@@ -153,7 +174,10 @@ kvq_status attention_common(const kvq_cache* cache, const uint16_t* q, const uin
     return KVQ_ERR_INVALID_ARG;
   if ((flags & ~(KVQ_FLAG_PRECISE_QUERY | KVQ_FLAG_NO_KV_SPLIT)) != 0) return KVQ_ERR_INVALID_ARG;
   const bool precise = (flags & KVQ_FLAG_PRECISE_QUERY) != 0;
-  const bool one_tile = precise || corr == KVQ_CORR_EXACT;   // one query tile per CTA
+  // one query tile per CTA: the precise-query split, or the exact correction
+  // computed in the attention kernel (per-channel keys take it from a pre-pass)
+  const bool one_tile =
+      precise || (corr == KVQ_CORR_EXACT && cache->key_mode != KVQ_KEYS_PER_CHANNEL);
   if (!std::isfinite(scale) || scale <= 0.f) return KVQ_ERR_INVALID_ARG;
   if ((p_s == nullptr) != (p_r == nullptr)) return KVQ_ERR_INVALID_ARG;
   if (mass_only && p_s == nullptr) return KVQ_ERR_INVALID_ARG;
@@ -172,14 +196,20 @@ kvq_status attention_common(const kvq_cache* cache, const uint16_t* q, const uin
   if (workspace == nullptr) return KVQ_ERR_INVALID_ARG;
   // key-range split when the grid would not fill the device (and the
   // workspace holds the partial results; otherwise one range)
+  const int n_ct = kvq::cached_tiles(g.key_mode, cache->len, cache->chunk_tokens, g.bpc);
+  // per-channel keys with a correction: a table of one number per row and
+  // cached tile
+  const bool kch = g.key_mode == KVQ_KEYS_PER_CHANNEL;
+  const int kch_tiles = kch && corr != KVQ_CORR_NONE ? n_ct : 0;
   int per = 0, splits = 1;
   if ((flags & KVQ_FLAG_NO_KV_SPLIT) == 0) {
     int max_splits = 64;
-    while (max_splits > 1 && carve(nullptr, g, n_q, n_r, max_splits).bytes > workspace_bytes)
+    while (max_splits > 1 &&
+           carve(nullptr, g, n_q, n_r, max_splits, kch_tiles).bytes > workspace_bytes)
       --max_splits;
-    splits = split_for(g, n_q, cache->len, n_r, one_tile, device_sm_count(), max_splits, &per);
+    splits = split_for(g, n_q, n_ct, n_r, one_tile, device_sm_count(), max_splits, &per);
   }
-  const Workspace ws = carve(workspace, g, n_q, n_r, splits);
+  const Workspace ws = carve(workspace, g, n_q, n_r, splits, kch_tiles);
   if (workspace_bytes < ws.bytes) return KVQ_ERR_INVALID_ARG;
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -229,6 +259,12 @@ kvq_status attention_common(const kvq_cache* cache, const uint16_t* q, const uin
   a.tiles_per_split = per;
   a.o_part = ws.o_part;
   a.st_part = ws.st_part;
+  a.key_mode = g.key_mode;
+  a.chunk = cache->chunk_tokens;
+  a.bpc = g.bpc;
+  a.kblk_per_head = cache->n_chunks * g.bpc;
+  a.n_ct = n_ct;
+  a.kch_c = kch_tiles > 0 ? ws.kch_c : nullptr;
   ProfScope prof(2, s);
   return kvq::launch_attention(a, g.d, g.bits, g.group, s);
 }
@@ -252,14 +288,27 @@ const char* kvq_status_string(kvq_status s) {
   return "unknown status";
 }
 
-int32_t kvq_abi_version(void) { return 1; }
+int32_t kvq_abi_version(void) { return 2; }
 
 kvq_status kvq_cache_bytes(const kvq_cache* cache, size_t* codes_bytes, size_t* sz_bytes) {
   kvq::Geometry g;
   const kvq_status st = check_geometry(cache, &g);
   if (st != KVQ_OK) return st;
+  size_t k = 0, v = 0;
+  meta_bytes(g, cache->n_chunks, &k, &v);
   if (codes_bytes) *codes_bytes = (size_t)g.bh * g.cap * g.code_bytes;
-  if (sz_bytes) *sz_bytes = (size_t)g.bh * g.cap * g.g * 4;
+  if (sz_bytes) *sz_bytes = k > v ? k : v;
+  return KVQ_OK;
+}
+
+kvq_status kvq_cache_meta_bytes(const kvq_cache* cache, size_t* k_sz_bytes, size_t* v_sz_bytes) {
+  kvq::Geometry g;
+  const kvq_status st = check_geometry(cache, &g);
+  if (st != KVQ_OK) return st;
+  size_t k = 0, v = 0;
+  meta_bytes(g, cache->n_chunks, &k, &v);
+  if (k_sz_bytes) *k_sz_bytes = k;
+  if (v_sz_bytes) *v_sz_bytes = v;
   return KVQ_OK;
 }
 
@@ -300,12 +349,24 @@ kvq_status kvq_quantize_append(kvq_cache* cache, const uint16_t* k_new, const ui
   a.first = first;
   for (int i = 0; i < 4; ++i) a.sign_bits[i] = cache->sign_bits[i];
   a.inv_sqrt_d = (float)(1.0 / std::sqrt((double)g.d));
+  a.v_only = g.key_mode == KVQ_KEYS_PER_CHANNEL ? 1 : 0;
+  a.kblk_first = cache->head_slot * g.bpc;
+  a.kblk_per_head = cache->n_chunks * g.bpc;
   bool supported = true;
-  ProfScope prof(0, static_cast<cudaStream_t>(stream));
-  if (kvq::launch_quantize_append(a, g.d, g.bits, g.group, static_cast<cudaStream_t>(stream),
-                                  &supported) != cudaSuccess)
-    return KVQ_ERR_CUDA;
-  if (!supported) return KVQ_ERR_UNSUPPORTED;
+  {
+    ProfScope prof(0, static_cast<cudaStream_t>(stream));
+    if (kvq::launch_quantize_append(a, g.d, g.bits, g.group, static_cast<cudaStream_t>(stream),
+                                    &supported) != cudaSuccess)
+      return KVQ_ERR_CUDA;
+    if (!supported) return KVQ_ERR_UNSUPPORTED;
+  }
+  if (g.key_mode == KVQ_KEYS_PER_CHANNEL) {
+    ProfScope prof(0, static_cast<cudaStream_t>(stream));
+    if (kvq::launch_quantize_key_channels(a, g.d, g.bits, static_cast<cudaStream_t>(stream),
+                                          &supported) != cudaSuccess)
+      return KVQ_ERR_CUDA;
+    if (!supported) return KVQ_ERR_UNSUPPORTED;
+  }
   cache->len = new_len;
   cache->head_slot = (cache->head_slot + 1) % cache->n_chunks;
   return KVQ_OK;
@@ -315,7 +376,7 @@ size_t kvq_workspace_bytes(const kvq_cache* cache, int32_t n_q, int32_t n_r) {
   kvq::Geometry g;
   if (check_geometry(cache, &g) != KVQ_OK || n_q < 0 || n_r < 0) return 0;
   // the split is sized for a full window (len can only grow up to capacity)
-  return workspace_bytes_any(g, n_q, g.cap, n_r);
+  return workspace_bytes_any(g, n_q, max_cached_tiles(g, cache->n_chunks, cache->chunk_tokens), n_r);
 }
 
 kvq_status kvq_attention_corrected(const kvq_cache* cache, const uint16_t* q,
@@ -448,7 +509,11 @@ extern "C" kvq_status kvq_attention_corrected_noalloc(const kvq_cache* cache, co
   const kvq_status st = check_geometry(cache, &g);
   if (st != KVQ_OK) return st;
   if (n_q < 0 || n_r < 0) return KVQ_ERR_INVALID_ARG;
-  if (carve(nullptr, g, n_q, n_r, 1).bytes > (size_t)KVQ_NOALLOC_SCRATCH_BYTES) return KVQ_ERR_TOO_LARGE;
+  const int kch_tiles = g.key_mode == KVQ_KEYS_PER_CHANNEL && corr != KVQ_CORR_NONE
+                            ? kvq::cached_tiles(g.key_mode, cache->len, cache->chunk_tokens, g.bpc)
+                            : 0;
+  if (carve(nullptr, g, n_q, n_r, 1, kch_tiles).bytes > (size_t)KVQ_NOALLOC_SCRATCH_BYTES)
+    return KVQ_ERR_TOO_LARGE;
   void* scratch = nullptr;
   const kvq_status sst = noalloc_scratch(&scratch);
   if (sst != KVQ_OK) return sst;

@@ -19,6 +19,8 @@ struct Geometry {
   int g;           // groups per token (d / group)
   int cap;         // tokens per head
   int code_bytes;  // packed bytes per token
+  int key_mode;    // KVQ_KEYS_PER_TOKEN / KVQ_KEYS_PER_CHANNEL
+  int bpc;         // key blocks per chunk slot (per-channel keys)
 };
 
 // Arguments of the quantize-append kernel.
@@ -35,6 +37,11 @@ struct QuantArgs {
   int first;       // first token written in every head
   uint32_t sign_bits[4];
   float inv_sqrt_d;
+  int v_only;      // per-channel key mode: the per-token kernels quantize the V rows only
+  // per-channel key mode: k_sz holds kblk_per_head blocks of d words per
+  // head; this append's blocks start at block kblk_first
+  int kblk_first;
+  int kblk_per_head;
 };
 
 // Arguments of the rotation kernel: up to two row segments in one launch.
@@ -67,6 +74,11 @@ cudaError_t ensure_smem_limit(Kernel kern, int bytes, std::atomic<uint64_t>& don
 
 cudaError_t launch_quantize_append(const QuantArgs& a, int d, int bits, int group,
                                    cudaStream_t stream, bool* supported);
+// per-channel key mode: the K rows of one append, per channel over blocks of
+// kKeyBlock tokens
+constexpr int kKeyBlock = 128;
+cudaError_t launch_quantize_key_channels(const QuantArgs& a, int d, int bits,
+                                         cudaStream_t stream, bool* supported);
 cudaError_t launch_rotate(const RotateArgs& a, int d, cudaStream_t stream);
 
 // Attention ---------------------------------------------------------------
@@ -100,7 +112,21 @@ struct AttnLaunch {
   int splits, tiles_per_split;
   float* o_part;    // [splits][bh][n_q][d] fp32
   float* st_part;   // [splits][bh][n_q][3] fp32
+  // per-channel keys (key_mode = KVQ_KEYS_PER_CHANNEL): cached tile t is key
+  // block t % bpc of chunk slot t / bpc; n_ct cached tiles; kch_c [bh][n_ct]
+  // [n_q] fp32 workspace for the per-(row, tile) correction
+  int key_mode, chunk, bpc, kblk_per_head, n_ct;
+  float* kch_c;
+  int* status;      // device status word, set by launch_attention
 };
+
+// cached key tiles of a window of n_s tokens: 128-token tiles, or with
+// per-channel keys the key blocks of each chunk slot
+inline int cached_tiles(int key_mode, int n_s, int chunk, int bpc) {
+  if (key_mode != KVQ_KEYS_PER_CHANNEL) return (n_s + 127) / 128;
+  const int full = n_s / chunk;
+  return full * bpc + (n_s - full * chunk + 127) / 128;
+}
 
 // Key-range split of a launch whose grid (bh * query tiles of rows_per_cta)
 // does not fill the GPU: enough ranges for about one wave of CTAs, each at
@@ -118,9 +144,9 @@ struct AttnLaunch {
 constexpr int kCtaFixed = 2;
 constexpr double kBytesPerTileTime = 12e6;
 
-inline void attention_split(long long bh, int n_q, int n_s, int n_r, int d, int rows_per_cta,
+inline void attention_split(long long bh, int n_q, int n_ct, int n_r, int d, int rows_per_cta,
                             int sms, int max_splits, int* splits, int* tiles_per_split) {
-  const int n_t = (n_s + 127) / 128 + (n_r + 127) / 128;
+  const int n_t = n_ct + (n_r + 127) / 128;
   *splits = 1;
   *tiles_per_split = n_t > 0 ? n_t : 1;
   const long long ctas = bh * ((n_q + rows_per_cta - 1) / rows_per_cta);
@@ -145,6 +171,12 @@ inline void attention_split(long long bh, int n_q, int n_s, int n_r, int d, int 
 
 kvq_status launch_attention(const AttnLaunch& a, int d, int bits, int group,
                             cudaStream_t stream);
+// the attention kernels of the exact correction and of per-channel keys,
+// built in translation units of their own (a.status must be set)
+kvq_status launch_attention_exact(const AttnLaunch& a, int d, int bits, int group,
+                                  cudaStream_t stream);
+kvq_status launch_attention_kch(const AttnLaunch& a, int d, int bits, int group,
+                                cudaStream_t stream);
 kvq_status read_and_clear_attention_status(int* status);
 cudaError_t launch_wait_selftest(unsigned long long limit_ns, cudaStream_t stream);
 

@@ -290,13 +290,14 @@ __global__ void __launch_bounds__(kQWarps * 32, kQBlocksPerSm)
   uint8_t* stage = qsm + wib * 2 * TILE;
   const unsigned per_kv = (unsigned)a.bh * (unsigned)a.n_new;   // < 2^30 (host check)
   const unsigned total = 2u * per_kv;
-  const unsigned n_tiles = (total + 31u) / 32u;
+  const unsigned row_begin = a.v_only ? per_kv : 0u;              // V rows only
+  const unsigned n_tiles = (total - row_begin + 31u) / 32u;
   const unsigned n_warps = gridDim.x * kQWarps;
   auto issue = [&](unsigned tile, uint8_t* dst) {
 #pragma unroll
     for (int j = 0; j < CH; ++j) {
       const int row = j * RPI + lane / CH, chunk = lane % CH;
-      const unsigned r = tile * 32u + (unsigned)row;
+      const unsigned r = row_begin + tile * 32u + (unsigned)row;
       if (r < total) {
         const bool is_v = r >= per_kv;
         const uint16_t* src = (is_v ? a.v_new : a.k_new) + (size_t)(is_v ? r - per_kv : r) * D + chunk * 8;
@@ -316,7 +317,7 @@ __global__ void __launch_bounds__(kQWarps * 32, kQBlocksPerSm)
       cp_async_wait<0>();
     }
     __syncwarp();
-    const unsigned r = tile * 32u + (unsigned)lane;
+    const unsigned r = row_begin + tile * 32u + (unsigned)lane;
     if (r < total) quantize_row<D, BITS, GROUP>(a, sg, stage + (k & 1) * TILE, lane, r, per_kv);
     // every lane is done with this stage before the copy two tiles on
     __syncwarp();
@@ -509,7 +510,7 @@ __global__ void __launch_bounds__(kSplitWarps * 32, kSplitBlocksPerSm)
     }
     cp_async_commit();
   };
-  unsigned tile = blockIdx.x * (kSplitWarps / 2) + (wib >> 1);
+  unsigned tile = (a.v_only ? tiles_per : 0u) + blockIdx.x * (kSplitWarps / 2) + (wib >> 1);
   if (tile < n_tiles) issue(tile, stages);
   int s = 0;
   for (int k = 0; tile < n_tiles; ++k, tile += n_pairs) {
@@ -532,6 +533,124 @@ __global__ void __launch_bounds__(kSplitWarps * 32, kSplitBlocksPerSm)
     else quantize_half_row<BITS, GROUP, 1>(a, sg, own, par, mm, pmm, lane, rk, valid, is_v, bar);
     __syncwarp();
     s = sn;
+  }
+}
+
+// ---- per-channel keys: Eq. (1) per channel over a block of tokens -----------
+//
+// One CTA per (block of up to kKeyBlock tokens of the appended chunk, batch *
+// head).  Thread t rotates token row t (the same fp32 butterflies as the
+// per-token kernels) into shared memory; thread c then takes channel c's
+// column, computes its step and zero point over the block's tokens with the
+// same Eq. (1) arithmetic as a per-token group, and writes its codes as
+// bytes; thread t finally packs token t's codes into the cache's word layout.
+constexpr int kKcThreads = kKeyBlock;
+
+template <int D, int BITS>
+__global__ void __launch_bounds__(kKcThreads) quantize_key_channels_kernel(const QuantArgs a,
+                                                                           const PairSigns sg) {
+  constexpr int CH = D / 4;                 // 16-byte chunks of an fp32 row
+  constexpr int CB = D / 16;                // 16-byte chunks of a code-byte row
+  extern __shared__ __align__(16) uint8_t ksm[];
+  float* rot = reinterpret_cast<float*>(ksm);                         // [kKeyBlock][D]
+  uint8_t* cb = ksm + kKeyBlock * D * 4;                              // [kKeyBlock][D] codes
+  const int tid = threadIdx.x;
+  const int blk = blockIdx.x;
+  const int bh = blockIdx.y;
+  const int t0 = blk * kKeyBlock;
+  const int n = min(kKeyBlock, a.n_new - t0);
+
+  // 1. token rows: fp32 rotation (sign flips, butterflies h = 1, ..., d/2,
+  //    times fl(1/sqrt(d))), 16-byte chunks XOR-swizzled by token
+  if (tid < n) {
+    const uint4* src = reinterpret_cast<const uint4*>(a.k_new + ((size_t)bh * a.n_new + t0 + tid) * D);
+    float x[D];
+#pragma unroll
+    for (int i = 0; i < D / 8; ++i) {
+      const uint4 raw = __ldg(src + i);
+      const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        x[8 * i + 2 * k] = __uint_as_float(w[k] << 16);
+        x[8 * i + 2 * k + 1] = __uint_as_float((w[k] ^ sg.m[4 * i + k]) & 0xFFFF0000u);
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < D; i += 2) {
+      const float u = x[i], v = x[i + 1];
+      x[i] = __fmaf_rn(sg.sl[i / 2], u, v);
+      x[i + 1] = __fmaf_rn(sg.sl[i / 2], u, -v);
+    }
+#pragma unroll
+    for (int h = 2; h < D; h <<= 1) {
+#pragma unroll
+      for (int i = 0; i < D; i += 2) {
+        if ((i & h) == 0) {
+          const uint64_t A = ptx::f2_pack(x[i], x[i + 1]);
+          const uint64_t B = ptx::f2_pack(x[i + h], x[i + h + 1]);
+          ptx::f2_unpack(ptx::f2_add(A, B), x[i], x[i + 1]);
+          ptx::f2_unpack(ptx::f2_sub(A, B), x[i + h], x[i + h + 1]);
+        }
+      }
+    }
+    const uint64_t s2 = ptx::f2_pack(a.inv_sqrt_d, a.inv_sqrt_d);
+#pragma unroll
+    for (int i = 0; i < D; i += 2) ptx::f2_unpack(ptx::f2_mul(ptx::f2_pack(x[i], x[i + 1]), s2), x[i], x[i + 1]);
+#pragma unroll
+    for (int i = 0; i < CH; ++i)
+      *reinterpret_cast<float4*>(rot + tid * D + 4 * (i ^ (tid & (CH - 1)))) =
+          make_float4(x[4 * i], x[4 * i + 1], x[4 * i + 2], x[4 * i + 3]);
+  }
+  __syncthreads();
+
+  // 2. channel columns: step, zero point and codes over the block's tokens
+  if (tid < D) {
+    const int c = tid;
+    float col[kKeyBlock];
+#pragma unroll
+    for (int t = 0; t < kKeyBlock; ++t) {
+      const int tt = t < n ? t : 0;   // past the block's end: a copy of token 0 (min / max unchanged)
+      col[t] = rot[tt * D + 4 * ((c >> 2) ^ (tt & (CH - 1))) + (c & 3)];
+    }
+    float mn, mx;
+    min_max<kKeyBlock>(col, mn, mx);
+    int zf;
+    const uint32_t rec = group_codes<BITS, kKeyBlock>(col, mn, mx, zf);
+    a.k_sz[((size_t)bh * a.kblk_per_head + a.kblk_first + blk) * D + c] = rec;
+    // each value now reads 1.5 * 2^23 + code - zf
+#pragma unroll
+    for (int t = 0; t < kKeyBlock; ++t) {
+      if (t < n)
+        cb[t * D + 16 * ((c >> 4) ^ (t & (CB - 1))) + (c & 15)] =
+            (uint8_t)((int)(__float_as_uint(col[t]) - 0x4B400000u) + zf);
+    }
+  }
+  __syncthreads();
+
+  // 3. token t's codes into the packed words: channel 16w + 2k + h (INT2) /
+  //    8w + 2k + h (INT4) at bits BITS*k + 16h of word w
+  if (tid < n) {
+    constexpr int PER_WORD = 32 / BITS;
+    constexpr int NW = D * BITS / 32;
+    uint32_t words[NW];
+#pragma unroll
+    for (int w = 0; w < NW; ++w) words[w] = 0u;
+#pragma unroll
+    for (int i = 0; i < CB; ++i) {
+      const uint4 v = *reinterpret_cast<const uint4*>(cb + tid * D + 16 * (i ^ (tid & (CB - 1))));
+      const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int e = 0; e < 16; ++e) {
+        const int ch = 16 * i + e;
+        const uint32_t code = (u[e >> 2] >> (8 * (e & 3))) & 0xFFu;
+        const int j = ch % PER_WORD;
+        words[ch / PER_WORD] |= code << (BITS * (j >> 1) + 16 * (j & 1));
+      }
+    }
+    uint4* dc = reinterpret_cast<uint4*>(a.k_codes + ((size_t)bh * a.cap + a.first + t0 + tid) * (D * BITS / 8));
+#pragma unroll
+    for (int i = 0; i < NW / 4; ++i)
+      dc[i] = make_uint4(words[4 * i], words[4 * i + 1], words[4 * i + 2], words[4 * i + 3]);
   }
 }
 
@@ -617,11 +736,12 @@ cudaError_t launch_q(const QuantArgs& a, cudaStream_t s) {
     sg.m[i] = (s0 << 15) | (s1 << 31);
     sg.sl[i] = s0 ? -1.0f : 1.0f;
   }
-  const long long rows = 2LL * a.bh * a.n_new;
+  const long long rows = (a.v_only ? 1LL : 2LL) * a.bh * a.n_new;
   if (rows == 0) return cudaSuccess;
   const long long tiles = (rows + 31) / 32;
   if constexpr (D == 128) {
-    const long long want = (tiles + 1) / 2;
+    const long long per = ((long long)a.bh * a.n_new + 31) / 32;   // tiles of one tensor
+    const long long want = ((a.v_only ? per : 2 * per) + 1) / 2;
     const long long cap = (long long)sm_count() * kSplitBlocksPerSm;
     const unsigned blocks = (unsigned)(want < cap ? want : cap);
     static std::atomic<uint64_t> limit_set{0};   // per template instance and device
@@ -658,6 +778,45 @@ cudaError_t launch_quantize_append(const QuantArgs& a, int d, int bits, int grou
   KVQ_Q(128, 4, 32)
   KVQ_Q(128, 4, 64)
 #undef KVQ_Q
+  *supported = false;
+  return cudaSuccess;
+}
+
+namespace {
+
+PairSigns pair_signs(const uint32_t (&sb)[4], int d) {
+  PairSigns sg;
+  for (int i = 0; i < 64; ++i) {
+    const int c0 = 2 * i, c1 = 2 * i + 1;
+    const uint32_t s0 = c0 < d ? (sb[c0 >> 5] >> (c0 & 31)) & 1u : 0u;
+    const uint32_t s1 = c1 < d ? (sb[c1 >> 5] >> (c1 & 31)) & 1u : 0u;
+    sg.m[i] = (s0 << 15) | (s1 << 31);
+    sg.sl[i] = s0 ? -1.0f : 1.0f;
+  }
+  return sg;
+}
+
+template <int D, int BITS>
+cudaError_t launch_kc(const QuantArgs& a, cudaStream_t s) {
+  if (a.n_new == 0 || a.bh == 0) return cudaSuccess;
+  const int smem = kKeyBlock * D * 5;   // fp32 rows + code bytes
+  static std::atomic<uint64_t> limit_set{0};   // per template instance and device
+  const cudaError_t e = ensure_smem_limit(quantize_key_channels_kernel<D, BITS>, smem, limit_set);
+  if (e != cudaSuccess) return e;
+  const dim3 grid((unsigned)((a.n_new + kKeyBlock - 1) / kKeyBlock), (unsigned)a.bh);
+  quantize_key_channels_kernel<D, BITS><<<grid, kKcThreads, smem, s>>>(a, pair_signs(a.sign_bits, D));
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_quantize_key_channels(const QuantArgs& a, int d, int bits, cudaStream_t stream,
+                                         bool* supported) {
+  *supported = true;
+  if (d == 64 && bits == 2) return launch_kc<64, 2>(a, stream);
+  if (d == 64 && bits == 4) return launch_kc<64, 4>(a, stream);
+  if (d == 128 && bits == 2) return launch_kc<128, 2>(a, stream);
+  if (d == 128 && bits == 4) return launch_kc<128, 4>(a, stream);
   *supported = false;
   return cudaSuccess;
 }

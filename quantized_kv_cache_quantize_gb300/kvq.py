@@ -24,6 +24,10 @@ KVQ_ERR_ALIGNMENT = 6
 KVQ_ERR_TOO_LARGE = 7
 NOALLOC_SCRATCH_BYTES = 32 << 20
 
+KEYS_PER_TOKEN = 0
+KEYS_PER_CHANNEL = 1
+KEY_BLOCK = 128
+
 CORR_NONE = 0
 CORR_TAYLOR = 1
 CORR_EXACT = 2
@@ -47,6 +51,7 @@ class CacheStruct(ctypes.Structure):
         ("sign_bits", ctypes.c_uint32 * 4),
         ("k_codes", ctypes.c_void_p), ("v_codes", ctypes.c_void_p),
         ("k_sz", ctypes.c_void_p), ("v_sz", ctypes.c_void_p),
+        ("key_mode", ctypes.c_int32),
     ]
 
 
@@ -56,6 +61,8 @@ _SIGNATURES = {
     "kvq_abi_version": (ctypes.c_int32, []),
     "kvq_cache_bytes": (ctypes.c_int, [_P, ctypes.POINTER(ctypes.c_size_t),
                                        ctypes.POINTER(ctypes.c_size_t)]),
+    "kvq_cache_meta_bytes": (ctypes.c_int, [_P, ctypes.POINTER(ctypes.c_size_t),
+                                            ctypes.POINTER(ctypes.c_size_t)]),
     "kvq_quantize_append": (ctypes.c_int, [_P, _P, _P, ctypes.c_int32, _P]),
     "kvq_workspace_bytes": (ctypes.c_size_t, [_P, ctypes.c_int32, ctypes.c_int32]),
     "kvq_attention_corrected": (ctypes.c_int, [_P, _P, _P, _P, ctypes.c_int32, ctypes.c_int32,
@@ -134,22 +141,27 @@ class KVCache:
     and its ``kvq_cache`` descriptor."""
 
     def __init__(self, batch: int, heads: int, head_dim: int, bits: int, group: int,
-                 chunk_tokens: int, n_chunks: int, signs, device="cuda"):
+                 chunk_tokens: int, n_chunks: int, signs, device="cuda",
+                 key_mode: int = KEYS_PER_TOKEN):
         c = CacheStruct()
         c.batch, c.heads, c.head_dim = batch, heads, head_dim
         c.bits, c.group = bits, group
         c.chunk_tokens, c.n_chunks = chunk_tokens, n_chunks
         c.len, c.head_slot = 0, 0
+        c.key_mode = key_mode
         for i, w in enumerate(sign_bits(signs)):
             c.sign_bits[i] = w
         codes_b, sz_b = ctypes.c_size_t(), ctypes.c_size_t()
         _check(lib().kvq_cache_bytes(ctypes.byref(c), ctypes.byref(codes_b), ctypes.byref(sz_b)),
                "kvq_cache_bytes")
+        k_b, v_b = ctypes.c_size_t(), ctypes.c_size_t()
+        _check(lib().kvq_cache_meta_bytes(ctypes.byref(c), ctypes.byref(k_b), ctypes.byref(v_b)),
+               "kvq_cache_meta_bytes")
         self.signs = np.asarray(signs, dtype=np.float32)
         self.k_codes = torch.zeros(codes_b.value, dtype=torch.uint8, device=device)
         self.v_codes = torch.zeros(codes_b.value, dtype=torch.uint8, device=device)
-        self.k_sz = torch.zeros(sz_b.value // 2, dtype=torch.int16, device=device)
-        self.v_sz = torch.zeros(sz_b.value // 2, dtype=torch.int16, device=device)
+        self.k_sz = torch.zeros(k_b.value // 2, dtype=torch.int16, device=device)
+        self.v_sz = torch.zeros(v_b.value // 2, dtype=torch.int16, device=device)
         c.k_codes, c.v_codes = self.k_codes.data_ptr(), self.v_codes.data_ptr()
         c.k_sz, c.v_sz = self.k_sz.data_ptr(), self.v_sz.data_ptr()
         self.struct = c
@@ -170,7 +182,14 @@ class KVCache:
         t = self.k_codes if which == "k" else self.v_codes
         return t.view(self.batch, self.heads, self.capacity, self.head_dim * self.bits // 8)
 
+    key_mode = property(lambda self: self.struct.key_mode)
+
     def sz_view(self, which: str) -> torch.Tensor:
+        """(step, zero) as int16 BF16 bits: [B, H, capacity, d / group, 2], or
+        for per-channel keys [B, H, n_chunks, blocks per chunk, d, 2]."""
+        if which == "k" and self.key_mode == KEYS_PER_CHANNEL:
+            bpc = (self.chunk_tokens + KEY_BLOCK - 1) // KEY_BLOCK
+            return self.k_sz.view(self.batch, self.heads, self.n_chunks, bpc, self.head_dim, 2)
         t = self.k_sz if which == "k" else self.v_sz
         return t.view(self.batch, self.heads, self.capacity, self.head_dim // self.group, 2)
 

@@ -52,3 +52,40 @@ def assert_close(o_gpu, o_ref, ps_gpu=None, ps_ref=None, pr_gpu=None, pr_ref=Non
         e_r = np.abs(np.asarray(pr_gpu, np.float64) - pr_ref).max()
         assert e_s <= MASS_TOL and e_r <= MASS_TOL, f"{what}: mass err {e_s:.3g} {e_r:.3g}"
     return err / ref
+
+
+def build_cache_kch(w: synth.Workload, x: dict, signs, n_s: int | None = None) -> kvq.KVCache:
+    """As build_cache, with per-channel key quantization."""
+    n_s = x["k_win"].shape[-2] if n_s is None else n_s
+    cache = kvq.KVCache(x["k_win"].shape[0], x["k_win"].shape[1], w.head_dim, w.bits, w.group,
+                        w.chunk_tokens, w.n_chunks, signs, key_mode=kvq.KEYS_PER_CHANNEL)
+    kw = x["k_win"].cuda()
+    vw = x["v_win"].cuda()
+    for c0 in range(0, n_s, w.chunk_tokens):
+        c1 = min(n_s, c0 + w.chunk_tokens)
+        kvq.quantize_append(cache, kw[:, :, c0:c1].contiguous(), vw[:, :, c0:c1].contiguous())
+    return cache
+
+
+def oracle_head_kch(w: synth.Workload, x: dict, signs, b: int, h: int, rows, corr: int,
+                    n_s: int | None = None):
+    """Oracle O, P_S, P_R with per-channel keys: each appended chunk's keys
+    quantized per channel over 128-token blocks, the correction with one
+    channel per group (the key's block steps)."""
+    n_s = x["k_win"].shape[-2] if n_s is None else n_s
+    kf = x["k_win"][b, h, :n_s].float().numpy()
+    vf = x["v_win"][b, h, :n_s].float().numpy()
+    kh, steps = [], []
+    for c0 in range(0, n_s, w.chunk_tokens):
+        part = kf[c0:c0 + w.chunk_tokens]
+        _, kd, kz, _, kc = O.quantize_key_chunk(part, signs, w.bits)
+        kh.append(O.dequantize_key_channels(kc, kd, kz))
+        steps.append(O.key_channel_token_steps(kd, part.shape[0]))
+    d = kf.shape[1]
+    kh = np.concatenate(kh) if kh else np.zeros((0, d))
+    steps = np.concatenate(steps) if steps else np.zeros((0, d))
+    _, vd, vz, _, vc = O.quantize_rows(vf, signs, w.bits, w.group)
+    q = x["q"][b, h].float().numpy()[rows]
+    return O.chunk_attention(q, kh, O.dequantize(vc, vd, vz, w.group), steps,
+                             x["k_cur"][b, h].float().numpy(), x["v_cur"][b, h].float().numpy(),
+                             signs, w.scale, 1, corr)

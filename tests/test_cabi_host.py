@@ -61,6 +61,26 @@ def test_cache_bytes(lib):
     c = _cache(bits=4, group=64)
     assert lib.kvq_cache_bytes(ctypes.byref(c), ctypes.byref(cb), ctypes.byref(sb)) == 0
     assert cb.value == 2 * 30 * 64 and sb.value == 2 * 30 * 2 * 4
+    kb, vb = ctypes.c_size_t(), ctypes.c_size_t()
+    assert lib.kvq_cache_meta_bytes(ctypes.byref(c), ctypes.byref(kb), ctypes.byref(vb)) == 0
+    assert kb.value == vb.value == sb.value
+
+
+def test_cache_bytes_per_channel_keys(lib):
+    """Per-channel keys: k_sz holds d (step, zero) words per 128-token block
+    of every chunk slot (blocks restart at each slot); v_sz is unchanged;
+    kvq_cache_bytes reports the larger of the two."""
+    cb, sb = ctypes.c_size_t(), ctypes.c_size_t()
+    kb, vb = ctypes.c_size_t(), ctypes.c_size_t()
+    for chunk, n_chunks in ((10, 3), (300, 4), (4680, 4)):
+        c = _cache(key_mode=kvq.KEYS_PER_CHANNEL, chunk_tokens=chunk, n_chunks=n_chunks)
+        assert lib.kvq_cache_meta_bytes(ctypes.byref(c), ctypes.byref(kb), ctypes.byref(vb)) == 0
+        bpc = -(-chunk // 128)
+        assert kb.value == 2 * n_chunks * bpc * 128 * 4
+        assert vb.value == 2 * chunk * n_chunks * 4 * 4
+        assert lib.kvq_cache_bytes(ctypes.byref(c), ctypes.byref(cb), ctypes.byref(sb)) == 0
+        assert sb.value == max(kb.value, vb.value)
+        assert cb.value == 2 * chunk * n_chunks * 32
 
 
 @pytest.mark.parametrize("field,value,status", [
@@ -71,6 +91,8 @@ def test_cache_bytes(lib):
     ("n_chunks", 0, kvq.KVQ_ERR_INVALID_ARG),
     ("len", 31, kvq.KVQ_ERR_INVALID_ARG),
     ("head_slot", 3, kvq.KVQ_ERR_INVALID_ARG),
+    ("key_mode", 2, kvq.KVQ_ERR_INVALID_ARG),
+    ("key_mode", -1, kvq.KVQ_ERR_INVALID_ARG),
 ])
 def test_bad_geometry(lib, field, value, status):
     c = _cache(**{field: value})

@@ -112,3 +112,64 @@ def test_append_workload_chunk(name):
     torch.cuda.synchronize()
     _check_slot(cache, "k", x["k_new"], s, 0, w.chunk_tokens)
     _check_slot(cache, "v", x["v_new"], s, 0, w.chunk_tokens)
+
+
+def _check_key_channel_slot(cache, x, signs, slot, n):
+    """Per-channel keys of one appended chunk x [B, H, n, d] in slot `slot`:
+    packed codes per token and (step, zero) per block and channel, against
+    the oracle's per-channel quantizer, bit for bit."""
+    C = cache.chunk_tokens
+    first = slot * C
+    codes = cache.codes_view("k")[:, :, first:first + n].cpu().numpy()
+    meta = cache.sz_view("k")[:, :, slot].cpu().numpy().view(np.uint16)   # [B, H, bpc, d, 2]
+    nb = -(-n // kvq.KEY_BLOCK)
+    for b in range(x.shape[0]):
+        for h in range(x.shape[1]):
+            packed, delta, zero, _, _ = O.quantize_key_chunk(x[b, h].float().numpy(), signs, cache.bits)
+            assert np.array_equal(codes[b, h], packed), f"key codes differ (b{b} h{h})"
+            assert np.array_equal(meta[b, h, :nb, :, 0], O.bf16_bits(delta)), "key steps differ"
+            assert np.array_equal(meta[b, h, :nb, :, 1], O.bf16_bits(zero)), "key zero points differ"
+
+
+@pytest.mark.parametrize("d,bits,group", [(128, 2, 32), (128, 4, 64), (64, 2, 32), (64, 4, 64)])
+def test_append_key_channels_bitexact_ring(d, bits, group):
+    """Per-channel key mode: 300-token chunks (two full 128-token blocks and a
+    44-token one) filling a 3-slot window and wrapping once, then a partial
+    chunk after a reset; keys bit-exact per block and channel, values
+    bit-exact per token and group."""
+    rng = np.random.default_rng(d + bits)
+    B, H, C, n = 1, 3, 300, 3
+    s = synth.hadamard_signs(d, seed=5)
+    cache = kvq.KVCache(B, H, d, bits, group, C, n, s, key_mode=kvq.KEYS_PER_CHANNEL)
+    for step in range(n + 1):
+        k = rng.standard_normal((B, H, C, d)) * 2 + rng.standard_normal((1, 1, 1, d)) * 3
+        k[..., :3] *= 10                                   # outlier channels
+        k = _bf16(k)
+        v = _bf16(rng.standard_normal((B, H, C, d)))
+        slot = cache.head_slot
+        kvq.quantize_append(cache, k.cuda(), v.cuda())
+        torch.cuda.synchronize()
+        _check_key_channel_slot(cache, k, s, slot, C)
+        _check_slot(cache, "v", v, s, slot * C, C)
+    part = kvq.KVCache(B, H, d, bits, group, C, n, s, key_mode=kvq.KEYS_PER_CHANNEL)
+    kvq.quantize_append(part, k.cuda(), v.cuda())
+    kvq.quantize_append(part, k[:, :, :1].contiguous().cuda(), v[:, :, :1].contiguous().cuda())
+    torch.cuda.synchronize()
+    assert part.len == C + 1
+    _check_key_channel_slot(part, k[:, :, :1], s, 1, 1)
+    _check_slot(part, "v", v[:, :, :1], s, C, 1)
+
+
+@pytest.mark.parametrize("name", ["w4_int2", "hires_t3"])
+def test_append_key_channels_workload_chunk(name):
+    """One full chunk of the workload (all heads) in the per-channel key mode,
+    bit-exact: 4680 or 14400 tokens, the last block partial."""
+    w = synth.WORKLOADS[name]
+    x = synth.inputs(w, n_q=1, n_s=1, n_r=1)
+    s = synth.hadamard_signs(w.head_dim)
+    cache = kvq.KVCache(1, w.heads, w.head_dim, w.bits, w.group, w.chunk_tokens, w.n_chunks, s,
+                        key_mode=kvq.KEYS_PER_CHANNEL)
+    kvq.quantize_append(cache, x["k_new"].cuda(), x["v_new"].cuda())
+    torch.cuda.synchronize()
+    _check_key_channel_slot(cache, x["k_new"], s, 0, w.chunk_tokens)
+    _check_slot(cache, "v", x["v_new"], s, 0, w.chunk_tokens)
