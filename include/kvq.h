@@ -174,9 +174,11 @@ kvq_status kvq_quantize_append(kvq_cache *cache, const uint16_t *k_new,
 /*
  * Workspace bytes kvq_attention_corrected / kvq_attention_mass need for n_q
  * queries and n_r current-chunk tokens: the rotated query (FP16 high and low
- * parts), the rotated current values (FP16) and, when the launch would not
- * fill the current device, the partial results of the key-range split
- * (fp32).  Depends on the current device's SM count.  0 on a bad geometry.
+ * parts), the rotated current values (FP16), when the launch would not fill
+ * the current device the partial results of the key-range split (fp32), and
+ * with per-channel keys one fp32 per query row and cached key block (the
+ * block's zero-point term minus the correction).  Depends on the current
+ * device's SM count.  0 on a bad geometry.
  */
 size_t kvq_workspace_bytes(const kvq_cache *cache, int32_t n_q, int32_t n_r);
 

@@ -107,8 +107,8 @@ int max_cached_tiles(const kvq::Geometry& g, int n_chunks, int chunk) {
   return kvq::cached_tiles(g.key_mode, n_chunks * chunk, chunk, g.bpc);
 }
 
-// kch_tiles: cached tiles the per-(row, tile) correction table holds (0
-// without per-channel keys)
+// kch_tiles: cached tiles the per-(row, tile) table of per-channel keys holds
+// (0 without them)
 Workspace carve(void* base, const kvq::Geometry& g, int n_q, int n_r, int splits, int kch_tiles) {
   Workspace w;
   const size_t qb = round_up((size_t)g.bh * n_q * g.d * 2, 256);
@@ -197,10 +197,9 @@ kvq_status attention_common(const kvq_cache* cache, const uint16_t* q, const uin
   // key-range split when the grid would not fill the device (and the
   // workspace holds the partial results; otherwise one range)
   const int n_ct = kvq::cached_tiles(g.key_mode, cache->len, cache->chunk_tokens, g.bpc);
-  // per-channel keys with a correction: a table of one number per row and
-  // cached tile
-  const bool kch = g.key_mode == KVQ_KEYS_PER_CHANNEL;
-  const int kch_tiles = kch && corr != KVQ_CORR_NONE ? n_ct : 0;
+  // per-channel keys: a table of one number per row and cached tile (the
+  // zero-point term and the correction)
+  const int kch_tiles = g.key_mode == KVQ_KEYS_PER_CHANNEL ? n_ct : 0;
   int per = 0, splits = 1;
   if ((flags & KVQ_FLAG_NO_KV_SPLIT) == 0) {
     int max_splits = 64;
@@ -509,7 +508,7 @@ extern "C" kvq_status kvq_attention_corrected_noalloc(const kvq_cache* cache, co
   const kvq_status st = check_geometry(cache, &g);
   if (st != KVQ_OK) return st;
   if (n_q < 0 || n_r < 0) return KVQ_ERR_INVALID_ARG;
-  const int kch_tiles = g.key_mode == KVQ_KEYS_PER_CHANNEL && corr != KVQ_CORR_NONE
+  const int kch_tiles = g.key_mode == KVQ_KEYS_PER_CHANNEL
                             ? kvq::cached_tiles(g.key_mode, cache->len, cache->chunk_tokens, g.bpc)
                             : 0;
   if (carve(nullptr, g, n_q, n_r, 1, kch_tiles).bytes > (size_t)KVQ_NOALLOC_SCRATCH_BYTES)

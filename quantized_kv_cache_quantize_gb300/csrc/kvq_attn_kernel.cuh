@@ -86,8 +86,8 @@ struct AttnParams {
   float* st_part;   // [splits][B*H][n_q][3]: base m (log2 units), l_S, l_R
   // per-channel keys: cached tile t is block t % bpc of chunk slot t / bpc;
   // k_sz holds kblk_per_head blocks of D (step, zero) words per head;
-  // kch_c [B*H][n_ct][n_q]: the correction per query row and tile (log2
-  // units, negated; null without correction)
+  // kch_c [B*H][n_ct][n_q]: zero-point term minus correction per query row
+  // and tile (log2 units)
   int chunk, bpc, kblk_per_head, n_ct;
   const float* kch_c;
   int* status;      // device status word (first error of a bounded wait)
@@ -120,7 +120,7 @@ struct Cfg {
   static constexpr int kDsq = 2 * kTile + kNExt * kExt;    // offset inside a stage
   static constexpr int kDsqBytes = EXACT ? 3072 : 0;
   // per-channel keys: per stage the key block's steps (FP16, [128]) and
-  // magic + zero points (FP16, [128]), padded like dsq
+  // -magic * steps (FP16, [128]), padded like dsq
   static constexpr int kKch = kDsq + kDsqBytes;
   static constexpr int kKchBytes = KCH ? 1024 : 0;
   static constexpr int kStageBytes = 2 * kTile + kNExt * kExt + kDsqBytes + kKchBytes;  // K, V, Kx [, dsq] [, kch]
@@ -281,25 +281,26 @@ __device__ __forceinline__ void dequant_row(const uint32_t (&words)[D * BITS / 3
 }
 
 // Per-channel keys: one packed key row into row r of a swizzled FP16 tile as
-// (code - z_c) * D_c (the integer difference exact, one rounding of the
-// product): kd holds the block's steps D_c, kzm the constants magic + z_c
-// (FP16, one per channel; magic as code_pair_f16 places the pair)
+// code * D_c = (magic + code) D_c - magic D_c in one FMA, exact for INT2 (the
+// zero-point term goes to the per-(row, tile) pre-pass): kd holds the block's
+// steps D_c, kmd the constants -magic D_c (FP16, one per channel; magic as
+// code_pair_f16 places the pair)
 template <int D, int BITS>
 __device__ __forceinline__ void dequant_row_kch(const uint32_t (&words)[D * BITS / 32],
-                                                const uint8_t* kd, const uint8_t* kzm,
+                                                const uint8_t* kd, const uint8_t* kmd,
                                                 uint8_t* tile, int r) {
 #pragma unroll
   for (int c = 0; c < D / 8; ++c) {
     const uint4 dv = *reinterpret_cast<const uint4*>(kd + 16 * c);
-    const uint4 zv = *reinterpret_cast<const uint4*>(kzm + 16 * c);
+    const uint4 mv = *reinterpret_cast<const uint4*>(kmd + 16 * c);
     const uint32_t d2[4] = {dv.x, dv.y, dv.z, dv.w};
-    const uint32_t z2[4] = {zv.x, zv.y, zv.z, zv.w};
+    const uint32_t m2[4] = {mv.x, mv.y, mv.z, mv.w};
     uint32_t out[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       const int k = BITS == 2 ? 4 * (c & 1) + i : i;
       const uint32_t v = BITS == 2 ? code_pair_f16<2>(words[c >> 1], k) : code_pair_f16<4>(words[c], k);
-      out[i] = as_u32(__hmul2(__hsub2(as_h2(v), as_h2(z2[i])), as_h2(d2[i])));
+      out[i] = as_u32(__hfma2(as_h2(v), as_h2(d2[i]), as_h2(m2[i])));
     }
     *reinterpret_cast<uint4*>(tile + (c >> 3) * kHalf + sw128(r, c & 7)) =
         make_uint4(out[0], out[1], out[2], out[3]);
@@ -719,6 +720,11 @@ __global__ void __launch_bounds__(Cfg<D, NQ, PRECISE, EXACT, KCH>::kThreads, 1)
 
     float m = -INFINITY, l_s = 0.f, l_r = 0.f;
     const float sl2 = p.scale_log2;
+    // per-channel keys: this row's column of the per-(row, tile) table
+    const float* kch_row = KCH ? p.kch_c + (size_t)bh * n_ct_all * p.n_q + min(q0 + q * kBlockM + r, p.n_q - 1)
+                               : nullptr;
+    float toff_next = 0.f;
+    if (KCH && n_ct > 0) toff_next = __ldg(kch_row + (size_t)kb * p.n_q);
     const uint32_t t_o = tmem + C::kTO + q * D + lane_off;
     for (int j = 0; j < n_t && ok; ++j) {
       const int b = NQ == 2 ? 0 : (j & 1);
@@ -731,12 +737,14 @@ __global__ void __launch_bounds__(Cfg<D, NQ, PRECISE, EXACT, KCH>::kThreads, 1)
       ptx::tc_fence_after();
       const int nv = j < n_ct ? ctile_count(kb + j)
                               : min(kBlockN, p.n_r - (cb + j - n_ct) * kBlockN);
-      // per-channel keys: the correction of this row and cached tile, one
-      // number (log2 units, negated), folded into the exponent base
+      // per-channel keys: zero-point term minus correction of this row and
+      // cached tile, one number (log2 units), folded into the exponent base;
+      // the next tile's is fetched now, a tile ahead of its use
       float toff = 0.f;
-      if (KCH && j < n_ct && p.kch_c != nullptr)
-        toff = __ldg(p.kch_c + ((size_t)bh * n_ct_all + (kb + j)) * p.n_q +
-                     min(q0 + q * kBlockM + r, p.n_q - 1));
+      if (KCH && j < n_ct) {
+        toff = toff_next;
+        if (j + 1 < n_ct) toff_next = __ldg(kch_row + (size_t)(kb + j + 1) * p.n_q);
+      }
       // One pass over the tile, 32 columns at a time, with the running base
       // m: P = 2^(s * scale * log2(e) - m).  The base only has to keep every
       // P inside the FP16 range, so it is raised only when a chunk's sum of
@@ -1028,7 +1036,7 @@ __global__ void __launch_bounds__(Cfg<D, NQ, PRECISE, EXACT, KCH>::kThreads, 1)
       if (j >= 2 && !wait_bar(BAR(kBarEmpty + s), ((j >> 1) - 1) & 1, lim, abort, p.status)) break;
       uint8_t* st = smem + C::kStages + s * C::kStageBytes;
       if (KCH) {
-        // the key block's per-channel steps and magic + zero points, shared
+        // the key block's per-channel steps and -magic * steps, shared
         // by the warpgroup through the stage's barrier (all 128 threads
         // arrive: a thread that writes here for tile j has waited on the
         // other stage's barrier for tile j - 1, so every thread is done
@@ -1037,7 +1045,7 @@ __global__ void __launch_bounds__(Cfg<D, NQ, PRECISE, EXACT, KCH>::kThreads, 1)
           const int k = BITS == 2 ? (r & 15) >> 1 : 0;
           reinterpret_cast<__half*>(st + C::kKch)[r] = __float2half_rn(bf16_lo(kmeta));
           reinterpret_cast<__half*>(st + C::kKch + 256)[r] =
-              __float2half_rn((float)pair_magic<BITS>(k) + bf16_hi(kmeta));
+              __float2half_rn(-(float)pair_magic<BITS>(k) * bf16_lo(kmeta));
         }
         ptx::mbar_arrive(BAR(kBarKch + s));
         if (!wait_bar(BAR(kBarKch + s), (j >> 1) & 1, lim, abort, p.status)) break;
@@ -1148,8 +1156,8 @@ __global__ void __launch_bounds__(Cfg<D, NQ, PRECISE, EXACT, KCH>::kThreads, 1)
           }
           // zero points and bias (its query columns are zero without the
           // correction); the precise layout spends a tile on each.  Per-
-          // channel key tiles carry their zero points themselves and take
-          // the correction in the softmax.
+          // channel key tiles take both from the per-(row, tile) pre-pass,
+          // in the softmax.
           if (!KCH) {
             const uint64_t dqx = at(dex, C::kQx + q * C::kNExt * kExt);
             const uint64_t dkx = at(dex, st + 2 * C::kTile);
@@ -1386,43 +1394,47 @@ __global__ void __launch_bounds__(256) merge_splits_kernel(const MergeArgs a) {
   }
 }
 
-// ---- per-channel keys: the correction per query row and cached tile ---------
+// ---- per-channel keys: zero points and correction per query row and tile ----
 //
-// With per-channel key steps D_c of a key block, the correction of a score
-// depends on the key only through its block: b = sum_c a_c^2 / 6 (Taylor;
-// = scale^2 / 24 sum_c q'_c^2 D_c^2) or sum_c log(sinh a_c / a_c) (exact),
-// a_c = scale/2 |q'_c| D_c.  One thread per query row computes it for
-// kKchTiles consecutive cached tiles and stores -log2(e) b.
+// A per-channel key tile holds code * D_c; what its scores still need is the
+// zero-point term scale * sum_c q'_c (-z_c D_c) minus the correction, and with
+// per-channel steps both depend on the key only through its block: the
+// correction is b = sum_c a_c^2 / 6 (Taylor; = scale^2 / 24 sum_c q'_c^2 D_c^2)
+// or sum_c log(sinh a_c / a_c) (exact), a_c = scale/2 |q'_c| D_c, 0 without.
+// One thread per query row computes log2(e) (zero-point term - b) for
+// kKchTiles consecutive cached tiles (fp32, with the rotated query the
+// tensor cores read: FP16, plus its remainder with the precise-query split).
 struct KchArgs {
   const uint16_t* q_hi;   // rotated query, FP16 [bh][n_q][D]
   const uint16_t* q_lo;   // its FP16 remainder, or null
   const uint32_t* k_sz;   // per-channel (step, zero) words [bh][kblk_per_head][D]
   float* out;             // [bh][n_ct][n_q]
   int n_q, n_ct, bpc, kblk_per_head;
-  float half_scale;
-  int exact;
+  float scale;
+  int corr;
 };
 constexpr int kKchTiles = 8;
 
 template <int D>
 __global__ void __launch_bounds__(128) kch_bias_kernel(const KchArgs a) {
-  __shared__ float dt[kKchTiles][D];
+  __shared__ __align__(16) float wz[kKchTiles][D];   // -z_c D_c
+  __shared__ __align__(16) float wd[kKchTiles][D];   // scale/2 D_c
   const int row = blockIdx.x * 128 + threadIdx.x;
   const int t0 = blockIdx.y * kKchTiles;
   const int bh = blockIdx.z;
   for (int i = threadIdx.x; i < kKchTiles * D; i += 128) {
     const int t = t0 + i / D, c = i % D;
-    float v = 0.f;
+    uint32_t w = 0u;
     if (t < a.n_ct) {
       const int slot = t / a.bpc;
-      v = a.half_scale *
-          bf16_lo(__ldg(a.k_sz + ((size_t)bh * a.kblk_per_head + slot * a.bpc + (t - slot * a.bpc)) * D + c));
+      w = __ldg(a.k_sz + ((size_t)bh * a.kblk_per_head + slot * a.bpc + (t - slot * a.bpc)) * D + c);
     }
-    dt[i / D][c] = v;
+    wz[i / D][c] = -bf16_hi(w) * bf16_lo(w);    // exact: integer z, 8-bit step
+    wd[i / D][c] = 0.5f * a.scale * bf16_lo(w);
   }
   __syncthreads();
   if (row >= a.n_q) return;
-  float qa[D];
+  float qv[D];
   const uint4* qh = reinterpret_cast<const uint4*>(a.q_hi + ((size_t)bh * a.n_q + row) * D);
   const uint4* ql = a.q_lo ? reinterpret_cast<const uint4*>(a.q_lo + ((size_t)bh * a.n_q + row) * D) : nullptr;
 #pragma unroll
@@ -1432,25 +1444,35 @@ __global__ void __launch_bounds__(128) kch_bias_kernel(const KchArgs a) {
     const uint32_t hw[4] = {h.x, h.y, h.z, h.w}, lw[4] = {l.x, l.y, l.z, l.w};
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
-      qa[8 * i + 2 * k] = fabsf(h_lo(hw[k]) + h_lo(lw[k]));
-      qa[8 * i + 2 * k + 1] = fabsf(h_hi(hw[k]) + h_hi(lw[k]));
+      qv[8 * i + 2 * k] = h_lo(hw[k]) + h_lo(lw[k]);
+      qv[8 * i + 2 * k + 1] = h_hi(hw[k]) + h_hi(lw[k]);
     }
   }
   for (int tt = 0; tt < kKchTiles && t0 + tt < a.n_ct; ++tt) {
-    float b = 0.f;
-    if (a.exact) {
-#pragma unroll 8
-      for (int c = 0; c < D; ++c) b += log_sinhc(qa[c] * dt[tt][c]);
-    } else {
-      float b2[2] = {0.f, 0.f};
+    uint64_t z2 = 0ull, b2 = 0ull;   // packed pairs of partial sums
 #pragma unroll
-      for (int c = 0; c < D; ++c) {
-        const float x = qa[c] * dt[tt][c];
-        b2[c & 1] = fmaf(x, x, b2[c & 1]);
+    for (int c = 0; c < D; c += 4) {
+      const float4 z4 = *reinterpret_cast<const float4*>(&wz[tt][c]);
+      const float4 d4 = *reinterpret_cast<const float4*>(&wd[tt][c]);
+      z2 = ptx::f2_fma(ptx::f2_pack(qv[c], qv[c + 1]), ptx::f2_pack(z4.x, z4.y), z2);
+      z2 = ptx::f2_fma(ptx::f2_pack(qv[c + 2], qv[c + 3]), ptx::f2_pack(z4.z, z4.w), z2);
+      if (a.corr == KVQ_CORR_TAYLOR) {
+        const uint64_t x0 = ptx::f2_mul(ptx::f2_pack(qv[c], qv[c + 1]), ptx::f2_pack(d4.x, d4.y));
+        const uint64_t x1 = ptx::f2_mul(ptx::f2_pack(qv[c + 2], qv[c + 3]), ptx::f2_pack(d4.z, d4.w));
+        b2 = ptx::f2_fma(x0, x0, b2);
+        b2 = ptx::f2_fma(x1, x1, b2);
       }
-      b = (b2[0] + b2[1]) * (1.0f / 6.0f);
     }
-    a.out[((size_t)bh * a.n_ct + t0 + tt) * a.n_q + row] = -kLog2e * b;
+    float zlo, zhi, blo, bhi;
+    ptx::f2_unpack(z2, zlo, zhi);
+    ptx::f2_unpack(b2, blo, bhi);
+    float b = (blo + bhi) * (1.0f / 6.0f);
+    if (a.corr == KVQ_CORR_EXACT) {
+      b = 0.f;
+#pragma unroll 8
+      for (int c = 0; c < D; ++c) b += log_sinhc(fabsf(qv[c]) * wd[tt][c]);
+    }
+    a.out[((size_t)bh * a.n_ct + t0 + tt) * a.n_q + row] = kLog2e * (a.scale * (zlo + zhi) - b);
   }
 }
 
@@ -1548,8 +1570,8 @@ kvq_status launch_t(const AttnLaunch& a, cudaStream_t stream) {
     k.n_ct = a.n_ct;
     k.bpc = a.bpc;
     k.kblk_per_head = a.kblk_per_head;
-    k.half_scale = 0.5f * a.scale;
-    k.exact = a.corr == KVQ_CORR_EXACT ? 1 : 0;
+    k.scale = a.scale;
+    k.corr = a.corr;
     const dim3 kg((a.n_q + 127) / 128, (a.n_ct + kKchTiles - 1) / kKchTiles, a.bh);
     kch_bias_kernel<D><<<kg, 128, 0, stream>>>(k);
     if (cudaGetLastError() != cudaSuccess) return KVQ_ERR_CUDA;
