@@ -578,18 +578,35 @@ __global__ void __launch_bounds__(Cfg<D, NQ, PRECISE, EXACT, KCH>::kThreads, 1)
   const int cb = max(0, jb - n_ct_all);     // current tile = cb + (j - n_ct) for j >= n_ct
   const bool mass_only = p.mass_only != 0;
   const unsigned long long lim = p.wait_limit_ns;
-  // first token and valid keys of cached tile t: 128-token tiles of the
-  // window, or (per-channel keys) the key blocks of each chunk slot
-  auto ctile_first = [&](int t) -> int {
-    if (!KCH) return t * kBlockN;
-    const int slot = t / p.bpc;
-    return slot * p.chunk + (t - slot * p.bpc) * kBlockN;
+  // Cached tiles are walked in order by every role: a CTile follows the
+  // position (tile t, and for per-channel keys its chunk slot and key block)
+  // with one division at the start, so the first token and the valid keys
+  // of each tile cost no division (128-token tiles of the window, or the key
+  // blocks of each chunk slot).
+  struct CTile {
+    int t, slot, blk;
   };
-  auto ctile_count = [&](int t) -> int {
-    if (!KCH) return min(kBlockN, p.n_s - t * kBlockN);
-    const int slot = t / p.bpc;
-    const int in_slot = min(p.chunk, p.n_s - slot * p.chunk);
-    return min(kBlockN, in_slot - (t - slot * p.bpc) * kBlockN);
+  auto ctile_at = [&](int t) -> CTile {
+    CTile c{t, 0, 0};
+    if (KCH) {
+      c.slot = t / p.bpc;
+      c.blk = t - c.slot * p.bpc;
+    }
+    return c;
+  };
+  auto ctile_next = [&](CTile& c) {
+    ++c.t;
+    if (KCH && ++c.blk == p.bpc) {
+      c.blk = 0;
+      ++c.slot;
+    }
+  };
+  auto ctile_first = [&](const CTile& c) -> int {
+    return KCH ? c.slot * p.chunk + c.blk * kBlockN : c.t * kBlockN;
+  };
+  auto ctile_count = [&](const CTile& c) -> int {
+    if (!KCH) return min(kBlockN, p.n_s - c.t * kBlockN);
+    return min(kBlockN, min(p.chunk, p.n_s - c.slot * p.chunk) - c.blk * kBlockN);
   };
 
   if (warp < C::kSoftmaxWarps) {
@@ -725,6 +742,7 @@ __global__ void __launch_bounds__(Cfg<D, NQ, PRECISE, EXACT, KCH>::kThreads, 1)
                                : nullptr;
     float toff_next = 0.f;
     if (KCH && n_ct > 0) toff_next = __ldg(kch_row + (size_t)kb * p.n_q);
+    CTile sm_tile = ctile_at(kb);
     const uint32_t t_o = tmem + C::kTO + q * D + lane_off;
     for (int j = 0; j < n_t && ok; ++j) {
       const int b = NQ == 2 ? 0 : (j & 1);
@@ -735,8 +753,9 @@ __global__ void __launch_bounds__(Cfg<D, NQ, PRECISE, EXACT, KCH>::kThreads, 1)
         break;
       }
       ptx::tc_fence_after();
-      const int nv = j < n_ct ? ctile_count(kb + j)
+      const int nv = j < n_ct ? ctile_count(sm_tile)
                               : min(kBlockN, p.n_r - (cb + j - n_ct) * kBlockN);
+      if (j < n_ct) ctile_next(sm_tile);
       // per-channel keys: zero-point term minus correction of this row and
       // cached tile, one number (log2 units), folded into the exponent base;
       // the next tile's is fetched now, a tile ahead of its use
@@ -991,8 +1010,9 @@ __global__ void __launch_bounds__(Cfg<D, NQ, PRECISE, EXACT, KCH>::kThreads, 1)
     const int r = tid - C::kDequantWarp * 32;
     const size_t head_tok = static_cast<size_t>(bh) * p.cap;
     // packed words of key r of tile j (zeros past the end of the window)
-    auto load_key = [&](int j, uint32_t (&kw)[NW], uint32_t (&ksz)[G], uint32_t (&vw)[NW],
-                        uint32_t (&vsz)[G], uint32_t& kmeta) {
+    // (the tile at local index j is `pos`)
+    auto load_key = [&](int j, const CTile& pos, uint32_t (&kw)[NW], uint32_t (&ksz)[G],
+                        uint32_t (&vw)[NW], uint32_t (&vsz)[G], uint32_t& kmeta) {
 #pragma unroll
       for (int i = 0; i < NW; ++i) kw[i] = vw[i] = 0u;
 #pragma unroll
@@ -1000,12 +1020,10 @@ __global__ void __launch_bounds__(Cfg<D, NQ, PRECISE, EXACT, KCH>::kThreads, 1)
       kmeta = 0u;
       if (j >= n_ct) return;
       // per-channel keys: thread r < D fetches the block's word of channel r
-      if (KCH && r < D) {
-        const int t = kb + j, slot = t / p.bpc;
-        kmeta = __ldg(p.k_sz + ((size_t)bh * p.kblk_per_head + slot * p.bpc + (t - slot * p.bpc)) * D + r);
-      }
-      if (r >= ctile_count(kb + j)) return;
-      const size_t tok = head_tok + (size_t)ctile_first(kb + j) + r;
+      if (KCH && r < D)
+        kmeta = __ldg(p.k_sz + ((size_t)bh * p.kblk_per_head + pos.slot * p.bpc + pos.blk) * D + r);
+      if (r >= ctile_count(pos)) return;
+      const size_t tok = head_tok + (size_t)ctile_first(pos) + r;
       const uint4* kc = reinterpret_cast<const uint4*>(p.k_codes + tok * CB);
 #pragma unroll
       for (int i = 0; i < NW / 4; ++i) {
@@ -1028,11 +1046,13 @@ __global__ void __launch_bounds__(Cfg<D, NQ, PRECISE, EXACT, KCH>::kThreads, 1)
       }
     };
     uint32_t kw[NW], ksz[G], vw[NW], vsz[G], kmeta;
-    load_key(0, kw, ksz, vw, vsz, kmeta);
+    CTile dq_tile = ctile_at(kb), dq_next = dq_tile;
+    ctile_next(dq_next);
+    load_key(0, dq_tile, kw, ksz, vw, vsz, kmeta);
     for (int j = 0; j < n_ct; ++j) {
       if (*abort) break;
       const int s = j & 1;
-      const bool valid = r < ctile_count(kb + j);
+      const bool valid = r < ctile_count(dq_tile);
       if (j >= 2 && !wait_bar(BAR(kBarEmpty + s), ((j >> 1) - 1) & 1, lim, abort, p.status)) break;
       uint8_t* st = smem + C::kStages + s * C::kStageBytes;
       if (KCH) {
@@ -1094,7 +1114,9 @@ __global__ void __launch_bounds__(Cfg<D, NQ, PRECISE, EXACT, KCH>::kThreads, 1)
       }
       // the next tile's words travel while this one is handed over and the
       // next stage is awaited
-      load_key(j + 1, kw, ksz, vw, vsz, kmeta);
+      load_key(j + 1, dq_next, kw, ksz, vw, vsz, kmeta);
+      dq_tile = dq_next;
+      ctile_next(dq_next);
       write_ext_row(st + 2 * C::kTile, r, cx);
       if (PRECISE) write_ext_row(st + 2 * C::kTile + kExt, r, cz);
       ptx::fence_proxy_async_smem();
@@ -1401,9 +1423,11 @@ __global__ void __launch_bounds__(256) merge_splits_kernel(const MergeArgs a) {
 // per-channel steps both depend on the key only through its block: the
 // correction is b = sum_c a_c^2 / 6 (Taylor; = scale^2 / 24 sum_c q'_c^2 D_c^2)
 // or sum_c log(sinh a_c / a_c) (exact), a_c = scale/2 |q'_c| D_c, 0 without.
-// One thread per query row computes log2(e) (zero-point term - b) for
-// kKchTiles consecutive cached tiles (fp32, with the rotated query the
-// tensor cores read: FP16, plus its remainder with the precise-query split).
+// The table log2(e) (zero-point term - b) [row][tile] is a small GEMM over the
+// channels: a CTA covers kKchRows query rows x kKchCols cached tiles of one
+// head, each thread a 4 x 4 block of it, with the channels staged through
+// shared memory 32 at a time (fp32, with the rotated query the tensor cores
+// read: FP16, plus its remainder with the precise-query split).
 struct KchArgs {
   const uint16_t* q_hi;   // rotated query, FP16 [bh][n_q][D]
   const uint16_t* q_lo;   // its FP16 remainder, or null
@@ -1413,66 +1437,97 @@ struct KchArgs {
   float scale;
   int corr;
 };
-constexpr int kKchTiles = 8;
+constexpr int kKchRows = 64;
+constexpr int kKchCols = 32;
+constexpr int kKchThreads = (kKchRows / 4) * (kKchCols / 4);   // 128
+constexpr int kKchPad = 4;   // shared-memory row padding (floats)
 
 template <int D>
-__global__ void __launch_bounds__(128) kch_bias_kernel(const KchArgs a) {
-  __shared__ __align__(16) float wz[kKchTiles][D];   // -z_c D_c
-  __shared__ __align__(16) float wd[kKchTiles][D];   // scale/2 D_c
-  const int row = blockIdx.x * 128 + threadIdx.x;
-  const int t0 = blockIdx.y * kKchTiles;
-  const int bh = blockIdx.z;
-  for (int i = threadIdx.x; i < kKchTiles * D; i += 128) {
-    const int t = t0 + i / D, c = i % D;
-    uint32_t w = 0u;
-    if (t < a.n_ct) {
-      const int slot = t / a.bpc;
-      w = __ldg(a.k_sz + ((size_t)bh * a.kblk_per_head + slot * a.bpc + (t - slot * a.bpc)) * D + c);
+__global__ void __launch_bounds__(kKchThreads) kch_bias_kernel(const KchArgs a) {
+  __shared__ __align__(16) float qs[32][kKchRows + kKchPad];   // q'_c of the rows
+  __shared__ __align__(16) float wz[32][kKchCols + kKchPad];   // -z_c D_c of the tiles
+  __shared__ __align__(16) float wd[32][kKchCols + kKchPad];   // scale/2 D_c of the tiles
+  const int tid = threadIdx.x;
+  const int ty = tid / (kKchCols / 4), tx = tid % (kKchCols / 4);
+  const int row0 = blockIdx.x * kKchRows, t0 = blockIdx.y * kKchCols, bh = blockIdx.z;
+  const bool exact = a.corr == KVQ_CORR_EXACT, taylor = a.corr == KVQ_CORR_TAYLOR;
+  float az[4][4], ab[4][4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int k = 0; k < 4; ++k) az[i][k] = ab[i][k] = 0.f;
+  for (int c0 = 0; c0 < D; c0 += 32) {
+    // rows: 64 x 32 channels, 8 channels (16 bytes) per load
+    for (int i = tid; i < kKchRows * 4; i += kKchThreads) {
+      const int rr = i >> 2, part = i & 3, row = row0 + rr;
+      float v[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      if (row < a.n_q) {
+        const size_t off = ((size_t)bh * a.n_q + row) * D + c0 + 8 * part;
+        const uint4 h = __ldg(reinterpret_cast<const uint4*>(a.q_hi + off));
+        const uint4 l = a.q_lo ? __ldg(reinterpret_cast<const uint4*>(a.q_lo + off)) : make_uint4(0u, 0u, 0u, 0u);
+        const uint32_t hw[4] = {h.x, h.y, h.z, h.w}, lw[4] = {l.x, l.y, l.z, l.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          v[2 * k] = h_lo(hw[k]) + h_lo(lw[k]);
+          v[2 * k + 1] = h_hi(hw[k]) + h_hi(lw[k]);
+        }
+      }
+#pragma unroll
+      for (int e = 0; e < 8; ++e) qs[8 * part + e][rr] = v[e];
     }
-    wz[i / D][c] = -bf16_hi(w) * bf16_lo(w);    // exact: integer z, 8-bit step
-    wd[i / D][c] = 0.5f * a.scale * bf16_lo(w);
-  }
-  __syncthreads();
-  if (row >= a.n_q) return;
-  float qv[D];
-  const uint4* qh = reinterpret_cast<const uint4*>(a.q_hi + ((size_t)bh * a.n_q + row) * D);
-  const uint4* ql = a.q_lo ? reinterpret_cast<const uint4*>(a.q_lo + ((size_t)bh * a.n_q + row) * D) : nullptr;
+    // tiles: 32 x 32 channels of (step, zero) words
+    for (int i = tid; i < kKchCols * 4; i += kKchThreads) {
+      const int tt = i >> 2, part = i & 3, t = t0 + tt;
+      uint32_t w[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+      if (t < a.n_ct) {
+        const int slot = t / a.bpc;
+        const uint4* src = reinterpret_cast<const uint4*>(
+            a.k_sz + ((size_t)bh * a.kblk_per_head + slot * a.bpc + (t - slot * a.bpc)) * D + c0 + 8 * part);
+        const uint4 x0 = __ldg(src), x1 = __ldg(src + 1);
+        w[0] = x0.x; w[1] = x0.y; w[2] = x0.z; w[3] = x0.w;
+        w[4] = x1.x; w[5] = x1.y; w[6] = x1.z; w[7] = x1.w;
+      }
 #pragma unroll
-  for (int i = 0; i < D / 8; ++i) {
-    const uint4 h = __ldg(qh + i);
-    const uint4 l = ql ? __ldg(ql + i) : make_uint4(0u, 0u, 0u, 0u);
-    const uint32_t hw[4] = {h.x, h.y, h.z, h.w}, lw[4] = {l.x, l.y, l.z, l.w};
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      qv[8 * i + 2 * k] = h_lo(hw[k]) + h_lo(lw[k]);
-      qv[8 * i + 2 * k + 1] = h_hi(hw[k]) + h_hi(lw[k]);
-    }
-  }
-  for (int tt = 0; tt < kKchTiles && t0 + tt < a.n_ct; ++tt) {
-    uint64_t z2 = 0ull, b2 = 0ull;   // packed pairs of partial sums
-#pragma unroll
-    for (int c = 0; c < D; c += 4) {
-      const float4 z4 = *reinterpret_cast<const float4*>(&wz[tt][c]);
-      const float4 d4 = *reinterpret_cast<const float4*>(&wd[tt][c]);
-      z2 = ptx::f2_fma(ptx::f2_pack(qv[c], qv[c + 1]), ptx::f2_pack(z4.x, z4.y), z2);
-      z2 = ptx::f2_fma(ptx::f2_pack(qv[c + 2], qv[c + 3]), ptx::f2_pack(z4.z, z4.w), z2);
-      if (a.corr == KVQ_CORR_TAYLOR) {
-        const uint64_t x0 = ptx::f2_mul(ptx::f2_pack(qv[c], qv[c + 1]), ptx::f2_pack(d4.x, d4.y));
-        const uint64_t x1 = ptx::f2_mul(ptx::f2_pack(qv[c + 2], qv[c + 3]), ptx::f2_pack(d4.z, d4.w));
-        b2 = ptx::f2_fma(x0, x0, b2);
-        b2 = ptx::f2_fma(x1, x1, b2);
+      for (int e = 0; e < 8; ++e) {
+        wz[8 * part + e][tt] = -bf16_hi(w[e]) * bf16_lo(w[e]);   // exact: integer z, 8-bit step
+        wd[8 * part + e][tt] = 0.5f * a.scale * bf16_lo(w[e]);
       }
     }
-    float zlo, zhi, blo, bhi;
-    ptx::f2_unpack(z2, zlo, zhi);
-    ptx::f2_unpack(b2, blo, bhi);
-    float b = (blo + bhi) * (1.0f / 6.0f);
-    if (a.corr == KVQ_CORR_EXACT) {
-      b = 0.f;
-#pragma unroll 8
-      for (int c = 0; c < D; ++c) b += log_sinhc(fabsf(qv[c]) * wd[tt][c]);
+    __syncthreads();
+#pragma unroll 4
+    for (int c = 0; c < 32; ++c) {
+      const float4 q4 = *reinterpret_cast<const float4*>(&qs[c][4 * ty]);
+      const float4 z4 = *reinterpret_cast<const float4*>(&wz[c][4 * tx]);
+      const float4 d4 = *reinterpret_cast<const float4*>(&wd[c][4 * tx]);
+      const float qv[4] = {q4.x, q4.y, q4.z, q4.w};
+      const float zv[4] = {z4.x, z4.y, z4.z, z4.w};
+      const float dv[4] = {d4.x, d4.y, d4.z, d4.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          az[i][k] = fmaf(qv[i], zv[k], az[i][k]);
+          if (taylor) {
+            const float x = qv[i] * dv[k];
+            ab[i][k] = fmaf(x, x, ab[i][k]);
+          } else if (exact) {
+            ab[i][k] += log_sinhc(fabsf(qv[i]) * dv[k]);
+          }
+        }
     }
-    a.out[((size_t)bh * a.n_ct + t0 + tt) * a.n_q + row] = kLog2e * (a.scale * (zlo + zhi) - b);
+    __syncthreads();
+  }
+  const float bscale = taylor ? 1.0f / 6.0f : 1.0f;
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const int t = t0 + 4 * tx + k;
+    if (t >= a.n_ct) continue;
+    float* dst = a.out + ((size_t)bh * a.n_ct + t) * a.n_q;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int row = row0 + 4 * ty + i;
+      if (row < a.n_q) dst[row] = kLog2e * (a.scale * az[i][k] - bscale * ab[i][k]);
+    }
   }
 }
 
@@ -1572,8 +1627,8 @@ kvq_status launch_t(const AttnLaunch& a, cudaStream_t stream) {
     k.kblk_per_head = a.kblk_per_head;
     k.scale = a.scale;
     k.corr = a.corr;
-    const dim3 kg((a.n_q + 127) / 128, (a.n_ct + kKchTiles - 1) / kKchTiles, a.bh);
-    kch_bias_kernel<D><<<kg, 128, 0, stream>>>(k);
+    const dim3 kg((a.n_q + kKchRows - 1) / kKchRows, (a.n_ct + kKchCols - 1) / kKchCols, a.bh);
+    kch_bias_kernel<D><<<kg, kKchThreads, 0, stream>>>(k);
     if (cudaGetLastError() != cudaSuccess) return KVQ_ERR_CUDA;
   }
   dim3 grid((a.n_q + kBlockM * NQ - 1) / (kBlockM * NQ), a.bh, split ? a.splits : 1);
