@@ -108,17 +108,25 @@ class ClockSampler:
                 "reasons": sorted(reasons)}
 
 
+def kernel_source_hash() -> str:
+    """First 16 hex digits of the SHA-256 of the attention kernel's source
+    (the kernel templates and the unit that instantiates the default mode)."""
+    h = hashlib.sha256()
+    for name in ("kvq_attn_kernel.cuh", "kvq_attn.cu"):
+        with open(os.path.join(ROOT, "quantized_kv_cache_quantize_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
 def _traffic_for_current_kernel():
     """DRAM bytes per attention launch from the committed ncu summary, or
     None when the kernel source changed since it was captured."""
     path = os.path.join(ROOT, "profiles", "attn_traffic.json")
-    src = os.path.join(ROOT, "quantized_kv_cache_quantize_gb300", "csrc", "kvq_attn.cu")
     if not os.path.exists(path):
         return None
     with open(path) as f:
         rec = json.load(f)
-    with open(src, "rb") as f:
-        h = hashlib.sha256(f.read()).hexdigest()[:16]
+    h = kernel_source_hash()
     if rec.get("source_sha256_16") != h:
         return None
     return rec.get("dram_bytes_per_launch_full")
