@@ -1436,6 +1436,7 @@ struct KchArgs {
   int n_q, n_ct, bpc, kblk_per_head;
   float scale;
   int corr;
+  int* status;            // device status word (the tensor-core form's bounded waits)
 };
 constexpr int kKchRows = 64;
 constexpr int kKchCols = 32;
@@ -1528,6 +1529,152 @@ __global__ void __launch_bounds__(kKchThreads) kch_bias_kernel(const KchArgs a) 
       const int row = row0 + 4 * ty + i;
       if (row < a.n_q) dst[row] = kLog2e * (a.scale * az[i][k] - bscale * ab[i][k]);
     }
+  }
+}
+
+// The same table on the tensor cores (no correction, or the Taylor term): per
+// (query row, cached tile) it is a dot product over a K of parts of D
+// channels each,
+//   part 0: q_hi . v_hi     part 1: q_hi . v_lo     part 2: q_lo . v_hi (precise)
+//   part 3: (q'^2 2^-6) . (u 2^6)                   (Taylor)
+// with v = scale log2(e) (-z_c D_c) split into FP16 high and low parts (the
+// products exact in the fp32 accumulator) and u = -log2(e) (scale/2)^2 D_c^2
+// / 6.  One CTA: 128 query rows x up to kKgN cached tiles (MMA N), K
+// streamed through shared memory 64 channels at a time.
+constexpr int kKgN = 128;
+
+template <int D>
+__global__ void __launch_bounds__(128) kch_gemm_kernel(const KchArgs a) {
+  extern __shared__ uint8_t kg_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(kg_raw) + 1023) &
+                                           ~static_cast<uintptr_t>(1023));
+  uint8_t* ta = sm;                       // A chunk: 128 rows x 64 FP16, 128-byte swizzle
+  uint8_t* tb = sm + 128 * 128;           // B chunk: kKgN rows x 64 FP16
+  uint64_t* bar = reinterpret_cast<uint64_t*>(sm + 128 * 128 + kKgN * 128);
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(bar + 1);
+  volatile int* abort = reinterpret_cast<volatile int*>(bar + 2);
+  const int tid = threadIdx.x, warp = tid >> 5;
+  const int row = blockIdx.x * 128 + tid;
+  const int t0 = blockIdx.y * kKgN, bh = blockIdx.z;
+  const int nt = min(kKgN, a.n_ct - t0);
+  const int npad = (nt + 15) & ~15;
+  const uint32_t bar_a = ptx::smem_u32(bar);
+  if (tid == 0) {
+    ptx::mbar_init(bar_a, 1);
+    *abort = 0;
+    ptx::fence_mbar_init();
+  }
+  if (warp == 0) {
+    ptx::tmem_alloc(ptx::smem_u32(tslot), kKgN);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = *tslot;
+  const bool taylor = a.corr == KVQ_CORR_TAYLOR;
+  const float sl2 = a.scale * kLog2e;
+  const float uc = -kLog2e * 0.25f * a.scale * a.scale * (1.0f / 6.0f) * 64.0f;
+  const size_t qoff = ((size_t)bh * a.n_q + min(row, a.n_q - 1)) * D;
+  const uint32_t idesc = ptx::idesc_f16kind(128, npad, false, false);
+  const uint64_t da = ptx::smem_desc(ptx::smem_u32(ta), 16, 1024, ptx::kLayoutSw128);
+  const uint64_t db = ptx::smem_desc(ptx::smem_u32(tb), 16, 1024, ptx::kLayoutSw128);
+  int phase = 0;
+  bool first = true;
+  for (int part = 0; part < 4; ++part) {
+    if ((part == 2 && a.q_lo == nullptr) || (part == 3 && !taylor)) continue;
+    for (int kc = 0; kc < D / 64; ++kc) {
+      // A: this thread's row, channels [64 kc, 64 kc + 64)
+#pragma unroll
+      for (int c8 = 0; c8 < 8; ++c8) {
+        const int ch = 64 * kc + 8 * c8;
+        const uint4 h = __ldg(reinterpret_cast<const uint4*>(a.q_hi + qoff + ch));
+        uint4 v = h;
+        if (part == 2 || part == 3) {
+          const uint4 l = a.q_lo ? __ldg(reinterpret_cast<const uint4*>(a.q_lo + qoff + ch))
+                                 : make_uint4(0u, 0u, 0u, 0u);
+          if (part == 2) {
+            v = l;
+          } else {
+            const uint32_t hw[4] = {h.x, h.y, h.z, h.w}, lw[4] = {l.x, l.y, l.z, l.w};
+            uint32_t o[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const float x0 = h_lo(hw[k]) + h_lo(lw[k]), x1 = h_hi(hw[k]) + h_hi(lw[k]);
+              o[k] = pack_h2(x0 * x0 * (1.0f / 64.0f), x1 * x1 * (1.0f / 64.0f));
+            }
+            v = make_uint4(o[0], o[1], o[2], o[3]);
+          }
+        }
+        *reinterpret_cast<uint4*>(ta + sw128(tid, c8)) = v;
+      }
+      // B: rows = cached tiles t0 + n (zero past the last), same channels
+      for (int idx = tid; idx < npad * 8; idx += 128) {
+        const int n = idx >> 3, c8 = idx & 7, t = t0 + n;
+        uint32_t o[4] = {0u, 0u, 0u, 0u};
+        if (n < nt) {
+          const int slot = t / a.bpc;
+          const uint4* src = reinterpret_cast<const uint4*>(
+              a.k_sz + ((size_t)bh * a.kblk_per_head + slot * a.bpc + (t - slot * a.bpc)) * D +
+              64 * kc + 8 * c8);
+          const uint4 x0 = __ldg(src), x1 = __ldg(src + 1);
+          const uint32_t w[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+          float f[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const float dl = bf16_lo(w[e]);
+            if (part == 3) {
+              f[e] = uc * dl * dl;
+            } else {
+              const float vv = sl2 * (-bf16_hi(w[e]) * dl);
+              const float vh = __half2float(__float2half_rn(vv));
+              f[e] = part == 1 ? vv - vh : vh;
+            }
+          }
+#pragma unroll
+          for (int k = 0; k < 4; ++k) o[k] = pack_h2(f[2 * k], f[2 * k + 1]);
+        }
+        *reinterpret_cast<uint4*>(tb + sw128(n, c8)) = make_uint4(o[0], o[1], o[2], o[3]);
+      }
+      ptx::fence_proxy_async_smem();
+      __syncthreads();
+      if (tid == 0) {
+        ptx::tc_fence_after();
+#pragma unroll
+        for (int s = 0; s < 4; ++s) ptx::mma_f16(tmem, da + (uint64_t)(s * 2), db + (uint64_t)(s * 2), idesc, first ? (s > 0) : 1u);
+        ptx::mma_commit(bar_a);
+      }
+      first = false;
+      // the chunk buffers are rewritten only once the MMAs have read them
+      wait_bar(bar_a, phase, 2000000000ull, abort, a.status);
+      phase ^= 1;
+      ptx::tc_fence_after();
+    }
+  }
+  // every MMA issued is complete before the tensor memory is read or freed
+  // (also after a wait that ran out)
+  if (tid == 0) ptx::mma_commit(bar_a);
+  int drained = 0;
+  wait_bar(bar_a, phase, 2000000000ull, &drained, a.status);
+  ptx::tc_fence_after();
+  // the tensor-memory loads are warp-collective: every lane takes part, only
+  // the rows of the chunk store
+  if (__all_sync(0xffffffffu, !first && !*abort)) {
+    for (int c = 0; c < npad; c += 32) {
+      uint32_t v[32];
+      ptx::tmem_ld32(tmem + c + ((uint32_t)(warp * 32) << 16), v);
+      if (row < a.n_q) {
+#pragma unroll
+        for (int k = 0; k < 32; ++k)
+          if (c + k < nt) a.out[((size_t)bh * a.n_ct + t0 + c + k) * a.n_q + row] = __uint_as_float(v[k]);
+      }
+    }
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, kKgN);
   }
 }
 
@@ -1627,8 +1774,20 @@ kvq_status launch_t(const AttnLaunch& a, cudaStream_t stream) {
     k.kblk_per_head = a.kblk_per_head;
     k.scale = a.scale;
     k.corr = a.corr;
-    const dim3 kg((a.n_q + kKchRows - 1) / kKchRows, (a.n_ct + kKchCols - 1) / kKchCols, a.bh);
-    kch_bias_kernel<D><<<kg, kKchThreads, 0, stream>>>(k);
+    k.status = a.status;
+    if (a.corr == KVQ_CORR_EXACT) {
+      // log(sinh a / a) per channel: the CUDA-core form
+      const dim3 kg((a.n_q + kKchRows - 1) / kKchRows, (a.n_ct + kKchCols - 1) / kKchCols, a.bh);
+      kch_bias_kernel<D><<<kg, kKchThreads, 0, stream>>>(k);
+    } else {
+      const dim3 kg((a.n_q + 127) / 128, (a.n_ct + kKgN - 1) / kKgN, a.bh);
+      // 33 KB used; 50 KB requested so that at most four CTAs (4 x 128
+      // tensor-memory columns) share an SM
+      const int smem = 50 * 1024;
+      static std::atomic<uint64_t> kg_limit{0};
+      if (ensure_smem_limit(kch_gemm_kernel<D>, smem, kg_limit) != cudaSuccess) return KVQ_ERR_CUDA;
+      kch_gemm_kernel<D><<<kg, 128, smem, stream>>>(k);
+    }
     if (cudaGetLastError() != cudaSuccess) return KVQ_ERR_CUDA;
   }
   dim3 grid((a.n_q + kBlockM * NQ - 1) / (kBlockM * NQ), a.bh, split ? a.splits : 1);
