@@ -329,7 +329,7 @@ def run_gpu(args):
     return result
 
 
-def _oracle_sample(w, head: int, rows: int, seed: int, corr: int = 1):
+def _oracle_sample(w, head: int, rows: int, seed: int, corr: int = 1, key_mode: int = 0):
     """One bounded sample of the step on the CPU oracle: quantize-append of
     one head's chunk (K and V) and the corrected attention of ``rows`` query
     rows of that head over its full window and current chunk."""
@@ -340,13 +340,26 @@ def _oracle_sample(w, head: int, rows: int, seed: int, corr: int = 1):
     x = synth.head_inputs(w, head, seed=seed)
     s = synth.hadamard_signs(w.head_dim, seed=seed)
     t0 = time.perf_counter()
-    O.quantize_rows(x["k_new"].float().numpy(), s, w.bits, w.group)
     O.quantize_rows(x["v_new"].float().numpy(), s, w.bits, w.group)
-    _, kd, kz, _, kc = O.quantize_rows(x["k_win"].float().numpy(), s, w.bits, w.group)
     _, vd, vz, _, vcod = O.quantize_rows(x["v_win"].float().numpy(), s, w.bits, w.group)
-    O.chunk_attention(x["q"].float().numpy()[:rows], O.dequantize(kc, kd, kz, w.group),
-                      O.dequantize(vcod, vd, vz, w.group), kd, x["k_cur"].float().numpy(),
-                      x["v_cur"].float().numpy(), s, w.scale, w.group, corr)
+    if key_mode:
+        # per-channel keys: each chunk per channel over 128-token blocks
+        O.quantize_key_chunk(x["k_new"].float().numpy(), s, w.bits)
+        kf = x["k_win"].float().numpy()
+        kh, steps = [], []
+        for c0 in range(0, kf.shape[0], w.chunk_tokens):
+            part = kf[c0:c0 + w.chunk_tokens]
+            _, kd, kz, _, kc = O.quantize_key_chunk(part, s, w.bits)
+            kh.append(O.dequantize_key_channels(kc, kd, kz))
+            steps.append(O.key_channel_token_steps(kd, part.shape[0]))
+        k_hat, k_steps, group = np.concatenate(kh), np.concatenate(steps), 1
+    else:
+        O.quantize_rows(x["k_new"].float().numpy(), s, w.bits, w.group)
+        _, kd, kz, _, kc = O.quantize_rows(x["k_win"].float().numpy(), s, w.bits, w.group)
+        k_hat, k_steps, group = O.dequantize(kc, kd, kz, w.group), kd, w.group
+    O.chunk_attention(x["q"].float().numpy()[:rows], k_hat, O.dequantize(vcod, vd, vz, w.group),
+                      k_steps, x["k_cur"].float().numpy(), x["v_cur"].float().numpy(), s, w.scale,
+                      group, corr)
     dt = time.perf_counter() - t0
     flops = w.attention_flops(n_q=rows, heads=1)
     return flops, dt
@@ -368,7 +381,7 @@ def cpu_baseline(w, args):
     rows = min(args.cpu_rows, w.n_q) if args.cpu_rows > 0 else (128 if args.corr == 2 else w.n_q)
     tot_f, tot_t, heads = 0.0, 0.0, 0
     while heads < w.heads and (heads == 0 or tot_t < args.cpu_seconds):
-        f, dt = _oracle_sample(w, heads, rows, args.seed, args.corr)
+        f, dt = _oracle_sample(w, heads, rows, args.seed, args.corr, args.key_mode)
         tot_f += f
         tot_t += dt
         heads += 1
@@ -388,10 +401,10 @@ def run_reference(args):
     w = _workload(args.workload)
     rows = args.ref_rows
     for _ in range(args.warmup):
-        _oracle_sample(w, 0, rows, args.seed, args.corr)
+        _oracle_sample(w, 0, rows, args.seed, args.corr, args.key_mode)
     tot_f, tot_t = 0.0, 0.0
     for k in range(args.steps):
-        f, dt = _oracle_sample(w, k % w.heads, rows, args.seed, args.corr)
+        f, dt = _oracle_sample(w, k % w.heads, rows, args.seed, args.corr, args.key_mode)
         tot_f += f
         tot_t += dt
     value = tot_f / tot_t / 1e12
