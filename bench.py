@@ -132,6 +132,18 @@ def _traffic_for_current_kernel():
     return rec.get("dram_bytes_per_launch_full")
 
 
+def max_over_ranks(value: float, world: int, device=None) -> float:
+    """The largest of every rank's value (a step time): the whole job is as
+    slow as its slowest rank.  One all-reduce; a no-op on one rank."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def run_gpu(args):
     import torch
     import torch.distributed as dist
@@ -200,10 +212,7 @@ def run_gpu(args):
     if status != 0:
         raise RuntimeError(f"device status {status} after the timed region")
 
-    t = torch.tensor([ms_step], device=dev)
-    if world > 1:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    ms_max = float(t.item())
+    ms_max = max_over_ranks(ms_step, world, dev)
     flops = w.attention_flops()
     value = flops * world / (ms_max * 1e-3) / 1e12
 
@@ -278,11 +287,7 @@ def run_gpu(args):
         e2e_step(i)
     e1.record(s_out)
     torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1) / e2e_steps
-    t = torch.tensor([e2e_ms], device=dev)
-    if world > 1:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, world, dev)
 
     result = None
     if rank == 0:
