@@ -230,7 +230,9 @@ def run_gpu(args):
     peak = bf16_sust if region_s >= 1.0 else bf16_burst
     q_bytes = w.append_bytes()
     k1_gbs = q_bytes / (k1_ms * 1e-3) / 1e9
-    rot_bytes = 2.0 * (w.n_q + 2 * w.n_r) * d * B * H * 2
+    # the rotation kernel reads the BF16 query and current values and writes
+    # them as FP16 (and the query's FP16 remainder with the precise split)
+    rot_bytes = (w.n_q + w.n_r) * d * B * H * 4.0 + (w.n_q * d * B * H * 2.0 if args.flags & 1 else 0.0)
     launches = sum(v["launches"] for v in prof.values())
 
     # end to end through the public API with host buffers (pinned), copies inside the timed

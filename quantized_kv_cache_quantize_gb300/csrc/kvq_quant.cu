@@ -25,6 +25,7 @@ namespace kvq {
 namespace {
 
 constexpr int kThreads = 256;
+constexpr int kRotUnroll = 4;   // rows per lane group in flight in the rotation kernel
 
 __device__ __forceinline__ uint32_t h_bits_rn(float v) {
   return (uint32_t)__half_as_ushort(__float2half_rn(v));
@@ -665,42 +666,55 @@ __global__ void __launch_bounds__(kThreads) rotate_kernel(const RotateArgs a) {
   const long long nwarps = ((long long)gridDim.x * blockDim.x) >> 5;
   const uint32_t sign_word = sign_word_for(a.sign_bits, t);
 
-  for (long long r0 = warp0 * RPW; r0 < total; r0 += nwarps * RPW) {
-    const long long r = r0 + lane / LPR;
-    const bool valid = r < total;
-    long long rr = valid ? r : 0;
-    const bool seg1 = rr >= a.rows[0];
-    if (seg1) rr -= a.rows[0];
-    const uint16_t* srcp = seg1 ? a.src[1] : a.src[0];
-    void* dstp = seg1 ? a.dst[1] : a.dst[0];
-    uint16_t* lop = seg1 ? a.dst_lo[1] : a.dst_lo[0];
-    uint4 raw = make_uint4(0u, 0u, 0u, 0u);
-    if (valid) raw = __ldg(reinterpret_cast<const uint4*>(srcp + rr * D + 8 * t));
-    float x[8];
-    load8_signed(raw, sign_word, t, x);
-    fwht_row<LPR>(x, t);
+  // kRotUnroll rows per lane group in flight: their loads are issued
+  // before any of them is transformed
+  constexpr int U = kRotUnroll;
+  const long long step = nwarps * RPW;
+  for (long long r0 = warp0 * RPW; r0 < total; r0 += step * U) {
+    uint4 raw[U];
+    long long rr[U];
+    bool valid[U], seg1[U];
 #pragma unroll
-    for (int e = 0; e < 8; ++e) x[e] = __fmul_rn(x[e], a.inv_sqrt_d);
-    if (!valid) continue;
-    if (a.out_f32) {
-      float4* dst = reinterpret_cast<float4*>(static_cast<float*>(dstp) + rr * D + 8 * t);
-      dst[0] = make_float4(x[0], x[1], x[2], x[3]);
-      dst[1] = make_float4(x[4], x[5], x[6], x[7]);
-    } else {
-      uint32_t hb[8];
+    for (int u = 0; u < U; ++u) {
+      const long long r = r0 + u * step + lane / LPR;
+      valid[u] = r < total;
+      rr[u] = valid[u] ? r : 0;
+      seg1[u] = rr[u] >= a.rows[0];
+      if (seg1[u]) rr[u] -= a.rows[0];
+      const uint16_t* srcp = seg1[u] ? a.src[1] : a.src[0];
+      raw[u] = valid[u] ? __ldg(reinterpret_cast<const uint4*>(srcp + rr[u] * D + 8 * t))
+                        : make_uint4(0u, 0u, 0u, 0u);
+    }
 #pragma unroll
-      for (int e = 0; e < 8; ++e) hb[e] = h_bits_rn(x[e]);
-      *reinterpret_cast<uint4*>(static_cast<uint16_t*>(dstp) + rr * D + 8 * t) =
-          make_uint4(hb[0] | (hb[1] << 16), hb[2] | (hb[3] << 16), hb[4] | (hb[5] << 16),
-                     hb[6] | (hb[7] << 16));
-      if (lop != nullptr) {
-        uint32_t lb[8];
+    for (int u = 0; u < U; ++u) {
+      void* dstp = seg1[u] ? a.dst[1] : a.dst[0];
+      uint16_t* lop = seg1[u] ? a.dst_lo[1] : a.dst_lo[0];
+      float x[8];
+      load8_signed(raw[u], sign_word, t, x);
+      fwht_row<LPR>(x, t);   // all lanes: warp-collective shuffles
 #pragma unroll
-        for (int e = 0; e < 8; ++e)
-          lb[e] = h_bits_rn(__fsub_rn(x[e], __half2float(__ushort_as_half((unsigned short)hb[e]))));
-        *reinterpret_cast<uint4*>(lop + rr * D + 8 * t) =
-            make_uint4(lb[0] | (lb[1] << 16), lb[2] | (lb[3] << 16), lb[4] | (lb[5] << 16),
-                       lb[6] | (lb[7] << 16));
+      for (int e = 0; e < 8; ++e) x[e] = __fmul_rn(x[e], a.inv_sqrt_d);
+      if (!valid[u]) continue;
+      if (a.out_f32) {
+        float4* dst = reinterpret_cast<float4*>(static_cast<float*>(dstp) + rr[u] * D + 8 * t);
+        dst[0] = make_float4(x[0], x[1], x[2], x[3]);
+        dst[1] = make_float4(x[4], x[5], x[6], x[7]);
+      } else {
+        uint32_t hb[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) hb[e] = h_bits_rn(x[e]);
+        *reinterpret_cast<uint4*>(static_cast<uint16_t*>(dstp) + rr[u] * D + 8 * t) =
+            make_uint4(hb[0] | (hb[1] << 16), hb[2] | (hb[3] << 16), hb[4] | (hb[5] << 16),
+                       hb[6] | (hb[7] << 16));
+        if (lop != nullptr) {
+          uint32_t lb[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e)
+            lb[e] = h_bits_rn(__fsub_rn(x[e], __half2float(__ushort_as_half((unsigned short)hb[e]))));
+          *reinterpret_cast<uint4*>(lop + rr[u] * D + 8 * t) =
+              make_uint4(lb[0] | (lb[1] << 16), lb[2] | (lb[3] << 16), lb[4] | (lb[5] << 16),
+                         lb[6] | (lb[7] << 16));
+        }
       }
     }
   }

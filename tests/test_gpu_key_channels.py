@@ -112,3 +112,42 @@ def test_full_workload_sampled_rows(name, corr, flags, heads, rows):
         o_ref, ps_ref, pr_ref = oracle_head_kch(w, x, s, 0, int(h), sel, corr)
         assert_close(out[0, h, sel].float().cpu().numpy(), o_ref, ps[0, h, sel].cpu().numpy(),
                      ps_ref, pr[0, h, sel].cpu().numpy(), pr_ref, what=f"{name} kch h{h}")
+
+
+def test_batch_and_heads_layout():
+    """batch 2 x heads 3 with per-channel keys: each (b, h) attends to its own
+    cache (its own per-block steps) and chunk."""
+    w = synth.Workload("kch_bh", heads=3, head_dim=128, chunk_tokens=200, n_chunks=2, bits=2,
+                       group=32, n_outliers_fixed=3, outlier_scale=10.0, offset_std=0.5)
+    xs = [synth.inputs(w, seed=sd, n_q=150, n_s=400, n_r=90) for sd in (1, 2)]
+    x = {k: torch.cat([xs[0][k], xs[1][k]], dim=0).contiguous() for k in xs[0]}
+    s = synth.hadamard_signs(128, seed=5)
+    cache = build_cache_kch(w, x, s)
+    out, ps, pr = kvq.attention_corrected(cache, x["q"].cuda(), x["k_cur"].cuda(),
+                                          x["v_cur"].cuda(), with_mass=True)
+    torch.cuda.synchronize()
+    for b in range(2):
+        for h in range(3):
+            o_ref, ps_ref, pr_ref = oracle_head_kch(w, x, s, b, h, np.arange(150), O.CORR_TAYLOR)
+            assert_close(out[b, h].float().cpu().numpy(), o_ref, ps[b, h].cpu().numpy(), ps_ref,
+                         pr[b, h].cpu().numpy(), pr_ref, what=f"kch b{b} h{h}")
+
+
+@pytest.mark.parametrize("corr", CORRS)
+def test_noalloc_matches_workspace(corr):
+    """The allocation-free entry point with per-channel keys (its built-in
+    scratch also holds the per-(row, tile) table) gives what the workspace
+    entry point gives."""
+    w = synth.Workload("kch_na", heads=2, head_dim=128, chunk_tokens=300, n_chunks=3, bits=2,
+                       group=32, n_outliers_fixed=3, outlier_scale=8.0, offset_std=0.4)
+    x = synth.inputs(w, seed=31, n_q=400, n_s=900, n_r=300)
+    s = synth.hadamard_signs(128, seed=31)
+    cache = build_cache_kch(w, x, s)
+    q, kc, vc = x["q"].cuda(), x["k_cur"].cuda(), x["v_cur"].cuda()
+    ref_o, ref_ps, _ = kvq.attention_corrected(cache, q, kc, vc, corr=corr, with_mass=True)
+    o, ps, _ = kvq.attention_corrected_noalloc(cache, q, kc, vc, corr=corr, with_mass=True)
+    torch.cuda.synchronize()
+    assert kvq.last_device_status() == kvq.KVQ_OK
+    ref = ref_o.float()
+    assert (o.float() - ref).abs().max().item() <= 2e-2 * ref.abs().max().item()
+    assert (ps - ref_ps).abs().max().item() <= 1e-3
