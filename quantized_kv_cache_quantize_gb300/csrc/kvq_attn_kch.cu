@@ -132,25 +132,30 @@ __global__ void __launch_bounds__(kKchThreads) kch_bias_kernel(const KchArgs a) 
 // / 6.  One CTA: 128 query rows x up to kKgN cached tiles (MMA N), K
 // streamed through shared memory 64 channels at a time.
 constexpr int kKgN = 128;
+constexpr int kKgThreads = 256;   // two threads per query row
 
 template <int D>
-__global__ void __launch_bounds__(128) kch_gemm_kernel(const KchArgs a) {
+__global__ void __launch_bounds__(kKgThreads) kch_gemm_kernel(const KchArgs a) {
   extern __shared__ uint8_t kg_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(kg_raw) + 1023) &
                                            ~static_cast<uintptr_t>(1023));
-  uint8_t* ta = sm;                       // A chunk: 128 rows x 64 FP16, 128-byte swizzle
-  uint8_t* tb = sm + 128 * 128;           // B chunk: kKgN rows x 64 FP16
-  uint64_t* bar = reinterpret_cast<uint64_t*>(sm + 128 * 128 + kKgN * 128);
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(bar + 1);
-  volatile int* abort = reinterpret_cast<volatile int*>(bar + 2);
+  // two chunk buffers, each A (128 rows x 64 FP16) then B (kKgN rows x 64
+  // FP16), 128-byte swizzle: chunk c + 1 is written while the MMAs of chunk
+  // c run
+  constexpr int kBuf = 128 * 128 + kKgN * 128;
+  uint64_t* bar = reinterpret_cast<uint64_t*>(sm + 2 * kBuf);   // [2] chunk MMAs done
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(bar + 2);
+  volatile int* abort = reinterpret_cast<volatile int*>(bar + 3);
   const int tid = threadIdx.x, warp = tid >> 5;
-  const int row = blockIdx.x * 128 + tid;
+  const int r = tid & 127, half = tid >> 7;   // row of the tile, half of its channels
+  const int row = blockIdx.x * 128 + r;
   const int t0 = blockIdx.y * kKgN, bh = blockIdx.z;
   const int nt = min(kKgN, a.n_ct - t0);
   const int npad = (nt + 15) & ~15;
-  const uint32_t bar_a = ptx::smem_u32(bar);
+  const uint32_t bar0 = ptx::smem_u32(bar);
   if (tid == 0) {
-    ptx::mbar_init(bar_a, 1);
+    ptx::mbar_init(bar0, 1);
+    ptx::mbar_init(bar0 + 8, 1);
     *abort = 0;
     ptx::fence_mbar_init();
   }
@@ -167,89 +172,94 @@ __global__ void __launch_bounds__(128) kch_gemm_kernel(const KchArgs a) {
   const float uc = -kLog2e * 0.25f * a.scale * a.scale * (1.0f / 6.0f) * 64.0f;
   const size_t qoff = ((size_t)bh * a.n_q + min(row, a.n_q - 1)) * D;
   const uint32_t idesc = ptx::idesc_f16kind(128, npad, false, false);
-  const uint64_t da = ptx::smem_desc(ptx::smem_u32(ta), 16, 1024, ptx::kLayoutSw128);
-  const uint64_t db = ptx::smem_desc(ptx::smem_u32(tb), 16, 1024, ptx::kLayoutSw128);
-  int phase = 0;
-  bool first = true;
-  for (int part = 0; part < 4; ++part) {
-    if ((part == 2 && a.q_lo == nullptr) || (part == 3 && !taylor)) continue;
-    for (int kc = 0; kc < D / 64; ++kc) {
-      // A: this thread's row, channels [64 kc, 64 kc + 64)
+  // the chunks: (part, 64-channel block) for the parts this launch needs
+  const int np = a.q_lo != nullptr ? 3 : 2;
+  const int n_chunks = (np + (taylor ? 1 : 0)) * (D / 64);
+  for (int ci = 0; ci < n_chunks; ++ci) {
+    const int pi = ci / (D / 64), kc = ci - pi * (D / 64);
+    const int part = pi < np ? pi : 3;
+    const int b = ci & 1;
+    uint8_t* ta = sm + b * kBuf;
+    uint8_t* tb = ta + 128 * 128;
+    // buffer b was last read by the MMAs of chunk ci - 2
+    if (ci >= 2) wait_bar(bar0 + 8 * b, ((ci - 2) >> 1) & 1, 2000000000ull, abort, a.status);
+    // A: this thread's half of its row's channels [64 kc, 64 kc + 64)
 #pragma unroll
-      for (int c8 = 0; c8 < 8; ++c8) {
-        const int ch = 64 * kc + 8 * c8;
-        const uint4 h = __ldg(reinterpret_cast<const uint4*>(a.q_hi + qoff + ch));
-        uint4 v = h;
-        if (part == 2 || part == 3) {
-          const uint4 l = a.q_lo ? __ldg(reinterpret_cast<const uint4*>(a.q_lo + qoff + ch))
-                                 : make_uint4(0u, 0u, 0u, 0u);
-          if (part == 2) {
-            v = l;
+    for (int c4 = 0; c4 < 4; ++c4) {
+      const int c8 = 4 * half + c4;
+      const int ch = 64 * kc + 8 * c8;
+      const uint4 h = __ldg(reinterpret_cast<const uint4*>(a.q_hi + qoff + ch));
+      uint4 v = h;
+      if (part == 2 || part == 3) {
+        const uint4 l = a.q_lo ? __ldg(reinterpret_cast<const uint4*>(a.q_lo + qoff + ch))
+                               : make_uint4(0u, 0u, 0u, 0u);
+        if (part == 2) {
+          v = l;
+        } else {
+          const uint32_t hw[4] = {h.x, h.y, h.z, h.w}, lw[4] = {l.x, l.y, l.z, l.w};
+          uint32_t o[4];
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const float x0 = h_lo(hw[k]) + h_lo(lw[k]), x1 = h_hi(hw[k]) + h_hi(lw[k]);
+            o[k] = pack_h2(x0 * x0 * (1.0f / 64.0f), x1 * x1 * (1.0f / 64.0f));
+          }
+          v = make_uint4(o[0], o[1], o[2], o[3]);
+        }
+      }
+      *reinterpret_cast<uint4*>(ta + sw128(r, c8)) = v;
+    }
+    // B: rows = cached tiles t0 + n (zero past the last), same channels
+    for (int idx = tid; idx < npad * 8; idx += kKgThreads) {
+      const int n = idx >> 3, c8 = idx & 7, t = t0 + n;
+      uint32_t o[4] = {0u, 0u, 0u, 0u};
+      if (n < nt) {
+        const int slot = t / a.bpc;
+        const uint4* src = reinterpret_cast<const uint4*>(
+            a.k_sz + ((size_t)bh * a.kblk_per_head + slot * a.bpc + (t - slot * a.bpc)) * D +
+            64 * kc + 8 * c8);
+        const uint4 x0 = __ldg(src), x1 = __ldg(src + 1);
+        const uint32_t w[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+        float f[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const float dl = bf16_lo(w[e]);
+          if (part == 3) {
+            f[e] = uc * dl * dl;
           } else {
-            const uint32_t hw[4] = {h.x, h.y, h.z, h.w}, lw[4] = {l.x, l.y, l.z, l.w};
-            uint32_t o[4];
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              const float x0 = h_lo(hw[k]) + h_lo(lw[k]), x1 = h_hi(hw[k]) + h_hi(lw[k]);
-              o[k] = pack_h2(x0 * x0 * (1.0f / 64.0f), x1 * x1 * (1.0f / 64.0f));
-            }
-            v = make_uint4(o[0], o[1], o[2], o[3]);
+            const float vv = sl2 * (-bf16_hi(w[e]) * dl);
+            const float vh = __half2float(__float2half_rn(vv));
+            f[e] = part == 1 ? vv - vh : vh;
           }
         }
-        *reinterpret_cast<uint4*>(ta + sw128(tid, c8)) = v;
-      }
-      // B: rows = cached tiles t0 + n (zero past the last), same channels
-      for (int idx = tid; idx < npad * 8; idx += 128) {
-        const int n = idx >> 3, c8 = idx & 7, t = t0 + n;
-        uint32_t o[4] = {0u, 0u, 0u, 0u};
-        if (n < nt) {
-          const int slot = t / a.bpc;
-          const uint4* src = reinterpret_cast<const uint4*>(
-              a.k_sz + ((size_t)bh * a.kblk_per_head + slot * a.bpc + (t - slot * a.bpc)) * D +
-              64 * kc + 8 * c8);
-          const uint4 x0 = __ldg(src), x1 = __ldg(src + 1);
-          const uint32_t w[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
-          float f[8];
 #pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            const float dl = bf16_lo(w[e]);
-            if (part == 3) {
-              f[e] = uc * dl * dl;
-            } else {
-              const float vv = sl2 * (-bf16_hi(w[e]) * dl);
-              const float vh = __half2float(__float2half_rn(vv));
-              f[e] = part == 1 ? vv - vh : vh;
-            }
-          }
-#pragma unroll
-          for (int k = 0; k < 4; ++k) o[k] = pack_h2(f[2 * k], f[2 * k + 1]);
-        }
-        *reinterpret_cast<uint4*>(tb + sw128(n, c8)) = make_uint4(o[0], o[1], o[2], o[3]);
+        for (int k = 0; k < 4; ++k) o[k] = pack_h2(f[2 * k], f[2 * k + 1]);
       }
-      ptx::fence_proxy_async_smem();
-      __syncthreads();
-      if (tid == 0) {
-        ptx::tc_fence_after();
-#pragma unroll
-        for (int s = 0; s < 4; ++s) ptx::mma_f16(tmem, da + (uint64_t)(s * 2), db + (uint64_t)(s * 2), idesc, first ? (s > 0) : 1u);
-        ptx::mma_commit(bar_a);
-      }
-      first = false;
-      // the chunk buffers are rewritten only once the MMAs have read them
-      wait_bar(bar_a, phase, 2000000000ull, abort, a.status);
-      phase ^= 1;
+      *reinterpret_cast<uint4*>(tb + sw128(n, c8)) = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+    ptx::fence_proxy_async_smem();
+    __syncthreads();
+    if (tid == 0) {
       ptx::tc_fence_after();
+      const uint64_t da = ptx::smem_desc(ptx::smem_u32(ta), 16, 1024, ptx::kLayoutSw128);
+      const uint64_t db = ptx::smem_desc(ptx::smem_u32(tb), 16, 1024, ptx::kLayoutSw128);
+#pragma unroll
+      for (int s4 = 0; s4 < 4; ++s4)
+        ptx::mma_f16(tmem, da + (uint64_t)(s4 * 2), db + (uint64_t)(s4 * 2), idesc,
+                     (ci > 0 || s4 > 0) ? 1u : 0u);
+      ptx::mma_commit(bar0 + 8 * b);
     }
   }
-  // every MMA issued is complete before the tensor memory is read or freed
-  // (also after a wait that ran out)
-  if (tid == 0) ptx::mma_commit(bar_a);
-  int drained = 0;
-  wait_bar(bar_a, phase, 2000000000ull, &drained, a.status);
+  // every MMA issued is complete (the last commit covers the earlier ones)
+  // before the tensor memory is read or freed, also after a wait that ran out
+  {
+    const int last = n_chunks - 1;
+    int drained = 0;
+    wait_bar(bar0 + 8 * (last & 1), (last >> 1) & 1, 2000000000ull, &drained, a.status);
+  }
   ptx::tc_fence_after();
-  // the tensor-memory loads are warp-collective: every lane takes part, only
-  // the rows of the chunk store
-  if (__all_sync(0xffffffffu, !first && !*abort)) {
+  // the tensor-memory loads are warp-collective: every lane of warps 0-3
+  // (lanes 0-127: the rows) takes part, only the rows of the chunk store
+  if (warp < 4 && __all_sync(0xffffffffu, !*abort)) {
     for (int c = 0; c < npad; c += 32) {
       uint32_t v[32];
       ptx::tmem_ld32(tmem + c + ((uint32_t)(warp * 32) << 16), v);
@@ -290,12 +300,12 @@ kvq_status launch_kch_table(const AttnLaunch& a, cudaStream_t stream) {
     kch_bias_kernel<D><<<kg, kKchThreads, 0, stream>>>(k);
   } else {
     const dim3 kg((a.n_q + 127) / 128, (a.n_ct + kKgN - 1) / kKgN, a.bh);
-    // 33 KB used; 50 KB requested so that at most four CTAs (4 x 128
-    // tensor-memory columns) share an SM
-    const int smem = 50 * 1024;
+    // two 32 KB chunk buffers (at most three CTAs, 3 x 128 tensor-memory
+    // columns, share an SM)
+    const int smem = 1024 + 2 * (128 * 128 + kKgN * 128) + 64;
     static std::atomic<uint64_t> kg_limit{0};
     if (ensure_smem_limit(kch_gemm_kernel<D>, smem, kg_limit) != cudaSuccess) return KVQ_ERR_CUDA;
-    kch_gemm_kernel<D><<<kg, 128, smem, stream>>>(k);
+    kch_gemm_kernel<D><<<kg, kKgThreads, smem, stream>>>(k);
   }
   return cudaGetLastError() == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
 }

@@ -259,3 +259,35 @@ def test_full_workload_exact_sampled(name, flags, heads, rows):
         o_ref, ps_ref, pr_ref = oracle_head(w, x, s, 0, int(h), sel, O.CORR_EXACT)
         assert_close(out[0, h, sel].float().cpu().numpy(), o_ref, ps[0, h, sel].cpu().numpy(),
                      ps_ref, pr[0, h, sel].cpu().numpy(), pr_ref, what=f"exact {name} h{h}")
+
+
+@pytest.mark.parametrize("key_mode", [kvq.KEYS_PER_TOKEN, kvq.KEYS_PER_CHANNEL])
+def test_cache_checkpoint_roundtrip(key_mode):
+    """The cache is the path's only state: its four buffers (sizes from
+    kvq_cache_bytes / kvq_cache_meta_bytes) and the ring state (len,
+    head_slot) copied to the host and into a fresh cache give the same
+    attention, bit for bit, and the same next append."""
+    w = synth.Workload("ckpt", heads=2, head_dim=128, chunk_tokens=200, n_chunks=3, bits=2,
+                       group=32, n_outliers_fixed=3, outlier_scale=8.0, offset_std=0.4)
+    x = synth.inputs(w, seed=41, n_q=150, n_s=500, n_r=120)
+    s = synth.hadamard_signs(128, seed=41)
+    cache = kvq.KVCache(1, 2, 128, 2, 32, 200, 3, s, key_mode=key_mode)
+    for c0 in range(0, 500, 200):
+        kvq.quantize_append(cache, x["k_win"][:, :, c0:c0 + 200].contiguous().cuda(),
+                            x["v_win"][:, :, c0:c0 + 200].contiguous().cuda())
+    saved = {k: getattr(cache, k).cpu() for k in ("k_codes", "v_codes", "k_sz", "v_sz")}
+    state = (cache.struct.len, cache.struct.head_slot)
+    restored = kvq.KVCache(1, 2, 128, 2, 32, 200, 3, s, key_mode=key_mode)
+    for k, v in saved.items():
+        getattr(restored, k).copy_(v)
+    restored.struct.len, restored.struct.head_slot = state
+    q, kc, vc = x["q"].cuda(), x["k_cur"].cuda(), x["v_cur"].cuda()
+    o1, ps1, _ = kvq.attention_corrected(cache, q, kc, vc, with_mass=True)
+    o2, ps2, _ = kvq.attention_corrected(restored, q, kc, vc, with_mass=True)
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2) and torch.equal(ps1, ps2)
+    nxt_k = x["k_cur"][:, :, :100].contiguous().cuda()
+    nxt_v = x["v_cur"][:, :, :100].contiguous().cuda()
+    with pytest.raises(kvq.KVQError):          # partial newest chunk: only whole chunks follow
+        kvq.quantize_append(restored, nxt_k, nxt_v)
+    assert (restored.len, restored.head_slot) == state
