@@ -81,6 +81,9 @@ typedef enum {
  *   keeps its form with one channel per group:
  *   b_ij = scale^2 / 24 * sum_c q'_{j,c}^2 * D_{c,blk(i)}^2 (TAYLOR), or the
  *   exact sum_c log(sinh a_c / a_c) with a_c = scale/2 |q'_{j,c}| D_{c,blk(i)}.
+ *   The attention adds a per-(query row, key block) table to the workspace
+ *   (see kvq_workspace_bytes); with TAYLOR its tensor-core pre-pass needs
+ *   rotated query values |q'| < 2047.
  */
 #define KVQ_KEYS_PER_TOKEN 0
 #define KVQ_KEYS_PER_CHANNEL 1
