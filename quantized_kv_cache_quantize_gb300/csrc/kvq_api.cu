@@ -349,6 +349,7 @@ kvq_status kvq_quantize_append(kvq_cache* cache, const uint16_t* k_new, const ui
   for (int i = 0; i < 4; ++i) a.sign_bits[i] = cache->sign_bits[i];
   a.inv_sqrt_d = (float)(1.0 / std::sqrt((double)g.d));
   a.v_only = g.key_mode == KVQ_KEYS_PER_CHANNEL ? 1 : 0;
+  kvq::row_divisor((uint32_t)n_new, &a.div_mul, &a.div_shift);
   a.kblk_first = cache->head_slot * g.bpc;
   a.kblk_per_head = cache->n_chunks * g.bpc;
   bool supported = true;

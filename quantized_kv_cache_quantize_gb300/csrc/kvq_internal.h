@@ -38,6 +38,11 @@ struct QuantArgs {
   uint32_t sign_bits[4];
   float inv_sqrt_d;
   int v_only;      // per-channel key mode: the per-token kernels quantize the V rows only
+  // row r of a tensor is token r - n_new * (r / n_new) of (batch, head)
+  // r / n_new, the quotient taken as umulhi(r, div_mul) >> div_shift
+  // (div_mul = 0: a power of two, r >> div_shift)
+  uint32_t div_mul;
+  int div_shift;
   // per-channel key mode: k_sz holds kblk_per_head blocks of d words per
   // head; this append's blocks start at block kblk_first
   int kblk_first;
@@ -74,6 +79,24 @@ cudaError_t ensure_smem_limit(Kernel kern, int bytes, std::atomic<uint64_t>& don
 
 cudaError_t launch_quantize_append(const QuantArgs& a, int d, int bits, int group,
                                    cudaStream_t stream, bool* supported);
+// Multiplier and shift of the quotient r / d for every r < 2^31 and
+// 1 <= d < 2^31 (division by an invariant integer, Granlund and Montgomery):
+// with l = floor(log2 d), d not a power of two, m = ceil(2^(32+l) / d) fits
+// 32 bits and umulhi(r, m) >> l = floor(r / d), because r * (m - 2^(32+l)/d)
+// / 2^(32+l) < r / 2^(32+l) < 1/d when r < 2^31 <= 2^(32+l)/d.  A power of
+// two is a plain shift (m = 0).
+inline void row_divisor(uint32_t d, uint32_t* mul, int* shift) {
+  int l = 0;
+  while ((2u << l) <= d && l < 31) ++l;   // 2^l <= d < 2^(l+1)
+  *shift = l;
+  if ((d & (d - 1)) == 0) {
+    *mul = 0;
+    return;
+  }
+  const unsigned long long num = 1ull << (32 + l);
+  *mul = (uint32_t)((num + d - 1) / d);
+}
+
 // per-channel key mode: the K rows of one append, per channel over blocks of
 // kKeyBlock tokens
 constexpr int kKeyBlock = 128;

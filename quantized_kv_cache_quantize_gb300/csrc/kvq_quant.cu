@@ -202,7 +202,7 @@ __device__ __forceinline__ void quantize_row(const QuantArgs& a, const PairSigns
 
   const bool is_v = r >= per_kv;
   const unsigned rk = is_v ? r - per_kv : r;
-  const unsigned bh = rk / (unsigned)a.n_new;
+  const unsigned bh = a.div_mul ? (__umulhi(rk, a.div_mul) >> a.div_shift) : (rk >> a.div_shift);
   const unsigned tok = rk - bh * (unsigned)a.n_new;
 
   const uint8_t* rowp = tile + row * (2 * D);
@@ -444,7 +444,7 @@ __device__ __forceinline__ void quantize_half_row(const QuantArgs& a, const Pair
       rec[part] = group_codes<BITS, Q>(x + Q * part, mn[part], mx[part], zf[part]);
   }
   if (!valid) return;
-  const unsigned bh = rk / (unsigned)a.n_new;
+  const unsigned bh = a.div_mul ? (__umulhi(rk, a.div_mul) >> a.div_shift) : (rk >> a.div_shift);
   const unsigned tok = rk - bh * (unsigned)a.n_new;
   const size_t dst_tok = (size_t)bh * a.cap + a.first + tok;
   // codes: channels [32 HF, 32 HF + 32) and [64 + 32 HF, ...) -> bytes

@@ -25,3 +25,19 @@ def test_division_step_matches_ieee_quotient():
         out = subprocess.run([exe, "-40", "20", "2000"], capture_output=True, text=True, timeout=300)
     assert out.returncode == 0, out.stdout + out.stderr
     assert "mismatches 0" in out.stdout
+
+
+@pytest.mark.skipif(shutil.which("g++") is None, reason="needs g++")
+def test_row_divisor_matches_integer_division():
+    """The quantize-append kernels find a row's (batch, head) as r / n_new by
+    a multiply-high and a shift (the host picks both once per call); the
+    quotient must equal the integer division for every row index below 2^31
+    (the host refuses larger launches)."""
+    cuda_inc = os.path.join(os.environ.get("CUDA_HOME", "/usr/local/cuda"), "include")
+    with tempfile.TemporaryDirectory() as tmp:
+        exe = os.path.join(tmp, "row_divisor_check")
+        subprocess.check_call(["g++", "-O2", "-std=c++17", "-I", cuda_inc, "-o", exe,
+                               os.path.join(HERE, "row_divisor_check.cpp")])
+        out = subprocess.run([exe], capture_output=True, text=True, timeout=300)
+    assert out.returncode == 0, out.stdout + out.stderr
+    assert "bad 0" in out.stdout
