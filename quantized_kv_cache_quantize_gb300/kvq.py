@@ -5,6 +5,7 @@ the first call raises."""
 from __future__ import annotations
 
 import ctypes
+import functools
 import math
 import os
 
@@ -99,6 +100,23 @@ def lib() -> ctypes.CDLL:
             f.argtypes = args
         _lib = h
     return _lib
+
+
+def _nvtx(name: str):
+    """Mark each call of the decorated entry point as an NVTX range (for
+    Nsight timelines and ncu --nvtx filters); host-side only."""
+    def deco(fn):
+        @functools.wraps(fn)
+        def wrapped(*args, **kwargs):
+            if not torch.cuda.is_available():
+                return fn(*args, **kwargs)
+            torch.cuda.nvtx.range_push(name)
+            try:
+                return fn(*args, **kwargs)
+            finally:
+                torch.cuda.nvtx.range_pop()
+        return wrapped
+    return deco
 
 
 def status_string(status: int) -> str:
@@ -197,6 +215,7 @@ class KVCache:
         return int(lib().kvq_workspace_bytes(ctypes.byref(self.struct), n_q, n_r))
 
 
+@_nvtx("kvq_quantize_append")
 def quantize_append(cache: KVCache, k_new: torch.Tensor, v_new: torch.Tensor, stream=None):
     """kvq_quantize_append: k_new/v_new [B, H, n_new, d] bf16 on the device."""
     _bf16_dev(k_new, "k_new")
@@ -208,6 +227,7 @@ def quantize_append(cache: KVCache, k_new: torch.Tensor, v_new: torch.Tensor, st
                                      n_new, _stream(stream)), "kvq_quantize_append")
 
 
+@_nvtx("kvq_attention_corrected")
 def attention_corrected(cache: KVCache, q, k_cur, v_cur, scale: float | None = None,
                         corr: int = CORR_TAYLOR, out=None, with_mass: bool = False,
                         workspace=None, stream=None, flags: int = 0):
@@ -235,6 +255,7 @@ def attention_corrected(cache: KVCache, q, k_cur, v_cur, scale: float | None = N
     return (out, ps, pr) if with_mass else out
 
 
+@_nvtx("kvq_attention_corrected_noalloc")
 def attention_corrected_noalloc(cache: KVCache, q, k_cur, v_cur, scale: float | None = None,
                                 corr: int = CORR_TAYLOR, out=None, with_mass: bool = False,
                                 stream=None, flags: int = 0):
@@ -260,6 +281,7 @@ def attention_corrected_noalloc(cache: KVCache, q, k_cur, v_cur, scale: float | 
     return (out, ps, pr) if with_mass else out
 
 
+@_nvtx("kvq_attention_mass")
 def attention_mass(cache: KVCache, q, k_cur, scale: float | None = None,
                    corr: int = CORR_TAYLOR, workspace=None, stream=None, flags: int = 0):
     """kvq_attention_mass: returns (p_s, p_r), each [B, H, n_q] fp32."""
@@ -279,6 +301,7 @@ def attention_mass(cache: KVCache, q, k_cur, scale: float | None = None,
     return ps, pr
 
 
+@_nvtx("kvq_rotate")
 def rotate(x: torch.Tensor, signs, out_dtype=torch.float32, stream=None) -> torch.Tensor:
     """kvq_rotate: x [..., d] bf16 -> H x in fp32 (the values the quantizer
     sees) or fp16 (the attention kernel's tensor-core operands)."""
