@@ -8,8 +8,9 @@ namespace {
 
 // ---- per-channel keys: zero points and correction per query row and tile ----
 //
-// A per-channel key tile holds code * D_c; what its scores still need is the
-// zero-point term scale * sum_c q'_c (-z_c D_c) minus the correction, and with
+// A per-channel key tile holds (code - o) * D_c (o the key code offset); what
+// its scores still need is the zero-point term scale * sum_c q'_c (o - z_c)
+// D_c minus the correction, and with
 // per-channel steps both depend on the key only through its block: the
 // correction is b = sum_c a_c^2 / 6 (Taylor; = scale^2 / 24 sum_c q'_c^2 D_c^2)
 // or sum_c log(sinh a_c / a_c) (exact), a_c = scale/2 |q'_c| D_c, 0 without.
@@ -27,6 +28,7 @@ struct KchArgs {
   float scale;
   int corr;
   int* status;            // device status word (the tensor-core form's bounded waits)
+  float code_offset;      // key tiles hold (code - code_offset) * D_c
 };
 constexpr int kKchRows = 64;
 constexpr int kKchCols = 32;
@@ -36,7 +38,7 @@ constexpr int kKchPad = 4;   // shared-memory row padding (floats)
 template <int D>
 __global__ void __launch_bounds__(kKchThreads) kch_bias_kernel(const KchArgs a) {
   __shared__ __align__(16) float qs[32][kKchRows + kKchPad];   // q'_c of the rows
-  __shared__ __align__(16) float wz[32][kKchCols + kKchPad];   // -z_c D_c of the tiles
+  __shared__ __align__(16) float wz[32][kKchCols + kKchPad];   // (o - z_c) D_c of the tiles
   __shared__ __align__(16) float wd[32][kKchCols + kKchPad];   // scale/2 D_c of the tiles
   const int tid = threadIdx.x;
   const int ty = tid / (kKchCols / 4), tx = tid % (kKchCols / 4);
@@ -80,7 +82,7 @@ __global__ void __launch_bounds__(kKchThreads) kch_bias_kernel(const KchArgs a) 
       }
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
-        wz[8 * part + e][tt] = -bf16_hi(w[e]) * bf16_lo(w[e]);   // exact: integer z, 8-bit step
+        wz[8 * part + e][tt] = (a.code_offset - bf16_hi(w[e])) * bf16_lo(w[e]);   // exact: integer, 8-bit step
         wd[8 * part + e][tt] = 0.5f * a.scale * bf16_lo(w[e]);
       }
     }
@@ -127,7 +129,7 @@ __global__ void __launch_bounds__(kKchThreads) kch_bias_kernel(const KchArgs a) 
 // channels each,
 //   part 0: q_hi . v_hi     part 1: q_hi . v_lo     part 2: q_lo . v_hi (precise)
 //   part 3: (q'^2 2^-6) . (u 2^6)                   (Taylor)
-// with v = scale log2(e) (-z_c D_c) split into FP16 high and low parts (the
+// with v = scale log2(e) (o - z_c) D_c split into FP16 high and low parts (the
 // products exact in the fp32 accumulator) and u = -log2(e) (scale/2)^2 D_c^2
 // / 6.  One CTA: 128 query rows x up to kKgN cached tiles (MMA N), K
 // streamed through shared memory 64 channels at a time.
@@ -226,7 +228,7 @@ __global__ void __launch_bounds__(kKgThreads) kch_gemm_kernel(const KchArgs a) {
           if (part == 3) {
             f[e] = uc * dl * dl;
           } else {
-            const float vv = sl2 * (-bf16_hi(w[e]) * dl);
+            const float vv = sl2 * ((a.code_offset - bf16_hi(w[e])) * dl);
             const float vh = __half2float(__float2half_rn(vv));
             f[e] = part == 1 ? vv - vh : vh;
           }
@@ -279,7 +281,7 @@ __global__ void __launch_bounds__(kKgThreads) kch_gemm_kernel(const KchArgs a) {
 }
 
 // the pre-pass of one launch: the table of zero-point term minus correction
-template <int D>
+template <int D, int BITS>
 kvq_status launch_kch_table(const AttnLaunch& a, cudaStream_t stream) {
   if (a.kch_c == nullptr || a.n_ct <= 0 || a.n_q <= 0) return KVQ_OK;
   KchArgs k;
@@ -294,6 +296,7 @@ kvq_status launch_kch_table(const AttnLaunch& a, cudaStream_t stream) {
   k.scale = a.scale;
   k.corr = a.corr;
   k.status = a.status;
+  k.code_offset = (float)key_code_offset<BITS>();
   if (a.corr == KVQ_CORR_EXACT) {
     // log(sinh a / a) per channel: the CUDA-core form
     const dim3 kg((a.n_q + kKchRows - 1) / kKchRows, (a.n_ct + kKchCols - 1) / kKchCols, a.bh);
@@ -312,7 +315,7 @@ kvq_status launch_kch_table(const AttnLaunch& a, cudaStream_t stream) {
 
 template <int D, int BITS, int GROUP>
 kvq_status launch_mode_kch(const AttnLaunch& a, cudaStream_t stream) {
-  const kvq_status st = launch_kch_table<D>(a, stream);
+  const kvq_status st = launch_kch_table<D, BITS>(a, stream);
   if (st != KVQ_OK) return st;
   if (a.precise_query) return launch_t<D, BITS, GROUP, 1, true, false, true>(a, stream);
   return launch_t<D, BITS, GROUP, 2, false, false, true>(a, stream);

@@ -25,10 +25,11 @@
 // Hand-offs are mbarriers (two K/V stages, S ready, P ready, stage free);
 // every wait is bounded by a time limit.
 //
-// Numerics.  Cached scores: the K tile holds code * D, exact in FP16 for INT2
-// (<= 10 significant bits); two rank-G terms enter through one 16-column
-// extension tile contracted on the tensor core: the keys' zero points
-// (sum_g (sum_{c in g} q'_c) * (-z_g D_g), three columns per group, FP16
+// Numerics.  Cached scores: the K tile holds code * D (INT2, <= 10
+// significant bits) or (code - 8) * D (INT4, <= 11), exact in FP16; two rank-G
+// terms enter through one 16-column extension tile contracted on the tensor
+// core: the keys' zero points (sum_g (sum_{c in g} q'_c) * (o - z_g) D_g,
+// o the code offset, three columns per group, FP16
 // high/low splits, so the products carry ~2^-21 relative error) and, with the
 // correction, the Jensen bias -(scale/24) sum_g ||q'_g||^2 D_g^2 (one column
 // per group, ~2^-11 relative error on a term that is a small fraction of the
@@ -252,9 +253,16 @@ __device__ __forceinline__ uint32_t code_pair_f16(uint32_t w, int k) {
   return pair_magic<2>(k) == 4 ? ((t & 0x03000300u) | 0x44004400u) : ((t & 0x00C000C0u) | 0x4C004C00u);
 }
 
+// Code offset of the key tiles: an INT4 key tile holds (code - 8) * D, whose
+// magnitude needs at most 3 significant bits times the 8 of the BF16 step (11
+// bits: exact in FP16, where code * D can need 12); the zero-point term
+// carries (8 - z) * D instead of -z * D.  INT2 codes need no offset.
+template <int BITS>
+__device__ __forceinline__ constexpr int key_code_offset() { return BITS == 4 ? 8 : 0; }
+
 // Dequantize one packed key row into row r of a swizzled FP16 tile.
-// ZERO = false (keys): code * D = (magic + code) D - magic D in one FMA,
-// exact for INT2.  ZERO = true (values): (code - z) * D, the integer
+// ZERO = false (keys): (code - o) * D = (magic + code) D - (magic + o) D in
+// one FMA, o the key code offset, exact.  ZERO = true (values): (code - z) * D, the integer
 // difference exact, one rounding of the product.
 template <int D, int BITS, int GROUP, bool ZERO>
 __device__ __forceinline__ void dequant_row(const uint32_t (&words)[D * BITS / 32],
@@ -270,7 +278,7 @@ __device__ __forceinline__ void dequant_row(const uint32_t (&words)[D * BITS / 3
       const int k = BITS == 2 ? 4 * (c & 1) + i : i;
       const float mg = (float)pair_magic<BITS>(k);
       const __half2 k2 = ZERO ? __float2half2_rn(mg + bf16_hi(sz[g]))
-                              : __float2half2_rn(-mg * bf16_lo(sz[g]));
+                              : __float2half2_rn(-(mg + (float)key_code_offset<BITS>()) * bf16_lo(sz[g]));
       const uint32_t v = BITS == 2 ? code_pair_f16<2>(words[c >> 1], k) : code_pair_f16<4>(words[c], k);
       const __half2 res = ZERO ? __hmul2(__hsub2(as_h2(v), k2), d2) : __hfma2(as_h2(v), d2, k2);
       out[i] = as_u32(res);
@@ -281,10 +289,11 @@ __device__ __forceinline__ void dequant_row(const uint32_t (&words)[D * BITS / 3
 }
 
 // Per-channel keys: one packed key row into row r of a swizzled FP16 tile as
-// code * D_c = (magic + code) D_c - magic D_c in one FMA, exact for INT2 (the
-// zero-point term goes to the per-(row, tile) pre-pass): kd holds the block's
-// steps D_c, kmd the constants -magic D_c (FP16, one per channel; magic as
-// code_pair_f16 places the pair)
+// (code - o) * D_c = (magic + code) D_c - (magic + o) D_c in one FMA, o the
+// key code offset, exact (the zero-point term goes to the per-(row, tile)
+// pre-pass): kd holds the block's steps D_c, kmd the constants
+// -(magic + o) D_c (FP16, one per channel; magic as code_pair_f16 places the
+// pair)
 template <int D, int BITS>
 __device__ __forceinline__ void dequant_row_kch(const uint32_t (&words)[D * BITS / 32],
                                                 const uint8_t* kd, const uint8_t* kmd,
@@ -1065,7 +1074,7 @@ __global__ void __launch_bounds__(Cfg<D, NQ, PRECISE, EXACT, KCH>::kThreads, 1)
           const int k = BITS == 2 ? (r & 15) >> 1 : 0;
           reinterpret_cast<__half*>(st + C::kKch)[r] = __float2half_rn(bf16_lo(kmeta));
           reinterpret_cast<__half*>(st + C::kKch + 256)[r] =
-              __float2half_rn(-(float)pair_magic<BITS>(k) * bf16_lo(kmeta));
+              __float2half_rn(-(float)(pair_magic<BITS>(k) + key_code_offset<BITS>()) * bf16_lo(kmeta));
         }
         ptx::mbar_arrive(BAR(kBarKch + s));
         if (!wait_bar(BAR(kBarKch + s), (j >> 1) & 1, lim, abort, p.status)) break;
@@ -1085,7 +1094,7 @@ __global__ void __launch_bounds__(Cfg<D, NQ, PRECISE, EXACT, KCH>::kThreads, 1)
           float hi, lo;
           const int zc = PRECISE ? 3 * g : G + 3 * g;
           float(&zt)[16] = PRECISE ? cz : cx;
-          split_h(-bf16_hi(ksz[g]) * dl * kZeroKeyScale, hi, lo);
+          split_h(((float)key_code_offset<BITS>() - bf16_hi(ksz[g])) * dl * kZeroKeyScale, hi, lo);
           zt[zc] = hi; zt[zc + 1] = lo; zt[zc + 2] = hi;
           if (PRECISE) {
             split_h(dl * dl * kBiasKeyScale, hi, lo);

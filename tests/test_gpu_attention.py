@@ -291,3 +291,34 @@ def test_cache_checkpoint_roundtrip(key_mode):
     with pytest.raises(kvq.KVQError):          # partial newest chunk: only whole chunks follow
         kvq.quantize_append(restored, nxt_k, nxt_v)
     assert (restored.len, restored.head_slot) == state
+
+
+@pytest.mark.parametrize("d,group", [(64, 32), (128, 64)])
+@pytest.mark.parametrize("corr,key_mode", [(kvq.CORR_TAYLOR, kvq.KEYS_PER_TOKEN),
+                                           (kvq.CORR_EXACT, kvq.KEYS_PER_TOKEN),
+                                           (kvq.CORR_TAYLOR, kvq.KEYS_PER_CHANNEL)])
+def test_int4_extreme_outliers(d, group, corr, key_mode):
+    """INT4 keys with outliers at 30x (scores ~100): the key tiles hold
+    (code - 8) * D, exact in FP16 (code * D would need 12 significant bits
+    and moved P_S by ~4e-3 here); every row against the oracle with the
+    precise-query split."""
+    w = synth.Workload("int4big", heads=2, head_dim=d, chunk_tokens=160, n_chunks=3, bits=4,
+                       group=group, n_outliers_fixed=4, outlier_scale=30.0, offset_std=1.0)
+    n_q, n_s, n_r = 200, 450, 100
+    x = synth.inputs(w, seed=4, n_q=n_q, n_s=n_s, n_r=n_r)
+    x = dict(x, q=(x["q"].float() * 1.5).bfloat16().contiguous())
+    s = synth.hadamard_signs(d, seed=9)
+    if key_mode == kvq.KEYS_PER_CHANNEL:
+        from tests.gpu_common import build_cache_kch, oracle_head_kch
+        cache, ref_fn = build_cache_kch(w, x, s, n_s=n_s), oracle_head_kch
+    else:
+        cache, ref_fn = build_cache(w, x, s, n_s=n_s), oracle_head
+    out, ps, pr = kvq.attention_corrected(cache, x["q"].cuda(), x["k_cur"].cuda(),
+                                          x["v_cur"].cuda(), corr=corr, with_mass=True,
+                                          flags=kvq.FLAG_PRECISE_QUERY)
+    torch.cuda.synchronize()
+    assert kvq.last_device_status() == 0
+    for h in range(w.heads):
+        o_ref, ps_ref, pr_ref = ref_fn(w, x, s, 0, h, np.arange(n_q), corr, n_s=n_s)
+        assert_close(out[0, h].float().cpu().numpy(), o_ref, ps[0, h].cpu().numpy(), ps_ref,
+                     pr[0, h].cpu().numpy(), pr_ref, what=f"int4 big d{d} g{group} h{h}")
