@@ -182,3 +182,17 @@ def test_noalloc_rejects_problems_beyond_its_scratch(lib):
                                              None, None)
     assert st == kvq.KVQ_ERR_TOO_LARGE
     assert "scratch" in kvq.status_string(st)
+
+
+def test_workspace_bytes_per_channel_keys(lib):
+    """Per-channel keys add one fp32 per query row and cached key block (the
+    blocks of every chunk slot: n_chunks x ceil(chunk / 128)) to the
+    workspace, rounded to 256 bytes; nothing else changes."""
+    for chunk, n_chunks, n_q, n_r in ((300, 4, 100, 10), (4680, 4, 4680, 4680), (1, 3, 7, 1)):
+        tok = _cache(chunk_tokens=chunk, n_chunks=n_chunks)
+        ch = _cache(chunk_tokens=chunk, n_chunks=n_chunks, key_mode=kvq.KEYS_PER_CHANNEL)
+        w_tok = lib.kvq_workspace_bytes(ctypes.byref(tok), n_q, n_r)
+        w_ch = lib.kvq_workspace_bytes(ctypes.byref(ch), n_q, n_r)
+        tiles = n_chunks * -(-chunk // 128)
+        table = -(-(tiles * 2 * n_q * 4) // 256) * 256          # 2 = batch x heads of _cache
+        assert w_ch - w_tok == table, (chunk, n_chunks, w_ch, w_tok, table)
