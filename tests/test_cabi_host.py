@@ -4,6 +4,9 @@ anything."""
 import ctypes
 import os
 import re
+import shutil
+import subprocess
+import tempfile
 
 import numpy as np
 import pytest
@@ -196,3 +199,20 @@ def test_workspace_bytes_per_channel_keys(lib):
         tiles = n_chunks * -(-chunk // 128)
         table = -(-(tiles * 2 * n_q * 4) // 256) * 256          # 2 = batch x heads of _cache
         assert w_ch - w_tok == table, (chunk, n_chunks, w_ch, w_tok, table)
+
+
+@pytest.mark.skipif(shutil.which("gcc") is None, reason="needs gcc")
+def test_plain_c_caller():
+    """include/kvq.h is a C header: a C11 program compiles against it, links
+    libkvq.so and gets the same sizes and host-side errors."""
+    here = os.path.dirname(os.path.abspath(__file__))
+    root = os.path.dirname(here)
+    pkg = os.path.join(root, "quantized_kv_cache_quantize_gb300")
+    with tempfile.TemporaryDirectory() as tmp:
+        exe = os.path.join(tmp, "c_abi_check")
+        subprocess.check_call(["gcc", "-std=c11", "-Wall", "-Werror", "-I", os.path.join(root, "include"),
+                               "-o", exe, os.path.join(here, "c_abi_check.c"), "-L", pkg, "-lkvq",
+                               "-Wl,-rpath," + pkg])
+        out = subprocess.run([exe], capture_output=True, text=True, timeout=120)
+    assert out.returncode == 0, out.stdout + out.stderr
+    assert out.stdout.strip().endswith("ok")
