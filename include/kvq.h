@@ -242,7 +242,8 @@ kvq_status kvq_attention_mass(const kvq_cache *cache, const uint16_t *q,
  * x' = H x per row of x [rows][d] BF16 device, written as fp32 [rows][d]
  * (out_f32) -- exactly the fp32 values kvq_quantize_append quantizes -- or
  * rounded to FP16 (out_f16) -- exactly the tensor-core operands the
- * attention kernels read for q and the current chunk.  Exactly one of
+ * attention kernels read for q and the current chunk's values (the current
+ * keys enter unrotated, in BF16).  Exactly one of
  * out_f32 / out_f16 must be non-NULL.  d in {64, 128}.
  */
 kvq_status kvq_rotate(const uint16_t *x, int64_t rows, int32_t d,
