@@ -5,6 +5,7 @@ keys take attention mass from the current chunk; the correction gives it
 back).  INT4 g64 and INT2 g32 run on the same seeds.
 
 Run on a GPU:  python tests/report_accuracy.py [--heads 3] [--rows 512]
+               [--corrs none,taylor,exact] [--keys token|channel]
 
 For every workload, sampled heads and query rows:
   err_O   max |O_gpu - O_oracle| / max |O_oracle|           (same quantized cache)
@@ -29,7 +30,10 @@ if ROOT not in sys.path:
 
 from oracle import kvq_oracle as O  # noqa: E402
 from quantized_kv_cache_quantize_gb300 import kvq, synth  # noqa: E402
-from tests.gpu_common import build_cache, oracle_head  # noqa: E402
+from tests.gpu_common import (build_cache, build_cache_kch, oracle_head,  # noqa: E402
+                              oracle_head_kch)
+
+CORRS = {"none": kvq.CORR_NONE, "taylor": kvq.CORR_TAYLOR, "exact": kvq.CORR_EXACT}
 
 
 def unquantized_head(w, x, signs, h, rows):
@@ -43,14 +47,16 @@ def unquantized_head(w, x, signs, h, rows):
                              signs, w.scale, w.group, O.CORR_NONE)
 
 
-def report(name, n_heads, n_rows, flags):
+def report(name, n_heads, n_rows, flags, corrs, keys):
     w = synth.WORKLOADS[name]
     x = synth.inputs(w)
     s = synth.hadamard_signs(w.head_dim)
-    cache = build_cache(w, x, s)
+    channel = keys == "channel"
+    cache = (build_cache_kch if channel else build_cache)(w, x, s)
+    ref_head = oracle_head_kch if channel else oracle_head
     q, kc, vc = x["q"].cuda(), x["k_cur"].cuda(), x["v_cur"].cuda()
     gpu = {}
-    for corr in (kvq.CORR_NONE, kvq.CORR_TAYLOR):
+    for corr in corrs:
         out, ps, pr = kvq.attention_corrected(cache, q, kc, vc, corr=corr, with_mass=True, flags=flags)
         torch.cuda.synchronize()
         assert kvq.last_device_status() == 0
@@ -65,7 +71,7 @@ def report(name, n_heads, n_rows, flags):
         _, ps_u, _ = unquantized_head(w, x, s, h, rows)
         ps_exact.append(ps_u)
         for corr in gpu:
-            o_ref, ps_ref, _ = oracle_head(w, x, s, 0, h, rows, corr)
+            o_ref, ps_ref, _ = ref_head(w, x, s, 0, h, rows, corr)
             o_g, ps_g = gpu[corr][0][0, h][rows], gpu[corr][1][0, h][rows]
             a = acc[corr]
             a["err_o"] = max(a["err_o"], float(np.abs(o_g - o_ref).max() / np.abs(o_ref).max()))
@@ -76,7 +82,8 @@ def report(name, n_heads, n_rows, flags):
     for corr, a in acc.items():
         p_gpu = float(np.mean(np.concatenate(a["ps_gpu"])))
         p_ora = float(np.mean(np.concatenate(a["ps_ora"])))
-        lines.append(f"| {name} | INT{w.bits} g{w.group} | {'taylor' if corr else 'none'} | "
+        cname = {v: k for k, v in CORRS.items()}[corr]
+        lines.append(f"| {name} | INT{w.bits} g{w.group} {keys} | {cname} | "
                      f"{a['err_o']:.2e} | {a['err_ps']:.2e} | {p_gpu:.5f} | {p_ora:.5f} | "
                      f"{p_exact:.5f} | {p_gpu - p_exact:+.5f} |")
     return lines
@@ -87,14 +94,19 @@ def main(argv=None):
     ap.add_argument("--heads", type=int, default=3)
     ap.add_argument("--rows", type=int, default=512)
     ap.add_argument("--workloads", default="w4_int2,w4_int4,w8_int2,hires_t3")
+    ap.add_argument("--corrs", default="none,taylor",
+                    help="comma-separated: none, taylor, exact (the oracle's exact term "
+                         "is slow on long windows: fewer rows)")
+    ap.add_argument("--keys", choices=["token", "channel"], default="token")
     args = ap.parse_args(argv)
+    corrs = [CORRS[c] for c in args.corrs.split(",")]
     print(f"sampled heads per workload: {args.heads}, query rows per head: {args.rows}")
     print("| workload | cache | correction | err_O | err_PS | P_S gpu | P_S oracle | "
           "P_S unquantized | shift (gpu - unquantized) |")
     print("|---|---|---|---|---|---|---|---|---|")
     for name in args.workloads.split(","):
         flags = kvq.FLAG_PRECISE_QUERY if name == "hires_t3" else 0
-        for line in report(name, args.heads, args.rows, flags):
+        for line in report(name, args.heads, args.rows, flags, corrs, args.keys):
             print(line, flush=True)
 
 
