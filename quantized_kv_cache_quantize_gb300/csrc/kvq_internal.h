@@ -151,9 +151,6 @@ inline int cached_tiles(int key_mode, int n_s, int chunk, int bpc) {
   return full * bpc + (n_s - full * chunk + 127) / 128;
 }
 
-// Key-range split of a launch whose grid (bh * query tiles of rows_per_cta)
-// does not fill the GPU: enough ranges for about one wave of CTAs, each at
-// least two key tiles of 128, at most 16.  1 when the grid is full.
 // Key-range split of the attention grid.  One attention CTA fills an SM
 // (its shared memory allows no second one), so a launch of n CTAs runs in
 // ceil(n / sms) waves.  Splitting every (head, query block) into ranges of
