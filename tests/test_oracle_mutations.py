@@ -118,6 +118,84 @@ def _chunk_blocks_whole_chunk(n_tokens, block=O.KEY_BLOCK):
     return [(0, n_tokens)]
 
 
+_real_log_sinhc = O.log_sinhc
+
+
+def _exact_no_half(q_rot, delta, scale, group):
+    # a_c without the factor 1/2 (noise half-width taken as the whole step)
+    q = np.abs(np.asarray(q_rot, dtype=np.float64))
+    dl = np.asarray(delta, dtype=np.float64)
+    out = np.zeros((q.shape[0], dl.shape[0]))
+    for c in range(q.shape[1]):
+        out += _real_log_sinhc(scale * q[:, c][:, None] * dl[:, c // group][None, :])
+    return out
+
+
+def _exact_group_norms(q_rot, delta, scale, group):
+    # one uniform term per group with the group's query norm, instead of one
+    # per channel
+    n = np.sqrt(O.group_sq_norms(q_rot, group))
+    dl = np.asarray(delta, dtype=np.float64)
+    out = np.zeros((n.shape[0], dl.shape[0]))
+    for g in range(n.shape[1]):
+        out += _real_log_sinhc(0.5 * scale * n[:, g][:, None] * dl[:, g][None, :])
+    return out
+
+
+def _log_sinh_without_division(a):
+    a = np.abs(np.asarray(a, dtype=np.float64))
+    return np.log(np.sinh(np.maximum(a, 1e-300)))
+
+
+def _bf16_truncate(x):
+    a = np.ascontiguousarray(np.asarray(x, dtype=np.float32))
+    return (a.view(np.uint32) & np.uint32(0xFFFF0000)).view(np.float32).reshape(a.shape)
+
+
+def _dequantize_plus_zero(codes, delta, zero, group):
+    c = np.asarray(codes, dtype=np.float64)
+    lead, d = c.shape[:-1], c.shape[-1]
+    cg = c.reshape(*lead, d // group, group)
+    out = (cg + np.asarray(zero, np.float64)[..., None]) * np.asarray(delta, np.float64)[..., None]
+    return out.reshape(*lead, d)
+
+
+def _rotation_signs_on_output(signs):
+    # diag(signs) * H instead of H * diag(signs)
+    s = np.asarray(signs, dtype=np.float64)
+    return s[:, None] * O.sylvester_hadamard(s.shape[0]) / np.sqrt(s.shape[0])
+
+
+_real_token_steps = O.key_channel_token_steps
+
+
+def _token_steps_first_block(values, n_tokens, block=O.KEY_BLOCK):
+    v = np.asarray(values)
+    return np.repeat(v[:1], n_tokens, axis=0)
+
+
+def _attention_masses_swapped(q, ks, vs, dk, kc, vc, signs, scale, group, corr=O.CORR_TAYLOR):
+    o, ps, pr = _real_attention(q, ks, vs, dk, kc, vc, signs, scale, group, corr)
+    return o, pr, ps
+
+
+def _attention_exact_uses_taylor(q, ks, vs, dk, kc, vc, signs, scale, group, corr=O.CORR_TAYLOR):
+    if corr == O.CORR_EXACT:
+        corr = O.CORR_TAYLOR
+    return _real_attention(q, ks, vs, dk, kc, vc, signs, scale, group, corr)
+
+
+_real_ring = O.ring_append
+
+
+def _ring_no_wrap(length, head_slot, n_new, chunk_tokens, n_chunks):
+    r = _real_ring(length, head_slot, n_new, chunk_tokens, n_chunks)
+    if r is None:
+        return None
+    start, new_len, nxt = r
+    return start, new_len, min(head_slot + 1, n_chunks - 1)
+
+
 MUTANTS = {
     "key_channels_per_token": ("quantize_key_channels", _key_channels_per_token),
     "key_blocks_whole_chunk": ("chunk_blocks", _chunk_blocks_whole_chunk),
@@ -132,6 +210,16 @@ MUTANTS = {
     "attention_drops_current": ("chunk_attention", _attention_drops_current),
     "attention_rotates_current_keys": ("chunk_attention", _attention_bias_on_current_too),
     "fwht_no_scale": ("rotate_fp32", _fwht_no_scale),
+    "exact_no_half": ("jensen_bias_exact", _exact_no_half),
+    "exact_group_norms": ("jensen_bias_exact", _exact_group_norms),
+    "log_sinh_without_division": ("log_sinhc", _log_sinh_without_division),
+    "bf16_truncate": ("bf16_round", _bf16_truncate),
+    "dequantize_plus_zero": ("dequantize", _dequantize_plus_zero),
+    "rotation_signs_on_output": ("rotation_matrix", _rotation_signs_on_output),
+    "key_steps_first_block": ("key_channel_token_steps", _token_steps_first_block),
+    "attention_masses_swapped": ("chunk_attention", _attention_masses_swapped),
+    "attention_exact_uses_taylor": ("chunk_attention", _attention_exact_uses_taylor),
+    "ring_no_wrap": ("ring_append", _ring_no_wrap),
 }
 
 
