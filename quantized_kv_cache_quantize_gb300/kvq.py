@@ -154,6 +154,53 @@ def _bf16_dev(t: torch.Tensor, name: str) -> torch.Tensor:
     return t
 
 
+def _check_bhnd(cache: "KVCache", t: torch.Tensor, name: str) -> int:
+    """The library reads [batch, heads, n, head_dim] rows of the cache's
+    geometry from a plain device pointer and cannot see the buffer's size, so
+    the tensor's shape is checked here, before its pointer is passed on.
+    Returns n."""
+    want = (cache.batch, cache.heads, cache.head_dim)
+    if t.dim() != 4 or (t.shape[0], t.shape[1], t.shape[3]) != want:
+        raise ValueError(f"{name} must have shape [{want[0]}, {want[1]}, n, {want[2]}] "
+                         f"(the cache's batch, heads and head_dim), got {list(t.shape)}")
+    return int(t.shape[2])
+
+
+def _check_device(cache: "KVCache", *tensors):
+    dev = cache.k_codes.device
+    for name, t in tensors:
+        if t is not None and t.device != dev:
+            raise ValueError(f"{name} is on {t.device}, the cache on {dev}")
+
+
+def _check_out(q: torch.Tensor, out: torch.Tensor):
+    if tuple(out.shape) != tuple(q.shape):
+        raise ValueError(f"out must have the shape of q {list(q.shape)}, got {list(out.shape)}")
+    _bf16_dev(out, "out")
+
+
+def _check_qkv(cache: "KVCache", q, k_cur, v_cur) -> tuple:
+    """Shapes, then dtype and device, of the attention inputs; returns
+    (n_q, n_r)."""
+    n_q = _check_bhnd(cache, q, "q")
+    n_r = _check_bhnd(cache, k_cur, "k_cur")
+    if v_cur is not None and tuple(v_cur.shape) != tuple(k_cur.shape):
+        raise ValueError(f"v_cur must have the shape of k_cur {list(k_cur.shape)}, "
+                         f"got {list(v_cur.shape)}")
+    _bf16_dev(q, "q")
+    _bf16_dev(k_cur, "k_cur")
+    if v_cur is not None:
+        _bf16_dev(v_cur, "v_cur")
+    _check_device(cache, ("q", q), ("k_cur", k_cur), ("v_cur", v_cur))
+    return n_q, n_r
+
+
+def _workspace_arg(workspace: torch.Tensor, device) -> tuple:
+    if not workspace.is_contiguous() or workspace.device != device:
+        raise ValueError(f"workspace must be a contiguous tensor on {device}")
+    return _ptr(workspace), workspace.numel() * workspace.element_size()
+
+
 class KVCache:
     """A quantized sliding-window KV cache in device memory (torch-allocated)
     and its ``kvq_cache`` descriptor."""
@@ -218,11 +265,12 @@ class KVCache:
 @_nvtx("kvq_quantize_append")
 def quantize_append(cache: KVCache, k_new: torch.Tensor, v_new: torch.Tensor, stream=None):
     """kvq_quantize_append: k_new/v_new [B, H, n_new, d] bf16 on the device."""
-    _bf16_dev(k_new, "k_new")
-    _bf16_dev(v_new, "v_new")
-    n_new = k_new.shape[-2] if k_new.dim() >= 2 else 0
+    n_new = _check_bhnd(cache, k_new, "k_new")
     if tuple(k_new.shape) != tuple(v_new.shape):
         raise ValueError("k_new and v_new shapes differ")
+    _bf16_dev(k_new, "k_new")
+    _bf16_dev(v_new, "v_new")
+    _check_device(cache, ("k_new", k_new), ("v_new", v_new))
     _check(lib().kvq_quantize_append(ctypes.byref(cache.struct), _ptr(k_new), _ptr(v_new),
                                      n_new, _stream(stream)), "kvq_quantize_append")
 
@@ -233,14 +281,13 @@ def attention_corrected(cache: KVCache, q, k_cur, v_cur, scale: float | None = N
                         workspace=None, stream=None, flags: int = 0):
     """kvq_attention_corrected.  q [B, H, n_q, d], k_cur/v_cur [B, H, n_r, d]
     bf16 on the device.  Returns out (and (p_s, p_r) when with_mass)."""
-    _bf16_dev(q, "q")
-    _bf16_dev(k_cur, "k_cur")
-    _bf16_dev(v_cur, "v_cur")
-    n_q, n_r = q.shape[-2], k_cur.shape[-2]
+    n_q, n_r = _check_qkv(cache, q, k_cur, v_cur)
     d = cache.head_dim
     scale = 1.0 / math.sqrt(d) if scale is None else scale
     if out is None:
         out = torch.empty_like(q)
+    _check_out(q, out)
+    _check_device(cache, ("out", out))
     ps = pr = None
     if with_mass:
         ps = torch.empty(q.shape[:-1], dtype=torch.float32, device=q.device)
@@ -248,9 +295,10 @@ def attention_corrected(cache: KVCache, q, k_cur, v_cur, scale: float | None = N
     ws_bytes = cache.workspace_bytes(n_q, n_r)
     if workspace is None:
         workspace = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=q.device)
+    ws_ptr, ws_size = _workspace_arg(workspace, q.device)
     _check(lib().kvq_attention_corrected(
         ctypes.byref(cache.struct), _ptr(q), _ptr(k_cur), _ptr(v_cur), n_q, n_r,
-        ctypes.c_float(scale), corr, flags, _ptr(workspace), workspace.numel(), _ptr(out),
+        ctypes.c_float(scale), corr, flags, ws_ptr, ws_size, _ptr(out),
         _ptr(ps), _ptr(pr), _stream(stream)), "kvq_attention_corrected")
     return (out, ps, pr) if with_mass else out
 
@@ -263,13 +311,12 @@ def attention_corrected_noalloc(cache: KVCache, q, k_cur, v_cur, scale: float | 
     library's built-in scratch buffer instead of a workspace (for callers
     that cannot allocate device memory when they call).  Outputs are still
     the caller's (allocated here by torch when not given)."""
-    _bf16_dev(q, "q")
-    _bf16_dev(k_cur, "k_cur")
-    _bf16_dev(v_cur, "v_cur")
-    n_q, n_r = q.shape[-2], k_cur.shape[-2]
+    n_q, n_r = _check_qkv(cache, q, k_cur, v_cur)
     scale = 1.0 / math.sqrt(cache.head_dim) if scale is None else scale
     if out is None:
         out = torch.empty_like(q)
+    _check_out(q, out)
+    _check_device(cache, ("out", out))
     ps = pr = None
     if with_mass:
         ps = torch.empty(q.shape[:-1], dtype=torch.float32, device=q.device)
@@ -285,18 +332,17 @@ def attention_corrected_noalloc(cache: KVCache, q, k_cur, v_cur, scale: float | 
 def attention_mass(cache: KVCache, q, k_cur, scale: float | None = None,
                    corr: int = CORR_TAYLOR, workspace=None, stream=None, flags: int = 0):
     """kvq_attention_mass: returns (p_s, p_r), each [B, H, n_q] fp32."""
-    _bf16_dev(q, "q")
-    _bf16_dev(k_cur, "k_cur")
-    n_q, n_r = q.shape[-2], k_cur.shape[-2]
+    n_q, n_r = _check_qkv(cache, q, k_cur, None)
     scale = 1.0 / math.sqrt(cache.head_dim) if scale is None else scale
     ps = torch.empty(q.shape[:-1], dtype=torch.float32, device=q.device)
     pr = torch.empty_like(ps)
     ws_bytes = cache.workspace_bytes(n_q, n_r)
     if workspace is None:
         workspace = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=q.device)
+    ws_ptr, ws_size = _workspace_arg(workspace, q.device)
     _check(lib().kvq_attention_mass(
         ctypes.byref(cache.struct), _ptr(q), _ptr(k_cur), n_q, n_r, ctypes.c_float(scale), corr,
-        flags, _ptr(workspace), workspace.numel(), _ptr(ps), _ptr(pr), _stream(stream)),
+        flags, ws_ptr, ws_size, _ptr(ps), _ptr(pr), _stream(stream)),
         "kvq_attention_mass")
     return ps, pr
 

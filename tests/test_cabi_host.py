@@ -216,3 +216,47 @@ def test_plain_c_caller():
         out = subprocess.run([exe], capture_output=True, text=True, timeout=120)
     assert out.returncode == 0, out.stdout + out.stderr
     assert out.stdout.strip().endswith("ok")
+
+
+def test_binding_checks_shapes_before_passing_pointers(lib):
+    """The library cannot see the size of a device buffer, so the binding
+    checks every tensor against the cache's batch, heads and head_dim before
+    it passes the pointer on; on the host (CPU tensors) a tensor of the right
+    shape gets as far as the device check, one of the wrong shape stops at
+    the shape check, and nothing reaches the library."""
+    import torch
+    cache = kvq.KVCache(1, 2, 128, 2, 32, 10, 3, np.ones(128), device="cpu")
+    bf = dict(dtype=torch.bfloat16)
+    good = torch.zeros(1, 2, 4, 128, **bf)
+    for bad in (torch.zeros(1, 3, 4, 128, **bf), torch.zeros(2, 2, 4, 128, **bf),
+                torch.zeros(1, 2, 4, 64, **bf), torch.zeros(2, 4, 128, **bf)):
+        with pytest.raises(ValueError, match="shape"):
+            kvq.quantize_append(cache, bad, bad)
+        with pytest.raises(ValueError, match="shape"):
+            kvq.attention_corrected(cache, bad, good, good)
+        with pytest.raises(ValueError, match="shape"):
+            kvq.attention_corrected(cache, good, bad, bad)
+        with pytest.raises(ValueError, match="shape"):
+            kvq.attention_corrected_noalloc(cache, bad, good, good)
+        with pytest.raises(ValueError, match="shape"):
+            kvq.attention_mass(cache, bad, good)
+    with pytest.raises(ValueError, match="v_cur"):
+        kvq.attention_corrected(cache, good, good, torch.zeros(1, 2, 5, 128, **bf))
+    with pytest.raises(ValueError, match="k_new and v_new"):
+        kvq.quantize_append(cache, good, torch.zeros(1, 2, 5, 128, **bf))
+    # right shapes: stopped by the dtype / device check instead
+    for call in (lambda: kvq.quantize_append(cache, good, good),
+                 lambda: kvq.attention_corrected(cache, good, good, good),
+                 lambda: kvq.attention_corrected_noalloc(cache, good, good, good),
+                 lambda: kvq.attention_mass(cache, good, good)):
+        with pytest.raises(ValueError, match="CUDA bfloat16"):
+            call()
+    assert cache.len == 0 and cache.head_slot == 0
+    with pytest.raises(ValueError, match="shape of q"):
+        kvq._check_out(good, torch.zeros(1, 2, 5, 128, **bf))
+    with pytest.raises(ValueError, match="CUDA bfloat16"):
+        kvq._check_out(good, torch.zeros(1, 2, 4, 128, **bf))
+    # the workspace size passed on is in bytes, whatever the element type
+    assert kvq._workspace_arg(torch.zeros(6, dtype=torch.float32), torch.device("cpu"))[1] == 24
+    with pytest.raises(ValueError, match="workspace"):
+        kvq._workspace_arg(torch.zeros(4, 4, dtype=torch.uint8).t(), torch.device("cpu"))
