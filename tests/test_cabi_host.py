@@ -260,3 +260,39 @@ def test_binding_checks_shapes_before_passing_pointers(lib):
     assert kvq._workspace_arg(torch.zeros(6, dtype=torch.float32), torch.device("cpu"))[1] == 24
     with pytest.raises(ValueError, match="workspace"):
         kvq._workspace_arg(torch.zeros(4, 4, dtype=torch.uint8).t(), torch.device("cpu"))
+
+
+def test_binding_mirrors_the_header():
+    """The Python binding's constants and its ctypes copy of kvq_cache agree
+    with include/kvq.h: enum values and #defines parsed from the header, and
+    every field's offset and the struct's size from a C compiler."""
+    src = open(os.path.join(ROOT, "include", "kvq.h")).read()
+    consts = dict((k, int(v)) for k, v in re.findall(r"\b(KVQ_[A-Z0-9_]+)\s*=\s*(\d+)", src))
+    consts.update((k, int(v)) for k, v in re.findall(r"#define\s+(KVQ_[A-Z0-9_]+)\s+(\d+)", src))
+    py = {"KVQ_CORR_NONE": kvq.CORR_NONE, "KVQ_CORR_TAYLOR": kvq.CORR_TAYLOR,
+          "KVQ_CORR_EXACT": kvq.CORR_EXACT, "KVQ_FLAG_PRECISE_QUERY": kvq.FLAG_PRECISE_QUERY,
+          "KVQ_FLAG_NO_KV_SPLIT": kvq.FLAG_NO_KV_SPLIT,
+          "KVQ_KEYS_PER_TOKEN": kvq.KEYS_PER_TOKEN, "KVQ_KEYS_PER_CHANNEL": kvq.KEYS_PER_CHANNEL,
+          "KVQ_KEY_BLOCK": kvq.KEY_BLOCK}
+    py.update((k, getattr(kvq, k)) for k in consts if k.startswith(("KVQ_OK", "KVQ_ERR_")))
+    assert set(py) == set(consts), set(py) ^ set(consts)
+    for k, v in consts.items():
+        assert py[k] == v, (k, py[k], v)
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("needs a C compiler")
+    fields = [f[0] for f in kvq.CacheStruct._fields_]
+    prog = ["#include <stddef.h>", "#include <stdio.h>", '#include "kvq.h"', "int main(void) {",
+            '  printf("%zu\\n", sizeof(kvq_cache));']
+    prog += [f'  printf("%zu\\n", offsetof(kvq_cache, {f}));' for f in fields]
+    prog += ["  return 0;", "}"]
+    with tempfile.TemporaryDirectory() as tmp:
+        c_path, exe = os.path.join(tmp, "layout.c"), os.path.join(tmp, "layout")
+        with open(c_path, "w") as f:
+            f.write("\n".join(prog) + "\n")
+        subprocess.check_call([cc, "-std=c11", "-I", os.path.join(ROOT, "include"), "-o", exe, c_path])
+        got = [int(v) for v in subprocess.run([exe], capture_output=True, text=True,
+                                              check=True).stdout.split()]
+    assert got[0] == ctypes.sizeof(kvq.CacheStruct)
+    for name, off in zip(fields, got[1:]):
+        assert getattr(kvq.CacheStruct, name).offset == off, name
