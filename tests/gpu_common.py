@@ -4,7 +4,6 @@ anything the CUDA path produced)."""
 from __future__ import annotations
 
 import numpy as np
-import torch
 
 from oracle import kvq_oracle as O
 from quantized_kv_cache_quantize_gb300 import kvq, synth

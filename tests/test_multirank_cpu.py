@@ -6,7 +6,6 @@ prints."""
 import os
 import socket
 
-import pytest
 import torch.multiprocessing as mp
 
 

@@ -7,7 +7,6 @@ second one runs over whatever the first left in the shared buffer -- must
 give what kvq_attention_corrected gives with a caller-allocated workspace,
 within the tolerances of the other attention tests.  Collected last, so a
 run that stops at its first failure has run everything else already."""
-import numpy as np
 import pytest
 import torch
 
