@@ -143,6 +143,21 @@ def max_over_ranks(value: float, world: int, device=None) -> float:
     return float(t.item())
 
 
+def check_world(gpus: int, env=None):
+    """--gpus N must match the number of ranks the launcher started (one
+    process per GPU: ``torchrun --nproc-per-node N bench.py --gpus N``); a
+    plain ``python bench.py`` is one rank.  A mismatch would time a different
+    number of replicas than the line reports, so it stops the run."""
+    env = os.environ if env is None else env
+    world = int(env.get("WORLD_SIZE", "1"))
+    if gpus != world:
+        sys.stderr.write(f"bench.py: --gpus {gpus} but {world} rank(s) were launched; run "
+                         f"`python -m torch.distributed.run --nproc-per-node {gpus} bench.py "
+                         f"--gpus {gpus}` (one process per GPU)\n")
+        raise SystemExit(2)
+    return world
+
+
 def run_gpu(args):
     import torch
     import torch.distributed as dist
@@ -483,6 +498,7 @@ def main(argv=None):
                     help="correction of the cached scores (default: the second-order Taylor "
                          "term; exact: log(sinh a / a) per channel)")
     args = ap.parse_args(argv)
+    check_world(args.gpus)
     args.warmup = max(3, args.warmup)   # at least 3 untimed warm-up steps
     args.corr = {v: k for k, v in CORR_NAMES.items()}[args.corr]
     args.key_mode = 1 if args.keys == "channel" else 0

@@ -20,6 +20,17 @@
  *   out) are recorded in a device status word read by
  *   kvq_last_device_status().
  * - Inputs must be finite.
+ * - FP16 operand range.  The attention's tensor-core operands are FP16, so
+ *   the call checks on the GPU, as it runs, that they stay finite:
+ *     rotated queries and current-chunk values |x'| < 65504 (with
+ *     KVQ_KEYS_PER_CHANNEL and KVQ_CORR_TAYLOR the rotated query |q'| < 2047,
+ *     which the correction pre-pass squares);
+ *     cached key step sizes D with (16 + o) D < 65504, o = 0 for INT2 and 8
+ *     for INT4 (INT2: D < 4094, INT4: D < 2729);
+ *     cached values (|z| + 2^bits - 1) D < 65504 per group.
+ *   A call that meets an operand outside these limits still runs to the end,
+ *   records KVQ_ERR_RANGE in the device status word (see
+ *   kvq_last_device_status) and its outputs are not valid.
  */
 #ifndef KVQ_H
 #define KVQ_H
@@ -39,7 +50,8 @@ typedef enum {
   KVQ_ERR_CUDA = 4,         /* a CUDA runtime/driver call failed            */
   KVQ_ERR_TIMEOUT = 5,      /* a kernel's bounded wait ran out              */
   KVQ_ERR_ALIGNMENT = 6,    /* a pointer is not 16-byte aligned             */
-  KVQ_ERR_TOO_LARGE = 7     /* needs more than the built-in scratch holds   */
+  KVQ_ERR_TOO_LARGE = 7,    /* needs more than the built-in scratch holds   */
+  KVQ_ERR_RANGE = 8         /* an operand left the FP16 range (see below)   */
 } kvq_status;
 
 /* Correction applied to cached-key scores before the softmax. */
@@ -214,7 +226,8 @@ size_t kvq_workspace_bytes(const kvq_cache *cache, int32_t n_q, int32_t n_r);
  * aligned; its contents are scratch (the rotated query as FP16 high and low
  * parts and the rotated current values in FP16: tensor-core operands; the
  * key-range split's partial results).
- * Values after rotation must stay within the FP16 range (|x| < 65504).  Requires cache->len + n_r >= 1 when
+ * The FP16 operand limits of the conventions above apply (KVQ_ERR_RANGE in
+ * the device status word when broken).  Requires cache->len + n_r >= 1 when
  * n_q > 0.  n_q == 0 is a no-op.
  */
 kvq_status kvq_attention_corrected(const kvq_cache *cache, const uint16_t *q,
@@ -251,9 +264,10 @@ kvq_status kvq_rotate(const uint16_t *x, int64_t rows, int32_t d,
                       uint16_t *out_f16, void *stream);
 
 /*
- * Synchronizes `stream`, then returns and clears the device status word
- * (KVQ_OK, or the first in-kernel error since the last call, e.g.
- * KVQ_ERR_TIMEOUT).  Returns KVQ_ERR_CUDA if the synchronization failed.
+ * Synchronizes `stream`, then returns and clears the device status word of
+ * the current device (KVQ_OK, or the first in-kernel error since the last
+ * call: KVQ_ERR_TIMEOUT or KVQ_ERR_RANGE).  Returns KVQ_ERR_CUDA if the
+ * synchronization failed.
  */
 kvq_status kvq_last_device_status(void *stream);
 
@@ -283,12 +297,19 @@ kvq_status kvq_selftest_wait_timeout(uint64_t limit_ns, void *stream);
  * Same arguments, meaning and results as kvq_attention_corrected, minus the
  * workspace.  The scratch space comes from one fixed device buffer of
  * KVQ_NOALLOC_SCRATCH_BYTES (32 MiB) inside the library; every device that
- * loads the library holds it until the process exits.  Problems that need
- * more (kvq_workspace_bytes(cache, n_q, n_r) > KVQ_NOALLOC_SCRATCH_BYTES)
- * return KVQ_ERR_TOO_LARGE before anything is launched.
- * - The first call on a device looks up the buffer's device address (once per
- *   device, with that device current); make that first call before any
- *   stream capture.
+ * loads the library holds it until the process exits.  The call is refused
+ * with KVQ_ERR_TOO_LARGE, before anything is launched, when the scratch of
+ * the unsplit launch for the cache's current window (the rotated query as
+ * FP16 high and low parts, the rotated current values, and with
+ * KVQ_KEYS_PER_CHANNEL one fp32 per query row and cached key block) exceeds
+ * KVQ_NOALLOC_SCRATCH_BYTES; when it fits, the key-range split (which needs
+ * room for partial results) takes the largest number of ranges whose
+ * scratch still fits, down to none.  The limit is therefore not
+ * kvq_workspace_bytes(), which sizes the split for a full window.
+ * - The first call on a device, and the first after the device's context
+ *   changed (after cudaDeviceReset, for instance), looks up the buffer's
+ *   device address in the current context (with that device current); make
+ *   those calls before any stream capture.
  * - All calls share the one buffer and it keeps the previous call's contents
  *   (nothing in it needs to start at zero: each call overwrites what it
  *   reads).  Calls whose kernels overlap on the GPU -- on different streams,

@@ -1,6 +1,7 @@
 // extern "C" entry points of libkvq: argument validation, the sliding-window
 // ring bookkeeping, workspace carving and kernel dispatch.  Every check here
 // runs on the host before anything is launched.
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <atomic>
@@ -212,6 +213,8 @@ kvq_status attention_common(const kvq_cache* cache, const uint16_t* q, const uin
   if (workspace_bytes < ws.bytes) return KVQ_ERR_INVALID_ARG;
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int* status = kvq::status_ptr();
+  if (status == nullptr) return KVQ_ERR_CUDA;
   // rotate Q (FP16 hi, and lo when precise) and V_cur (FP16) into the workspace
   kvq::RotateArgs ra{};
   ra.src[0] = q;
@@ -225,6 +228,13 @@ kvq_status attention_common(const kvq_cache* cache, const uint16_t* q, const uin
   for (int i = 0; i < 4; ++i) ra.sign_bits[i] = cache->sign_bits[i];
   ra.inv_sqrt_d = (float)(1.0 / std::sqrt((double)g.d));
   ra.out_f32 = 0;
+  // FP16 operand limits: every rotated value below 65504; with per-channel
+  // keys and the Taylor term the pre-pass squares the query (q'^2 / 64 in
+  // FP16): |q'| < 2047
+  ra.status = status;
+  ra.range_limit[0] = (g.key_mode == KVQ_KEYS_PER_CHANNEL && corr == KVQ_CORR_TAYLOR) ? 2047.0f
+                                                                                     : 65504.0f;
+  ra.range_limit[1] = 65504.0f;
   {
     ProfScope prof(1, s);
     if (kvq::launch_rotate(ra, g.d, s) != cudaSuccess) return KVQ_ERR_CUDA;
@@ -283,6 +293,8 @@ const char* kvq_status_string(kvq_status s) {
     case KVQ_ERR_ALIGNMENT: return "pointer not 16-byte aligned";
     case KVQ_ERR_TOO_LARGE:
       return "problem needs more scratch than kvq_attention_corrected_noalloc's built-in buffer";
+    case KVQ_ERR_RANGE:
+      return "an operand left the FP16 range of the tensor-core operands (results invalid)";
   }
   return "unknown status";
 }
@@ -469,6 +481,73 @@ kvq_status kvq_profile_end(double ms_total[3], int32_t launches[3]) {
 
 }  // extern "C"
 
+// ---- device addresses of the library's __device__ variables -----------------
+
+namespace {
+
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long*);
+
+// unique id of the calling thread's current context (false when there is
+// none yet or the driver does not offer the query)
+bool current_context_id(unsigned long long* id) {
+  static CtxGetCurrentFn get_current = nullptr;
+  static CtxGetIdFn get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 4000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<CtxGetCurrentFn>(f);
+    f = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<CtxGetIdFn>(f);
+  });
+  if (get_current == nullptr || get_id == nullptr) return false;
+  CUcontext ctx = nullptr;
+  if (get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return false;
+  return get_id(ctx, id) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+namespace kvq {
+
+cudaError_t device_symbol_address(const void* symbol, SymbolSlot& slot, void** out) {
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  unsigned long long id = 0;
+  const bool have_id = current_context_id(&id);
+  std::lock_guard<std::mutex> lock(slot.mu);
+  if (have_id && slot.ptr[dev] != nullptr && slot.ctx_id[dev] == id) {
+    *out = slot.ptr[dev];
+    return cudaSuccess;
+  }
+  void* p = nullptr;
+  e = cudaGetSymbolAddress(&p, symbol);
+  if (e != cudaSuccess) return e;
+  if (p == nullptr) return cudaErrorInvalidSymbol;
+  // the lookup itself may have created the context: take its id afterwards
+  // (without an id the address is not kept, and every call looks it up)
+  unsigned long long id_after = 0;
+  if (current_context_id(&id_after)) {
+    slot.ctx_id[dev] = id_after;
+    slot.ptr[dev] = p;
+  } else {
+    slot.ptr[dev] = nullptr;
+  }
+  *out = p;
+  return cudaSuccess;
+}
+
+}  // namespace kvq
+
 // ---- attention without a workspace argument ---------------------------------
 // Scratch of kvq_attention_corrected_noalloc: one fixed device buffer, present
 // on every device that loads the library until the process exits.  In host
@@ -478,24 +557,14 @@ static __device__ __align__(256) uint8_t g_noalloc_scratch[KVQ_NOALLOC_SCRATCH_B
 
 namespace {
 
-constexpr int kMaxDevices = 64;
-std::mutex g_noalloc_mutex;
-void* g_noalloc_ptr[kMaxDevices] = {nullptr};
+kvq::SymbolSlot g_noalloc_slot;
 
-// Device address of the scratch buffer on the current device, looked up once
-// per device (with that device current).
+// Device address of the scratch buffer in the current device's current
+// context (looked up with that device current, once per device and context).
 kvq_status noalloc_scratch(void** ptr) {
-  int dev = -1;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return KVQ_ERR_CUDA;
-  std::lock_guard<std::mutex> lock(g_noalloc_mutex);
-  if (g_noalloc_ptr[dev] == nullptr) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr)
-      return KVQ_ERR_CUDA;
-    g_noalloc_ptr[dev] = p;
-  }
-  *ptr = g_noalloc_ptr[dev];
-  return KVQ_OK;
+  return kvq::device_symbol_address(&g_noalloc_scratch, g_noalloc_slot, ptr) == cudaSuccess
+             ? KVQ_OK
+             : KVQ_ERR_CUDA;
 }
 
 }  // namespace

@@ -3,8 +3,6 @@
 // kernels are in kvq_attn_kernel.cuh; this unit instantiates the per-token
 // key modes with the Taylor correction or none, kvq_attn_exact.cu the exact
 // correction and kvq_attn_kch.cu the per-channel keys.
-#include <mutex>
-
 #include "kvq_attn_kernel.cuh"
 
 namespace kvq {
@@ -34,24 +32,16 @@ kvq_status launch_mode(const AttnLaunch& a, cudaStream_t stream) {
   return launch_t<D, BITS, GROUP, 2, false, false, false>(a, stream);
 }
 
-// device address of the status word on the current device (looked up once
-// per device)
-int* status_ptr() {
-  constexpr int kMaxDevices = 64;
-  static std::mutex mu;
-  static int* ptr[kMaxDevices] = {nullptr};
-  int dev = -1;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
-  std::lock_guard<std::mutex> lock(mu);
-  if (ptr[dev] == nullptr) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_attn_status) != cudaSuccess) return nullptr;
-    ptr[dev] = static_cast<int*>(p);
-  }
-  return ptr[dev];
-}
+SymbolSlot g_status_slot;
 
 }  // namespace
+
+// device address of the status word in the current device's current context
+int* status_ptr() {
+  void* p = nullptr;
+  if (device_symbol_address(&g_attn_status, g_status_slot, &p) != cudaSuccess) return nullptr;
+  return static_cast<int*>(p);
+}
 
 kvq_status launch_attention(const AttnLaunch& a_in, int d, int bits, int group, cudaStream_t stream) {
   AttnLaunch a = a_in;

@@ -29,6 +29,7 @@ struct KchArgs {
   int corr;
   int* status;            // device status word (the tensor-core form's bounded waits)
   float code_offset;      // key tiles hold (code - code_offset) * D_c
+  unsigned long long wait_limit_ns;   // limit of every bounded wait
 };
 constexpr int kKchRows = 64;
 constexpr int kKchCols = 32;
@@ -177,14 +178,18 @@ __global__ void __launch_bounds__(kKgThreads) kch_gemm_kernel(const KchArgs a) {
   // the chunks: (part, 64-channel block) for the parts this launch needs
   const int np = a.q_lo != nullptr ? 3 : 2;
   const int n_chunks = (np + (taylor ? 1 : 0)) * (D / 64);
+  int issued = 0;   // chunks whose MMAs were issued
   for (int ci = 0; ci < n_chunks; ++ci) {
     const int pi = ci / (D / 64), kc = ci - pi * (D / 64);
     const int part = pi < np ? pi : 3;
     const int b = ci & 1;
     uint8_t* ta = sm + b * kBuf;
     uint8_t* tb = ta + 128 * 128;
-    // buffer b was last read by the MMAs of chunk ci - 2
-    if (ci >= 2) wait_bar(bar0 + 8 * b, ((ci - 2) >> 1) & 1, 2000000000ull, abort, a.status);
+    // buffer b was last read by the MMAs of chunk ci - 2; if that wait ran
+    // out (or another thread's did), no further chunk is written or issued
+    bool free_ok = true;
+    if (ci >= 2) free_ok = wait_bar(bar0 + 8 * b, ((ci - 2) >> 1) & 1, a.wait_limit_ns, abort, a.status);
+    if (!__syncthreads_and(free_ok && !*abort)) break;
     // A: this thread's half of its row's channels [64 kc, 64 kc + 64)
 #pragma unroll
     for (int c4 = 0; c4 < 4; ++c4) {
@@ -250,18 +255,21 @@ __global__ void __launch_bounds__(kKgThreads) kch_gemm_kernel(const KchArgs a) {
                      (ci > 0 || s4 > 0) ? 1u : 0u);
       ptx::mma_commit(bar0 + 8 * b);
     }
+    issued = ci + 1;
   }
   // every MMA issued is complete (the last commit covers the earlier ones)
   // before the tensor memory is read or freed, also after a wait that ran out
-  {
-    const int last = n_chunks - 1;
+  if (issued > 0) {
+    const int last = issued - 1;
     int drained = 0;
-    wait_bar(bar0 + 8 * (last & 1), (last >> 1) & 1, 2000000000ull, &drained, a.status);
+    wait_bar(bar0 + 8 * (last & 1), (last >> 1) & 1, a.wait_limit_ns, &drained, a.status);
   }
   ptx::tc_fence_after();
   // the tensor-memory loads are warp-collective: every lane of warps 0-3
-  // (lanes 0-127: the rows) takes part, only the rows of the chunk store
-  if (warp < 4 && __all_sync(0xffffffffu, !*abort)) {
+  // (lanes 0-127: the rows) takes part, only the rows of the chunk store;
+  // nothing is read after an aborted chunk loop
+  const bool complete = __syncthreads_and(issued == n_chunks && !*abort);
+  if (warp < 4 && complete) {
     for (int c = 0; c < npad; c += 32) {
       uint32_t v[32];
       ptx::tmem_ld32(tmem + c + ((uint32_t)(warp * 32) << 16), v);
@@ -297,6 +305,7 @@ kvq_status launch_kch_table(const AttnLaunch& a, cudaStream_t stream) {
   k.corr = a.corr;
   k.status = a.status;
   k.code_offset = (float)key_code_offset<BITS>();
+  k.wait_limit_ns = a.wait_limit_ns;
   if (a.corr == KVQ_CORR_EXACT) {
     // log(sinh a / a) per channel: the CUDA-core form
     const dim3 kg((a.n_q + kKchRows - 1) / kKchRows, (a.n_ct + kKchCols - 1) / kKchCols, a.bh);

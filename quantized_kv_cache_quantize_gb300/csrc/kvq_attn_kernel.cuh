@@ -53,6 +53,7 @@
 #include <cudaTypedefs.h>
 
 #include <mutex>
+#include <type_traits>
 
 #include "kvq_fwht.cuh"
 #include "kvq_internal.h"
@@ -99,6 +100,7 @@ constexpr int kBlockN = 128;
 constexpr int kHalf = 16384;   // one [128 rows][64 x 16-bit] swizzled sub-tile
 constexpr int kExt = 4096;     // one [128 rows][16 x 16-bit] tile, no swizzle
 constexpr float kChunkSumLimit = 32768.0f;  // 2^15: every P of the chunk stays FP16
+constexpr float kF16Max = 65504.0f;
 
 // Extension-column scalings keeping every FP16 operand in range: bias
 // a * 2^8 against D^2 * 2^-8, zero-point term q-sum * 2^4 against -z D * 2^-4.
@@ -146,19 +148,28 @@ struct Cfg {
 };
 
 // mbarrier slots
+//
+// A cached stage is handed over in two parts: its K half (key rows and
+// extension rows) and its V half (value rows, and the exact correction's
+// per-key step terms).  The K half is free again once both query tiles'
+// QK MMAs of the tile are done, the V half once their PV MMAs are, so the
+// dequant warps can fill the next K half about a tile period before the MMA
+// needs it instead of in the gap between the last PV and the next QK.
 enum : int {
   kBarQ = 0,        // query tiles landed (phase 0: rotated, phase 1: original)
   kBarQFree = 1,    // all cached-tile QK MMAs done: query buffers reusable
   kBarQx = 2,       // query extension columns written (NQ * 128 arrivals)
-  kBarFullDq = 3,   // [2] cached stage dequantized (128 arrivals)
+  kBarFullK = 3,    // [2] cached stage: K half dequantized (128 arrivals)
   kBarFullTma = 5,  // [2] current stage loaded (TMA)
-  kBarEmpty = 7,    // [2] stage consumed (MMA commit)
+  kBarEmptyV = 7,   // [2] stage's V half consumed (MMA commit after the last PV)
   kBarS = 9,        // [2] S buffer ready (MMA commit)
   kBarP = 11,       // [NQ] P written, O rescaled (128 arrivals)
   kBarOStep = 13,   // [NQ] PV of a tile done (MMA commit; one-tile schedule)
   kBarODone = 15,   // [NQ] every MMA done (MMA commit)
   kBarKch = 17,     // [2] per-channel keys: the stage's block steps written (128 arrivals)
-  kBarCount = 19
+  kBarFullV = 19,   // [2] cached stage: V half dequantized (128 arrivals)
+  kBarEmptyK = 21,  // [2] stage's K half consumed (MMA commit after the last QK)
+  kBarCount = 23
 };
 constexpr int kAbortOffset = kBarCount * 8;
 constexpr int kTmemSlotOffset = kAbortOffset + 4;
@@ -318,7 +329,10 @@ __device__ __forceinline__ void dequant_row_kch(const uint32_t (&words)[D * BITS
 
 // Exponentials of one 32-column chunk of scores against the base m: P pairs
 // in FP16 (low column in the low half) and the packed pair of partial sums;
-// columns at or past `valid` give 0.
+// with MASKED, columns at or past `valid` give 0 (the last tile of a
+// segment; every other tile takes the unmasked form, which has no per-column
+// compare and select).
+template <bool MASKED>
 __device__ __forceinline__ uint64_t exp_chunk(const uint32_t (&s)[32], uint64_t sl2x2, float m,
                                               int valid, uint32_t (&pk)[16]) {
   const uint64_t negm2 = ptx::f2_pack(-m, -m);
@@ -331,7 +345,7 @@ __device__ __forceinline__ uint64_t exp_chunk(const uint32_t (&s)[32], uint64_t 
                    x0, x1);
     float e0 = ptx::ex2_approx(x0);
     float e1 = ptx::ex2_approx(x1);
-    if (valid < 32) {
+    if (MASKED && valid < 32) {
       e0 = (2 * k < valid) ? e0 : 0.f;
       e1 = (2 * k + 1 < valid) ? e1 : 0.f;
     }
@@ -380,6 +394,7 @@ __device__ __forceinline__ float log_sinhc(float a) {
 
 // exp_chunk with a per-column additive term nb (log2 units, pairs packed):
 // 2^(s * scale * log2(e) + nb - m)
+template <bool MASKED>
 __device__ __forceinline__ uint64_t exp_chunk_b(const uint32_t (&s)[32], const uint64_t (&nb)[16],
                                                 uint64_t sl2x2, float m, int valid,
                                                 uint32_t (&pk)[16]) {
@@ -393,7 +408,7 @@ __device__ __forceinline__ uint64_t exp_chunk_b(const uint32_t (&s)[32], const u
                    x0, x1);
     float e0 = ptx::ex2_approx(x0);
     float e1 = ptx::ex2_approx(x1);
-    if (valid < 32) {
+    if (MASKED && valid < 32) {
       e0 = (2 * k < valid) ? e0 : 0.f;
       e1 = (2 * k + 1 < valid) ? e1 : 0.f;
     }
@@ -553,9 +568,11 @@ __global__ void __launch_bounds__(Cfg<D, NQ, PRECISE, EXACT, KCH>::kThreads, 1)
     ptx::mbar_init(BAR(kBarQFree), 1);
     ptx::mbar_init(BAR(kBarQx), NQ * 128);
     for (int s = 0; s < 2; ++s) {
-      ptx::mbar_init(BAR(kBarFullDq + s), 128);
+      ptx::mbar_init(BAR(kBarFullK + s), 128);
+      ptx::mbar_init(BAR(kBarFullV + s), 128);
       ptx::mbar_init(BAR(kBarFullTma + s), 1);
-      ptx::mbar_init(BAR(kBarEmpty + s), 1);
+      ptx::mbar_init(BAR(kBarEmptyK + s), 1);
+      ptx::mbar_init(BAR(kBarEmptyV + s), 1);
       ptx::mbar_init(BAR(kBarS + s), 1);
       ptx::mbar_init(BAR(kBarP + s), 128);
       ptx::mbar_init(BAR(kBarOStep + s), 1);
@@ -785,15 +802,17 @@ __global__ void __launch_bounds__(Cfg<D, NQ, PRECISE, EXACT, KCH>::kThreads, 1)
       uint64_t acc = ptx::f2_pack(0.f, 0.f);
       // exact correction on cached tiles: (scale D_g / 2)^2 of the tile's keys
       // from the dequant warps, read after acquiring their writes through the
-      // stage's dequant barrier (its phase for this tile has completed and
-      // cannot advance before this tile's P is handed over); the series alone
-      // when every group of every key stays within T <= 1
+      // stage's V-half barrier (its phase for this tile has completed, and the
+      // V half is not refilled before this tile's P is handed over and its PV
+      // done); the series alone when every group of every key stays within
+      // T <= 1
       const bool exact_tile = EXACT && j < n_ct;
       const float* dq =
           reinterpret_cast<const float*>(smem + C::kStages + (j & 1) * C::kStageBytes + C::kDsq);
       bool fast = true;
       if (exact_tile) {
-        if (!__all_sync(0xffffffffu, wait_bar(BAR(kBarFullDq + (j & 1)), (j >> 1) & 1, lim, abort, p.status))) {
+        if (!__all_sync(0xffffffffu,
+                        wait_bar(BAR(kBarFullV + (j & 1)), (j >> 1) & 1, lim, abort, p.status))) {
           ok = false;
           break;
         }
@@ -806,63 +825,74 @@ __global__ void __launch_bounds__(Cfg<D, NQ, PRECISE, EXACT, KCH>::kThreads, 1)
         }
         fast = __all_sync(0xffffffffu, fast);
       }
+      // Full tiles take the chunk pass without column masks; only the last
+      // tile of a segment (nv < 128 valid keys) masks its columns.
+      auto chunk_pass = [&](auto masked_tag) {
+        constexpr bool MASKED = decltype(masked_tag)::value;
 #pragma unroll(EXACT ? 1 : 2)
-      for (int c = 0; c < kBlockN / 32; ++c) {
-        uint64_t nb[16];
-        if (exact_tile) {   // before the scores are loaded: fewer live registers
-          exact_series<GE>(dq + 32 * c, mu2, a2, nb);
-          if (!fast) exact_fix<GE, D, GROUP>(dq + 32 * c, mu2, a2, t_q, nb);
-        }
-        uint32_t cur[32];
-        ptx::tmem_ld32(t_s + 32 * c, cur);
-        uint32_t pk[16];
-        uint64_t cs = exact_tile ? exp_chunk_b(cur, nb, sl2x2, m, nv - 32 * c, pk)
-                                 : exp_chunk(cur, sl2x2, m - toff, nv - 32 * c, pk);
-        float cs_lo, cs_hi;
-        ptx::f2_unpack(cs, cs_lo, cs_hi);
-        // NaN-safe: an infinite or undefined sum also takes the slow path
-        if (__any_sync(0xffffffffu, !(cs_lo + cs_hi <= kChunkSumLimit))) {
-          float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-          float cmax;
-          if (exact_tile) {
-#pragma unroll
-            for (int k2 = 0; k2 < 16; ++k2) {
-              float b0, b1;
-              ptx::f2_unpack(nb[k2], b0, b1);
-              const float x0 = fmaf(__uint_as_float(cur[2 * k2]), sl2, b0);
-              const float x1 = fmaf(__uint_as_float(cur[2 * k2 + 1]), sl2, b1);
-              m4[(2 * k2) & 3] = (32 * c + 2 * k2 < nv) ? fmaxf(m4[(2 * k2) & 3], x0) : m4[(2 * k2) & 3];
-              m4[(2 * k2 + 1) & 3] =
-                  (32 * c + 2 * k2 + 1 < nv) ? fmaxf(m4[(2 * k2 + 1) & 3], x1) : m4[(2 * k2 + 1) & 3];
-            }
-            cmax = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
-          } else {
-#pragma unroll
-            for (int k = 0; k < 32; ++k)
-              m4[k & 3] = (32 * c + k < nv) ? fmaxf(m4[k & 3], __uint_as_float(cur[k])) : m4[k & 3];
-            cmax = fmaf(fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])), sl2, toff);
+        for (int c = 0; c < kBlockN / 32; ++c) {
+          uint64_t nb[16];
+          if (exact_tile) {   // before the scores are loaded: fewer live registers
+            exact_series<GE>(dq + 32 * c, mu2, a2, nb);
+            if (!fast) exact_fix<GE, D, GROUP>(dq + 32 * c, mu2, a2, t_q, nb);
           }
-          const float m_new = fmaxf(m, cmax);
-          const float alpha = exp2f(m - m_new);   // 0 from the initial -inf base
-          acc = ptx::f2_mul(acc, ptx::f2_pack(alpha, alpha));
-          if (!mass_only && c > 0) {
-            ptx::tmem_st_wait();
-            for (int cc = 0; cc < c; ++cc) {
-              uint32_t v[16];
-              ptx::tmem_ld16(t_s + 16 * cc, v);
+          uint32_t cur[32];
+          ptx::tmem_ld32(t_s + 32 * c, cur);
+          uint32_t pk[16];
+          uint64_t cs = exact_tile ? exp_chunk_b<MASKED>(cur, nb, sl2x2, m, nv - 32 * c, pk)
+                                   : exp_chunk<MASKED>(cur, sl2x2, m - toff, nv - 32 * c, pk);
+          float cs_lo, cs_hi;
+          ptx::f2_unpack(cs, cs_lo, cs_hi);
+          // NaN-safe: an infinite or undefined sum also takes the slow path
+          if (__any_sync(0xffffffffu, !(cs_lo + cs_hi <= kChunkSumLimit))) {
+            float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+            float cmax;
+            if (exact_tile) {
 #pragma unroll
-              for (int k = 0; k < 16; ++k) v[k] = ptx::f16x2_rn(h_lo(v[k]) * alpha, h_hi(v[k]) * alpha);
-              ptx::tmem_st16(t_s + 16 * cc, v);
+              for (int k2 = 0; k2 < 16; ++k2) {
+                float b0, b1;
+                ptx::f2_unpack(nb[k2], b0, b1);
+                const float x0 = fmaf(__uint_as_float(cur[2 * k2]), sl2, b0);
+                const float x1 = fmaf(__uint_as_float(cur[2 * k2 + 1]), sl2, b1);
+                const int i0 = (2 * k2) & 3, i1 = (2 * k2 + 1) & 3;
+                m4[i0] = (!MASKED || 32 * c + 2 * k2 < nv) ? fmaxf(m4[i0], x0) : m4[i0];
+                m4[i1] = (!MASKED || 32 * c + 2 * k2 + 1 < nv) ? fmaxf(m4[i1], x1) : m4[i1];
+              }
+              cmax = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+            } else {
+#pragma unroll
+              for (int k = 0; k < 32; ++k)
+                m4[k & 3] =
+                    (!MASKED || 32 * c + k < nv) ? fmaxf(m4[k & 3], __uint_as_float(cur[k])) : m4[k & 3];
+              cmax = fmaf(fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])), sl2, toff);
             }
+            const float m_new = fmaxf(m, cmax);
+            const float alpha = exp2f(m - m_new);   // 0 from the initial -inf base
+            acc = ptx::f2_mul(acc, ptx::f2_pack(alpha, alpha));
+            if (!mass_only && c > 0) {
+              ptx::tmem_st_wait();
+              for (int cc = 0; cc < c; ++cc) {
+                uint32_t v[16];
+                ptx::tmem_ld16(t_s + 16 * cc, v);
+#pragma unroll
+                for (int k = 0; k < 16; ++k) v[k] = ptx::f16x2_rn(h_lo(v[k]) * alpha, h_hi(v[k]) * alpha);
+                ptx::tmem_st16(t_s + 16 * cc, v);
+              }
+            }
+            m = m_new;
+            cs = exact_tile ? exp_chunk_b<MASKED>(cur, nb, sl2x2, m, nv - 32 * c, pk)
+                            : exp_chunk<MASKED>(cur, sl2x2, m - toff, nv - 32 * c, pk);
           }
-          m = m_new;
-          cs = exact_tile ? exp_chunk_b(cur, nb, sl2x2, m, nv - 32 * c, pk)
-                          : exp_chunk(cur, sl2x2, m - toff, nv - 32 * c, pk);
+          acc = ptx::f2_add(acc, cs);
+          // P of columns [32c, 32c + 32) -> TMEM columns [16c, 16c + 16): all
+          // of them already read
+          if (!mass_only) ptx::tmem_st16(t_s + 16 * c, pk);
         }
-        acc = ptx::f2_add(acc, cs);
-        // P of columns [32c, 32c + 32) -> TMEM columns [16c, 16c + 16): all
-        // of them already read
-        if (!mass_only) ptx::tmem_st16(t_s + 16 * c, pk);
+      };
+      if (nv < kBlockN) {
+        chunk_pass(std::true_type{});
+      } else {
+        chunk_pass(std::false_type{});
       }
       if (NQ == 1 && j > 0) {
         // one-tile schedule: QK of this tile was issued before the previous
@@ -1018,14 +1048,15 @@ __global__ void __launch_bounds__(Cfg<D, NQ, PRECISE, EXACT, KCH>::kThreads, 1)
     // =========================== dequant ===========================
     const int r = tid - C::kDequantWarp * 32;
     const size_t head_tok = static_cast<size_t>(bh) * p.cap;
-    // packed words of key r of tile j (zeros past the end of the window)
-    // (the tile at local index j is `pos`)
-    auto load_key = [&](int j, const CTile& pos, uint32_t (&kw)[NW], uint32_t (&ksz)[G],
-                        uint32_t (&vw)[NW], uint32_t (&vsz)[G], uint32_t& kmeta) {
+    // packed words of key r of tile j (zeros past the end of the window; the
+    // tile at local index j is `pos`): the key half (codes, per-token steps,
+    // or the per-channel block word of channel r) and the value half
+    auto load_k = [&](int j, const CTile& pos, uint32_t (&kw)[NW], uint32_t (&ksz)[G],
+                      uint32_t& kmeta) {
 #pragma unroll
-      for (int i = 0; i < NW; ++i) kw[i] = vw[i] = 0u;
+      for (int i = 0; i < NW; ++i) kw[i] = 0u;
 #pragma unroll
-      for (int g = 0; g < G; ++g) ksz[g] = vsz[g] = 0u;
+      for (int g = 0; g < G; ++g) ksz[g] = 0u;
       kmeta = 0u;
       if (j >= n_ct) return;
       // per-channel keys: thread r < D fetches the block's word of channel r
@@ -1043,27 +1074,42 @@ __global__ void __launch_bounds__(Cfg<D, NQ, PRECISE, EXACT, KCH>::kThreads, 1)
 #pragma unroll
         for (int g = 0; g < G; ++g) ksz[g] = __ldg(p.k_sz + tok * G + g);
       }
-      if (!mass_only) {
-        const uint4* vc = reinterpret_cast<const uint4*>(p.v_codes + tok * CB);
+    };
+    auto load_v = [&](int j, const CTile& pos, uint32_t (&vw)[NW], uint32_t (&vsz)[G]) {
 #pragma unroll
-        for (int i = 0; i < NW / 4; ++i) {
-          const uint4 v = __ldg(vc + i);
-          vw[4 * i] = v.x; vw[4 * i + 1] = v.y; vw[4 * i + 2] = v.z; vw[4 * i + 3] = v.w;
-        }
+      for (int i = 0; i < NW; ++i) vw[i] = 0u;
 #pragma unroll
-        for (int g = 0; g < G; ++g) vsz[g] = __ldg(p.v_sz + tok * G + g);
+      for (int g = 0; g < G; ++g) vsz[g] = 0u;
+      if (j >= n_ct || mass_only || r >= ctile_count(pos)) return;
+      const size_t tok = head_tok + (size_t)ctile_first(pos) + r;
+      const uint4* vc = reinterpret_cast<const uint4*>(p.v_codes + tok * CB);
+#pragma unroll
+      for (int i = 0; i < NW / 4; ++i) {
+        const uint4 v = __ldg(vc + i);
+        vw[4 * i] = v.x; vw[4 * i + 1] = v.y; vw[4 * i + 2] = v.z; vw[4 * i + 3] = v.w;
       }
+#pragma unroll
+      for (int g = 0; g < G; ++g) vsz[g] = __ldg(p.v_sz + tok * G + g);
     };
     uint32_t kw[NW], ksz[G], vw[NW], vsz[G], kmeta;
+    // FP16 operand limits of the cached tiles (KVQ_ERR_RANGE when broken):
+    // the key constant -(magic + o) D with magic <= 16 (which also keeps the
+    // bias factor D^2 / 256 finite) and the value (code - z) D, at most
+    // (|z| + 2^B - 1) D in magnitude
+    constexpr float kKeyConst = 16.0f + (float)key_code_offset<BITS>();
+    constexpr float kQmax = (float)((1 << BITS) - 1);
+    bool range_bad = false;
     CTile dq_tile = ctile_at(kb), dq_next = dq_tile;
     ctile_next(dq_next);
-    load_key(0, dq_tile, kw, ksz, vw, vsz, kmeta);
+    load_k(0, dq_tile, kw, ksz, kmeta);
+    load_v(0, dq_tile, vw, vsz);
     for (int j = 0; j < n_ct; ++j) {
       if (*abort) break;
       const int s = j & 1;
       const bool valid = r < ctile_count(dq_tile);
-      if (j >= 2 && !wait_bar(BAR(kBarEmpty + s), ((j >> 1) - 1) & 1, lim, abort, p.status)) break;
       uint8_t* st = smem + C::kStages + s * C::kStageBytes;
+      // ---- K half: key rows and their extension rows ----
+      if (j >= 2 && !wait_bar(BAR(kBarEmptyK + s), ((j >> 1) - 1) & 1, lim, abort, p.status)) break;
       if (KCH) {
         // the key block's per-channel steps and -magic * steps, shared
         // by the warpgroup through the stage's barrier (all 128 threads
@@ -1071,6 +1117,7 @@ __global__ void __launch_bounds__(Cfg<D, NQ, PRECISE, EXACT, KCH>::kThreads, 1)
         // other stage's barrier for tile j - 1, so every thread is done
         // with this stage's previous tile)
         if (r < D) {
+          range_bad |= !(bf16_lo(kmeta) * kKeyConst < kF16Max);
           const int k = BITS == 2 ? (r & 15) >> 1 : 0;
           reinterpret_cast<__half*>(st + C::kKch)[r] = __float2half_rn(bf16_lo(kmeta));
           reinterpret_cast<__half*>(st + C::kKch + 256)[r] =
@@ -1082,15 +1129,24 @@ __global__ void __launch_bounds__(Cfg<D, NQ, PRECISE, EXACT, KCH>::kThreads, 1)
       float cx[16], cz[16];
 #pragma unroll
       for (int i = 0; i < 16; ++i) cx[i] = cz[i] = 0.f;
+      // exact correction: (scale D_g / 2)^2 of this key (0 past the window),
+      // written with the V half
+      float dsq[EXACT ? G : 1];
+      if (EXACT) {
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+          const float dt = p.half_scale * bf16_lo(ksz[g]);
+          dsq[g] = dt * dt;
+        }
+      }
       if (valid && KCH) {
         dequant_row_kch<D, BITS>(kw, st + C::kKch, st + C::kKch + 256, st, r);
-        if (!mass_only) dequant_row<D, BITS, GROUP, true>(vw, vsz, st + C::kTile, r);
       } else if (valid) {
         dequant_row<D, BITS, GROUP, false>(kw, ksz, st, r);
-        if (!mass_only) dequant_row<D, BITS, GROUP, true>(vw, vsz, st + C::kTile, r);
 #pragma unroll
         for (int g = 0; g < G; ++g) {
           const float dl = bf16_lo(ksz[g]);
+          range_bad |= !(dl * kKeyConst < kF16Max);
           float hi, lo;
           const int zc = PRECISE ? 3 * g : G + 3 * g;
           float(&zt)[16] = PRECISE ? cz : cx;
@@ -1105,32 +1161,46 @@ __global__ void __launch_bounds__(Cfg<D, NQ, PRECISE, EXACT, KCH>::kThreads, 1)
         }
       } else {
         zero_row<D>(st, r);
-        if (!mass_only) zero_row<D>(st + C::kTile, r);
+      }
+      write_ext_row(st + 2 * C::kTile, r, cx);
+      if (PRECISE) write_ext_row(st + 2 * C::kTile + kExt, r, cz);
+      ptx::fence_proxy_async_smem();
+      ptx::mbar_arrive(BAR(kBarFullK + s));
+      // the next tile's key words travel while the V half is awaited and
+      // written
+      load_k(j + 1, dq_next, kw, ksz, kmeta);
+      // ---- V half: value rows (and the exact correction's step terms) ----
+      if (j >= 2 && !wait_bar(BAR(kBarEmptyV + s), ((j >> 1) - 1) & 1, lim, abort, p.status)) break;
+      if (!mass_only) {
+        if (valid) {
+#pragma unroll
+          for (int g = 0; g < G; ++g)
+            range_bad |= !((fabsf(bf16_hi(vsz[g])) + kQmax) * bf16_lo(vsz[g]) < kF16Max);
+          dequant_row<D, BITS, GROUP, true>(vw, vsz, st + C::kTile, r);
+        } else {
+          zero_row<D>(st + C::kTile, r);
+        }
       }
       if (EXACT) {
-        // (scale D_g / 2)^2 of this key (0 past the window) and, per group,
-        // the maximum over the warp's 32 keys
+        // per group the maximum over the warp's 32 keys as well
         float* dq = reinterpret_cast<float*>(st + C::kDsq);
 #pragma unroll
         for (int g = 0; g < G; ++g) {
-          float dt = p.half_scale * bf16_lo(ksz[g]);
-          dt *= dt;
+          float dt = dsq[g];
           dq[g * kBlockN + r] = dt;
 #pragma unroll
           for (int o = 16; o > 0; o >>= 1) dt = fmaxf(dt, __shfl_xor_sync(0xffffffffu, dt, o));
           if ((r & 31) == 0) dq[4 * kBlockN + 4 * g + (r >> 5)] = dt;
         }
       }
-      // the next tile's words travel while this one is handed over and the
-      // next stage is awaited
-      load_key(j + 1, dq_next, kw, ksz, vw, vsz, kmeta);
+      ptx::fence_proxy_async_smem();
+      ptx::mbar_arrive(BAR(kBarFullV + s));
+      load_v(j + 1, dq_next, vw, vsz);
       dq_tile = dq_next;
       ctile_next(dq_next);
-      write_ext_row(st + 2 * C::kTile, r, cx);
-      if (PRECISE) write_ext_row(st + 2 * C::kTile + kExt, r, cz);
-      ptx::fence_proxy_async_smem();
-      ptx::mbar_arrive(BAR(kBarFullDq + s));
     }
+    // a step size or value the FP16 tiles cannot carry: recorded, not fatal
+    if (__any_sync(0xffffffffu, range_bad) && (r & 31) == 0) atomicCAS(p.status, 0, (int)KVQ_ERR_RANGE);
   } else if (warp == C::kMmaWarp) {
     // ============================= MMA =============================
     if (lane == 0) {
@@ -1147,12 +1217,20 @@ __global__ void __launch_bounds__(Cfg<D, NQ, PRECISE, EXACT, KCH>::kThreads, 1)
         // cached tiles are uses 0, 1, ... of their stage's dequant barrier;
         // current tiles count only the TMA barrier's own uses of that stage
         const int use = j < n_ct ? (j >> 1) : (j >> 1) - ((n_ct + 1 - s) >> 1);
-        if (!wait_bar(BAR(j < n_ct ? kBarFullDq + s : kBarFullTma + s), use & 1, lim, abort, p.status))
+        if (!wait_bar(BAR(j < n_ct ? kBarFullK + s : kBarFullTma + s), use & 1, lim, abort, p.status))
           return false;
         if (j >= n_ct && !q_orig_ready) {
           if (!wait_bar(BAR(kBarQ), 1, lim, abort, p.status)) return false;
           q_orig_ready = true;
         }
+        ptx::tc_fence_after();
+        return true;
+      };
+      // the V half of a cached stage, before its first PV (current tiles
+      // arrive whole through the TMA barrier awaited for their QK)
+      auto wait_full_v = [&](int j) -> bool {
+        if (j >= n_ct || mass_only) return true;
+        if (!wait_bar(BAR(kBarFullV + (j & 1)), (j >> 1) & 1, lim, abort, p.status)) return false;
         ptx::tc_fence_after();
         return true;
       };
@@ -1218,11 +1296,13 @@ __global__ void __launch_bounds__(Cfg<D, NQ, PRECISE, EXACT, KCH>::kThreads, 1)
             ptx::mma_commit(BAR(kBarS + 0));
             issue_qk(0, 1, tmem + 128);
             ptx::mma_commit(BAR(kBarS + 1));
+            ptx::mma_commit(BAR(kBarEmptyK + 0));
             after_qk(0, 1);
           }
           for (int j = 0; j < n_t && ok; ++j) {
             if (!(ok = wait_bar(BAR(kBarP + 0), j & 1, lim, abort, p.status))) break;
             ptx::tc_fence_after();
+            if (!(ok = wait_full_v(j))) break;
             if (!mass_only) issue_pv(j, 0, tmem);
             const bool more = j + 1 < n_t;
             if (more) {
@@ -1233,10 +1313,11 @@ __global__ void __launch_bounds__(Cfg<D, NQ, PRECISE, EXACT, KCH>::kThreads, 1)
             if (!(ok = wait_bar(BAR(kBarP + 1), j & 1, lim, abort, p.status))) break;
             ptx::tc_fence_after();
             if (!mass_only) issue_pv(j, 1, tmem + 128);
-            ptx::mma_commit(BAR(kBarEmpty + (j & 1)));
+            ptx::mma_commit(BAR(kBarEmptyV + (j & 1)));
             if (more) {
               issue_qk(j + 1, 1, tmem + 128);
               ptx::mma_commit(BAR(kBarS + 1));
+              ptx::mma_commit(BAR(kBarEmptyK + ((j + 1) & 1)));
               after_qk(j + 1, 1);
             }
           }
@@ -1245,6 +1326,7 @@ __global__ void __launch_bounds__(Cfg<D, NQ, PRECISE, EXACT, KCH>::kThreads, 1)
           if (ok) {
             issue_qk(0, 0, tmem);
             ptx::mma_commit(BAR(kBarS + 0));
+            ptx::mma_commit(BAR(kBarEmptyK + 0));
             after_qk(0, 0);
           }
           for (int j = 0; j < n_t && ok; ++j) {
@@ -1252,14 +1334,16 @@ __global__ void __launch_bounds__(Cfg<D, NQ, PRECISE, EXACT, KCH>::kThreads, 1)
               if (!(ok = wait_full(j + 1))) break;
               issue_qk(j + 1, 0, tmem + ((j + 1) & 1) * 128);
               ptx::mma_commit(BAR(kBarS + ((j + 1) & 1)));
+              ptx::mma_commit(BAR(kBarEmptyK + ((j + 1) & 1)));
               after_qk(j + 1, 0);
             }
             if (!(ok = wait_bar(BAR(kBarP + 0), j & 1, lim, abort, p.status))) break;
             ptx::tc_fence_after();
+            if (!(ok = wait_full_v(j))) break;
             if (!mass_only) issue_pv(j, 0, tmem + (j & 1) * 128);
             // also in mass-only mode: keeps the softmax one tile behind
             ptx::mma_commit(BAR(kBarOStep));
-            ptx::mma_commit(BAR(kBarEmpty + (j & 1)));
+            ptx::mma_commit(BAR(kBarEmptyV + (j & 1)));
           }
         }
       }
@@ -1304,7 +1388,9 @@ __global__ void __launch_bounds__(Cfg<D, NQ, PRECISE, EXACT, KCH>::kThreads, 1)
                                q_row(q), bh, BAR(kBarQ));
           q_orig_issued = true;
         }
-        if (j >= 2 && !wait_bar(BAR(kBarEmpty + s), ((j >> 1) - 1) & 1, lim, abort, p.status)) break;
+        // the V half's barrier: its commit follows the K half's, so both
+        // halves of the stage are free
+        if (j >= 2 && !wait_bar(BAR(kBarEmptyV + s), ((j >> 1) - 1) & 1, lim, abort, p.status)) break;
         const int key0 = (cb + j - n_ct) * kBlockN;
         const uint32_t st = s_base + C::kStages + s * C::kStageBytes;
         ptx::mbar_expect_tx(BAR(kBarFullTma + s), (mass_only ? 1 : 2) * NKH * kHalf);

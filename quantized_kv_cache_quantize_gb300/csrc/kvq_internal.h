@@ -5,6 +5,7 @@
 #include <stdint.h>
 
 #include <atomic>
+#include <mutex>
 
 #include "../../include/kvq.h"
 
@@ -52,6 +53,8 @@ struct QuantArgs {
 // Arguments of the rotation kernel: up to two row segments in one launch.
 // Per segment: fp32 output (out_f32), or FP16 output in dst plus, when
 // dst_lo is set, the FP16 rounding remainder fp16(x - fp16(x)) in dst_lo.
+// With status set, a segment whose range_limit[i] > 0 records KVQ_ERR_RANGE
+// there when a rotated value reaches that magnitude (FP16 outputs only).
 struct RotateArgs {
   const uint16_t* src[2];
   void* dst[2];
@@ -60,6 +63,8 @@ struct RotateArgs {
   uint32_t sign_bits[4];
   float inv_sqrt_d;
   int out_f32;
+  int* status;
+  float range_limit[2];
 };
 
 // Raise a kernel's dynamic shared-memory limit once per device (the
@@ -76,6 +81,22 @@ cudaError_t ensure_smem_limit(Kernel kern, int bytes, std::atomic<uint64_t>& don
   if (e == cudaSuccess && bit != 0) done.fetch_or(bit, std::memory_order_release);
   return e;
 }
+
+// Device address of one of this library's __device__ variables, valid in
+// the calling thread's current context.  In host code the variable's name is
+// only a host-side stand-in, so the address comes from cudaGetSymbolAddress;
+// it is cached per device together with the unique id of the context it was
+// looked up in, and looked up again when that context changes (after
+// cudaDeviceReset, or with another context made current).  The lookup may
+// load the library's device code: the first call on a device, and the first
+// after a context change, must come before any stream capture.
+constexpr int kMaxDevices = 64;
+struct SymbolSlot {
+  std::mutex mu;
+  unsigned long long ctx_id[kMaxDevices] = {};
+  void* ptr[kMaxDevices] = {};
+};
+cudaError_t device_symbol_address(const void* symbol, SymbolSlot& slot, void** out);
 
 cudaError_t launch_quantize_append(const QuantArgs& a, int d, int bits, int group,
                                    cudaStream_t stream, bool* supported);
@@ -191,6 +212,9 @@ inline void attention_split(long long bh, int n_q, int n_ct, int n_r, int d, int
 
 kvq_status launch_attention(const AttnLaunch& a, int d, int bits, int group,
                             cudaStream_t stream);
+// device address of the attention status word (first in-kernel error since
+// it was last read) in the current device's current context, or null
+int* status_ptr();
 // the attention kernels of the exact correction and of per-channel keys,
 // built in translation units of their own (a.status must be set)
 kvq_status launch_attention_exact(const AttnLaunch& a, int d, int bits, int group,

@@ -670,6 +670,7 @@ __global__ void __launch_bounds__(kThreads) rotate_kernel(const RotateArgs a) {
   // before any of them is transformed
   constexpr int U = kRotUnroll;
   const long long step = nwarps * RPW;
+  bool out_of_range = false;
   for (long long r0 = warp0 * RPW; r0 < total; r0 += step * U) {
     uint4 raw[U];
     long long rr[U];
@@ -695,6 +696,9 @@ __global__ void __launch_bounds__(kThreads) rotate_kernel(const RotateArgs a) {
 #pragma unroll
       for (int e = 0; e < 8; ++e) x[e] = __fmul_rn(x[e], a.inv_sqrt_d);
       if (!valid[u]) continue;
+      const float lim = a.range_limit[seg1[u] ? 1 : 0];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) out_of_range |= !(fabsf(x[e]) < lim) && lim > 0.f;
       if (a.out_f32) {
         float4* dst = reinterpret_cast<float4*>(static_cast<float*>(dstp) + rr[u] * D + 8 * t);
         dst[0] = make_float4(x[0], x[1], x[2], x[3]);
@@ -718,6 +722,10 @@ __global__ void __launch_bounds__(kThreads) rotate_kernel(const RotateArgs a) {
       }
     }
   }
+  // a rotated value the FP16 operands cannot carry: recorded, not fatal
+  // (the loop bounds are warp-uniform, so every lane arrives here)
+  if (__any_sync(0xffffffffu, out_of_range) && lane == 0 && a.status != nullptr)
+    atomicCAS(a.status, 0, (int)KVQ_ERR_RANGE);
 }
 
 int sm_count() {

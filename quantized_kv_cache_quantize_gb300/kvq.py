@@ -4,6 +4,7 @@ device memory and streams.  There is no CPU fallback: if libkvq.so is missing
 the first call raises."""
 from __future__ import annotations
 
+import contextlib
 import ctypes
 import functools
 import math
@@ -23,6 +24,7 @@ KVQ_ERR_CUDA = 4
 KVQ_ERR_TIMEOUT = 5
 KVQ_ERR_ALIGNMENT = 6
 KVQ_ERR_TOO_LARGE = 7
+KVQ_ERR_RANGE = 8
 NOALLOC_SCRATCH_BYTES = 32 << 20
 
 KEYS_PER_TOKEN = 0
@@ -128,10 +130,25 @@ def _check(status: int, what: str):
         raise KVQError(status, what)
 
 
-def _stream(stream) -> ctypes.c_void_p:
+def _stream(stream, device=None) -> ctypes.c_void_p:
+    """The stream handle for a call on ``device``: torch's current stream of
+    that device when none is given; a torch stream of another device is
+    refused (its kernels would run on the wrong GPU)."""
     if stream is None:
-        stream = torch.cuda.current_stream()
+        stream = torch.cuda.current_stream(device)
+    elif device is not None and getattr(stream, "device", device) != device:
+        raise ValueError(f"stream belongs to {stream.device}, the call's tensors to {device}")
     return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _on_device(device):
+    """Make ``device`` the current CUDA device for the duration of a call.
+    The library launches on the current device and looks its status word and
+    scratch up there, so a call whose tensors live on another GPU than the
+    current one must switch first.  No-op for host tensors (shape checks)."""
+    if device is None or device.type != "cuda":
+        return contextlib.nullcontext()
+    return torch.cuda.device(device)
 
 
 def _ptr(t: torch.Tensor | None) -> ctypes.c_void_p:
@@ -271,8 +288,10 @@ def quantize_append(cache: KVCache, k_new: torch.Tensor, v_new: torch.Tensor, st
     _bf16_dev(k_new, "k_new")
     _bf16_dev(v_new, "v_new")
     _check_device(cache, ("k_new", k_new), ("v_new", v_new))
-    _check(lib().kvq_quantize_append(ctypes.byref(cache.struct), _ptr(k_new), _ptr(v_new),
-                                     n_new, _stream(stream)), "kvq_quantize_append")
+    dev = cache.k_codes.device
+    with _on_device(dev):
+        _check(lib().kvq_quantize_append(ctypes.byref(cache.struct), _ptr(k_new), _ptr(v_new),
+                                         n_new, _stream(stream, dev)), "kvq_quantize_append")
 
 
 @_nvtx("kvq_attention_corrected")
@@ -292,14 +311,16 @@ def attention_corrected(cache: KVCache, q, k_cur, v_cur, scale: float | None = N
     if with_mass:
         ps = torch.empty(q.shape[:-1], dtype=torch.float32, device=q.device)
         pr = torch.empty_like(ps)
-    ws_bytes = cache.workspace_bytes(n_q, n_r)
-    if workspace is None:
-        workspace = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=q.device)
-    ws_ptr, ws_size = _workspace_arg(workspace, q.device)
-    _check(lib().kvq_attention_corrected(
-        ctypes.byref(cache.struct), _ptr(q), _ptr(k_cur), _ptr(v_cur), n_q, n_r,
-        ctypes.c_float(scale), corr, flags, ws_ptr, ws_size, _ptr(out),
-        _ptr(ps), _ptr(pr), _stream(stream)), "kvq_attention_corrected")
+    with _on_device(q.device):
+        # the workspace size depends on the device's SM count
+        ws_bytes = cache.workspace_bytes(n_q, n_r)
+        if workspace is None:
+            workspace = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=q.device)
+        ws_ptr, ws_size = _workspace_arg(workspace, q.device)
+        _check(lib().kvq_attention_corrected(
+            ctypes.byref(cache.struct), _ptr(q), _ptr(k_cur), _ptr(v_cur), n_q, n_r,
+            ctypes.c_float(scale), corr, flags, ws_ptr, ws_size, _ptr(out),
+            _ptr(ps), _ptr(pr), _stream(stream, q.device)), "kvq_attention_corrected")
     return (out, ps, pr) if with_mass else out
 
 
@@ -321,10 +342,11 @@ def attention_corrected_noalloc(cache: KVCache, q, k_cur, v_cur, scale: float | 
     if with_mass:
         ps = torch.empty(q.shape[:-1], dtype=torch.float32, device=q.device)
         pr = torch.empty_like(ps)
-    _check(lib().kvq_attention_corrected_noalloc(
-        ctypes.byref(cache.struct), _ptr(q), _ptr(k_cur), _ptr(v_cur), n_q, n_r,
-        ctypes.c_float(scale), corr, flags, _ptr(out), _ptr(ps), _ptr(pr), _stream(stream)),
-        "kvq_attention_corrected_noalloc")
+    with _on_device(q.device):
+        _check(lib().kvq_attention_corrected_noalloc(
+            ctypes.byref(cache.struct), _ptr(q), _ptr(k_cur), _ptr(v_cur), n_q, n_r,
+            ctypes.c_float(scale), corr, flags, _ptr(out), _ptr(ps), _ptr(pr),
+            _stream(stream, q.device)), "kvq_attention_corrected_noalloc")
     return (out, ps, pr) if with_mass else out
 
 
@@ -336,14 +358,15 @@ def attention_mass(cache: KVCache, q, k_cur, scale: float | None = None,
     scale = 1.0 / math.sqrt(cache.head_dim) if scale is None else scale
     ps = torch.empty(q.shape[:-1], dtype=torch.float32, device=q.device)
     pr = torch.empty_like(ps)
-    ws_bytes = cache.workspace_bytes(n_q, n_r)
-    if workspace is None:
-        workspace = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=q.device)
-    ws_ptr, ws_size = _workspace_arg(workspace, q.device)
-    _check(lib().kvq_attention_mass(
-        ctypes.byref(cache.struct), _ptr(q), _ptr(k_cur), n_q, n_r, ctypes.c_float(scale), corr,
-        flags, ws_ptr, ws_size, _ptr(ps), _ptr(pr), _stream(stream)),
-        "kvq_attention_mass")
+    with _on_device(q.device):
+        ws_bytes = cache.workspace_bytes(n_q, n_r)
+        if workspace is None:
+            workspace = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=q.device)
+        ws_ptr, ws_size = _workspace_arg(workspace, q.device)
+        _check(lib().kvq_attention_mass(
+            ctypes.byref(cache.struct), _ptr(q), _ptr(k_cur), n_q, n_r, ctypes.c_float(scale),
+            corr, flags, ws_ptr, ws_size, _ptr(ps), _ptr(pr), _stream(stream, q.device)),
+            "kvq_attention_mass")
     return ps, pr
 
 
@@ -360,13 +383,17 @@ def rotate(x: torch.Tensor, signs, out_dtype=torch.float32, stream=None) -> torc
         raise ValueError("out_dtype must be float32 or float16")
     f32 = out if out_dtype == torch.float32 else None
     f16 = out if out_dtype == torch.float16 else None
-    _check(lib().kvq_rotate(_ptr(x), rows, d, sb, _ptr(f32), _ptr(f16), _stream(stream)),
-           "kvq_rotate")
+    with _on_device(x.device):
+        _check(lib().kvq_rotate(_ptr(x), rows, d, sb, _ptr(f32), _ptr(f16),
+                                _stream(stream, x.device)), "kvq_rotate")
     return out
 
 
-def last_device_status(stream=None) -> int:
-    return int(lib().kvq_last_device_status(_stream(stream)))
+def last_device_status(stream=None, device=None) -> int:
+    """kvq_last_device_status on ``device`` (default: the current device)."""
+    dev = None if device is None else torch.device(device)
+    with _on_device(dev):
+        return int(lib().kvq_last_device_status(_stream(stream, dev)))
 
 
 def set_wait_limit_ns(limit_ns: int):

@@ -39,8 +39,9 @@ def test_exports_every_declared_symbol(lib):
 
 
 def test_status_strings(lib):
-    for s in range(7):
-        assert kvq.status_string(s)
+    for s in range(9):
+        assert kvq.status_string(s) != "unknown status"
+    assert "FP16" in kvq.status_string(kvq.KVQ_ERR_RANGE)
     assert kvq.status_string(99) == "unknown status"
 
 
@@ -185,6 +186,58 @@ def test_noalloc_rejects_problems_beyond_its_scratch(lib):
                                              None, None)
     assert st == kvq.KVQ_ERR_TOO_LARGE
     assert "scratch" in kvq.status_string(st)
+
+
+def _unsplit_scratch(bh, n_q, n_r, d, kch_tiles=0):
+    """Bytes of the unsplit launch's scratch as kvq.h defines it: the rotated
+    query as FP16 high and low parts and the rotated current values (each
+    region rounded up to 256 bytes), plus the per-channel key table."""
+    up = lambda x: -(-x // 256) * 256
+    return 2 * up(bh * n_q * d * 2) + up(bh * n_r * d * 2) + up(kch_tiles * bh * n_q * 4)
+
+
+def test_noalloc_refusal_is_the_unsplit_scratch_of_the_current_window(lib):
+    """The allocation-free entry point refuses a problem exactly when the
+    unsplit launch's scratch exceeds its buffer, not when
+    kvq_workspace_bytes (sized for the split of a full window) does: just
+    below the bound the call passes the size check (and, with no GPU here,
+    fails at its first CUDA call instead); just above it is refused."""
+    P = 0x10000
+    c = _cache(len=30, heads=64)
+    bh, d, n_r = 64, 128, 16
+    # largest n_q whose unsplit scratch fits the 32 MiB buffer
+    n_q = max(n for n in range(1000, 1200) if _unsplit_scratch(bh, n, n_r, d) <= kvq.NOALLOC_SCRATCH_BYTES)
+    assert _unsplit_scratch(bh, n_q + 1, n_r, d) > kvq.NOALLOC_SCRATCH_BYTES
+    args = lambda n: (ctypes.byref(c), P, P, P, n, n_r, 0.1, 1, 0, P, None, None, None)
+    assert lib.kvq_attention_corrected_noalloc(*args(n_q)) != kvq.KVQ_ERR_TOO_LARGE
+    assert lib.kvq_attention_corrected_noalloc(*args(n_q + 1)) == kvq.KVQ_ERR_TOO_LARGE
+    # per-channel keys: the table of the cached key blocks of the current
+    # window counts too (30 tokens in 3 slots of 10: one block each)
+    ch = _cache(len=30, heads=64, key_mode=kvq.KEYS_PER_CHANNEL)
+    n_q = max(n for n in range(900, 1200)
+              if _unsplit_scratch(bh, n, n_r, d, 3) <= kvq.NOALLOC_SCRATCH_BYTES)
+    argc = lambda n: (ctypes.byref(ch), P, P, P, n, n_r, 0.1, 1, 0, P, None, None, None)
+    assert lib.kvq_attention_corrected_noalloc(*argc(n_q)) != kvq.KVQ_ERR_TOO_LARGE
+    assert lib.kvq_attention_corrected_noalloc(*argc(n_q + 1)) == kvq.KVQ_ERR_TOO_LARGE
+
+
+def test_binding_makes_the_tensors_device_current():
+    """The library launches on the current device and looks its status word
+    up there: the binding switches to the tensors' device for each call and
+    refuses a stream of another device (checked without running a kernel)."""
+    import torch
+    assert isinstance(kvq._on_device(torch.device("cpu")), type(__import__("contextlib").nullcontext()))
+    assert isinstance(kvq._on_device(None), type(__import__("contextlib").nullcontext()))
+    g = kvq._on_device(torch.device("cuda", 1))
+    assert isinstance(g, torch.cuda.device) and g.idx == 1
+
+    class FakeStream:
+        device = torch.device("cuda", 1)
+        cuda_stream = 1234
+
+    with pytest.raises(ValueError, match="stream belongs to cuda:1"):
+        kvq._stream(FakeStream(), torch.device("cuda", 0))
+    assert kvq._stream(FakeStream(), torch.device("cuda", 1)).value == 1234
 
 
 def test_workspace_bytes_per_channel_keys(lib):

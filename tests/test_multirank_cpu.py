@@ -55,5 +55,23 @@ def test_reference_arm_runs_on_rank_zero_only(monkeypatch, capsys):
     monkeypatch.setenv("RANK", "1")
     calls = []
     monkeypatch.setattr(bench, "_oracle_sample", lambda *a, **k: calls.append(a) or (1.0, 1.0))
-    assert bench.main(["--impl", "reference", "--steps", "1", "--warmup", "0"]) is None
+    assert bench.main(["--gpus", "2", "--impl", "reference", "--steps", "1", "--warmup", "0"]) is None
     assert calls == [] and capsys.readouterr().out == ""
+
+
+def test_gpus_flag_must_match_the_launched_ranks(monkeypatch, capsys):
+    """--gpus N is honoured, not ignored: a run whose launcher started a
+    different number of ranks stops before any work (exit status 2), so a
+    replicas run cannot be reported under the wrong GPU count."""
+    import pytest
+
+    import bench
+    monkeypatch.delenv("WORLD_SIZE", raising=False)
+    with pytest.raises(SystemExit) as e:
+        bench.main(["--gpus", "2", "--impl", "reference", "--steps", "1"])
+    assert e.value.code == 2
+    assert "--nproc-per-node 2" in capsys.readouterr().err
+    assert bench.check_world(1, {}) == 1
+    assert bench.check_world(4, {"WORLD_SIZE": "4"}) == 4
+    with pytest.raises(SystemExit):
+        bench.check_world(8, {"WORLD_SIZE": "2"})

@@ -1,17 +1,20 @@
-"""The allocation-free attention entry point against the ordinary one.
+"""The allocation-free attention entry point against the ordinary one and the
+oracle.
 
 kvq_attention_corrected_noalloc serves callers that cannot allocate device
 memory when they call (its scratch is a fixed buffer inside the library).
 Through the C ABI, two calls in a row -- different problem sizes, so the
 second one runs over whatever the first left in the shared buffer -- must
 give what kvq_attention_corrected gives with a caller-allocated workspace,
-within the tolerances of the other attention tests.  Collected last, so a
-run that stops at its first failure has run everything else already."""
+within the tolerances of the other attention tests, and what the CPU oracle
+gives for every row of one head.  Collected last, so a run that stops at its
+first failure has run everything else already."""
+import numpy as np
 import pytest
 import torch
 
 from quantized_kv_cache_quantize_gb300 import kvq, synth
-from tests.gpu_common import MASS_TOL, O_TOL, build_cache
+from tests.gpu_common import MASS_TOL, O_TOL, assert_close, build_cache, oracle_head
 
 pytestmark = pytest.mark.gpu
 
@@ -22,10 +25,10 @@ def _case(name, heads, d, chunk, n_chunks, n_q, n_s, n_r, seed):
     x = synth.inputs(w, seed=seed, n_q=n_q, n_s=n_s, n_r=n_r)
     s = synth.hadamard_signs(d, seed=seed)
     cache = build_cache(w, x, s, n_s=n_s)
-    return cache, {k: v.cuda() for k, v in x.items()}
+    return cache, {k: v.cuda() for k, v in x.items()}, (w, x, s)
 
 
-def _compare(cache, x, flags):
+def _compare(cache, x, host, flags):
     ref_o, ref_ps, ref_pr = kvq.attention_corrected(cache, x["q"], x["k_cur"], x["v_cur"],
                                                     with_mass=True, flags=flags)
     o, ps, pr = kvq.attention_corrected_noalloc(cache, x["q"], x["k_cur"], x["v_cur"],
@@ -37,6 +40,12 @@ def _compare(cache, x, flags):
     assert err <= O_TOL * ref.abs().max().item()
     assert (ps - ref_ps).abs().max().item() <= MASS_TOL
     assert (pr - ref_pr).abs().max().item() <= MASS_TOL
+    # and the oracle, from the same seeded inputs, on every row of head 0
+    w, xh, s = host
+    rows = np.arange(xh["q"].shape[2])
+    o_ref, ps_ref, pr_ref = oracle_head(w, xh, s, 0, 0, rows, kvq.CORR_TAYLOR)
+    assert_close(o[0, 0].float().cpu().numpy(), o_ref, ps[0, 0].cpu().numpy(), ps_ref,
+                 pr[0, 0].cpu().numpy(), pr_ref, what="noalloc vs oracle")
 
 
 def test_noalloc_matches_workspace_entry_point_twice():
