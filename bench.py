@@ -489,8 +489,11 @@ def main(argv=None):
     ap.add_argument("--ref-rows", type=int, default=128,
                     help="query rows per step of the --impl reference sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--precise-query", dest="flags", action="store_const", const=1, default=0,
+    ap.add_argument("--precise-query", action="store_true",
                     help="split the rotated query into FP16 high + low parts")
+    ap.add_argument("--one-cta", action="store_true",
+                    help="run the one-CTA attention kernel where the SM-pair kernel applies "
+                         "(for comparisons)")
     ap.add_argument("--keys", choices=["token", "channel"], default="token",
                     help="key quantization: per token and group (default) or per channel over "
                          "128-token blocks of each chunk (KIVI-style)")
@@ -501,6 +504,7 @@ def main(argv=None):
     check_world(args.gpus)
     args.warmup = max(3, args.warmup)   # at least 3 untimed warm-up steps
     args.corr = {v: k for k, v in CORR_NAMES.items()}[args.corr]
+    args.flags = (1 if args.precise_query else 0) | (4 if args.one_cta else 0)
     args.key_mode = 1 if args.keys == "channel" else 0
     if args.impl == "reference":
         return run_reference(args)

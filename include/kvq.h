@@ -65,11 +65,22 @@ typedef enum {
  * Attention flags.
  * KVQ_FLAG_PRECISE_QUERY: the rotated query, a tensor-core operand of the
  *   cached-segment scores, is split into FP16 high and low parts and both are
- *   contracted with the cached keys (one extra QK^T pass on cached tiles,
- *   ~+40 % time).  Without it the rotated query carries one FP16 rounding
- *   (2^-11 relative), which moves a score by ~2^-12 of its magnitude: below
- *   1e-3 on the attention masses for moderate scores, but not for keys with
- *   extreme outliers (scores of order 100).  No counterpart in the paper.
+ *   contracted with the cached keys (one extra QK^T pass on cached tiles),
+ *   and the correction's factors get the same split, for every (batch,
+ *   head).  Without the flag a rotated query carries one FP16 rounding
+ *   (2^-11 relative), which moves a score by ~2^-12 of scale * |q'| |k'|:
+ *   below 1e-3 on the attention masses for moderate keys, but not for keys
+ *   with extreme outliers (scores of order 100).  So without the flag, for
+ *   head_dim 128 with per-token keys and the Taylor term or none, the
+ *   library decides per (batch, head), on the GPU and without a host
+ *   synchronization: a head takes the split when
+ *     scale * 2^-12 * max_j ||q'_j|| * max_i B_i >= 0.08,
+ *     B_i^2 = sum_g group * (max(|z_ig|, 2^bits - 1 - z_ig) D_ig)^2
+ *   (B_i bounds ||k_hat'_i|| from the cached key's steps and zero points).
+ *   The threshold is empirical: it separates Gaussian keys with outlier
+ *   channels (mass error <= 4e-4 without the split) from Student-t(3) keys
+ *   (up to 2.8e-3).  The other configurations take the split only with the
+ *   flag.  No counterpart in the paper.
  */
 #define KVQ_FLAG_PRECISE_QUERY 1
 /*
@@ -80,6 +91,14 @@ typedef enum {
  * split off (for comparisons).
  */
 #define KVQ_FLAG_NO_KV_SPLIT 2
+/*
+ * KVQ_FLAG_ONE_CTA: head_dim 128 with per-token keys and no correction or the
+ * Taylor term runs by default on SM pairs (two CTAs of a cluster share each
+ * key tile's dequantization and one M = 256 tensor-core MMA); this flag runs
+ * the one-CTA kernel instead (for comparisons).  Same results within the
+ * tolerances; an implementation choice of this library.
+ */
+#define KVQ_FLAG_ONE_CTA 4
 
 /*
  * Key quantization scheme of a cache (kvq_cache.key_mode).
@@ -192,8 +211,9 @@ kvq_status kvq_quantize_append(kvq_cache *cache, const uint16_t *k_new,
  * parts), the rotated current values (FP16), when the launch would not fill
  * the current device the partial results of the key-range split (fp32), and
  * with per-channel keys one fp32 per query row and cached key block (the
- * block's zero-point term minus the correction).  Depends on the current
- * device's SM count.  0 on a bad geometry.
+ * block's zero-point term minus the correction), and two floats per (batch,
+ * head) (the per-head choice of the precise-query split, below).  Depends on
+ * the current device's SM count.  0 on a bad geometry.
  */
 size_t kvq_workspace_bytes(const kvq_cache *cache, int32_t n_q, int32_t n_r);
 
@@ -218,7 +238,8 @@ size_t kvq_workspace_bytes(const kvq_cache *cache, int32_t n_q, int32_t n_r);
  *          (exact products, fp32 accumulation);
  *   one softmax over both segments; out = sum_i p_ij v_i in the ORIGINAL
  *   basis (cached values un-rotated).
- * flags: 0, KVQ_FLAG_PRECISE_QUERY, KVQ_FLAG_NO_KV_SPLIT or both.
+ * flags: any combination of KVQ_FLAG_PRECISE_QUERY, KVQ_FLAG_NO_KV_SPLIT and
+ * KVQ_FLAG_ONE_CTA (0 for none).
  * out: BF16 [batch][heads][n_q][d] device (required).  p_s, p_r: optional
  * (NULL to skip) fp32 [batch][heads][n_q] device: the attention masses of the
  * cached block and of the current chunk per query row (Figure 2 caption).
@@ -300,8 +321,9 @@ kvq_status kvq_selftest_wait_timeout(uint64_t limit_ns, void *stream);
  * loads the library holds it until the process exits.  The call is refused
  * with KVQ_ERR_TOO_LARGE, before anything is launched, when the scratch of
  * the unsplit launch for the cache's current window (the rotated query as
- * FP16 high and low parts, the rotated current values, and with
- * KVQ_KEYS_PER_CHANNEL one fp32 per query row and cached key block) exceeds
+ * FP16 high and low parts, the rotated current values, two floats per
+ * (batch, head), and with KVQ_KEYS_PER_CHANNEL one fp32 per query row and
+ * cached key block) exceeds
  * KVQ_NOALLOC_SCRATCH_BYTES; when it fits, the key-range split (which needs
  * room for partial results) takes the largest number of ranges whose
  * scratch still fits, down to none.  The limit is therefore not

@@ -100,6 +100,8 @@ struct Workspace {
   float* o_part;   // key-range split: partial O, fp32 (splits > 1)
   float* st_part;  // key-range split: base and sums per row (splits > 1)
   float* kch_c;    // per-channel keys: correction per row and cached tile
+  float* qn2;      // per head: max ||q'||^2 (the kernel choice of kModeAuto)
+  float* kn2;      // per head: max key-norm bound (the same)
   size_t bytes;
 };
 
@@ -117,6 +119,7 @@ Workspace carve(void* base, const kvq::Geometry& g, int n_q, int n_r, int splits
   const size_t ob = splits > 1 ? round_up((size_t)splits * g.bh * n_q * g.d * 4, 256) : 0;
   const size_t sb = splits > 1 ? round_up((size_t)splits * g.bh * n_q * 3 * 4, 256) : 0;
   const size_t cb = round_up((size_t)kch_tiles * g.bh * n_q * 4, 256);
+  const size_t nb = round_up((size_t)g.bh * 4, 256);
   uint8_t* p = static_cast<uint8_t*>(base);
   w.q_hi = reinterpret_cast<uint16_t*>(p);
   w.q_lo = reinterpret_cast<uint16_t*>(p + qb);
@@ -124,7 +127,9 @@ Workspace carve(void* base, const kvq::Geometry& g, int n_q, int n_r, int splits
   w.o_part = reinterpret_cast<float*>(p + 2 * qb + rb);
   w.st_part = reinterpret_cast<float*>(p + 2 * qb + rb + ob);
   w.kch_c = reinterpret_cast<float*>(p + 2 * qb + rb + ob + sb);
-  w.bytes = 2 * qb + rb + ob + sb + cb;
+  w.qn2 = reinterpret_cast<float*>(p + 2 * qb + rb + ob + sb + cb);
+  w.kn2 = reinterpret_cast<float*>(p + 2 * qb + rb + ob + sb + cb + nb);
+  w.bytes = 2 * qb + rb + ob + sb + cb + 2 * nb;
   return w;
 }
 
@@ -135,29 +140,21 @@ int device_sm_count() {
   return sms;
 }
 
-// key-range split of one launch (1 = none); rows per CTA: 256, or 128 with
-// the precise-query flag or the exact correction (one query tile per CTA)
-int split_for(const kvq::Geometry& g, int n_q, int n_ct, int n_r, bool one_tile, int sms,
-              int max_splits, int* per) {
-  int splits = 1;
-  kvq::attention_split(g.bh, n_q, n_ct, n_r, g.d, one_tile ? 128 : 256, sms, max_splits, &splits,
-                       per);
-  return splits;
-}
-
-// workspace for either CTA shape (two query tiles or one), with room for the
-// split the current device takes on a full window (n_s = the cache's
-// capacity); a shorter window whose best split needs more room takes the best
-// split that fits
+// workspace for any kernel shape (one-CTA or SM-pair kernel, one or two
+// query tiles per CTA), with room for the split the current device takes on
+// a full window (n_s = the cache's capacity); a shorter window whose best
+// split needs more room takes the best split that fits
 size_t workspace_bytes_any(const kvq::Geometry& g, int n_q, int n_ct, int n_r) {
   const int sms = device_sm_count();
   const int kch = g.key_mode == KVQ_KEYS_PER_CHANNEL ? n_ct : 0;
   size_t best = 0;
-  for (int one_tile = 0; one_tile < 2; ++one_tile) {
-    int per = 0;
-    const int sp = split_for(g, n_q, n_ct, n_r, one_tile != 0, sms, 64, &per);
-    const size_t b = carve(nullptr, g, n_q, n_r, sp, kch).bytes;
-    if (b > best) best = b;
+  for (int mode = kvq::kModeOneCta; mode <= kvq::kModePair; ++mode) {
+    for (int one_tile = 0; one_tile < 2; ++one_tile) {
+      const kvq::AttnShape sh =
+          kvq::attention_shape(g.bh, n_q, n_ct, n_r, g.d, mode, one_tile != 0, sms, 64);
+      const size_t b = carve(nullptr, g, n_q, n_r, sh.splits, kch).bytes;
+      if (b > best) best = b;
+    }
   }
   return best;
 }
@@ -173,7 +170,8 @@ kvq_status attention_common(const kvq_cache* cache, const uint16_t* q, const uin
   if (n_q < 0 || n_r < 0 || n_q > (1 << 30) || n_r > (1 << 30)) return KVQ_ERR_INVALID_ARG;
   if (corr != KVQ_CORR_NONE && corr != KVQ_CORR_TAYLOR && corr != KVQ_CORR_EXACT)
     return KVQ_ERR_INVALID_ARG;
-  if ((flags & ~(KVQ_FLAG_PRECISE_QUERY | KVQ_FLAG_NO_KV_SPLIT)) != 0) return KVQ_ERR_INVALID_ARG;
+  if ((flags & ~(KVQ_FLAG_PRECISE_QUERY | KVQ_FLAG_NO_KV_SPLIT | KVQ_FLAG_ONE_CTA)) != 0)
+    return KVQ_ERR_INVALID_ARG;
   const bool precise = (flags & KVQ_FLAG_PRECISE_QUERY) != 0;
   // one query tile per CTA: the precise-query split, or the exact correction
   // computed in the attention kernel (per-channel keys take it from a pre-pass)
@@ -201,25 +199,35 @@ kvq_status attention_common(const kvq_cache* cache, const uint16_t* q, const uin
   // per-channel keys: a table of one number per row and cached tile (the
   // zero-point term and the correction)
   const int kch_tiles = g.key_mode == KVQ_KEYS_PER_CHANNEL ? n_ct : 0;
-  int per = 0, splits = 1;
+  // the SM-pair kernel: head_dim 128, per-token keys, Taylor term or none;
+  // with the precise-query flag it runs alone, without it each head takes
+  // the pair kernel with the precise split or the one-CTA kernel without,
+  // as the GPU finds from the head's norms (kvq::kPreciseSelect)
+  const bool pair_ok = g.d == 128 && g.key_mode == KVQ_KEYS_PER_TOKEN && corr != KVQ_CORR_EXACT &&
+                       (flags & KVQ_FLAG_ONE_CTA) == 0;
+  const int mode = !pair_ok ? kvq::kModeOneCta : precise ? kvq::kModePair : kvq::kModeAuto;
+  int max_splits = 1;
   if ((flags & KVQ_FLAG_NO_KV_SPLIT) == 0) {
-    int max_splits = 64;
+    max_splits = 64;
     while (max_splits > 1 &&
            carve(nullptr, g, n_q, n_r, max_splits, kch_tiles).bytes > workspace_bytes)
       --max_splits;
-    splits = split_for(g, n_q, n_ct, n_r, one_tile, device_sm_count(), max_splits, &per);
   }
+  const kvq::AttnShape shape = kvq::attention_shape(g.bh, n_q, n_ct, n_r, g.d, mode, one_tile,
+                                                    device_sm_count(), max_splits);
+  const int splits = shape.splits, per = shape.tiles_per_split;
   const Workspace ws = carve(workspace, g, n_q, n_r, splits, kch_tiles);
   if (workspace_bytes < ws.bytes) return KVQ_ERR_INVALID_ARG;
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   int* status = kvq::status_ptr();
   if (status == nullptr) return KVQ_ERR_CUDA;
-  // rotate Q (FP16 hi, and lo when precise) and V_cur (FP16) into the workspace
+  // rotate Q (FP16 hi, and lo when the precise split may run) and V_cur
+  // (FP16) into the workspace
   kvq::RotateArgs ra{};
   ra.src[0] = q;
   ra.dst[0] = ws.q_hi;
-  ra.dst_lo[0] = precise ? ws.q_lo : nullptr;
+  ra.dst_lo[0] = (precise || mode == kvq::kModeAuto) ? ws.q_lo : nullptr;
   ra.rows[0] = (long long)g.bh * n_q;
   ra.src[1] = v_cur;
   ra.dst[1] = ws.v;
@@ -237,6 +245,12 @@ kvq_status attention_common(const kvq_cache* cache, const uint16_t* q, const uin
   ra.range_limit[1] = 65504.0f;
   {
     ProfScope prof(1, s);
+    // kModeAuto: the per-head norms that choose each head's kernel
+    if (mode == kvq::kModeAuto &&
+        kvq::launch_select_norms(reinterpret_cast<const uint32_t*>(cache->k_sz), q, g.bh,
+                                 cache->len, g.cap, n_q, g.g, g.group, g.bits, ws.kn2, ws.qn2,
+                                 s) != cudaSuccess)
+      return KVQ_ERR_CUDA;
     if (kvq::launch_rotate(ra, g.d, s) != cudaSuccess) return KVQ_ERR_CUDA;
   }
 
@@ -274,6 +288,9 @@ kvq_status attention_common(const kvq_cache* cache, const uint16_t* q, const uin
   a.kblk_per_head = cache->n_chunks * g.bpc;
   a.n_ct = n_ct;
   a.kch_c = kch_tiles > 0 ? ws.kch_c : nullptr;
+  a.mode = shape.mode;
+  a.qn2 = ws.qn2;
+  a.kn2 = ws.kn2;
   ProfScope prof(2, s);
   return kvq::launch_attention(a, g.d, g.bits, g.group, s);
 }

@@ -93,7 +93,22 @@ struct AttnParams {
   int chunk, bpc, kblk_per_head, n_ct;
   const float* kch_c;
   int* status;      // device status word (first error of a bounded wait)
+  // per-head kernel choice (two kernels share one call): select = 0 runs
+  // every (batch, head); +1 only the heads whose precise-query criterion
+  // holds, -1 only the others (criterion: select_scale * sqrt(qn2 * kn2)
+  // >= kPreciseSelect)
+  int select;
+  float select_scale;
+  const float* qn2;
+  const float* kn2;
 };
+
+// whether this CTA's (batch, head) belongs to the other kernel of the call
+__device__ __forceinline__ bool head_not_mine(const AttnParams& p, int bh) {
+  if (p.select == 0) return false;
+  const bool precise = !(p.select_scale * sqrtf(p.qn2[bh] * p.kn2[bh]) < kPreciseSelect);
+  return precise != (p.select > 0);
+}
 
 constexpr int kBlockM = 128;
 constexpr int kBlockN = 128;
@@ -556,6 +571,8 @@ __global__ void __launch_bounds__(Cfg<D, NQ, PRECISE, EXACT, KCH>::kThreads, 1)
   const int lane = tid & 31;
   const int q0 = blockIdx.x * (kBlockM * NQ);
   const int bh = blockIdx.y;
+  // a head the call gives to the other kernel: nothing set up yet, leave
+  if (head_not_mine(p, bh)) return;
 
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kBar);
   volatile int* abort = reinterpret_cast<volatile int*>(smem + C::kBar + kAbortOffset);
@@ -1528,14 +1545,15 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// 3-D map over a [bh][n][d] 16-bit tensor, box [1][128][64], 128-byte
+// 3-D map over a [bh][n][d] 16-bit tensor, box [1][box_rows][64], 128-byte
 // swizzle, zero fill outside the tensor.
-bool make_map(CUtensorMap* m, const void* base, int d, int n, int bh, bool bf16) {
+bool make_map(CUtensorMap* m, const void* base, int d, int n, int bh, bool bf16,
+              int box_rows = 128) {
   auto fn = encode_fn();
   if (fn == nullptr) return false;
   cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)n, (cuuint64_t)bh};
   cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)n * d * 2};
-  cuuint32_t box[3] = {64, 128, 1};
+  cuuint32_t box[3] = {64, (cuuint32_t)box_rows, 1};
   cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = fn(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
                   const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -1544,8 +1562,30 @@ bool make_map(CUtensorMap* m, const void* base, int d, int n, int bh, bool bf16)
   return r == CUDA_SUCCESS;
 }
 
+// the merge of a key-range split's partial results (one launch)
+template <int D>
+kvq_status launch_merge(const AttnLaunch& a, float inv_sqrt_d, cudaStream_t stream) {
+  MergeArgs m;
+  m.o_part = a.o_part;
+  m.st_part = a.st_part;
+  m.splits = a.splits;
+  m.rows = (long long)a.bh * a.n_q;
+  m.out = a.out;
+  m.p_s = a.p_s;
+  m.p_r = a.p_r;
+  for (int i = 0; i < 4; ++i) m.sign_bits[i] = a.sign_bits[i];
+  m.inv_sqrt_d = inv_sqrt_d;
+  m.mass_only = a.mass_only;
+  const long long warps = (m.rows + (32 / (D / 8)) - 1) / (32 / (D / 8));
+  const unsigned blocks = (unsigned)((warps + 7) / 8);
+  merge_splits_kernel<D><<<blocks, 256, 0, stream>>>(m);
+  return cudaGetLastError() == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
+}
+
+// One launch of the one-CTA kernel (the dispatcher launches the merge of a
+// key-range split); select as in AttnParams.
 template <int D, int BITS, int GROUP, int NQ, bool PRECISE, bool EXACT, bool KCH>
-kvq_status launch_t(const AttnLaunch& a, cudaStream_t stream) {
+kvq_status launch_t(const AttnLaunch& a, cudaStream_t stream, int select = 0) {
   using C = Cfg<D, NQ, PRECISE, EXACT, KCH>;
   static std::atomic<uint64_t> limit_set{0};   // per template instance and device
   auto kern = attn_kernel<D, BITS, GROUP, NQ, PRECISE, EXACT, KCH>;
@@ -1565,7 +1605,7 @@ kvq_status launch_t(const AttnLaunch& a, cudaStream_t stream) {
     mk = mq;
     mv = mq;
   }
-  AttnParams p;
+  AttnParams p{};
   p.k_codes = a.k_codes;
   p.v_codes = a.v_codes;
   p.k_sz = a.k_sz;
@@ -1595,27 +1635,13 @@ kvq_status launch_t(const AttnLaunch& a, cudaStream_t stream) {
   p.n_ct = a.n_ct;
   p.kch_c = a.kch_c;
   p.status = a.status;
+  p.select = select;
+  p.select_scale = a.scale * (1.0f / 4096.0f);
+  p.qn2 = a.qn2;
+  p.kn2 = a.kn2;
   dim3 grid((a.n_q + kBlockM * NQ - 1) / (kBlockM * NQ), a.bh, split ? a.splits : 1);
   kern<<<grid, C::kThreads, C::kAlloc, stream>>>(mq, mqlo, mqo, mk, mv, p);
-  if (cudaGetLastError() != cudaSuccess) return KVQ_ERR_CUDA;
-  if (split) {
-    MergeArgs m;
-    m.o_part = a.o_part;
-    m.st_part = a.st_part;
-    m.splits = a.splits;
-    m.rows = (long long)a.bh * a.n_q;
-    m.out = a.out;
-    m.p_s = a.p_s;
-    m.p_r = a.p_r;
-    for (int i = 0; i < 4; ++i) m.sign_bits[i] = a.sign_bits[i];
-    m.inv_sqrt_d = p.inv_sqrt_d;
-    m.mass_only = a.mass_only;
-    const long long warps = (m.rows + (32 / (D / 8)) - 1) / (32 / (D / 8));
-    const unsigned blocks = (unsigned)((warps + 7) / 8);
-    merge_splits_kernel<D><<<blocks, 256, 0, stream>>>(m);
-    if (cudaGetLastError() != cudaSuccess) return KVQ_ERR_CUDA;
-  }
-  return KVQ_OK;
+  return cudaGetLastError() == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
 }
 
 }  // namespace

@@ -162,6 +162,12 @@ struct AttnLaunch {
   int key_mode, chunk, bpc, kblk_per_head, n_ct;
   float* kch_c;
   int* status;      // device status word, set by launch_attention
+  // kernels (attention_shape): kModeOneCta / kModePair / kModeAuto; with
+  // kModeAuto the per-head maxima of ||q'||^2 and of the key-norm bound
+  // (workspace, [bh] each) that pick each head's kernel
+  int mode;
+  const float* qn2;
+  const float* kn2;
 };
 
 // cached key tiles of a window of n_s tokens: 128-token tiles, or with
@@ -185,29 +191,86 @@ inline int cached_tiles(int key_mode, int n_s, int chunk, int bpc) {
 constexpr int kCtaFixed = 2;
 constexpr double kBytesPerTileTime = 12e6;
 
+// CTAs of one unsplit launch: one per (head, block of rows_per_cta query
+// rows), or with SM pairs two per block of 2 * rows_per_cta rows
+inline long long attention_ctas(long long bh, int n_q, int rows_per_cta, bool pair) {
+  if (!pair) return bh * ((n_q + rows_per_cta - 1) / rows_per_cta);
+  return 2 * bh * ((n_q + 2 * rows_per_cta - 1) / (2 * rows_per_cta));
+}
+
+// cost: when not null, the estimated time of the chosen plan in tile-times
+// (of a CTA of this shape)
 inline void attention_split(long long bh, int n_q, int n_ct, int n_r, int d, int rows_per_cta,
-                            int sms, int max_splits, int* splits, int* tiles_per_split) {
+                            int sms, int max_splits, int* splits, int* tiles_per_split,
+                            bool pair = false, double* cost = nullptr) {
   const int n_t = n_ct + (n_r + 127) / 128;
   *splits = 1;
   *tiles_per_split = n_t > 0 ? n_t : 1;
-  const long long ctas = bh * ((n_q + rows_per_cta - 1) / rows_per_cta);
+  const long long ctas = attention_ctas(bh, n_q, rows_per_cta, pair);
+  const long long waves1 = sms > 0 ? (ctas + sms - 1) / sms : 1;
+  double best = (double)waves1 * (n_t + kCtaFixed);
+  if (cost != nullptr) *cost = best;
   if (n_t < 4 || ctas <= 0 || sms <= 0 || max_splits < 2) return;
   int lim = n_t / 2;
   if (lim > 64) lim = 64;
   if (lim > max_splits) lim = max_splits;
-  double best = (double)((ctas + sms - 1) / sms) * (n_t + kCtaFixed);
   const double row_bytes = 2.0 * (double)bh * n_q * (4.0 * d + 12.0);
   for (int sp = 2; sp <= lim; ++sp) {
     const int per = (n_t + sp - 1) / sp;
     const int used = (n_t + per - 1) / per;
-    const double cost = (double)((ctas * used + sms - 1) / sms) * (per + kCtaFixed) + 1.0 +
-                        used * row_bytes / kBytesPerTileTime;
-    if (cost < best) {
-      best = cost;
+    const double c = (double)((ctas * used + sms - 1) / sms) * (per + kCtaFixed) + 1.0 +
+                     used * row_bytes / kBytesPerTileTime;
+    if (c < best) {
+      best = c;
       *splits = used;
       *tiles_per_split = per;
     }
   }
+  if (cost != nullptr) *cost = best;
+}
+
+// Kernels of one attention call (head_dim, key mode and correction decide):
+//   kModeOneCta  the one-CTA kernel alone: two query tiles per CTA, or one
+//                with the precise-query split or the exact correction;
+//   kModePair    the SM-pair kernel alone (kvq_attn_pair.cuh: head_dim 128,
+//                per-token keys, Taylor term or none) with the precise-query
+//                split, two query tiles per CTA;
+//   kModeAuto    both, each (batch, head) run by one of them: heads whose
+//                FP16 query rounding can move the masses noticeably take the
+//                pair kernel with the precise split, the others the one-CTA
+//                kernel (the choice is made on the GPU from per-head norms,
+//                see kPreciseSelect).
+// Both kernels hold 256 query rows per SM and share one key-range split.
+enum : int { kModeOneCta = 0, kModePair = 1, kModeAuto = 2 };
+
+// Per-head choice of the precise-query split in kModeAuto.  A rotated query
+// q' carries one FP16 rounding per channel (|dq_c| <= 2^-11 |q'_c|), so a
+// cached score moves by scale * dq . k' and the masses by a fraction of
+// that.  The GPU evaluates, per (batch, head),
+//   e = scale * 2^-12 * max_j ||q'_j|| * B,
+//   B^2 = max over cached keys of sum_g group * (max(|z_g|, 2^bits-1-z_g) D_g)^2
+// (an upper bound of ||k_hat'||^2 from the keys' steps and zero points), and
+// takes the precise split when e >= kPreciseSelect.  This is an empirical
+// criterion: on the synthetic workloads e is at most 0.042 where keys are
+// Gaussian with outlier channels (mass error of the FP16 query <= 3.8e-4)
+// and at least 0.27 where keys are Student-t(3) (mass error up to 2.8e-3
+// without the split); the threshold sits between them.  Callers that want
+// the split regardless pass KVQ_FLAG_PRECISE_QUERY.
+constexpr float kPreciseSelect = 0.08f;
+
+struct AttnShape {
+  int mode;             // kModeOneCta, kModePair or kModeAuto
+  int nq;               // one-CTA kernel: query tiles of 128 rows per CTA
+  int splits, tiles_per_split;
+};
+inline AttnShape attention_shape(long long bh, int n_q, int n_ct, int n_r, int d, int mode,
+                                 bool one_tile, int sms, int max_splits) {
+  AttnShape sh{mode, mode == kModeOneCta && one_tile ? 1 : 2, 1, 1};
+  // kModeAuto plans for the one-CTA grid (the pair kernel runs the same
+  // ranges over its own grid)
+  attention_split(bh, n_q, n_ct, n_r, d, 128 * sh.nq, sms, max_splits, &sh.splits,
+                  &sh.tiles_per_split, mode == kModePair);
+  return sh;
 }
 
 kvq_status launch_attention(const AttnLaunch& a, int d, int bits, int group,
@@ -220,6 +283,17 @@ int* status_ptr();
 kvq_status launch_attention_exact(const AttnLaunch& a, int d, int bits, int group,
                                   cudaStream_t stream);
 kvq_status launch_attention_kch(const AttnLaunch& a, int d, int bits, int group,
+                                cudaStream_t stream);
+// the SM-pair kernel with the precise-query split (head_dim 128; a.status
+// must be set); select: 0 every head, +1 only the heads kModeAuto gives it
+kvq_status launch_attention_pair(const AttnLaunch& a, int bits, int group, int select,
+                                 cudaStream_t stream);
+// kModeAuto: per (batch, head) the two maxima of kPreciseSelect -- kn2[bh]
+// the bound B^2 over the head's cached keys, qn2[bh] = max_j ||q_j||^2 over
+// its queries (= ||q'_j||^2: the rotation is orthogonal) -- from the cache's
+// steps and zero points and the BF16 queries q [bh][n_q][128].
+cudaError_t launch_select_norms(const uint32_t* k_sz, const uint16_t* q, int bh, int n_s, int cap,
+                                int n_q, int g, int group, int bits, float* kn2, float* qn2,
                                 cudaStream_t stream);
 kvq_status read_and_clear_attention_status(int* status);
 cudaError_t launch_wait_selftest(unsigned long long limit_ns, cudaStream_t stream);

@@ -36,6 +36,7 @@ CORR_TAYLOR = 1
 CORR_EXACT = 2
 FLAG_PRECISE_QUERY = 1
 FLAG_NO_KV_SPLIT = 2
+FLAG_ONE_CTA = 4
 
 
 class KVQError(RuntimeError):

@@ -141,7 +141,7 @@ def test_attention_argument_checks(lib):
     # bad correction mode, bad flags, bad scale, missing output, workspace too small
     assert f(ctypes.byref(c), P, P, P, 100, 10, 0.1, 7, 0, P, ws, P, None, None, None) == 1
     assert f(ctypes.byref(c), P, P, P, 100, 10, 0.1, 3, 0, P, ws, P, None, None, None) == 1
-    assert f(ctypes.byref(c), P, P, P, 100, 10, 0.1, 1, 6, P, ws, P, None, None, None) == 1
+    assert f(ctypes.byref(c), P, P, P, 100, 10, 0.1, 1, 8, P, ws, P, None, None, None) == 1
     assert f(ctypes.byref(c), P, P, P, 100, 10, float("nan"), 1, 0, P, ws, P, None, None, None) == 1
     assert f(ctypes.byref(c), P, P, P, 100, 10, -1.0, 1, 0, P, ws, P, None, None, None) == 1
     assert f(ctypes.byref(c), P, P, P, 100, 10, 0.1, 1, 0, P, ws, None, None, None, None) == 1
@@ -191,9 +191,11 @@ def test_noalloc_rejects_problems_beyond_its_scratch(lib):
 def _unsplit_scratch(bh, n_q, n_r, d, kch_tiles=0):
     """Bytes of the unsplit launch's scratch as kvq.h defines it: the rotated
     query as FP16 high and low parts and the rotated current values (each
-    region rounded up to 256 bytes), plus the per-channel key table."""
+    region rounded up to 256 bytes), the per-channel key table, and two
+    floats per (batch, head) for the per-head kernel choice."""
     up = lambda x: -(-x // 256) * 256
-    return 2 * up(bh * n_q * d * 2) + up(bh * n_r * d * 2) + up(kch_tiles * bh * n_q * 4)
+    return (2 * up(bh * n_q * d * 2) + up(bh * n_r * d * 2) + up(kch_tiles * bh * n_q * 4)
+            + 2 * up(bh * 4))
 
 
 def test_noalloc_refusal_is_the_unsplit_scratch_of_the_current_window(lib):
@@ -324,7 +326,7 @@ def test_binding_mirrors_the_header():
     consts.update((k, int(v)) for k, v in re.findall(r"#define\s+(KVQ_[A-Z0-9_]+)\s+(\d+)", src))
     py = {"KVQ_CORR_NONE": kvq.CORR_NONE, "KVQ_CORR_TAYLOR": kvq.CORR_TAYLOR,
           "KVQ_CORR_EXACT": kvq.CORR_EXACT, "KVQ_FLAG_PRECISE_QUERY": kvq.FLAG_PRECISE_QUERY,
-          "KVQ_FLAG_NO_KV_SPLIT": kvq.FLAG_NO_KV_SPLIT,
+          "KVQ_FLAG_NO_KV_SPLIT": kvq.FLAG_NO_KV_SPLIT, "KVQ_FLAG_ONE_CTA": kvq.FLAG_ONE_CTA,
           "KVQ_KEYS_PER_TOKEN": kvq.KEYS_PER_TOKEN, "KVQ_KEYS_PER_CHANNEL": kvq.KEYS_PER_CHANNEL,
           "KVQ_KEY_BLOCK": kvq.KEY_BLOCK}
     py.update((k, getattr(kvq, k)) for k in consts if k.startswith(("KVQ_OK", "KVQ_ERR_")))

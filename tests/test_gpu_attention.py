@@ -116,13 +116,16 @@ def test_correction_restores_mass():
 
 @pytest.mark.parametrize("name,flags", [("w4_int2", 0), ("w4_int4", 0), ("w8_int2", 0),
                                         ("w4_int2", kvq.FLAG_PRECISE_QUERY),
+                                        ("w4_int2", kvq.FLAG_ONE_CTA),
+                                        ("hires_t3", 0),
                                         ("hires_t3", kvq.FLAG_PRECISE_QUERY)])
 def test_full_workload_sampled_rows(name, flags):
     """Full-size workloads in the launch configuration the benchmark times:
     all heads, 48 sampled query rows per head (always including the first
     and last rows) against the oracle.  The heavy-tailed high-resolution case
     (scores of order 100) needs the precise-query split to hold the 1e-3 mass
-    bound; the others hold it without."""
+    bound: the default call (flags 0) picks it per head on the GPU, the flag
+    forces it; the Gaussian-key workloads hold the bound without it."""
     w = synth.WORKLOADS[name]
     x = synth.inputs(w)
     s = synth.hadamard_signs(w.head_dim)
@@ -138,6 +141,42 @@ def test_full_workload_sampled_rows(name, flags):
         o_ref, ps_ref, pr_ref = oracle_head(w, x, s, 0, int(h), rows, O.CORR_TAYLOR)
         assert_close(out[0, h, rows].float().cpu().numpy(), o_ref, ps[0, h, rows].cpu().numpy(),
                      ps_ref, pr[0, h, rows].cpu().numpy(), pr_ref, what=f"{name} h{h}")
+
+
+def test_precise_split_chosen_per_head():
+    """Default call, one head with Gaussian keys and one with Student-t(3)
+    keys and x12 outlier channels: the GPU gives the first head to the
+    one-CTA kernel without the precise split (its output is bit for bit that
+    of a call forced onto that kernel) and the second to the SM-pair kernel
+    with the split (bit for bit that of a call with the precise flag), and
+    both heads match the oracle."""
+    common = dict(head_dim=128, chunk_tokens=256, n_chunks=4, bits=2, group=32)
+    wg = synth.Workload("gauss", heads=1, n_outliers_fixed=3, outlier_scale=10.0, offset_std=0.5,
+                        **common)
+    wt = synth.Workload("t3", heads=1, key_dist="t3", n_outliers_fixed=2, outlier_scale=12.0,
+                        **common)
+    sizes = dict(n_q=600, n_s=1024, n_r=256)
+    xg, xt = synth.inputs(wg, seed=5, **sizes), synth.inputs(wt, seed=6, **sizes)
+    x = {k: torch.cat([xg[k], xt[k]], dim=1).contiguous() for k in xg}
+    w = synth.Workload("mixed", heads=2, **common)
+    s = synth.hadamard_signs(128, seed=5)
+    cache = build_cache(w, x, s)
+    args = (cache, x["q"].cuda(), x["k_cur"].cuda(), x["v_cur"].cuda())
+    split = kvq.FLAG_NO_KV_SPLIT
+    auto = kvq.attention_corrected(*args, with_mass=True, flags=split)
+    one_cta = kvq.attention_corrected(*args, with_mass=True, flags=split | kvq.FLAG_ONE_CTA)
+    precise = kvq.attention_corrected(*args, with_mass=True, flags=split | kvq.FLAG_PRECISE_QUERY)
+    torch.cuda.synchronize()
+    assert kvq.last_device_status() == 0
+    for a, b in zip(auto, one_cta):
+        assert torch.equal(a[0, 0], b[0, 0])
+    for a, b in zip(auto, precise):
+        assert torch.equal(a[0, 1], b[0, 1])
+    rows = np.arange(sizes["n_q"])
+    for h in range(2):
+        o_ref, ps_ref, pr_ref = oracle_head(w, x, s, 0, h, rows, O.CORR_TAYLOR)
+        assert_close(auto[0][0, h].float().cpu().numpy(), o_ref, auto[1][0, h].cpu().numpy(), ps_ref,
+                     auto[2][0, h].cpu().numpy(), pr_ref, what=f"mixed h{h}")
 
 
 def test_bounded_wait_reports_timeout():

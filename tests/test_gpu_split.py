@@ -72,8 +72,10 @@ def test_split_workspace_and_small_workspace():
     (the launch falls back to one range)."""
     case = SPLIT[1]
     w, x, s, cache = _setup(case, seed=9)
-    d, n_q, n_r = case[0], case[3], case[5]
-    unsplit = 2 * ((n_q * d * 2 + 255) // 256 * 256) + (n_r * d * 2 + 255) // 256 * 256
+    d, n_q, n_r, bh = case[0], case[3], case[5], case[8]
+    up = lambda b: (b + 255) // 256 * 256
+    # rotated query (high, low), rotated current values, two floats per head
+    unsplit = 2 * up(bh * n_q * d * 2) + up(bh * n_r * d * 2) + 2 * up(bh * 4)
     assert cache.workspace_bytes(n_q, n_r) > unsplit
     q, kc, vc = x["q"].cuda(), x["k_cur"].cuda(), x["v_cur"].cuda()
     small = torch.empty(unsplit, dtype=torch.uint8, device="cuda")
