@@ -308,6 +308,10 @@ def run_gpu(args):
     result = None
     if rank == 0:
         cpu = cpu_baseline(w, args) if (world == 1 and not args.no_cpu_baseline) else None
+        acc = None
+        if not args.no_accuracy:
+            same = w.name in ACCURACY_WORKLOADS and args.seed == 0
+            acc = accuracy_report(x if same else synth.inputs(_workload("w4_int2")), dev)
         ws_bytes = (w.append_bytes() + 2 * w.n_s * d * w.bits / 8 * B * H
                     + 3 * w.n_q * d * 2 * B * H)
         result = {
@@ -343,11 +347,116 @@ def run_gpu(args):
                          "traffic": _traffic_for_current_kernel(),
                          "kernel": "attention (fused corrected chunk attention)"},
             "cpu_baseline": cpu,
+            "accuracy": acc,
         }
         print(json.dumps(result), flush=True)
     if world > 1:
         dist.destroy_process_group()
     return result
+
+
+ACCURACY_REFS = os.path.join(ROOT, "tests", "golden", "accuracy_w4.npz")
+ACCURACY_WORKLOADS = ("w4_int2", "w4_int4")
+
+
+def _input_fingerprint(x: dict, h: int) -> str:
+    """SHA-256 over the BF16 bit patterns of head h's q, k_cur, v_cur, k_win,
+    v_win (as fp32, an exact widening): the key the stored answers carry."""
+    fp = hashlib.sha256()
+    for k in ("q", "k_cur", "v_cur", "k_win", "v_win"):
+        fp.update(x[k][0, h].float().numpy().tobytes())
+    return fp.hexdigest()
+
+
+def accuracy_report(x, dev, reps: int = 10):
+    """INT2 g32 against INT4 g64 on the same seeded inputs (24 heads, head_dim
+    128, 4680-token chunk, 18720-token window): for each cache and each
+    correction mode, the CUDA path's O and P_S / P_R on the sampled heads and
+    rows against the oracle's stored answers (tests/golden/accuracy_w4.npz,
+    written from the oracle alone by tests/golden/make_accuracy_refs.py), the
+    mean attention mass on the cache and its shift from the unquantized
+    window ("Quantized Keys Steal Attention": abstract, section 1, Figure 2),
+    and the attention's throughput with the default (Taylor) correction.
+    ``x``: the workload's seeded BF16 inputs (both caches use the same ones)."""
+    import numpy as np
+    import torch
+
+    from quantized_kv_cache_quantize_gb300 import kvq, synth
+
+    if not os.path.exists(ACCURACY_REFS):
+        return {"unavailable": "tests/golden/accuracy_w4.npz not found"}
+    z = np.load(ACCURACY_REFS)
+    signs = synth.hadamard_signs(128)
+    q, kc, vc = x["q"].to(dev), x["k_cur"].to(dev), x["v_cur"].to(dev)
+    rep = {"refs": "tests/golden/accuracy_w4.npz (oracle answers on sampled heads and rows)",
+           "metrics": "err_o = max|O - O_oracle| / max|O_oracle|; err_ps, err_pr = max abs "
+                      "error of the masses; ps_mean = mean P_S on the sampled rows; shift = "
+                      "ps_mean - the oracle's mean P_S over the unquantized BF16 window"}
+    for name in ACCURACY_WORKLOADS:
+        w = synth.WORKLOADS[name]
+        heads, rows = z[f"{name}/heads"], z[f"{name}/rows"]
+        entry = {"cache": f"INT{w.bits} g{w.group}",
+                 "heads": [int(h) for h in heads], "rows_per_head": int(len(rows))}
+        match = all(_input_fingerprint(x, int(h)) == str(z[f"{name}/fp"][i])
+                    for i, h in enumerate(heads))
+        entry["inputs_match_refs"] = bool(match)
+        cache = kvq.KVCache(w.batch, w.heads, w.head_dim, w.bits, w.group, w.chunk_tokens,
+                            w.n_chunks, signs, device=dev)
+        kw, vw = x["k_win"].to(dev), x["v_win"].to(dev)
+        for c in range(w.n_chunks):
+            sl = slice(c * w.chunk_tokens, (c + 1) * w.chunk_tokens)
+            kvq.quantize_append(cache, kw[:, :, sl].contiguous(), vw[:, :, sl].contiguous())
+        del kw, vw
+        ps_u = z[f"{name}/ps_unquantized"]
+        entry["ps_unquantized_mean"] = round(float(ps_u.mean()), 6)
+        for cname, corr in (("none", kvq.CORR_NONE), ("taylor", kvq.CORR_TAYLOR),
+                            ("exact", kvq.CORR_EXACT)):
+            out, ps, pr = kvq.attention_corrected(cache, q, kc, vc, corr=corr, with_mass=True)
+            torch.cuda.synchronize()
+            if kvq.last_device_status() != 0:
+                raise RuntimeError(f"device status after the {name} {cname} accuracy call")
+            idx = torch.as_tensor(rows, device=dev)
+            o_g = out[0][:, idx][torch.as_tensor(heads, device=dev)].float().cpu().numpy()
+            ps_g = ps[0][:, idx][torch.as_tensor(heads, device=dev)].cpu().numpy().astype(np.float64)
+            pr_g = pr[0][:, idx][torch.as_tensor(heads, device=dev)].cpu().numpy().astype(np.float64)
+            o_r = z[f"{name}/o_{cname}"].astype(np.float64)
+            entry[cname] = {
+                "err_o": float(f"{np.abs(o_g - o_r).max() / np.abs(o_r).max():.3e}"),
+                "err_ps": float(f"{np.abs(ps_g - z[f'{name}/ps_{cname}']).max():.3e}"),
+                "err_pr": float(f"{np.abs(pr_g - z[f'{name}/pr_{cname}']).max():.3e}"),
+                "ps_mean": round(float(ps_g.mean()), 6),
+                "shift": round(float(ps_g.mean() - ps_u.mean()), 6),
+            }
+        # throughput of the default call (Taylor correction) on this cache
+        out = torch.empty_like(q)
+        ps = torch.empty(q.shape[:-1], dtype=torch.float32, device=dev)
+        pr = torch.empty_like(ps)
+        ws = torch.empty(cache.workspace_bytes(w.n_q, w.n_r), dtype=torch.uint8, device=dev)
+        stream = torch.cuda.current_stream(dev)
+
+        def call():
+            kvq.lib().kvq_attention_corrected(
+                kvq.ctypes.byref(cache.struct), kvq._ptr(q), kvq._ptr(kc), kvq._ptr(vc), w.n_q,
+                w.n_r, kvq.ctypes.c_float(w.scale), kvq.CORR_TAYLOR, 0, kvq._ptr(ws), ws.numel(),
+                kvq._ptr(out), kvq._ptr(ps), kvq._ptr(pr), kvq._stream(stream))
+
+        for _ in range(3):
+            call()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(reps):
+            call()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / reps
+        entry["attention_ms"] = round(ms, 4)
+        entry["attention_tflops"] = round(w.attention_flops() / (ms * 1e-3) / 1e12, 2)
+        entry["cache_mb"] = round(w.batch * w.heads * w.n_s * 2 *
+                                  (w.head_dim * w.bits / 8 + 4 * w.head_dim / w.group) / 1e6, 2)
+        rep[name] = entry
+        del cache
+    return rep
 
 
 def _oracle_sample(w, head: int, rows: int, seed: int, corr: int = 1, key_mode: int = 0):
@@ -489,6 +598,9 @@ def main(argv=None):
     ap.add_argument("--ref-rows", type=int, default=128,
                     help="query rows per step of the --impl reference sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-accuracy", action="store_true",
+                    help="skip the INT2 g32 / INT4 g64 accuracy report (CUDA path against the "
+                         "oracle's stored answers, attention-mass shift, throughput)")
     ap.add_argument("--precise-query", action="store_true",
                     help="split the rotated query into FP16 high + low parts")
     ap.add_argument("--one-cta", action="store_true",

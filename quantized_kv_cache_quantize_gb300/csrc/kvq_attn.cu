@@ -55,9 +55,10 @@ kvq_status launch_one_cta(const AttnLaunch& a, int d, int bits, int group, cudaS
 // [0, key_blocks) of grid.x take kSelectTokens cached keys each: thread per
 // key, its G (step, zero) words in one load, B^2 = sum_g group *
 // (max(|z_g|, 2^bits - 1 - z_g) D_g)^2 >= ||k_hat'||^2.  The other blocks
-// take kSelectTokens query rows each: 16 lanes per row of 128 BF16 values,
-// ||q||^2 (= ||q'||^2).
+// take kSelectRows query rows each: 16 lanes per row of 128 BF16 values,
+// four rows per lane group in flight, ||q||^2 (= ||q'||^2).
 constexpr int kSelectTokens = 2048;
+constexpr int kSelectRows = 256;
 template <int G>
 __global__ void __launch_bounds__(256) select_norms_kernel(const uint32_t* k_sz, const uint16_t* q,
                                                            int n_s, int cap, int n_q,
@@ -91,26 +92,34 @@ __global__ void __launch_bounds__(256) select_norms_kernel(const uint32_t* k_sz,
       mx = fmaxf(mx, b * (float)group);
     }
   } else {
-    const int r0 = ((int)blockIdx.x - key_blocks) * kSelectTokens;
-    const int r1 = min(n_q, r0 + kSelectTokens);
+    const int r0 = ((int)blockIdx.x - key_blocks) * kSelectRows;
+    const int r1 = min(n_q, r0 + kSelectRows);
     const int sub = threadIdx.x & 15;   // 8 channels of the row
     const uint16_t* base = q + (size_t)bh * n_q * 128;
-    // every lane runs the same number of iterations (shuffles below)
-    for (int rb = r0; rb < r1; rb += 16) {
-      const int r = rb + (threadIdx.x >> 4);
-      float n2 = 0.f;
-      if (r < r1) {
-        const uint4 v = __ldg(reinterpret_cast<const uint4*>(base + (size_t)r * 128 + 8 * sub));
-        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    // every lane runs the same number of iterations (shuffles below); the
+    // 16-row steps of four iterations are loaded before any is reduced
+    constexpr int kU = 4;
+    for (int rb = r0; rb < r1; rb += 16 * kU) {
+      uint4 v[kU];
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+        const int r = rb + 16 * u + (threadIdx.x >> 4);
+        v[u] = r < r1 ? __ldg(reinterpret_cast<const uint4*>(base + (size_t)r * 128 + 8 * sub))
+                      : make_uint4(0u, 0u, 0u, 0u);
+      }
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+        const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+        float n2 = 0.f;
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           n2 = fmaf(bf16_lo(w[i]), bf16_lo(w[i]), n2);
           n2 = fmaf(bf16_hi(w[i]), bf16_hi(w[i]), n2);
         }
-      }
 #pragma unroll
-      for (int o = 1; o < 16; o <<= 1) n2 += __shfl_xor_sync(0xffffffffu, n2, o);
-      mx = fmaxf(mx, n2);
+        for (int o = 1; o < 16; o <<= 1) n2 += __shfl_xor_sync(0xffffffffu, n2, o);
+        mx = fmaxf(mx, n2);
+      }
     }
   }
 #pragma unroll
@@ -141,7 +150,7 @@ cudaError_t launch_select_norms(const uint32_t* k_sz, const uint16_t* q, int bh,
   if (e == cudaSuccess) e = cudaMemsetAsync(qn2, 0, (size_t)bh * sizeof(float), stream);
   if (e != cudaSuccess) return e;
   const int kblocks = (n_s + kSelectTokens - 1) / kSelectTokens;
-  const int qblocks = (n_q + kSelectTokens - 1) / kSelectTokens;
+  const int qblocks = (n_q + kSelectRows - 1) / kSelectRows;
   if (kblocks + qblocks == 0) return cudaSuccess;
   const dim3 grid((unsigned)(kblocks + qblocks), (unsigned)bh);
   const float qmax = (float)((1 << bits) - 1);
