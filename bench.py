@@ -245,8 +245,16 @@ def run_gpu(args):
     q_bytes = w.append_bytes()
     k1_gbs = q_bytes / (k1_ms * 1e-3) / 1e9
     # the rotation kernel reads the BF16 query and current values and writes
-    # them as FP16 (and the query's FP16 remainder with the precise split)
-    rot_bytes = (w.n_q + w.n_r) * d * B * H * 4.0 + (w.n_q * d * B * H * 2.0 if args.flags & 1 else 0.0)
+    # them as FP16, and the query's FP16 remainder whenever the precise split
+    # may run: with the flag, or in the per-head automatic choice (head_dim
+    # 128, per-token keys, Taylor or no correction, no one-CTA flag)
+    auto = (d == 128 and args.key_mode == 0 and args.corr != 2 and not args.flags & 4)
+    rot_bytes = (w.n_q + w.n_r) * d * B * H * 4.0 + \
+        (w.n_q * d * B * H * 2.0 if (args.flags & 1 or auto) else 0.0)
+    # in the automatic choice the same timed scope holds the per-head selection
+    # pass: it reads the window's (step, zero) words and the BF16 query
+    if auto:
+        rot_bytes += w.n_s * (d // w.group) * 4.0 * B * H + w.n_q * d * 2.0 * B * H
     launches = sum(v["launches"] for v in prof.values())
 
     # end to end through the public API with host buffers (pinned), copies inside the timed
@@ -339,6 +347,8 @@ def run_gpu(args):
             "quantize_gbs": round(k1_gbs, 1),
             "quantize_frac_of_hbm": round(k1_gbs / hbm, 4),
             "rotate_gbs": round(rot_bytes / (k2_ms * 1e-3) / 1e9, 1),
+            "rotate_frac_of_hbm": round(rot_bytes / (k2_ms * 1e-3) / 1e9 / hbm, 4),
+            "rotate_scope": "rotation of Q and V_R" + (" + per-head selection pass" if auto else ""),
             "roofline": {"bound": "tensor", "achieved": round(k3_tflops, 2),
                          "peak": peak, "unit": "TFLOP/s", "frac": round(k3_tflops / peak, 4),
                          "peak_source": f"{peak_kind} bf16 "

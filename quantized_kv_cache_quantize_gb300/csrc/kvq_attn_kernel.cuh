@@ -376,32 +376,38 @@ __device__ __forceinline__ uint64_t exp_chunk(const uint32_t (&s)[32], uint64_t 
 // E[exp(delta_ij)] = prod_c sinh(a_c) / a_c with a_c = (scale / 2) |q'_c| D_g(c),
 // so the exact correction is b_ij = sum_c f(a_c), f(a) = log(sinh(a) / a).
 // f has the power series f(a) = sum_k c_k a^(2k), c_k = 2^(2k) B_2k / (2k (2k)!)
-// (B_2k the Bernoulli numbers), convergent for a < pi.  For one query row and
-// group g with mu_g = max_{c in g} q'_c^2 and T = mu_g (scale D_g / 2)^2, the
-// group's term is sum_k c_k M_k T^k with the row's normalized moments
-// M_k = sum_{c in g} (q'_c^2 / mu_g)^k: a polynomial in the key's T, exact to
-// |c_8| T^8 <= 1.4e-9 per channel while T <= 1 (every a_c of the group <= 1).
-// Larger T takes the per-channel evaluation.
-constexpr int kSeriesTerms = 7;
-__host__ __device__ constexpr float sinhc_coef(int k) {   // c_(k+1)
-  return k == 0 ? 1.0f / 6.0f
-       : k == 1 ? -1.0f / 180.0f
-       : k == 2 ? 1.0f / 2835.0f
-       : k == 3 ? -1.0f / 37800.0f
-       : k == 4 ? 1.0f / 467775.0f
-       : k == 5 ? -691.0f / 3831077250.0f
-                : 2.0f / 127702575.0f;
+// (B_2k the Bernoulli numbers), convergent for a < pi.  The kernels use a
+// polynomial of the same form with kFitTerms terms p_k, the Chebyshev
+// interpolant of f(a) / a^2 on a^2 in [0, kFitTmax] rewritten in powers of
+// a^2 (sinhc_fit.py beside this header derives the constants): within
+// 3e-7 of f per channel for a <= 3.  For one query row and group g with
+// mu_g = max_{c in g} q'_c^2 and T = mu_g (scale D_g / 2)^2, the group's term
+// is then sum_k p_k M_k T^k with the row's normalized moments
+// M_k = sum_{c in g} (q'_c^2 / mu_g)^k: a polynomial in the key's T, valid
+// while T <= kFitTmax (every a_c of the group <= 3).  Larger T takes the
+// per-channel evaluation.
+constexpr int kFitTerms = 8;
+constexpr float kFitTmax = 9.0f;
+__host__ __device__ constexpr float sinhc_fit(int k) {    // p_(k+1)
+  return k == 0 ? 1.666666567e-01f
+       : k == 1 ? -5.555371288e-03f
+       : k == 2 ? 3.522899351e-04f
+       : k == 3 ? -2.603568646e-05f
+       : k == 4 ? 1.934644388e-06f
+       : k == 5 ? -1.229594915e-07f
+       : k == 6 ? 5.371698197e-09f
+                : -1.124628862e-10f;
 }
 constexpr float kLog2e = 1.4426950408889634f;
 
-// f(a) = log(sinh(a) / a) for a >= 0: the series above for a < 1, else
-// a + log((1 - exp(-2a)) / (2a))
+// f(a) = log(sinh(a) / a) for a >= 0: the fitted polynomial for a <= 3
+// (fused multiply-adds only), else a + log((1 - exp(-2a)) / (2a))
 __device__ __forceinline__ float log_sinhc(float a) {
-  if (a < 1.0f) {
-    const float t = a * a;
-    float p = sinhc_coef(kSeriesTerms - 1);
+  const float t = a * a;
+  if (t <= kFitTmax) {
+    float p = sinhc_fit(kFitTerms - 1);
 #pragma unroll
-    for (int k = kSeriesTerms - 2; k >= 0; --k) p = fmaf(p, t, sinhc_coef(k));
+    for (int k = kFitTerms - 2; k >= 0; --k) p = fmaf(p, t, sinhc_fit(k));
     return p * t;
   }
   return a + __logf(__fdividef(1.0f - __expf(-2.0f * a), a + a));
@@ -434,14 +440,14 @@ __device__ __forceinline__ uint64_t exp_chunk_b(const uint32_t (&s)[32], const u
 }
 
 // The exact correction of 32 cached keys for one query row, in log2 units
-// and negated (nb = -log2(e) b), by the series: dq points at the chunk's
-// (scale D_g / 2)^2 values ([group][128 keys] layout), mu2 / a2 hold the row's
-// mu_g and -log2(e) c_k M_k as packed pairs.  Valid for the keys whose
-// T = mu_g (scale D_g / 2)^2 <= 1 in every group; the others get whatever
-// the polynomial gives (exact_fix replaces them).
+// and negated (nb = -log2(e) b), by the fitted polynomial: dq points at the
+// chunk's (scale D_g / 2)^2 values ([group][128 keys] layout), mu2 / a2 hold
+// the row's mu_g and -log2(e) p_k M_k as packed pairs.  Valid for the keys
+// whose T = mu_g (scale D_g / 2)^2 <= kFitTmax in every group; the others get
+// whatever the polynomial gives (exact_fix replaces them).
 template <int G>
 __device__ __forceinline__ void exact_series(const float* dq, const uint64_t (&mu2)[G],
-                                             const uint64_t (&a2)[G][kSeriesTerms],
+                                             const uint64_t (&a2)[G][kFitTerms],
                                              uint64_t (&nb)[16]) {
 #pragma unroll
   for (int k = 0; k < 16; ++k) nb[k] = 0ull;   // (+0, +0)
@@ -453,23 +459,23 @@ __device__ __forceinline__ void exact_series(const float* dq, const uint64_t (&m
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         const uint64_t t2 = ptx::f2_mul(mu2[g], h ? ptx::f2_pack(d4.z, d4.w) : ptx::f2_pack(d4.x, d4.y));
-        uint64_t pp = a2[g][kSeriesTerms - 1];
+        uint64_t pp = a2[g][kFitTerms - 1];
 #pragma unroll
-        for (int i = kSeriesTerms - 2; i >= 0; --i) pp = ptx::f2_fma(pp, t2, a2[g][i]);
+        for (int i = kFitTerms - 2; i >= 0; --i) pp = ptx::f2_fma(pp, t2, a2[g][i]);
         nb[2 * k4 + h] = ptx::f2_fma(pp, t2, nb[2 * k4 + h]);
       }
     }
   }
 }
 
-// Keys of the chunk with T > 1 in some group (some a_c above 1): their term
-// is rebuilt from the series of the other groups and, for the groups above
-// the bound, the per-channel sum of log(sinh(a_c) / a_c) over the row's
-// rotated query in tensor memory (t_q, fp32).  Warp-collective (tensor
-// memory loads): called by whole warps.
+// Keys of the chunk with T > kFitTmax in some group (some a_c above 3):
+// their term is rebuilt from the polynomial of the other groups and, for the
+// groups above the bound, the per-channel sum of log(sinh(a_c) / a_c) over
+// the row's rotated query in tensor memory (t_q, fp32).  Warp-collective
+// (tensor memory loads): called by whole warps.
 template <int G, int D, int GROUP>
 __device__ __noinline__ void exact_fix(const float* dq, const uint64_t (&mu2)[G],
-                                       const uint64_t (&a2)[G][kSeriesTerms], uint32_t t_q,
+                                       const uint64_t (&a2)[G][kFitTerms], uint32_t t_q,
                                        uint64_t (&nb)[16]) {
   float mu[G];
 #pragma unroll
@@ -483,7 +489,7 @@ __device__ __noinline__ void exact_fix(const float* dq, const uint64_t (&mu2)[G]
   for (int g = 0; g < G; ++g) {
     vm[g] = 0u;
 #pragma unroll 4
-    for (int k = 0; k < 32; ++k) vm[g] |= (mu[g] * dq[g * kBlockN + k] > 1.0f ? 1u : 0u) << k;
+    for (int k = 0; k < 32; ++k) vm[g] |= (mu[g] * dq[g * kBlockN + k] > kFitTmax ? 1u : 0u) << k;
     any |= vm[g];
   }
   if (!__any_sync(0xffffffffu, any != 0u)) return;
@@ -496,12 +502,12 @@ __device__ __noinline__ void exact_fix(const float* dq, const uint64_t (&mu2)[G]
 #pragma unroll
       for (int g = 0; g < G; ++g) {
         const float t = mu[g] * dq[g * kBlockN + k];
-        if (t <= 1.0f) {
+        if (t <= kFitTmax) {
           float a, unused;
-          ptx::f2_unpack(a2[g][kSeriesTerms - 1], a, unused);
+          ptx::f2_unpack(a2[g][kFitTerms - 1], a, unused);
           float pp = a;
 #pragma unroll
-          for (int i = kSeriesTerms - 2; i >= 0; --i) {
+          for (int i = kFitTerms - 2; i >= 0; --i) {
             ptx::f2_unpack(a2[g][i], a, unused);
             pp = fmaf(pp, t, a);
           }
@@ -711,16 +717,16 @@ __global__ void __launch_bounds__(Cfg<D, NQ, PRECISE, EXACT, KCH>::kThreads, 1)
     // Read from the query tile before the first QK can be issued (the tile is
     // overwritten once the cached QKs are done).
     constexpr int GE = EXACT ? G : 1;
-    uint64_t mu2[GE], a2[GE][kSeriesTerms];
+    uint64_t mu2[GE], a2[GE][kFitTerms];
     const uint32_t t_q = tmem + C::kTQ + lane_off;
     if (EXACT) {
       const uint8_t* qt = smem + C::kQ + q * C::kTile;
-      float mu[GE], mom[GE][kSeriesTerms];
+      float mu[GE], mom[GE][kFitTerms];
 #pragma unroll
       for (int g = 0; g < GE; ++g) {
         mu[g] = 0.f;
 #pragma unroll
-        for (int k = 0; k < kSeriesTerms; ++k) mom[g][k] = 0.f;
+        for (int k = 0; k < kFitTerms; ++k) mom[g][k] = 0.f;
       }
 #pragma unroll
       for (int cc = 0; cc < D / 32; ++cc) {
@@ -759,7 +765,7 @@ __global__ void __launch_bounds__(Cfg<D, NQ, PRECISE, EXACT, KCH>::kThreads, 1)
           float pw = u;
           mom[g][0] += pw;
 #pragma unroll
-          for (int t = 1; t < kSeriesTerms; ++t) {
+          for (int t = 1; t < kFitTerms; ++t) {
             pw *= u;
             mom[g][t] += pw;
           }
@@ -769,8 +775,8 @@ __global__ void __launch_bounds__(Cfg<D, NQ, PRECISE, EXACT, KCH>::kThreads, 1)
       for (int g = 0; g < GE; ++g) {
         mu2[g] = ptx::f2_pack(mu[g], mu[g]);
 #pragma unroll
-        for (int t = 0; t < kSeriesTerms; ++t) {
-          const float a = -kLog2e * sinhc_coef(t) * mom[g][t];
+        for (int t = 0; t < kFitTerms; ++t) {
+          const float a = -kLog2e * sinhc_fit(t) * mom[g][t];
           a2[g][t] = ptx::f2_pack(a, a);
         }
       }
@@ -822,11 +828,13 @@ __global__ void __launch_bounds__(Cfg<D, NQ, PRECISE, EXACT, KCH>::kThreads, 1)
       // stage's V-half barrier (its phase for this tile has completed, and the
       // V half is not refilled before this tile's P is handed over and its PV
       // done); the series alone when every group of every key stays within
-      // T <= 1
+      // T <= kFitTmax
       const bool exact_tile = EXACT && j < n_ct;
       const float* dq =
           reinterpret_cast<const float*>(smem + C::kStages + (j & 1) * C::kStageBytes + C::kDsq);
-      bool fast = true;
+      // bit c of `slow`: some row of the warp has, in 32-key chunk c, a key
+      // with T > kFitTmax in some group (from the chunks' per-group maxima)
+      uint32_t slow = 0u;
       if (exact_tile) {
         if (!__all_sync(0xffffffffu,
                         wait_bar(BAR(kBarFullV + (j & 1)), (j >> 1) & 1, lim, abort, p.status))) {
@@ -838,9 +846,10 @@ __global__ void __launch_bounds__(Cfg<D, NQ, PRECISE, EXACT, KCH>::kThreads, 1)
           const float4 tm = *reinterpret_cast<const float4*>(dq + 4 * kBlockN + 4 * g);
           float mu, unused;
           ptx::f2_unpack(mu2[g], mu, unused);
-          fast = fast && mu * fmaxf(fmaxf(tm.x, tm.y), fmaxf(tm.z, tm.w)) <= 1.0f;
+          slow |= (mu * tm.x > kFitTmax ? 1u : 0u) | (mu * tm.y > kFitTmax ? 2u : 0u) |
+                  (mu * tm.z > kFitTmax ? 4u : 0u) | (mu * tm.w > kFitTmax ? 8u : 0u);
         }
-        fast = __all_sync(0xffffffffu, fast);
+        slow = __reduce_or_sync(0xffffffffu, slow);
       }
       // Full tiles take the chunk pass without column masks; only the last
       // tile of a segment (nv < 128 valid keys) masks its columns.
@@ -851,7 +860,7 @@ __global__ void __launch_bounds__(Cfg<D, NQ, PRECISE, EXACT, KCH>::kThreads, 1)
           uint64_t nb[16];
           if (exact_tile) {   // before the scores are loaded: fewer live registers
             exact_series<GE>(dq + 32 * c, mu2, a2, nb);
-            if (!fast) exact_fix<GE, D, GROUP>(dq + 32 * c, mu2, a2, t_q, nb);
+            if ((slow >> c) & 1u) exact_fix<GE, D, GROUP>(dq + 32 * c, mu2, a2, t_q, nb);
           }
           uint32_t cur[32];
           ptx::tmem_ld32(t_s + 32 * c, cur);

@@ -1,6 +1,5 @@
 // Warp-shuffle fast Walsh-Hadamard transform of one row held by a group of
-// lanes (8 channels per lane), used by the quantize-append and rotation
-// kernels.
+// lanes (8 channels per lane), and BF16 bit helpers.
 //
 // Rotation (paper section 3, "Hadamard rotation"): x' = (1/sqrt(d)) *
 // Sylvester(d) * diag(sigma) * x.  The butterflies run in the order
@@ -41,34 +40,6 @@ __device__ __forceinline__ void fwht_row(float (&x)[8], int t) {
       x[e] = __fmaf_rn(sgn, x[e], p);
     }
   }
-}
-
-// Sign-bit masks of channels 8t .. 8t + 7 (bit 31 set where sigma_c = -1).
-__device__ __forceinline__ void sign_masks(uint32_t sign_word, int t, uint32_t (&m)[8]) {
-  const uint32_t sbits = (sign_word >> ((t & 3) * 8)) & 0xFFu;
-#pragma unroll
-  for (int e = 0; e < 8; ++e) m[e] = ((sbits >> e) & 1u) << 31;
-}
-
-// Unpack 8 BF16 values (one 16-byte vector) to fp32 and flip the signs given
-// by the masks (exact: only the sign bit changes).
-__device__ __forceinline__ void load8_masked(const uint4& raw, const uint32_t (&m)[8],
-                                             float (&x)[8]) {
-  const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    x[2 * i] = __uint_as_float((w[i] << 16) ^ m[2 * i]);
-    x[2 * i + 1] = __uint_as_float((w[i] & 0xFFFF0000u) ^ m[2 * i + 1]);
-  }
-}
-
-// Unpack 8 BF16 values (one 16-byte vector) to fp32 and apply the sign flips
-// of channels 8t .. 8t + 7.
-__device__ __forceinline__ void load8_signed(const uint4& raw, uint32_t sign_word, int t,
-                                             float (&x)[8]) {
-  uint32_t m[8];
-  sign_masks(sign_word, t, m);
-  load8_masked(raw, m, x);
 }
 
 __device__ __forceinline__ uint32_t bf16_bits_rn(float v) {

@@ -24,12 +24,6 @@ namespace kvq {
 
 namespace {
 
-constexpr int kThreads = 256;
-constexpr int kRotUnroll = 4;   // rows per lane group in flight in the rotation kernel
-
-__device__ __forceinline__ uint32_t h_bits_rn(float v) {
-  return (uint32_t)__half_as_ushort(__float2half_rn(v));
-}
 
 // sign word of lane t's channels without indexing a kernel-parameter array at
 // run time (which would copy the parameters to local memory)
@@ -70,16 +64,22 @@ __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
-// Eq. (1) for one group (or the part of it one thread holds) given the
-// group's min and max: step covering [min, max] and integer zero point, both
-// stored BF16 and returned as the record (step | zero << 16); the n values
-// xg[0..n) are replaced by 1.5 * 2^23 + code - zfold, zfold being the zero
-// point when it is left for the packing to add (0 otherwise).
-template <int BITS, int N>
-__device__ __forceinline__ uint32_t group_codes(float* xg, float mn, float mx, int& zfold) {
-  const float qmax = float((1 << BITS) - 1);
-  // Eq. (1): step covering [min, max], integer zero point, both stored BF16
+// Eq. (1) for one group given its min and max: the step covering
+// [min, max] and the integer zero point, both stored BF16 (the record is
+// step | zero << 16), and what the code decision needs.
+struct QHdr {
+  float delta, rcp, zero;
+  int zf;          // the zero point as an integer
+  bool fast;       // quotients by the reciprocal and one residual step
+  bool clamp;      // some code of the group leaves [0, 2^B - 1]
+  uint32_t rec;
+};
+
+template <int BITS>
+__device__ __forceinline__ QHdr group_header(float mn, float mx) {
+  constexpr float qmax = float((1 << BITS) - 1);
   constexpr float kInvQmax = 1.0f / float((1 << BITS) - 1);   // fl(1 / qmax)
+  QHdr h;
   const float span = __fsub_rn(mx, mn);
   uint32_t dbits = bf16_bits_rn(span >= 0x1p-100f && span < 0x1p100f
                                     ? div_step(span, qmax, kInvQmax)
@@ -88,33 +88,64 @@ __device__ __forceinline__ uint32_t group_codes(float* xg, float mn, float mx, i
     dbits = bf16_bits_rn(fabsf(mn));
     if (bf16_value(dbits) == 0.0f) dbits = 0x3F80u;  // 1.0
   }
-  const float delta = bf16_value(dbits);
-  const float rcp = __frcp_rn(delta);
-  const bool fast = rcp < 0x1p100f && fabsf(mn) * rcp < 0x1p21f && fabsf(mx) * rcp < 0x1p21f;
-  const float zq = fast ? div_step(-mn, delta, rcp) : __fdiv_rn(-mn, delta);
+  h.delta = bf16_value(dbits);
+  h.rcp = __frcp_rn(h.delta);
+  h.fast = h.rcp < 0x1p100f && fabsf(mn) * h.rcp < 0x1p21f && fabsf(mx) * h.rcp < 0x1p21f;
+  const float zq = h.fast ? div_step(-mn, h.delta, h.rcp) : __fdiv_rn(-mn, h.delta);
   const uint32_t zbits = bf16_bits_rn(__fadd_rn(rintf(zq), 0.0f));
-  const float zero = bf16_value(zbits);
-
-  // codes.  Fast route: q = fl(x / delta) exactly, from the correctly
-  // rounded reciprocal r and one residual step (q0 = fl(x r), e = x - q0 delta
-  // exact by FMA, q = fl(q0 + e r): correctly rounded while nothing over- or
-  // underflows); rint(q) by adding 1.5 * 2^23 (ties to even, |q| < 2^21);
-  // the integer zero point added after the rounding.  K = 1.5 * 2^23 + code
-  // then carries the code in its low mantissa bits.  Codes are monotone in
-  // x, so those of the group's min and max bound them all and the clamp to
-  // [0, 2^B - 1] is needed only when one of those two falls outside; when
-  // it is not, the zero point is left to the packing (which adds it to a
-  // whole half-word of codes at once).
+  h.zero = bf16_value(zbits);
+  h.zf = __float2int_rn(h.zero);
+  h.rec = dbits | (zbits << 16);
+  // codes are monotone in x: those of the group's min and max bound them all
   const float kMagic = 12582912.0f;   // 1.5 * 2^23
-  if (fast) {
-    auto code_of = [&](float v) {
-      const float q0 = __fmul_rn(v, rcp);
-      const float q = __fmaf_rn(__fmaf_rn(-q0, delta, v), rcp, q0);
-      return __fadd_rn(__fadd_rn(q, kMagic), zero) - kMagic;
-    };
-    const bool clamp = code_of(mn) < 0.0f || code_of(mx) > qmax;
-    const uint64_t r2 = ptx::f2_pack(rcp, rcp);
-    const uint64_t nd2 = ptx::f2_pack(-delta, -delta);
+  auto code_of = [&](float v) {
+    const float q0 = __fmul_rn(v, h.rcp);
+    const float q = __fmaf_rn(__fmaf_rn(-q0, h.delta, v), h.rcp, q0);
+    return __fadd_rn(__fadd_rn(q, kMagic), h.zero) - kMagic;
+  };
+  h.clamp = h.fast && (code_of(mn) < 0.0f || code_of(mx) > qmax);
+  return h;
+}
+
+// The code of one value of a group with header h (the arithmetic of
+// group_codes below, one value at a time).
+template <int BITS>
+__device__ __forceinline__ uint32_t code_of_value(float v, const QHdr& h) {
+  constexpr float qmax = float((1 << BITS) - 1);
+  const float kMagic = 12582912.0f;   // 1.5 * 2^23
+  if (h.fast) {
+    const float q0 = __fmul_rn(v, h.rcp);
+    const float q = __fmaf_rn(__fmaf_rn(-q0, h.delta, v), h.rcp, q0);
+    const float t = __fadd_rn(q, kMagic);
+    if (h.clamp) return __float_as_uint(fminf(fmaxf(__fadd_rn(t, h.zero), kMagic), kMagic + qmax)) - 0x4B400000u;
+    return (uint32_t)((int)(__float_as_uint(t) - 0x4B400000u) + h.zf);
+  }
+  const float t = fminf(fmaxf(__fadd_rn(rintf(__fdiv_rn(v, h.delta)), h.zero), 0.0f), qmax);
+  return (uint32_t)__float2int_rn(t);
+}
+
+// Eq. (1) for one group (or the part of it one thread holds) given the
+// group's min and max; the n values xg[0..n) are replaced by
+// 1.5 * 2^23 + code - zfold, zfold being the zero point when it is left for
+// the packing to add (0 otherwise).  Returns the record (step | zero << 16).
+//
+// Fast route: q = fl(x / delta) exactly, from the correctly rounded
+// reciprocal r and one residual step (q0 = fl(x r), e = x - q0 delta exact
+// by FMA, q = fl(q0 + e r): correctly rounded while nothing over- or
+// underflows); rint(q) by adding 1.5 * 2^23 (ties to even, |q| < 2^21); the
+// integer zero point added after the rounding.  K = 1.5 * 2^23 + code then
+// carries the code in its low mantissa bits.  The clamp to [0, 2^B - 1] is
+// needed only when the code of the group's min or max falls outside; when
+// it is not, the zero point is left to the packing (which adds it to a whole
+// half-word of codes at once).
+template <int BITS, int N>
+__device__ __forceinline__ uint32_t group_codes(float* xg, float mn, float mx, int& zfold) {
+  const float qmax = float((1 << BITS) - 1);
+  const QHdr h = group_header<BITS>(mn, mx);
+  const float kMagic = 12582912.0f;   // 1.5 * 2^23
+  if (h.fast) {
+    const uint64_t r2 = ptx::f2_pack(h.rcp, h.rcp);
+    const uint64_t nd2 = ptx::f2_pack(-h.delta, -h.delta);
     const uint64_t m2 = ptx::f2_pack(kMagic, kMagic);
 #pragma unroll
     for (int c = 0; c < N; c += 2) {
@@ -124,10 +155,10 @@ __device__ __forceinline__ uint32_t group_codes(float* xg, float mn, float mx, i
       const uint64_t q = ptx::f2_fma(e, r2, q0);
       ptx::f2_unpack(ptx::f2_add(q, m2), xg[c], xg[c + 1]);
     }
-    zfold = __float2int_rn(zero);
-    if (clamp) {
+    zfold = h.zf;
+    if (h.clamp) {
 #pragma unroll
-      for (int c = 0; c < N; ++c) xg[c] = fminf(fmaxf(__fadd_rn(xg[c], zero), kMagic), kMagic + qmax);
+      for (int c = 0; c < N; ++c) xg[c] = fminf(fmaxf(__fadd_rn(xg[c], h.zero), kMagic), kMagic + qmax);
       zfold = 0;
     }
   } else {
@@ -140,14 +171,14 @@ __device__ __forceinline__ uint32_t group_codes(float* xg, float mn, float mx, i
     for (int c = 0; c < N; ++c) tmp[c] = xg[c];
 #pragma unroll 1
     for (int c = 0; c < N; ++c) {
-      float t = __fadd_rn(rintf(__fdiv_rn(tmp[c], delta)), zero);
+      float t = __fadd_rn(rintf(__fdiv_rn(tmp[c], h.delta)), h.zero);
       t = fminf(fmaxf(t, 0.0f), qmax);
       tmp[c] = __fadd_rn(t, kMagic);
     }
 #pragma unroll
     for (int c = 0; c < N; ++c) xg[c] = tmp[c];
   }
-  return dbits | (zbits << 16);
+  return h.rec;
 }
 
 // One packed word from the 32/BITS consecutive channels xw[0..) (each value
@@ -336,12 +367,21 @@ __global__ void __launch_bounds__(kQWarps * 32, kQBlocksPerSm)
 // HF = 0 owns channels [0, 32) and [64, 96), HF = 1 owns [32, 64) and
 // [96, 128).  Groups of 32 channels then lie in one warp; groups of 64 swap
 // their partial min / max once more.
+//
+// Both warps run one code path (one copy of the unrolled code in the
+// instruction cache): warp 1 takes channels 96..127 with their signs flipped
+// (an exact negation that every butterfly carries along), so its h = 32
+// step leaves channels 96..127 in the first half of its registers, as warp 0
+// has channels 0..31 there; both then keep their first half and send their
+// second.  Warp 1's differences of the h = 64 step come out negated and take
+// the scale -fl(1/sqrt(d)) (again exact).  Every value is the same fp32
+// result as in the textbook order.
 constexpr int kSplitWarps = 4;                  // two warp pairs per block
 constexpr int kSplitBlocksPerSm = 4;
 constexpr int kSplitStages = 3;
 constexpr int kHalfRowBytes = 128;              // 64 BF16 channels
 constexpr int kSplitTile = 32 * kHalfRowBytes;  // one warp's 32 half-rows
-constexpr int kSplitSmem = kSplitWarps * (kSplitStages * kSplitTile + 32 * 4 * 4);
+constexpr int kSplitSmem = kSplitWarps * (kSplitStages * kSplitTile + 32 * 4 * 4) + 64 * 4;
 
 // named barrier of one warp pair (ids 1 and 2; 0 is __syncthreads)
 __device__ __forceinline__ void pair_sync(int id) {
@@ -352,10 +392,10 @@ __device__ __forceinline__ void pair_sync(int id) {
 // quarter-warp's eight lanes use eight different bank groups
 __device__ __forceinline__ int half_slot(int l, int i) { return l * kHalfRowBytes + ((i ^ (l & 7)) << 4); }
 
-template <int BITS, int GROUP, int HF>
-__device__ __forceinline__ void quantize_half_row(const QuantArgs& a, const PairSigns sg,
+template <int BITS, int GROUP>
+__device__ __forceinline__ void quantize_half_row(const QuantArgs& a, const uint32_t* msk,
                                                   uint8_t* own, const uint8_t* partner,
-                                                  float* mm, const float* pmm, int lane,
+                                                  float* mm, const float* pmm, int lane, int HF,
                                                   unsigned rk, bool valid, bool is_v, int bar) {
   constexpr int H = 64, Q = 32;
   constexpr int G = 128 / GROUP;
@@ -363,19 +403,15 @@ __device__ __forceinline__ void quantize_half_row(const QuantArgs& a, const Pair
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
     const uint4 raw = *reinterpret_cast<const uint4*>(own + half_slot(lane, i));
-    const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+    const uint4 mv = *reinterpret_cast<const uint4*>(msk + 4 * i);
+    const uint32_t w[4] = {raw.x ^ mv.x, raw.y ^ mv.y, raw.z ^ mv.z, raw.w ^ mv.w};
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
-      const int pl = 4 * i + k, pg = HF * 32 + pl;  // pair within the half / the row
-      x[2 * pl] = __uint_as_float(w[k] << 16);      // sign applied below
-      x[2 * pl + 1] = __uint_as_float((w[k] ^ sg.m[pg]) & 0xFFFF0000u);
+      const int pl = 4 * i + k;
+      const float lo = __uint_as_float(w[k] << 16), hi = __uint_as_float(w[k] & 0xFFFF0000u);
+      x[2 * pl] = __fadd_rn(lo, hi);          // h = 1
+      x[2 * pl + 1] = __fsub_rn(lo, hi);
     }
-  }
-#pragma unroll
-  for (int pl = 0; pl < H / 2; ++pl) {
-    const float u = x[2 * pl], v = x[2 * pl + 1];
-    x[2 * pl] = __fmaf_rn(sg.sl[HF * 32 + pl], u, v);
-    x[2 * pl + 1] = __fmaf_rn(sg.sl[HF * 32 + pl], u, -v);
   }
 #pragma unroll
   for (int h = 2; h < H; h <<= 1) {
@@ -389,19 +425,23 @@ __device__ __forceinline__ void quantize_half_row(const QuantArgs& a, const Pair
       }
     }
   }
-  // h = 64 across the pair: every lane has read its staged half-row, so the
-  // stage slot carries the 32 values the partner needs
-  constexpr int kSend = HF == 0 ? Q : 0, kKeep = HF == 0 ? 0 : Q;
+  // h = 64 across the pair.  Warp 1 took its channels 96..127 negated, so
+  // its h = 32 butterflies left channels 96..127 (true values) in x[0..32)
+  // and 64..95 in x[32..64): both warps keep x[0..32) (channels 32 HF ..
+  // 32 HF + 31 before this step) and send x[32..64)
   __syncwarp();
 #pragma unroll
   for (int i = 0; i < 8; ++i)
     *reinterpret_cast<uint4*>(own + half_slot(lane, i)) =
-        make_uint4(__float_as_uint(x[kSend + 4 * i]), __float_as_uint(x[kSend + 4 * i + 1]),
-                   __float_as_uint(x[kSend + 4 * i + 2]), __float_as_uint(x[kSend + 4 * i + 3]));
+        make_uint4(__float_as_uint(x[Q + 4 * i]), __float_as_uint(x[Q + 4 * i + 1]),
+                   __float_as_uint(x[Q + 4 * i + 2]), __float_as_uint(x[Q + 4 * i + 3]));
   pair_sync(bar);
-  // in place: x[0..32) <- channels 32 HF + j (sums), x[32..64) <- channels
-  // 64 + 32 HF + j (differences); the low channel of each butterfly first
+  // kept + received -> channel 32 HF + j; kept - received -> channel 64 +
+  // 32 HF + j, negated in warp 1 (its kept values are the high channels):
+  // the negation rides on the scale (exact)
   const uint64_t s2 = ptx::f2_pack(a.inv_sqrt_d, a.inv_sqrt_d);
+  const float sd = HF ? -a.inv_sqrt_d : a.inv_sqrt_d;
+  const uint64_t sd2 = ptx::f2_pack(sd, sd);
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
     const uint4 v = *reinterpret_cast<const uint4*>(partner + half_slot(lane, i));
@@ -410,11 +450,10 @@ __device__ __forceinline__ void quantize_half_row(const QuantArgs& a, const Pair
 #pragma unroll
     for (int e = 0; e < 4; e += 2) {
       const int j = 4 * i + e;
-      const uint64_t kept = ptx::f2_pack(x[kKeep + j], x[kKeep + j + 1]);
+      const uint64_t kept = ptx::f2_pack(x[j], x[j + 1]);
       const uint64_t recv = ptx::f2_pack(rv[e], rv[e + 1]);
-      const uint64_t lo = HF == 0 ? kept : recv, hi = HF == 0 ? recv : kept;
-      ptx::f2_unpack(ptx::f2_mul(ptx::f2_add(lo, hi), s2), x[j], x[j + 1]);
-      ptx::f2_unpack(ptx::f2_mul(ptx::f2_sub(lo, hi), s2), x[Q + j], x[Q + j + 1]);
+      ptx::f2_unpack(ptx::f2_mul(ptx::f2_add(kept, recv), s2), x[j], x[j + 1]);
+      ptx::f2_unpack(ptx::f2_mul(ptx::f2_sub(kept, recv), sd2), x[Q + j], x[Q + j + 1]);
     }
   }
   uint32_t rec[2];
@@ -492,6 +531,19 @@ __global__ void __launch_bounds__(kSplitWarps * 32, kSplitBlocksPerSm)
   float* mm_base = reinterpret_cast<float*>(qsm + kSplitWarps * kSplitStages * kSplitTile);
   float* mm = mm_base + wib * 128;
   const float* pmm = mm_base + (wib ^ 1) * 128;
+  // sign masks of the two halves (bit 15: channel 2p, bit 31: channel 2p + 1
+  // of pair p); the second half takes channels 96..127 negated as well
+  uint32_t* msk_base = reinterpret_cast<uint32_t*>(mm_base + kSplitWarps * 128);
+  if (threadIdx.x < 64) {
+    const int p = threadIdx.x;   // pair of the row
+    uint32_t m = sg.m[0];
+#pragma unroll
+    for (int q = 1; q < 64; ++q) m = q == p ? sg.m[q] : m;
+    if (p >= 48) m ^= 0x80008000u;
+    msk_base[p] = m;
+  }
+  __syncthreads();
+  const uint32_t* msk = msk_base + 32 * hf;
   const unsigned per_kv = (unsigned)a.bh * (unsigned)a.n_new;   // < 2^30 (host check)
   const unsigned tiles_per = (per_kv + 31u) / 32u;
   const unsigned n_tiles = 2u * tiles_per;
@@ -530,8 +582,7 @@ __global__ void __launch_bounds__(kSplitWarps * 32, kSplitBlocksPerSm)
     uint8_t* own = stages + s * kSplitTile;
     const uint8_t* par = pstages + s * kSplitTile;
     const int bar = 1 + (wib >> 1);
-    if (hf == 0) quantize_half_row<BITS, GROUP, 0>(a, sg, own, par, mm, pmm, lane, rk, valid, is_v, bar);
-    else quantize_half_row<BITS, GROUP, 1>(a, sg, own, par, mm, pmm, lane, rk, valid, is_v, bar);
+    quantize_half_row<BITS, GROUP>(a, msk, own, par, mm, pmm, lane, hf, rk, valid, is_v, bar);
     __syncwarp();
     s = sn;
   }
@@ -539,53 +590,306 @@ __global__ void __launch_bounds__(kSplitWarps * 32, kSplitBlocksPerSm)
 
 // ---- per-channel keys: Eq. (1) per channel over a block of tokens -----------
 //
-// One CTA per (block of up to kKeyBlock tokens of the appended chunk, batch *
-// head).  Thread t rotates token row t (the same fp32 butterflies as the
-// per-token kernels) into shared memory; thread c then takes channel c's
-// column, computes its step and zero point over the block's tokens with the
-// same Eq. (1) arithmetic as a per-token group, and writes its codes as
-// bytes; thread t finally packs token t's codes into the cache's word layout.
-constexpr int kKcThreads = kKeyBlock;
+// One CTA of kKcThreads per (block of up to kKeyBlock tokens of the appended
+// chunk, batch * head).
+// 1. Rotation: LPR = d / 32 lanes per token row, 32 channels per lane,
+//    butterflies h = 1 .. 16 in registers, the row written to shared memory,
+//    read back transposed (lane j: channels {32u + (32 / LPR) j + v}), h = 32
+//    (and 64) and the multiply by fl(1/sqrt(d)) in registers, written back in
+//    place: the same fp32 operations in the same order as the per-token
+//    kernels.  Rows are XOR-swizzled in 16-byte chunks (chunk c of lane jj's
+//    channels at c ^ (2 jj + (t & 1)) for d = 128, c ^ (4 jj + (t & 3)) for
+//    d = 64), which keeps a quarter-warp on eight bank groups.
+// 2. Channel columns: kKcThreads / d threads per channel, each over a slice
+//    of the tokens: min and max, combined through shared memory, the
+//    channel's step and zero point (Eq. (1), the per-token group arithmetic),
+//    then each value's code as a byte.
+// 3. Token rows: two threads per token pack its codes into the cache's word
+//    layout.
+constexpr int kKcThreads = 256;
+
+template <int D>
+__device__ __forceinline__ int kc_swz(int jj, int t) {
+  return D == 128 ? 2 * jj + (t & 1) : 4 * jj + (t & 3);
+}
+
+// float offset of channel c in a rotated row (token t)
+template <int D>
+__device__ __forceinline__ int kc_pos(int c, int t) {
+  return 32 * (c >> 5) + 4 * (((c >> 2) & 7) ^ kc_swz<D>(c >> 5, t)) + (c & 3);
+}
 
 template <int D, int BITS>
-__global__ void __launch_bounds__(kKcThreads) quantize_key_channels_kernel(const QuantArgs a,
-                                                                           const PairSigns sg) {
-  constexpr int CH = D / 4;                 // 16-byte chunks of an fp32 row
-  constexpr int CB = D / 16;                // 16-byte chunks of a code-byte row
+__global__ void __launch_bounds__(kKcThreads) quantize_key_channels_kernel(const QuantArgs a) {
+  constexpr int LPR = D / 32;                  // lanes per token row
+  constexpr int VW = 32 / LPR;                 // channels per lane and run after the transpose
+  constexpr int RPP = kKcThreads / LPR;        // rows per pass
+  constexpr int P = kKcThreads / D;            // threads per channel column
+  constexpr int SLICE = kKeyBlock / P;         // tokens per column thread
+  constexpr int CB = D / 16;                   // 16-byte chunks of a code-byte row
   extern __shared__ __align__(16) uint8_t ksm[];
-  float* rot = reinterpret_cast<float*>(ksm);                         // [kKeyBlock][D]
-  uint8_t* cb = ksm + kKeyBlock * D * 4;                              // [kKeyBlock][D] codes
+  float* rot = reinterpret_cast<float*>(ksm);                                   // [kKeyBlock][D]
+  uint8_t* cb = ksm + kKeyBlock * D * 4;                                        // [kKeyBlock][D]
+  float* mm = reinterpret_cast<float*>(cb + kKeyBlock * D);                     // [P][D][2]
   const int tid = threadIdx.x;
   const int blk = blockIdx.x;
   const int bh = blockIdx.y;
   const int t0 = blk * kKeyBlock;
   const int n = min(kKeyBlock, a.n_new - t0);
 
-  // 1. token rows: fp32 rotation (sign flips, butterflies h = 1, ..., d/2,
-  //    times fl(1/sqrt(d))), 16-byte chunks XOR-swizzled by token
-  if (tid < n) {
-    const uint4* src = reinterpret_cast<const uint4*>(a.k_new + ((size_t)bh * a.n_new + t0 + tid) * D);
-    float x[D];
+  // 1. rotation of the block's token rows
+  {
+    const int j = (tid & 31) % LPR;
+    const uint32_t sw = j == 0 ? a.sign_bits[0] : j == 1 ? a.sign_bits[1] : j == 2 ? a.sign_bits[2]
+                                                                                    : a.sign_bits[3];
+    uint32_t z = 0;   // bit k: channel 2k of the lane's 32; bit 16 + k: channel 2k + 1
 #pragma unroll
-    for (int i = 0; i < D / 8; ++i) {
-      const uint4 raw = __ldg(src + i);
-      const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+    for (int k = 0; k < 16; ++k) z |= (((sw >> (2 * k)) & 1u) << k) | (((sw >> (2 * k + 1)) & 1u) << (16 + k));
+    // the lane's rows (kKeyBlock / RPP of them), all loaded before any is
+    // transformed
+    constexpr int NR = kKeyBlock / RPP;
+    uint4 rawr[NR][4];
+#pragma unroll
+    for (int rr = 0; rr < NR; ++rr) {
+      const int t = tid / LPR + rr * RPP;
+      const bool live = t < n;
+      const uint4* src = reinterpret_cast<const uint4*>(a.k_new + ((size_t)bh * a.n_new + t0 + (live ? t : 0)) * D + 32 * j);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) rawr[rr][k] = live ? __ldg(src + k) : make_uint4(0u, 0u, 0u, 0u);
+    }
+#pragma unroll
+    for (int rr = 0; rr < NR; ++rr) {   // the same rows count in every lane
+      const int t = tid / LPR + rr * RPP;
+      float* row = rot + t * D;
+      const uint4 (&raw)[4] = rawr[rr];
+      float x[32];
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
-        x[8 * i + 2 * k] = __uint_as_float(w[k] << 16);
-        x[8 * i + 2 * k + 1] = __uint_as_float((w[k] ^ sg.m[4 * i + k]) & 0xFFFF0000u);
+        const uint32_t w[4] = {raw[k].x, raw[k].y, raw[k].z, raw[k].w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const uint32_t u = w[i] ^ ((z << (15 - (4 * k + i))) & 0x80008000u);
+          const float lo = __uint_as_float(u << 16), hi = __uint_as_float(u & 0xFFFF0000u);
+          x[8 * k + 2 * i] = __fadd_rn(lo, hi);       // h = 1
+          x[8 * k + 2 * i + 1] = __fsub_rn(lo, hi);
+        }
+      }
+#pragma unroll
+      for (int h = 2; h < 32; h <<= 1) {
+#pragma unroll
+        for (int i = 0; i < 32; i += 2) {
+          if ((i & h) == 0) {
+            const uint64_t A = ptx::f2_pack(x[i], x[i + 1]);
+            const uint64_t B = ptx::f2_pack(x[i + h], x[i + h + 1]);
+            ptx::f2_unpack(ptx::f2_add(A, B), x[i], x[i + 1]);
+            ptx::f2_unpack(ptx::f2_sub(A, B), x[i + h], x[i + h + 1]);
+          }
+        }
+      }
+      const int sj = kc_swz<D>(j, t);
+#pragma unroll
+      for (int c = 0; c < 8; ++c)
+        *reinterpret_cast<float4*>(row + 32 * j + 4 * (c ^ sj)) =
+            make_float4(x[4 * c], x[4 * c + 1], x[4 * c + 2], x[4 * c + 3]);
+      __syncwarp();
+      float y[32];
+#pragma unroll
+      for (int u = 0; u < LPR; ++u) {
+        const int su = kc_swz<D>(u, t);
+#pragma unroll
+        for (int w4 = 0; w4 < VW / 4; ++w4) {
+          const float4 v = *reinterpret_cast<const float4*>(row + 32 * u + 4 * (((VW / 4) * j + w4) ^ su));
+          y[VW * u + 4 * w4] = v.x; y[VW * u + 4 * w4 + 1] = v.y;
+          y[VW * u + 4 * w4 + 2] = v.z; y[VW * u + 4 * w4 + 3] = v.w;
+        }
+      }
+#pragma unroll
+      for (int hu = 1; hu < LPR; hu <<= 1) {
+#pragma unroll
+        for (int u = 0; u < LPR; ++u) {
+          if ((u & hu) == 0) {
+#pragma unroll
+            for (int v = 0; v < VW; v += 2) {
+              const uint64_t A = ptx::f2_pack(y[VW * u + v], y[VW * u + v + 1]);
+              const uint64_t B = ptx::f2_pack(y[VW * (u + hu) + v], y[VW * (u + hu) + v + 1]);
+              ptx::f2_unpack(ptx::f2_add(A, B), y[VW * u + v], y[VW * u + v + 1]);
+              ptx::f2_unpack(ptx::f2_sub(A, B), y[VW * (u + hu) + v], y[VW * (u + hu) + v + 1]);
+            }
+          }
+        }
+      }
+      const uint64_t s2 = ptx::f2_pack(a.inv_sqrt_d, a.inv_sqrt_d);
+#pragma unroll
+      for (int i = 0; i < 32; i += 2) ptx::f2_unpack(ptx::f2_mul(ptx::f2_pack(y[i], y[i + 1]), s2), y[i], y[i + 1]);
+      // back to the places read (each lane its own): the final rotated row
+#pragma unroll
+      for (int u = 0; u < LPR; ++u) {
+        const int su = kc_swz<D>(u, t);
+#pragma unroll
+        for (int w4 = 0; w4 < VW / 4; ++w4)
+          *reinterpret_cast<float4*>(row + 32 * u + 4 * (((VW / 4) * j + w4) ^ su)) =
+              make_float4(y[VW * u + 4 * w4], y[VW * u + 4 * w4 + 1], y[VW * u + 4 * w4 + 2], y[VW * u + 4 * w4 + 3]);
+      }
+      __syncwarp();
+    }
+  }
+  __syncthreads();
+
+  // 2. channel columns: thread (part, c) takes tokens [part * SLICE, ...)
+  const int c = tid % D;
+  const int part = tid / D;
+  const int ta = part * SLICE, tb = min(n, ta + SLICE);
+  {
+    // four independent running pairs (min and max are exact in any order)
+    float mn[4] = {INFINITY, INFINITY, INFINITY, INFINITY};
+    float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll 2
+    for (int t = ta; t < tb; t += 4) {
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        if (t + u < tb) {
+          const float v = rot[(t + u) * D + kc_pos<D>(c, t + u)];
+          mn[u] = fminf(mn[u], v);
+          mx[u] = fmaxf(mx[u], v);
+        }
+      }
+    }
+    mm[(part * D + c) * 2] = fminf(fminf(mn[0], mn[1]), fminf(mn[2], mn[3]));
+    mm[(part * D + c) * 2 + 1] = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+  }
+  __syncthreads();
+  {
+    float mn = mm[2 * c], mx = mm[2 * c + 1];
+#pragma unroll
+    for (int p2 = 1; p2 < P; ++p2) {
+      mn = fminf(mn, mm[(p2 * D + c) * 2]);
+      mx = fmaxf(mx, mm[(p2 * D + c) * 2 + 1]);
+    }
+    const QHdr h = group_header<BITS>(mn, mx);
+    if (part == 0) a.k_sz[((size_t)bh * a.kblk_per_head + a.kblk_first + blk) * D + c] = h.rec;
+#pragma unroll 8
+    for (int t = ta; t < tb; ++t) {
+      const float v = rot[t * D + kc_pos<D>(c, t)];
+      cb[t * D + 16 * ((c >> 4) ^ (t & (CB - 1))) + (c & 15)] = (uint8_t)code_of_value<BITS>(v, h);
+    }
+  }
+  __syncthreads();
+
+  // 3. token t's codes into the packed words (two threads per token, half
+  //    the words each): channel 16w + 2k + h (INT2) / 8w + 2k + h (INT4) at
+  //    bits BITS*k + 16h of word w
+  {
+    constexpr int PER_WORD = 32 / BITS;
+    constexpr int NW = D * BITS / 32;
+    constexpr int NWH = NW / 2;             // words per thread
+    constexpr int CH = NWH * PER_WORD / 16;  // 16-byte code chunks per thread
+    const int t = tid >> 1, hw = tid & 1;
+    if (t < n) {
+      uint32_t words[NWH];
+#pragma unroll
+      for (int w = 0; w < NWH; ++w) words[w] = 0u;
+#pragma unroll
+      for (int i = 0; i < CH; ++i) {
+        const int ci = hw * CH + i;   // code chunk of the row
+        const uint4 v = *reinterpret_cast<const uint4*>(cb + t * D + 16 * (ci ^ (t & (CB - 1))));
+        const uint32_t uu[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const int ch = 16 * i + e;   // channel within this thread's half
+          const uint32_t code = (uu[e >> 2] >> (8 * (e & 3))) & 0xFFu;
+          const int jw = ch % PER_WORD;
+          words[ch / PER_WORD] |= code << (BITS * (jw >> 1) + 16 * (jw & 1));
+        }
+      }
+      uint8_t* drow = a.k_codes + ((size_t)bh * a.cap + a.first + t0 + t) * (D * BITS / 8) + hw * NWH * 4;
+      if constexpr (NWH >= 4) {
+#pragma unroll
+        for (int i = 0; i < NWH / 4; ++i)
+          reinterpret_cast<uint4*>(drow)[i] = make_uint4(words[4 * i], words[4 * i + 1], words[4 * i + 2], words[4 * i + 3]);
+      } else {
+        *reinterpret_cast<uint2*>(drow) = make_uint2(words[0], words[1 % NWH]);
+      }
+    }
+  }
+}
+
+// Rotation of Q and V_R (FP16 out, with the FP16 remainder when asked) or of
+// any BF16 rows (fp32 out).  LPR = d / 32 lanes per row, 32 channels per
+// lane: lane j first holds channels [32j, 32j + 32) and runs the butterflies
+// h = 1 .. 16 in registers; one transpose through shared memory then gives
+// it channels {32u + (32 / LPR) j + v} (u < LPR, v < 32 / LPR), whose
+// butterflies h = 32 (and 64) are again in registers.  Same fp32 operations
+// in the same order as the textbook transform (h = 1, 2, ..., d/2, then the
+// multiply by fl(1/sqrt(d))), so the fp32 output is bit for bit the
+// quantizer's rotation.  Each lane's next row is loaded before the current
+// one is transformed.
+constexpr int kRotThreads = 256;
+constexpr int kRotBlocksPerSm = 2;
+
+template <int D>
+__global__ void __launch_bounds__(kRotThreads, kRotBlocksPerSm) rotate_kernel(const RotateArgs a) {
+  constexpr int LPR = D / 32;          // lanes per row
+  constexpr int RPW = 32 / LPR;        // rows per warp
+  constexpr int VW = 32 / LPR;         // contiguous channels per lane after the transpose
+  __shared__ __align__(16) float tbuf[kRotThreads / 32][RPW][D];
+  const int lane = threadIdx.x & 31;
+  const int j = lane % LPR;            // channel block of the lane
+  const int g = lane / LPR;            // row within the warp's rows
+  float* rowbuf = tbuf[threadIdx.x >> 5][g];
+  const long long total = a.rows[0] + a.rows[1];
+  const long long warp0 = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const long long step = (((long long)gridDim.x * blockDim.x) >> 5) * RPW;
+
+  // the lane's 32 sign bits regrouped: bit k = channel 2k, bit 16 + k =
+  // channel 2k + 1, so that (z << (15 - k)) & 0x80008000 is the sign mask of
+  // the 32-bit word holding channels 2k (low half) and 2k + 1 (high half)
+  const uint32_t sw = sign_word_for(a.sign_bits, 4 * j);
+  uint32_t z = 0;
+#pragma unroll
+  for (int k = 0; k < 16; ++k) z |= (((sw >> (2 * k)) & 1u) << k) | (((sw >> (2 * k + 1)) & 1u) << (16 + k));
+  const long long rows0 = a.rows[0];
+  const uint16_t* src0 = a.src[0];
+  const uint16_t* src1 = a.src[1];
+
+  auto load = [&](long long r, uint4 (&raw)[4]) {
+    if (r < total) {
+      const bool s1 = r >= rows0;
+      const uint16_t* srcp = (s1 ? src1 : src0) + (s1 ? r - rows0 : r) * D + 32 * j;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) raw[k] = __ldg(reinterpret_cast<const uint4*>(srcp) + k);
+    } else {
+#pragma unroll
+      for (int k = 0; k < 4; ++k) raw[k] = make_uint4(0u, 0u, 0u, 0u);
+    }
+  };
+
+  bool out_of_range = false;
+  long long r = warp0 * RPW + g;
+  uint4 nxt[4];
+  load(r, nxt);
+  // the loop bounds are warp-uniform (r - g steps by whole warps)
+  for (; r - g < total; r += step) {
+    uint4 raw[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) raw[k] = nxt[k];
+    load(r + step, nxt);
+
+    float x[32];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const uint32_t w[4] = {raw[k].x, raw[k].y, raw[k].z, raw[k].w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const uint32_t t = w[i] ^ ((z << (15 - (4 * k + i))) & 0x80008000u);
+        const float lo = __uint_as_float(t << 16), hi = __uint_as_float(t & 0xFFFF0000u);
+        x[8 * k + 2 * i] = __fadd_rn(lo, hi);       // h = 1
+        x[8 * k + 2 * i + 1] = __fsub_rn(lo, hi);
       }
     }
 #pragma unroll
-    for (int i = 0; i < D; i += 2) {
-      const float u = x[i], v = x[i + 1];
-      x[i] = __fmaf_rn(sg.sl[i / 2], u, v);
-      x[i + 1] = __fmaf_rn(sg.sl[i / 2], u, -v);
-    }
+    for (int h = 2; h < 32; h <<= 1) {
 #pragma unroll
-    for (int h = 2; h < D; h <<= 1) {
-#pragma unroll
-      for (int i = 0; i < D; i += 2) {
+      for (int i = 0; i < 32; i += 2) {
         if ((i & h) == 0) {
           const uint64_t A = ptx::f2_pack(x[i], x[i + 1]);
           const uint64_t B = ptx::f2_pack(x[i + h], x[i + h + 1]);
@@ -594,130 +898,94 @@ __global__ void __launch_bounds__(kKcThreads) quantize_key_channels_kernel(const
         }
       }
     }
-    const uint64_t s2 = ptx::f2_pack(a.inv_sqrt_d, a.inv_sqrt_d);
+    // transpose through the row's buffer.  Chunk c (4 floats) of the
+    // channels of lane jj sits at float 32 jj + 4 (c ^ sw(jj)), sw(jj) =
+    // (32 / LPR) / 4 * jj + (g mod 8 / LPR): the eight lanes of a quarter-warp
+    // meet eight different bank groups on both the writes and the reads
+    auto swz = [&](int jj) { return (VW / 4) * jj + (g & (8 / LPR - 1)); };
+    __syncwarp();
+    {
+      const int sj = swz(j);
 #pragma unroll
-    for (int i = 0; i < D; i += 2) ptx::f2_unpack(ptx::f2_mul(ptx::f2_pack(x[i], x[i + 1]), s2), x[i], x[i + 1]);
-#pragma unroll
-    for (int i = 0; i < CH; ++i)
-      *reinterpret_cast<float4*>(rot + tid * D + 4 * (i ^ (tid & (CH - 1)))) =
-          make_float4(x[4 * i], x[4 * i + 1], x[4 * i + 2], x[4 * i + 3]);
-  }
-  __syncthreads();
-
-  // 2. channel columns: step, zero point and codes over the block's tokens
-  if (tid < D) {
-    const int c = tid;
-    float col[kKeyBlock];
-#pragma unroll
-    for (int t = 0; t < kKeyBlock; ++t) {
-      const int tt = t < n ? t : 0;   // past the block's end: a copy of token 0 (min / max unchanged)
-      col[t] = rot[tt * D + 4 * ((c >> 2) ^ (tt & (CH - 1))) + (c & 3)];
+      for (int c = 0; c < 8; ++c)
+        *reinterpret_cast<float4*>(rowbuf + 32 * j + 4 * (c ^ sj)) =
+            make_float4(x[4 * c], x[4 * c + 1], x[4 * c + 2], x[4 * c + 3]);
     }
-    float mn, mx;
-    min_max<kKeyBlock>(col, mn, mx);
-    int zf;
-    const uint32_t rec = group_codes<BITS, kKeyBlock>(col, mn, mx, zf);
-    a.k_sz[((size_t)bh * a.kblk_per_head + a.kblk_first + blk) * D + c] = rec;
-    // each value now reads 1.5 * 2^23 + code - zf
+    __syncwarp();
+    // read: y[VW u + v] = channel 32u + VW j + v
+    float y[32];
 #pragma unroll
-    for (int t = 0; t < kKeyBlock; ++t) {
-      if (t < n)
-        cb[t * D + 16 * ((c >> 4) ^ (t & (CB - 1))) + (c & 15)] =
-            (uint8_t)((int)(__float_as_uint(col[t]) - 0x4B400000u) + zf);
-    }
-  }
-  __syncthreads();
-
-  // 3. token t's codes into the packed words: channel 16w + 2k + h (INT2) /
-  //    8w + 2k + h (INT4) at bits BITS*k + 16h of word w
-  if (tid < n) {
-    constexpr int PER_WORD = 32 / BITS;
-    constexpr int NW = D * BITS / 32;
-    uint32_t words[NW];
+    for (int u = 0; u < LPR; ++u) {
+      const int su = swz(u);
 #pragma unroll
-    for (int w = 0; w < NW; ++w) words[w] = 0u;
-#pragma unroll
-    for (int i = 0; i < CB; ++i) {
-      const uint4 v = *reinterpret_cast<const uint4*>(cb + tid * D + 16 * (i ^ (tid & (CB - 1))));
-      const uint32_t u[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-      for (int e = 0; e < 16; ++e) {
-        const int ch = 16 * i + e;
-        const uint32_t code = (u[e >> 2] >> (8 * (e & 3))) & 0xFFu;
-        const int j = ch % PER_WORD;
-        words[ch / PER_WORD] |= code << (BITS * (j >> 1) + 16 * (j & 1));
+      for (int w4 = 0; w4 < VW / 4; ++w4) {
+        const float4 v = *reinterpret_cast<const float4*>(rowbuf + 32 * u + 4 * (((VW / 4) * j + w4) ^ su));
+        y[VW * u + 4 * w4] = v.x; y[VW * u + 4 * w4 + 1] = v.y;
+        y[VW * u + 4 * w4 + 2] = v.z; y[VW * u + 4 * w4 + 3] = v.w;
       }
     }
-    uint4* dc = reinterpret_cast<uint4*>(a.k_codes + ((size_t)bh * a.cap + a.first + t0 + tid) * (D * BITS / 8));
+    // h = 32 (and 64): pairs (u, u + h/32) at the same v
 #pragma unroll
-    for (int i = 0; i < NW / 4; ++i)
-      dc[i] = make_uint4(words[4 * i], words[4 * i + 1], words[4 * i + 2], words[4 * i + 3]);
-  }
-}
-
-template <int D>
-__global__ void __launch_bounds__(kThreads) rotate_kernel(const RotateArgs a) {
-  constexpr int LPR = D / 8;
-  constexpr int RPW = 32 / LPR;
-  const int lane = threadIdx.x & 31;
-  const int t = lane % LPR;
-  const long long total = a.rows[0] + a.rows[1];
-  const long long warp0 = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  const long long nwarps = ((long long)gridDim.x * blockDim.x) >> 5;
-  const uint32_t sign_word = sign_word_for(a.sign_bits, t);
-
-  // kRotUnroll rows per lane group in flight: their loads are issued
-  // before any of them is transformed
-  constexpr int U = kRotUnroll;
-  const long long step = nwarps * RPW;
-  bool out_of_range = false;
-  for (long long r0 = warp0 * RPW; r0 < total; r0 += step * U) {
-    uint4 raw[U];
-    long long rr[U];
-    bool valid[U], seg1[U];
+    for (int hu = 1; hu < LPR; hu <<= 1) {
 #pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const long long r = r0 + u * step + lane / LPR;
-      valid[u] = r < total;
-      rr[u] = valid[u] ? r : 0;
-      seg1[u] = rr[u] >= a.rows[0];
-      if (seg1[u]) rr[u] -= a.rows[0];
-      const uint16_t* srcp = seg1[u] ? a.src[1] : a.src[0];
-      raw[u] = valid[u] ? __ldg(reinterpret_cast<const uint4*>(srcp + rr[u] * D + 8 * t))
-                        : make_uint4(0u, 0u, 0u, 0u);
+      for (int u = 0; u < LPR; ++u) {
+        if ((u & hu) == 0) {
+#pragma unroll
+          for (int v = 0; v < VW; v += 2) {
+            const uint64_t A = ptx::f2_pack(y[VW * u + v], y[VW * u + v + 1]);
+            const uint64_t B = ptx::f2_pack(y[VW * (u + hu) + v], y[VW * (u + hu) + v + 1]);
+            ptx::f2_unpack(ptx::f2_add(A, B), y[VW * u + v], y[VW * u + v + 1]);
+            ptx::f2_unpack(ptx::f2_sub(A, B), y[VW * (u + hu) + v], y[VW * (u + hu) + v + 1]);
+          }
+        }
+      }
+    }
+    {
+      const uint64_t s2 = ptx::f2_pack(a.inv_sqrt_d, a.inv_sqrt_d);
+#pragma unroll
+      for (int i = 0; i < 32; i += 2) ptx::f2_unpack(ptx::f2_mul(ptx::f2_pack(y[i], y[i + 1]), s2), y[i], y[i + 1]);
+    }
+    if (r >= total) continue;
+    const bool s1 = r >= rows0;
+    const long long rr = s1 ? r - rows0 : r;
+    void* dstp = s1 ? a.dst[1] : a.dst[0];
+    uint16_t* lop = s1 ? a.dst_lo[1] : a.dst_lo[0];
+    const float lim = s1 ? a.range_limit[1] : a.range_limit[0];
+    if (lim > 0.f) {
+      // largest magnitude, NaN propagated (a NaN is out of range too)
+      float mx = 0.f;
+#pragma unroll
+      for (int i = 0; i < 32; ++i) asm("max.NaN.f32 %0, %0, %1;" : "+f"(mx) : "f"(fabsf(y[i])));
+      out_of_range |= !(mx < lim);
     }
 #pragma unroll
-    for (int u = 0; u < U; ++u) {
-      void* dstp = seg1[u] ? a.dst[1] : a.dst[0];
-      uint16_t* lop = seg1[u] ? a.dst_lo[1] : a.dst_lo[0];
-      float x[8];
-      load8_signed(raw[u], sign_word, t, x);
-      fwht_row<LPR>(x, t);   // all lanes: warp-collective shuffles
-#pragma unroll
-      for (int e = 0; e < 8; ++e) x[e] = __fmul_rn(x[e], a.inv_sqrt_d);
-      if (!valid[u]) continue;
-      const float lim = a.range_limit[seg1[u] ? 1 : 0];
-#pragma unroll
-      for (int e = 0; e < 8; ++e) out_of_range |= !(fabsf(x[e]) < lim) && lim > 0.f;
+    for (int u = 0; u < LPR; ++u) {
+      const long long off = rr * D + 32 * u + VW * j;   // first channel of this run
       if (a.out_f32) {
-        float4* dst = reinterpret_cast<float4*>(static_cast<float*>(dstp) + rr[u] * D + 8 * t);
-        dst[0] = make_float4(x[0], x[1], x[2], x[3]);
-        dst[1] = make_float4(x[4], x[5], x[6], x[7]);
+        float4* dst = reinterpret_cast<float4*>(static_cast<float*>(dstp) + off);
+#pragma unroll
+        for (int q4 = 0; q4 < VW / 4; ++q4)
+          dst[q4] = make_float4(y[VW * u + 4 * q4], y[VW * u + 4 * q4 + 1], y[VW * u + 4 * q4 + 2],
+                                y[VW * u + 4 * q4 + 3]);
       } else {
-        uint32_t hb[8];
+        uint32_t hw[VW / 2], lw[VW / 2];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) hb[e] = h_bits_rn(x[e]);
-        *reinterpret_cast<uint4*>(static_cast<uint16_t*>(dstp) + rr[u] * D + 8 * t) =
-            make_uint4(hb[0] | (hb[1] << 16), hb[2] | (hb[3] << 16), hb[4] | (hb[5] << 16),
-                       hb[6] | (hb[7] << 16));
+        for (int q2 = 0; q2 < VW / 2; ++q2) {
+          const float e0 = y[VW * u + 2 * q2], e1 = y[VW * u + 2 * q2 + 1];
+          hw[q2] = ptx::f16x2_rn(e0, e1);
+          const float b0 = __half2float(__ushort_as_half((unsigned short)(hw[q2] & 0xFFFFu)));
+          const float b1 = __half2float(__ushort_as_half((unsigned short)(hw[q2] >> 16)));
+          lw[q2] = ptx::f16x2_rn(__fsub_rn(e0, b0), __fsub_rn(e1, b1));
+        }
+        uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(dstp) + off);
+#pragma unroll
+        for (int q8 = 0; q8 < VW / 8; ++q8)
+          dst[q8] = make_uint4(hw[4 * q8], hw[4 * q8 + 1], hw[4 * q8 + 2], hw[4 * q8 + 3]);
         if (lop != nullptr) {
-          uint32_t lb[8];
+          uint4* dl = reinterpret_cast<uint4*>(lop + off);
 #pragma unroll
-          for (int e = 0; e < 8; ++e)
-            lb[e] = h_bits_rn(__fsub_rn(x[e], __half2float(__ushort_as_half((unsigned short)hb[e]))));
-          *reinterpret_cast<uint4*>(lop + rr[u] * D + 8 * t) =
-              make_uint4(lb[0] | (lb[1] << 16), lb[2] | (lb[3] << 16), lb[4] | (lb[5] << 16),
-                         lb[6] | (lb[7] << 16));
+          for (int q8 = 0; q8 < VW / 8; ++q8)
+            dl[q8] = make_uint4(lw[4 * q8], lw[4 * q8 + 1], lw[4 * q8 + 2], lw[4 * q8 + 3]);
         }
       }
     }
@@ -740,9 +1008,9 @@ int sm_count() {
   return n;
 }
 
-long long grid_for_rows(long long rows, int rows_per_block) {
+long long grid_for_rows(long long rows, int rows_per_block, int blocks_per_sm) {
   long long blocks = (rows + rows_per_block - 1) / rows_per_block;
-  const long long cap = (long long)sm_count() * 8;  // 8 blocks of 256 threads per SM
+  const long long cap = (long long)sm_count() * blocks_per_sm;   // one resident wave
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
   return blocks;
@@ -806,27 +1074,16 @@ cudaError_t launch_quantize_append(const QuantArgs& a, int d, int bits, int grou
 
 namespace {
 
-PairSigns pair_signs(const uint32_t (&sb)[4], int d) {
-  PairSigns sg;
-  for (int i = 0; i < 64; ++i) {
-    const int c0 = 2 * i, c1 = 2 * i + 1;
-    const uint32_t s0 = c0 < d ? (sb[c0 >> 5] >> (c0 & 31)) & 1u : 0u;
-    const uint32_t s1 = c1 < d ? (sb[c1 >> 5] >> (c1 & 31)) & 1u : 0u;
-    sg.m[i] = (s0 << 15) | (s1 << 31);
-    sg.sl[i] = s0 ? -1.0f : 1.0f;
-  }
-  return sg;
-}
-
 template <int D, int BITS>
 cudaError_t launch_kc(const QuantArgs& a, cudaStream_t s) {
   if (a.n_new == 0 || a.bh == 0) return cudaSuccess;
-  const int smem = kKeyBlock * D * 5;   // fp32 rows + code bytes
+  // fp32 rows + code bytes + per-part column min / max
+  const int smem = kKeyBlock * D * 5 + (kKcThreads / D) * D * 2 * 4;
   static std::atomic<uint64_t> limit_set{0};   // per template instance and device
   const cudaError_t e = ensure_smem_limit(quantize_key_channels_kernel<D, BITS>, smem, limit_set);
   if (e != cudaSuccess) return e;
   const dim3 grid((unsigned)((a.n_new + kKeyBlock - 1) / kKeyBlock), (unsigned)a.bh);
-  quantize_key_channels_kernel<D, BITS><<<grid, kKcThreads, smem, s>>>(a, pair_signs(a.sign_bits, D));
+  quantize_key_channels_kernel<D, BITS><<<grid, kKcThreads, smem, s>>>(a);
   return cudaGetLastError();
 }
 
@@ -846,12 +1103,12 @@ cudaError_t launch_quantize_key_channels(const QuantArgs& a, int d, int bits, cu
 cudaError_t launch_rotate(const RotateArgs& a, int d, cudaStream_t stream) {
   const long long rows = a.rows[0] + a.rows[1];
   if (rows == 0) return cudaSuccess;
-  const int rows_per_block = (kThreads / 32) * (32 / (d / 8));
-  const unsigned grid = (unsigned)grid_for_rows(rows, rows_per_block);
+  const int rows_per_block = (kRotThreads / 32) * (32 / (d / 32));
+  const unsigned grid = (unsigned)grid_for_rows(rows, rows_per_block, kRotBlocksPerSm);
   if (d == 64) {
-    rotate_kernel<64><<<grid, kThreads, 0, stream>>>(a);
+    rotate_kernel<64><<<grid, kRotThreads, 0, stream>>>(a);
   } else {
-    rotate_kernel<128><<<grid, kThreads, 0, stream>>>(a);
+    rotate_kernel<128><<<grid, kRotThreads, 0, stream>>>(a);
   }
   return cudaGetLastError();
 }

@@ -1,12 +1,17 @@
-"""The exact correction's power series, checked on the CPU.
+"""The exact correction's polynomial, checked on the CPU.
 
-The GPU evaluates log(sinh a / a) = sum_k c_k a^(2k) through k = 7 (the
-coefficients are constants of the attention kernel header).  Here a host
-program built from that header with nvcc prints them, and they are compared
-with c_k = 2^(2k) B_2k / (2k (2k)!) (B the Bernoulli numbers) and with the
-oracle's log_sinhc: the truncated series must meet it within the bound the
-kernels rely on (|c_8| a^16 per channel for a <= 1)."""
+The GPU evaluates log(sinh a / a) as sum_k p_k a^(2k) through k = 8 for
+a <= 3: over a group's channels through the query's power sums and the key's
+step (the separable form), and per channel where a group leaves that range.
+The p_k are a Chebyshev fit (derived by sinhc_fit.py beside the kernel
+header).  A host program built from the header with nvcc prints them; they
+must equal the generator's, rounded to fp32, and the polynomial evaluated in
+fp32 the way the kernels do must meet the oracle's log_sinhc within 5e-7 on
+0 <= a <= 3.  The first coefficients must also approach the Taylor series'
+c_k = 2^(2k) B_2k / (2k (2k)!) (B the Bernoulli numbers), which the fit
+reproduces near a = 0."""
 import fractions
+import importlib.util
 import os
 import shutil
 import subprocess
@@ -20,7 +25,7 @@ from oracle import kvq_oracle as O
 HERE = os.path.dirname(os.path.abspath(__file__))
 
 
-def _coef(k: int) -> fractions.Fraction:
+def _taylor(k: int) -> fractions.Fraction:
     sympy = pytest.importorskip("sympy")
     b = sympy.bernoulli(2 * k)
     return fractions.Fraction(2 ** (2 * k)) * fractions.Fraction(int(b.p), int(b.q)) / (
@@ -34,8 +39,16 @@ def _nvcc():
     return None
 
 
+def _generator():
+    path = os.path.join(HERE, "..", "quantized_kv_cache_quantize_gb300", "csrc", "sinhc_fit.py")
+    spec = importlib.util.spec_from_file_location("sinhc_fit", path)
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    return mod
+
+
 @pytest.mark.skipif(_nvcc() is None, reason="needs nvcc")
-def test_kernel_series_coefficients():
+def test_kernel_fit_coefficients():
     with tempfile.TemporaryDirectory() as tmp:
         exe = os.path.join(tmp, "series_coef_check")
         subprocess.check_call([_nvcc(), "-std=c++17", "-gencode", "arch=compute_103a,code=sm_103a",
@@ -43,15 +56,23 @@ def test_kernel_series_coefficients():
         out = subprocess.run([exe], capture_output=True, text=True, timeout=60)
     assert out.returncode == 0, out.stderr
     vals = out.stdout.split()
-    n = int(vals[0])
-    got = [float(v) for v in vals[1:]]
-    assert n == len(got) == 7
-    for k, g in enumerate(got, start=1):
-        want = float(_coef(k))
-        assert abs(g - want) <= 2 ** -23 * abs(want), (k, g, want)
-    # the truncated series against the oracle's log(sinh a / a) on a <= 1
-    a = np.linspace(0.0, 1.0, 1001)
-    t = a * a
-    series = sum(float(_coef(k)) * t ** k for k in range(1, n + 1))
-    bound = abs(float(_coef(n + 1))) * t ** (n + 1) * 1.01 + 1e-16
-    assert np.all(np.abs(series - O.log_sinhc(a)) <= bound)
+    nf, t_max = int(vals[0]), float(vals[1])
+    fit = np.array([float(v) for v in vals[2:2 + nf]])
+    assert len(fit) == nf
+    mod = _generator()
+    assert (nf, t_max) == (mod.N_TERMS, mod.T_MAX) == (8, 9.0)
+    # the header's constants are the generator's, rounded to fp32 (printed
+    # with 10 significant digits, which round-trip fp32)
+    np.testing.assert_array_equal(fit.astype(np.float32), mod.fit_coefficients().astype(np.float32))
+    # fp32 Horner in t = a^2, as the kernels evaluate it, against the oracle
+    a = np.linspace(0.0, np.sqrt(t_max), 4001)
+    t = (a * a).astype(np.float32)
+    acc = np.full_like(t, np.float32(fit[-1]))
+    for c in fit[-2::-1]:
+        acc = (acc * t + np.float32(c)).astype(np.float32)
+    err = np.abs((acc * t).astype(np.float64) - O.log_sinhc(a))
+    assert err.max() <= 5e-7, err.max()
+    # near 0 the fit is the Taylor series: c_1 = 1/6, c_2 = -1/180
+    for k in (1, 2):
+        want = float(_taylor(k))
+        assert abs(fit[k - 1] - want) <= 1e-3 * abs(want), (k, fit[k - 1], want)
