@@ -109,9 +109,11 @@ class ClockSampler:
 
 def kernel_source_hash() -> str:
     """First 16 hex digits of the SHA-256 of the attention kernel's source
-    (the kernel templates and the unit that instantiates the default mode)."""
+    (the kernel templates, the headers they include and the unit that
+    instantiates the default mode)."""
     h = hashlib.sha256()
-    for name in ("kvq_attn_kernel.cuh", "kvq_attn.cu"):
+    for name in ("kvq_attn_kernel.cuh", "kvq_attn.cu", "kvq_sm100.cuh", "kvq_checks.cuh",
+                 "kvq_fwht.cuh"):
         with open(os.path.join(ROOT, "quantized_kv_cache_quantize_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
@@ -217,6 +219,7 @@ def run_gpu(args):
         step()
     e1.record(stream)
     torch.cuda.synchronize()
+    launches = kvq.profile_kernel_launches()
     prof = kvq.profile_end()
     if world > 1:
         dist.barrier()
@@ -255,7 +258,6 @@ def run_gpu(args):
     # pass: it reads the window's (step, zero) words and the BF16 query
     if auto:
         rot_bytes += w.n_s * (d // w.group) * 4.0 * B * H + w.n_q * d * 2.0 * B * H
-    launches = sum(v["launches"] for v in prof.values())
 
     # end to end through the public API with host buffers (pinned), copies inside the timed
     # region.  Serving-style pipeline: step i's inputs are copied in on one stream while
@@ -613,6 +615,9 @@ def main(argv=None):
                          "oracle's stored answers, attention-mass shift, throughput)")
     ap.add_argument("--precise-query", action="store_true",
                     help="split the rotated query into FP16 high + low parts")
+    ap.add_argument("--staged-words", action="store_true",
+                    help="stage the cached tiles' packed words into shared memory with TMA bulk "
+                         "copies (head_dim 128, INT2 g32; for comparisons)")
     ap.add_argument("--one-cta", action="store_true",
                     help="run the one-CTA attention kernel where the SM-pair kernel applies "
                          "(for comparisons)")
@@ -626,7 +631,8 @@ def main(argv=None):
     check_world(args.gpus)
     args.warmup = max(3, args.warmup)   # at least 3 untimed warm-up steps
     args.corr = {v: k for k, v in CORR_NAMES.items()}[args.corr]
-    args.flags = (1 if args.precise_query else 0) | (4 if args.one_cta else 0)
+    args.flags = (1 if args.precise_query else 0) | (4 if args.one_cta else 0) | \
+        (8 if args.staged_words else 0)
     args.key_mode = 1 if args.keys == "channel" else 0
     if args.impl == "reference":
         return run_reference(args)

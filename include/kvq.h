@@ -51,7 +51,8 @@ typedef enum {
   KVQ_ERR_TIMEOUT = 5,      /* a kernel's bounded wait ran out              */
   KVQ_ERR_ALIGNMENT = 6,    /* a pointer is not 16-byte aligned             */
   KVQ_ERR_TOO_LARGE = 7,    /* needs more than the built-in scratch holds   */
-  KVQ_ERR_RANGE = 8         /* an operand left the FP16 range (see below)   */
+  KVQ_ERR_RANGE = 8,        /* an operand left the FP16 range (see below)   */
+  KVQ_ERR_BOUNDS = 9        /* checked build only: an index left its buffer */
 } kvq_status;
 
 /* Correction applied to cached-key scores before the softmax. */
@@ -92,13 +93,24 @@ typedef enum {
  */
 #define KVQ_FLAG_NO_KV_SPLIT 2
 /*
- * KVQ_FLAG_ONE_CTA: head_dim 128 with per-token keys and no correction or the
- * Taylor term runs by default on SM pairs (two CTAs of a cluster share each
- * key tile's dequantization and one M = 256 tensor-core MMA); this flag runs
- * the one-CTA kernel instead (for comparisons).  Same results within the
- * tolerances; an implementation choice of this library.
+ * KVQ_FLAG_ONE_CTA: with head_dim 128, per-token keys and no correction or
+ * the Taylor term, the library chooses per head whether the rotated query
+ * needs the precise split, and runs those heads on SM pairs (two CTAs of a
+ * cluster share each key tile's dequantization and one M = 256 tensor-core
+ * MMA).  This flag turns the choice off: every head runs on the one-CTA
+ * kernel without the split (for comparisons; KVQ_FLAG_PRECISE_QUERY still
+ * forces the split).  An implementation choice of this library.
  */
 #define KVQ_FLAG_ONE_CTA 4
+/*
+ * KVQ_FLAG_STAGED_WORDS: for head_dim 128, INT2 groups of 32 and the heads
+ * that run without the precise split, the one-CTA kernel stages each cached
+ * tile's packed codes and (step, zero) words into shared memory with TMA
+ * bulk copies, one tile ahead, instead of loading them per thread.  Same
+ * results (bit for bit); measured ~7 % slower on GB300, so off by default.
+ * Other geometries ignore it.  An implementation choice of this library.
+ */
+#define KVQ_FLAG_STAGED_WORDS 8
 
 /*
  * Key quantization scheme of a cache (kvq_cache.key_mode).
@@ -238,8 +250,8 @@ size_t kvq_workspace_bytes(const kvq_cache *cache, int32_t n_q, int32_t n_r);
  *          (exact products, fp32 accumulation);
  *   one softmax over both segments; out = sum_i p_ij v_i in the ORIGINAL
  *   basis (cached values un-rotated).
- * flags: any combination of KVQ_FLAG_PRECISE_QUERY, KVQ_FLAG_NO_KV_SPLIT and
- * KVQ_FLAG_ONE_CTA (0 for none).
+ * flags: any combination of KVQ_FLAG_PRECISE_QUERY, KVQ_FLAG_NO_KV_SPLIT,
+ * KVQ_FLAG_ONE_CTA and KVQ_FLAG_STAGED_WORDS (0 for none).
  * out: BF16 [batch][heads][n_q][d] device (required).  p_s, p_r: optional
  * (NULL to skip) fp32 [batch][heads][n_q] device: the attention masses of the
  * cached block and of the current chunk per query row (Figure 2 caption).
@@ -287,10 +299,26 @@ kvq_status kvq_rotate(const uint16_t *x, int64_t rows, int32_t d,
 /*
  * Synchronizes `stream`, then returns and clears the device status word of
  * the current device (KVQ_OK, or the first in-kernel error since the last
- * call: KVQ_ERR_TIMEOUT or KVQ_ERR_RANGE).  Returns KVQ_ERR_CUDA if the
- * synchronization failed.
+ * call: KVQ_ERR_TIMEOUT, KVQ_ERR_RANGE, or in the checked build
+ * KVQ_ERR_BOUNDS).  Returns KVQ_ERR_CUDA if the synchronization failed.
  */
 kvq_status kvq_last_device_status(void *stream);
+
+/*
+ * Checked build (the same sources compiled with -DKVQ_DEBUG_BOUNDS into
+ * libkvq_checked.so; a debugging aid, not the product's fast path): every
+ * kernel tests the indices of its global-memory accesses to the caches, the
+ * inputs and the outputs against the extents the call passed, skips an
+ * access that falls outside, and records KVQ_ERR_BOUNDS in the device status
+ * word and the source line of the first such check in a site word.
+ * Synchronizes `stream`, then stores and clears that line in *line (0 when
+ * no check failed; always 0 in the regular build, whose checks compile to
+ * nothing).  Returns KVQ_ERR_INVALID_ARG for a NULL line, KVQ_ERR_CUDA if
+ * the synchronization or the read failed.
+ */
+kvq_status kvq_debug_bounds_site(int32_t *line, void *stream);
+/* 1 in the checked build, 0 in the regular one. */
+int32_t kvq_debug_bounds_build(void);
 
 /*
  * Limit, in nanoseconds, of every bounded wait inside the kernels (default
@@ -348,14 +376,20 @@ kvq_status kvq_attention_corrected_noalloc(const kvq_cache *cache, const uint16_
 /*
  * Instrumentation (no counterpart in the paper).  Between kvq_profile_begin
  * and kvq_profile_end the library records a pair of CUDA events around each
- * of its kernel launches, on the stream the kernel is launched on.
- * kvq_profile_end waits for those events and returns, per kernel kind
+ * phase of a call, on the stream the call runs on: the quantize-append (one
+ * kernel, two with per-channel keys), the rotation (the rotation kernel, and
+ * the per-head selection pass before it in the automatic choice of the
+ * precise split), the attention (its kernels and the merge of a key-range
+ * split).  kvq_profile_end waits for those events and returns, per kind
  * (0 quantize-append, 1 rotation, 2 attention), the summed device time in
- * milliseconds and the number of launches, then stops recording.  At most
- * 16384 launches per kind are recorded.  Process-global; not thread-safe.
+ * milliseconds and the number of recorded phases, then stops recording.  At
+ * most 16384 phases per kind are recorded.  kvq_profile_kernel_launches
+ * returns the number of kernels the library launched since the last
+ * kvq_profile_begin while recording.  Process-global; not thread-safe.
  */
 kvq_status kvq_profile_begin(void);
 kvq_status kvq_profile_end(double ms_total[3], int32_t launches[3]);
+int64_t kvq_profile_kernel_launches(void);
 
 #ifdef __cplusplus
 }

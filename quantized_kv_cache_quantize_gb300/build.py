@@ -31,10 +31,16 @@ def nvcc() -> str:
     raise RuntimeError("nvcc not found")
 
 
-def _compile(src: str, verbose_ptxas: bool) -> str:
-    obj = os.path.join(BUILD, os.path.splitext(src)[0] + ".o")
+CHECKED_LIB = os.path.join(PKG, "libkvq_checked.so")
+
+
+def _compile(src: str, verbose_ptxas: bool, checked: bool = False) -> str:
+    out_dir = os.path.join(BUILD, "checked") if checked else BUILD
+    obj = os.path.join(out_dir, os.path.splitext(src)[0] + ".o")
     cmd = [nvcc(), "-O3", "-std=c++17", *ARCH, "-lineinfo", "-Xcompiler", "-fPIC",
            "-I", os.path.join(ROOT, "include"), "-c", os.path.join(CSRC, src), "-o", obj]
+    if checked:
+        cmd[1:1] = ["-DKVQ_DEBUG_BOUNDS"]
     if verbose_ptxas:
         cmd[1:1] = ["-Xptxas", "-v"]
     r = subprocess.run(cmd, capture_output=True, text=True)
@@ -45,18 +51,22 @@ def _compile(src: str, verbose_ptxas: bool) -> str:
     return obj
 
 
-def build(verbose_ptxas: bool = False) -> str:
-    os.makedirs(BUILD, exist_ok=True)
+def build(verbose_ptxas: bool = False, checked: bool = False) -> str:
+    """libkvq.so, or with checked=True libkvq_checked.so: the same sources with
+    -DKVQ_DEBUG_BOUNDS, whose kernels test their global-memory indices (a
+    debugging build; see kvq_debug_bounds_site in include/kvq.h)."""
+    os.makedirs(os.path.join(BUILD, "checked") if checked else BUILD, exist_ok=True)
     with ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
-        objs = list(ex.map(lambda s: _compile(s, verbose_ptxas), SOURCES))
-    tmp = LIB + ".tmp"
+        objs = list(ex.map(lambda s: _compile(s, verbose_ptxas, checked), SOURCES))
+    lib = CHECKED_LIB if checked else LIB
+    tmp = lib + ".tmp"
     cmd = [nvcc(), "-shared", *ARCH, "-o", tmp, *objs]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":
-    print(build(verbose_ptxas="-v" in sys.argv))
+    print(build(verbose_ptxas="-v" in sys.argv, checked="--checked" in sys.argv))

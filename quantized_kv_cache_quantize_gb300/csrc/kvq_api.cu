@@ -29,6 +29,7 @@ struct Profiler {
   int used[kKinds] = {0, 0, 0};
 };
 Profiler g_prof;
+std::atomic<long long> g_kernel_launches{0};
 
 struct ProfScope {
   int kind;
@@ -170,7 +171,8 @@ kvq_status attention_common(const kvq_cache* cache, const uint16_t* q, const uin
   if (n_q < 0 || n_r < 0 || n_q > (1 << 30) || n_r > (1 << 30)) return KVQ_ERR_INVALID_ARG;
   if (corr != KVQ_CORR_NONE && corr != KVQ_CORR_TAYLOR && corr != KVQ_CORR_EXACT)
     return KVQ_ERR_INVALID_ARG;
-  if ((flags & ~(KVQ_FLAG_PRECISE_QUERY | KVQ_FLAG_NO_KV_SPLIT | KVQ_FLAG_ONE_CTA)) != 0)
+  if ((flags & ~(KVQ_FLAG_PRECISE_QUERY | KVQ_FLAG_NO_KV_SPLIT | KVQ_FLAG_ONE_CTA |
+                 KVQ_FLAG_STAGED_WORDS)) != 0)
     return KVQ_ERR_INVALID_ARG;
   const bool precise = (flags & KVQ_FLAG_PRECISE_QUERY) != 0;
   // one query tile per CTA: the precise-query split, or the exact correction
@@ -240,6 +242,7 @@ kvq_status attention_common(const kvq_cache* cache, const uint16_t* q, const uin
   // keys and the Taylor term the pre-pass squares the query (q'^2 / 64 in
   // FP16): |q'| < 2047
   ra.status = status;
+  ra.bounds_site = kvq::bounds_site_ptr();
   ra.range_limit[0] = (g.key_mode == KVQ_KEYS_PER_CHANNEL && corr == KVQ_CORR_TAYLOR) ? 2047.0f
                                                                                      : 65504.0f;
   ra.range_limit[1] = 65504.0f;
@@ -272,6 +275,7 @@ kvq_status attention_common(const kvq_cache* cache, const uint16_t* q, const uin
   a.scale = scale;
   a.corr = corr;
   a.precise_query = precise ? 1 : 0;
+  a.staged_words = (flags & KVQ_FLAG_STAGED_WORDS) != 0 ? 1 : 0;
   a.mass_only = mass_only ? 1 : 0;
   a.out = out;
   a.p_s = p_s;
@@ -312,6 +316,8 @@ const char* kvq_status_string(kvq_status s) {
       return "problem needs more scratch than kvq_attention_corrected_noalloc's built-in buffer";
     case KVQ_ERR_RANGE:
       return "an operand left the FP16 range of the tensor-core operands (results invalid)";
+    case KVQ_ERR_BOUNDS:
+      return "checked build: an index left its buffer (see kvq_debug_bounds_site)";
   }
   return "unknown status";
 }
@@ -381,6 +387,8 @@ kvq_status kvq_quantize_append(kvq_cache* cache, const uint16_t* k_new, const ui
   kvq::row_divisor((uint32_t)n_new, &a.div_mul, &a.div_shift);
   a.kblk_first = cache->head_slot * g.bpc;
   a.kblk_per_head = cache->n_chunks * g.bpc;
+  a.status = kvq::status_ptr();
+  a.bounds_site = kvq::bounds_site_ptr();
   bool supported = true;
   {
     ProfScope prof(0, static_cast<cudaStream_t>(stream));
@@ -444,6 +452,10 @@ kvq_status kvq_rotate(const uint16_t* x, int64_t rows, int32_t d, const uint32_t
   for (int i = 0; i < 4; ++i) a.sign_bits[i] = sign_bits[i];
   a.inv_sqrt_d = (float)(1.0 / std::sqrt((double)d));
   a.out_f32 = out_f32 ? 1 : 0;
+  // no FP16 range limits here (range_limit 0); the status word serves the
+  // checked build's index checks
+  a.status = kvq::status_ptr();
+  a.bounds_site = kvq::bounds_site_ptr();
   return kvq::launch_rotate(a, d, static_cast<cudaStream_t>(stream)) == cudaSuccess ? KVQ_OK
                                                                                     : KVQ_ERR_CUDA;
 }
@@ -453,6 +465,23 @@ kvq_status kvq_last_device_status(void* stream) {
   int st = 0;
   if (kvq::read_and_clear_attention_status(&st) != KVQ_OK) return KVQ_ERR_CUDA;
   return static_cast<kvq_status>(st);
+}
+
+kvq_status kvq_debug_bounds_site(int32_t* line, void* stream) {
+  if (line == nullptr) return KVQ_ERR_INVALID_ARG;
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return KVQ_ERR_CUDA;
+  int v = 0;
+  if (kvq::read_and_clear_bounds_site(&v) != KVQ_OK) return KVQ_ERR_CUDA;
+  *line = v;
+  return KVQ_OK;
+}
+
+int32_t kvq_debug_bounds_build(void) {
+#ifdef KVQ_DEBUG_BOUNDS
+  return 1;
+#else
+  return 0;
+#endif
 }
 
 kvq_status kvq_set_wait_limit_ns(uint64_t limit_ns) {
@@ -470,9 +499,12 @@ kvq_status kvq_selftest_wait_timeout(uint64_t limit_ns, void* stream) {
 
 kvq_status kvq_profile_begin(void) {
   for (int k = 0; k < kKinds; ++k) g_prof.used[k] = 0;
+  g_kernel_launches.store(0);
   g_prof.on = true;
   return KVQ_OK;
 }
+
+int64_t kvq_profile_kernel_launches(void) { return g_kernel_launches.load(); }
 
 kvq_status kvq_profile_end(double ms_total[3], int32_t launches[3]) {
   g_prof.on = false;
@@ -533,6 +565,10 @@ bool current_context_id(unsigned long long* id) {
 }  // namespace
 
 namespace kvq {
+
+void note_launch() {
+  if (g_prof.on) g_kernel_launches.fetch_add(1, std::memory_order_relaxed);
+}
 
 cudaError_t device_symbol_address(const void* symbol, SymbolSlot& slot, void** out) {
   int dev = -1;

@@ -11,6 +11,8 @@ namespace {
 
 // first error of a bounded wait in any attention kernel (KVQ_OK if none)
 __device__ int g_attn_status;
+// checked build: the source line of the first failed index check
+__device__ int g_bounds_site;
 
 __global__ void wait_selftest_kernel(unsigned long long limit_ns) {
   __shared__ __align__(8) uint64_t b;
@@ -29,6 +31,9 @@ __global__ void wait_selftest_kernel(unsigned long long limit_ns) {
 template <int D, int BITS, int GROUP>
 kvq_status launch_mode(const AttnLaunch& a, cudaStream_t stream, int select) {
   if (a.precise_query) return launch_t<D, BITS, GROUP, 1, true, false, false>(a, stream, select);
+  if constexpr (D == 128 && BITS == 2 && GROUP == 32) {
+    if (a.staged_words) return launch_t<D, BITS, GROUP, 2, false, false, false, true>(a, stream, select);
+  }
   return launch_t<D, BITS, GROUP, 2, false, false, false>(a, stream, select);
 }
 
@@ -133,6 +138,7 @@ __global__ void __launch_bounds__(256) select_norms_kernel(const uint32_t* k_sz,
 }
 
 SymbolSlot g_status_slot;
+SymbolSlot g_site_slot;
 
 }  // namespace
 
@@ -141,6 +147,20 @@ int* status_ptr() {
   void* p = nullptr;
   if (device_symbol_address(&g_attn_status, g_status_slot, &p) != cudaSuccess) return nullptr;
   return static_cast<int*>(p);
+}
+
+// device address of the checked build's site word (current device and context)
+int* bounds_site_ptr() {
+  void* p = nullptr;
+  if (device_symbol_address(&g_bounds_site, g_site_slot, &p) != cudaSuccess) return nullptr;
+  return static_cast<int*>(p);
+}
+
+kvq_status read_and_clear_bounds_site(int* line) {
+  int zero = 0;
+  if (cudaMemcpyFromSymbol(line, g_bounds_site, sizeof(int)) != cudaSuccess) return KVQ_ERR_CUDA;
+  if (cudaMemcpyToSymbol(g_bounds_site, &zero, sizeof(int)) != cudaSuccess) return KVQ_ERR_CUDA;
+  return KVQ_OK;
 }
 
 cudaError_t launch_select_norms(const uint32_t* k_sz, const uint16_t* q, int bh, int n_s, int cap,
@@ -157,12 +177,15 @@ cudaError_t launch_select_norms(const uint32_t* k_sz, const uint16_t* q, int bh,
   if (g == 4) {
     select_norms_kernel<4><<<grid, 256, 0, stream>>>(k_sz, q, n_s, cap, n_q, kblocks, group, qmax,
                                                      kn2, qn2);
+    note_launch();
   } else if (g == 2) {
     select_norms_kernel<2><<<grid, 256, 0, stream>>>(k_sz, q, n_s, cap, n_q, kblocks, group, qmax,
                                                      kn2, qn2);
+    note_launch();
   } else {
     select_norms_kernel<1><<<grid, 256, 0, stream>>>(k_sz, q, n_s, cap, n_q, kblocks, group, qmax,
                                                      kn2, qn2);
+    note_launch();
   }
   return cudaGetLastError();
 }
@@ -171,6 +194,7 @@ kvq_status launch_attention(const AttnLaunch& a_in, int d, int bits, int group, 
   AttnLaunch a = a_in;
   a.status = status_ptr();
   if (a.status == nullptr) return KVQ_ERR_CUDA;
+  a.bounds_site = bounds_site_ptr();
   kvq_status st;
   if (a.mode == kModePair) {
     st = launch_attention_pair(a, bits, group, 0, stream);
@@ -208,6 +232,7 @@ kvq_status read_and_clear_attention_status(int* status) {
 
 cudaError_t launch_wait_selftest(unsigned long long limit_ns, cudaStream_t stream) {
   wait_selftest_kernel<<<1, 32, 0, stream>>>(limit_ns);
+  note_launch();
   return cudaGetLastError();
 }
 

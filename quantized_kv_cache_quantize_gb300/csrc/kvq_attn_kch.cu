@@ -310,6 +310,7 @@ kvq_status launch_kch_table(const AttnLaunch& a, cudaStream_t stream) {
     // log(sinh a / a) per channel: the CUDA-core form
     const dim3 kg((a.n_q + kKchRows - 1) / kKchRows, (a.n_ct + kKchCols - 1) / kKchCols, a.bh);
     kch_bias_kernel<D><<<kg, kKchThreads, 0, stream>>>(k);
+    note_launch();
   } else {
     const dim3 kg((a.n_q + 127) / 128, (a.n_ct + kKgN - 1) / kKgN, a.bh);
     // two 32 KB chunk buffers (at most three CTAs, 3 x 128 tensor-memory
@@ -318,6 +319,7 @@ kvq_status launch_kch_table(const AttnLaunch& a, cudaStream_t stream) {
     static std::atomic<uint64_t> kg_limit{0};
     if (ensure_smem_limit(kch_gemm_kernel<D>, smem, kg_limit) != cudaSuccess) return KVQ_ERR_CUDA;
     kch_gemm_kernel<D><<<kg, kKgThreads, smem, stream>>>(k);
+    note_launch();
   }
   return cudaGetLastError() == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
 }

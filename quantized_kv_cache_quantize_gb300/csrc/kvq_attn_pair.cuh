@@ -847,6 +847,7 @@ kvq_status launch_pair_t(const AttnLaunch& a, cudaStream_t stream, int select) {
   p.o_part = split ? a.o_part : nullptr;
   p.st_part = split ? a.st_part : nullptr;
   p.status = a.status;
+  p.bounds_site = a.bounds_site;
   p.select = select;
   p.select_scale = a.scale * (1.0f / 4096.0f);
   p.qn2 = a.qn2;
@@ -854,6 +855,7 @@ kvq_status launch_pair_t(const AttnLaunch& a, cudaStream_t stream, int select) {
   const unsigned pairs = (unsigned)((a.n_q + 2 * kBlockM * NQ - 1) / (2 * kBlockM * NQ));
   const dim3 grid(2 * pairs, a.bh, split ? a.splits : 1);
   kern<<<grid, C::kThreads, C::kAlloc, stream>>>(mq, mqlo, mqo, mk, mv, p);
+  note_launch();
   return cudaGetLastError() == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
 }
 

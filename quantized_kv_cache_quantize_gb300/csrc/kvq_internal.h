@@ -48,6 +48,9 @@ struct QuantArgs {
   // head; this append's blocks start at block kblk_first
   int kblk_first;
   int kblk_per_head;
+  // checked build: where a failed index check is recorded
+  int* status;
+  int* bounds_site;
 };
 
 // Arguments of the rotation kernel: up to two row segments in one launch.
@@ -65,6 +68,7 @@ struct RotateArgs {
   int out_f32;
   int* status;
   float range_limit[2];
+  int* bounds_site;   // checked build: source line of the first failed index check
 };
 
 // Raise a kernel's dynamic shared-memory limit once per device (the
@@ -146,6 +150,7 @@ struct AttnLaunch {
   float scale;
   int corr;
   int precise_query;
+  int staged_words;   // KVQ_FLAG_STAGED_WORDS: cached packed words staged by TMA
   int mass_only;
   uint16_t* out;
   float* p_s;
@@ -162,6 +167,7 @@ struct AttnLaunch {
   int key_mode, chunk, bpc, kblk_per_head, n_ct;
   float* kch_c;
   int* status;      // device status word, set by launch_attention
+  int* bounds_site; // checked build's site word, set by launch_attention
   // kernels (attention_shape): kModeOneCta / kModePair / kModeAuto; with
   // kModeAuto the per-head maxima of ||q'||^2 and of the key-norm bound
   // (workspace, [bh] each) that pick each head's kernel
@@ -278,6 +284,10 @@ kvq_status launch_attention(const AttnLaunch& a, int d, int bits, int group,
 // device address of the attention status word (first in-kernel error since
 // it was last read) in the current device's current context, or null
 int* status_ptr();
+// counts a kernel launch of this library while kvq_profile_begin/end records
+void note_launch();
+int* bounds_site_ptr();
+kvq_status read_and_clear_bounds_site(int* line);
 // the attention kernels of the exact correction and of per-channel keys,
 // built in translation units of their own (a.status must be set)
 kvq_status launch_attention_exact(const AttnLaunch& a, int d, int bits, int group,

@@ -16,6 +16,7 @@
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
+#include "kvq_checks.cuh"
 #include "kvq_fwht.cuh"
 #include "kvq_internal.h"
 #include "kvq_sm100.cuh"
@@ -289,6 +290,9 @@ __device__ __forceinline__ void quantize_row(const QuantArgs& a, const PairSigns
 #pragma unroll
   for (int w = 0; w < D * BITS / 32; ++w) words[w] = pack_word<BITS>(x + PER_WORD * w, zf[(PER_WORD * w) / GROUP]);
 
+  if (!KVQ_IN_BOUNDS(a.first + tok, a.cap, a.status, a.bounds_site) ||
+      !KVQ_IN_BOUNDS(bh, a.bh, a.status, a.bounds_site))
+    return;
   const size_t dst_tok = (size_t)bh * a.cap + a.first + tok;
   uint4* dc = reinterpret_cast<uint4*>((is_v ? a.v_codes : a.k_codes) + dst_tok * CODE_BYTES);
 #pragma unroll
@@ -485,6 +489,9 @@ __device__ __forceinline__ void quantize_half_row(const QuantArgs& a, const uint
   if (!valid) return;
   const unsigned bh = a.div_mul ? (__umulhi(rk, a.div_mul) >> a.div_shift) : (rk >> a.div_shift);
   const unsigned tok = rk - bh * (unsigned)a.n_new;
+  if (!KVQ_IN_BOUNDS(a.first + tok, a.cap, a.status, a.bounds_site) ||
+      !KVQ_IN_BOUNDS(bh, a.bh, a.status, a.bounds_site))
+    return;
   const size_t dst_tok = (size_t)bh * a.cap + a.first + tok;
   // codes: channels [32 HF, 32 HF + 32) and [64 + 32 HF, ...) -> bytes
   // [4 HF BITS, ...) and [8 BITS + 4 HF BITS, ...)
@@ -766,7 +773,8 @@ __global__ void __launch_bounds__(kKcThreads) quantize_key_channels_kernel(const
       mx = fmaxf(mx, mm[(p2 * D + c) * 2 + 1]);
     }
     const QHdr h = group_header<BITS>(mn, mx);
-    if (part == 0) a.k_sz[((size_t)bh * a.kblk_per_head + a.kblk_first + blk) * D + c] = h.rec;
+    if (part == 0 && KVQ_IN_BOUNDS(a.kblk_first + blk, a.kblk_per_head, a.status, a.bounds_site))
+      a.k_sz[((size_t)bh * a.kblk_per_head + a.kblk_first + blk) * D + c] = h.rec;
 #pragma unroll 8
     for (int t = ta; t < tb; ++t) {
       const float v = rot[t * D + kc_pos<D>(c, t)];
@@ -784,7 +792,7 @@ __global__ void __launch_bounds__(kKcThreads) quantize_key_channels_kernel(const
     constexpr int NWH = NW / 2;             // words per thread
     constexpr int CH = NWH * PER_WORD / 16;  // 16-byte code chunks per thread
     const int t = tid >> 1, hw = tid & 1;
-    if (t < n) {
+    if (t < n && KVQ_IN_BOUNDS(a.first + t0 + t, a.cap, a.status, a.bounds_site)) {
       uint32_t words[NWH];
 #pragma unroll
       for (int w = 0; w < NWH; ++w) words[w] = 0u;
@@ -948,6 +956,7 @@ __global__ void __launch_bounds__(kRotThreads, kRotBlocksPerSm) rotate_kernel(co
     if (r >= total) continue;
     const bool s1 = r >= rows0;
     const long long rr = s1 ? r - rows0 : r;
+    if (!KVQ_IN_BOUNDS(rr, s1 ? a.rows[1] : a.rows[0], a.status, a.bounds_site)) continue;
     void* dstp = s1 ? a.dst[1] : a.dst[0];
     uint16_t* lop = s1 ? a.dst_lo[1] : a.dst_lo[0];
     const float lim = s1 ? a.range_limit[1] : a.range_limit[0];
@@ -1038,6 +1047,7 @@ cudaError_t launch_q(const QuantArgs& a, cudaStream_t s) {
     const cudaError_t e = ensure_smem_limit(quantize_split_kernel<BITS, GROUP>, kSplitSmem, limit_set);
     if (e != cudaSuccess) return e;
     quantize_split_kernel<BITS, GROUP><<<blocks, kSplitWarps * 32, kSplitSmem, s>>>(a, sg);
+    note_launch();
     return cudaGetLastError();
   } else {
     const long long want = (tiles + kQWarps - 1) / kQWarps;
@@ -1048,6 +1058,7 @@ cudaError_t launch_q(const QuantArgs& a, cudaStream_t s) {
     const cudaError_t e = ensure_smem_limit(quantize_rows_kernel<D, BITS, GROUP>, smem, limit_set);
     if (e != cudaSuccess) return e;
     quantize_rows_kernel<D, BITS, GROUP><<<blocks, kQWarps * 32, smem, s>>>(a, sg);
+    note_launch();
     return cudaGetLastError();
   }
 }
@@ -1084,6 +1095,7 @@ cudaError_t launch_kc(const QuantArgs& a, cudaStream_t s) {
   if (e != cudaSuccess) return e;
   const dim3 grid((unsigned)((a.n_new + kKeyBlock - 1) / kKeyBlock), (unsigned)a.bh);
   quantize_key_channels_kernel<D, BITS><<<grid, kKcThreads, smem, s>>>(a);
+  note_launch();
   return cudaGetLastError();
 }
 
@@ -1107,8 +1119,10 @@ cudaError_t launch_rotate(const RotateArgs& a, int d, cudaStream_t stream) {
   const unsigned grid = (unsigned)grid_for_rows(rows, rows_per_block, kRotBlocksPerSm);
   if (d == 64) {
     rotate_kernel<64><<<grid, kRotThreads, 0, stream>>>(a);
+    note_launch();
   } else {
     rotate_kernel<128><<<grid, kRotThreads, 0, stream>>>(a);
+    note_launch();
   }
   return cudaGetLastError();
 }

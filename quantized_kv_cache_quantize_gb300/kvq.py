@@ -14,7 +14,9 @@ import numpy as np
 import torch
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_HERE, "libkvq.so")
+# KVQ_LIBRARY selects another build of the same C ABI, e.g. the checked
+# build (libkvq_checked.so, index checks in every kernel)
+LIB_PATH = os.environ.get("KVQ_LIBRARY") or os.path.join(_HERE, "libkvq.so")
 
 KVQ_OK = 0
 KVQ_ERR_INVALID_ARG = 1
@@ -25,6 +27,7 @@ KVQ_ERR_TIMEOUT = 5
 KVQ_ERR_ALIGNMENT = 6
 KVQ_ERR_TOO_LARGE = 7
 KVQ_ERR_RANGE = 8
+KVQ_ERR_BOUNDS = 9
 NOALLOC_SCRATCH_BYTES = 32 << 20
 
 KEYS_PER_TOKEN = 0
@@ -37,6 +40,7 @@ CORR_EXACT = 2
 FLAG_PRECISE_QUERY = 1
 FLAG_NO_KV_SPLIT = 2
 FLAG_ONE_CTA = 4
+FLAG_STAGED_WORDS = 8
 
 
 class KVQError(RuntimeError):
@@ -77,6 +81,9 @@ _SIGNATURES = {
                                           ctypes.c_size_t, _P, _P, _P]),
     "kvq_rotate": (ctypes.c_int, [_P, ctypes.c_int64, ctypes.c_int32, _P, _P, _P, _P]),
     "kvq_last_device_status": (ctypes.c_int, [_P]),
+    "kvq_debug_bounds_site": (ctypes.c_int, [ctypes.POINTER(ctypes.c_int32), _P]),
+    "kvq_debug_bounds_build": (ctypes.c_int32, []),
+    "kvq_profile_kernel_launches": (ctypes.c_int64, []),
     "kvq_set_wait_limit_ns": (ctypes.c_int, [ctypes.c_uint64]),
     "kvq_selftest_wait_timeout": (ctypes.c_int, [ctypes.c_uint64, _P]),
     "kvq_attention_corrected_noalloc": (ctypes.c_int, [_P, _P, _P, _P, ctypes.c_int32,
@@ -397,6 +404,22 @@ def last_device_status(stream=None, device=None) -> int:
         return int(lib().kvq_last_device_status(_stream(stream, dev)))
 
 
+def debug_bounds_site(stream=None, device=None) -> int:
+    """kvq_debug_bounds_site: the source line of the first failed index
+    check of the checked build since the last call (0: none)."""
+    dev = None if device is None else torch.device(device)
+    line = ctypes.c_int32(0)
+    with _on_device(dev):
+        _check(lib().kvq_debug_bounds_site(ctypes.byref(line), _stream(stream, dev)),
+               "kvq_debug_bounds_site")
+    return int(line.value)
+
+
+def debug_bounds_build() -> bool:
+    """True when the loaded library is the checked build."""
+    return bool(lib().kvq_debug_bounds_build())
+
+
 def set_wait_limit_ns(limit_ns: int):
     _check(lib().kvq_set_wait_limit_ns(int(limit_ns)), "kvq_set_wait_limit_ns")
 
@@ -409,6 +432,11 @@ def selftest_wait_timeout(limit_ns: int, stream=None):
 def profile_begin():
     """Start recording CUDA events around every libkvq kernel launch."""
     _check(lib().kvq_profile_begin(), "kvq_profile_begin")
+
+
+def profile_kernel_launches() -> int:
+    """Kernels launched by the library since profile_begin (while recording)."""
+    return int(lib().kvq_profile_kernel_launches())
 
 
 def profile_end() -> dict:

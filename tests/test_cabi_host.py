@@ -39,7 +39,7 @@ def test_exports_every_declared_symbol(lib):
 
 
 def test_status_strings(lib):
-    for s in range(9):
+    for s in range(10):
         assert kvq.status_string(s) != "unknown status"
     assert "FP16" in kvq.status_string(kvq.KVQ_ERR_RANGE)
     assert kvq.status_string(99) == "unknown status"
@@ -141,7 +141,7 @@ def test_attention_argument_checks(lib):
     # bad correction mode, bad flags, bad scale, missing output, workspace too small
     assert f(ctypes.byref(c), P, P, P, 100, 10, 0.1, 7, 0, P, ws, P, None, None, None) == 1
     assert f(ctypes.byref(c), P, P, P, 100, 10, 0.1, 3, 0, P, ws, P, None, None, None) == 1
-    assert f(ctypes.byref(c), P, P, P, 100, 10, 0.1, 1, 8, P, ws, P, None, None, None) == 1
+    assert f(ctypes.byref(c), P, P, P, 100, 10, 0.1, 1, 16, P, ws, P, None, None, None) == 1
     assert f(ctypes.byref(c), P, P, P, 100, 10, float("nan"), 1, 0, P, ws, P, None, None, None) == 1
     assert f(ctypes.byref(c), P, P, P, 100, 10, -1.0, 1, 0, P, ws, P, None, None, None) == 1
     assert f(ctypes.byref(c), P, P, P, 100, 10, 0.1, 1, 0, P, ws, None, None, None, None) == 1
@@ -327,6 +327,7 @@ def test_binding_mirrors_the_header():
     py = {"KVQ_CORR_NONE": kvq.CORR_NONE, "KVQ_CORR_TAYLOR": kvq.CORR_TAYLOR,
           "KVQ_CORR_EXACT": kvq.CORR_EXACT, "KVQ_FLAG_PRECISE_QUERY": kvq.FLAG_PRECISE_QUERY,
           "KVQ_FLAG_NO_KV_SPLIT": kvq.FLAG_NO_KV_SPLIT, "KVQ_FLAG_ONE_CTA": kvq.FLAG_ONE_CTA,
+          "KVQ_FLAG_STAGED_WORDS": kvq.FLAG_STAGED_WORDS,
           "KVQ_KEYS_PER_TOKEN": kvq.KEYS_PER_TOKEN, "KVQ_KEYS_PER_CHANNEL": kvq.KEYS_PER_CHANNEL,
           "KVQ_KEY_BLOCK": kvq.KEY_BLOCK}
     py.update((k, getattr(kvq, k)) for k in consts if k.startswith(("KVQ_OK", "KVQ_ERR_")))

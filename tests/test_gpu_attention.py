@@ -51,7 +51,8 @@ RAGGED = [
     (kvq.CORR_TAYLOR, 0), (kvq.CORR_NONE, 0), (kvq.CORR_TAYLOR, kvq.FLAG_PRECISE_QUERY),
     (kvq.CORR_TAYLOR, kvq.FLAG_NO_KV_SPLIT),
     (kvq.CORR_NONE, kvq.FLAG_PRECISE_QUERY | kvq.FLAG_NO_KV_SPLIT),
-    (kvq.CORR_EXACT, 0), (kvq.CORR_EXACT, kvq.FLAG_PRECISE_QUERY | kvq.FLAG_NO_KV_SPLIT)])
+    (kvq.CORR_EXACT, 0), (kvq.CORR_EXACT, kvq.FLAG_PRECISE_QUERY | kvq.FLAG_NO_KV_SPLIT),
+    (kvq.CORR_TAYLOR, kvq.FLAG_STAGED_WORDS)])
 def test_ragged_all_rows(case, corr, flags):
     """Sizes that are not multiples of the 128-token tile, an empty cache, an
     empty current chunk, single tokens; with and without the key-range split
@@ -117,6 +118,7 @@ def test_correction_restores_mass():
 @pytest.mark.parametrize("name,flags", [("w4_int2", 0), ("w4_int4", 0), ("w8_int2", 0),
                                         ("w4_int2", kvq.FLAG_PRECISE_QUERY),
                                         ("w4_int2", kvq.FLAG_ONE_CTA),
+                                        ("w4_int2", kvq.FLAG_STAGED_WORDS),
                                         ("hires_t3", 0),
                                         ("hires_t3", kvq.FLAG_PRECISE_QUERY)])
 def test_full_workload_sampled_rows(name, flags):
@@ -141,6 +143,28 @@ def test_full_workload_sampled_rows(name, flags):
         o_ref, ps_ref, pr_ref = oracle_head(w, x, s, 0, int(h), rows, O.CORR_TAYLOR)
         assert_close(out[0, h, rows].float().cpu().numpy(), o_ref, ps[0, h, rows].cpu().numpy(),
                      ps_ref, pr[0, h, rows].cpu().numpy(), pr_ref, what=f"{name} h{h}")
+
+
+def test_staged_words_bit_equal():
+    """KVQ_FLAG_STAGED_WORDS (the cached tiles' packed words staged into
+    shared memory by TMA bulk copies) changes where the words come from, not
+    what is computed: output and masses bit for bit those of the default
+    call, on a window with a partial last tile."""
+    w = synth.with_sizes(synth.WORKLOADS["w4_int2"], heads=3, chunk_tokens=1000, n_chunks=3)
+    x = synth.inputs(w, n_q=700, n_s=2900, n_r=300)
+    s = synth.hadamard_signs(w.head_dim)
+    cache = build_cache(w, x, s)
+    args = (cache, x["q"].cuda(), x["k_cur"].cuda(), x["v_cur"].cuda())
+    o0, ps0, pr0 = kvq.attention_corrected(*args, with_mass=True)
+    o1, ps1, pr1 = kvq.attention_corrected(*args, with_mass=True, flags=kvq.FLAG_STAGED_WORDS)
+    torch.cuda.synchronize()
+    assert kvq.last_device_status() == 0
+    assert torch.equal(o0, o1) and torch.equal(ps0, ps1) and torch.equal(pr0, pr1)
+    for h in range(w.heads):
+        rows = np.array([0, 1, 350, 699])
+        o_ref, ps_ref, pr_ref = oracle_head(w, x, s, 0, h, rows, O.CORR_TAYLOR)
+        assert_close(o1[0, h, rows].float().cpu().numpy(), o_ref, ps1[0, h, rows].cpu().numpy(),
+                     ps_ref, pr1[0, h, rows].cpu().numpy(), pr_ref, what=f"staged h{h}")
 
 
 def test_precise_split_chosen_per_head():

@@ -52,6 +52,7 @@ def test_kernel_fit_coefficients():
     with tempfile.TemporaryDirectory() as tmp:
         exe = os.path.join(tmp, "series_coef_check")
         subprocess.check_call([_nvcc(), "-std=c++17", "-gencode", "arch=compute_103a,code=sm_103a",
+                               "-I", os.path.join(HERE, "..", "include"),
                                "-o", exe, os.path.join(HERE, "series_coef_check.cu")])
         out = subprocess.run([exe], capture_output=True, text=True, timeout=60)
     assert out.returncode == 0, out.stderr
