@@ -318,6 +318,9 @@ def run_gpu(args):
     result = None
     if rank == 0:
         cpu = cpu_baseline(w, args) if (world == 1 and not args.no_cpu_baseline) else None
+        others = None
+        if world == 1 and not args.no_other_configs:
+            others = other_configs(dev, bf16_burst, hbm)
         acc = None
         if not args.no_accuracy:
             same = w.name in ACCURACY_WORKLOADS and args.seed == 0
@@ -360,6 +363,7 @@ def run_gpu(args):
                          "kernel": "attention (fused corrected chunk attention)"},
             "cpu_baseline": cpu,
             "accuracy": acc,
+            "other_configs": others,
         }
         print(json.dumps(result), flush=True)
     if world > 1:
@@ -469,6 +473,77 @@ def accuracy_report(x, dev, reps: int = 10):
         rep[name] = entry
         del cache
     return rep
+
+
+OTHER_WORKLOADS = ("w8_int2", "hires_t3")
+
+
+def other_configs(dev, peak: float, hbm: float, reps: int = 5):
+    """The larger configurations in one line each (default call: Taylor
+    term, per-head choice of the precise split): the attention call's
+    device time (CUDA events, `reps` calls after 2 untimed ones) and the
+    quantize-append of one chunk, on the workloads' seeded inputs."""
+    import torch
+
+    from quantized_kv_cache_quantize_gb300 import kvq, synth
+
+    out_rep = {}
+    for name in OTHER_WORKLOADS:
+        w = synth.WORKLOADS[name]
+        x = synth.inputs(w)
+        signs = synth.hadamard_signs(w.head_dim)
+        cache = kvq.KVCache(w.batch, w.heads, w.head_dim, w.bits, w.group, w.chunk_tokens,
+                            w.n_chunks, signs, device=dev)
+        kw, vw = x["k_win"].to(dev), x["v_win"].to(dev)
+        for c in range(w.n_chunks):
+            sl = slice(c * w.chunk_tokens, (c + 1) * w.chunk_tokens)
+            kvq.quantize_append(cache, kw[:, :, sl].contiguous(), vw[:, :, sl].contiguous())
+        del kw, vw
+        q, kc, vc = x["q"].to(dev), x["k_cur"].to(dev), x["v_cur"].to(dev)
+        kn, vn = x["k_new"].to(dev), x["v_new"].to(dev)
+        out = torch.empty_like(q)
+        ps = torch.empty(q.shape[:-1], dtype=torch.float32, device=dev)
+        pr = torch.empty_like(ps)
+        ws = torch.empty(cache.workspace_bytes(w.n_q, w.n_r), dtype=torch.uint8, device=dev)
+        stream = torch.cuda.current_stream(dev)
+
+        def attn():
+            kvq.lib().kvq_attention_corrected(
+                kvq.ctypes.byref(cache.struct), kvq._ptr(q), kvq._ptr(kc), kvq._ptr(vc), w.n_q,
+                w.n_r, kvq.ctypes.c_float(w.scale), kvq.CORR_TAYLOR, 0, kvq._ptr(ws), ws.numel(),
+                kvq._ptr(out), kvq._ptr(ps), kvq._ptr(pr), kvq._stream(stream))
+
+        def timed(fn, n):
+            for _ in range(2):
+                fn()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(n):
+                fn()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            return e0.elapsed_time(e1) / n
+
+        a_ms = timed(attn, reps)
+        q_ms = timed(lambda: kvq.quantize_append(cache, kn, vn, stream=stream), max(reps, 10))
+        if kvq.last_device_status() != 0:
+            raise RuntimeError(f"device status after the {name} runs")
+        flops = w.attention_flops()
+        out_rep[name] = {
+            "workload": _config(w)["workload"],
+            "attention_ms": round(a_ms, 4),
+            "attention_tflops": round(flops / (a_ms * 1e-3) / 1e12, 2),
+            "attention_frac": round(flops / (a_ms * 1e-3) / 1e12 / peak, 4),
+            "quantize_append_us": round(q_ms * 1e3, 2),
+            "quantize_gbs": round(w.append_bytes() / (q_ms * 1e-3) / 1e9, 1),
+            "quantize_frac_of_hbm": round(w.append_bytes() / (q_ms * 1e-3) / 1e9 / hbm, 4),
+        }
+        del cache, x, q, kc, vc, kn, vn, out, ps, pr, ws
+        torch.cuda.empty_cache()
+    out_rep["timing"] = (f"attention: CUDA events around {reps} calls after 2 untimed ones "
+                         "(bias term counted, burst peak); quantize-append: one chunk, 10 calls")
+    return out_rep
 
 
 def _oracle_sample(w, head: int, rows: int, seed: int, corr: int = 1, key_mode: int = 0):
@@ -610,6 +685,9 @@ def main(argv=None):
     ap.add_argument("--ref-rows", type=int, default=128,
                     help="query rows per step of the --impl reference sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-other-configs", action="store_true",
+                    help="skip the one-line timings of the 32-head long-window and the 40-head "
+                         "high-resolution workloads")
     ap.add_argument("--no-accuracy", action="store_true",
                     help="skip the INT2 g32 / INT4 g64 accuracy report (CUDA path against the "
                          "oracle's stored answers, attention-mass shift, throughput)")
