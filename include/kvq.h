@@ -199,14 +199,19 @@ kvq_status kvq_cache_meta_bytes(const kvq_cache *cache, size_t *k_sz_bytes,
  * Quantize-append one chunk (paper section 3: Hadamard rotation, then
  * Eq. (1) per token and group; Figure 1 caption: keys AND values, QuaRot +
  * RTN).  k_new, v_new: BF16 [batch][heads][n_new][head_dim] device.
- * Per row: x' = H x in fp32 (fast Walsh-Hadamard transform, butterflies in
- * the order h = 1, 2, ..., d/2, then times fl(1/sqrt(d))); per group
- * mn/mx; D = bf16((mx - mn) / (2^bits - 1)) (constant group: D = bf16(|mn|),
- * or 1); z = bf16(rint(-mn / D)); code = clamp(rint(x' / D) + z, 0, 2^bits-1)
- * (IEEE fp32, ties to even).  Writes slot `head_slot` (tokens
- * [head_slot * chunk_tokens, + n_new)).  With KVQ_KEYS_PER_CHANNEL the keys
- * take the same steps per channel over each block of KVQ_KEY_BLOCK tokens of
- * the chunk (mn/mx over the block's values of that channel).
+ * Per row: x' = fl(1/sqrt(d)) * S with S = Sylvester(d) diag(sigma) x summed
+ * in fp32 by the tensor cores (every product exact; the summation order is
+ * the hardware's, deterministic: a row gives the same bits wherever it sits
+ * in the input; kvq_rotate's fp32 output returns exactly these values); per
+ * group mn/mx; D = bf16((mx - mn) / (2^bits - 1)) (constant group:
+ * D = bf16(|mn|), or 1); z = bf16(rint(-mn / D)); code =
+ * clamp(rint(x' / D) + z, 0, 2^bits-1) (IEEE fp32, ties to even).  Writes
+ * slot `head_slot` (tokens [head_slot * chunk_tokens, + n_new)).  With
+ * KVQ_KEYS_PER_CHANNEL the keys take the same steps per channel over each
+ * block of KVQ_KEY_BLOCK tokens of the chunk (mn/mx over the block's values
+ * of that channel), on x' from the fast Walsh-Hadamard transform
+ * (butterflies in the order h = 1, 2, ..., d/2 in fp32, then times
+ * fl(1/sqrt(d))); the values stay per token as above.
  * Window rules: 0 <= n_new <= chunk_tokens (0 is a no-op); while the cache is
  * not full every earlier slot must be full (a partial chunk can only be the
  * last one appended); once full only whole chunks overwrite the oldest slot.
@@ -285,12 +290,17 @@ kvq_status kvq_attention_mass(const kvq_cache *cache, const uint16_t *q,
 
 /*
  * The rotation alone (paper section 3 "Hadamard rotation"), for checking:
- * x' = H x per row of x [rows][d] BF16 device, written as fp32 [rows][d]
- * (out_f32) -- exactly the fp32 values kvq_quantize_append quantizes -- or
- * rounded to FP16 (out_f16) -- exactly the tensor-core operands the
- * attention kernels read for q and the current chunk's values (the current
- * keys enter unrotated, in BF16).  Exactly one of
- * out_f32 / out_f16 must be non-NULL.  d in {64, 128}.
+ * x' = H x per row of x [rows][d] BF16 device, either
+ *   out_f32: fp32 [rows][d], the tensor-core product -- exactly the values
+ *            kvq_quantize_append quantizes per token; or
+ *   out_f16: FP16 [rows][d], the fast Walsh-Hadamard transform in fp32
+ *            (butterflies h = 1, 2, ..., d/2, then times fl(1/sqrt(d)))
+ *            rounded to FP16 -- exactly the tensor-core operands the
+ *            attention kernels read for q and the current chunk's values
+ *            (the current keys enter unrotated, in BF16).
+ * The two fp32 evaluations differ by rounding only (a few units of 2^-24
+ * relative to sum |x|).  Exactly one of out_f32 / out_f16 must be non-NULL.
+ * d in {64, 128}.
  */
 kvq_status kvq_rotate(const uint16_t *x, int64_t rows, int32_t d,
                       const uint32_t sign_bits[4], float *out_f32,

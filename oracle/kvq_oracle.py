@@ -29,11 +29,15 @@ Compression in Video Diffusion" (Tuncer, Becker, Pfeil), cited below as
   mode below quantizes each key channel over blocks of 128 tokens with the
   same Eq. (1), and the correction keeps its form with one channel per group.
 
-Everything is fp64 except two steps that are fp32 on purpose, because the
-GPU must reproduce them bit for bit: the rotation that feeds the quantizer
-(``rotate_fp32``, the textbook fast Walsh-Hadamard transform in fp32) and the
-code decision (``quantize_groups``).  Where the paper is silent the readings
-are listed in each docstring.
+Everything is fp64 except the steps that are fp32 on purpose, because the
+GPU reproduces them bit for bit: the code decision (``quantize_groups``) and
+the butterfly rotation (``rotate_fp32``, the textbook fast Walsh-Hadamard
+transform in fp32) that the attention's FP16 operands and the per-channel
+key quantizer use.  The per-token quantizer rotates on the tensor cores,
+which sum in an order of their own: for it ``rotation_bounds`` bounds every
+fp32 summation order and ``quantize_groups_admissible`` lists every answer
+Eq. (1) gives inside those bounds (one answer wherever the bounds fix it).
+Where the paper is silent the readings are listed in each docstring.
 
 Parity status: every function here is pinned by ``tests/test_oracle_pins.py``
 (closed forms, hand-worked fixtures under ``tests/golden``, brute force,
@@ -306,6 +310,140 @@ def quantize_rows(x_bf16, signs, bits: int, group: int):
     y = rotate_fp32(np.asarray(x_bf16, dtype=np.float32), signs)
     codes, delta, zero = quantize_groups(y, bits, group)
     return pack_codes(codes, bits), delta, zero, y, codes
+
+
+# ---------------------------------------------------------------------------
+# The rotation known to within a rounding bound, and every answer Eq. (1)
+# can give inside it.  For an fp32 rotation whose summation order is not
+# fixed (a tensor-core product sums the d exact products sigma_k H[n][k] x_k
+# in an order and with internal rounding of the hardware's choosing) the
+# codes are not one value but a small set; away from rounding boundaries
+# the set has one element.
+# ---------------------------------------------------------------------------
+
+
+def _round32(v, up: bool) -> np.ndarray:
+    """fp64 values rounded to fp32 toward +inf (up) or toward -inf."""
+    v = np.asarray(v, dtype=np.float64)
+    r = v.astype(np.float32)
+    if up:
+        return np.where(r.astype(np.float64) < v, np.nextafter(r, np.float32(np.inf)), r)
+    return np.where(r.astype(np.float64) > v, np.nextafter(r, np.float32(-np.inf)), r)
+
+
+def _lsb_exponent(x) -> np.ndarray:
+    """For fp32 values: q with x an odd multiple of 2^q (a large q for 0)."""
+    m, e = np.frexp(np.asarray(x, dtype=np.float64))      # x = m 2^e, 0.5 <= |m| < 1
+    mi = np.abs(m * 2.0 ** 24).astype(np.int64)              # 24-bit integer significand
+    tz = np.zeros_like(mi)
+    nz = mi != 0
+    low = mi[nz] & -mi[nz]                                   # lowest set bit
+    tz[nz] = np.log2(low.astype(np.float64)).astype(np.int64)
+    q = e.astype(np.int64) - 24 + tz
+    return np.where(nz, q, np.int64(1 << 20))
+
+
+def rotation_bounds(x, signs):
+    """Bounds [y_lo, y_hi] (fp32, elementwise) on any fp32 rotation of rows
+    x [..., d] computed as y = fl(S * fl(1/sqrt(d))), S an fp32 sum of the d
+    exact products sigma_k Sylvester(d)[n][k] x_k taken in any order, each
+    addition rounded to nearest or toward zero.
+
+    Bound on the sum (recursive summation, Higham, "Accuracy and Stability
+    of Numerical Algorithms", section 4.2): |S - sum| <= gamma_{d-1} *
+    sum_k |x_k|, gamma_n = n u / (1 - n u), u = 2^-23 (one unit of the 24-bit
+    significand, which covers truncation as well as rounding to nearest).
+    The bound is 0 for a row whose values are all multiples of 2^q with
+    sum_k |x_k| <= 2^(24 + q): every partial sum of such a row is an fp32
+    number, so every order gives the exact sum.  The exact sums are formed in
+    fp64 (exact for such rows; otherwise their own error, at most
+    d 2^-53 sum |x|, is added to the bound).  Then S lies in [RU(lo), RD(hi)]
+    and the multiply is monotone."""
+    x = np.asarray(x, dtype=np.float32)
+    d = x.shape[-1]
+    s = np.asarray(signs, dtype=np.float64)
+    exact_sum = x.astype(np.float64) @ (sylvester_hadamard(d) * s[None, :]).T   # [..., d]
+    abs_sum = np.abs(x.astype(np.float64)).sum(axis=-1, keepdims=True)
+    n = d - 1
+    u = 2.0 ** -23
+    gamma = n * u / (1.0 - n * u)
+    q = _lsb_exponent(x).min(axis=-1, keepdims=True)
+    on_grid = abs_sum <= np.ldexp(1.0, (24 + np.minimum(q, 990)).astype(np.int64))
+    eps = np.where(on_grid, 0.0, gamma * abs_sum + d * 2.0 ** -53 * abs_sum)
+    s_lo = _round32(exact_sum - eps, up=True).astype(np.float64)
+    s_hi = _round32(exact_sum + eps, up=False).astype(np.float64)
+    inv = np.float64(np.float32(1.0 / math.sqrt(float(d))))
+    return (s_lo * inv).astype(np.float32), (s_hi * inv).astype(np.float32)
+
+
+def _step_of(mn, mx, qmax):
+    """Eq. (1)'s BF16 step for one (min, max) pair, as quantize_groups; and
+    whether the constant-group rule (step 0 -> |min|, or 1) decided it."""
+    delta = bf16_round((mx - mn) / qmax)
+    fb = bf16_round(np.abs(mn))
+    fb = np.where(fb == 0, np.float32(1.0), fb).astype(np.float32)
+    return np.where(delta == 0, fb, delta).astype(np.float32), delta == 0
+
+
+def _zero_of(mn, delta):
+    return bf16_round(np.rint((-np.asarray(mn, np.float32)) / delta) + np.float32(0.0))
+
+
+def quantize_groups_admissible(y_lo, y_hi, bits: int, group: int):
+    """Every answer quantize_groups can give for fp32 rows y with
+    y_lo <= y <= y_hi elementwise.
+
+    Each step of quantize_groups is monotone given the ones before it: the
+    group's min and max in the values; the fp32 subtraction, the fp32
+    division by 2^B - 1 and the BF16 rounding in the span; the zero point
+    (decreasing) in the min for a fixed step; a code in its value for a fixed
+    step and zero point.  So the step lies between its values at the
+    smallest span (min_hi, max_lo) and the largest (min_lo, max_hi); for each
+    of those two steps the zero point between its values at min_hi and
+    min_lo; for each (step, zero) pair a code between its values at y_lo and
+    y_hi.  Returns four candidates per group: delta, zero [..., G, 4] and
+    code_lo, code_hi [..., G, 4, group] (uint8).  Raises ValueError where the
+    bounds are too wide for that enumeration (steps or zero points more than
+    one representable value apart, or a group that may or may not be
+    constant)."""
+    lo = np.asarray(y_lo, dtype=np.float32)
+    hi = np.asarray(y_hi, dtype=np.float32)
+    if np.any(lo > hi):
+        raise ValueError("y_lo > y_hi")
+    d = lo.shape[-1]
+    lead = lo.shape[:-1]
+    g_n = d // group
+    lo_g = lo.reshape(*lead, g_n, group)
+    hi_g = hi.reshape(*lead, g_n, group)
+    mn_lo, mn_hi = lo_g.min(axis=-1), hi_g.min(axis=-1)
+    mx_lo, mx_hi = lo_g.max(axis=-1), hi_g.max(axis=-1)
+    qmax = np.float32(2 ** bits - 1)
+    d_small, c_small = _step_of(mn_hi, mx_lo, qmax)
+    d_large, c_large = _step_of(mn_lo, mx_hi, qmax)
+    if np.any(c_small != c_large) or np.any(c_small & (mn_lo != mn_hi)):
+        raise ValueError("a group may or may not be constant within the bounds")
+    next_bf16 = from_bf16_bits((bf16_bits(d_small).astype(np.uint32) + 1).astype(np.uint16))
+    if np.any(d_large > next_bf16):
+        raise ValueError("steps more than one BF16 value apart")
+    deltas, zeros = [], []
+    for dl in (d_small, d_large):
+        z_a = _zero_of(mn_hi, dl)   # largest min: smallest zero point
+        z_b = _zero_of(mn_lo, dl)
+        if np.any(z_b - z_a > 1):
+            raise ValueError("zero points more than one apart")
+        for z in (z_a, z_b):
+            deltas.append(dl)
+            zeros.append(z)
+    delta = np.stack(deltas, axis=-1)                        # [..., G, 4]
+    zero = np.stack(zeros, axis=-1)
+
+    def codes(y, dl, z):
+        c = np.rint(y / dl[..., None]) + z[..., None]
+        return np.clip(c, np.float32(0.0), qmax).astype(np.uint8)
+
+    code_lo = np.stack([codes(lo_g, delta[..., i], zero[..., i]) for i in range(4)], axis=-2)
+    code_hi = np.stack([codes(hi_g, delta[..., i], zero[..., i]) for i in range(4)], axis=-2)
+    return delta, zero, code_lo, code_hi
 
 
 # ---------------------------------------------------------------------------

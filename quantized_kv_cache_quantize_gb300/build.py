@@ -19,7 +19,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libkvq.so")
-SOURCES = ["kvq_api.cu", "kvq_quant.cu", "kvq_attn.cu", "kvq_attn_exact.cu", "kvq_attn_kch.cu",
+SOURCES = ["kvq_api.cu", "kvq_quant.cu", "kvq_quant_mma.cu", "kvq_attn.cu", "kvq_attn_exact.cu", "kvq_attn_kch.cu",
            "kvq_attn_pair.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

@@ -389,11 +389,14 @@ kvq_status kvq_quantize_append(kvq_cache* cache, const uint16_t* k_new, const ui
   a.kblk_per_head = cache->n_chunks * g.bpc;
   a.status = kvq::status_ptr();
   a.bounds_site = kvq::bounds_site_ptr();
+  a.wait_limit_ns = g_wait_limit_ns.load();
+  if (a.status == nullptr) return KVQ_ERR_CUDA;
   bool supported = true;
   {
     ProfScope prof(0, static_cast<cudaStream_t>(stream));
-    if (kvq::launch_quantize_append(a, g.d, g.bits, g.group, static_cast<cudaStream_t>(stream),
-                                    &supported) != cudaSuccess)
+    if (kvq::launch_quantize_append_mma(a, g.d, g.bits, g.group,
+                                        static_cast<cudaStream_t>(stream),
+                                        &supported) != cudaSuccess)
       return KVQ_ERR_CUDA;
     if (!supported) return KVQ_ERR_UNSUPPORTED;
   }
@@ -443,6 +446,16 @@ kvq_status kvq_rotate(const uint16_t* x, int64_t rows, int32_t d, const uint32_t
   if (x == nullptr) return KVQ_ERR_INVALID_ARG;
   if (!aligned16(x) || (out_f32 && !aligned16(out_f32)) || (out_f16 && !aligned16(out_f16)))
     return KVQ_ERR_ALIGNMENT;
+  if (out_f32 != nullptr) {
+    // the per-token quantizer's rotation (tensor cores), exactly its values
+    int* status = kvq::status_ptr();
+    if (status == nullptr) return KVQ_ERR_CUDA;
+    return kvq::launch_rotate_mma_f32(x, rows, d, sign_bits, out_f32, status,
+                                      kvq::bounds_site_ptr(), g_wait_limit_ns.load(),
+                                      static_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? KVQ_OK
+               : KVQ_ERR_CUDA;
+  }
   kvq::RotateArgs a{};
   a.src[0] = x;
   a.dst[0] = out_f32 ? static_cast<void*>(out_f32) : static_cast<void*>(out_f16);

@@ -57,6 +57,7 @@
 
 #include "kvq_checks.cuh"
 #include "kvq_fwht.cuh"
+#include "kvq_tmap.cuh"
 #include "kvq_internal.h"
 #include "kvq_sm100.cuh"
 
@@ -1647,38 +1648,6 @@ __global__ void __launch_bounds__(256) merge_splits_kernel(const MergeArgs a) {
 }
 
 // ---- host side -------------------------------------------------------------
-
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void* f = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess) {
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
-    }
-  });
-  return fn;
-}
-
-// 3-D map over a [bh][n][d] 16-bit tensor, box [1][box_rows][64], 128-byte
-// swizzle, zero fill outside the tensor.
-bool make_map(CUtensorMap* m, const void* base, int d, int n, int bh, bool bf16,
-              int box_rows = 128) {
-  auto fn = encode_fn();
-  if (fn == nullptr) return false;
-  cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)n, (cuuint64_t)bh};
-  cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)n * d * 2};
-  cuuint32_t box[3] = {64, (cuuint32_t)box_rows, 1};
-  cuuint32_t estr[3] = {1, 1, 1};
-  CUresult r = fn(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
-                  const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
-}
 
 // the merge of a key-range split's partial results (one launch)
 template <int D>

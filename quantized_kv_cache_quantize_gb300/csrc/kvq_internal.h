@@ -51,6 +51,7 @@ struct QuantArgs {
   // checked build: where a failed index check is recorded
   int* status;
   int* bounds_site;
+  unsigned long long wait_limit_ns;   // bounded waits of the tensor-core quantizer
 };
 
 // Arguments of the rotation kernel: up to two row segments in one launch.
@@ -102,8 +103,6 @@ struct SymbolSlot {
 };
 cudaError_t device_symbol_address(const void* symbol, SymbolSlot& slot, void** out);
 
-cudaError_t launch_quantize_append(const QuantArgs& a, int d, int bits, int group,
-                                   cudaStream_t stream, bool* supported);
 // Multiplier and shift of the quotient r / d for every r < 2^31 and
 // 1 <= d < 2^31 (division by an invariant integer, Granlund and Montgomery):
 // with l = floor(log2 d), d not a power of two, m = ceil(2^(32+l) / d) fits
@@ -128,6 +127,15 @@ constexpr int kKeyBlock = 128;
 cudaError_t launch_quantize_key_channels(const QuantArgs& a, int d, int bits,
                                          cudaStream_t stream, bool* supported);
 cudaError_t launch_rotate(const RotateArgs& a, int d, cudaStream_t stream);
+// The per-token quantize-append with the rotation on the tensor cores
+// (kvq_quant_mma.cu), and its rotation alone: fp32 x' of `rows` BF16 rows,
+// exactly the values that quantizer quantizes.
+cudaError_t launch_quantize_append_mma(const QuantArgs& a, int d, int bits, int group,
+                                       cudaStream_t stream, bool* supported);
+cudaError_t launch_rotate_mma_f32(const uint16_t* x, long long rows, int d,
+                                  const uint32_t sign_bits[4], float* out, int* status,
+                                  int* bounds_site, unsigned long long wait_limit_ns,
+                                  cudaStream_t stream);
 
 // Attention ---------------------------------------------------------------
 

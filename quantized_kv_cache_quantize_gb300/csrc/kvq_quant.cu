@@ -1,22 +1,21 @@
-// Quantize-append and rotation kernels (sm_103a).
+// The rotation kernel and the per-channel key quantizer (sm_103a).
 //
-// Quantize-append: for every new K and V row, rotate (randomized Hadamard,
-// paper section 3), quantize per token and group with Eq. (1) (asymmetric
-// round-to-nearest, step and zero point covering [min, max]) and pack the
-// codes into the chunk slot of the sliding-window cache.
-//
-// Mapping: one thread per row (the whole row in registers, so the rotation
-// needs no data exchange between threads); each warp owns tiles of 32 rows
-// and stages the next tile into shared memory with asynchronous 16-byte
-// copies while it quantizes the current one.  Codes leave in 16-byte
-// stores, the (step, zero) records of a token in one store.  The kernel is
-// bound by HBM bandwidth: per row it reads 2d bytes and writes
-// d*bits/8 + 4*(d/group) bytes.
+// Both rotate with the fast Walsh-Hadamard transform (paper section 3,
+// "Hadamard rotation"): fp32 butterflies in the order h = 1, 2, ..., d/2,
+// then one multiply by fl(1/sqrt(d)), every step a correctly rounded fp32
+// operation, so the result is fixed bit for bit.
+// - rotate_kernel: the attention's operands (the query as FP16 high and low
+//   parts, the current chunk's values as FP16), and its range check.
+// - quantize_key_channels_kernel: the keys of an appended chunk in the
+//   per-channel key mode, Eq. (1) per channel over blocks of tokens.
+// The per-token quantize-append (keys and values, or values only in the
+// per-channel key mode) rotates on the tensor cores: kvq_quant_mma.cu.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 #include "kvq_checks.cuh"
+#include "kvq_eq1.cuh"
 #include "kvq_fwht.cuh"
 #include "kvq_internal.h"
 #include "kvq_sm100.cuh"
@@ -31,568 +30,6 @@ namespace {
 __device__ __forceinline__ uint32_t sign_word_for(const uint32_t (&sb)[4], int t) {
   const int i = (8 * t) >> 5;
   return i == 0 ? sb[0] : i == 1 ? sb[1] : i == 2 ? sb[2] : sb[3];
-}
-
-// Sign flips of the randomized rotation: word i of a BF16 row holds channels
-// 2i (low half) and 2i + 1 (high half).  XOR with m[i] flips the sign bit of
-// channel 2i + 1 (bit 31); channel 2i enters the first butterfly through an
-// FMA by sl[i] = +-1 (an exact product, so the butterfly still rounds once).
-struct PairSigns {
-  uint32_t m[64];
-  float sl[64];
-};
-
-// fl(x / d) from r = fl(1 / d): q0 = fl(x r), the exact residual x - q0 d by
-// FMA, one correction step.  Correctly rounded while neither the residual
-// nor the quotient leaves the normal range (Markstein's correction with a
-// correctly rounded reciprocal).
-__device__ __forceinline__ float div_step(float x, float d, float r) {
-  const float q0 = __fmul_rn(x, r);
-  return __fmaf_rn(__fmaf_rn(-q0, d, x), r, q0);
-}
-
-constexpr int kQWarps = 4;        // warps per block of the quantizer
-constexpr int kQBlocksPerSm = 3;
-
-__device__ __forceinline__ void cp_async16(void* smem_dst, const void* gmem_src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(ptx::smem_u32(smem_dst)),
-               "l"(gmem_src)
-               : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
-
-// Eq. (1) for one group given its min and max: the step covering
-// [min, max] and the integer zero point, both stored BF16 (the record is
-// step | zero << 16), and what the code decision needs.
-struct QHdr {
-  float delta, rcp, zero;
-  int zf;          // the zero point as an integer
-  bool fast;       // quotients by the reciprocal and one residual step
-  bool clamp;      // some code of the group leaves [0, 2^B - 1]
-  uint32_t rec;
-};
-
-template <int BITS>
-__device__ __forceinline__ QHdr group_header(float mn, float mx) {
-  constexpr float qmax = float((1 << BITS) - 1);
-  constexpr float kInvQmax = 1.0f / float((1 << BITS) - 1);   // fl(1 / qmax)
-  QHdr h;
-  const float span = __fsub_rn(mx, mn);
-  uint32_t dbits = bf16_bits_rn(span >= 0x1p-100f && span < 0x1p100f
-                                    ? div_step(span, qmax, kInvQmax)
-                                    : __fdiv_rn(span, qmax));
-  if (bf16_value(dbits) == 0.0f) {
-    dbits = bf16_bits_rn(fabsf(mn));
-    if (bf16_value(dbits) == 0.0f) dbits = 0x3F80u;  // 1.0
-  }
-  h.delta = bf16_value(dbits);
-  h.rcp = __frcp_rn(h.delta);
-  h.fast = h.rcp < 0x1p100f && fabsf(mn) * h.rcp < 0x1p21f && fabsf(mx) * h.rcp < 0x1p21f;
-  const float zq = h.fast ? div_step(-mn, h.delta, h.rcp) : __fdiv_rn(-mn, h.delta);
-  const uint32_t zbits = bf16_bits_rn(__fadd_rn(rintf(zq), 0.0f));
-  h.zero = bf16_value(zbits);
-  h.zf = __float2int_rn(h.zero);
-  h.rec = dbits | (zbits << 16);
-  // codes are monotone in x: those of the group's min and max bound them all
-  const float kMagic = 12582912.0f;   // 1.5 * 2^23
-  auto code_of = [&](float v) {
-    const float q0 = __fmul_rn(v, h.rcp);
-    const float q = __fmaf_rn(__fmaf_rn(-q0, h.delta, v), h.rcp, q0);
-    return __fadd_rn(__fadd_rn(q, kMagic), h.zero) - kMagic;
-  };
-  h.clamp = h.fast && (code_of(mn) < 0.0f || code_of(mx) > qmax);
-  return h;
-}
-
-// The code of one value of a group with header h (the arithmetic of
-// group_codes below, one value at a time).
-template <int BITS>
-__device__ __forceinline__ uint32_t code_of_value(float v, const QHdr& h) {
-  constexpr float qmax = float((1 << BITS) - 1);
-  const float kMagic = 12582912.0f;   // 1.5 * 2^23
-  if (h.fast) {
-    const float q0 = __fmul_rn(v, h.rcp);
-    const float q = __fmaf_rn(__fmaf_rn(-q0, h.delta, v), h.rcp, q0);
-    const float t = __fadd_rn(q, kMagic);
-    if (h.clamp) return __float_as_uint(fminf(fmaxf(__fadd_rn(t, h.zero), kMagic), kMagic + qmax)) - 0x4B400000u;
-    return (uint32_t)((int)(__float_as_uint(t) - 0x4B400000u) + h.zf);
-  }
-  const float t = fminf(fmaxf(__fadd_rn(rintf(__fdiv_rn(v, h.delta)), h.zero), 0.0f), qmax);
-  return (uint32_t)__float2int_rn(t);
-}
-
-// Eq. (1) for one group (or the part of it one thread holds) given the
-// group's min and max; the n values xg[0..n) are replaced by
-// 1.5 * 2^23 + code - zfold, zfold being the zero point when it is left for
-// the packing to add (0 otherwise).  Returns the record (step | zero << 16).
-//
-// Fast route: q = fl(x / delta) exactly, from the correctly rounded
-// reciprocal r and one residual step (q0 = fl(x r), e = x - q0 delta exact
-// by FMA, q = fl(q0 + e r): correctly rounded while nothing over- or
-// underflows); rint(q) by adding 1.5 * 2^23 (ties to even, |q| < 2^21); the
-// integer zero point added after the rounding.  K = 1.5 * 2^23 + code then
-// carries the code in its low mantissa bits.  The clamp to [0, 2^B - 1] is
-// needed only when the code of the group's min or max falls outside; when
-// it is not, the zero point is left to the packing (which adds it to a whole
-// half-word of codes at once).
-template <int BITS, int N>
-__device__ __forceinline__ uint32_t group_codes(float* xg, float mn, float mx, int& zfold) {
-  const float qmax = float((1 << BITS) - 1);
-  const QHdr h = group_header<BITS>(mn, mx);
-  const float kMagic = 12582912.0f;   // 1.5 * 2^23
-  if (h.fast) {
-    const uint64_t r2 = ptx::f2_pack(h.rcp, h.rcp);
-    const uint64_t nd2 = ptx::f2_pack(-h.delta, -h.delta);
-    const uint64_t m2 = ptx::f2_pack(kMagic, kMagic);
-#pragma unroll
-    for (int c = 0; c < N; c += 2) {
-      const uint64_t xv = ptx::f2_pack(xg[c], xg[c + 1]);
-      const uint64_t q0 = ptx::f2_mul(xv, r2);
-      const uint64_t e = ptx::f2_fma(q0, nd2, xv);
-      const uint64_t q = ptx::f2_fma(e, r2, q0);
-      ptx::f2_unpack(ptx::f2_add(q, m2), xg[c], xg[c + 1]);
-    }
-    zfold = h.zf;
-    if (h.clamp) {
-#pragma unroll
-      for (int c = 0; c < N; ++c) xg[c] = fminf(fmaxf(__fadd_rn(xg[c], h.zero), kMagic), kMagic + qmax);
-      zfold = 0;
-    }
-  } else {
-    zfold = 0;
-    // exact division element by element (huge quotients, tiny steps): a rare
-    // path, kept as one rolled loop over a local copy so that its divisions
-    // do not sit unrolled in the kernel's hot code
-    float tmp[N];
-#pragma unroll
-    for (int c = 0; c < N; ++c) tmp[c] = xg[c];
-#pragma unroll 1
-    for (int c = 0; c < N; ++c) {
-      float t = __fadd_rn(rintf(__fdiv_rn(tmp[c], h.delta)), h.zero);
-      t = fminf(fmaxf(t, 0.0f), qmax);
-      tmp[c] = __fadd_rn(t, kMagic);
-    }
-#pragma unroll
-    for (int c = 0; c < N; ++c) xg[c] = tmp[c];
-  }
-  return h.rec;
-}
-
-// One packed word from the 32/BITS consecutive channels xw[0..) (each value
-// 1.5 * 2^23 + code): channel 2k + h of the word at bits BITS*k + 16h.  The
-// low 16 bits of 1.5 * 2^23 are zero, so a Horner sum of the bit patterns
-// (times 2^BITS per code) leaves the codes in the low half-word, given the
-// group's folded zero point (all channels of a word share one group).
-template <int BITS>
-__device__ __forceinline__ uint32_t pack_word(const float* xw, int zfold) {
-  constexpr int PER_WORD = 32 / BITS;
-  // zfold times (1 + 2^BITS + 2^(2 BITS) + ...) over a half-word's codes
-  constexpr uint32_t kOnes = BITS == 2 ? 0x5555u : 0x1111u;
-  uint32_t half[2];
-#pragma unroll
-  for (int hh = 0; hh < 2; ++hh) {
-    uint32_t acc = __float_as_uint(xw[hh + 2 * (PER_WORD / 2 - 1)]);
-#pragma unroll
-    for (int k = PER_WORD / 2 - 2; k >= 0; --k) acc = acc * (1u << BITS) + __float_as_uint(xw[hh + 2 * k]);
-    half[hh] = acc + (uint32_t)zfold * kOnes;
-  }
-  return __byte_perm(half[0], half[1], 0x5410);
-}
-
-// min and max of n values (two new values per 3-input min / max)
-template <int N>
-__device__ __forceinline__ void min_max(const float* v, float& mn, float& mx) {
-  mn = v[0];
-  mx = v[0];
-#pragma unroll
-  for (int c = 1; c < N; c += 2) {
-    const float u = v[c], w = c + 1 < N ? v[c + 1] : u;
-    mn = fminf(mn, fminf(u, w));
-    mx = fmaxf(mx, fmaxf(u, w));
-  }
-}
-
-// One row (one token's K or V row of one head), read from its warp's staged
-// tile: d/8 16-byte chunks, chunk i of the tile's row `row` stored at
-// 16 (i ^ (row mod d/8)) so that neither the copies nor the reads of a
-// quarter-warp meet in a shared-memory bank.  fp32 butterflies in the order
-// h = 1, 2, ..., d/2 (packed fp32 pairs from h = 2 on: each lane is the same
-// correctly rounded add or subtract), per-group min/max, Eq. (1) codes,
-// packed 16-byte stores.
-template <int D, int BITS, int GROUP>
-__device__ __forceinline__ void quantize_row(const QuantArgs& a, const PairSigns& sg,
-                                             const uint8_t* tile, int row, unsigned r,
-                                             unsigned per_kv) {
-  constexpr int G = D / GROUP;
-  constexpr int CODE_BYTES = D * BITS / 8;
-  constexpr int PER_WORD = 32 / BITS;
-  constexpr int CH = D / 8;
-
-  const bool is_v = r >= per_kv;
-  const unsigned rk = is_v ? r - per_kv : r;
-  const unsigned bh = a.div_mul ? (__umulhi(rk, a.div_mul) >> a.div_shift) : (rk >> a.div_shift);
-  const unsigned tok = rk - bh * (unsigned)a.n_new;
-
-  const uint8_t* rowp = tile + row * (2 * D);
-  float x[D];
-#pragma unroll
-  for (int i = 0; i < D / 8; ++i) {
-    const uint4 raw = *reinterpret_cast<const uint4*>(rowp + ((i ^ (row & (CH - 1))) << 4));
-    const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      x[8 * i + 2 * k] = __uint_as_float(w[k] << 16);               // sign applied below
-      x[8 * i + 2 * k + 1] = __uint_as_float((w[k] ^ sg.m[4 * i + k]) & 0xFFFF0000u);
-    }
-  }
-  // butterflies: h = 1 on scalars (with the low channel's sign), then
-  // packed pairs (x_i, x_i+1)
-#pragma unroll
-  for (int i = 0; i < D; i += 2) {
-    const float u = x[i], v = x[i + 1];
-    x[i] = __fmaf_rn(sg.sl[i / 2], u, v);
-    x[i + 1] = __fmaf_rn(sg.sl[i / 2], u, -v);
-  }
-#pragma unroll
-  for (int h = 2; h < D; h <<= 1) {
-#pragma unroll
-    for (int i = 0; i < D; i += 2) {
-      if ((i & h) == 0) {
-        const uint64_t A = ptx::f2_pack(x[i], x[i + 1]);
-        const uint64_t B = ptx::f2_pack(x[i + h], x[i + h + 1]);
-        ptx::f2_unpack(ptx::f2_add(A, B), x[i], x[i + 1]);
-        ptx::f2_unpack(ptx::f2_sub(A, B), x[i + h], x[i + h + 1]);
-      }
-    }
-  }
-  {
-    const uint64_t s2 = ptx::f2_pack(a.inv_sqrt_d, a.inv_sqrt_d);
-#pragma unroll
-    for (int i = 0; i < D; i += 2) ptx::f2_unpack(ptx::f2_mul(ptx::f2_pack(x[i], x[i + 1]), s2), x[i], x[i + 1]);
-  }
-
-  uint32_t rec[G];
-  int zf[G];
-#pragma unroll
-  for (int g = 0; g < G; ++g) {
-    float mn, mx;
-    min_max<GROUP>(x + GROUP * g, mn, mx);
-    rec[g] = group_codes<BITS, GROUP>(x + GROUP * g, mn, mx, zf[g]);
-  }
-
-  // pack: channel ch = 16w + 2k + h (INT2) / 8w + 2k + h (INT4) -> bits
-  // BITS*k + 16h
-  uint32_t words[D * BITS / 32];
-#pragma unroll
-  for (int w = 0; w < D * BITS / 32; ++w) words[w] = pack_word<BITS>(x + PER_WORD * w, zf[(PER_WORD * w) / GROUP]);
-
-  if (!KVQ_IN_BOUNDS(a.first + tok, a.cap, a.status, a.bounds_site) ||
-      !KVQ_IN_BOUNDS(bh, a.bh, a.status, a.bounds_site))
-    return;
-  const size_t dst_tok = (size_t)bh * a.cap + a.first + tok;
-  uint4* dc = reinterpret_cast<uint4*>((is_v ? a.v_codes : a.k_codes) + dst_tok * CODE_BYTES);
-#pragma unroll
-  for (int i = 0; i < CODE_BYTES / 16; ++i)
-    dc[i] = make_uint4(words[4 * i], words[4 * i + 1], words[4 * i + 2], words[4 * i + 3]);
-  uint32_t* ds = (is_v ? a.v_sz : a.k_sz) + dst_tok * G;
-  if (G == 4) {
-    *reinterpret_cast<uint4*>(ds) = make_uint4(rec[0], rec[1 % G], rec[2 % G], rec[3 % G]);
-  } else if (G == 2) {
-    *reinterpret_cast<uint2*>(ds) = make_uint2(rec[0], rec[1 % G]);
-  } else {
-    ds[0] = rec[0];
-  }
-}
-
-// Each warp walks tiles of 32 consecutive rows (the K rows of all (batch,
-// head) pairs, then the V rows) with stride = all warps of the grid; the
-// next tile is copied into the warp's other shared-memory stage (each copy
-// instruction moves 32/(d/8) whole rows, 512 contiguous bytes) while the
-// current one is quantized.
-template <int D, int BITS, int GROUP>
-__global__ void __launch_bounds__(kQWarps * 32, kQBlocksPerSm)
-    quantize_rows_kernel(const QuantArgs a, const PairSigns sg) {
-  constexpr int RB = 2 * D;          // bytes of one BF16 row
-  constexpr int CH = D / 8;          // 16-byte chunks per row
-  constexpr int RPI = 32 / CH;       // rows per copy instruction
-  constexpr int TILE = 32 * RB;      // one warp's 32 rows
-  extern __shared__ __align__(16) uint8_t qsm[];
-  const int lane = threadIdx.x & 31;
-  const int wib = threadIdx.x >> 5;
-  uint8_t* stage = qsm + wib * 2 * TILE;
-  const unsigned per_kv = (unsigned)a.bh * (unsigned)a.n_new;   // < 2^30 (host check)
-  const unsigned total = 2u * per_kv;
-  const unsigned row_begin = a.v_only ? per_kv : 0u;              // V rows only
-  const unsigned n_tiles = (total - row_begin + 31u) / 32u;
-  const unsigned n_warps = gridDim.x * kQWarps;
-  auto issue = [&](unsigned tile, uint8_t* dst) {
-#pragma unroll
-    for (int j = 0; j < CH; ++j) {
-      const int row = j * RPI + lane / CH, chunk = lane % CH;
-      const unsigned r = row_begin + tile * 32u + (unsigned)row;
-      if (r < total) {
-        const bool is_v = r >= per_kv;
-        const uint16_t* src = (is_v ? a.v_new : a.k_new) + (size_t)(is_v ? r - per_kv : r) * D + chunk * 8;
-        cp_async16(dst + row * RB + ((chunk ^ (row & (CH - 1))) << 4), src);
-      }
-    }
-    cp_async_commit();
-  };
-  unsigned tile = blockIdx.x * kQWarps + wib;
-  if (tile < n_tiles) issue(tile, stage);
-  for (int k = 0; tile < n_tiles; ++k, tile += n_warps) {
-    const unsigned next = tile + n_warps;
-    if (next < n_tiles) {
-      issue(next, stage + ((k + 1) & 1) * TILE);
-      cp_async_wait<1>();
-    } else {
-      cp_async_wait<0>();
-    }
-    __syncwarp();
-    const unsigned r = row_begin + tile * 32u + (unsigned)lane;
-    if (r < total) quantize_row<D, BITS, GROUP>(a, sg, stage + (k & 1) * TILE, lane, r, per_kv);
-    // every lane is done with this stage before the copy two tiles on
-    __syncwarp();
-  }
-}
-
-// ---- d = 128: each row split between the two warps of a pair ----------------
-//
-// Warp HF of a pair holds channels [64 HF, 64 HF + 64) of the pair's 32 rows
-// (one row per lane), so a thread keeps 64 values instead of 128: half the
-// registers and half the code per warp.  The butterflies h = 1 .. 32 stay
-// inside a half; h = 64 pairs channel c with c + 64 across the two warps and
-// goes through shared memory: HF = 0 keeps channels [0, 32) and sends
-// [32, 64), HF = 1 keeps [96, 128) and sends [64, 96), so that afterwards
-// HF = 0 owns channels [0, 32) and [64, 96), HF = 1 owns [32, 64) and
-// [96, 128).  Groups of 32 channels then lie in one warp; groups of 64 swap
-// their partial min / max once more.
-//
-// Both warps run one code path (one copy of the unrolled code in the
-// instruction cache): warp 1 takes channels 96..127 with their signs flipped
-// (an exact negation that every butterfly carries along), so its h = 32
-// step leaves channels 96..127 in the first half of its registers, as warp 0
-// has channels 0..31 there; both then keep their first half and send their
-// second.  Warp 1's differences of the h = 64 step come out negated and take
-// the scale -fl(1/sqrt(d)) (again exact).  Every value is the same fp32
-// result as in the textbook order.
-constexpr int kSplitWarps = 4;                  // two warp pairs per block
-constexpr int kSplitBlocksPerSm = 4;
-constexpr int kSplitStages = 3;
-constexpr int kHalfRowBytes = 128;              // 64 BF16 channels
-constexpr int kSplitTile = 32 * kHalfRowBytes;  // one warp's 32 half-rows
-constexpr int kSplitSmem = kSplitWarps * (kSplitStages * kSplitTile + 32 * 4 * 4) + 64 * 4;
-
-// named barrier of one warp pair (ids 1 and 2; 0 is __syncthreads)
-__device__ __forceinline__ void pair_sync(int id) {
-  asm volatile("bar.sync %0, 64;" ::"r"(id) : "memory");
-}
-
-// 16-byte chunk i (0..7) of lane l's 128-byte slot, XOR-swizzled so that a
-// quarter-warp's eight lanes use eight different bank groups
-__device__ __forceinline__ int half_slot(int l, int i) { return l * kHalfRowBytes + ((i ^ (l & 7)) << 4); }
-
-template <int BITS, int GROUP>
-__device__ __forceinline__ void quantize_half_row(const QuantArgs& a, const uint32_t* msk,
-                                                  uint8_t* own, const uint8_t* partner,
-                                                  float* mm, const float* pmm, int lane, int HF,
-                                                  unsigned rk, bool valid, bool is_v, int bar) {
-  constexpr int H = 64, Q = 32;
-  constexpr int G = 128 / GROUP;
-  float x[H];
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const uint4 raw = *reinterpret_cast<const uint4*>(own + half_slot(lane, i));
-    const uint4 mv = *reinterpret_cast<const uint4*>(msk + 4 * i);
-    const uint32_t w[4] = {raw.x ^ mv.x, raw.y ^ mv.y, raw.z ^ mv.z, raw.w ^ mv.w};
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const int pl = 4 * i + k;
-      const float lo = __uint_as_float(w[k] << 16), hi = __uint_as_float(w[k] & 0xFFFF0000u);
-      x[2 * pl] = __fadd_rn(lo, hi);          // h = 1
-      x[2 * pl + 1] = __fsub_rn(lo, hi);
-    }
-  }
-#pragma unroll
-  for (int h = 2; h < H; h <<= 1) {
-#pragma unroll
-    for (int i = 0; i < H; i += 2) {
-      if ((i & h) == 0) {
-        const uint64_t A = ptx::f2_pack(x[i], x[i + 1]);
-        const uint64_t B = ptx::f2_pack(x[i + h], x[i + h + 1]);
-        ptx::f2_unpack(ptx::f2_add(A, B), x[i], x[i + 1]);
-        ptx::f2_unpack(ptx::f2_sub(A, B), x[i + h], x[i + h + 1]);
-      }
-    }
-  }
-  // h = 64 across the pair.  Warp 1 took its channels 96..127 negated, so
-  // its h = 32 butterflies left channels 96..127 (true values) in x[0..32)
-  // and 64..95 in x[32..64): both warps keep x[0..32) (channels 32 HF ..
-  // 32 HF + 31 before this step) and send x[32..64)
-  __syncwarp();
-#pragma unroll
-  for (int i = 0; i < 8; ++i)
-    *reinterpret_cast<uint4*>(own + half_slot(lane, i)) =
-        make_uint4(__float_as_uint(x[Q + 4 * i]), __float_as_uint(x[Q + 4 * i + 1]),
-                   __float_as_uint(x[Q + 4 * i + 2]), __float_as_uint(x[Q + 4 * i + 3]));
-  pair_sync(bar);
-  // kept + received -> channel 32 HF + j; kept - received -> channel 64 +
-  // 32 HF + j, negated in warp 1 (its kept values are the high channels):
-  // the negation rides on the scale (exact)
-  const uint64_t s2 = ptx::f2_pack(a.inv_sqrt_d, a.inv_sqrt_d);
-  const float sd = HF ? -a.inv_sqrt_d : a.inv_sqrt_d;
-  const uint64_t sd2 = ptx::f2_pack(sd, sd);
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const uint4 v = *reinterpret_cast<const uint4*>(partner + half_slot(lane, i));
-    const float rv[4] = {__uint_as_float(v.x), __uint_as_float(v.y), __uint_as_float(v.z),
-                         __uint_as_float(v.w)};
-#pragma unroll
-    for (int e = 0; e < 4; e += 2) {
-      const int j = 4 * i + e;
-      const uint64_t kept = ptx::f2_pack(x[j], x[j + 1]);
-      const uint64_t recv = ptx::f2_pack(rv[e], rv[e + 1]);
-      ptx::f2_unpack(ptx::f2_mul(ptx::f2_add(kept, recv), s2), x[j], x[j + 1]);
-      ptx::f2_unpack(ptx::f2_mul(ptx::f2_sub(kept, recv), sd2), x[Q + j], x[Q + j + 1]);
-    }
-  }
-  uint32_t rec[2];
-  int zf[2];
-  if (GROUP == 32) {
-    // x[0..32) is group HF, x[32..64) group 2 + HF
-#pragma unroll
-    for (int part = 0; part < 2; ++part) {
-      float mn, mx;
-      min_max<Q>(x + Q * part, mn, mx);
-      rec[part] = group_codes<BITS, Q>(x + Q * part, mn, mx, zf[part]);
-    }
-  } else {
-    // x[0..32) is half of group 0, x[32..64) half of group 1
-    float mn[2], mx[2];
-#pragma unroll
-    for (int part = 0; part < 2; ++part) min_max<Q>(x + Q * part, mn[part], mx[part]);
-    *reinterpret_cast<float4*>(mm + 4 * lane) = make_float4(mn[0], mx[0], mn[1], mx[1]);
-    pair_sync(bar);
-    const float4 o = *reinterpret_cast<const float4*>(pmm + 4 * lane);
-    mn[0] = fminf(mn[0], o.x);
-    mx[0] = fmaxf(mx[0], o.y);
-    mn[1] = fminf(mn[1], o.z);
-    mx[1] = fmaxf(mx[1], o.w);
-#pragma unroll
-    for (int part = 0; part < 2; ++part)
-      rec[part] = group_codes<BITS, Q>(x + Q * part, mn[part], mx[part], zf[part]);
-  }
-  if (!valid) return;
-  const unsigned bh = a.div_mul ? (__umulhi(rk, a.div_mul) >> a.div_shift) : (rk >> a.div_shift);
-  const unsigned tok = rk - bh * (unsigned)a.n_new;
-  if (!KVQ_IN_BOUNDS(a.first + tok, a.cap, a.status, a.bounds_site) ||
-      !KVQ_IN_BOUNDS(bh, a.bh, a.status, a.bounds_site))
-    return;
-  const size_t dst_tok = (size_t)bh * a.cap + a.first + tok;
-  // codes: channels [32 HF, 32 HF + 32) and [64 + 32 HF, ...) -> bytes
-  // [4 HF BITS, ...) and [8 BITS + 4 HF BITS, ...)
-  constexpr int PER_WORD = 32 / BITS;
-  constexpr int WPP = Q / PER_WORD;   // words per 32-channel part
-  uint8_t* dc = (is_v ? a.v_codes : a.k_codes) + dst_tok * (128 * BITS / 8);
-#pragma unroll
-  for (int part = 0; part < 2; ++part) {
-    uint32_t wd[WPP];
-#pragma unroll
-    for (int w = 0; w < WPP; ++w) wd[w] = pack_word<BITS>(x + Q * part + PER_WORD * w, zf[part]);
-    uint8_t* d = dc + (part * 64 + HF * 32) * BITS / 8;
-    if (WPP == 2) {
-      *reinterpret_cast<uint2*>(d) = make_uint2(wd[0], wd[1 % WPP]);
-    } else {
-      *reinterpret_cast<uint4*>(d) = make_uint4(wd[0], wd[1 % WPP], wd[2 % WPP], wd[3 % WPP]);
-    }
-  }
-  uint32_t* ds = (is_v ? a.v_sz : a.k_sz) + dst_tok * G;
-  if (GROUP == 32) {
-    ds[HF] = rec[0];
-    ds[2 + HF] = rec[1];
-  } else if (HF == 0) {
-    *reinterpret_cast<uint2*>(ds) = make_uint2(rec[0], rec[1]);
-  }
-}
-
-// Warp pairs walk tiles of 32 consecutive rows of one tensor (the K rows of
-// all (batch, head) pairs in tiles [0, T), then the V rows in tiles [T, 2T))
-// with stride = all pairs of the grid; each warp copies its half of the next
-// tile (128-byte runs) into the next of its three shared-memory stages while
-// it works on the current one.  Three stages because a stage slot also
-// carries the h = 64 exchange: the copy into it waits until the partner has
-// passed the following exchange.
-template <int BITS, int GROUP>
-__global__ void __launch_bounds__(kSplitWarps * 32, kSplitBlocksPerSm)
-    quantize_split_kernel(const QuantArgs a, const PairSigns sg) {
-  extern __shared__ __align__(16) uint8_t qsm[];
-  const int lane = threadIdx.x & 31;
-  const int wib = threadIdx.x >> 5;
-  const int hf = wib & 1;
-  uint8_t* stages = qsm + wib * kSplitStages * kSplitTile;
-  const uint8_t* pstages = qsm + (wib ^ 1) * kSplitStages * kSplitTile;
-  float* mm_base = reinterpret_cast<float*>(qsm + kSplitWarps * kSplitStages * kSplitTile);
-  float* mm = mm_base + wib * 128;
-  const float* pmm = mm_base + (wib ^ 1) * 128;
-  // sign masks of the two halves (bit 15: channel 2p, bit 31: channel 2p + 1
-  // of pair p); the second half takes channels 96..127 negated as well
-  uint32_t* msk_base = reinterpret_cast<uint32_t*>(mm_base + kSplitWarps * 128);
-  if (threadIdx.x < 64) {
-    const int p = threadIdx.x;   // pair of the row
-    uint32_t m = sg.m[0];
-#pragma unroll
-    for (int q = 1; q < 64; ++q) m = q == p ? sg.m[q] : m;
-    if (p >= 48) m ^= 0x80008000u;
-    msk_base[p] = m;
-  }
-  __syncthreads();
-  const uint32_t* msk = msk_base + 32 * hf;
-  const unsigned per_kv = (unsigned)a.bh * (unsigned)a.n_new;   // < 2^30 (host check)
-  const unsigned tiles_per = (per_kv + 31u) / 32u;
-  const unsigned n_tiles = 2u * tiles_per;
-  const unsigned n_pairs = gridDim.x * (kSplitWarps / 2);
-  // this lane's share of a copy: rows 4j + lane / 8, chunk lane % 8
-  const int crow = lane >> 3, cchunk = lane & 7;
-  const int src_lane = crow * 128 + hf * 64 + cchunk * 8;   // BF16 elements
-  const int dst_even = half_slot(crow, cchunk), dst_odd = half_slot(crow + 4, cchunk);
-  auto issue = [&](unsigned tile, uint8_t* dst) {
-    const bool v = tile >= tiles_per;
-    const unsigned row0 = (v ? tile - tiles_per : tile) * 32u;
-    const uint16_t* src = (v ? a.v_new : a.k_new) + (size_t)row0 * 128 + src_lane;
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      if (row0 + 4u * j + (unsigned)crow < per_kv)
-        cp_async16(dst + 512 * (j & ~1) + ((j & 1) ? dst_odd : dst_even), src + 512 * j);
-    }
-    cp_async_commit();
-  };
-  unsigned tile = (a.v_only ? tiles_per : 0u) + blockIdx.x * (kSplitWarps / 2) + (wib >> 1);
-  if (tile < n_tiles) issue(tile, stages);
-  int s = 0;
-  for (int k = 0; tile < n_tiles; ++k, tile += n_pairs) {
-    const unsigned next = tile + n_pairs;
-    const int sn = s == kSplitStages - 1 ? 0 : s + 1;
-    if (next < n_tiles) {
-      issue(next, stages + sn * kSplitTile);
-      cp_async_wait<1>();
-    } else {
-      cp_async_wait<0>();
-    }
-    __syncwarp();
-    const bool is_v = tile >= tiles_per;
-    const unsigned rk = (is_v ? tile - tiles_per : tile) * 32u + (unsigned)lane;
-    const bool valid = rk < per_kv;
-    uint8_t* own = stages + s * kSplitTile;
-    const uint8_t* par = pstages + s * kSplitTile;
-    const int bar = 1 + (wib >> 1);
-    quantize_half_row<BITS, GROUP>(a, msk, own, par, mm, pmm, lane, hf, rk, valid, is_v, bar);
-    __syncwarp();
-    s = sn;
-  }
 }
 
 // ---- per-channel keys: Eq. (1) per channel over a block of tokens -----------
@@ -1025,63 +462,7 @@ long long grid_for_rows(long long rows, int rows_per_block, int blocks_per_sm) {
   return blocks;
 }
 
-template <int D, int BITS, int GROUP>
-cudaError_t launch_q(const QuantArgs& a, cudaStream_t s) {
-  PairSigns sg;
-  for (int i = 0; i < 64; ++i) {
-    const int c0 = 2 * i, c1 = 2 * i + 1;
-    const uint32_t s0 = c0 < D ? (a.sign_bits[c0 >> 5] >> (c0 & 31)) & 1u : 0u;
-    const uint32_t s1 = c1 < D ? (a.sign_bits[c1 >> 5] >> (c1 & 31)) & 1u : 0u;
-    sg.m[i] = (s0 << 15) | (s1 << 31);
-    sg.sl[i] = s0 ? -1.0f : 1.0f;
-  }
-  const long long rows = (a.v_only ? 1LL : 2LL) * a.bh * a.n_new;
-  if (rows == 0) return cudaSuccess;
-  const long long tiles = (rows + 31) / 32;
-  if constexpr (D == 128) {
-    const long long per = ((long long)a.bh * a.n_new + 31) / 32;   // tiles of one tensor
-    const long long want = ((a.v_only ? per : 2 * per) + 1) / 2;
-    const long long cap = (long long)sm_count() * kSplitBlocksPerSm;
-    const unsigned blocks = (unsigned)(want < cap ? want : cap);
-    static std::atomic<uint64_t> limit_set{0};   // per template instance and device
-    const cudaError_t e = ensure_smem_limit(quantize_split_kernel<BITS, GROUP>, kSplitSmem, limit_set);
-    if (e != cudaSuccess) return e;
-    quantize_split_kernel<BITS, GROUP><<<blocks, kSplitWarps * 32, kSplitSmem, s>>>(a, sg);
-    note_launch();
-    return cudaGetLastError();
-  } else {
-    const long long want = (tiles + kQWarps - 1) / kQWarps;
-    const long long cap = (long long)sm_count() * kQBlocksPerSm;
-    const unsigned blocks = (unsigned)(want < cap ? want : cap);
-    const int smem = kQWarps * 2 * 32 * 2 * D;
-    static std::atomic<uint64_t> limit_set{0};   // per template instance and device
-    const cudaError_t e = ensure_smem_limit(quantize_rows_kernel<D, BITS, GROUP>, smem, limit_set);
-    if (e != cudaSuccess) return e;
-    quantize_rows_kernel<D, BITS, GROUP><<<blocks, kQWarps * 32, smem, s>>>(a, sg);
-    note_launch();
-    return cudaGetLastError();
-  }
-}
-
 }  // namespace
-
-cudaError_t launch_quantize_append(const QuantArgs& a, int d, int bits, int group,
-                                   cudaStream_t stream, bool* supported) {
-  *supported = true;
-#define KVQ_Q(D_, B_, G_) \
-  if (d == D_ && bits == B_ && group == G_) return launch_q<D_, B_, G_>(a, stream);
-  KVQ_Q(64, 2, 32)
-  KVQ_Q(64, 2, 64)
-  KVQ_Q(64, 4, 32)
-  KVQ_Q(64, 4, 64)
-  KVQ_Q(128, 2, 32)
-  KVQ_Q(128, 2, 64)
-  KVQ_Q(128, 4, 32)
-  KVQ_Q(128, 4, 64)
-#undef KVQ_Q
-  *supported = false;
-  return cudaSuccess;
-}
 
 namespace {
 

@@ -59,6 +59,12 @@ __device__ __forceinline__ uint64_t globaltimer() {
   return t;
 }
 
+// Wait until the grids this one depends on (programmatic dependent launch)
+// have completed and their memory is visible; a no-op otherwise.
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // ---- async proxy ----------------------------------------------------------
 // Orders this thread's generic-proxy shared-memory writes before later
 // async-proxy accesses (tensor-core operand reads, TMA).
@@ -67,12 +73,26 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
 }
 
 // ---- TMA ------------------------------------------------------------------
+// Fetch a tensor map (a __grid_constant__ kernel parameter) ahead of its
+// first use by a TMA copy.
+__device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int c0, int c1,
                                             int c2, uint32_t bar) {
   asm volatile(
       "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
       " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int c0, int c1,
+                                            uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar)
       : "memory");
 }
 

@@ -40,6 +40,26 @@ def oracle_head(w: synth.Workload, x: dict, signs, b: int, h: int, rows, corr: i
                              signs, w.scale, w.group, corr)
 
 
+def admissible(x, signs, bits: int, group: int, packed, sz_bits):
+    """Check packed codes and (step, zero) BF16 bits [..., G, 2] that the
+    GPU wrote for BF16 rows x [..., d] against every answer the oracle
+    allows: the rotation known to within its fp32 summation bound
+    (O.rotation_bounds; exact for rows whose partial sums are all fp32
+    numbers) and Eq. (1) over that interval (O.quantize_groups_admissible).
+    Returns (per-group bool: the GPU's step, zero point and codes form one
+    admissible answer; the fraction of codes the bounds determine)."""
+    xf = x.float().numpy() if hasattr(x, "float") else np.asarray(x, np.float32)
+    lo, hi = O.rotation_bounds(xf, signs)
+    cd, cz, clo, chi = O.quantize_groups_admissible(lo, hi, bits, group)
+    d = xf.shape[-1]
+    lead = xf.shape[:-1]
+    codes = O.unpack_codes(packed, bits, d).reshape(*lead, d // group, group)
+    sz = np.asarray(sz_bits).view(np.uint16)
+    ok = ((O.bf16_bits(cd) == sz[..., 0][..., None]) & (O.bf16_bits(cz) == sz[..., 1][..., None]) &
+          np.all((clo <= codes[..., None, :]) & (codes[..., None, :] <= chi), axis=-1))
+    return ok.any(axis=-1), float(np.mean(clo == chi))
+
+
 def assert_close(o_gpu, o_ref, ps_gpu=None, ps_ref=None, pr_gpu=None, pr_ref=None, what=""):
     o_gpu = np.asarray(o_gpu, dtype=np.float64)
     err = np.abs(o_gpu - o_ref).max()

@@ -78,6 +78,99 @@ def check_fwht_fp32_matches_fp64():
         assert np.array_equal(O.rotate_fp32(e, s), want.astype(np.float32))
 
 
+def _bf16_rows(rng, n, d):
+    x = rng.standard_normal((n, d)) * rng.uniform(0.01, 50, (n, 1))
+    x[:, :3] *= 12                                   # outlier channels
+    return O.bf16_round(x.astype(np.float32))
+
+
+def check_rotation_bounds():
+    """rotation_bounds holds every fp32 summation order: the butterfly
+    order, sequential sums in random orders and the exact sum (times the
+    fp32 constant) all lie inside; rows on a coarse grid have exact sums, so
+    their bounds collapse onto the butterfly result; the bounds are no wider
+    than the recursive-summation bound allows."""
+    rng = np.random.default_rng(21)
+    for d in (64, 128):
+        s = np.where(rng.integers(0, 2, d) == 1, -1.0, 1.0).astype(np.float32)
+        x = _bf16_rows(rng, 300, d)
+        lo, hi = O.rotation_bounds(x, s)
+        assert lo.dtype == np.float32 and np.all(lo <= hi)
+        y32 = O.rotate_fp32(x, s)
+        assert np.all((lo <= y32) & (y32 <= hi))
+        inv = np.float64(np.float32(1.0 / math.sqrt(d)))
+        w = O.sylvester_hadamard(d) * s.astype(np.float64)[None, :]
+        center = (x.astype(np.float64) @ w.T) * inv
+        # the exact sum rounded to fp32 once, times the constant: one order
+        c32 = ((x.astype(np.float64) @ w.T).astype(np.float32).astype(np.float64) * inv).astype(np.float32)
+        assert np.all((lo <= c32) & (c32 <= hi))
+        for r in range(0, 300, 15):
+            for n in rng.integers(0, d, 4):
+                terms = (x[r].astype(np.float64) * w[n]).astype(np.float32)   # exact products
+                acc = np.float32(0.0)
+                for k in rng.permutation(d):
+                    acc = np.float32(acc + terms[k])
+                y = np.float32(np.float64(acc) * inv)
+                assert lo[r, n] <= y <= hi[r, n], (d, r, n)
+        gamma = (d - 1) * 2.0 ** -23 / (1 - (d - 1) * 2.0 ** -23)
+        width = (hi.astype(np.float64) - lo) / inv
+        allowed = 2 * (gamma + d * 2.0 ** -53) * np.abs(x.astype(np.float64)).sum(1, keepdims=True)
+        assert np.all(width <= allowed + 4 * np.spacing(np.abs(center).astype(np.float32)) / inv)
+        # values m * 2^e, |m| <= 255: every partial sum is an fp32 number
+        m = np.clip(np.rint(rng.standard_normal((200, d)) * 40), -255, 255)
+        xg = (m * 2.0 ** rng.integers(-12, 12, (200, 1))).astype(np.float32)
+        lo, hi = O.rotation_bounds(xg, s)
+        assert np.array_equal(lo, hi) and np.array_equal(lo, O.rotate_fp32(xg, s))
+
+
+def check_quantize_admissible():
+    """quantize_groups_admissible: with exact inputs its four candidates are
+    quantize_groups' one answer; with interval inputs every fp32 row inside
+    the bounds (sampled: each element at its low end, its high end or a value
+    between) has its quantize_groups answer among the candidates; and the
+    candidate set stays tight (almost every code determined)."""
+    rng = np.random.default_rng(22)
+    for bits, group in ((2, 32), (4, 64), (2, 64), (4, 32)):
+        y = (rng.standard_normal((400, 128)) * rng.uniform(0.1, 5, (400, 1))).astype(np.float32)
+        codes, delta, zero = O.quantize_groups(y, bits, group)
+        cd, cz, clo, chi = O.quantize_groups_admissible(y, y, bits, group)
+        g_n = 128 // group
+        cg = codes.reshape(400, g_n, group)
+        for i in range(4):
+            assert np.array_equal(cd[..., i], delta) and np.array_equal(cz[..., i], zero)
+            assert np.array_equal(clo[..., i, :], cg) and np.array_equal(chi[..., i, :], cg)
+        # bounds a few units wide around y
+        ulps = rng.integers(0, 40, y.shape)
+        lo = y - (np.spacing(np.abs(y)) * ulps).astype(np.float32)
+        hi = y + (np.spacing(np.abs(y)) * rng.integers(0, 40, y.shape)).astype(np.float32)
+        cd, cz, clo, chi = O.quantize_groups_admissible(lo, hi, bits, group)
+        for _ in range(12):
+            pick = rng.integers(0, 3, y.shape)
+            mid = (lo + (hi - lo) * rng.uniform(0, 1, y.shape).astype(np.float32)).astype(np.float32)
+            mid = np.clip(mid, lo, hi)
+            ys = np.where(pick == 0, lo, np.where(pick == 1, hi, mid)).astype(np.float32)
+            c, dl, z = O.quantize_groups(ys, bits, group)
+            cgs = c.reshape(400, g_n, group)
+            ok = ((cd == dl[..., None]) & (cz == z[..., None]) &
+                  np.all((clo <= cgs[..., None, :]) & (cgs[..., None, :] <= chi), axis=-1))
+            assert ok.any(axis=-1).all(), (bits, group)
+        assert np.mean(clo == chi) > 0.99
+    # a zero point on a tie: min -1.5, max 1.5, INT2 -> step 1 and
+    # -min / step = 1.5 (rint -> 2); one unit either side of the min moves
+    # the zero point to 1 or keeps it at 2, with the step unchanged
+    y = np.linspace(-1.5, 1.5, 32, dtype=np.float32)[None]
+    lo, hi = y.copy(), y.copy()
+    lo[0, 0] = np.nextafter(np.float32(-1.5), np.float32(-2))
+    hi[0, 0] = np.nextafter(np.float32(-1.5), np.float32(0))
+    cd, cz, clo, chi = O.quantize_groups_admissible(lo, hi, 2, 32)
+    for ys in (lo, hi, y):
+        c, dl, z = O.quantize_groups(ys, 2, 32)
+        ok = ((cd == dl[..., None]) & (cz == z[..., None]) &
+              np.all((clo <= c[:, None, None, :]) & (c[:, None, None, :] <= chi), axis=-1))
+        assert ok.any(), (ys[0, 0], z)
+    assert set(np.unique(cz)) == {1.0, 2.0}
+
+
 def check_bf16_round_matches_torch():
     rng = np.random.default_rng(3)
     x = np.concatenate([

@@ -196,7 +196,35 @@ def _ring_no_wrap(length, head_slot, n_new, chunk_tokens, n_chunks):
     return start, new_len, min(head_slot + 1, n_chunks - 1)
 
 
+def _rotation_bounds_no_error(x, signs):
+    x = np.asarray(x, dtype=np.float32)
+    d = x.shape[-1]
+    w = O.sylvester_hadamard(d) * np.asarray(signs, np.float64)[None, :]
+    inv = np.float64(np.float32(1.0 / np.sqrt(d)))
+    y = ((x.astype(np.float64) @ w.T).astype(np.float32).astype(np.float64) * inv).astype(np.float32)
+    return y, y
+
+
+_real_admissible = O.quantize_groups_admissible
+
+
+def _admissible_zero_one_end(y_lo, y_hi, bits, group):
+    cd, cz, clo, chi = _real_admissible(y_lo, y_hi, bits, group)
+    cz = cz.copy()
+    cz[..., 1] = cz[..., 0]
+    cz[..., 3] = cz[..., 2]
+    return cd, cz, clo, chi
+
+
+def _admissible_codes_any(y_lo, y_hi, bits, group):
+    cd, cz, clo, chi = _real_admissible(y_lo, y_hi, bits, group)
+    return cd, cz, np.zeros_like(clo), np.full_like(chi, 2 ** bits - 1)
+
+
 MUTANTS = {
+    "rotation_bounds_no_error": ("rotation_bounds", _rotation_bounds_no_error),
+    "admissible_zero_one_end": ("quantize_groups_admissible", _admissible_zero_one_end),
+    "admissible_codes_any": ("quantize_groups_admissible", _admissible_codes_any),
     "key_channels_per_token": ("quantize_key_channels", _key_channels_per_token),
     "key_blocks_whole_chunk": ("chunk_blocks", _chunk_blocks_whole_chunk),
     "bias_sign_flipped": ("jensen_bias_taylor", _bias_sign_flipped),
