@@ -333,15 +333,19 @@ int32_t kvq_debug_bounds_build(void);
 /*
  * Limit, in nanoseconds, of every bounded wait inside the kernels (default
  * 2e9).  Exceeding it makes the kernel record KVQ_ERR_TIMEOUT, release its
- * tensor memory and return.  Host setting, applies to later launches.
+ * tensor memory and return.  Host setting, applies to later launches.  (The
+ * quantizer waits for its own copies and MMAs in flight for at least 100 ms
+ * before it exits, whatever the limit.)
  */
 kvq_status kvq_set_wait_limit_ns(uint64_t limit_ns);
 
 /*
- * Self-test of the bounded-wait path: one block waits on a shared-memory
- * barrier that nothing ever arrives on, for at most limit_ns, then records
- * KVQ_ERR_TIMEOUT and returns.  No counterpart in the paper; it exists so the
- * error path can be exercised without faulting or hanging a GPU.
+ * Self-test of the bounded-wait path: two one-block kernels, one with the
+ * attention kernels' wait and one with the tensor-core quantizer's, each
+ * wait on a shared-memory barrier that nothing ever arrives on, for at most
+ * limit_ns, then record KVQ_ERR_TIMEOUT and return.  No counterpart in the
+ * paper; it exists so the error path can be exercised without faulting or
+ * hanging a GPU.
  */
 kvq_status kvq_selftest_wait_timeout(uint64_t limit_ns, void *stream);
 

@@ -234,6 +234,24 @@ def quantize_key_channels(y, bits: int, block: int = KEY_BLOCK):
     return codes, delta, zero
 
 
+def quantize_key_channels_admissible(y_lo, y_hi, bits: int, block: int = KEY_BLOCK):
+    """Every answer ``quantize_key_channels`` can give for fp32 keys y [n, d]
+    with y_lo <= y <= y_hi elementwise: per block of tokens,
+    ``quantize_groups_admissible`` over each channel's values in the block
+    (the group running along tokens, as in ``quantize_key_channels``).
+    Returns one tuple per block: delta, zero [d, 4] and code_lo, code_hi
+    [d, 4, block tokens] (the block's codes transposed: channel, candidate,
+    token)."""
+    lo = np.asarray(y_lo, dtype=np.float32)
+    hi = np.asarray(y_hi, dtype=np.float32)
+    out = []
+    for a, b in chunk_blocks(lo.shape[0], block):
+        cd, cz, clo, chi = quantize_groups_admissible(np.ascontiguousarray(lo[a:b].T),
+                                                      np.ascontiguousarray(hi[a:b].T), bits, b - a)
+        out.append((cd[:, 0], cz[:, 0], clo[:, 0], chi[:, 0]))
+    return out
+
+
 def key_channel_token_steps(values, n_tokens: int, block: int = KEY_BLOCK) -> np.ndarray:
     """Per-token view [n, d] of per-block, per-channel values [n_blocks, d]
     (each token gets the row of its block)."""
@@ -418,12 +436,19 @@ def quantize_groups_admissible(y_lo, y_hi, bits: int, group: int):
     mn_lo, mn_hi = lo_g.min(axis=-1), hi_g.min(axis=-1)
     mx_lo, mx_hi = lo_g.max(axis=-1), hi_g.max(axis=-1)
     qmax = np.float32(2 ** bits - 1)
-    d_small, c_small = _step_of(mn_hi, mx_lo, qmax)
-    d_large, c_large = _step_of(mn_lo, mx_hi, qmax)
-    if np.any(c_small != c_large) or np.any(c_small & (mn_lo != mn_hi)):
+    if group == 1:
+        # one value: its min and max are the same number, the span is 0
+        d_small, c_small = _step_of(mn_hi, mn_hi, qmax)
+        d_large, c_large = _step_of(mn_lo, mn_lo, qmax)
+    else:
+        d_small, c_small = _step_of(mn_hi, np.maximum(mx_lo, mn_hi), qmax)
+        d_large, c_large = _step_of(mn_lo, mx_hi, qmax)
+    if np.any(c_small != c_large) or np.any(c_small & (mn_lo < 0) & (mn_hi > 0)):
         raise ValueError("a group may or may not be constant within the bounds")
-    next_bf16 = from_bf16_bits((bf16_bits(d_small).astype(np.uint32) + 1).astype(np.uint16))
-    if np.any(d_large > next_bf16):
+    # (a constant group's step |min| may come out in either order)
+    d_lo, d_hi = np.minimum(d_small, d_large), np.maximum(d_small, d_large)
+    next_bf16 = from_bf16_bits((bf16_bits(d_lo).astype(np.uint32) + 1).astype(np.uint16))
+    if np.any(d_hi > next_bf16):
         raise ValueError("steps more than one BF16 value apart")
     deltas, zeros = [], []
     for dl in (d_small, d_large):

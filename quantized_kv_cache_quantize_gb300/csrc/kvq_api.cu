@@ -402,8 +402,8 @@ kvq_status kvq_quantize_append(kvq_cache* cache, const uint16_t* k_new, const ui
   }
   if (g.key_mode == KVQ_KEYS_PER_CHANNEL) {
     ProfScope prof(0, static_cast<cudaStream_t>(stream));
-    if (kvq::launch_quantize_key_channels(a, g.d, g.bits, static_cast<cudaStream_t>(stream),
-                                          &supported) != cudaSuccess)
+    if (kvq::launch_quantize_key_channels_mma(a, g.d, g.bits, static_cast<cudaStream_t>(stream),
+                                              &supported) != cudaSuccess)
       return KVQ_ERR_CUDA;
     if (!supported) return KVQ_ERR_UNSUPPORTED;
   }
@@ -505,9 +505,13 @@ kvq_status kvq_set_wait_limit_ns(uint64_t limit_ns) {
 
 kvq_status kvq_selftest_wait_timeout(uint64_t limit_ns, void* stream) {
   if (limit_ns == 0 || limit_ns > 10000000000ull) return KVQ_ERR_INVALID_ARG;
-  return kvq::launch_wait_selftest(limit_ns, static_cast<cudaStream_t>(stream)) == cudaSuccess
-             ? KVQ_OK
-             : KVQ_ERR_CUDA;
+  int* status = kvq::status_ptr();
+  if (status == nullptr) return KVQ_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // the attention kernels' wait and the tensor-core quantizer's, one after the other
+  if (kvq::launch_wait_selftest(limit_ns, s) != cudaSuccess) return KVQ_ERR_CUDA;
+  return kvq::launch_quant_wait_selftest(limit_ns, status, s) == cudaSuccess ? KVQ_OK
+                                                                             : KVQ_ERR_CUDA;
 }
 
 kvq_status kvq_profile_begin(void) {

@@ -124,14 +124,18 @@ inline void row_divisor(uint32_t d, uint32_t* mul, int* shift) {
 // per-channel key mode: the K rows of one append, per channel over blocks of
 // kKeyBlock tokens
 constexpr int kKeyBlock = 128;
-cudaError_t launch_quantize_key_channels(const QuantArgs& a, int d, int bits,
-                                         cudaStream_t stream, bool* supported);
 cudaError_t launch_rotate(const RotateArgs& a, int d, cudaStream_t stream);
 // The per-token quantize-append with the rotation on the tensor cores
 // (kvq_quant_mma.cu), and its rotation alone: fp32 x' of `rows` BF16 rows,
 // exactly the values that quantizer quantizes.
 cudaError_t launch_quantize_append_mma(const QuantArgs& a, int d, int bits, int group,
                                        cudaStream_t stream, bool* supported);
+// The per-channel key quantizer on the same tensor-core pipeline: one
+// 128-token block of one head per tile.
+cudaError_t launch_quantize_key_channels_mma(const QuantArgs& a, int d, int bits,
+                                             cudaStream_t stream, bool* supported);
+cudaError_t launch_quant_wait_selftest(unsigned long long limit_ns, int* status,
+                                      cudaStream_t stream);
 cudaError_t launch_rotate_mma_f32(const uint16_t* x, long long rows, int d,
                                   const uint32_t sign_bits[4], float* out, int* status,
                                   int* bounds_site, unsigned long long wait_limit_ns,

@@ -1,15 +1,11 @@
-// The rotation kernel and the per-channel key quantizer (sm_103a).
-//
-// Both rotate with the fast Walsh-Hadamard transform (paper section 3,
-// "Hadamard rotation"): fp32 butterflies in the order h = 1, 2, ..., d/2,
+// The rotation kernel (sm_103a): the attention's operands (the query as FP16
+// high and low parts, the current chunk's values as FP16) and its range
+// check.  It rotates with the fast Walsh-Hadamard transform (paper section
+// 3, "Hadamard rotation"): fp32 butterflies in the order h = 1, 2, ..., d/2,
 // then one multiply by fl(1/sqrt(d)), every step a correctly rounded fp32
-// operation, so the result is fixed bit for bit.
-// - rotate_kernel: the attention's operands (the query as FP16 high and low
-//   parts, the current chunk's values as FP16), and its range check.
-// - quantize_key_channels_kernel: the keys of an appended chunk in the
-//   per-channel key mode, Eq. (1) per channel over blocks of tokens.
-// The per-token quantize-append (keys and values, or values only in the
-// per-channel key mode) rotates on the tensor cores: kvq_quant_mma.cu.
+// operation, so the result is fixed bit for bit.  The quantize-append
+// (per token and group, and the per-channel keys) rotates on the tensor
+// cores: kvq_quant_mma.cu.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -30,232 +26,6 @@ namespace {
 __device__ __forceinline__ uint32_t sign_word_for(const uint32_t (&sb)[4], int t) {
   const int i = (8 * t) >> 5;
   return i == 0 ? sb[0] : i == 1 ? sb[1] : i == 2 ? sb[2] : sb[3];
-}
-
-// ---- per-channel keys: Eq. (1) per channel over a block of tokens -----------
-//
-// One CTA of kKcThreads per (block of up to kKeyBlock tokens of the appended
-// chunk, batch * head).
-// 1. Rotation: LPR = d / 32 lanes per token row, 32 channels per lane,
-//    butterflies h = 1 .. 16 in registers, the row written to shared memory,
-//    read back transposed (lane j: channels {32u + (32 / LPR) j + v}), h = 32
-//    (and 64) and the multiply by fl(1/sqrt(d)) in registers, written back in
-//    place: the same fp32 operations in the same order as the per-token
-//    kernels.  Rows are XOR-swizzled in 16-byte chunks (chunk c of lane jj's
-//    channels at c ^ (2 jj + (t & 1)) for d = 128, c ^ (4 jj + (t & 3)) for
-//    d = 64), which keeps a quarter-warp on eight bank groups.
-// 2. Channel columns: kKcThreads / d threads per channel, each over a slice
-//    of the tokens: min and max, combined through shared memory, the
-//    channel's step and zero point (Eq. (1), the per-token group arithmetic),
-//    then each value's code as a byte.
-// 3. Token rows: two threads per token pack its codes into the cache's word
-//    layout.
-constexpr int kKcThreads = 256;
-
-template <int D>
-__device__ __forceinline__ int kc_swz(int jj, int t) {
-  return D == 128 ? 2 * jj + (t & 1) : 4 * jj + (t & 3);
-}
-
-// float offset of channel c in a rotated row (token t)
-template <int D>
-__device__ __forceinline__ int kc_pos(int c, int t) {
-  return 32 * (c >> 5) + 4 * (((c >> 2) & 7) ^ kc_swz<D>(c >> 5, t)) + (c & 3);
-}
-
-template <int D, int BITS>
-__global__ void __launch_bounds__(kKcThreads) quantize_key_channels_kernel(const QuantArgs a) {
-  constexpr int LPR = D / 32;                  // lanes per token row
-  constexpr int VW = 32 / LPR;                 // channels per lane and run after the transpose
-  constexpr int RPP = kKcThreads / LPR;        // rows per pass
-  constexpr int P = kKcThreads / D;            // threads per channel column
-  constexpr int SLICE = kKeyBlock / P;         // tokens per column thread
-  constexpr int CB = D / 16;                   // 16-byte chunks of a code-byte row
-  extern __shared__ __align__(16) uint8_t ksm[];
-  float* rot = reinterpret_cast<float*>(ksm);                                   // [kKeyBlock][D]
-  uint8_t* cb = ksm + kKeyBlock * D * 4;                                        // [kKeyBlock][D]
-  float* mm = reinterpret_cast<float*>(cb + kKeyBlock * D);                     // [P][D][2]
-  const int tid = threadIdx.x;
-  const int blk = blockIdx.x;
-  const int bh = blockIdx.y;
-  const int t0 = blk * kKeyBlock;
-  const int n = min(kKeyBlock, a.n_new - t0);
-
-  // 1. rotation of the block's token rows
-  {
-    const int j = (tid & 31) % LPR;
-    const uint32_t sw = j == 0 ? a.sign_bits[0] : j == 1 ? a.sign_bits[1] : j == 2 ? a.sign_bits[2]
-                                                                                    : a.sign_bits[3];
-    uint32_t z = 0;   // bit k: channel 2k of the lane's 32; bit 16 + k: channel 2k + 1
-#pragma unroll
-    for (int k = 0; k < 16; ++k) z |= (((sw >> (2 * k)) & 1u) << k) | (((sw >> (2 * k + 1)) & 1u) << (16 + k));
-    // the lane's rows (kKeyBlock / RPP of them), all loaded before any is
-    // transformed
-    constexpr int NR = kKeyBlock / RPP;
-    uint4 rawr[NR][4];
-#pragma unroll
-    for (int rr = 0; rr < NR; ++rr) {
-      const int t = tid / LPR + rr * RPP;
-      const bool live = t < n;
-      const uint4* src = reinterpret_cast<const uint4*>(a.k_new + ((size_t)bh * a.n_new + t0 + (live ? t : 0)) * D + 32 * j);
-#pragma unroll
-      for (int k = 0; k < 4; ++k) rawr[rr][k] = live ? __ldg(src + k) : make_uint4(0u, 0u, 0u, 0u);
-    }
-#pragma unroll
-    for (int rr = 0; rr < NR; ++rr) {   // the same rows count in every lane
-      const int t = tid / LPR + rr * RPP;
-      float* row = rot + t * D;
-      const uint4 (&raw)[4] = rawr[rr];
-      float x[32];
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const uint32_t w[4] = {raw[k].x, raw[k].y, raw[k].z, raw[k].w};
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const uint32_t u = w[i] ^ ((z << (15 - (4 * k + i))) & 0x80008000u);
-          const float lo = __uint_as_float(u << 16), hi = __uint_as_float(u & 0xFFFF0000u);
-          x[8 * k + 2 * i] = __fadd_rn(lo, hi);       // h = 1
-          x[8 * k + 2 * i + 1] = __fsub_rn(lo, hi);
-        }
-      }
-#pragma unroll
-      for (int h = 2; h < 32; h <<= 1) {
-#pragma unroll
-        for (int i = 0; i < 32; i += 2) {
-          if ((i & h) == 0) {
-            const uint64_t A = ptx::f2_pack(x[i], x[i + 1]);
-            const uint64_t B = ptx::f2_pack(x[i + h], x[i + h + 1]);
-            ptx::f2_unpack(ptx::f2_add(A, B), x[i], x[i + 1]);
-            ptx::f2_unpack(ptx::f2_sub(A, B), x[i + h], x[i + h + 1]);
-          }
-        }
-      }
-      const int sj = kc_swz<D>(j, t);
-#pragma unroll
-      for (int c = 0; c < 8; ++c)
-        *reinterpret_cast<float4*>(row + 32 * j + 4 * (c ^ sj)) =
-            make_float4(x[4 * c], x[4 * c + 1], x[4 * c + 2], x[4 * c + 3]);
-      __syncwarp();
-      float y[32];
-#pragma unroll
-      for (int u = 0; u < LPR; ++u) {
-        const int su = kc_swz<D>(u, t);
-#pragma unroll
-        for (int w4 = 0; w4 < VW / 4; ++w4) {
-          const float4 v = *reinterpret_cast<const float4*>(row + 32 * u + 4 * (((VW / 4) * j + w4) ^ su));
-          y[VW * u + 4 * w4] = v.x; y[VW * u + 4 * w4 + 1] = v.y;
-          y[VW * u + 4 * w4 + 2] = v.z; y[VW * u + 4 * w4 + 3] = v.w;
-        }
-      }
-#pragma unroll
-      for (int hu = 1; hu < LPR; hu <<= 1) {
-#pragma unroll
-        for (int u = 0; u < LPR; ++u) {
-          if ((u & hu) == 0) {
-#pragma unroll
-            for (int v = 0; v < VW; v += 2) {
-              const uint64_t A = ptx::f2_pack(y[VW * u + v], y[VW * u + v + 1]);
-              const uint64_t B = ptx::f2_pack(y[VW * (u + hu) + v], y[VW * (u + hu) + v + 1]);
-              ptx::f2_unpack(ptx::f2_add(A, B), y[VW * u + v], y[VW * u + v + 1]);
-              ptx::f2_unpack(ptx::f2_sub(A, B), y[VW * (u + hu) + v], y[VW * (u + hu) + v + 1]);
-            }
-          }
-        }
-      }
-      const uint64_t s2 = ptx::f2_pack(a.inv_sqrt_d, a.inv_sqrt_d);
-#pragma unroll
-      for (int i = 0; i < 32; i += 2) ptx::f2_unpack(ptx::f2_mul(ptx::f2_pack(y[i], y[i + 1]), s2), y[i], y[i + 1]);
-      // back to the places read (each lane its own): the final rotated row
-#pragma unroll
-      for (int u = 0; u < LPR; ++u) {
-        const int su = kc_swz<D>(u, t);
-#pragma unroll
-        for (int w4 = 0; w4 < VW / 4; ++w4)
-          *reinterpret_cast<float4*>(row + 32 * u + 4 * (((VW / 4) * j + w4) ^ su)) =
-              make_float4(y[VW * u + 4 * w4], y[VW * u + 4 * w4 + 1], y[VW * u + 4 * w4 + 2], y[VW * u + 4 * w4 + 3]);
-      }
-      __syncwarp();
-    }
-  }
-  __syncthreads();
-
-  // 2. channel columns: thread (part, c) takes tokens [part * SLICE, ...)
-  const int c = tid % D;
-  const int part = tid / D;
-  const int ta = part * SLICE, tb = min(n, ta + SLICE);
-  {
-    // four independent running pairs (min and max are exact in any order)
-    float mn[4] = {INFINITY, INFINITY, INFINITY, INFINITY};
-    float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll 2
-    for (int t = ta; t < tb; t += 4) {
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        if (t + u < tb) {
-          const float v = rot[(t + u) * D + kc_pos<D>(c, t + u)];
-          mn[u] = fminf(mn[u], v);
-          mx[u] = fmaxf(mx[u], v);
-        }
-      }
-    }
-    mm[(part * D + c) * 2] = fminf(fminf(mn[0], mn[1]), fminf(mn[2], mn[3]));
-    mm[(part * D + c) * 2 + 1] = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
-  }
-  __syncthreads();
-  {
-    float mn = mm[2 * c], mx = mm[2 * c + 1];
-#pragma unroll
-    for (int p2 = 1; p2 < P; ++p2) {
-      mn = fminf(mn, mm[(p2 * D + c) * 2]);
-      mx = fmaxf(mx, mm[(p2 * D + c) * 2 + 1]);
-    }
-    const QHdr h = group_header<BITS>(mn, mx);
-    if (part == 0 && KVQ_IN_BOUNDS(a.kblk_first + blk, a.kblk_per_head, a.status, a.bounds_site))
-      a.k_sz[((size_t)bh * a.kblk_per_head + a.kblk_first + blk) * D + c] = h.rec;
-#pragma unroll 8
-    for (int t = ta; t < tb; ++t) {
-      const float v = rot[t * D + kc_pos<D>(c, t)];
-      cb[t * D + 16 * ((c >> 4) ^ (t & (CB - 1))) + (c & 15)] = (uint8_t)code_of_value<BITS>(v, h);
-    }
-  }
-  __syncthreads();
-
-  // 3. token t's codes into the packed words (two threads per token, half
-  //    the words each): channel 16w + 2k + h (INT2) / 8w + 2k + h (INT4) at
-  //    bits BITS*k + 16h of word w
-  {
-    constexpr int PER_WORD = 32 / BITS;
-    constexpr int NW = D * BITS / 32;
-    constexpr int NWH = NW / 2;             // words per thread
-    constexpr int CH = NWH * PER_WORD / 16;  // 16-byte code chunks per thread
-    const int t = tid >> 1, hw = tid & 1;
-    if (t < n && KVQ_IN_BOUNDS(a.first + t0 + t, a.cap, a.status, a.bounds_site)) {
-      uint32_t words[NWH];
-#pragma unroll
-      for (int w = 0; w < NWH; ++w) words[w] = 0u;
-#pragma unroll
-      for (int i = 0; i < CH; ++i) {
-        const int ci = hw * CH + i;   // code chunk of the row
-        const uint4 v = *reinterpret_cast<const uint4*>(cb + t * D + 16 * (ci ^ (t & (CB - 1))));
-        const uint32_t uu[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const int ch = 16 * i + e;   // channel within this thread's half
-          const uint32_t code = (uu[e >> 2] >> (8 * (e & 3))) & 0xFFu;
-          const int jw = ch % PER_WORD;
-          words[ch / PER_WORD] |= code << (BITS * (jw >> 1) + 16 * (jw & 1));
-        }
-      }
-      uint8_t* drow = a.k_codes + ((size_t)bh * a.cap + a.first + t0 + t) * (D * BITS / 8) + hw * NWH * 4;
-      if constexpr (NWH >= 4) {
-#pragma unroll
-        for (int i = 0; i < NWH / 4; ++i)
-          reinterpret_cast<uint4*>(drow)[i] = make_uint4(words[4 * i], words[4 * i + 1], words[4 * i + 2], words[4 * i + 3]);
-      } else {
-        *reinterpret_cast<uint2*>(drow) = make_uint2(words[0], words[1 % NWH]);
-      }
-    }
-  }
 }
 
 // Rotation of Q and V_R (FP16 out, with the FP16 remainder when asked) or of
@@ -463,35 +233,6 @@ long long grid_for_rows(long long rows, int rows_per_block, int blocks_per_sm) {
 }
 
 }  // namespace
-
-namespace {
-
-template <int D, int BITS>
-cudaError_t launch_kc(const QuantArgs& a, cudaStream_t s) {
-  if (a.n_new == 0 || a.bh == 0) return cudaSuccess;
-  // fp32 rows + code bytes + per-part column min / max
-  const int smem = kKeyBlock * D * 5 + (kKcThreads / D) * D * 2 * 4;
-  static std::atomic<uint64_t> limit_set{0};   // per template instance and device
-  const cudaError_t e = ensure_smem_limit(quantize_key_channels_kernel<D, BITS>, smem, limit_set);
-  if (e != cudaSuccess) return e;
-  const dim3 grid((unsigned)((a.n_new + kKeyBlock - 1) / kKeyBlock), (unsigned)a.bh);
-  quantize_key_channels_kernel<D, BITS><<<grid, kKcThreads, smem, s>>>(a);
-  note_launch();
-  return cudaGetLastError();
-}
-
-}  // namespace
-
-cudaError_t launch_quantize_key_channels(const QuantArgs& a, int d, int bits, cudaStream_t stream,
-                                         bool* supported) {
-  *supported = true;
-  if (d == 64 && bits == 2) return launch_kc<64, 2>(a, stream);
-  if (d == 64 && bits == 4) return launch_kc<64, 4>(a, stream);
-  if (d == 128 && bits == 2) return launch_kc<128, 2>(a, stream);
-  if (d == 128 && bits == 4) return launch_kc<128, 4>(a, stream);
-  *supported = false;
-  return cudaSuccess;
-}
 
 cudaError_t launch_rotate(const RotateArgs& a, int d, cudaStream_t stream) {
   const long long rows = a.rows[0] + a.rows[1];

@@ -50,18 +50,38 @@ namespace kvq {
 namespace {
 
 constexpr int kMqRows = 128;                       // rows per tile (the MMA's M)
+static_assert(kMqRows == kKeyBlock, "a per-channel key block is one tile");
 constexpr int kMqAcc = 4;                          // accumulators in tensor memory
 constexpr int kMqRanks = 4;                        // epilogue warps per TMEM lane quarter
 constexpr int kMqThreads = 64 + 128 * kMqRanks;    // TMA warp, MMA warp, epilogue
 
-template <int D>
+// what a launch computes
+constexpr int kMqTokens = 0;        // per-token groups: codes and records (K and V rows)
+constexpr int kMqRotOnly = 1;       // the fp32 rotation alone (kvq_rotate)
+constexpr int kMqKeyChannels = 2;   // keys per channel over 128-token blocks
+
+template <int D, int MODE>
 struct MqCfg {
-  static constexpr int kStages = D == 128 ? 4 : 6;
+  static constexpr bool kKch = MODE == kMqKeyChannels;
+  static constexpr int kStages = D == 64 ? 6 : kKch ? 3 : 4;
   static constexpr int kBox = kMqRows * 128;       // one [128][64] BF16 box (bytes)
   static constexpr int kTile = kBox * (D / 64);
   static constexpr int kWBox = D * 128;            // W: [D][64] per 64 input channels
   static constexpr int kWOff = kStages * kTile;
-  static constexpr int kBarOff = kWOff + kWBox * (D / 64);
+  // per-channel keys: the scaled tile [128 tokens][D] fp32, the column
+  // passes' partial min / max [kKcParts][D][2] and the channel headers
+  // [D] x (rcp, step, zero, flags)
+  static constexpr int kKcParts = 4 * kMqRanks * 32 / D;
+  static constexpr int kTOff = kWOff + kWBox * (D / 64);
+  static constexpr int kMmOff = kTOff + (kKch ? kMqRows * D * 4 : 0);
+  // headers: per channel (rcp, step, zero, flags) [D] float4; per channel
+  // pair (rcp, rcp', -step, -step') [D / 2] float4 and (zero, zero') [D / 2]
+  // float2 for the packed fp32 code pass; one flag per 32-channel chunk
+  static constexpr int kHdrOff = kMmOff + (kKch ? kKcParts * D * 8 : 0);
+  static constexpr int kHdrPairOff = kHdrOff + D * 16;
+  static constexpr int kHdrZeroOff = kHdrPairOff + D * 8;
+  static constexpr int kChunkFlagOff = kHdrZeroOff + D * 4;
+  static constexpr int kBarOff = kKch ? kChunkFlagOff + 16 : kHdrOff;
   static constexpr int kFull = 0;                  // [kStages] tile landed (TMA)
   static constexpr int kEmpty = kStages;           // [kStages] tile read by the MMAs
   static constexpr int kAccFull = 2 * kStages;     // [kMqAcc] accumulator written
@@ -78,8 +98,26 @@ struct MqArgs {
   float* rot_out;      // rotation only: fp32 [rows][d]
   int rows;            // rows of one tensor (batch * heads * n_new)
   int tiles_k;         // tiles of the K rows (0 when only V is quantized)
-  int tiles;           // all tiles (K tiles, then V tiles)
+  int tiles;           // all tiles (K tiles, then V tiles; per-channel keys:
+                       // batch * heads * blocks, block-major within a head)
+  int blocks;          // per-channel keys: 128-token blocks of the chunk
 };
+
+// Named barrier of the 16 epilogue warps (id 1; 0 is __syncthreads), and
+// the same barrier returning whether `v` held in every thread.
+__device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, 512;" ::: "memory"); }
+__device__ __forceinline__ bool epi_all(bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.and.pred q, 1, 512, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}\n"
+      : "=r"(r)
+      : "r"((uint32_t)v)
+      : "memory");
+  return r != 0;
+}
 
 // Bounded wait on an mbarrier phase: false when the limit ran out (status
 // and the CTA's abort flag set) or another role aborted.
@@ -99,12 +137,31 @@ __device__ bool mq_wait(uint32_t bar, uint32_t parity, unsigned long long limit_
 }
 
 // The same wait for work this thread issued itself, before the CTA exits:
-// bounded, and not cut short by the abort flag.
+// bounded, not cut short by the abort flag, and never shorter than
+// kMinDrainNs (copies and MMAs in flight finish within microseconds; a tiny
+// wait limit set by the caller must not let the CTA exit before them).
+constexpr unsigned long long kMinDrainNs = 100000000ull;   // 100 ms
 __device__ void mq_drain(uint32_t bar, uint32_t parity, unsigned long long limit_ns) {
+  if (limit_ns < kMinDrainNs) limit_ns = kMinDrainNs;
   const uint64_t t0 = ptx::globaltimer();
   while (!ptx::mbar_try_wait(bar, parity)) {
     if (ptx::globaltimer() - t0 > limit_ns) return;
   }
+}
+
+// The bounded wait on a barrier nothing arrives on (kvq_selftest_wait_timeout):
+// it runs out after limit_ns, records KVQ_ERR_TIMEOUT and returns.
+__global__ void quant_wait_selftest_kernel(unsigned long long limit_ns, int* status) {
+  __shared__ __align__(8) uint64_t b;
+  __shared__ int abort_flag;
+  const uint32_t a = ptx::smem_u32(&b);
+  if (threadIdx.x == 0) {
+    ptx::mbar_init(a, 1);
+    abort_flag = 0;
+    ptx::fence_mbar_init();
+  }
+  __syncthreads();
+  mq_wait(a, 0, limit_ns, &abort_flag, status);
 }
 
 // One group of one row (this thread's TMEM lane, channels [GROUP slot,
@@ -112,7 +169,7 @@ __device__ void mq_drain(uint32_t bar, uint32_t parity, unsigned long long limit
 // loads): every lane runs it, rows past the tensor's end (zero-filled by the
 // TMA) store nothing.  At most 32 values are live: a group of 64 is read
 // twice from tensor memory (min/max, then codes), by 32-channel chunks.
-template <int D, int BITS, int GROUP, bool ROT_ONLY>
+template <int D, int BITS, int GROUP, int MODE>
 __device__ __forceinline__ void mq_group(const MqArgs& m, uint32_t taddr, int row, bool is_v,
                                          int slot) {
   const QuantArgs& a = m.q;
@@ -133,7 +190,7 @@ __device__ __forceinline__ void mq_group(const MqArgs& m, uint32_t taddr, int ro
       ptx::f2_unpack(ptx::f2_mul(p, s2), x[j], x[j + 1]);
     }
   };
-  if constexpr (ROT_ONLY) {
+  if constexpr (MODE == kMqRotOnly) {
 #pragma unroll
     for (int c = 0; c < NCH; ++c) {
       float x[32];
@@ -188,11 +245,203 @@ __device__ __forceinline__ void mq_group(const MqArgs& m, uint32_t taddr, int ro
   }
 }
 
-template <int D, int BITS, int GROUP, bool ROT_ONLY>
+// The code of one value from its channel's header h = (rcp, step, zero,
+// flags: 1 fast route, 2 clamp), as apply_codes does for a group: returns
+// 1.5 * 2^23 + code (the zero point added, clamped when the channel needs
+// it).
+template <int BITS>
+__device__ __forceinline__ float kc_code_one(float v, const float4 h) {
+  constexpr float qmax = float((1 << BITS) - 1);
+  const float kMagic = 12582912.0f;   // 1.5 * 2^23
+  const uint32_t f = __float_as_uint(h.w);
+  if (f & 1u) {
+    const float q0 = __fmul_rn(v, h.x);
+    const float q = __fmaf_rn(__fmaf_rn(-q0, h.y, v), h.x, q0);
+    const float t = __fadd_rn(__fadd_rn(q, kMagic), h.z);
+    return (f & 2u) ? fminf(fmaxf(t, kMagic), kMagic + qmax) : t;
+  }
+  // off the fast route: one IEEE division
+  return __fadd_rn(fminf(fmaxf(__fadd_rn(rintf(__fdiv_rn(v, h.y)), h.z), 0.0f), qmax), kMagic);
+}
+
+// Per-channel keys, one 128-token block of one head (tile t), by the 16
+// epilogue warps together.  Warp (quarter, rank) holds tokens
+// 32 quarter + lane and channels [32 rank, 32 rank + 32) (d = 64: ranks 0
+// and 1; ranks 2 and 3 only help with the column passes).
+// 1. the accumulator times fl(1/sqrt(d)) into registers and into the
+//    shared tile T[token][channel] (16-byte chunk cc of a row at
+//    cc ^ (token mod 8): the row writes and the column reads of a warp meet
+//    32 different banks); the accumulator is released;
+// 2. column passes: thread (part, c) takes channel c over tokens
+//    [part * 128 / P, ...) of the block: min and max;
+// 3. thread c combines the P partial results, computes the channel's header
+//    (Eq. (1), group_header) and stores the block's record;
+// 4. each thread reads its 32 values back from the tile, codes them with the
+//    headers (broadcast reads; packed pairs when the chunk's channels all
+//    take the fast route), packs them and stores the words.
+template <int D, int BITS>
+__device__ __forceinline__ void mq_kc_tile(const MqArgs& m, uint8_t* sm, uint32_t tacc, int t,
+                                           int quarter, int rank, int lane, int tid_e,
+                                           uint32_t acc_empty_bar) {
+  using C = MqCfg<D, kMqKeyChannels>;
+  const QuantArgs& a = m.q;
+  constexpr int NCH = D / 32;
+  constexpr int P = C::kKcParts;
+  constexpr int SLICE = kMqRows / P;
+  constexpr int PER_WORD = 32 / BITS;
+  constexpr int WPC = 32 / PER_WORD;   // code words per 32-channel chunk
+  float* T = reinterpret_cast<float*>(sm + C::kTOff);
+  float2* mm = reinterpret_cast<float2*>(sm + C::kMmOff);
+  float4* hdr = reinterpret_cast<float4*>(sm + C::kHdrOff);
+  const int bh = t / m.blocks, blk = t - bh * m.blocks;
+  const int t0 = blk * kMqRows;
+  const int nb = min(kMqRows, a.n_new - t0);
+  const int tok = 32 * quarter + lane;
+  const bool active = rank < NCH;
+  float* row = T + tok * D;
+  if (active) {
+    uint32_t r[32];
+    ptx::tmem_ld32(tacc + (uint32_t)(32 * rank), r);
+    const uint64_t s2 = ptx::f2_pack(a.inv_sqrt_d, a.inv_sqrt_d);
+#pragma unroll
+    for (int cc = 0; cc < 8; ++cc) {
+      float y[4];
+      ptx::f2_unpack(ptx::f2_mul(ptx::f2_pack(__uint_as_float(r[4 * cc]), __uint_as_float(r[4 * cc + 1])), s2),
+                     y[0], y[1]);
+      ptx::f2_unpack(ptx::f2_mul(ptx::f2_pack(__uint_as_float(r[4 * cc + 2]), __uint_as_float(r[4 * cc + 3])), s2),
+                     y[2], y[3]);
+      *reinterpret_cast<float4*>(row + 4 * ((8 * rank + cc) ^ (tok & 7))) = make_float4(y[0], y[1], y[2], y[3]);
+    }
+  }
+  ptx::tc_fence_before();
+  __syncwarp();
+  if (lane == 0) ptx::mbar_arrive(acc_empty_bar);
+  epi_sync();
+  {
+    static_assert(SLICE % 8 == 0, "a column pass covers whole swizzle periods");
+    const int c = tid_e % D, part = tid_e / D;
+    const int ta = part * SLICE, tb = min(nb, ta + SLICE);
+    // channel c of token k sits at k D + off[k mod 8]
+    int off[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) off[u] = 4 * ((c >> 2) ^ u) + (c & 3);
+    // four independent running pairs (min and max are exact in any order)
+    float mn[4] = {INFINITY, INFINITY, INFINITY, INFINITY};
+    float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+    for (int tt = ta; tt < ta + SLICE; tt += 8) {
+      const float* base = T + tt * D;
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        if (tt + u < tb) {
+          const float v = base[u * D + off[u]];
+          mn[u & 3] = fminf(mn[u & 3], v);
+          mx[u & 3] = fmaxf(mx[u & 3], v);
+        }
+      }
+    }
+    mm[part * D + c] = make_float2(fminf(fminf(mn[0], mn[1]), fminf(mn[2], mn[3])),
+                                   fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])));
+  }
+  epi_sync();
+  if (tid_e < D) {
+    const int c = tid_e;
+    float mn = mm[c].x, mx = mm[c].y;
+#pragma unroll
+    for (int p2 = 1; p2 < P; ++p2) {
+      mn = fminf(mn, mm[p2 * D + c].x);
+      mx = fmaxf(mx, mm[p2 * D + c].y);
+    }
+    const QHdr h = group_header<BITS>(mn, mx);
+    hdr[c] = make_float4(h.rcp, h.delta, h.zero,
+                         __uint_as_float((h.fast ? 1u : 0u) | (h.clamp ? 2u : 0u)));
+    float* hp = reinterpret_cast<float*>(sm + C::kHdrPairOff) + 4 * (c >> 1) + (c & 1);
+    hp[0] = h.rcp;
+    hp[2] = -h.delta;
+    reinterpret_cast<float*>(sm + C::kHdrZeroOff)[c] = h.zero;
+    // a chunk whose 32 channels all take the fast route (clamped or not:
+    // the packed pass clamps every value, which changes nothing where no
+    // code leaves [0, 2^B - 1])
+    const bool simple = __all_sync(0xffffffffu, h.fast);
+    if ((c & 31) == 0) reinterpret_cast<int*>(sm + C::kChunkFlagOff)[c >> 5] = simple ? 1 : 0;
+    if (KVQ_IN_BOUNDS(a.kblk_first + blk, a.kblk_per_head, a.status, a.bounds_site) &&
+        KVQ_IN_BOUNDS(bh, a.bh, a.status, a.bounds_site))
+      a.k_sz[((size_t)bh * a.kblk_per_head + a.kblk_first + blk) * D + c] = h.rec;
+  }
+  epi_sync();
+  if (active) {
+    // the token's 32 values of the chunk, back from the tile (the same
+    // swizzled places: conflict-free, and nothing held across the passes)
+    float x[32];
+#pragma unroll
+    for (int cc = 0; cc < 8; ++cc) {
+      const float4 v = *reinterpret_cast<const float4*>(row + 4 * ((8 * rank + cc) ^ (tok & 7)));
+      x[4 * cc] = v.x;
+      x[4 * cc + 1] = v.y;
+      x[4 * cc + 2] = v.z;
+      x[4 * cc + 3] = v.w;
+    }
+    if (reinterpret_cast<const int*>(sm + C::kChunkFlagOff)[rank]) {
+      // every channel on the fast route: packed pairs, the headers in pair
+      // layout (one 16-byte and one 8-byte broadcast load), every value
+      // clamped to [1.5 * 2^23, 1.5 * 2^23 + 2^B - 1]
+      const float4* hp = reinterpret_cast<const float4*>(sm + C::kHdrPairOff) + 16 * rank;
+      const float2* hz = reinterpret_cast<const float2*>(sm + C::kHdrZeroOff) + 16 * rank;
+      const float kMagic = 12582912.0f;   // 1.5 * 2^23
+      const float kTop = kMagic + float((1 << BITS) - 1);
+      const uint64_t m2 = ptx::f2_pack(kMagic, kMagic);
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const float4 hq = hp[i];
+        const float2 z = hz[i];
+        const uint64_t xv = ptx::f2_pack(x[2 * i], x[2 * i + 1]);
+        const uint64_t r2 = ptx::f2_pack(hq.x, hq.y);
+        const uint64_t q0 = ptx::f2_mul(xv, r2);
+        const uint64_t e = ptx::f2_fma(q0, ptx::f2_pack(hq.z, hq.w), xv);
+        const uint64_t q = ptx::f2_fma(e, r2, q0);
+        float t0, t1;
+        ptx::f2_unpack(ptx::f2_add(ptx::f2_add(q, m2), ptx::f2_pack(z.x, z.y)), t0, t1);
+        x[2 * i] = fminf(fmaxf(t0, kMagic), kTop);
+        x[2 * i + 1] = fminf(fmaxf(t1, kMagic), kTop);
+      }
+    } else {
+      // some channel off the fast route or clamped: value by value, in place
+      // in the tile (one rolled loop), then back into registers
+#pragma unroll 1
+      for (int i = 0; i < 32; ++i) {
+        float* pv = row + 4 * ((8 * rank + (i >> 2)) ^ (tok & 7)) + (i & 3);
+        *pv = kc_code_one<BITS>(*pv, hdr[32 * rank + i]);
+      }
+#pragma unroll
+      for (int cc = 0; cc < 8; ++cc) {
+        const float4 v = *reinterpret_cast<const float4*>(row + 4 * ((8 * rank + cc) ^ (tok & 7)));
+        x[4 * cc] = v.x;
+        x[4 * cc + 1] = v.y;
+        x[4 * cc + 2] = v.z;
+        x[4 * cc + 3] = v.w;
+      }
+    }
+    uint32_t words[WPC];
+#pragma unroll
+    for (int w = 0; w < WPC; ++w) words[w] = pack_word<BITS>(x + PER_WORD * w, 0);
+    if (tok < nb && KVQ_IN_BOUNDS(a.first + t0 + tok, a.cap, a.status, a.bounds_site) &&
+        KVQ_IN_BOUNDS(bh, a.bh, a.status, a.bounds_site)) {
+      uint8_t* dc = a.k_codes + ((size_t)bh * a.cap + a.first + t0 + tok) * (D * BITS / 8) +
+                    32 * rank * BITS / 8;
+      if constexpr (WPC == 2) {
+        *reinterpret_cast<uint2*>(dc) = make_uint2(words[0], words[1 % WPC]);
+      } else {
+        *reinterpret_cast<uint4*>(dc) = make_uint4(words[0], words[1 % WPC], words[2 % WPC], words[3 % WPC]);
+      }
+    }
+  }
+}
+
+template <int D, int BITS, int GROUP, int MODE>
 __global__ void __launch_bounds__(kMqThreads, 1)
     quantize_mma_kernel(const __grid_constant__ CUtensorMap map_k,
                         const __grid_constant__ CUtensorMap map_v, const MqArgs m) {
-  using C = MqCfg<D>;
+  using C = MqCfg<D, MODE>;
   extern __shared__ uint8_t mq_raw[];
   // 128-byte swizzled operands: every box starts on a 1024-byte boundary
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(mq_raw) + 1023) &
@@ -209,21 +458,32 @@ __global__ void __launch_bounds__(kMqThreads, 1)
   // tile i of this CTA (t = blockIdx.x + i * grid) into stage i mod kStages
   auto issue = [&](int i, int t) {
     const int st = i % C::kStages;
-    const bool v = t >= m.tiles_k;
-    const int row0 = (v ? t - m.tiles_k : t) * kMqRows;
     ptx::mbar_expect_tx(bar(C::kFull + st), C::kTile);
+    if constexpr (MODE == kMqKeyChannels) {
+      // block blk of head bh: tokens [128 blk, 128 blk + 128) of a [bh][n][d]
+      // map (tokens past the chunk read as zeros)
+      const int bh = t / m.blocks, blk = t - bh * m.blocks;
 #pragma unroll
-    for (int b = 0; b < D / 64; ++b)
-      ptx::tma_load_2d(sbase + st * C::kTile + b * C::kBox, v ? &map_v : &map_k, 64 * b, row0,
-                       bar(C::kFull + st));
+      for (int b = 0; b < D / 64; ++b)
+        ptx::tma_load_3d(sbase + st * C::kTile + b * C::kBox, &map_k, 64 * b, blk * kMqRows, bh,
+                         bar(C::kFull + st));
+    } else {
+      const bool v = t >= m.tiles_k;
+      const int row0 = (v ? t - m.tiles_k : t) * kMqRows;
+#pragma unroll
+      for (int b = 0; b < D / 64; ++b)
+        ptx::tma_load_2d(sbase + st * C::kTile + b * C::kBox, v ? &map_v : &map_k, 64 * b, row0,
+                         bar(C::kFull + st));
+    }
   };
   int issued = 0;   // thread 0: tiles whose loads are issued
   if (threadIdx.x == 0) {
     ptx::prefetch_tensormap(&map_k);
     ptx::prefetch_tensormap(&map_v);
-    // an accumulator is released by the 4 D / GROUP warps of the team that read it
-    for (int i = 0; i < C::kBars; ++i)
-      ptx::mbar_init(bar(i), i >= C::kAccEmpty ? (uint32_t)(4 * (D / GROUP)) : 1u);
+    // an accumulator is released by the warps that read it: the 4 D / GROUP
+    // warps of a team, or all 16 epilogue warps for per-channel keys
+    constexpr uint32_t kReaders = MODE == kMqKeyChannels ? 4 * kMqRanks : 4 * (D / GROUP);
+    for (int i = 0; i < C::kBars; ++i) ptx::mbar_init(bar(i), i >= C::kAccEmpty ? kReaders : 1u);
     *abort_flag = 0;
     ptx::fence_mbar_init();
     // the inputs may come from the kernel launched before this one (a
@@ -306,6 +566,20 @@ __global__ void __launch_bounds__(kMqThreads, 1)
       // every MMA issued is complete before the TMEM is freed
       if (i > 0) mq_drain(bar(C::kAccFull + (i - 1) % kMqAcc), ((i - 1) / kMqAcc) & 1, lim);
     }
+  } else if constexpr (MODE == kMqKeyChannels) {
+    const int quarter = warp & 3;             // TMEM lanes 32 quarter .. + 31
+    const int rank = (warp - 2) >> 2;
+    const int tid_e = (int)threadIdx.x - 64;
+    int i = 0;
+    for (int t = (int)blockIdx.x; t < m.tiles; t += grid, ++i) {
+      const int ac = i % kMqAcc;
+      const bool ok = mq_wait(bar(C::kAccFull + ac), (i / kMqAcc) & 1, lim, abort_flag, a.status);
+      // one decision for the whole epilogue: its warps meet at named barriers
+      if (!epi_all(ok)) break;
+      ptx::tc_fence_after();
+      mq_kc_tile<D, BITS>(m, sm, tmem + (uint32_t)(ac * D) + ((uint32_t)(32 * quarter) << 16), t,
+                          quarter, rank, lane, tid_e, bar(C::kAccEmpty + ac));
+    }
   } else {
     // the four warps of a rank cover the four TMEM lane quarters; the ranks
     // split a tile's groups (D / GROUP of them, one rank each) and the
@@ -324,7 +598,7 @@ __global__ void __launch_bounds__(kMqThreads, 1)
       ptx::tc_fence_after();
       const bool v = t >= m.tiles_k;
       const int row = (v ? t - m.tiles_k : t) * kMqRows + 32 * quarter + lane;
-      mq_group<D, BITS, GROUP, ROT_ONLY>(
+      mq_group<D, BITS, GROUP, MODE>(
           m, tmem + (uint32_t)(ac * D) + ((uint32_t)(32 * quarter) << 16), row, v, slot);
       ptx::tc_fence_before();
       __syncwarp();
@@ -347,12 +621,12 @@ int mq_sm_count() {
   return n;
 }
 
-template <int D, int BITS, int GROUP, bool ROT_ONLY>
+template <int D, int BITS, int GROUP, int MODE>
 cudaError_t launch_mq(const MqArgs& m, const CUtensorMap& mk, const CUtensorMap& mv,
                       cudaStream_t s) {
-  using C = MqCfg<D>;
+  using C = MqCfg<D, MODE>;
   if (m.tiles <= 0) return cudaSuccess;
-  auto kern = quantize_mma_kernel<D, BITS, GROUP, ROT_ONLY>;
+  auto kern = quantize_mma_kernel<D, BITS, GROUP, MODE>;
   static std::atomic<uint64_t> limit_set{0};   // per template instance and device
   const cudaError_t e = ensure_smem_limit(kern, C::kSmem, limit_set);
   if (e != cudaSuccess) return e;
@@ -391,7 +665,22 @@ cudaError_t launch_quant_t(const QuantArgs& a, cudaStream_t s) {
   } else if (!make_rows_map(&mk, a.k_new, D, m.rows, kMqRows)) {
     return cudaErrorInvalidValue;
   }
-  return launch_mq<D, BITS, GROUP, false>(m, mk, mv, s);
+  return launch_mq<D, BITS, GROUP, kMqTokens>(m, mk, mv, s);
+}
+
+template <int D, int BITS>
+cudaError_t launch_kc_t(const QuantArgs& a, cudaStream_t s) {
+  if (a.n_new == 0 || a.bh == 0) return cudaSuccess;
+  MqArgs m{};
+  m.q = a;
+  m.rot_out = nullptr;
+  m.rows = a.n_new;
+  m.blocks = (a.n_new + kMqRows - 1) / kMqRows;
+  m.tiles = a.bh * m.blocks;
+  m.tiles_k = m.tiles;
+  CUtensorMap mk;
+  if (!make_map(&mk, a.k_new, D, a.n_new, a.bh, true, kMqRows)) return cudaErrorInvalidValue;
+  return launch_mq<D, BITS, 32, kMqKeyChannels>(m, mk, mk, s);
 }
 
 }  // namespace
@@ -414,6 +703,24 @@ cudaError_t launch_quantize_append_mma(const QuantArgs& a, int d, int bits, int 
   return cudaSuccess;
 }
 
+cudaError_t launch_quantize_key_channels_mma(const QuantArgs& a, int d, int bits,
+                                             cudaStream_t stream, bool* supported) {
+  *supported = true;
+  if (d == 64 && bits == 2) return launch_kc_t<64, 2>(a, stream);
+  if (d == 64 && bits == 4) return launch_kc_t<64, 4>(a, stream);
+  if (d == 128 && bits == 2) return launch_kc_t<128, 2>(a, stream);
+  if (d == 128 && bits == 4) return launch_kc_t<128, 4>(a, stream);
+  *supported = false;
+  return cudaSuccess;
+}
+
+cudaError_t launch_quant_wait_selftest(unsigned long long limit_ns, int* status,
+                                      cudaStream_t stream) {
+  quant_wait_selftest_kernel<<<1, 32, 0, stream>>>(limit_ns, status);
+  note_launch();
+  return cudaGetLastError();
+}
+
 cudaError_t launch_rotate_mma_f32(const uint16_t* x, long long rows, int d,
                                   const uint32_t sign_bits[4], float* out, int* status,
                                   int* bounds_site, unsigned long long wait_limit_ns,
@@ -434,8 +741,8 @@ cudaError_t launch_rotate_mma_f32(const uint16_t* x, long long rows, int d,
     m.tiles = m.tiles_k;
     CUtensorMap mk;
     if (!make_rows_map(&mk, x + off * d, d, n, kMqRows)) return cudaErrorInvalidValue;
-    const cudaError_t e = d == 64 ? launch_mq<64, 2, 32, true>(m, mk, mk, stream)
-                                  : launch_mq<128, 2, 32, true>(m, mk, mk, stream);
+    const cudaError_t e = d == 64 ? launch_mq<64, 2, 32, kMqRotOnly>(m, mk, mk, stream)
+                                  : launch_mq<128, 2, 32, kMqRotOnly>(m, mk, mk, stream);
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;

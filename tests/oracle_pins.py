@@ -171,6 +171,42 @@ def check_quantize_admissible():
     assert set(np.unique(cz)) == {1.0, 2.0}
 
 
+def check_key_channels_admissible():
+    """quantize_key_channels_admissible: exact bounds give the per-channel
+    quantizer's one answer (every block, the last one short); keys sampled
+    inside interval bounds always have their answer among the candidates."""
+    rng = np.random.default_rng(23)
+    for bits in (2, 4):
+        y = (rng.standard_normal((300, 64)) * 2 + rng.standard_normal((1, 64)) * 3).astype(np.float32)
+        codes, delta, zero = O.quantize_key_channels(y, bits)
+        blocks = O.chunk_blocks(300)
+        adm = O.quantize_key_channels_admissible(y, y, bits)
+        assert len(adm) == len(blocks) == 3
+        for (a, b), (cd, cz, clo, chi), dl, z in zip(blocks, adm, delta, zero):
+            for i in range(4):
+                assert np.array_equal(cd[:, i], dl) and np.array_equal(cz[:, i], z)
+                assert np.array_equal(clo[:, i, :], codes[a:b].T) and np.array_equal(chi[:, i, :], codes[a:b].T)
+        lo = y - (np.spacing(np.abs(y)) * rng.integers(0, 40, y.shape)).astype(np.float32)
+        hi = y + (np.spacing(np.abs(y)) * rng.integers(0, 40, y.shape)).astype(np.float32)
+        # a one-token block: every channel a constant group (step |value|)
+        c1, d1, z1 = O.quantize_key_channels(y[:1], bits)
+        (cd1, cz1, clo1, chi1), = O.quantize_key_channels_admissible(lo[:1], hi[:1], bits)
+        ok1 = ((cd1 == d1[0][:, None]) & (cz1 == z1[0][:, None]) &
+               np.all((clo1 <= c1.T[:, None, :]) & (c1.T[:, None, :] <= chi1), axis=-1))
+        assert ok1.any(axis=-1).all()
+        (cd1, _, _, _), = O.quantize_key_channels_admissible(y[:1], y[:1], bits)
+        assert np.array_equal(cd1[:, 0], d1[0]) and np.array_equal(d1[0], O.bf16_round(np.abs(y[0])))
+        adm = O.quantize_key_channels_admissible(lo, hi, bits)
+        for _ in range(8):
+            ys = np.where(rng.integers(0, 2, y.shape) == 1, lo, hi).astype(np.float32)
+            c, dl, z = O.quantize_key_channels(ys, bits)
+            for (a, b), (cd, cz, clo, chi), dlb, zb in zip(blocks, adm, dl, z):
+                cb = c[a:b].T[:, None, :]
+                ok = ((cd == dlb[:, None]) & (cz == zb[:, None]) &
+                      np.all((clo <= cb) & (cb <= chi), axis=-1))
+                assert ok.any(axis=-1).all(), bits
+
+
 def check_bf16_round_matches_torch():
     rng = np.random.default_rng(3)
     x = np.concatenate([

@@ -204,11 +204,17 @@ def test_precise_split_chosen_per_head():
 
 
 def test_bounded_wait_reports_timeout():
-    """A kernel waits on a barrier nothing arrives on: the wait runs out after
-    the limit, the kernel returns, the status reads TIMEOUT once, and the
-    context stays usable."""
+    """Kernels wait on a barrier nothing arrives on (the attention kernels'
+    bounded wait and the tensor-core quantizer's): each wait runs out after
+    the limit, the kernels return, the status reads TIMEOUT once, and the
+    context stays usable.  Both run out: each takes at least the limit."""
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
     kvq.selftest_wait_timeout(2_000_000)          # 2 ms
+    e1.record()
     assert kvq.last_device_status() == kvq.KVQ_ERR_TIMEOUT
+    assert e0.elapsed_time(e1) >= 2 * 2.0 * 0.99   # ms
     assert kvq.last_device_status() == kvq.KVQ_OK
     t = torch.ones(10, device="cuda")
     assert float(t.sum().item()) == 10.0

@@ -160,43 +160,62 @@ def test_append_workload_chunk(name):
     _check_slot(cache, "v", x["v_new"], s, 0, w.chunk_tokens)
 
 
-def _check_key_channel_slot(cache, x, signs, slot, n):
+def _check_key_channel_slot(cache, x, signs, slot, n, min_unique=0.99):
     """Per-channel keys of one appended chunk x [B, H, n, d] in slot `slot`:
     packed codes per token and (step, zero) per block and channel, against
-    the oracle's per-channel quantizer, bit for bit."""
+    the oracle's admissible answers for the rotation known to within its
+    fp32 summation bound; `min_unique` of the codes must be fixed by the
+    bounds (1.0 on grid rows, which the oracle then matches bit for bit)."""
     C = cache.chunk_tokens
     first = slot * C
+    d = cache.head_dim
     codes = cache.codes_view("k")[:, :, first:first + n].cpu().numpy()
     meta = cache.sz_view("k")[:, :, slot].cpu().numpy().view(np.uint16)   # [B, H, bpc, d, 2]
-    nb = -(-n // kvq.KEY_BLOCK)
+    fixed = total = 0
     for b in range(x.shape[0]):
         for h in range(x.shape[1]):
-            packed, delta, zero, _, _ = O.quantize_key_chunk(x[b, h].float().numpy(), signs, cache.bits)
-            assert np.array_equal(codes[b, h], packed), f"key codes differ (b{b} h{h})"
-            assert np.array_equal(meta[b, h, :nb, :, 0], O.bf16_bits(delta)), "key steps differ"
-            assert np.array_equal(meta[b, h, :nb, :, 1], O.bf16_bits(zero)), "key zero points differ"
+            lo, hi = O.rotation_bounds(x[b, h].float().numpy(), signs)
+            got = O.unpack_codes(codes[b, h], cache.bits, d)                  # [n, d]
+            for i, ((a0, a1), (cd, cz, clo, chi)) in enumerate(
+                    zip(O.chunk_blocks(n), O.quantize_key_channels_admissible(lo, hi, cache.bits))):
+                g = got[a0:a1].T[:, None, :]                                  # [d, 1, tokens]
+                ok = ((O.bf16_bits(cd) == meta[b, h, i, :, 0][:, None]) &
+                      (O.bf16_bits(cz) == meta[b, h, i, :, 1][:, None]) &
+                      np.all((clo <= g) & (g <= chi), axis=-1))
+                assert ok.any(axis=-1).all(), f"key block {i} (b{b} h{h}) outside the admissible answers"
+                fixed += int(np.sum(clo == chi))
+                total += clo.size
+    assert fixed / total >= min_unique, f"only {fixed / total:.5f} of the key codes determined"
 
 
 @pytest.mark.parametrize("d,bits,group", [(128, 2, 32), (128, 4, 64), (64, 2, 32), (64, 4, 64)])
 def test_append_key_channels_bitexact_ring(d, bits, group):
     """Per-channel key mode: 300-token chunks (two full 128-token blocks and a
     44-token one) filling a 3-slot window and wrapping once, then a partial
-    chunk after a reset; keys bit-exact per block and channel, values per
-    token and group among the admissible answers."""
+    chunk after a reset; keys per block and channel and values per token and
+    group among the oracle's admissible answers (grid rows on the last step:
+    exactly the oracle's answer)."""
     rng = np.random.default_rng(d + bits)
     B, H, C, n = 1, 3, 300, 3
     s = synth.hadamard_signs(d, seed=5)
     cache = kvq.KVCache(B, H, d, bits, group, C, n, s, key_mode=kvq.KEYS_PER_CHANNEL)
     for step in range(n + 1):
-        k = rng.standard_normal((B, H, C, d)) * 2 + rng.standard_normal((1, 1, 1, d)) * 3
-        k[..., :3] *= 10                                   # outlier channels
-        k = _bf16(k)
+        grid = step == n
+        if grid:
+            k = _grid(rng, (B, H, C, d))
+        else:
+            k = rng.standard_normal((B, H, C, d)) * 2 + rng.standard_normal((1, 1, 1, d)) * 3
+            k[..., :3] *= 10                                   # outlier channels
+            k = _bf16(k)
         v = _bf16(rng.standard_normal((B, H, C, d)))
         slot = cache.head_slot
         kvq.quantize_append(cache, k.cuda(), v.cuda())
         torch.cuda.synchronize()
-        _check_key_channel_slot(cache, k, s, slot, C)
+        _check_key_channel_slot(cache, k, s, slot, C, 1.0 if grid else 0.99)
         _check_slot(cache, "v", v, s, slot * C, C)
+        if grid:
+            packed = O.quantize_key_chunk(k[0, 0].float().numpy(), s, bits)[0]
+            assert np.array_equal(cache.codes_view("k")[0, 0, slot * C:(slot + 1) * C].cpu().numpy(), packed)
     part = kvq.KVCache(B, H, d, bits, group, C, n, s, key_mode=kvq.KEYS_PER_CHANNEL)
     kvq.quantize_append(part, k.cuda(), v.cuda())
     kvq.quantize_append(part, k[:, :, :1].contiguous().cuda(), v[:, :, :1].contiguous().cuda())
@@ -209,8 +228,8 @@ def test_append_key_channels_bitexact_ring(d, bits, group):
 @pytest.mark.parametrize("name", ["w4_int2", "hires_t3"])
 def test_append_key_channels_workload_chunk(name):
     """One full chunk of the workload (all heads) in the per-channel key mode,
-    keys bit-exact, values admissible: 4680 or 14400 tokens, the last block
-    partial."""
+    keys and values among the admissible answers: 4680 or 14400 tokens, the
+    last block partial."""
     w = synth.WORKLOADS[name]
     x = synth.inputs(w, n_q=1, n_s=1, n_r=1)
     s = synth.hadamard_signs(w.head_dim)
