@@ -237,7 +237,6 @@ kvq_status attention_common(const kvq_cache* cache, const uint16_t* q, const uin
   ra.rows[1] = mass_only ? 0 : (long long)g.bh * n_r;
   for (int i = 0; i < 4; ++i) ra.sign_bits[i] = cache->sign_bits[i];
   ra.inv_sqrt_d = (float)(1.0 / std::sqrt((double)g.d));
-  ra.out_f32 = 0;
   // FP16 operand limits: every rotated value below 65504; with per-channel
   // keys and the Taylor term the pre-pass squares the query (q'^2 / 64 in
   // FP16): |q'| < 2047
@@ -458,13 +457,12 @@ kvq_status kvq_rotate(const uint16_t* x, int64_t rows, int32_t d, const uint32_t
   }
   kvq::RotateArgs a{};
   a.src[0] = x;
-  a.dst[0] = out_f32 ? static_cast<void*>(out_f32) : static_cast<void*>(out_f16);
+  a.dst[0] = out_f16;
   a.dst_lo[0] = nullptr;
   a.rows[0] = rows;
   a.rows[1] = 0;
   for (int i = 0; i < 4; ++i) a.sign_bits[i] = sign_bits[i];
   a.inv_sqrt_d = (float)(1.0 / std::sqrt((double)d));
-  a.out_f32 = out_f32 ? 1 : 0;
   // no FP16 range limits here (range_limit 0); the status word serves the
   // checked build's index checks
   a.status = kvq::status_ptr();

@@ -55,8 +55,8 @@ struct QuantArgs {
 };
 
 // Arguments of the rotation kernel: up to two row segments in one launch.
-// Per segment: fp32 output (out_f32), or FP16 output in dst plus, when
-// dst_lo is set, the FP16 rounding remainder fp16(x - fp16(x)) in dst_lo.
+// Per segment: FP16 output in dst plus, when dst_lo is set, the FP16
+// rounding remainder fp16(x - fp16(x)) in dst_lo.
 // With status set, a segment whose range_limit[i] > 0 records KVQ_ERR_RANGE
 // there when a rotated value reaches that magnitude (FP16 outputs only).
 struct RotateArgs {
@@ -66,7 +66,6 @@ struct RotateArgs {
   long long rows[2];
   uint32_t sign_bits[4];
   float inv_sqrt_d;
-  int out_f32;
   int* status;
   float range_limit[2];
   int* bounds_site;   // checked build: source line of the first failed index check

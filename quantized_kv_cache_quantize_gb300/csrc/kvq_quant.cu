@@ -28,16 +28,16 @@ __device__ __forceinline__ uint32_t sign_word_for(const uint32_t (&sb)[4], int t
   return i == 0 ? sb[0] : i == 1 ? sb[1] : i == 2 ? sb[2] : sb[3];
 }
 
-// Rotation of Q and V_R (FP16 out, with the FP16 remainder when asked) or of
-// any BF16 rows (fp32 out).  LPR = d / 32 lanes per row, 32 channels per
+// Rotation of Q and V_R to FP16 (with the FP16 remainder when asked).
+// LPR = d / 32 lanes per row, 32 channels per
 // lane: lane j first holds channels [32j, 32j + 32) and runs the butterflies
 // h = 1 .. 16 in registers; one transpose through shared memory then gives
 // it channels {32u + (32 / LPR) j + v} (u < LPR, v < 32 / LPR), whose
 // butterflies h = 32 (and 64) are again in registers.  Same fp32 operations
 // in the same order as the textbook transform (h = 1, 2, ..., d/2, then the
-// multiply by fl(1/sqrt(d))), so the fp32 output is bit for bit the
-// quantizer's rotation.  Each lane's next row is loaded before the current
-// one is transformed.
+// multiply by fl(1/sqrt(d))), so the FP16 outputs are the oracle's fp32
+// rotation rounded.  Each lane's next row is loaded before the current one
+// is transformed.
 constexpr int kRotThreads = 256;
 constexpr int kRotBlocksPerSm = 2;
 
@@ -177,13 +177,7 @@ __global__ void __launch_bounds__(kRotThreads, kRotBlocksPerSm) rotate_kernel(co
 #pragma unroll
     for (int u = 0; u < LPR; ++u) {
       const long long off = rr * D + 32 * u + VW * j;   // first channel of this run
-      if (a.out_f32) {
-        float4* dst = reinterpret_cast<float4*>(static_cast<float*>(dstp) + off);
-#pragma unroll
-        for (int q4 = 0; q4 < VW / 4; ++q4)
-          dst[q4] = make_float4(y[VW * u + 4 * q4], y[VW * u + 4 * q4 + 1], y[VW * u + 4 * q4 + 2],
-                                y[VW * u + 4 * q4 + 3]);
-      } else {
+      {
         uint32_t hw[VW / 2], lw[VW / 2];
 #pragma unroll
         for (int q2 = 0; q2 < VW / 2; ++q2) {

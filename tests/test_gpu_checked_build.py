@@ -60,6 +60,7 @@ for d, bits, group, n_q, n_s, n_r, chunk, n_chunks, heads, km in cases:
     clean(("mass", d, bits, km))
 xr = synth.inputs(synth.WORKLOADS["tiny"], seed=1, n_q=300)["q"].cuda()
 kvq.rotate(xr, synth.hadamard_signs(64))
+kvq.rotate(xr, synth.hadamard_signs(64), torch.float16)
 clean("rotate")
 print("checked build clean")
 '''
