@@ -113,7 +113,7 @@ def kernel_source_hash() -> str:
     instantiates the default mode)."""
     h = hashlib.sha256()
     for name in ("kvq_attn_kernel.cuh", "kvq_attn.cu", "kvq_sm100.cuh", "kvq_checks.cuh",
-                 "kvq_fwht.cuh"):
+                 "kvq_fwht.cuh", "kvq_tmap.cuh"):
         with open(os.path.join(ROOT, "quantized_kv_cache_quantize_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
