@@ -145,7 +145,7 @@ def test_append_partial_and_degenerate(d, bits, group):
     assert e.value.status == kvq.KVQ_ERR_CAPACITY
 
 
-@pytest.mark.parametrize("name", ["tiny", "w4_int2", "w4_int4"])
+@pytest.mark.parametrize("name", ["tiny", "w4_int2", "w4_int4", "hires_t3"])
 def test_append_workload_chunk(name):
     """One full chunk of the workload's key/value distribution (all heads):
     outlier channels, per-channel offsets; admissible answers, and the
@@ -239,3 +239,35 @@ def test_append_key_channels_workload_chunk(name):
     torch.cuda.synchronize()
     _check_key_channel_slot(cache, x["k_new"], s, 0, w.chunk_tokens)
     _check_slot(cache, "v", x["v_new"], s, 0, w.chunk_tokens)
+
+
+def test_append_waits_for_the_previous_attention():
+    """The append is launched so that its start may overlap the end of the
+    kernel before it in the stream; it must not write the cache slot that
+    kernel still reads.  A full window, an attention call over it and, with
+    no synchronization between them, an append overwriting the oldest slot:
+    the attention's output is the one computed before the append, bit for
+    bit (the attention kernels are deterministic)."""
+    w = synth.WORKLOADS["w4_int2"]
+    x = synth.inputs(w, n_q=512, n_r=256)
+    s = synth.hadamard_signs(w.head_dim)
+    cache = kvq.KVCache(1, w.heads, w.head_dim, w.bits, w.group, w.chunk_tokens, w.n_chunks, s)
+    kw, vw = x["k_win"].cuda(), x["v_win"].cuda()
+    for c in range(w.n_chunks):
+        sl = slice(c * w.chunk_tokens, (c + 1) * w.chunk_tokens)
+        kvq.quantize_append(cache, kw[:, :, sl].contiguous(), vw[:, :, sl].contiguous())
+    q, kc, vc = x["q"].cuda(), x["k_cur"].cuda(), x["v_cur"].cuda()
+    ref = kvq.attention_corrected(cache, q, kc, vc)
+    torch.cuda.synchronize()
+    kn, vn = x["k_new"].cuda(), x["v_new"].cuda()
+    for _ in range(3):
+        out = kvq.attention_corrected(cache, q, kc, vc)
+        kvq.quantize_append(cache, kn, vn)          # overwrites a slot the attention reads
+        torch.cuda.synchronize()
+        assert torch.equal(out, ref)
+        # put the window back: the same chunks in the same slots
+        c = (cache.head_slot - 1) % w.n_chunks
+        sl = slice(c * w.chunk_tokens, (c + 1) * w.chunk_tokens)
+        cache.struct.head_slot = c
+        kvq.quantize_append(cache, kw[:, :, sl].contiguous(), vw[:, :, sl].contiguous())
+    assert kvq.last_device_status() == kvq.KVQ_OK
