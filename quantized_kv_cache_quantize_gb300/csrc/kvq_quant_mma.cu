@@ -1,4 +1,6 @@
-// Per-token quantize-append with the rotation on the tensor cores (sm_103a).
+// Quantize-append with the rotation on the tensor cores (sm_103a): keys and
+// values per token and group, keys per channel over 128-token blocks (the
+// per-channel key mode), and the rotation alone (kvq_rotate's fp32 output).
 //
 // The randomized Hadamard rotation of a row (paper section 3, "Hadamard
 // rotation") is the product x' = fl(1/sqrt(d)) * (W x) with the +-1 matrix
@@ -28,9 +30,11 @@
 //              one of kMqAcc accumulators and commits them to the stage's
 //              "empty" and the accumulator's "full" barrier;
 //   warps 2-17 the epilogue: warp w reads TMEM lanes 32 (w mod 4) .. + 31
-//              (a rank of four warps covers a tile's 128 rows) and codes
-//              one group of those rows; the d / GROUP ranks of a team share
-//              a tile, and the 4 GROUP / d teams take tiles in turn.
+//              (a rank of four warps covers a tile's 128 rows).  Per token:
+//              each warp codes one group of those rows; the d / GROUP ranks
+//              of a team share a tile, and the 4 GROUP / d teams take tiles
+//              in turn.  Per channel: all 16 warps take each tile together
+//              (mq_kc_tile: a tile is one 128-token block of one head).
 // Every mbarrier wait is bounded (the library's wait limit): when one runs
 // out the kernel records KVQ_ERR_TIMEOUT, the other roles stop at their next
 // wait, the TMA thread waits (bounded) for its copies in flight, the MMA
