@@ -33,8 +33,9 @@
 //              (a rank of four warps covers a tile's 128 rows).  Per token:
 //              each warp codes one group of those rows; the d / GROUP ranks
 //              of a team share a tile, and the 4 GROUP / d teams take tiles
-//              in turn.  Per channel: all 16 warps take each tile together
-//              (mq_kc_tile: a tile is one 128-token block of one head).
+//              in turn.  Per channel (a tile is one 128-token block of one
+//              head): warps 2-9 take the statistics (mq_kc_stats) and warps
+//              10-17 the codes (mq_kc_codes) of consecutive tiles at once.
 // Every mbarrier wait is bounded (the library's wait limit): when one runs
 // out the kernel records KVQ_ERR_TIMEOUT, the other roles stop at their next
 // wait, the TMA thread waits (bounded) for its copies in flight, the MMA
@@ -73,24 +74,28 @@ struct MqCfg {
   static constexpr int kWBox = D * 128;            // W: [D][64] per 64 input channels
   static constexpr int kWOff = kStages * kTile;
   // per-channel keys: the scaled tile [128 tokens][D] fp32, the column
-  // passes' partial min / max [kKcParts][D][2] and the channel headers
-  // [D] x (rcp, step, zero, flags)
-  static constexpr int kKcParts = 4 * kMqRanks * 32 / D;
+  // passes' partial min / max [kKcParts][D][2] (kKcStatThreads threads), and
+  // two buffers of channel headers (tile i in buffer i mod 2): per channel
+  // (rcp, step, zero, flags) [D] float4; per channel pair (rcp, rcp', -step,
+  // -step') [D / 2] float4 and (zero, zero') [D / 2] float2 for the packed
+  // fp32 code pass; one flag per 32-channel chunk
+  static constexpr int kKcStatThreads = 256;
+  static constexpr int kKcParts = kKcStatThreads / D;
   static constexpr int kTOff = kWOff + kWBox * (D / 64);
   static constexpr int kMmOff = kTOff + (kKch ? kMqRows * D * 4 : 0);
-  // headers: per channel (rcp, step, zero, flags) [D] float4; per channel
-  // pair (rcp, rcp', -step, -step') [D / 2] float4 and (zero, zero') [D / 2]
-  // float2 for the packed fp32 code pass; one flag per 32-channel chunk
   static constexpr int kHdrOff = kMmOff + (kKch ? kKcParts * D * 8 : 0);
-  static constexpr int kHdrPairOff = kHdrOff + D * 16;
-  static constexpr int kHdrZeroOff = kHdrPairOff + D * 8;
-  static constexpr int kChunkFlagOff = kHdrZeroOff + D * 4;
-  static constexpr int kBarOff = kKch ? kChunkFlagOff + 16 : kHdrOff;
+  static constexpr int kHdrPair = D * 16;              // offsets inside a header buffer
+  static constexpr int kHdrZero = kHdrPair + D * 8;
+  static constexpr int kChunkFlag = kHdrZero + D * 4;
+  static constexpr int kHdrBytes = kChunkFlag + 16;
+  static constexpr int kBarOff = kKch ? kHdrOff + 2 * kHdrBytes : kHdrOff;
   static constexpr int kFull = 0;                  // [kStages] tile landed (TMA)
   static constexpr int kEmpty = kStages;           // [kStages] tile read by the MMAs
   static constexpr int kAccFull = 2 * kStages;     // [kMqAcc] accumulator written
-  static constexpr int kAccEmpty = 2 * kStages + kMqAcc;   // [kMqAcc] read (a team's warps)
-  static constexpr int kBars = 2 * kStages + 2 * kMqAcc;
+  static constexpr int kAccEmpty = 2 * kStages + kMqAcc;   // [kMqAcc] read (its readers)
+  static constexpr int kHdrFull = 2 * kStages + 2 * kMqAcc;   // [2] per-channel headers written
+  static constexpr int kHdrEmpty = kHdrFull + 2;              // [2] headers used by the code warps
+  static constexpr int kBars = 2 * kStages + 2 * kMqAcc + (kKch ? 4 : 0);
   static constexpr int kAbortOff = kBarOff + 8 * kBars;
   static constexpr int kTmemSlotOff = kAbortOff + 4;
   static constexpr int kSmem = kTmemSlotOff + 4 + 1024;   // + room to align the base
@@ -107,15 +112,16 @@ struct MqArgs {
   int blocks;          // per-channel keys: 128-token blocks of the chunk
 };
 
-// Named barrier of the 16 epilogue warps (id 1; 0 is __syncthreads), and
-// the same barrier returning whether `v` held in every thread.
-__device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, 512;" ::: "memory"); }
-__device__ __forceinline__ bool epi_all(bool v) {
+// Named barrier of the per-channel statistics warps (id 1, 256 threads; 0
+// is __syncthreads), and the same barrier returning whether `v` held in
+// every one of them.
+__device__ __forceinline__ void stat_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
+__device__ __forceinline__ bool stat_all(bool v) {
   uint32_t r;
   asm volatile(
       "{\n\t.reg .pred p, q;\n\t"
       "setp.ne.u32 p, %1, 0;\n\t"
-      "bar.red.and.pred q, 1, 512, p;\n\t"
+      "bar.red.and.pred q, 1, 256, p;\n\t"
       "selp.u32 %0, 1, 0, q;\n\t}\n"
       : "=r"(r)
       : "r"((uint32_t)v)
@@ -268,62 +274,70 @@ __device__ __forceinline__ float kc_code_one(float v, const float4 h) {
   return __fadd_rn(fminf(fmaxf(__fadd_rn(rintf(__fdiv_rn(v, h.y)), h.z), 0.0f), qmax), kMagic);
 }
 
-// Per-channel keys, one 128-token block of one head (tile t), by the 16
-// epilogue warps together.  Warp (quarter, rank) holds tokens
-// 32 quarter + lane and channels [32 rank, 32 rank + 32) (d = 64: ranks 0
-// and 1; ranks 2 and 3 only help with the column passes).
-// 1. the accumulator times fl(1/sqrt(d)) into registers and into the
-//    shared tile T[token][channel] (16-byte chunk cc of a row at
-//    cc ^ (token mod 8): the row writes and the column reads of a warp meet
-//    32 different banks); the accumulator is released;
-// 2. column passes: thread (part, c) takes channel c over tokens
-//    [part * 128 / P, ...) of the block: min and max;
-// 3. thread c combines the P partial results, computes the channel's header
-//    (Eq. (1), group_header) and stores the block's record;
-// 4. each thread reads its 32 values back from the tile, codes them with the
-//    headers (broadcast reads; packed pairs when the chunk's channels all
-//    take the fast route), packs them and stores the words.
+// Per-channel keys: a tile is one 128-token block of one head.  Two roles of
+// eight warps each work on consecutive tiles at once; warp (quarter,
+// rank) covers tokens 32 quarter + lane and channels [64 rank, 64 rank + 64)
+// (d = 64: [32 rank, 32 rank + 32)).
+// Statistics warps (mq_kc_stats), tile i:
+//   1. the accumulator times fl(1/sqrt(d)) into the shared tile
+//      T[token][channel] (16-byte chunk cc of a row at cc ^ (token mod 8):
+//      conflict-free row writes and column reads); they release their read
+//      of the accumulator;
+//   2. column passes: thread (part, c) takes channel c over 128 / P of the
+//      block's tokens: min and max;
+//   3. thread c (< d) combines the P partial results, computes the channel's
+//      header (Eq. (1), group_header), stores the block's record and writes
+//      the header into buffer i mod 2, once the code warps are done with
+//      tile i - 2's.
+// Code warps (mq_kc_codes), tile i once its headers are written: each warp
+// reads its 32 tokens' channels from the accumulator again, codes them with
+// the headers (broadcast reads; packed pairs when a chunk's channels all
+// take the fast route, one value at a time otherwise), packs and stores them,
+// and releases the accumulator and the header buffer.
 template <int D, int BITS>
-__device__ __forceinline__ void mq_kc_tile(const MqArgs& m, uint8_t* sm, uint32_t tacc, int t,
-                                           int quarter, int rank, int lane, int tid_e,
-                                           uint32_t acc_empty_bar) {
+__device__ __forceinline__ bool mq_kc_stats(const MqArgs& m, uint8_t* sm, uint32_t tacc, int t, int i,
+                                            int quarter, int rank, int lane, int tid_s,
+                                            uint32_t acc_empty_bar, uint32_t hdr_full_bar,
+                                            uint32_t hdr_empty_bar, unsigned long long lim,
+                                            volatile int* abort_flag) {
   using C = MqCfg<D, kMqKeyChannels>;
   const QuantArgs& a = m.q;
   constexpr int NCH = D / 32;
+  constexpr int CPW = NCH / 2;         // 32-channel chunks per warp
   constexpr int P = C::kKcParts;
   constexpr int SLICE = kMqRows / P;
-  constexpr int PER_WORD = 32 / BITS;
-  constexpr int WPC = 32 / PER_WORD;   // code words per 32-channel chunk
   float* T = reinterpret_cast<float*>(sm + C::kTOff);
   float2* mm = reinterpret_cast<float2*>(sm + C::kMmOff);
-  float4* hdr = reinterpret_cast<float4*>(sm + C::kHdrOff);
+  uint8_t* hb = sm + C::kHdrOff + (i & 1) * C::kHdrBytes;
   const int bh = t / m.blocks, blk = t - bh * m.blocks;
-  const int t0 = blk * kMqRows;
-  const int nb = min(kMqRows, a.n_new - t0);
+  const int nb = min(kMqRows, a.n_new - blk * kMqRows);
   const int tok = 32 * quarter + lane;
-  const bool active = rank < NCH;
-  float* row = T + tok * D;
-  if (active) {
-    uint32_t r[32];
-    ptx::tmem_ld32(tacc + (uint32_t)(32 * rank), r);
+  {
+    float* row = T + tok * D;
     const uint64_t s2 = ptx::f2_pack(a.inv_sqrt_d, a.inv_sqrt_d);
+#pragma unroll 1
+    for (int u = 0; u < CPW; ++u) {
+      const int ch = CPW * rank + u;
+      uint32_t r[32];
+      ptx::tmem_ld32(tacc + (uint32_t)(32 * ch), r);
 #pragma unroll
-    for (int cc = 0; cc < 8; ++cc) {
-      float y[4];
-      ptx::f2_unpack(ptx::f2_mul(ptx::f2_pack(__uint_as_float(r[4 * cc]), __uint_as_float(r[4 * cc + 1])), s2),
-                     y[0], y[1]);
-      ptx::f2_unpack(ptx::f2_mul(ptx::f2_pack(__uint_as_float(r[4 * cc + 2]), __uint_as_float(r[4 * cc + 3])), s2),
-                     y[2], y[3]);
-      *reinterpret_cast<float4*>(row + 4 * ((8 * rank + cc) ^ (tok & 7))) = make_float4(y[0], y[1], y[2], y[3]);
+      for (int cc = 0; cc < 8; ++cc) {
+        float y[4];
+        ptx::f2_unpack(ptx::f2_mul(ptx::f2_pack(__uint_as_float(r[4 * cc]), __uint_as_float(r[4 * cc + 1])), s2),
+                       y[0], y[1]);
+        ptx::f2_unpack(ptx::f2_mul(ptx::f2_pack(__uint_as_float(r[4 * cc + 2]), __uint_as_float(r[4 * cc + 3])), s2),
+                       y[2], y[3]);
+        *reinterpret_cast<float4*>(row + 4 * ((8 * ch + cc) ^ (tok & 7))) = make_float4(y[0], y[1], y[2], y[3]);
+      }
     }
   }
   ptx::tc_fence_before();
   __syncwarp();
   if (lane == 0) ptx::mbar_arrive(acc_empty_bar);
-  epi_sync();
+  stat_sync();
   {
     static_assert(SLICE % 8 == 0, "a column pass covers whole swizzle periods");
-    const int c = tid_e % D, part = tid_e / D;
+    const int c = tid_s % D, part = tid_s / D;
     const int ta = part * SLICE, tb = min(nb, ta + SLICE);
     // channel c of token k sits at k D + off[k mod 8]
     int off[8];
@@ -332,7 +346,7 @@ __device__ __forceinline__ void mq_kc_tile(const MqArgs& m, uint8_t* sm, uint32_
     // four independent running pairs (min and max are exact in any order)
     float mn[4] = {INFINITY, INFINITY, INFINITY, INFINITY};
     float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll
+#pragma unroll 2
     for (int tt = ta; tt < ta + SLICE; tt += 8) {
       const float* base = T + tt * D;
 #pragma unroll
@@ -347,9 +361,10 @@ __device__ __forceinline__ void mq_kc_tile(const MqArgs& m, uint8_t* sm, uint32_
     mm[part * D + c] = make_float2(fminf(fminf(mn[0], mn[1]), fminf(mn[2], mn[3])),
                                    fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])));
   }
-  epi_sync();
-  if (tid_e < D) {
-    const int c = tid_e;
+  stat_sync();
+  bool ok = true;
+  if (tid_s < D) {
+    const int c = tid_s;
     float mn = mm[c].x, mx = mm[c].y;
 #pragma unroll
     for (int p2 = 1; p2 < P; ++p2) {
@@ -357,81 +372,102 @@ __device__ __forceinline__ void mq_kc_tile(const MqArgs& m, uint8_t* sm, uint32_
       mx = fmaxf(mx, mm[p2 * D + c].y);
     }
     const QHdr h = group_header<BITS>(mn, mx);
-    hdr[c] = make_float4(h.rcp, h.delta, h.zero,
-                         __uint_as_float((h.fast ? 1u : 0u) | (h.clamp ? 2u : 0u)));
-    float* hp = reinterpret_cast<float*>(sm + C::kHdrPairOff) + 4 * (c >> 1) + (c & 1);
+    if (KVQ_IN_BOUNDS(a.kblk_first + blk, a.kblk_per_head, a.status, a.bounds_site) &&
+        KVQ_IN_BOUNDS(bh, a.bh, a.status, a.bounds_site))
+      a.k_sz[((size_t)bh * a.kblk_per_head + a.kblk_first + blk) * D + c] = h.rec;
+    // the buffer held tile i - 2's headers: the code warps are done with it
+    if (i >= 2) ok = mq_wait(hdr_empty_bar, ((i >> 1) - 1) & 1, lim, abort_flag, a.status);
+    reinterpret_cast<float4*>(hb)[c] =
+        make_float4(h.rcp, h.delta, h.zero, __uint_as_float((h.fast ? 1u : 0u) | (h.clamp ? 2u : 0u)));
+    float* hp = reinterpret_cast<float*>(hb + C::kHdrPair) + 4 * (c >> 1) + (c & 1);
     hp[0] = h.rcp;
     hp[2] = -h.delta;
-    reinterpret_cast<float*>(sm + C::kHdrZeroOff)[c] = h.zero;
+    reinterpret_cast<float*>(hb + C::kHdrZero)[c] = h.zero;
     // a chunk whose 32 channels all take the fast route (clamped or not:
     // the packed pass clamps every value, which changes nothing where no
     // code leaves [0, 2^B - 1])
     const bool simple = __all_sync(0xffffffffu, h.fast);
-    if ((c & 31) == 0) reinterpret_cast<int*>(sm + C::kChunkFlagOff)[c >> 5] = simple ? 1 : 0;
-    if (KVQ_IN_BOUNDS(a.kblk_first + blk, a.kblk_per_head, a.status, a.bounds_site) &&
-        KVQ_IN_BOUNDS(bh, a.bh, a.status, a.bounds_site))
-      a.k_sz[((size_t)bh * a.kblk_per_head + a.kblk_first + blk) * D + c] = h.rec;
+    if ((c & 31) == 0) reinterpret_cast<int*>(hb + C::kChunkFlag)[c >> 5] = simple ? 1 : 0;
+    __threadfence_block();
+    __syncwarp();
+    if (lane == 0) ptx::mbar_arrive(hdr_full_bar);
   }
-  epi_sync();
-  if (active) {
-    // the token's 32 values of the chunk, back from the tile (the same
-    // swizzled places: conflict-free, and nothing held across the passes)
+  return ok;
+}
+
+template <int D, int BITS>
+__device__ __forceinline__ void mq_kc_codes(const MqArgs& m, const uint8_t* sm, uint32_t tacc, int t,
+                                            int i, int quarter, int rank, int lane) {
+  using C = MqCfg<D, kMqKeyChannels>;
+  const QuantArgs& a = m.q;
+  constexpr int NCH = D / 32;
+  constexpr int CPW = NCH / 2;
+  constexpr int PER_WORD = 32 / BITS;
+  constexpr int WPC = 32 / PER_WORD;   // code words per 32-channel chunk
+  const uint8_t* hb = sm + C::kHdrOff + (i & 1) * C::kHdrBytes;
+  const float4* hdr = reinterpret_cast<const float4*>(hb);
+  const int bh = t / m.blocks, blk = t - bh * m.blocks;
+  const int t0 = blk * kMqRows;
+  const int nb = min(kMqRows, a.n_new - t0);
+  const int tok = 32 * quarter + lane;
+  const uint64_t s2 = ptx::f2_pack(a.inv_sqrt_d, a.inv_sqrt_d);
+  const bool store = tok < nb && KVQ_IN_BOUNDS(a.first + t0 + tok, a.cap, a.status, a.bounds_site) &&
+                     KVQ_IN_BOUNDS(bh, a.bh, a.status, a.bounds_site);
+  uint8_t* drow = a.k_codes + ((size_t)bh * a.cap + a.first + t0 + tok) * (D * BITS / 8);
+#pragma unroll 1
+  for (int u = 0; u < CPW; ++u) {
+    const int ch = CPW * rank + u;
     float x[32];
+    {
+      uint32_t r[32];
+      ptx::tmem_ld32(tacc + (uint32_t)(32 * ch), r);
 #pragma unroll
-    for (int cc = 0; cc < 8; ++cc) {
-      const float4 v = *reinterpret_cast<const float4*>(row + 4 * ((8 * rank + cc) ^ (tok & 7)));
-      x[4 * cc] = v.x;
-      x[4 * cc + 1] = v.y;
-      x[4 * cc + 2] = v.z;
-      x[4 * cc + 3] = v.w;
+      for (int j = 0; j < 32; j += 2)
+        ptx::f2_unpack(ptx::f2_mul(ptx::f2_pack(__uint_as_float(r[j]), __uint_as_float(r[j + 1])), s2),
+                       x[j], x[j + 1]);
     }
-    if (reinterpret_cast<const int*>(sm + C::kChunkFlagOff)[rank]) {
+    if (reinterpret_cast<const int*>(hb + C::kChunkFlag)[ch]) {
       // every channel on the fast route: packed pairs, the headers in pair
       // layout (one 16-byte and one 8-byte broadcast load), every value
       // clamped to [1.5 * 2^23, 1.5 * 2^23 + 2^B - 1]
-      const float4* hp = reinterpret_cast<const float4*>(sm + C::kHdrPairOff) + 16 * rank;
-      const float2* hz = reinterpret_cast<const float2*>(sm + C::kHdrZeroOff) + 16 * rank;
+      const float4* hp = reinterpret_cast<const float4*>(hb + C::kHdrPair) + 16 * ch;
+      const float2* hz = reinterpret_cast<const float2*>(hb + C::kHdrZero) + 16 * ch;
       const float kMagic = 12582912.0f;   // 1.5 * 2^23
       const float kTop = kMagic + float((1 << BITS) - 1);
       const uint64_t m2 = ptx::f2_pack(kMagic, kMagic);
 #pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        const float4 hq = hp[i];
-        const float2 z = hz[i];
-        const uint64_t xv = ptx::f2_pack(x[2 * i], x[2 * i + 1]);
+      for (int k = 0; k < 16; ++k) {
+        const float4 hq = hp[k];
+        const float2 z = hz[k];
+        const uint64_t xv = ptx::f2_pack(x[2 * k], x[2 * k + 1]);
         const uint64_t r2 = ptx::f2_pack(hq.x, hq.y);
         const uint64_t q0 = ptx::f2_mul(xv, r2);
         const uint64_t e = ptx::f2_fma(q0, ptx::f2_pack(hq.z, hq.w), xv);
         const uint64_t q = ptx::f2_fma(e, r2, q0);
-        float t0, t1;
-        ptx::f2_unpack(ptx::f2_add(ptx::f2_add(q, m2), ptx::f2_pack(z.x, z.y)), t0, t1);
-        x[2 * i] = fminf(fmaxf(t0, kMagic), kTop);
-        x[2 * i + 1] = fminf(fmaxf(t1, kMagic), kTop);
+        float c0, c1;
+        ptx::f2_unpack(ptx::f2_add(ptx::f2_add(q, m2), ptx::f2_pack(z.x, z.y)), c0, c1);
+        x[2 * k] = fminf(fmaxf(c0, kMagic), kTop);
+        x[2 * k + 1] = fminf(fmaxf(c1, kMagic), kTop);
       }
     } else {
-      // some channel off the fast route or clamped: value by value, in place
-      // in the tile (one rolled loop), then back into registers
 #pragma unroll 1
-      for (int i = 0; i < 32; ++i) {
-        float* pv = row + 4 * ((8 * rank + (i >> 2)) ^ (tok & 7)) + (i & 3);
-        *pv = kc_code_one<BITS>(*pv, hdr[32 * rank + i]);
-      }
+      for (int k = 0; k < 32; k += 2) {
+        const float c0 = kc_code_one<BITS>(x[0], hdr[32 * ch + k]);
+        const float c1 = kc_code_one<BITS>(x[1], hdr[32 * ch + k + 1]);
+        // rotate the 32 values by two places (a rolled loop with
+        // compile-time register indices): after 16 steps the codes are in
+        // x[0..32) in channel order
 #pragma unroll
-      for (int cc = 0; cc < 8; ++cc) {
-        const float4 v = *reinterpret_cast<const float4*>(row + 4 * ((8 * rank + cc) ^ (tok & 7)));
-        x[4 * cc] = v.x;
-        x[4 * cc + 1] = v.y;
-        x[4 * cc + 2] = v.z;
-        x[4 * cc + 3] = v.w;
+        for (int j = 0; j < 30; ++j) x[j] = x[j + 2];
+        x[30] = c0;
+        x[31] = c1;
       }
     }
     uint32_t words[WPC];
 #pragma unroll
     for (int w = 0; w < WPC; ++w) words[w] = pack_word<BITS>(x + PER_WORD * w, 0);
-    if (tok < nb && KVQ_IN_BOUNDS(a.first + t0 + tok, a.cap, a.status, a.bounds_site) &&
-        KVQ_IN_BOUNDS(bh, a.bh, a.status, a.bounds_site)) {
-      uint8_t* dc = a.k_codes + ((size_t)bh * a.cap + a.first + t0 + tok) * (D * BITS / 8) +
-                    32 * rank * BITS / 8;
+    if (store) {
+      uint8_t* dc = drow + 32 * ch * BITS / 8;
       if constexpr (WPC == 2) {
         *reinterpret_cast<uint2*>(dc) = make_uint2(words[0], words[1 % WPC]);
       } else {
@@ -485,9 +521,17 @@ __global__ void __launch_bounds__(kMqThreads, 1)
     ptx::prefetch_tensormap(&map_k);
     ptx::prefetch_tensormap(&map_v);
     // an accumulator is released by the warps that read it: the 4 D / GROUP
-    // warps of a team, or all 16 epilogue warps for per-channel keys
+    // warps of a team, or all 16 epilogue warps for per-channel keys (8
+    // statistics and 8 code warps); a header buffer is written by the d / 32
+    // warps that compute the headers and released by the 8 code warps
     constexpr uint32_t kReaders = MODE == kMqKeyChannels ? 4 * kMqRanks : 4 * (D / GROUP);
-    for (int i = 0; i < C::kBars; ++i) ptx::mbar_init(bar(i), i >= C::kAccEmpty ? kReaders : 1u);
+    for (int i = 0; i < C::kBars; ++i) {
+      uint32_t count = 1u;
+      if (i >= C::kAccEmpty && i < C::kAccEmpty + kMqAcc) count = kReaders;
+      if (C::kKch && i >= C::kHdrFull && i < C::kHdrFull + 2) count = D / 32;
+      if (C::kKch && i >= C::kHdrEmpty && i < C::kHdrEmpty + 2) count = 8u;
+      ptx::mbar_init(bar(i), count);
+    }
     *abort_flag = 0;
     ptx::fence_mbar_init();
     // the inputs may come from the kernel launched before this one (a
@@ -572,17 +616,47 @@ __global__ void __launch_bounds__(kMqThreads, 1)
     }
   } else if constexpr (MODE == kMqKeyChannels) {
     const int quarter = warp & 3;             // TMEM lanes 32 quarter .. + 31
-    const int rank = (warp - 2) >> 2;
-    const int tid_e = (int)threadIdx.x - 64;
-    int i = 0;
-    for (int t = (int)blockIdx.x; t < m.tiles; t += grid, ++i) {
-      const int ac = i % kMqAcc;
-      const bool ok = mq_wait(bar(C::kAccFull + ac), (i / kMqAcc) & 1, lim, abort_flag, a.status);
-      // one decision for the whole epilogue: its warps meet at named barriers
-      if (!epi_all(ok)) break;
-      ptx::tc_fence_after();
-      mq_kc_tile<D, BITS>(m, sm, tmem + (uint32_t)(ac * D) + ((uint32_t)(32 * quarter) << 16), t,
-                          quarter, rank, lane, tid_e, bar(C::kAccEmpty + ac));
+    if (warp < 10) {
+      // statistics warps 2-9
+      const int rank = (warp - 2) >> 2;
+      const int tid_s = (int)threadIdx.x - 64;
+      bool ok = true;
+      int i = 0;
+      for (int t = (int)blockIdx.x; t < m.tiles; t += grid, ++i) {
+        const int ac = i % kMqAcc;
+        ok = ok && mq_wait(bar(C::kAccFull + ac), (i / kMqAcc) & 1, lim, abort_flag, a.status);
+        // one decision for the whole role: its warps meet at named barriers
+        if (!stat_all(ok)) break;
+        ptx::tc_fence_after();
+        ok = mq_kc_stats<D, BITS>(m, sm, tmem + (uint32_t)(ac * D) + ((uint32_t)(32 * quarter) << 16),
+                                  t, i, quarter, rank, lane, tid_s, bar(C::kAccEmpty + ac),
+                                  bar(C::kHdrFull + (i & 1)), bar(C::kHdrEmpty + (i & 1)), lim,
+                                  abort_flag);
+      }
+    } else {
+      // code warps 10-17
+      const int rank = (warp - 10) >> 2;
+      int i = 0;
+      for (int t = (int)blockIdx.x; t < m.tiles; t += grid, ++i) {
+        const int ac = i % kMqAcc;
+        if (!__all_sync(0xffffffffu, mq_wait(bar(C::kHdrFull + (i & 1)), (i >> 1) & 1, lim,
+                                              abort_flag, a.status)))
+          break;
+        // (complete already: the statistics warps waited for it) orders this
+        // warp's tensor-memory reads after the MMAs
+        if (!__all_sync(0xffffffffu, mq_wait(bar(C::kAccFull + ac), (i / kMqAcc) & 1, lim,
+                                              abort_flag, a.status)))
+          break;
+        ptx::tc_fence_after();
+        mq_kc_codes<D, BITS>(m, sm, tmem + (uint32_t)(ac * D) + ((uint32_t)(32 * quarter) << 16), t,
+                             i, quarter, rank, lane);
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          ptx::mbar_arrive(bar(C::kAccEmpty + ac));
+          ptx::mbar_arrive(bar(C::kHdrEmpty + (i & 1)));
+        }
+      }
     }
   } else {
     // the four warps of a rank cover the four TMEM lane quarters; the ranks
