@@ -176,8 +176,8 @@ def check_key_channels_admissible():
     quantizer's one answer (every block, the last one short); keys sampled
     inside interval bounds always have their answer among the candidates."""
     rng = np.random.default_rng(23)
-    for bits in (2, 4):
-        y = (rng.standard_normal((300, 64)) * 2 + rng.standard_normal((1, 64)) * 3).astype(np.float32)
+    for d, bits in ((64, 2), (64, 4), (128, 2)):
+        y = (rng.standard_normal((300, d)) * 2 + rng.standard_normal((1, d)) * 3).astype(np.float32)
         codes, delta, zero = O.quantize_key_channels(y, bits)
         blocks = O.chunk_blocks(300)
         adm = O.quantize_key_channels_admissible(y, y, bits)

@@ -221,7 +221,25 @@ def _admissible_codes_any(y_lo, y_hi, bits, group):
     return cd, cz, np.zeros_like(clo), np.full_like(chi, 2 ** bits - 1)
 
 
+def _key_admissible_along_channels(y_lo, y_hi, bits, block=O.KEY_BLOCK):
+    # a full block grouped along channels (per token) instead of along
+    # tokens: the transpose forgotten (shapes agree when the block has d tokens)
+    lo = np.asarray(y_lo, np.float32)
+    hi = np.asarray(y_hi, np.float32)
+    out = []
+    for a, b in O.chunk_blocks(lo.shape[0], block):
+        n = b - a
+        if n == lo.shape[1]:
+            cd, cz, clo, chi = _real_admissible(lo[a:b], hi[a:b], bits, n)
+        else:
+            cd, cz, clo, chi = _real_admissible(np.ascontiguousarray(lo[a:b].T),
+                                                np.ascontiguousarray(hi[a:b].T), bits, n)
+        out.append((cd[:, 0], cz[:, 0], clo[:, 0], chi[:, 0]))
+    return out
+
+
 MUTANTS = {
+    "key_admissible_along_channels": ("quantize_key_channels_admissible", _key_admissible_along_channels),
     "rotation_bounds_no_error": ("rotation_bounds", _rotation_bounds_no_error),
     "admissible_zero_one_end": ("quantize_groups_admissible", _admissible_zero_one_end),
     "admissible_codes_any": ("quantize_groups_admissible", _admissible_codes_any),
