@@ -145,7 +145,7 @@ def test_append_partial_and_degenerate(d, bits, group):
     assert e.value.status == kvq.KVQ_ERR_CAPACITY
 
 
-@pytest.mark.parametrize("name", ["tiny", "w4_int2", "w4_int4", "hires_t3"])
+@pytest.mark.parametrize("name", ["tiny", "w4_int2", "w4_int4", "w8_int2", "hires_t3"])
 def test_append_workload_chunk(name):
     """One full chunk of the workload's key/value distribution (all heads):
     outlier channels, per-channel offsets; admissible answers, and the
