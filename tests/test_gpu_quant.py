@@ -271,3 +271,37 @@ def test_append_waits_for_the_previous_attention():
         cache.struct.head_slot = c
         kvq.quantize_append(cache, kw[:, :, sl].contiguous(), vw[:, :, sl].contiguous())
     assert kvq.last_device_status() == kvq.KVQ_OK
+
+
+@pytest.mark.parametrize("d,bits,group", [(128, 2, 32), (128, 4, 64), (64, 2, 32)])
+def test_append_division_route(d, bits, group):
+    """Rows scaled near 2^-112 (grid values m 2^e, |m| <= 255, so the sums are
+    exact): every step is below 2^-100, where Eq. (1)'s quotients leave the
+    reciprocal route for one IEEE division per value -- per token and group
+    (keys and values) and, in the per-channel key mode, per channel; the
+    oracle's answer bit for bit."""
+    rng = np.random.default_rng(900 + d + bits)
+    B, H, C = 1, 2, 200
+    s = synth.hadamard_signs(d, seed=9)
+    m = np.clip(np.rint(rng.standard_normal((B, H, C, d)) * 40), -255, 255)
+    k = _bf16(m * 2.0 ** rng.integers(-114, -110, (B, H, C, 1)).astype(np.float64))
+    m = np.clip(np.rint(rng.standard_normal((B, H, C, d)) * 40), -255, 255)
+    v = _bf16(m * 2.0 ** rng.integers(-114, -110, (B, H, C, 1)).astype(np.float64))
+    assert float(k.abs().max()) < 2.0 ** -100
+    cache = kvq.KVCache(B, H, d, bits, group, C, 2, s)
+    kvq.quantize_append(cache, k.cuda(), v.cuda())
+    torch.cuda.synchronize()
+    for which, x in (("k", k), ("v", v)):
+        packed, delta, zero, _, _ = O.quantize_rows(x.float().numpy(), s, bits, group)
+        assert float(np.max(delta)) < 2.0 ** -100
+        assert np.array_equal(cache.codes_view(which)[:, :, :C].cpu().numpy(), packed), which
+        sz = cache.sz_view(which)[:, :, :C].cpu().numpy().view(np.uint16)
+        assert np.array_equal(sz[..., 0], O.bf16_bits(delta)) and np.array_equal(sz[..., 1], O.bf16_bits(zero))
+    kc = kvq.KVCache(B, H, d, bits, group, C, 2, s, key_mode=kvq.KEYS_PER_CHANNEL)
+    kvq.quantize_append(kc, k.cuda(), v.cuda())
+    torch.cuda.synchronize()
+    _check_key_channel_slot(kc, k, s, 0, C, 1.0)
+    for h in range(H):
+        packed = O.quantize_key_chunk(k[0, h].float().numpy(), s, bits)[0]
+        assert np.array_equal(kc.codes_view("k")[0, h, :C].cpu().numpy(), packed)
+    assert kvq.last_device_status() == kvq.KVQ_OK
